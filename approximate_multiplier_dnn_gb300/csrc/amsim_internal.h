@@ -1,0 +1,75 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "amsim.h"
+
+struct amsim_lut_s {
+    int M = 0;
+    int device = -1;
+    int width_bits = 32;   // narrowed entry width: 8, 16 or 32
+    int shift = 0;         // canonical entry = narrowed << shift
+    bool symmetric = false;
+    void *d_base = nullptr;       // one allocation holding everything below
+    const uint32_t *d_canon = nullptr;   // 2^(2M) canonical entries, index p<<M|q
+    const void *d_narrow = nullptr;      // narrowed, index [first operand][second operand]
+    const void *d_narrow_t = nullptr;    // narrowed, index [second operand][first operand]
+    size_t narrow_bytes = 0;
+};
+
+namespace amsim {
+
+// Maximum dynamic shared memory a CTA may use on sm_100-family parts.
+constexpr int kMaxSmemPerCta = 227 * 1024;
+
+int check_lut(amsim_lut_t lut);   // AMSIM_OK if usable on the current device
+int cuda_status(cudaError_t e);   // maps to AMSIM_OK / AMSIM_ECUDA / AMSIM_ENOMEM
+
+// One GEMM operand in the kernel's terms: element (row r, reduction index k).
+// Dense: value at ptr[batch*batch_stride + r*s_row + k*s_k].
+// Gather (implicit im2col): k = (k2*kD1 + k1)*kD0 + k0 and r = (r2*rE1 + r1)*rE0 + r0
+// contribute y = ry + ky, x = rx + kx, base = rb + kb (per-level linear coefficients);
+// the value is ptr[base + (y/sy * IW + x/sx) * Cs] when y, x are divisible by
+// sy, sx and in [0, IH*sy) x [0, IW*sx) after division, else a zero operand.
+struct OperandDesc {
+    const float *ptr;
+    int64_t batch_stride;
+    int rows;
+    int gather;          // 0 dense, 1 gather
+    int64_t s_row, s_k;  // dense strides
+    // gather geometry
+    int kD0, kD1;
+    int kcy[3], kcx[3];
+    int64_t kcb[3];
+    int rE0, rE1;
+    int rcy[3], rcx[3];
+    int64_t rcb[3];
+    int ry0, rx0;        // constant offsets added to the row part
+    int IH, IW, Cs, sy, sx;
+};
+
+// A contraction as the kernels see it: out[u][l] = sum_k AMSim-product of the
+// U operand's (u,k) and the L operand's (l,k) element, where the LUT index has
+// the U element's mantissa in the high bits when `u_is_first` (the original
+// first operand), else in the low bits (the kernel then reads the transposed
+// table).  Output element (u,l) of batch b lives at c_ptr + b*c_bs + u*c_su + l*c_sl.
+struct Problem {
+    OperandDesc U, L;
+    int K;               // reduction length
+    int batch;
+    bool u_is_first;
+    float *c_ptr;
+    int64_t c_bs, c_su, c_sl;
+    float alpha, beta;
+};
+
+// Launch the LUT-GEMM for a problem.  ws may be null; split-K is used only if
+// ws_bytes allows it.  Returns an amsim status.
+int run_problem(const Problem &p, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream);
+size_t problem_workspace(const Problem &p, amsim_lut_t lut);
+
+}  // namespace amsim

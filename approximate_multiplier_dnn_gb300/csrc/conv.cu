@@ -1,0 +1,210 @@
+// Conv2D forward / preceding-layer gradient / weight gradient as implicit GEMMs
+// over NHWC activations and RSCK filters (ApproxTrain Sec. VI-B, Algorithms 3
+// and 4, Fig. 8).  The page's IM2COL, IM2COL_PLG, IM2COL_Weight and
+// TransposeAndReverse kernels become operand addressing inside the LUT-GEMM:
+// no column buffer is materialised.
+#include <algorithm>
+
+#include "amsim_internal.h"
+
+namespace {
+
+using amsim::OperandDesc;
+using amsim::Problem;
+
+struct Geo {
+    int N, H, W, C, K, R, S, sh, sw, ph, pw, dh, dw, P, Q;
+};
+
+int geometry(const amsim_conv_desc *d, Geo *g)
+{
+    if (!d) return AMSIM_EINVAL;
+    *g = {d->N, d->H, d->W, d->C, d->K, d->R, d->S, d->stride_h, d->stride_w, d->pad_h, d->pad_w,
+          d->dil_h, d->dil_w, 0, 0};
+    if (g->N < 0 || g->H < 1 || g->W < 1 || g->C < 1 || g->K < 1 || g->R < 1 || g->S < 1) return AMSIM_EINVAL;
+    if (g->sh < 1 || g->sw < 1 || g->ph < 0 || g->pw < 0 || g->dh < 1 || g->dw < 1) return AMSIM_EINVAL;
+    const long long hh = (long long)g->H + 2LL * g->ph - (long long)g->dh * (g->R - 1) - 1;
+    const long long ww = (long long)g->W + 2LL * g->pw - (long long)g->dw * (g->S - 1) - 1;
+    if (hh < 0 || ww < 0) return AMSIM_EINVAL;
+    g->P = (int)(hh / g->sh + 1);
+    g->Q = (int)(ww / g->sw + 1);
+    // index arithmetic inside the kernels is 32-bit per coordinate, 64-bit per address
+    const long long px = (long long)g->N * std::max(g->H * (long long)g->W, (long long)g->P * g->Q);
+    if (px > 0x7FFFFFFFLL || (long long)g->R * g->S * std::max(g->C, g->K) > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
+    return AMSIM_OK;
+}
+
+OperandDesc blank(const float *ptr, int rows)
+{
+    OperandDesc d = {};
+    d.ptr = ptr;
+    d.rows = rows;
+    d.kD0 = d.kD1 = d.rE0 = d.rE1 = 1;
+    d.IH = d.IW = 1;
+    d.sy = d.sx = 1;
+    return d;
+}
+
+OperandDesc dense(const float *ptr, int rows, long long s_row, long long s_k)
+{
+    OperandDesc d = blank(ptr, rows);
+    d.s_row = s_row;
+    d.s_k = s_k;
+    return d;
+}
+
+// x viewed as the im2col matrix of the forward pass: row = output pixel
+// (n,p,q), k = (r,s,c); value x[n, p*sh - ph + r*dh, q*sw - pw + s*dw, c].
+OperandDesc x_im2col(const Geo &g, const float *x)
+{
+    OperandDesc d = blank(x, g.N * g.P * g.Q);
+    d.gather = 1;
+    d.rE0 = g.Q; d.rE1 = g.P;
+    d.rcx[0] = g.sw; d.rcy[1] = g.sh; d.rcb[2] = (long long)g.H * g.W * g.C;
+    d.ry0 = -g.ph; d.rx0 = -g.pw;
+    d.kD0 = g.C; d.kD1 = g.S;
+    d.kcb[0] = 1; d.kcx[1] = g.dw; d.kcy[2] = g.dh;
+    d.IH = g.H; d.IW = g.W; d.Cs = g.C;
+    return d;
+}
+
+// x viewed for the weight gradient: row = (r,s,c), k = (n,p,q).
+OperandDesc x_im2col_weight(const Geo &g, const float *x)
+{
+    OperandDesc d = blank(x, g.R * g.S * g.C);
+    d.gather = 1;
+    d.rE0 = g.C; d.rE1 = g.S;
+    d.rcb[0] = 1; d.rcx[1] = g.dw; d.rcy[2] = g.dh;
+    d.ry0 = -g.ph; d.rx0 = -g.pw;
+    d.kD0 = g.Q; d.kD1 = g.P;
+    d.kcx[0] = g.sw; d.kcy[1] = g.sh; d.kcb[2] = (long long)g.H * g.W * g.C;
+    d.IH = g.H; d.IW = g.W; d.Cs = g.C;
+    return d;
+}
+
+// dy viewed as the padded-dilated error columns of the preceding-layer
+// gradient: row = input pixel (n,h,w), k = (r,s,k); value dy[n,p,q,k] with
+// p = (h + ph - r*dh)/sh, q = (w + pw - s*dw)/sw when integral and in range.
+OperandDesc dy_im2col_plg(const Geo &g, const float *dy)
+{
+    OperandDesc d = blank(dy, g.N * g.H * g.W);
+    d.gather = 1;
+    d.rE0 = g.W; d.rE1 = g.H;
+    d.rcx[0] = 1; d.rcy[1] = 1; d.rcb[2] = (long long)g.P * g.Q * g.K;
+    d.ry0 = g.ph; d.rx0 = g.pw;
+    d.kD0 = g.K; d.kD1 = g.S;
+    d.kcb[0] = 1; d.kcx[1] = -g.dw; d.kcy[2] = -g.dh;
+    d.IH = g.P; d.IW = g.Q; d.Cs = g.K;
+    d.sy = g.sh; d.sx = g.sw;
+    return d;
+}
+
+// Filter transposed (in/out channels swapped) for the preceding-layer
+// gradient: row = c, k = (r,s,k); value w[r,s,c,k].  The spatial reversal of
+// TransposeAndReverse is carried by the dy addressing above.
+OperandDesc w_transposed(const Geo &g, const float *w)
+{
+    OperandDesc d = blank(w, g.C);
+    d.gather = 1;
+    d.rE0 = g.C; d.rE1 = 1;
+    d.rcb[0] = g.K;
+    d.kD0 = g.K; d.kD1 = g.S;
+    d.kcb[0] = 1; d.kcb[1] = (long long)g.C * g.K; d.kcb[2] = (long long)g.S * g.C * g.K;
+    d.IH = 1; d.IW = 1; d.Cs = 0;
+    return d;
+}
+
+void set_out(Problem *pr, float *out, long long c_su, long long c_sl)
+{
+    pr->c_ptr = out;
+    pr->c_bs = 0;
+    pr->c_su = c_su;
+    pr->c_sl = c_sl;
+    pr->alpha = 1.0f;
+    pr->beta = 0.0f;
+    pr->batch = 1;
+}
+
+int build(const amsim_conv_desc *desc, int which, const float *t0, const float *t1, float *out, Problem *pr)
+{
+    Geo g;
+    int rc = geometry(desc, &g);
+    if (rc) return rc;
+    if (which == 0) {            // y = conv(x, w): first operand x
+        pr->U = dense(t1, g.K, 1, g.K);                  // w[(r,s,c)][k]: row k, index rsc
+        pr->L = x_im2col(g, t0);
+        pr->K = g.R * g.S * g.C;
+        pr->u_is_first = false;
+        set_out(pr, out, 1, g.K);                        // y[(n,p,q)][k]
+    } else if (which == 1) {     // dx from (dy, w): first operand dy
+        pr->U = w_transposed(g, t1);
+        pr->L = dy_im2col_plg(g, t0);
+        pr->K = g.R * g.S * g.K;
+        pr->u_is_first = false;
+        set_out(pr, out, 1, g.C);                        // dx[(n,h,w)][c]
+    } else {                     // dw from (x, dy): first operand x
+        pr->U = dense(t1, g.K, 1, g.K);                  // dy[(n,p,q)][k]: row k, index npq
+        pr->L = x_im2col_weight(g, t0);
+        pr->K = g.N * g.P * g.Q;
+        pr->u_is_first = false;
+        set_out(pr, out, 1, g.K);                        // dw[(r,s,c)][k]
+    }
+    const long long outs = (long long)pr->U.rows * pr->L.rows;
+    if (outs > 0 && (!t0 || !t1 || !out)) return AMSIM_EINVAL;
+    if (pr->L.rows == 0) return AMSIM_OK;
+    return AMSIM_OK;
+}
+
+int run(const amsim_conv_desc *desc, int which, const float *t0, const float *t1, float *out, amsim_lut_t lut,
+        void *ws, size_t ws_bytes, amsim_stream_t stream)
+{
+    int rc = amsim::check_lut(lut);
+    if (rc) return rc;
+    Problem pr;
+    rc = build(desc, which, t0, t1, out, &pr);
+    if (rc) return rc;
+    return amsim::run_problem(pr, lut, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int amsim_conv2d_out_hw(const amsim_conv_desc *desc, int *P, int *Q)
+{
+    Geo g;
+    int rc = geometry(desc, &g);
+    if (rc) return rc;
+    if (P) *P = g.P;
+    if (Q) *Q = g.Q;
+    return AMSIM_OK;
+}
+
+int amsim_conv2d_fwd(const amsim_conv_desc *desc, const float *x, const float *w, float *y, amsim_lut_t lut,
+                     void *ws, size_t ws_bytes, amsim_stream_t stream)
+{
+    return run(desc, 0, x, w, y, lut, ws, ws_bytes, stream);
+}
+
+int amsim_conv2d_bwd_data(const amsim_conv_desc *desc, const float *dy, const float *w, float *dx, amsim_lut_t lut,
+                          void *ws, size_t ws_bytes, amsim_stream_t stream)
+{
+    return run(desc, 1, dy, w, dx, lut, ws, ws_bytes, stream);
+}
+
+int amsim_conv2d_bwd_filter(const amsim_conv_desc *desc, const float *x, const float *dy, float *dw,
+                            amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream)
+{
+    return run(desc, 2, x, dy, dw, lut, ws, ws_bytes, stream);
+}
+
+size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim_lut_t lut)
+{
+    if (!lut || which < 0 || which > 2) return 0;
+    static const float dummy = 0.0f;
+    Problem pr;
+    if (build(desc, which, &dummy, &dummy, const_cast<float *>(&dummy), &pr)) return 0;
+    return amsim::problem_workspace(pr, lut);
+}
+
+}  // extern "C"

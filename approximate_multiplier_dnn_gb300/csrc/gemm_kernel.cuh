@@ -1,0 +1,536 @@
+// LUT-GEMM kernel family: out[u][l] = sum_k AMSim(U[u][k], L[l][k]) with fp32
+// accumulation (ApproxTrain Sec. V-B Algorithm 2 per product; Sec. VI-D GEMM
+// kernel; Sec. VI-B Algorithms 3/4 as implicit GEMM through gather operands).
+//
+// Design (sm_103a, no tensor cores -- the multiply is not an IEEE multiply):
+//  * The narrowed mantissa-product LUT sits in shared memory (global memory,
+//    read-only path, when it does not fit).  Each warp owns TM "uniform" rows
+//    (same U element for all 32 lanes in one lookup) and 32*TN lane columns, so
+//    every LUT load of a warp reads one LUT row: with 8-bit entries a row of
+//    128 entries is 32 words, one per bank, and the lookup is conflict-free.
+//  * Operand tiles are staged through registers (loads for tile t+1 are in
+//    flight while tile t is computed) and pre-decoded once per CTA into
+//    (LUT byte offset, signed power-of-two scale): the decode applies the
+//    denormal-as-zero, NaN and infinity rules of the ABI.
+//  * Per product: one index add, one LUT load, one integer multiply-add that
+//    rebuilds v = 1.mantissa * 2^carry as an fp32 bit pattern, and half of a
+//    packed fp32x2 multiply (scale = sa*sb, flush-to-zero gives the page's
+//    "zero when the biased exponent is not above zero") and half of a packed
+//    fp32x2 FMA acc += v*scale.  v*scale is exact unless it overflows; tiles
+//    holding an operand with |x| >= 2^64 take a slower path that rounds the
+//    product to fp32 (infinity on overflow) before the add, exactly as
+//    Algorithm 2 then an fp32 add would.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "amsim_internal.h"
+
+namespace amsim {
+namespace kern {
+
+constexpr int NT = 256;            // threads per CTA
+constexpr int BU = 64;             // uniform rows per CTA tile
+constexpr int BL = 256;            // lane columns per CTA tile
+constexpr int BK = 16;             // reduction depth per stage
+constexpr int TM = 16;             // uniform rows per warp
+constexpr int TN = 4;              // lane columns per thread
+constexpr int WU = BU / TM;        // 4 warps along U
+constexpr int WL = BL / (32 * TN); // 2 warps along L
+constexpr int UST = BU + 4;        // decoded U row stride (words), 16-B aligned, few bank conflicts
+constexpr int LST = BL + 4;        // decoded L row stride (words)
+constexpr int NUE = BU * BK / NT;  // U elements loaded per thread per stage (4)
+constexpr int NLE = BL * BK / NT;  // L elements loaded per thread per stage (16)
+static_assert(WU * WL * 32 == NT, "warp layout");
+
+struct RowInfo {
+    int y, x;
+    long long b;
+};
+
+struct KParams {
+    OperandDesc U, L;
+    int K, batch;
+    int tiles_u, tiles_l, splits, kt_per_split, kt_total;
+    const void *table;
+    int table_bytes;     // bytes staged to shared memory (0 when read from global)
+    int M;
+    uint32_t mul;        // 1 << shift: rebuilds a canonical entry from a narrowed one
+    int wlog;            // log2(entry bytes)
+    float *c_ptr;
+    long long c_bs, c_su, c_sl;
+    float alpha, beta;
+    float *ws;           // split partials [batch][split][U.rows][ws_ld] when splits > 1
+    int ws_ld;
+    int u_kfast, l_kfast;
+};
+
+// Shared-memory layout (bytes) after the LUT region.
+constexpr int kUdecBytes = 2 * BK * UST * 4;   // one array (offsets or scales), 2 stages
+constexpr int kLdecBytes = 2 * BK * LST * 4;
+constexpr int kRowTabBytes = (BU + BL) * (int)sizeof(RowInfo);
+constexpr int kFixedSmem = 2 * kUdecBytes + 2 * kLdecBytes + kRowTabBytes;
+
+__host__ __device__ constexpr int lut_region_bytes(int table_bytes) { return (table_bytes + 127) & ~127; }
+
+// ------------------------------------------------------------------ fp32x2 helpers
+__device__ __forceinline__ float2 fmul2_ftz(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.ftz.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// ------------------------------------------------------------------ LUT access
+template <int W, bool GL>
+__device__ __forceinline__ uint32_t lut_ld(const uint8_t *lut, uint32_t off)
+{
+    if constexpr (GL) {
+        if constexpr (W == 8) return __ldg(lut + off);
+        else if constexpr (W == 16) return __ldg(reinterpret_cast<const uint16_t *>(lut + off));
+        else return __ldg(reinterpret_cast<const uint32_t *>(lut + off));
+    } else {
+        if constexpr (W == 8) return *(lut + off);
+        else if constexpr (W == 16) return *reinterpret_cast<const uint16_t *>(lut + off);
+        else return *reinterpret_cast<const uint32_t *>(lut + off);
+    }
+}
+
+// v = 2^carry * 1.mantissa as fp32: canonical entry + the bit pattern of 1.0f.
+__device__ __forceinline__ float expand(uint32_t narrowed, uint32_t mul)
+{
+    return __uint_as_float(narrowed * mul + 0x3F800000u);
+}
+
+// Operand decode (once per element per CTA): byte offset of the mantissa's LUT
+// row/column and the signed power-of-two scale 2^(e-127).  Zero and denormal
+// inputs give a signed zero scale, infinities an infinite scale, NaN a NaN scale.
+__device__ __forceinline__ void decode(float v, int M, int offshift, uint32_t &off, float &s, int &big)
+{
+    const uint32_t x = __float_as_uint(v);
+    const uint32_t e = (x >> 23) & 0xFFu;
+    const uint32_t f = x & 0x7FFFFFu;
+    off = (f >> (23 - M)) << offshift;
+    uint32_t sb = x & 0xFF800000u;          // e == 0 leaves only the sign
+    if (e == 255u && f) sb = 0x7FC00000u;
+    s = __uint_as_float(sb);
+    big |= (e >= 191u);
+}
+
+// ------------------------------------------------------------------ gather state
+struct KState {
+    int k0, k1;
+    int y, x;
+    long long b;
+};
+
+__device__ __forceinline__ KState kstate_at(const OperandDesc &d, int k)
+{
+    KState s;
+    int t = k / d.kD0;
+    s.k0 = k - t * d.kD0;
+    int k2 = t / d.kD1;
+    s.k1 = t - k2 * d.kD1;
+    s.y = s.k0 * d.kcy[0] + s.k1 * d.kcy[1] + k2 * d.kcy[2];
+    s.x = s.k0 * d.kcx[0] + s.k1 * d.kcx[1] + k2 * d.kcx[2];
+    s.b = (long long)s.k0 * d.kcb[0] + (long long)s.k1 * d.kcb[1] + (long long)k2 * d.kcb[2];
+    return s;
+}
+
+// Advance by delta >= 0 with carries between levels (no division).
+__device__ __forceinline__ void kstate_advance(const OperandDesc &d, KState &s, int delta)
+{
+    s.k0 += delta;
+    s.y += delta * d.kcy[0];
+    s.x += delta * d.kcx[0];
+    s.b += (long long)delta * d.kcb[0];
+    while (s.k0 >= d.kD0) {
+        s.k0 -= d.kD0;
+        s.y += d.kcy[1] - d.kD0 * d.kcy[0];
+        s.x += d.kcx[1] - d.kD0 * d.kcx[0];
+        s.b += d.kcb[1] - (long long)d.kD0 * d.kcb[0];
+        if (++s.k1 >= d.kD1) {
+            s.k1 = 0;
+            s.y += d.kcy[2] - d.kD1 * d.kcy[1];
+            s.x += d.kcx[2] - d.kD1 * d.kcx[1];
+            s.b += d.kcb[2] - (long long)d.kD1 * d.kcb[1];
+        }
+    }
+}
+
+__device__ __forceinline__ RowInfo row_info(const OperandDesc &d, int r)
+{
+    RowInfo ri;
+    if (r >= d.rows) {
+        ri.y = -(1 << 29);     // never in range
+        ri.x = 0;
+        ri.b = 0;
+        return ri;
+    }
+    int t = r / d.rE0;
+    int r0 = r - t * d.rE0;
+    int r2 = t / d.rE1;
+    int r1 = t - r2 * d.rE1;
+    ri.y = d.ry0 + r0 * d.rcy[0] + r1 * d.rcy[1] + r2 * d.rcy[2];
+    ri.x = d.rx0 + r0 * d.rcx[0] + r1 * d.rcx[1] + r2 * d.rcx[2];
+    ri.b = (long long)r0 * d.rcb[0] + (long long)r1 * d.rcb[1] + (long long)r2 * d.rcb[2];
+    return ri;
+}
+
+__device__ __forceinline__ float gather_value(const OperandDesc &d, const float *base, const RowInfo &ri,
+                                              const KState &ks)
+{
+    int y = ri.y + ks.y, x = ri.x + ks.x;
+    if (d.sy > 1) {
+        if (y < 0 || y % d.sy) return 0.0f;
+        y /= d.sy;
+    }
+    if (d.sx > 1) {
+        if (x < 0 || x % d.sx) return 0.0f;
+        x /= d.sx;
+    }
+    if ((unsigned)y >= (unsigned)d.IH || (unsigned)x >= (unsigned)d.IW) return 0.0f;
+    return __ldg(base + ri.b + ks.b + ((long long)y * d.IW + x) * d.Cs);
+}
+
+// ------------------------------------------------------------------ operand loader
+// R rows per tile, N elements per thread per stage.  "k-fast": thread t owns
+// reduction slot t % BK and rows t/BK + (NT/BK) e; "row-fast": thread t owns
+// row t % R and reduction slots t/R + (NT/R) e.  The host picks the mapping
+// that makes consecutive threads touch consecutive addresses.
+template <int R, int N>
+struct Loader {
+    int rsub, rstep, ksub0, kstep;
+    int row0;               // global row of tile row 0
+    const float *base;      // operand pointer + batch offset
+    KState ks;              // gather state at k = stage*BK + ksub0
+    float v[N];
+
+    __device__ __forceinline__ void init(const OperandDesc &d, bool kfast, int tid, int row_tile0, int b,
+                                         int kt_first)
+    {
+        if (kfast) { rsub = tid / BK; rstep = NT / BK; ksub0 = tid % BK; kstep = 0; }
+        else { rsub = tid % R; rstep = 0; ksub0 = tid / R; kstep = NT / R; }
+        row0 = row_tile0;
+        base = d.ptr + (long long)b * d.batch_stride;
+        if (d.gather) ks = kstate_at(d, kt_first * BK + ksub0);
+    }
+
+    __device__ __forceinline__ void load(const OperandDesc &d, const RowInfo *rowtab, int kt, int K)
+    {
+        const int kbase = kt * BK + ksub0;
+        if (!d.gather) {
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                const int r = row0 + rsub + rstep * e;
+                const int k = kbase + kstep * e;
+                v[e] = (r < d.rows && k < K) ? __ldg(base + (long long)r * d.s_row + (long long)k * d.s_k) : 0.0f;
+            }
+        } else {
+            KState s = ks;
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                const int k = kbase + kstep * e;
+                if (e > 0 && kstep) kstate_advance(d, s, kstep);
+                const RowInfo ri = rowtab[rsub + rstep * e];
+                v[e] = (k < K) ? gather_value(d, base, ri, s) : 0.0f;
+            }
+            kstate_advance(d, ks, BK);
+        }
+    }
+
+    // Decode into the stage buffers: off[k][row], scale[k][row] (row stride ST words).
+    template <int ST>
+    __device__ __forceinline__ void store(uint32_t *off, float *scl, int M, int offshift, int &big) const
+    {
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            const int r = rsub + rstep * e;
+            const int k = ksub0 + kstep * e;
+            uint32_t o;
+            float s;
+            decode(v[e], M, offshift, o, s, big);
+            off[k * ST + r] = o;
+            scl[k * ST + r] = s;
+        }
+    }
+};
+
+// ------------------------------------------------------------------ compute
+template <int W, bool GL, bool SLOW>
+__device__ __forceinline__ void compute_stage(float2 (&acc)[TM][TN / 2], const uint32_t *__restrict__ Uo,
+                                              const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
+                                              const float *__restrict__ Ls, const uint8_t *lut, uint32_t mul,
+                                              int urow, int lcol)
+{
+#pragma unroll 2
+    for (int kk = 0; kk < BK; ++kk) {
+        const uint4 lo = *reinterpret_cast<const uint4 *>(Lo + kk * LST + lcol);
+        const float4 ls = *reinterpret_cast<const float4 *>(Ls + kk * LST + lcol);
+        const float2 ls01 = make_float2(ls.x, ls.y), ls23 = make_float2(ls.z, ls.w);
+#pragma unroll
+        for (int ig = 0; ig < TM / 4; ++ig) {
+            const uint4 uo = *reinterpret_cast<const uint4 *>(Uo + kk * UST + urow + 4 * ig);
+            const float4 us = *reinterpret_cast<const float4 *>(Us + kk * UST + urow + 4 * ig);
+            const uint32_t uov[4] = {uo.x, uo.y, uo.z, uo.w};
+            const float usv[4] = {us.x, us.y, us.z, us.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t e0 = lut_ld<W, GL>(lut, uov[i] + lo.x);
+                const uint32_t e1 = lut_ld<W, GL>(lut, uov[i] + lo.y);
+                const uint32_t e2 = lut_ld<W, GL>(lut, uov[i] + lo.z);
+                const uint32_t e3 = lut_ld<W, GL>(lut, uov[i] + lo.w);
+                const float2 su = make_float2(usv[i], usv[i]);
+                const float2 s01 = fmul2_ftz(su, ls01);
+                const float2 s23 = fmul2_ftz(su, ls23);
+                const float2 v01 = make_float2(expand(e0, mul), expand(e1, mul));
+                const float2 v23 = make_float2(expand(e2, mul), expand(e3, mul));
+                float2 &a01 = acc[4 * ig + i][0];
+                float2 &a23 = acc[4 * ig + i][1];
+                if constexpr (SLOW) {
+                    a01 = fadd2(a01, fmul2(v01, s01));
+                    a23 = fadd2(a23, fmul2(v23, s23));
+                } else {
+                    a01 = ffma2(v01, s01, a01);
+                    a23 = ffma2(v23, s23, a23);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int W, bool GL>
+__global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ KParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int wu = warp / WL, wl = warp % WL;
+    const int tl = blockIdx.x % p.tiles_l, tu = blockIdx.x / p.tiles_l;
+    const int sp = blockIdx.y, b = blockIdx.z;
+    const int u_tile0 = tu * BU, l_tile0 = tl * BL;
+
+    const int lut_bytes = GL ? 0 : lut_region_bytes(p.table_bytes);
+    uint8_t *lut_s = smem;
+    uint32_t *Uoff = reinterpret_cast<uint32_t *>(smem + lut_bytes);
+    float *Uscl = reinterpret_cast<float *>(smem + lut_bytes + kUdecBytes);
+    uint32_t *Loff = reinterpret_cast<uint32_t *>(smem + lut_bytes + 2 * kUdecBytes);
+    float *Lscl = reinterpret_cast<float *>(smem + lut_bytes + 2 * kUdecBytes + kLdecBytes);
+    RowInfo *rowU = reinterpret_cast<RowInfo *>(smem + lut_bytes + 2 * kUdecBytes + 2 * kLdecBytes);
+    RowInfo *rowL = rowU + BU;
+
+    // LUT -> shared memory (the allocation is padded to 256 bytes, so whole
+    // 16-byte vectors stay inside it).
+    if constexpr (!GL) {
+        const uint4 *src = static_cast<const uint4 *>(p.table);
+        uint4 *dst = reinterpret_cast<uint4 *>(lut_s);
+        const int nvec = (p.table_bytes + 15) >> 4;
+        for (int i = tid; i < nvec; i += NT) dst[i] = __ldg(src + i);
+    }
+    if (p.U.gather)
+        for (int r = tid; r < BU; r += NT) rowU[r] = row_info(p.U, u_tile0 + r);
+    if (p.L.gather)
+        for (int r = tid; r < BL; r += NT) rowL[r] = row_info(p.L, l_tile0 + r);
+    __syncthreads();
+
+    const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.table) : lut_s;
+    const int kt0 = sp * p.kt_per_split;
+    const int kt1 = min(kt0 + p.kt_per_split, p.kt_total);
+    const int offU = p.M + p.wlog, offL = p.wlog;
+
+    float2 acc[TM][TN / 2];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+
+    if (kt0 < kt1) {
+        Loader<BU, NUE> ldU;
+        Loader<BL, NLE> ldL;
+        ldU.init(p.U, p.u_kfast, tid, u_tile0, b, kt0);
+        ldL.init(p.L, p.l_kfast, tid, l_tile0, b, kt0);
+        ldU.load(p.U, rowU, kt0, p.K);
+        ldL.load(p.L, rowL, kt0, p.K);
+        int big = 0;
+        ldU.template store<UST>(Uoff, Uscl, p.M, offU, big);
+        ldL.template store<LST>(Loff, Lscl, p.M, offL, big);
+        int slow = __syncthreads_or(big);
+
+        const int urow = wu * TM;
+        const int lcol = wl * 32 * TN + lane * TN;
+        for (int kt = kt0; kt < kt1; ++kt) {
+            const int buf = (kt - kt0) & 1;
+            const bool more = kt + 1 < kt1;
+            if (more) {
+                ldU.load(p.U, rowU, kt + 1, p.K);
+                ldL.load(p.L, rowL, kt + 1, p.K);
+            }
+            const uint32_t *Uo = Uoff + buf * BK * UST;
+            const float *Us = Uscl + buf * BK * UST;
+            const uint32_t *Lo = Loff + buf * BK * LST;
+            const float *Ls = Lscl + buf * BK * LST;
+            if (slow) compute_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, p.mul, urow, lcol);
+            else compute_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, p.mul, urow, lcol);
+            int nbig = 0;
+            if (more) {
+                const int nb = buf ^ 1;
+                ldU.template store<UST>(Uoff + nb * BK * UST, Uscl + nb * BK * UST, p.M, offU, nbig);
+                ldL.template store<LST>(Loff + nb * BK * LST, Lscl + nb * BK * LST, p.M, offL, nbig);
+            }
+            slow = __syncthreads_or(nbig);
+        }
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    const int u0 = u_tile0 + wu * TM;
+    const int l0 = l_tile0 + wl * 32 * TN + lane * TN;
+    const int nU = p.U.rows, nL = p.L.rows;
+    if (p.splits > 1) {
+        float *w = p.ws + (((long long)b * p.splits + sp) * nU) * p.ws_ld;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int u = u0 + i;
+            if (u >= nU) break;
+            float *row = w + (long long)u * p.ws_ld + l0;
+            if (l0 + TN <= p.ws_ld) {
+                *reinterpret_cast<float4 *>(row) = make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
+            }
+        }
+        return;
+    }
+    float *C = p.c_ptr + (long long)b * p.c_bs;
+    const float alpha = p.alpha, beta = p.beta;
+    const bool vec_l = p.c_sl == 1 && (p.c_su & 3) == 0 && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
+    const bool vec_u = p.c_su == 1 && (p.c_sl & 3) == 0 && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
+    if (vec_l && l0 + TN <= nL) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int u = u0 + i;
+            if (u >= nU) break;
+            float4 *dst = reinterpret_cast<float4 *>(C + (long long)u * p.c_su + l0);
+            float4 r = make_float4(alpha * acc[i][0].x, alpha * acc[i][0].y, alpha * acc[i][1].x,
+                                   alpha * acc[i][1].y);
+            if (beta != 0.0f) {
+                const float4 o = *dst;
+                r.x = fmaf(beta, o.x, r.x); r.y = fmaf(beta, o.y, r.y);
+                r.z = fmaf(beta, o.z, r.z); r.w = fmaf(beta, o.w, r.w);
+            }
+            *dst = r;
+        }
+    } else if (vec_u && u0 + TM <= nU) {
+#pragma unroll
+        for (int t = 0; t < TN; ++t) {
+            const int l = l0 + t;
+            if (l >= nL) break;
+            float *col = C + (long long)l * p.c_sl + u0;
+#pragma unroll
+            for (int i4 = 0; i4 < TM / 4; ++i4) {
+                float4 r;
+                r.x = alpha * ((t & 1) ? acc[4 * i4 + 0][t >> 1].y : acc[4 * i4 + 0][t >> 1].x);
+                r.y = alpha * ((t & 1) ? acc[4 * i4 + 1][t >> 1].y : acc[4 * i4 + 1][t >> 1].x);
+                r.z = alpha * ((t & 1) ? acc[4 * i4 + 2][t >> 1].y : acc[4 * i4 + 2][t >> 1].x);
+                r.w = alpha * ((t & 1) ? acc[4 * i4 + 3][t >> 1].y : acc[4 * i4 + 3][t >> 1].x);
+                float4 *dst = reinterpret_cast<float4 *>(col + 4 * i4);
+                if (beta != 0.0f) {
+                    const float4 o = *dst;
+                    r.x = fmaf(beta, o.x, r.x); r.y = fmaf(beta, o.y, r.y);
+                    r.z = fmaf(beta, o.z, r.z); r.w = fmaf(beta, o.w, r.w);
+                }
+                *dst = r;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int u = u0 + i;
+            if (u >= nU) break;
+#pragma unroll
+            for (int t = 0; t < TN; ++t) {
+                const int l = l0 + t;
+                if (l >= nL) break;
+                float *dst = C + (long long)u * p.c_su + (long long)l * p.c_sl;
+                float r = alpha * ((t & 1) ? acc[i][t >> 1].y : acc[i][t >> 1].x);
+                if (beta != 0.0f) r = fmaf(beta, *dst, r);
+                *dst = r;
+            }
+        }
+    }
+}
+
+}  // namespace kern
+}  // namespace amsim
+
+namespace amsim {
+namespace kern {
+
+// Host-side launcher for one instance; sets the dynamic shared-memory limit
+// once per device.
+template <int W, bool GL>
+int launch_instance(const KParams &p, dim3 grid, size_t smem, cudaStream_t st)
+{
+    static bool attr_done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AMSIM_ECUDA;
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(lutgemm_kernel<W, GL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kMaxSmemPerCta);
+        if (e != cudaSuccess) return cuda_status(e);
+        attr_done[dev] = true;
+    }
+    lutgemm_kernel<W, GL><<<grid, NT, smem, st>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_w8(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+int launch_w16(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+int launch_w32(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+
+}  // namespace kern
+}  // namespace amsim

@@ -1,0 +1,13 @@
+// Instances of the LUT-GEMM kernel for 8-bit narrowed LUT entries.
+#include "gemm_kernel.cuh"
+
+namespace amsim {
+namespace kern {
+
+int launch_w8(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st)
+{
+    return gl ? launch_instance<8, true>(p, grid, smem, st) : launch_instance<8, false>(p, grid, smem, st);
+}
+
+}  // namespace kern
+}  // namespace amsim

@@ -1,0 +1,224 @@
+"""The five layer workloads as sequences of library calls (device tensors in,
+device tensors out).  Each ``run()`` is one pass of the workload's contractions
+through the C ABI on one stream; the benchmark, the smoke check and the
+full-size parity tests all drive these same objects, so they time and check
+the same launch configuration.
+
+Operand order of every contraction follows the layer's data flow:
+Dense forward (x, w); preceding-layer gradient (dy, w); weight gradient
+(x, dy); conv likewise; attention (q, k) then (p, v).
+"""
+from __future__ import annotations
+
+from . import (ConvDesc, amsim_conv2d_bwd_data, amsim_conv2d_bwd_filter, amsim_conv2d_fwd,
+               amsim_conv2d_out_hw, amsim_conv2d_workspace_size, amsim_gemm, amsim_gemm_strided_batched,
+               amsim_gemm_workspace_size, amsim_softmax_rows, workspace)
+
+
+def _dev(t, device):
+    import torch
+    if isinstance(t, torch.Tensor):
+        return t.to(device)
+    return torch.from_numpy(t).to(device)
+
+
+class GemmCall:
+    """One row-major GEMM C = alpha op(A) op(B) + beta C on device tensors."""
+
+    def __init__(self, A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0):
+        self.A, self.B, self.C = A, B, C
+        self.tA, self.tB = ("T" if transA else "N"), ("T" if transB else "N")
+        self.m = A.shape[1] if transA else A.shape[0]
+        self.k = A.shape[0] if transA else A.shape[1]
+        self.n = B.shape[0] if transB else B.shape[1]
+        self.alpha, self.beta = alpha, beta
+
+    @property
+    def macs(self) -> int:
+        return self.m * self.n * self.k
+
+    def ws_bytes(self, lut) -> int:
+        return amsim_gemm_workspace_size(self.tA, self.tB, self.m, self.n, self.k, 1, lut)
+
+    def __call__(self, lut, ws, stream=None):
+        amsim_gemm(self.tA, self.tB, self.m, self.n, self.k, self.alpha, self.A, max(1, self.A.shape[1]),
+                   self.B, max(1, self.B.shape[1]), self.beta, self.C, max(1, self.n), lut, ws=ws,
+                   stream=stream)
+
+
+class MLPStep:
+    """3-layer MLP (784-1000-500-10, batch 256): forward Y_l = X_l W_l, then
+    for every layer dX_l = dY_l W_l^T and dW_l = X_l^T dY_l (pure linear
+    layers; X_{l+1} = Y_l; dY_l synthetic per layer)."""
+
+    def __init__(self, data: dict, lut, device="cuda"):
+        import torch
+        self.lut = lut
+        d = {k: _dev(v, device) for k, v in data.items()}
+        self.inputs = d
+        f32 = dict(dtype=torch.float32, device=device)
+        X = d["X"]
+        self.Y, self.dX, self.dW, self.calls = [], [], [], []
+        xin = X
+        for l in range(3):
+            W = d[f"W{l + 1}"]
+            Y = torch.empty((X.shape[0], W.shape[1]), **f32)
+            self.calls.append(GemmCall(xin, W, Y))
+            self.Y.append(Y)
+            xin = Y
+        xs = [X, self.Y[0], self.Y[1]]
+        for l in range(3):
+            W, dY = d[f"W{l + 1}"], d[f"dY{l + 1}"]
+            dX = torch.empty((dY.shape[0], W.shape[0]), **f32)
+            dW = torch.empty_like(W)
+            self.calls.append(GemmCall(dY, W, dX, transB=True))
+            self.calls.append(GemmCall(xs[l], dY, dW, transA=True))
+            self.dX.append(dX)
+            self.dW.append(dW)
+        self.ws = workspace(max(c.ws_bytes(lut) for c in self.calls), device)
+
+    @property
+    def macs(self) -> int:
+        return sum(c.macs for c in self.calls)
+
+    def outputs(self) -> list:
+        return self.Y + self.dX + self.dW
+
+    def parts(self, stream=None):
+        """(name, zero-argument launcher, approximate MACs, kernel launches) per ABI call."""
+        names = ["fwd1", "fwd2", "fwd3", "dX1", "dW1", "dX2", "dW2", "dX3", "dW3"]
+        out = []
+        for nm, c in zip(names, self.calls):
+            out.append((nm, (lambda c=c: c(self.lut, self.ws, stream)), c.macs, 1 + (c.ws_bytes(self.lut) > 0)))
+        return out
+
+    def run(self, stream=None):
+        for c in self.calls:
+            c(self.lut, self.ws, stream)
+
+
+class ConvStep:
+    """Conv2D forward, preceding-layer gradient and weight gradient of one
+    NHWC layer (implicit GEMMs)."""
+
+    def __init__(self, data: dict, geom: dict, lut, device="cuda", passes=(0, 1, 2)):
+        import torch
+        self.lut = lut
+        g = geom
+        self.desc = ConvDesc.make(g["N"], g["H"], g["W"], g["C"], g["K"], g["R"], g["S"], g["stride"], g["pad"],
+                                  g["dil"])
+        self.P, self.Q = amsim_conv2d_out_hw(self.desc)
+        self.x = _dev(data["x"], device)
+        self.w = _dev(data["w"], device)
+        self.dy = _dev(data["dy"], device) if "dy" in data else None
+        self.passes = tuple(passes)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.y = torch.empty((g["N"], self.P, self.Q, g["K"]), **f32)
+        self.dx = torch.empty_like(self.x) if 1 in self.passes else None
+        self.dw = torch.empty_like(self.w) if 2 in self.passes else None
+        self.g = g
+        self.ws = workspace(max(amsim_conv2d_workspace_size(self.desc, p, lut) for p in self.passes), device)
+
+    @property
+    def macs(self) -> int:
+        g = self.g
+        return len(self.passes) * g["N"] * self.P * self.Q * g["K"] * g["R"] * g["S"] * g["C"]
+
+    def outputs(self) -> list:
+        return [t for t in (self.y, self.dx, self.dw) if t is not None]
+
+    def parts(self, stream=None):
+        g = self.g
+        per = g["N"] * self.P * self.Q * g["K"] * g["R"] * g["S"] * g["C"]
+        fns = {0: ("fwd", lambda: amsim_conv2d_fwd(self.desc, self.x, self.w, self.y, self.lut, ws=self.ws,
+                                                   stream=stream)),
+               1: ("bwd_data", lambda: amsim_conv2d_bwd_data(self.desc, self.dy, self.w, self.dx, self.lut,
+                                                             ws=self.ws, stream=stream)),
+               2: ("bwd_filter", lambda: amsim_conv2d_bwd_filter(self.desc, self.x, self.dy, self.dw, self.lut,
+                                                                 ws=self.ws, stream=stream))}
+        return [(fns[p][0], fns[p][1], per, 1 + (amsim_conv2d_workspace_size(self.desc, p, self.lut) > 0))
+                for p in self.passes]
+
+    def run(self, stream=None):
+        if 0 in self.passes:
+            amsim_conv2d_fwd(self.desc, self.x, self.w, self.y, self.lut, ws=self.ws, stream=stream)
+        if 1 in self.passes:
+            amsim_conv2d_bwd_data(self.desc, self.dy, self.w, self.dx, self.lut, ws=self.ws, stream=stream)
+        if 2 in self.passes:
+            amsim_conv2d_bwd_filter(self.desc, self.x, self.dy, self.dw, self.lut, ws=self.ws, stream=stream)
+
+
+class SquareGemmStep:
+    def __init__(self, data: dict, lut, device="cuda"):
+        import torch
+        self.lut = lut
+        self.A = _dev(data["A"], device)
+        self.B = _dev(data["B"], device)
+        self.C = torch.empty((self.A.shape[0], self.B.shape[1]), dtype=torch.float32, device=device)
+        self.call = GemmCall(self.A, self.B, self.C)
+        self.ws = workspace(self.call.ws_bytes(lut), device)
+
+    @property
+    def macs(self) -> int:
+        return self.call.macs
+
+    def outputs(self) -> list:
+        return [self.C]
+
+    def parts(self, stream=None):
+        return [("gemm", lambda: self.call(self.lut, self.ws, stream), self.call.macs,
+                 1 + (self.call.ws_bytes(self.lut) > 0))]
+
+    def run(self, stream=None):
+        self.call(self.lut, self.ws, stream)
+
+
+class AttentionStep:
+    """S = Q K^T / sqrt(d) (batched over batch*heads), exact fp32 row softmax,
+    O = P V (batched).  Q, K, V: (batch, heads, seq, dim)."""
+
+    def __init__(self, data: dict, lut, device="cuda"):
+        import torch
+        self.lut = lut
+        self.Q = _dev(data["Q"], device)
+        self.K = _dev(data["K"], device)
+        self.V = _dev(data["V"], device)
+        b, h, s, dd = self.Q.shape
+        self.bh, self.s, self.d = b * h, s, dd
+        f32 = dict(dtype=torch.float32, device=device)
+        self.S = torch.empty((b, h, s, s), **f32)
+        self.P = torch.empty((b, h, s, s), **f32)
+        self.O = torch.empty((b, h, s, dd), **f32)
+        self.scale = 1.0 / float(dd) ** 0.5
+        n1 = amsim_gemm_workspace_size("N", "T", s, s, dd, self.bh, lut)
+        n2 = amsim_gemm_workspace_size("N", "N", s, dd, s, self.bh, lut)
+        self.ws = workspace(max(n1, n2), device)
+
+    @property
+    def macs(self) -> int:
+        return 2 * self.bh * self.s * self.s * self.d
+
+    def outputs(self) -> list:
+        return [self.S, self.P, self.O]
+
+    def parts(self, stream=None):
+        s, d, bh = self.s, self.d, self.bh
+        n1 = amsim_gemm_workspace_size("N", "T", s, s, d, bh, self.lut) > 0
+        n2 = amsim_gemm_workspace_size("N", "N", s, d, s, bh, self.lut) > 0
+        return [
+            ("scores", lambda: amsim_gemm_strided_batched("N", "T", s, s, d, self.scale, self.Q, d, s * d, self.K, d,
+                                                          s * d, 0.0, self.S, s, s * s, bh, self.lut, ws=self.ws,
+                                                          stream=stream), bh * s * s * d, 1 + n1),
+            ("softmax", lambda: amsim_softmax_rows(self.S, self.P, bh * s, s, stream=stream), 0, 1),
+            ("pv", lambda: amsim_gemm_strided_batched("N", "N", s, d, s, 1.0, self.P, s, s * s, self.V, d, s * d,
+                                                      0.0, self.O, d, s * d, bh, self.lut, ws=self.ws,
+                                                      stream=stream), bh * s * s * d, 1 + n2),
+        ]
+
+    def run(self, stream=None):
+        s, d, bh = self.s, self.d, self.bh
+        amsim_gemm_strided_batched("N", "T", s, s, d, self.scale, self.Q, d, s * d, self.K, d, s * d, 0.0, self.S,
+                                   s, s * s, bh, self.lut, ws=self.ws, stream=stream)
+        amsim_softmax_rows(self.S, self.P, bh * s, s, stream=stream)
+        amsim_gemm_strided_batched("N", "N", s, d, s, 1.0, self.P, s, s * s, self.V, d, s * d, 0.0, self.O, d,
+                                   s * d, bh, self.lut, ws=self.ws, stream=stream)

@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of the LUT-multiplier contractions on one GB300 (or N replicas).
+
+Default workload: the 3-layer MLP 784-1000-500-10 at batch 256, forward
+Y = XW plus backward dX = dY W^T and dW = X^T dY for every layer, all products
+through the Mitchell M=7 LUT (989,952,000 approximate MACs per step).  Other
+workloads (--workload) exist for the design tables; they print the same line.
+
+Prints one JSON line (rank 0).  Timing: W warm-up steps, then K steps, each
+bracketed by CUDA events on the launching stream; before each timed step the
+L2 is flushed (256 MiB write) and the GPU is held by a short sleep kernel so
+that all launches of the step are queued before it starts (neither is inside
+the events).  ``--impl reference`` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "approx-GMAC/s for LUT-multiplier GEMM/conv at M=7"
+UNIT = "approx-GMAC/s"
+LOOKUPS_PER_CLK_PER_SM = 32     # one 4-byte shared-memory wavefront per clock per SM
+
+WORKLOADS = ("mlp", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "gemm64")
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+# ---------------------------------------------------------------- workloads
+def make_step(name, lut_for):
+    from approximate_multiplier_dnn_gb300 import steps
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    if name == "mlp":
+        return steps.MLPStep(wl.mlp(), lut_for("mitchell", 7)), "mlp_784-1000-500-10_b256_fwd+dX+dW_mitchell_M7"
+    if name == "conv3x3":
+        return (steps.ConvStep(wl.conv3x3(), wl.CONV3X3, lut_for("mitchell", 7)),
+                "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_mitchell_M7")
+    if name == "conv3x3_exact":
+        return (steps.ConvStep(wl.conv3x3(), wl.CONV3X3, lut_for("exact", 7)),
+                "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_exact_M7")
+    if name == "gemm4096":
+        return steps.SquareGemmStep(wl.square_gemm(4096), lut_for("mitchell", 7)), "gemm_4096^3_mitchell_M7"
+    if name == "attention":
+        return steps.AttentionStep(wl.attention(), lut_for("mitchell", 7)), "attention_32x16x512x64_mitchell_M7"
+    if name == "conv1x1":
+        return (steps.ConvStep(wl.conv1x1(), wl.CONV1X1, lut_for("mitchell", 7), passes=(0,)),
+                "conv1x1_nhwc_64x56x56x256_k256_fwd_mitchell_M7")
+    if name == "gemm64":
+        from approximate_multiplier_dnn_gb300 import steps as st
+        import torch
+        d = wl.gemm_small()
+        s = st.SquareGemmStep(d, lut_for("mitchell", 7))
+        return s, "gemm_64x128x64_mitchell_M7"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def oracle_parts(name):
+    """(oracle callable over a row subset, rows, MACs per row) for the reference
+    leg: the same contractions the GPU step runs, one row range at a time."""
+    import numpy as np
+    import oracle
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    out = []
+    if name == "mlp":
+        d = wl.mlp()
+        # layers 2 and 3 take synthetic activations of the right shape here
+        # (the oracle's cost does not depend on the values)
+        xs = [d["X"], wl.normal((256, 1000), 1.0, 90), wl.normal((256, 500), 1.0, 91)]
+        for l in range(3):
+            W, dY = d[f"W{l + 1}"], d[f"dY{l + 1}"]
+            X = xs[l]
+            out.append((lambda rows, X=X, W=W: oracle.gemm("mitchell", 7, X, W, rows=rows), X.shape[0],
+                        W.shape[0] * W.shape[1]))
+            out.append((lambda rows, dY=dY, W=W: oracle.gemm("mitchell", 7, dY, W, transB=True, rows=rows),
+                        dY.shape[0], W.shape[0] * W.shape[1]))
+            out.append((lambda rows, X=X, dY=dY: oracle.gemm("mitchell", 7, X, dY, transA=True, rows=rows),
+                        X.shape[1], dY.shape[0] * dY.shape[1]))
+        return out
+    if name == "gemm4096":
+        d = wl.square_gemm(4096)
+        return [(lambda rows: oracle.gemm("mitchell", 7, d["A"], d["B"], rows=rows), 4096, 4096 * 4096)]
+    raise SystemExit(f"no oracle sampler for workload {name}")
+
+
+def run_oracle_sample(parts, target_s, nthreads, start=0):
+    """Run row chunks of each contraction round-robin until target_s has
+    elapsed; returns (MACs done, seconds)."""
+    import numpy as np
+    t0 = time.perf_counter()
+    macs = 0
+    i = start
+    while True:
+        for fn, nrows, per_row in parts:
+            r = np.arange(i * nthreads, (i + 1) * nthreads) % nrows
+            fn(r.astype(np.int32))
+            macs += per_row * r.size
+        i += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    return macs, time.perf_counter() - t0
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu_id)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    try:
+        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    if vis:
+        return vis.split(",")[torch.cuda.current_device()]
+    return torch.cuda.current_device()
+
+
+# ---------------------------------------------------------------- traffic record
+def recorded_traffic(workload):
+    """Per-launch DRAM bytes of the LUT-GEMM kernel from a committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    src = os.path.join(ROOT, "approximate_multiplier_dnn_gb300", "csrc", "gemm_kernel.cuh")
+    try:
+        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
+            for line in f:
+                kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
+                if kv.get("workload") == workload and kv.get("kernel_sha1") == sha:
+                    return float(kv["bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- reference arm
+def reference_arm(args, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    parts = oracle_parts(args.workload)
+    cores = os.cpu_count() or 1
+    # warm-up then K bounded steps: each step one row chunk per contraction
+    for w in range(args.warmup):
+        run_oracle_sample(parts, 0.0, cores, start=w)
+    macs = 0
+    secs = 0.0
+    for s in range(args.steps):
+        m, t = run_oracle_sample(parts, 0.0, cores, start=args.warmup + s)
+        macs += m
+        secs += t
+    value = macs / secs / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "sample": f"{cores} rows of each contraction per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{cores} output rows of each contraction per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mlp", choices=WORKLOADS)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank, world = env_int("RANK", 0), env_int("WORLD_SIZE", 1)
+    local = env_int("LOCAL_RANK", 0)
+
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import approximate_multiplier_dnn_gb300 as am
+
+    am.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    luts = {}
+
+    def lut_for(kind, M):
+        if (kind, M) not in luts:
+            luts[(kind, M)] = am.Lut.build(kind, M)
+        return luts[(kind, M)]
+
+    step, wname = make_step(args.workload, lut_for)
+    stream = torch.cuda.current_stream()
+    parts = step.parts()
+    props = torch.cuda.get_device_properties(local)
+    sms = props.multi_processor_count
+
+    # warm-up (also sets kernel attributes) and enqueue-time estimate
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        for p in parts:
+            p[1]()
+    enqueue_s = (time.perf_counter() - t0) / 5
+    torch.cuda.synchronize()
+    sleep_cycles = int(min(max(2.0 * enqueue_s, 50e-6), 20e-3) * 2.1e9)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
+
+    sampler = ClockSampler(gpu_id_for_smi(torch))
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for s in range(K):
+        flush.fill_(float(s))
+        torch.cuda._sleep(sleep_cycles)
+        evs[s][0].record(stream)
+        for i, p in enumerate(parts):
+            p[1]()
+            evs[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+
+    step_ms = [evs[s][0].elapsed_time(evs[s][-1]) for s in range(K)]
+    part_ms = [sum(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(K)) / K for i in range(len(parts))]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    macs = step.macs
+    value = world * macs * K / (total_ms * 1e-3) / 1e9
+    ms_per_step = total_ms / K
+
+    # dominant kernel: the LUT-GEMM (every part with MACs), lookups = MACs
+    lut_parts = [i for i, p in enumerate(parts) if p[2] > 0]
+    lut_ms = sum(part_ms[i] for i in lut_parts)
+    lut_macs = sum(parts[i][2] for i in lut_parts)
+    launches_lut = sum(1 for _ in lut_parts)
+    achieved = lut_macs / (lut_ms * 1e-3) / 1e9            # Glookup/s
+    mhz = clocks["sm_mhz"] or props.clock_rate / 1e3
+    peak = sms * LOOKUPS_PER_CLK_PER_SM * mhz * 1e6 / 1e9   # Glookup/s
+    traffic = recorded_traffic(wname)
+
+    # end to end: pinned host inputs -> device, step, outputs -> pinned host
+    e2e = None
+    if hasattr(step, "inputs"):
+        inputs = step.inputs
+    elif hasattr(step, "x"):
+        inputs = {k: getattr(step, k) for k in ("x", "w", "dy") if getattr(step, k, None) is not None}
+    elif hasattr(step, "Q"):
+        inputs = {"Q": step.Q, "K": step.K, "V": step.V}
+    else:
+        inputs = {"A": step.A, "B": step.B}
+    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu()) for k, v in inputs.items()}
+    outs = step.outputs()
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    E = max(1, min(args.e2e_steps, K))
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E)]
+    torch.cuda.synchronize()
+    for s in range(E):
+        torch.cuda._sleep(sleep_cycles * 2)
+        e_ev[s][0].record(stream)
+        for k, v in inputs.items():
+            v.copy_(host_in[k], non_blocking=True)
+        step.run()
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+        e_ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e_ev) / E
+    e2e = {"value": world * macs / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("mlp", "gemm4096"):
+        import oracle
+        oracle.build()
+        cores = os.cpu_count() or 1
+        m, secs = run_oracle_sample(oracle_parts(args.workload), args.cpu_seconds, cores)
+        cpu = {"value": m / secs / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{m} MACs: round-robin chunks of {cores} output rows over every contraction, "
+                         f"{secs:.1f} s wall"}
+
+    launches_per_step = sum(p[3] for p in parts)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wname, "macs_per_step": macs, "l2": "flushed before every timed step "
+                       "(256 MiB write, outside the timed events)", "parallelism": f"replicas{world}"},
+            "roofline": {"bound": "alu", "pipe": "shared-memory LUT lookups: SMs x 32 per clock x SM clock",
+                         "achieved": achieved, "peak": peak, "unit": "Glookup/s", "frac": achieved / peak,
+                         "traffic": traffic, "kernel": "lutgemm_kernel (+ split-K reduce inside the same calls)",
+                         "launches_timed": launches_lut, "sms": sms, "sm_mhz": mhz},
+            "parts_ms": {p[0]: round(t, 5) for p, t in zip(parts, part_ms)},
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * K,
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
+                       "samples": clocks["samples"]},
+            "wall_s": wall,
+        }
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

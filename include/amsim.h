@@ -1,0 +1,229 @@
+/*
+ * amsim.h -- C ABI of the GB300 (sm_103a) library that simulates approximate
+ * floating-point multipliers inside DNN contractions with a mantissa-product
+ * lookup table, after "ApproxTrain: Fast Simulation of Approximate Multipliers
+ * for DNN Training and Inference" (arXiv 2209.04161).
+ *
+ * Every scalar product a*b inside the contractions below is replaced by the
+ * AMSim product of Sec. V-B, Algorithm 2:
+ *   sign      = sign(a) XOR sign(b)
+ *   index     = (top-M fraction bits of a) << M | (top-M fraction bits of b)
+ *   entry     = LUT[index] = carry << 23 | 23-bit mantissa     (Sec. V-A, fn. 2)
+ *   e0        = biased exp(a) + biased exp(b) - 127
+ *   result    = signed zero      if e0 <= 0 or an input is zero,
+ *               signed infinity  if e0 >= 255,
+ *               sign | (e0 + carry) << 23 | mantissa   otherwise.
+ * Readings of points the page leaves open (the design notes list them):
+ *   denormal inputs count as zero; NaN in -> NaN; infinity times zero or a
+ *   denormal -> NaN; infinity times anything else -> signed infinity; an
+ *   exponent that reaches 255 through the carry -> signed infinity; the zero
+ *   test precedes the carry adjustment.  Accumulation is IEEE fp32; alpha and
+ *   beta are IEEE fp32 scalings, not simulated.
+ *
+ * Conventions for every call:
+ *   - All tensors are fp32, dense, row-major (C order), owned by the caller.
+ *     Pointers named "host_*" are host memory; all others are device memory
+ *     of the device that was current when the LUT handle was built.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work: they do not synchronise, do not allocate device memory and
+ *     do not copy to or from the host (the LUT build calls excepted).
+ *   - `ws`/`ws_bytes` is optional caller-owned device scratch (256-byte
+ *     aligned).  With less than the size the matching *_workspace_size query
+ *     returns, a call still runs correctly with a plan that needs less
+ *     scratch (possibly slower).  A call never reads scratch contents left by
+ *     an earlier call; calls sharing one scratch buffer must be ordered on the
+ *     GPU (same stream or events).
+ *   - Return value: AMSIM_OK or an amsim_status code.  Arguments are checked
+ *     on the host before anything is enqueued; on error nothing is enqueued
+ *     and outputs are untouched.  A failed launch returns AMSIM_ECUDA.
+ *     Kernels contain no device-side asserts or traps.
+ *   - Results are deterministic: the same call on the same inputs with the
+ *     same scratch size gives bit-identical outputs.
+ */
+#ifndef AMSIM_H
+#define AMSIM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct amsim_lut_s *amsim_lut_t;  /* opaque; owns its device table */
+typedef void *amsim_stream_t;             /* a cudaStream_t */
+
+enum amsim_kind {
+    AMSIM_EXACT = 0,     /* exact product of the M-bit-truncated mantissas: (1+x)(1+y) */
+    AMSIM_MITCHELL = 1   /* Mitchell logarithmic multiplier: 1+x+y if x+y<1, else 2(x+y) */
+};
+
+enum amsim_status {
+    AMSIM_OK = 0,
+    AMSIM_EINVAL = 1,        /* bad argument (null pointer, negative size, bad stride, wrong device) */
+    AMSIM_EUNSUPPORTED = 2,  /* M outside [1,11], unknown kind, a LUT entry outside carry 0/1 */
+    AMSIM_ENOMEM = 3,        /* the LUT's device (or host) allocation failed */
+    AMSIM_ECUDA = 4          /* a CUDA runtime call or kernel launch failed */
+};
+
+/* Human-readable text for a status code (static storage). */
+const char *amsim_status_string(int status);
+
+/* ------------------------------------------------------------------ LUTs */
+
+/*
+ * Algorithm 1 (Sec. V-A) on the host: for every mantissa pair (p, q) in
+ * [0,2^M)^2, form A = 1.p and B = 1.q with non-special exponents, multiply them
+ * with the closed-form model of `kind`, compare the product's exponent with the
+ * unnormalised one to find the carry, and store carry << 23 | mantissa at
+ * index p << M | q.  `host_entries` receives 2^(2M) uint32 values (4 B each, as
+ * fn. 2 prescribes: M=7 -> 65,536 B, M=11 -> 16,777,216 B).  No device work.
+ * Errors: AMSIM_EUNSUPPORTED for M outside [1,11] or an unknown kind,
+ * AMSIM_EINVAL for a null pointer.
+ */
+int amsim_lut_generate(int kind, int M, uint32_t *host_entries);
+
+/*
+ * Algorithm 1 with a user-supplied multiplier model `approx_mul` (the "C/C++
+ * approximate multiplication function" of Sec. V-A / Fig. 7).  The function is
+ * called with normal operands in [1,2) and must return a positive normal
+ * product in [1,4).  An entry whose exponent moves by anything but 0 or +1
+ * yields AMSIM_EUNSUPPORTED.  Host only.
+ */
+typedef float (*amsim_approx_mul_fn)(float a, float b);
+int amsim_lut_generate_from_fn(amsim_approx_mul_fn approx_mul, int M, uint32_t *host_entries);
+
+/*
+ * Build a device-resident LUT handle on the current device from Algorithm 1
+ * for `kind` (host generation + one synchronous upload; call once, outside any
+ * timed or captured region).  The handle keeps the canonical 4-byte entries and
+ * a losslessly narrowed copy (8, 16 or 32 bits per entry, whichever is the
+ * narrowest that holds every entry exactly) in both index orders, which the
+ * contraction kernels stage in shared memory when it fits.
+ */
+int amsim_lut_build(int kind, int M, amsim_lut_t *out);
+
+/*
+ * Same as amsim_lut_build for an arbitrary table of 2^(2M) canonical entries
+ * (carry << 23 | mantissa, carry in {0,1}), e.g. produced by
+ * amsim_lut_generate_from_fn or loaded from a file at run time (Sec. VI,
+ * "LUTs are loaded into the operator library at run time").  The table need
+ * not be symmetric.  Errors: AMSIM_EUNSUPPORTED if an entry has bits above 23.
+ */
+int amsim_lut_build_from_entries(const uint32_t *host_entries, int M, amsim_lut_t *out);
+
+/* Copy the 2^(2M) canonical entries of a handle back to host memory (synchronous). */
+int amsim_lut_entries(amsim_lut_t lut, uint32_t *host_dst);
+
+/* M, narrowed entry width in bits, and the left shift that restores an entry. */
+int amsim_lut_info(amsim_lut_t lut, int *M, int *width_bits, int *shift);
+
+/* Free the handle's device memory.  NULL is ignored. */
+void amsim_lut_destroy(amsim_lut_t lut);
+
+/* ------------------------------------------------------------------ elementwise */
+
+/*
+ * c[i] = AMSim(a[i], b[i]) for i < n (Sec. V-B, Algorithm 2), bit-exact, NaN
+ * results canonical (0x7FC00000).  a, b, c: device fp32 arrays of n elements;
+ * c may alias a or b.  n == 0 is a no-op.
+ */
+int amsim_mul(const float *a, const float *b, float *c, int64_t n, amsim_lut_t lut,
+              amsim_stream_t stream);
+
+/* ------------------------------------------------------------------ GEMM */
+
+/*
+ * C = alpha * op(A) op(B) + beta * C with every product an AMSim product whose
+ * first operand (high LUT index bits) is the element of A (Sec. VI-D, "GEMM
+ * kernel"; Sec. VI-C AMDENSE forward and gradients).  Row-major:
+ *   op(A) is m x k: A is m x k (lda >= k) for transA 'N', k x m (lda >= m) for 'T';
+ *   op(B) is k x n: B is k x n (ldb >= n) for transB 'N', n x k (ldb >= k) for 'T';
+ *   C is m x n with ldc >= n.
+ * beta == 0 does not read C.  m, n or k == 0 is allowed (k == 0 gives beta*C).
+ * Scratch: see amsim_gemm_workspace_size.
+ */
+int amsim_gemm(char transA, char transB, int m, int n, int k, float alpha,
+               const float *A, int lda, const float *B, int ldb, float beta,
+               float *C, int ldc, amsim_lut_t lut, void *ws, size_t ws_bytes,
+               amsim_stream_t stream);
+
+/*
+ * `batch` independent GEMMs as above; problem i uses A + i*strideA,
+ * B + i*strideB, C + i*strideC (element strides, >= 0).  Used for the two
+ * contractions of attention (S = Q K^T with transB 'T', O = P V).
+ */
+int amsim_gemm_strided_batched(char transA, char transB, int m, int n, int k, float alpha,
+                               const float *A, int lda, int64_t strideA,
+                               const float *B, int ldb, int64_t strideB, float beta,
+                               float *C, int ldc, int64_t strideC, int batch,
+                               amsim_lut_t lut, void *ws, size_t ws_bytes,
+                               amsim_stream_t stream);
+
+/* Bytes of scratch with which the GEMM calls above run their fastest plan. */
+size_t amsim_gemm_workspace_size(char transA, char transB, int m, int n, int k, int batch,
+                                 amsim_lut_t lut);
+
+/* ------------------------------------------------------------------ Conv2D */
+
+/*
+ * Convolution geometry.  Activations are NHWC, filters RSCK (TF's HWIO, the
+ * layout of the TensorFlow ops ApproxTrain replaces), outputs NPQK with
+ *   P = (H + 2 pad_h - dil_h (R-1) - 1) / stride_h + 1, Q likewise.
+ * The operation is cross-correlation; padded taps are zero operands.
+ */
+typedef struct amsim_conv_desc {
+    int N, H, W, C;     /* input batch, height, width, channels */
+    int K, R, S;        /* output channels, filter height, filter width */
+    int stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
+} amsim_conv_desc;
+
+/* Output height/width of a descriptor; AMSIM_EINVAL if the geometry is empty. */
+int amsim_conv2d_out_hw(const amsim_conv_desc *desc, int *P, int *Q);
+
+/*
+ * Forward (Sec. VI-B, Algorithm 3, Fig. 8a, IM2COL + GEMM, here an implicit
+ * GEMM with the im2col addressing fused into the operand loads):
+ *   y[n,p,q,k] = sum_{r,s,c} AMSim(x[n, p*sh - ph + r*dh, q*sw - pw + s*dw, c], w[r,s,c,k]).
+ * x: N*H*W*C, w: R*S*C*K, y: N*P*Q*K (written, not accumulated).
+ */
+int amsim_conv2d_fwd(const amsim_conv_desc *desc, const float *x, const float *w, float *y,
+                     amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);
+
+/*
+ * Preceding-layer gradient (Algorithm 4 lines 6-8: IM2COL_PLG over the
+ * padded-dilated errors and TransposeAndReverse of the filter, here folded into
+ * the operand addressing):
+ *   dx[n,h,w,c] = sum_{r,s,k} AMSim(dy[n,p,q,k], w[r,s,c,k]),
+ *   p = (h + ph - r*dh)/sh, q = (w + pw - s*dw)/sw where integral and in range.
+ * dy: N*P*Q*K, w: R*S*C*K, dx: N*H*W*C (written).
+ */
+int amsim_conv2d_bwd_data(const amsim_conv_desc *desc, const float *dy, const float *w, float *dx,
+                          amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);
+
+/*
+ * Weight gradient (Algorithm 4 lines 4-5: IM2COL_Weight + GEMM):
+ *   dw[r,s,c,k] = sum_{n,p,q} AMSim(x[n, p*sh - ph + r*dh, q*sw - pw + s*dw, c], dy[n,p,q,k]).
+ * x: N*H*W*C, dy: N*P*Q*K, dw: R*S*C*K (written).  The long reduction over
+ * N*P*Q is split across CTAs when scratch allows, reduced in a fixed order.
+ */
+int amsim_conv2d_bwd_filter(const amsim_conv_desc *desc, const float *x, const float *dy, float *dw,
+                            amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);
+
+/* which: 0 forward, 1 bwd_data, 2 bwd_filter. Bytes of scratch for the fastest plan. */
+size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim_lut_t lut);
+
+/* ------------------------------------------------------------------ glue */
+
+/*
+ * Exact fp32 row softmax P[r,:] = exp(S[r,:] - max) / sum(...) for `rows` rows of
+ * `cols` contiguous values (ld = cols).  Not simulated: attention's softmax
+ * sits between its two approximate contractions.  P may alias S.
+ */
+int amsim_softmax_rows(const float *S, float *P, int64_t rows, int cols, amsim_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AMSIM_H */

@@ -29,3 +29,31 @@ def orc():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def amd():
+    """The built library on a CUDA device (fails loudly when either is missing)."""
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import approximate_multiplier_dnn_gb300 as am
+    am.build()
+    am.lib()
+    torch.cuda.set_device(0)
+    return am
+
+
+@pytest.fixture(scope="session")
+def luts(amd):
+    """Device LUT handles, built once per (kind, M)."""
+    cache = {}
+
+    def get(kind, M):
+        key = (kind, M)
+        if key not in cache:
+            cache[key] = amd.Lut.build(kind, M)
+        return cache[key]
+
+    yield get
+    for v in cache.values():
+        v.close()

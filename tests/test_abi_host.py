@@ -1,0 +1,101 @@
+"""Host-side checks of libamsim (no GPU needed): the library loads, exports
+every function include/amsim.h declares, its host-only Algorithm 1 LUT
+generator agrees with the oracle's for every mantissa width and both kinds,
+user-supplied multiplier models go through the same generator, and argument
+errors are reported before any device work."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import approximate_multiplier_dnn_gb300 as am
+
+
+@pytest.fixture(scope="module")
+def L():
+    am.build()
+    return am.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = am.header_functions()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for s in range(5):
+        assert am.status_string(s)
+    assert am.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("kind", ["exact", "mitchell"])
+@pytest.mark.parametrize("M", list(range(1, 12)))
+def test_lut_generate_matches_oracle(L, orc, kind, M):
+    assert np.array_equal(am.amsim_lut_generate(kind, M), orc.lut(kind, M))
+
+
+def test_lut_generate_errors(L):
+    buf = np.zeros(4, np.uint32)
+    assert L.amsim_lut_generate(0, 0, buf.ctypes.data) == am.AMSIM_EUNSUPPORTED
+    assert L.amsim_lut_generate(0, 12, buf.ctypes.data) == am.AMSIM_EUNSUPPORTED
+    assert L.amsim_lut_generate(7, 1, buf.ctypes.data) == am.AMSIM_EUNSUPPORTED
+    assert L.amsim_lut_generate(0, 1, None) == am.AMSIM_EINVAL
+
+
+def test_lut_generate_from_user_function(L, orc):
+    """A user model (here: Python callbacks of the two closed forms on floats)
+    goes through Algorithm 1 and must reproduce the built-in tables."""
+    def exact(a, b):
+        return float(np.float32(a) * np.float32(b))
+
+    def mitchell(a, b):
+        x, y = a - 1.0, b - 1.0
+        return 1.0 + x + y if x + y < 1.0 else 2.0 * (x + y)
+
+    for M in (1, 3, 5):
+        assert np.array_equal(am.amsim_lut_generate_from_fn(exact, M), orc.lut("exact", M))
+        assert np.array_equal(am.amsim_lut_generate_from_fn(mitchell, M), orc.lut("mitchell", M))
+
+
+def test_lut_generate_from_fn_rejects_bad_model(L):
+    with pytest.raises(am.AmsimError) as e:
+        am.amsim_lut_generate_from_fn(lambda a, b: 0.25 * a * b, 3)   # exponent drops below the operands'
+    assert e.value.status == am.AMSIM_EUNSUPPORTED
+    with pytest.raises(am.AmsimError):
+        am.amsim_lut_generate_from_fn(lambda a, b: -a * b, 3)          # negative product
+
+
+def test_conv_out_hw_matches_oracle(L, orc):
+    cases = [(2, 7, 6, 3, 4, 3, 3, (1, 1), (1, 1), (1, 1)), (1, 9, 8, 2, 5, 3, 2, (2, 1), (1, 0), (1, 1)),
+             (2, 8, 9, 3, 2, 3, 3, (1, 2), (2, 2), (2, 1)), (128, 32, 32, 64, 64, 3, 3, (1, 1), (1, 1), (1, 1))]
+    for N, H, W, C, K, R, S, st, pd, dl in cases:
+        d = am.ConvDesc.make(N, H, W, C, K, R, S, st, pd, dl)
+        assert am.amsim_conv2d_out_hw(d) == orc.conv_out_hw(orc.conv_desc(N, H, W, C, K, R, S, st, pd, dl))
+    with pytest.raises(am.AmsimError):
+        am.amsim_conv2d_out_hw(am.ConvDesc.make(1, 2, 2, 1, 1, 5, 5))
+
+
+def test_calls_reject_null_lut_without_device_work(L):
+    vp = ctypes.c_void_p
+    assert L.amsim_mul(None, None, None, 4, None, None) == am.AMSIM_EINVAL
+    assert L.amsim_gemm(b"N", b"N", 2, 2, 2, 1.0, None, 2, None, 2, 0.0, None, 2, None, None, 0,
+                        None) == am.AMSIM_EINVAL
+    d = am.ConvDesc.make(1, 4, 4, 1, 1, 3, 3)
+    assert L.amsim_conv2d_fwd(ctypes.byref(d), None, None, None, None, None, 0, None) == am.AMSIM_EINVAL
+    assert L.amsim_gemm_workspace_size(b"N", b"N", 8, 8, 8, 1, None) == 0
+    assert L.amsim_conv2d_workspace_size(ctypes.byref(d), 0, None) == 0
+    L.amsim_lut_destroy(vp(None))     # NULL is ignored
+    assert L.amsim_lut_info(None, None, None, None) == am.AMSIM_EINVAL
+    assert L.amsim_lut_entries(None, None) == am.AMSIM_EINVAL
+    assert L.amsim_softmax_rows(None, None, -1, 4, None) == am.AMSIM_EINVAL
+    assert L.amsim_softmax_rows(None, None, 0, 4, None) == am.AMSIM_OK
+
+
+def test_lut_build_from_entries_rejects_wide_entries(L):
+    e = np.zeros(16, np.uint32)
+    e[3] = 1 << 24
+    h = ctypes.c_void_p(0)
+    assert L.amsim_lut_build_from_entries(e.ctypes.data, 2, ctypes.byref(h)) == am.AMSIM_EUNSUPPORTED
+    assert L.amsim_lut_build_from_entries(e.ctypes.data, 0, ctypes.byref(h)) == am.AMSIM_EUNSUPPORTED

@@ -1,0 +1,178 @@
+"""LUT-GEMM on the GPU against the CPU oracle (ApproxTrain Sec. VI-D GEMM
+kernel, Sec. VI-C AMDENSE): all transpose combinations, ragged shapes that span
+several CTA tiles, alpha/beta, split-K with and without scratch, special
+operands, batched strided GEMMs, guard canaries and run-to-run determinism.
+Tolerance: |gpu - oracle| <= 1e-5 * sum_k |AMSim product| per element."""
+import numpy as np
+import pytest
+
+from gpu_helpers import REL, assert_close, guarded, guards_intact, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_gemm(amd, lut, A, B, ta, tb, alpha=1.0, beta=0.0, C0=None, ws="auto", batch_strides=None):
+    import torch
+    m = A.shape[1] if ta else A.shape[0]
+    k = A.shape[0] if ta else A.shape[1]
+    n = B.shape[0] if tb else B.shape[1]
+    dA, dB = to_dev(A), to_dev(B)
+    buf, C = guarded((m, n), C0 if C0 is not None else np.zeros((m, n), np.float32))
+    tA, tB = ("T" if ta else "N"), ("T" if tb else "N")
+    if ws == "auto":
+        nbytes = amd.amsim_gemm_workspace_size(tA, tB, m, n, k, 1, lut)
+        wsb = amd.workspace(nbytes)
+    else:
+        wsb = ws
+    amd.amsim_gemm(tA, tB, m, n, k, alpha, dA, max(1, A.shape[1]), dB, max(1, B.shape[1]), beta, C, max(1, n),
+                   lut, ws=wsb)
+    torch.cuda.synchronize()
+    assert guards_intact(buf), "write outside C"
+    return C.cpu().numpy()
+
+
+def check(orc, kind, M, A, B, ta, tb, got, alpha=1.0, beta=0.0, C0=None, what=""):
+    ref, sa = orc.gemm(kind, M, A, B, transA=ta, transB=tb, alpha=alpha, beta=beta, C0=C0)
+    scale = abs(alpha) * sa
+    if C0 is not None and beta != 0.0:
+        scale = scale + abs(beta) * np.abs(C0.astype(np.float64)) / REL * 2.0 ** -23
+    assert_close(got, ref, scale + 1e-30, what)
+
+
+def rnd(rng, shape, kind="normal"):
+    if kind == "normal":
+        return rng.standard_normal(shape).astype(np.float32)
+    return rng.uniform(-1, 1, size=shape).astype(np.float32)
+
+
+@pytest.mark.parametrize("kind", ["mitchell", "exact"])
+def test_small_gemm_workload(amd, orc, luts, kind):
+    """64x128 by 128x64, U[-1,1], seed 0 (the small GEMM workload)."""
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    d = wl.gemm_small()
+    got = gpu_gemm(amd, luts(kind, 7), d["A"], d["B"], False, False)
+    check(orc, kind, 7, d["A"], d["B"], False, False, got, what=f"gemm64 {kind}")
+
+
+SHAPES = [(1, 1, 1), (3, 17, 31), (33, 65, 129), (100, 300, 50), (257, 10, 500), (10, 257, 77),
+          (130, 520, 40), (64, 256, 16), (65, 257, 17)]
+
+
+@pytest.mark.parametrize("ta", [False, True])
+@pytest.mark.parametrize("tb", [False, True])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_shapes_and_transposes(amd, orc, luts, shape, ta, tb):
+    m, n, k = shape
+    rng = np.random.default_rng(m * 10007 + n * 101 + k + 2 * ta + tb)
+    A = rnd(rng, (k, m) if ta else (m, k))
+    B = rnd(rng, (n, k) if tb else (k, n))
+    got = gpu_gemm(amd, luts("mitchell", 7), A, B, ta, tb)
+    check(orc, "mitchell", 7, A, B, ta, tb, got, what=f"{shape} {ta}{tb}")
+
+
+@pytest.mark.parametrize("M", [4, 7, 8, 11])
+@pytest.mark.parametrize("kind", ["mitchell", "exact"])
+def test_widths_and_residency(amd, orc, luts, kind, M):
+    """8/16/32-bit narrowed tables; shared-memory and global-memory residency."""
+    rng = np.random.default_rng(M)
+    A = rnd(rng, (70, 90), "uniform")
+    B = rnd(rng, (90, 300), "uniform")
+    got = gpu_gemm(amd, luts(kind, M), A, B, False, False)
+    check(orc, kind, M, A, B, False, False, got, what=f"{kind} M={M}")
+
+
+def test_alpha_beta(amd, orc, luts):
+    rng = np.random.default_rng(5)
+    A, B = rnd(rng, (50, 70)), rnd(rng, (70, 90))
+    C0 = rnd(rng, (50, 90))
+    got = gpu_gemm(amd, luts("mitchell", 7), A, B, False, False, alpha=0.125, beta=-1.5, C0=C0)
+    check(orc, "mitchell", 7, A, B, False, False, got, alpha=0.125, beta=-1.5, C0=C0, what="alpha/beta")
+
+
+def test_k_zero_gives_beta_c(amd, luts):
+    rng = np.random.default_rng(6)
+    C0 = rnd(rng, (5, 7))
+    got = gpu_gemm(amd, luts("mitchell", 7), np.zeros((5, 0), np.float32), np.zeros((0, 7), np.float32),
+                   False, False, alpha=1.0, beta=2.0, C0=C0)
+    assert np.array_equal(got, (2.0 * C0).astype(np.float32))
+
+
+@pytest.mark.parametrize("with_ws", [True, False])
+def test_split_k(amd, orc, luts, with_ws):
+    """Few output tiles and a long reduction: split across CTAs when scratch is
+    given (fixed-order reduction), a single pass otherwise."""
+    rng = np.random.default_rng(7)
+    A, B = rnd(rng, (60, 4000)), rnd(rng, (4000, 70))
+    lut = luts("mitchell", 7)
+    assert amd.amsim_gemm_workspace_size("N", "N", 60, 70, 4000, 1, lut) > 0
+    got = gpu_gemm(amd, lut, A, B, False, False, ws="auto" if with_ws else None)
+    check(orc, "mitchell", 7, A, B, False, False, got, what=f"split-k ws={with_ws}")
+
+
+def test_special_operands(amd, orc, luts):
+    """Zeros, denormals, infinities, NaNs and huge values (|x| >= 2^64, the
+    slower exact-overflow path) inside the operands."""
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    rng = np.random.default_rng(8)
+    a, b = wl.special_values_mix(40 * 96 + 96 * 50, seed=9)
+    A = a[:40 * 96].reshape(40, 96).copy()
+    B = b[40 * 96:40 * 96 + 96 * 50].reshape(96, 50).copy()
+    # keep most rows/columns finite so most outputs are finite
+    A[:, :] = np.where(rng.random(A.shape) < 0.9, rng.standard_normal(A.shape), A).astype(np.float32)
+    B[:, :] = np.where(rng.random(B.shape) < 0.9, rng.standard_normal(B.shape), B).astype(np.float32)
+    for kind in ("mitchell", "exact"):
+        got = gpu_gemm(amd, luts(kind, 7), A, B, False, False)
+        check(orc, kind, 7, A, B, False, False, got, what=f"specials {kind}")
+
+
+def test_huge_values_overflow_to_inf(amd, orc, luts):
+    """Products whose exponent reaches 255 through the LUT carry give infinity."""
+    A = np.full((4, 8), np.float32(1.5 * 2.0 ** 127))
+    B = np.full((8, 4), np.float32(1.5))
+    got = gpu_gemm(amd, luts("mitchell", 7), A, B, False, False)
+    ref, _ = orc.gemm("mitchell", 7, A, B)
+    assert np.all(np.isinf(ref)) and np.array_equal(got, ref)
+
+
+def test_batched_strided_attention_like(amd, orc, luts):
+    import torch
+    rng = np.random.default_rng(10)
+    batch, s, d = 3, 70, 64
+    Q = rnd(rng, (batch, s, d))
+    K = rnd(rng, (batch, s, d))
+    lut = luts("mitchell", 7)
+    dQ, dK = to_dev(Q), to_dev(K)
+    buf, S = guarded((batch, s, s))
+    nb = amd.amsim_gemm_workspace_size("N", "T", s, s, d, batch, lut)
+    amd.amsim_gemm_strided_batched("N", "T", s, s, d, 0.125, dQ, d, s * d, dK, d, s * d, 0.0, S, s, s * s, batch,
+                                   lut, ws=amd.workspace(nb))
+    torch.cuda.synchronize()
+    assert guards_intact(buf)
+    got = S.cpu().numpy()
+    for b in range(batch):
+        ref, sa = orc.gemm("mitchell", 7, Q[b], K[b], transB=True, alpha=0.125)
+        assert_close(got[b], ref, 0.125 * sa, f"batch {b}")
+
+
+def test_deterministic(amd, luts):
+    rng = np.random.default_rng(11)
+    A, B = rnd(rng, (300, 500)), rnd(rng, (500, 200))
+    lut = luts("mitchell", 7)
+    g1 = gpu_gemm(amd, lut, A, B, False, False)
+    g2 = gpu_gemm(amd, lut, A, B, False, False)
+    assert np.array_equal(g1.view(np.uint32), g2.view(np.uint32))
+
+
+def test_argument_errors(amd, luts):
+    import torch
+    lut = luts("mitchell", 7)
+    x = torch.zeros(64, device="cuda")
+    with pytest.raises(amd.AmsimError) as e:
+        amd.amsim_gemm("N", "N", 4, 4, 4, 1.0, x, 3, x, 4, 0.0, x, 4, lut)    # lda < k
+    assert e.value.status == amd.AMSIM_EINVAL
+    with pytest.raises(amd.AmsimError):
+        amd.amsim_gemm("X", "N", 4, 4, 4, 1.0, x, 4, x, 4, 0.0, x, 4, lut)
+    with pytest.raises(amd.AmsimError):
+        amd.amsim_gemm("N", "N", -1, 4, 4, 1.0, x, 4, x, 4, 0.0, x, 4, lut)
+    with pytest.raises(amd.AmsimError):
+        amd.amsim_gemm("N", "N", 4, 4, 4, 1.0, None, 4, x, 4, 0.0, x, 4, lut)
