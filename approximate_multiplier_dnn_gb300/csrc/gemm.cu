@@ -47,10 +47,10 @@ Plan make_plan(const Problem &p, int sms, size_t ws_avail)
     pl.kt_per_split = std::max(1, pl.kt_total);
     pl.ws_bytes = 0;
     const long long tiles = (long long)pl.tiles_u * pl.tiles_l * p.batch;
-    // Split the reduction only when the output tiles leave SMs idle; keep at
-    // least 4 stages per split and one wave of CTAs.
-    if (tiles < sms && pl.kt_total >= 8) {
-        int want = (int)std::min<long long>(sms / tiles, pl.kt_total / 4);
+    // Split the reduction only when the output tiles leave SMs idle: as many
+    // splits as fit in one wave, at least two stages per split.
+    if (tiles < sms && pl.kt_total >= 4) {
+        int want = (int)std::min<long long>(sms / tiles, pl.kt_total / 2);
         want = std::min(want, 65535);
         if (want > 1) {
             int kps = ceil_div(pl.kt_total, want);
@@ -122,7 +122,8 @@ int run_problem(const Problem &p, amsim_lut_t lut, void *ws, size_t ws_bytes, cu
     kp.kt_per_split = pl.kt_per_split;
     kp.kt_total = pl.kt_total;
     kp.table = p.u_is_first ? lut->d_narrow : lut->d_narrow_t;
-    const bool gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
+    const bool gl = lut->narrow_bytes > (size_t)kMaxSmemLut ||
+                    (size_t)kern::kFixedSmem + kern::lut_region_bytes((int)lut->narrow_bytes) > (size_t)kMaxSmemPerCta;
     kp.table_bytes = gl ? 0 : (int)lut->narrow_bytes;
     kp.M = lut->M;
     kp.mul = 1u << lut->shift;

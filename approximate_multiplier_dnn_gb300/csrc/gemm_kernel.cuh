@@ -29,18 +29,38 @@
 namespace amsim {
 namespace kern {
 
-constexpr int NT = 256;            // threads per CTA
-constexpr int BU = 64;             // uniform rows per CTA tile
-constexpr int BL = 256;            // lane columns per CTA tile
-constexpr int BK = 16;             // reduction depth per stage
-constexpr int TM = 16;             // uniform rows per warp
-constexpr int TN = 4;              // lane columns per thread
-constexpr int WU = BU / TM;        // 4 warps along U
-constexpr int WL = BL / (32 * TN); // 2 warps along L
+#ifndef AMSIM_NT
+#define AMSIM_NT 256
+#endif
+#ifndef AMSIM_BU
+#define AMSIM_BU 64
+#endif
+#ifndef AMSIM_BL
+#define AMSIM_BL 256
+#endif
+#ifndef AMSIM_BK
+#define AMSIM_BK 16
+#endif
+#ifndef AMSIM_TM
+#define AMSIM_TM 16
+#endif
+#ifndef AMSIM_TN
+#define AMSIM_TN 4
+#endif
+constexpr int NT = AMSIM_NT;       // threads per CTA
+constexpr int BU = AMSIM_BU;       // uniform rows per CTA tile
+constexpr int BL = AMSIM_BL;       // lane columns per CTA tile
+constexpr int BK = AMSIM_BK;       // reduction depth per stage
+constexpr int TM = AMSIM_TM;       // uniform rows per warp (processed in pairs)
+constexpr int TN = AMSIM_TN;       // lane columns per thread
+constexpr int WU = BU / TM;        // warps along U
+constexpr int WL = BL / (32 * TN); // warps along L
 constexpr int UST = BU + 4;        // decoded U row stride (words), 16-B aligned, few bank conflicts
 constexpr int LST = BL + 4;        // decoded L row stride (words)
-constexpr int NUE = BU * BK / NT;  // U elements loaded per thread per stage (4)
-constexpr int NLE = BL * BK / NT;  // L elements loaded per thread per stage (16)
+constexpr int NUE = BU * BK / NT;  // U elements loaded per thread per stage
+constexpr int NLE = BL * BK / NT;  // L elements loaded per thread per stage
+static_assert(TM % 4 == 0 && TN % 4 == 0, "micro-tile");
+static_assert(NT % BU == 0 && NT % BL == 0 && NT % BK == 0, "loader mapping");
 static_assert(WU * WL * 32 == NT, "warp layout");
 
 struct RowInfo {
@@ -143,9 +163,28 @@ __device__ __forceinline__ uint32_t lut_ld(const uint8_t *lut, uint32_t off)
 }
 
 // v = 2^carry * 1.mantissa as fp32: canonical entry + the bit pattern of 1.0f.
+#ifndef AMSIM_EXPAND_MODE
+#define AMSIM_EXPAND_MODE 0
+#endif
 __device__ __forceinline__ float expand(uint32_t narrowed, uint32_t mul)
 {
+#if AMSIM_EXPAND_MODE == 1
+    uint32_t r;
+    asm("shl.b32 %0, %1, 16;\n\tadd.u32 %0, %0, 0x3F800000;" : "=r"(r) : "r"(narrowed));
+    return __uint_as_float(r);
+#else
     return __uint_as_float(narrowed * mul + 0x3F800000u);
+#endif
+}
+__device__ __forceinline__ float expand_alu(uint32_t narrowed, uint32_t mul)
+{
+#if AMSIM_EXPAND_MODE == 2
+    uint32_t r;
+    asm("shl.b32 %0, %1, 16;\n\tadd.u32 %0, %0, 0x3F800000;" : "=r"(r) : "r"(narrowed));
+    return __uint_as_float(r);
+#else
+    return expand(narrowed, mul);
+#endif
 }
 
 // Operand decode (once per element per CTA): byte offset of the mantissa's LUT
@@ -303,42 +342,58 @@ struct Loader {
 };
 
 // ------------------------------------------------------------------ compute
+// Accumulator of uniform row i, lane column t.
+__device__ __forceinline__ float accv(const float2 (&acc)[TM / 2][TN], int i, int t)
+{
+    return (i & 1) ? acc[i >> 1][t].y : acc[i >> 1][t].x;
+}
+
+// One stage of BK reduction steps.  acc[p][t] holds rows (2p, 2p+1) of the
+// warp's TM uniform rows for lane column t, so the U scales pair up straight
+// from the vector loads and only the L scale is duplicated (once per column).
 template <int W, bool GL, bool SLOW>
-__device__ __forceinline__ void compute_stage(float2 (&acc)[TM][TN / 2], const uint32_t *__restrict__ Uo,
+__device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                               const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
                                               const float *__restrict__ Ls, const uint8_t *lut, uint32_t mul,
                                               int urow, int lcol)
 {
-#pragma unroll 2
+#pragma unroll 1
     for (int kk = 0; kk < BK; ++kk) {
-        const uint4 lo = *reinterpret_cast<const uint4 *>(Lo + kk * LST + lcol);
-        const float4 ls = *reinterpret_cast<const float4 *>(Ls + kk * LST + lcol);
-        const float2 ls01 = make_float2(ls.x, ls.y), ls23 = make_float2(ls.z, ls.w);
+        uint32_t lo[TN];
+        float2 sb[TN];
+#pragma unroll
+        for (int t4 = 0; t4 < TN / 4; ++t4) {
+            const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * LST + lcol + 4 * t4);
+            const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * LST + lcol + 4 * t4);
+            lo[4 * t4 + 0] = o.x; lo[4 * t4 + 1] = o.y; lo[4 * t4 + 2] = o.z; lo[4 * t4 + 3] = o.w;
+            sb[4 * t4 + 0] = make_float2(sc.x, sc.x);
+            sb[4 * t4 + 1] = make_float2(sc.y, sc.y);
+            sb[4 * t4 + 2] = make_float2(sc.z, sc.z);
+            sb[4 * t4 + 3] = make_float2(sc.w, sc.w);
+        }
 #pragma unroll
         for (int ig = 0; ig < TM / 4; ++ig) {
             const uint4 uo = *reinterpret_cast<const uint4 *>(Uo + kk * UST + urow + 4 * ig);
             const float4 us = *reinterpret_cast<const float4 *>(Us + kk * UST + urow + 4 * ig);
             const uint32_t uov[4] = {uo.x, uo.y, uo.z, uo.w};
-            const float usv[4] = {us.x, us.y, us.z, us.w};
+            const float2 sa[2] = {make_float2(us.x, us.y), make_float2(us.z, us.w)};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t e0 = lut_ld<W, GL>(lut, uov[i] + lo.x);
-                const uint32_t e1 = lut_ld<W, GL>(lut, uov[i] + lo.y);
-                const uint32_t e2 = lut_ld<W, GL>(lut, uov[i] + lo.z);
-                const uint32_t e3 = lut_ld<W, GL>(lut, uov[i] + lo.w);
-                const float2 su = make_float2(usv[i], usv[i]);
-                const float2 s01 = fmul2_ftz(su, ls01);
-                const float2 s23 = fmul2_ftz(su, ls23);
-                const float2 v01 = make_float2(expand(e0, mul), expand(e1, mul));
-                const float2 v23 = make_float2(expand(e2, mul), expand(e3, mul));
-                float2 &a01 = acc[4 * ig + i][0];
-                float2 &a23 = acc[4 * ig + i][1];
-                if constexpr (SLOW) {
-                    a01 = fadd2(a01, fmul2(v01, s01));
-                    a23 = fadd2(a23, fmul2(v23, s23));
-                } else {
-                    a01 = ffma2(v01, s01, a01);
-                    a23 = ffma2(v23, s23, a23);
+            for (int ip = 0; ip < 2; ++ip) {
+#pragma unroll
+                for (int t = 0; t < TN; ++t) {
+                    const uint32_t ea = lut_ld<W, GL>(lut, uov[2 * ip] + lo[t]);
+                    const uint32_t eb = lut_ld<W, GL>(lut, uov[2 * ip + 1] + lo[t]);
+                    const float2 v = make_float2(expand(ea, mul), expand_alu(eb, mul));
+                    const float2 s = fmul2_ftz(sa[ip], sb[t]);
+                    float2 &a = acc[2 * ig + ip][t];
+                    if constexpr (SLOW) {
+                        // product rounded to fp32 first (infinity on overflow), then added;
+                        // the _rn intrinsics are never contracted into an FMA
+                        a.x = __fadd_rn(a.x, __fmul_rn(v.x, s.x));
+                        a.y = __fadd_rn(a.y, __fmul_rn(v.y, s.y));
+                    } else {
+                        a = ffma2(v, s, a);
+                    }
                 }
             }
         }
@@ -385,11 +440,11 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
     const int kt1 = min(kt0 + p.kt_per_split, p.kt_total);
     const int offU = p.M + p.wlog, offL = p.wlog;
 
-    float2 acc[TM][TN / 2];
+    float2 acc[TM / 2][TN];
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
+    for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
-        for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+        for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
     if (kt0 < kt1) {
         Loader<BU, NUE> ldU;
@@ -439,30 +494,38 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
             const int u = u0 + i;
             if (u >= nU) break;
             float *row = w + (long long)u * p.ws_ld + l0;
-            if (l0 + TN <= p.ws_ld) {
-                *reinterpret_cast<float4 *>(row) = make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
+#pragma unroll
+            for (int t4 = 0; t4 < TN / 4; ++t4) {
+                if (l0 + 4 * t4 + 4 <= p.ws_ld)
+                    *reinterpret_cast<float4 *>(row + 4 * t4) =
+                        make_float4(accv(acc, i, 4 * t4), accv(acc, i, 4 * t4 + 1), accv(acc, i, 4 * t4 + 2),
+                                    accv(acc, i, 4 * t4 + 3));
             }
         }
         return;
     }
     float *C = p.c_ptr + (long long)b * p.c_bs;
     const float alpha = p.alpha, beta = p.beta;
-    const bool vec_l = p.c_sl == 1 && (p.c_su & 3) == 0 && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
-    const bool vec_u = p.c_su == 1 && (p.c_sl & 3) == 0 && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
+    const bool aligned = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+    const bool vec_l = aligned && p.c_sl == 1 && (p.c_su & 3) == 0;
+    const bool vec_u = aligned && p.c_su == 1 && (p.c_sl & 3) == 0;
     if (vec_l && l0 + TN <= nL) {
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             const int u = u0 + i;
             if (u >= nU) break;
-            float4 *dst = reinterpret_cast<float4 *>(C + (long long)u * p.c_su + l0);
-            float4 r = make_float4(alpha * acc[i][0].x, alpha * acc[i][0].y, alpha * acc[i][1].x,
-                                   alpha * acc[i][1].y);
-            if (beta != 0.0f) {
-                const float4 o = *dst;
-                r.x = fmaf(beta, o.x, r.x); r.y = fmaf(beta, o.y, r.y);
-                r.z = fmaf(beta, o.z, r.z); r.w = fmaf(beta, o.w, r.w);
+#pragma unroll
+            for (int t4 = 0; t4 < TN / 4; ++t4) {
+                float4 *dst = reinterpret_cast<float4 *>(C + (long long)u * p.c_su + l0 + 4 * t4);
+                float4 r = make_float4(alpha * accv(acc, i, 4 * t4), alpha * accv(acc, i, 4 * t4 + 1),
+                                       alpha * accv(acc, i, 4 * t4 + 2), alpha * accv(acc, i, 4 * t4 + 3));
+                if (beta != 0.0f) {
+                    const float4 o = *dst;
+                    r.x = fmaf(beta, o.x, r.x); r.y = fmaf(beta, o.y, r.y);
+                    r.z = fmaf(beta, o.z, r.z); r.w = fmaf(beta, o.w, r.w);
+                }
+                *dst = r;
             }
-            *dst = r;
         }
     } else if (vec_u && u0 + TM <= nU) {
 #pragma unroll
@@ -472,11 +535,8 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
             float *col = C + (long long)l * p.c_sl + u0;
 #pragma unroll
             for (int i4 = 0; i4 < TM / 4; ++i4) {
-                float4 r;
-                r.x = alpha * ((t & 1) ? acc[4 * i4 + 0][t >> 1].y : acc[4 * i4 + 0][t >> 1].x);
-                r.y = alpha * ((t & 1) ? acc[4 * i4 + 1][t >> 1].y : acc[4 * i4 + 1][t >> 1].x);
-                r.z = alpha * ((t & 1) ? acc[4 * i4 + 2][t >> 1].y : acc[4 * i4 + 2][t >> 1].x);
-                r.w = alpha * ((t & 1) ? acc[4 * i4 + 3][t >> 1].y : acc[4 * i4 + 3][t >> 1].x);
+                float4 r = make_float4(alpha * accv(acc, 4 * i4, t), alpha * accv(acc, 4 * i4 + 1, t),
+                                       alpha * accv(acc, 4 * i4 + 2, t), alpha * accv(acc, 4 * i4 + 3, t));
                 float4 *dst = reinterpret_cast<float4 *>(col + 4 * i4);
                 if (beta != 0.0f) {
                     const float4 o = *dst;
@@ -496,7 +556,7 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
                 const int l = l0 + t;
                 if (l >= nL) break;
                 float *dst = C + (long long)u * p.c_su + (long long)l * p.c_sl;
-                float r = alpha * ((t & 1) ? acc[i][t >> 1].y : acc[i][t >> 1].x);
+                float r = alpha * accv(acc, i, t);
                 if (beta != 0.0f) r = fmaf(beta, *dst, r);
                 *dst = r;
             }
