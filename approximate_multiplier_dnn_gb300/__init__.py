@@ -49,6 +49,22 @@ class ConvDesc(ctypes.Structure):
 APPROX_MUL_FN = ctypes.CFUNCTYPE(ctypes.c_float, ctypes.c_float, ctypes.c_float)
 
 
+class GemmProblem(ctypes.Structure):
+    """amsim_gemm_problem: one GEMM of a grouped launch."""
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+                ("strideA", ctypes.c_int64), ("strideB", ctypes.c_int64), ("strideC", ctypes.c_int64),
+                ("m", ctypes.c_int), ("n", ctypes.c_int), ("k", ctypes.c_int), ("lda", ctypes.c_int),
+                ("ldb", ctypes.c_int), ("ldc", ctypes.c_int), ("batch", ctypes.c_int),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("transA", ctypes.c_char), ("transB", ctypes.c_char)]
+
+    @classmethod
+    def make(cls, transA, transB, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, strideA=0, strideB=0, strideC=0,
+             batch=1):
+        return cls(_ptr(A), _ptr(B), _ptr(C), strideA, strideB, strideC, m, n, k, lda, ldb, ldc, batch,
+                   float(alpha), float(beta), transA.encode(), transB.encode())
+
+
 def build():
     from . import build_ext
     return build_ext.build()
@@ -78,6 +94,8 @@ def lib():
         "amsim_gemm_strided_batched": ([ch, ch, i32, i32, i32, f32, vp, i32, i64, vp, i32, i64, f32, vp, i32,
                                         i64, i32, vp, vp, sz, vp], i32),
         "amsim_gemm_workspace_size": ([ch, ch, i32, i32, i32, i32, vp], sz),
+        "amsim_gemm_grouped": ([i32, ctypes.POINTER(GemmProblem), vp, vp, sz, vp], i32),
+        "amsim_gemm_grouped_workspace_size": ([i32, ctypes.POINTER(GemmProblem), vp], sz),
         "amsim_conv2d_out_hw": ([ctypes.POINTER(ConvDesc), ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "amsim_conv2d_fwd": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
         "amsim_conv2d_bwd_data": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
@@ -253,6 +271,28 @@ def amsim_gemm_strided_batched(transA, transB, m, n, k, alpha, A, lda, strideA, 
 
 def amsim_gemm_workspace_size(transA, transB, m, n, k, batch, lut) -> int:
     return int(lib().amsim_gemm_workspace_size(transA.encode(), transB.encode(), m, n, k, batch, _h(lut)))
+
+
+def _problem_array(problems):
+    if isinstance(problems, ctypes.Array):
+        return problems
+    arr = (GemmProblem * len(problems))()
+    for i, p in enumerate(problems):
+        arr[i] = p
+    return arr
+
+
+def amsim_gemm_grouped(problems, lut, ws=None, ws_bytes=None, stream=None):
+    """problems: a sequence of GemmProblem (or a ctypes array of them)."""
+    arr = _problem_array(problems)
+    ws_bytes = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("amsim_gemm_grouped", lib().amsim_gemm_grouped(len(arr), arr, _h(lut), _ptr(ws), ws_bytes,
+                                                          _stream(stream)))
+
+
+def amsim_gemm_grouped_workspace_size(problems, lut) -> int:
+    arr = _problem_array(problems)
+    return int(lib().amsim_gemm_grouped_workspace_size(len(arr), arr, _h(lut)))
 
 
 def amsim_conv2d_out_hw(desc: ConvDesc):

@@ -67,9 +67,12 @@ struct Problem {
     float alpha, beta;
 };
 
-// Launch the LUT-GEMM for a problem.  ws may be null; split-K is used only if
-// ws_bytes allows it.  Returns an amsim status.
+// Launch the LUT-GEMM for a problem.  ws may be null; the stream-K schedule
+// (partial tiles in scratch) is used only if ws_bytes allows it.
 int run_problem(const Problem &p, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream);
 size_t problem_workspace(const Problem &p, amsim_lut_t lut);
+// Up to ten independent problems in one launch (one LUT for all).
+int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream);
+size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut);
 
 }  // namespace amsim

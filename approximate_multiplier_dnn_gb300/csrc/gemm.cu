@@ -31,136 +31,118 @@ int device_sms(int dev)
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
+// Launch plan for a group of problems sharing one LUT.
 struct Plan {
-    int tiles_u, tiles_l, kt_total, splits, kt_per_split, ws_ld;
-    size_t ws_bytes;
+    int tiles_u[kern::kMaxProblems], tiles_l[kern::kMaxProblems], kt[kern::kMaxProblems];
+    long long tiles[kern::kMaxProblems], iter0[kern::kMaxProblems];
+    long long total_tiles, iters;
+    bool streamk;
+    int ctas;
+    size_t ws_bytes;   // scratch the chosen plan uses
+    size_t sk_bytes;   // scratch stream-K would use
 };
 
-Plan make_plan(const Problem &p, int sms, size_t ws_avail)
+Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail)
 {
-    Plan pl;
-    pl.tiles_u = std::max(1, ceil_div(p.U.rows, BU));
-    pl.tiles_l = std::max(1, ceil_div(p.L.rows, BL));
-    pl.kt_total = ceil_div(p.K, BK);
-    pl.ws_ld = (p.L.rows + 3) & ~3;
-    pl.splits = 1;
-    pl.kt_per_split = std::max(1, pl.kt_total);
-    pl.ws_bytes = 0;
-    const long long tiles = (long long)pl.tiles_u * pl.tiles_l * p.batch;
-    // Split the reduction only when the output tiles leave SMs idle: as many
-    // splits as fit in one wave, at least two stages per split.
-    if (tiles < sms && pl.kt_total >= 4) {
-        int want = (int)std::min<long long>(sms / tiles, pl.kt_total / 2);
-        want = std::min(want, 65535);
-        if (want > 1) {
-            int kps = ceil_div(pl.kt_total, want);
-            int splits = ceil_div(pl.kt_total, kps);
-            size_t need = (size_t)p.batch * splits * (size_t)p.U.rows * pl.ws_ld * sizeof(float);
-            if (splits > 1 && need <= ws_avail) {
-                pl.splits = splits;
-                pl.kt_per_split = kps;
-                pl.ws_bytes = need;
-            }
-        }
+    Plan pl = {};
+    for (int i = 0; i < n; ++i) {
+        const bool empty = p[i].U.rows == 0 || p[i].L.rows == 0 || p[i].batch == 0;
+        pl.tiles_u[i] = std::max(1, ceil_div(p[i].U.rows, BU));
+        pl.tiles_l[i] = std::max(1, ceil_div(p[i].L.rows, BL));
+        pl.kt[i] = std::max(1, ceil_div(p[i].K, BK));
+        pl.tiles[i] = empty ? 0 : (long long)pl.tiles_u[i] * pl.tiles_l[i] * p[i].batch;
+        pl.iter0[i] = pl.iters;
+        pl.iters += pl.tiles[i] * pl.kt[i];
+        pl.total_tiles += pl.tiles[i];
     }
+    pl.ctas = (int)std::min<long long>(std::min(sms, kern::kMaxFixupParts), pl.iters);
+    pl.sk_bytes = (size_t)2 * pl.ctas * BU * BL * sizeof(float);
+    // Data parallel (one CTA per tile) when the tiles fill the SMs in nearly
+    // whole waves; otherwise stream-K over (tile, stage) iterations.
+    const long long waves = (pl.total_tiles + sms - 1) / std::max(1, sms);
+    const double dp_eff = pl.total_tiles > 0 ? (double)pl.total_tiles / (double)(waves * sms) : 1.0;
+    pl.streamk = pl.ctas > 1 && dp_eff < 0.9 && pl.sk_bytes <= ws_avail;
+    pl.ws_bytes = pl.streamk ? pl.sk_bytes : 0;
     return pl;
 }
 
-__global__ void splitk_reduce(const float *__restrict__ ws, int splits, int nU, int nL, int ws_ld, int batch,
-                              float *C, long long c_bs, long long c_su, long long c_sl, float alpha, float beta,
-                              bool u_fastest)
+int launch_w(int width, const kern::KParams &kp, bool gl, dim3 grid, size_t smem, cudaStream_t st)
 {
-    const long long total = (long long)batch * nU * nL;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        int u, l;
-        long long b;
-        if (u_fastest) {
-            u = (int)(i % nU);
-            long long t = i / nU;
-            l = (int)(t % nL);
-            b = t / nL;
-        } else {
-            l = (int)(i % nL);
-            long long t = i / nL;
-            u = (int)(t % nU);
-            b = t / nU;
-        }
-        const float *src = ws + ((b * splits) * nU + u) * (long long)ws_ld + l;
-        const long long sstride = (long long)nU * ws_ld;
-        float s = 0.0f;
-        for (int sp = 0; sp < splits; ++sp) s += src[sp * sstride];
-        float *dst = C + b * c_bs + (long long)u * c_su + (long long)l * c_sl;
-        float r = alpha * s;
-        if (beta != 0.0f) r = fmaf(beta, *dst, r);
-        *dst = r;
+    switch (width) {
+    case 8: return kern::launch_w8(kp, gl, grid, smem, st);
+    case 16: return kern::launch_w16(kp, gl, grid, smem, st);
+    default: return kern::launch_w32(kp, gl, grid, smem, st);
     }
 }
 
 }  // namespace
 
-size_t problem_workspace(const Problem &p, amsim_lut_t lut)
+size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
 {
-    int dev = lut ? lut->device : 0;
-    return make_plan(p, device_sms(dev), (size_t)-1).ws_bytes;
+    if (n <= 0 || n > kern::kMaxProblems) return 0;
+    const int dev = lut ? lut->device : 0;
+    const int sms = device_sms(dev);
+    Plan pl = make_plan(p, n, sms, (size_t)-1);
+    return pl.ws_bytes;
+}
+
+size_t problem_workspace(const Problem &p, amsim_lut_t lut) { return problems_workspace(&p, 1, lut); }
+
+int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (n <= 0) return AMSIM_OK;
+    if (n > kern::kMaxProblems) return AMSIM_EINVAL;
+    const int sms = device_sms(lut->device);
+    const Plan pl = make_plan(p, n, sms, ws ? ws_bytes : 0);
+    if (pl.total_tiles == 0) return AMSIM_OK;
+
+    const bool gl = lut->narrow_bytes > (size_t)kMaxSmemLut ||
+                    (size_t)kern::kFixedSmem + kern::lut_region_bytes((int)lut->narrow_bytes) > (size_t)kMaxSmemPerCta;
+    kern::KParams kp = {};
+    int np = 0;
+    for (int i = 0; i < n; ++i) {
+        if (pl.tiles[i] == 0) continue;
+        kern::ProbParams &q = kp.pr[np++];
+        q.U = p[i].U;
+        q.L = p[i].L;
+        q.K = p[i].K;
+        q.batch = p[i].batch;
+        q.tiles_u = pl.tiles_u[i];
+        q.tiles_l = pl.tiles_l[i];
+        q.kt_total = pl.kt[i];
+        q.tiles = pl.tiles[i];
+        q.iter0 = pl.iter0[i];
+        q.table = p[i].u_is_first ? lut->d_narrow : lut->d_narrow_t;
+        q.c_ptr = p[i].c_ptr;
+        q.c_bs = p[i].c_bs;
+        q.c_su = p[i].c_su;
+        q.c_sl = p[i].c_sl;
+        q.alpha = p[i].alpha;
+        q.beta = p[i].beta;
+        q.u_kfast = p[i].U.gather ? (p[i].U.kcb[0] == 1) : (p[i].U.s_k == 1 && p[i].U.s_row != 1);
+        q.l_kfast = p[i].L.gather ? (p[i].L.kcb[0] == 1) : (p[i].L.s_k == 1 && p[i].L.s_row != 1);
+    }
+    kp.nprob = np;
+    kp.streamk = pl.streamk ? 1 : 0;
+    kp.iters = pl.iters;
+    kp.ctas = pl.ctas;
+    kp.table_bytes = gl ? 0 : (int)lut->narrow_bytes;
+    kp.M = lut->M;
+    kp.wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
+    kp.ws = static_cast<float *>(ws);
+
+    const size_t smem = (size_t)kern::kFixedSmem + (gl ? 0 : kern::lut_region_bytes(kp.table_bytes));
+    if (smem > (size_t)kMaxSmemPerCta) return AMSIM_EUNSUPPORTED;
+    const long long blocks = pl.streamk ? pl.ctas : pl.total_tiles;
+    if (blocks > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
+    int rc = launch_w(lut->width_bits, kp, gl, dim3((unsigned)blocks), smem, stream);
+    if (rc || !pl.streamk) return rc;
+    return kern::launch_fixup(kp, pl.ctas - 1, stream);
 }
 
 int run_problem(const Problem &p, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
-    if (p.U.rows == 0 || p.L.rows == 0 || p.batch == 0) return AMSIM_OK;
-    const int sms = device_sms(lut->device);
-    const Plan pl = make_plan(p, sms, ws ? ws_bytes : 0);
-
-    kern::KParams kp;
-    kp.U = p.U;
-    kp.L = p.L;
-    kp.K = p.K;
-    kp.batch = p.batch;
-    kp.tiles_u = pl.tiles_u;
-    kp.tiles_l = pl.tiles_l;
-    kp.splits = pl.splits;
-    kp.kt_per_split = pl.kt_per_split;
-    kp.kt_total = pl.kt_total;
-    kp.table = p.u_is_first ? lut->d_narrow : lut->d_narrow_t;
-    const bool gl = lut->narrow_bytes > (size_t)kMaxSmemLut ||
-                    (size_t)kern::kFixedSmem + kern::lut_region_bytes((int)lut->narrow_bytes) > (size_t)kMaxSmemPerCta;
-    kp.table_bytes = gl ? 0 : (int)lut->narrow_bytes;
-    kp.M = lut->M;
-    kp.mul = 1u << lut->shift;
-    kp.wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
-    kp.c_ptr = p.c_ptr;
-    kp.c_bs = p.c_bs;
-    kp.c_su = p.c_su;
-    kp.c_sl = p.c_sl;
-    kp.alpha = p.alpha;
-    kp.beta = p.beta;
-    kp.ws = static_cast<float *>(ws);
-    kp.ws_ld = pl.ws_ld;
-    kp.u_kfast = p.U.gather ? 1 : (p.U.s_k == 1 && p.U.s_row != 1);
-    kp.l_kfast = p.L.gather ? 1 : (p.L.s_k == 1 && p.L.s_row != 1);
-    if (p.U.gather && p.U.kcb[0] != 1) kp.u_kfast = 0;
-    if (p.L.gather && p.L.kcb[0] != 1) kp.l_kfast = 0;
-
-    const size_t smem = (size_t)kern::kFixedSmem + (gl ? 0 : kern::lut_region_bytes(kp.table_bytes));
-    if (smem > (size_t)kMaxSmemPerCta) return AMSIM_EUNSUPPORTED;
-    const long long tiles = (long long)pl.tiles_u * pl.tiles_l;
-    if (tiles > 0x7FFFFFFFLL || p.batch > 65535) return AMSIM_EUNSUPPORTED;
-    dim3 grid((unsigned)tiles, (unsigned)pl.splits, (unsigned)p.batch);
-    int rc;
-    switch (lut->width_bits) {
-    case 8: rc = kern::launch_w8(kp, gl, grid, smem, stream); break;
-    case 16: rc = kern::launch_w16(kp, gl, grid, smem, stream); break;
-    default: rc = kern::launch_w32(kp, gl, grid, smem, stream); break;
-    }
-    if (rc || pl.splits == 1) return rc;
-
-    const long long total = (long long)p.batch * p.U.rows * p.L.rows;
-    long long blocks = std::min<long long>((total + 255) / 256, (long long)sms * 16);
-    const bool u_fastest = p.c_su == 1 && p.c_sl != 1;
-    splitk_reduce<<<(unsigned)std::max(1LL, blocks), 256, 0, stream>>>(
-        kp.ws, pl.splits, p.U.rows, p.L.rows, pl.ws_ld, p.batch, p.c_ptr, p.c_bs, p.c_su, p.c_sl, p.alpha, p.beta,
-        u_fastest);
-    return cuda_status(cudaGetLastError());
+    return run_problems(&p, 1, lut, ws, ws_bytes, stream);
 }
 
 }  // namespace amsim
@@ -255,6 +237,46 @@ int amsim_gemm(char transA, char transB, int m, int n, int k, float alpha, const
 {
     return amsim_gemm_strided_batched(transA, transB, m, n, k, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1, lut,
                                       ws, ws_bytes, stream);
+}
+
+static int grouped_build(const amsim_gemm_problem *g, Problem *pr)
+{
+    return build_gemm(g->transA, g->transB, g->m, g->n, g->k, g->alpha, g->A, g->lda, g->strideA, g->B, g->ldb,
+                      g->strideB, g->beta, g->C, g->ldc, g->strideC, g->batch, pr);
+}
+
+int amsim_gemm_grouped(int count, const amsim_gemm_problem *problems, amsim_lut_t lut, void *ws, size_t ws_bytes,
+                       amsim_stream_t stream)
+{
+    int rc = amsim::check_lut(lut);
+    if (rc) return rc;
+    if (count < 0 || (count > 0 && !problems)) return AMSIM_EINVAL;
+    Problem pr[amsim::kern::kMaxProblems];
+    for (int i = 0; i < count; ++i) {           // validate everything before enqueuing anything
+        rc = grouped_build(&problems[i], &pr[0]);
+        if (rc) return rc;
+    }
+    for (int base = 0; base < count; base += amsim::kern::kMaxProblems) {
+        const int n = std::min(count - base, amsim::kern::kMaxProblems);
+        for (int i = 0; i < n; ++i) grouped_build(&problems[base + i], &pr[i]);
+        rc = amsim::run_problems(pr, n, lut, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+        if (rc) return rc;
+    }
+    return AMSIM_OK;
+}
+
+size_t amsim_gemm_grouped_workspace_size(int count, const amsim_gemm_problem *problems, amsim_lut_t lut)
+{
+    if (!lut || count <= 0 || !problems) return 0;
+    Problem pr[amsim::kern::kMaxProblems];
+    size_t best = 0;
+    for (int base = 0; base < count; base += amsim::kern::kMaxProblems) {
+        const int n = std::min(count - base, amsim::kern::kMaxProblems);
+        for (int i = 0; i < n; ++i)
+            if (grouped_build(&problems[base + i], &pr[i])) return 0;
+        best = std::max(best, amsim::problems_workspace(pr, n, lut));
+    }
+    return best;
 }
 
 size_t amsim_gemm_workspace_size(char transA, char transB, int m, int n, int k, int batch, amsim_lut_t lut)

@@ -68,21 +68,37 @@ struct RowInfo {
     long long b;
 };
 
-struct KParams {
+constexpr int kMaxProblems = 10;     // contractions fused into one launch
+constexpr int kMaxFixupParts = 1024;  // stream-K CTAs per launch (at most one per SM)
+
+// One contraction of a launch (see Problem in amsim_internal.h).
+struct ProbParams {
     OperandDesc U, L;
     int K, batch;
-    int tiles_u, tiles_l, splits, kt_per_split, kt_total;
-    const void *table;
-    int table_bytes;     // bytes staged to shared memory (0 when read from global)
-    int M;
-    uint32_t mul;        // 1 << shift: rebuilds a canonical entry from a narrowed one
-    int wlog;            // log2(entry bytes)
+    int tiles_u, tiles_l, kt_total;
+    long long tiles;        // tiles_u * tiles_l * batch
+    long long iter0;        // first iteration of this problem in the launch's iteration space
+    const void *table;      // LUT oriented [U mantissa][L mantissa]
     float *c_ptr;
     long long c_bs, c_su, c_sl;
     float alpha, beta;
-    float *ws;           // split partials [batch][split][U.rows][ws_ld] when splits > 1
-    int ws_ld;
     int u_kfast, l_kfast;
+};
+
+// A launch: the (problem, tile, stage) iterations of all problems laid end to
+// end.  Data-parallel mode: CTA c runs tile c whole.  Stream-K mode: CTA c
+// runs iterations [c*W/G, (c+1)*W/G); a tile cut between CTAs leaves partial
+// sums in per-CTA slots that a fixup kernel adds in CTA order.
+struct KParams {
+    ProbParams pr[kMaxProblems];
+    int nprob;
+    int streamk;
+    long long iters;        // W
+    int ctas;               // G (stream-K)
+    int table_bytes;        // bytes staged to shared memory (0 when read from global)
+    int M;
+    int wlog;               // log2(entry bytes)
+    float *ws;              // stream-K partial slots [G][2][BU*BL]
 };
 
 // Shared-memory layout (bytes) after the LUT region.
@@ -162,29 +178,20 @@ __device__ __forceinline__ uint32_t lut_ld(const uint8_t *lut, uint32_t off)
     }
 }
 
-// v = 2^carry * 1.mantissa as fp32: canonical entry + the bit pattern of 1.0f.
-#ifndef AMSIM_EXPAND_MODE
-#define AMSIM_EXPAND_MODE 0
-#endif
-__device__ __forceinline__ float expand(uint32_t narrowed, uint32_t mul)
+// v = 2^carry * 1.mantissa as fp32: the canonical entry (narrowed entry <<
+// (24 - W) for 8/16-bit tables, the entry itself for 32-bit ones) plus the bit
+// pattern of 1.0f.  A shift and an add keep this off the FMA pipes, which
+// carry the scale multiply and the accumulation.
+template <int W>
+__device__ __forceinline__ float expand(uint32_t narrowed)
 {
-#if AMSIM_EXPAND_MODE == 1
     uint32_t r;
-    asm("shl.b32 %0, %1, 16;\n\tadd.u32 %0, %0, 0x3F800000;" : "=r"(r) : "r"(narrowed));
+    if constexpr (W == 32) {
+        r = narrowed + 0x3F800000u;
+    } else {
+        asm("shl.b32 %0, %1, %2;\n\tadd.u32 %0, %0, 0x3F800000;" : "=r"(r) : "r"(narrowed), "n"(24 - W));
+    }
     return __uint_as_float(r);
-#else
-    return __uint_as_float(narrowed * mul + 0x3F800000u);
-#endif
-}
-__device__ __forceinline__ float expand_alu(uint32_t narrowed, uint32_t mul)
-{
-#if AMSIM_EXPAND_MODE == 2
-    uint32_t r;
-    asm("shl.b32 %0, %1, 16;\n\tadd.u32 %0, %0, 0x3F800000;" : "=r"(r) : "r"(narrowed));
-    return __uint_as_float(r);
-#else
-    return expand(narrowed, mul);
-#endif
 }
 
 // Operand decode (once per element per CTA): byte offset of the mantissa's LUT
@@ -354,8 +361,7 @@ __device__ __forceinline__ float accv(const float2 (&acc)[TM / 2][TN], int i, in
 template <int W, bool GL, bool SLOW>
 __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                               const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
-                                              const float *__restrict__ Ls, const uint8_t *lut, uint32_t mul,
-                                              int urow, int lcol)
+                                              const float *__restrict__ Ls, const uint8_t *lut, int urow, int lcol)
 {
 #pragma unroll 1
     for (int kk = 0; kk < BK; ++kk) {
@@ -383,7 +389,7 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
                 for (int t = 0; t < TN; ++t) {
                     const uint32_t ea = lut_ld<W, GL>(lut, uov[2 * ip] + lo[t]);
                     const uint32_t eb = lut_ld<W, GL>(lut, uov[2 * ip + 1] + lo[t]);
-                    const float2 v = make_float2(expand(ea, mul), expand_alu(eb, mul));
+                    const float2 v = make_float2(expand<W>(ea), expand<W>(eb));
                     const float2 s = fmul2_ftz(sa[ip], sb[t]);
                     float2 &a = acc[2 * ig + ip][t];
                     if constexpr (SLOW) {
@@ -401,114 +407,31 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int W, bool GL>
-__global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ KParams p)
+struct Smem {
+    uint8_t *lut;
+    uint32_t *Uoff;
+    float *Uscl;
+    uint32_t *Loff;
+    float *Lscl;
+    RowInfo *rowU, *rowL;
+};
+
+__device__ __forceinline__ float4 acc4(const float2 (&acc)[TM / 2][TN], int i, int t0)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int wu = warp / WL, wl = warp % WL;
-    const int tl = blockIdx.x % p.tiles_l, tu = blockIdx.x / p.tiles_l;
-    const int sp = blockIdx.y, b = blockIdx.z;
-    const int u_tile0 = tu * BU, l_tile0 = tl * BL;
+    return make_float4(accv(acc, i, t0), accv(acc, i, t0 + 1), accv(acc, i, t0 + 2), accv(acc, i, t0 + 3));
+}
 
-    const int lut_bytes = GL ? 0 : lut_region_bytes(p.table_bytes);
-    uint8_t *lut_s = smem;
-    uint32_t *Uoff = reinterpret_cast<uint32_t *>(smem + lut_bytes);
-    float *Uscl = reinterpret_cast<float *>(smem + lut_bytes + kUdecBytes);
-    uint32_t *Loff = reinterpret_cast<uint32_t *>(smem + lut_bytes + 2 * kUdecBytes);
-    float *Lscl = reinterpret_cast<float *>(smem + lut_bytes + 2 * kUdecBytes + kLdecBytes);
-    RowInfo *rowU = reinterpret_cast<RowInfo *>(smem + lut_bytes + 2 * kUdecBytes + 2 * kLdecBytes);
-    RowInfo *rowL = rowU + BU;
-
-    // LUT -> shared memory (the allocation is padded to 256 bytes, so whole
-    // 16-byte vectors stay inside it).
-    if constexpr (!GL) {
-        const uint4 *src = static_cast<const uint4 *>(p.table);
-        uint4 *dst = reinterpret_cast<uint4 *>(lut_s);
-        const int nvec = (p.table_bytes + 15) >> 4;
-        for (int i = tid; i < nvec; i += NT) dst[i] = __ldg(src + i);
-    }
-    if (p.U.gather)
-        for (int r = tid; r < BU; r += NT) rowU[r] = row_info(p.U, u_tile0 + r);
-    if (p.L.gather)
-        for (int r = tid; r < BL; r += NT) rowL[r] = row_info(p.L, l_tile0 + r);
-    __syncthreads();
-
-    const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.table) : lut_s;
-    const int kt0 = sp * p.kt_per_split;
-    const int kt1 = min(kt0 + p.kt_per_split, p.kt_total);
-    const int offU = p.M + p.wlog, offL = p.wlog;
-
-    float2 acc[TM / 2][TN];
-#pragma unroll
-    for (int i = 0; i < TM / 2; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-
-    if (kt0 < kt1) {
-        Loader<BU, NUE> ldU;
-        Loader<BL, NLE> ldL;
-        ldU.init(p.U, p.u_kfast, tid, u_tile0, b, kt0);
-        ldL.init(p.L, p.l_kfast, tid, l_tile0, b, kt0);
-        ldU.load(p.U, rowU, kt0, p.K);
-        ldL.load(p.L, rowL, kt0, p.K);
-        int big = 0;
-        ldU.template store<UST>(Uoff, Uscl, p.M, offU, big);
-        ldL.template store<LST>(Loff, Lscl, p.M, offL, big);
-        int slow = __syncthreads_or(big);
-
-        const int urow = wu * TM;
-        const int lcol = wl * 32 * TN + lane * TN;
-        for (int kt = kt0; kt < kt1; ++kt) {
-            const int buf = (kt - kt0) & 1;
-            const bool more = kt + 1 < kt1;
-            if (more) {
-                ldU.load(p.U, rowU, kt + 1, p.K);
-                ldL.load(p.L, rowL, kt + 1, p.K);
-            }
-            const uint32_t *Uo = Uoff + buf * BK * UST;
-            const float *Us = Uscl + buf * BK * UST;
-            const uint32_t *Lo = Loff + buf * BK * LST;
-            const float *Ls = Lscl + buf * BK * LST;
-            if (slow) compute_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, p.mul, urow, lcol);
-            else compute_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, p.mul, urow, lcol);
-            int nbig = 0;
-            if (more) {
-                const int nb = buf ^ 1;
-                ldU.template store<UST>(Uoff + nb * BK * UST, Uscl + nb * BK * UST, p.M, offU, nbig);
-                ldL.template store<LST>(Loff + nb * BK * LST, Lscl + nb * BK * LST, p.M, offL, nbig);
-            }
-            slow = __syncthreads_or(nbig);
-        }
-    }
-
-    // ---------------------------------------------------------------- epilogue
-    const int u0 = u_tile0 + wu * TM;
-    const int l0 = l_tile0 + wl * 32 * TN + lane * TN;
-    const int nU = p.U.rows, nL = p.L.rows;
-    if (p.splits > 1) {
-        float *w = p.ws + (((long long)b * p.splits + sp) * nU) * p.ws_ld;
-#pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const int u = u0 + i;
-            if (u >= nU) break;
-            float *row = w + (long long)u * p.ws_ld + l0;
-#pragma unroll
-            for (int t4 = 0; t4 < TN / 4; ++t4) {
-                if (l0 + 4 * t4 + 4 <= p.ws_ld)
-                    *reinterpret_cast<float4 *>(row + 4 * t4) =
-                        make_float4(accv(acc, i, 4 * t4), accv(acc, i, 4 * t4 + 1), accv(acc, i, 4 * t4 + 2),
-                                    accv(acc, i, 4 * t4 + 3));
-            }
-        }
-        return;
-    }
-    float *C = p.c_ptr + (long long)b * p.c_bs;
-    const float alpha = p.alpha, beta = p.beta;
+// Write a finished tile: C = alpha*acc + beta*C with 128-bit stores when the
+// output is contiguous along L (or along U, for transposed outputs).
+__device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&acc)[TM / 2][TN], int b, int u0,
+                                           int l0)
+{
+    const int nU = q.U.rows, nL = q.L.rows;
+    float *C = q.c_ptr + (long long)b * q.c_bs;
+    const float alpha = q.alpha, beta = q.beta;
     const bool aligned = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
-    const bool vec_l = aligned && p.c_sl == 1 && (p.c_su & 3) == 0;
-    const bool vec_u = aligned && p.c_su == 1 && (p.c_sl & 3) == 0;
+    const bool vec_l = aligned && q.c_sl == 1 && (q.c_su & 3) == 0;
+    const bool vec_u = aligned && q.c_su == 1 && (q.c_sl & 3) == 0;
     if (vec_l && l0 + TN <= nL) {
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
@@ -516,9 +439,9 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
             if (u >= nU) break;
 #pragma unroll
             for (int t4 = 0; t4 < TN / 4; ++t4) {
-                float4 *dst = reinterpret_cast<float4 *>(C + (long long)u * p.c_su + l0 + 4 * t4);
-                float4 r = make_float4(alpha * accv(acc, i, 4 * t4), alpha * accv(acc, i, 4 * t4 + 1),
-                                       alpha * accv(acc, i, 4 * t4 + 2), alpha * accv(acc, i, 4 * t4 + 3));
+                float4 *dst = reinterpret_cast<float4 *>(C + (long long)u * q.c_su + l0 + 4 * t4);
+                const float4 a = acc4(acc, i, 4 * t4);
+                float4 r = make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w);
                 if (beta != 0.0f) {
                     const float4 o = *dst;
                     r.x = fmaf(beta, o.x, r.x); r.y = fmaf(beta, o.y, r.y);
@@ -532,7 +455,7 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
         for (int t = 0; t < TN; ++t) {
             const int l = l0 + t;
             if (l >= nL) break;
-            float *col = C + (long long)l * p.c_sl + u0;
+            float *col = C + (long long)l * q.c_sl + u0;
 #pragma unroll
             for (int i4 = 0; i4 < TM / 4; ++i4) {
                 float4 r = make_float4(alpha * accv(acc, 4 * i4, t), alpha * accv(acc, 4 * i4 + 1, t),
@@ -555,12 +478,230 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
             for (int t = 0; t < TN; ++t) {
                 const int l = l0 + t;
                 if (l >= nL) break;
-                float *dst = C + (long long)u * p.c_su + (long long)l * p.c_sl;
+                float *dst = C + (long long)u * q.c_su + (long long)l * q.c_sl;
                 float r = alpha * accv(acc, i, t);
                 if (beta != 0.0f) r = fmaf(beta, *dst, r);
                 *dst = r;
             }
         }
+    }
+}
+
+// Stages [s0, s1) of tile `tile` of problem q; returns with acc holding the
+// partial (or full) sum of those stages.
+template <int W, bool GL>
+__device__ __forceinline__ void run_stages(const KParams &p, const ProbParams &q, const Smem &sm, int b, int u_tile0,
+                                           int l_tile0, int s0, int s1, float2 (&acc)[TM / 2][TN])
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int wu = warp / WL, wl = warp % WL;
+    const int offU = p.M + p.wlog, offL = p.wlog;
+    const uint8_t *lut = GL ? static_cast<const uint8_t *>(q.table) : sm.lut;
+
+    Loader<BU, NUE> ldU;
+    Loader<BL, NLE> ldL;
+    ldU.init(q.U, q.u_kfast, tid, u_tile0, b, s0);
+    ldL.init(q.L, q.l_kfast, tid, l_tile0, b, s0);
+    ldU.load(q.U, sm.rowU, s0, q.K);
+    ldL.load(q.L, sm.rowL, s0, q.K);
+    int big = 0;
+    ldU.template store<UST>(sm.Uoff, sm.Uscl, p.M, offU, big);
+    ldL.template store<LST>(sm.Loff, sm.Lscl, p.M, offL, big);
+    int slow = __syncthreads_or(big);
+
+    const int urow = wu * TM;
+    const int lcol = wl * 32 * TN + lane * TN;
+    for (int kt = s0; kt < s1; ++kt) {
+        const int buf = (kt - s0) & 1;
+        const bool more = kt + 1 < s1;
+        if (more) {
+            ldU.load(q.U, sm.rowU, kt + 1, q.K);
+            ldL.load(q.L, sm.rowL, kt + 1, q.K);
+        }
+        const uint32_t *Uo = sm.Uoff + buf * BK * UST;
+        const float *Us = sm.Uscl + buf * BK * UST;
+        const uint32_t *Lo = sm.Loff + buf * BK * LST;
+        const float *Ls = sm.Lscl + buf * BK * LST;
+        if (slow) compute_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+        else compute_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+        int nbig = 0;
+        if (more) {
+            const int nb = buf ^ 1;
+            ldU.template store<UST>(sm.Uoff + nb * BK * UST, sm.Uscl + nb * BK * UST, p.M, offU, nbig);
+            ldL.template store<LST>(sm.Loff + nb * BK * LST, sm.Lscl + nb * BK * LST, p.M, offL, nbig);
+        }
+        slow = __syncthreads_or(nbig);
+    }
+}
+
+__device__ __forceinline__ long long sk_begin(long long W, int G, int c) { return W * c / G; }
+
+template <int W, bool GL>
+__global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ KParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int wu = warp / WL, wl = warp % WL;
+
+    const int lut_bytes = GL ? 0 : lut_region_bytes(p.table_bytes);
+    Smem sm;
+    sm.lut = smem;
+    sm.Uoff = reinterpret_cast<uint32_t *>(smem + lut_bytes);
+    sm.Uscl = reinterpret_cast<float *>(smem + lut_bytes + kUdecBytes);
+    sm.Loff = reinterpret_cast<uint32_t *>(smem + lut_bytes + 2 * kUdecBytes);
+    sm.Lscl = reinterpret_cast<float *>(smem + lut_bytes + 2 * kUdecBytes + kLdecBytes);
+    sm.rowU = reinterpret_cast<RowInfo *>(smem + lut_bytes + 2 * kUdecBytes + 2 * kLdecBytes);
+    sm.rowL = sm.rowU + BU;
+
+    long long it, it_end;
+    if (p.streamk) {
+        it = sk_begin(p.iters, p.ctas, blockIdx.x);
+        it_end = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
+    } else {
+        // data parallel: CTA x runs the x-th tile of the launch whole
+        long long t = blockIdx.x;
+        int pi = 0;
+        while (pi + 1 < p.nprob && t >= p.pr[pi].tiles) t -= p.pr[pi++].tiles;
+        it = p.pr[pi].iter0 + t * p.pr[pi].kt_total;
+        it_end = it + p.pr[pi].kt_total;
+    }
+
+    const void *staged = nullptr;
+    bool first_segment = true;
+    while (it < it_end) {
+        int pi = 0;
+        while (pi + 1 < p.nprob && it >= p.pr[pi + 1].iter0) ++pi;
+        const ProbParams &q = p.pr[pi];
+        const long long local = it - q.iter0;
+        const int S = q.kt_total;
+        const long long tile = local / S;
+        const int s0 = (int)(local - tile * S);
+        const int s1 = (int)min((long long)S, s0 + (it_end - it));
+        const int per_batch = q.tiles_u * q.tiles_l;
+        const int b = (int)(tile / per_batch);
+        const int rem = (int)(tile - (long long)b * per_batch);
+        const int u_tile0 = (rem / q.tiles_l) * BU, l_tile0 = (rem % q.tiles_l) * BL;
+
+        if (!first_segment) __syncthreads();      // previous segment done with shared memory
+        if constexpr (!GL) {
+            if (q.table != staged) {
+                // LUT -> shared memory (the device allocation is padded to 256
+                // bytes, so whole 16-byte vectors stay inside it)
+                const uint4 *src = static_cast<const uint4 *>(q.table);
+                uint4 *dst = reinterpret_cast<uint4 *>(sm.lut);
+                const int nvec = (p.table_bytes + 15) >> 4;
+                for (int i = tid; i < nvec; i += NT) dst[i] = __ldg(src + i);
+                staged = q.table;
+            }
+        }
+        if (q.U.gather)
+            for (int r = tid; r < BU; r += NT) sm.rowU[r] = row_info(q.U, u_tile0 + r);
+        if (q.L.gather)
+            for (int r = tid; r < BL; r += NT) sm.rowL[r] = row_info(q.L, l_tile0 + r);
+        __syncthreads();
+
+        float2 acc[TM / 2][TN];
+#pragma unroll
+        for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+        run_stages<W, GL>(p, q, sm, b, u_tile0, l_tile0, s0, s1, acc);
+
+        const int u0 = u_tile0 + wu * TM;
+        const int l0 = l_tile0 + wl * 32 * TN + lane * TN;
+        if (s0 == 0 && s1 == S) {
+            store_tile(q, acc, b, u0, l0);
+        } else {
+            // partial tile: slot 0 holds the CTA's first segment, slot 1 its last
+            float *slot = p.ws + ((long long)blockIdx.x * 2 + (first_segment ? 0 : 1)) * (BU * BL);
+            const int ur = wu * TM, lr = wl * 32 * TN + lane * TN;
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int t4 = 0; t4 < TN / 4; ++t4)
+                    *reinterpret_cast<float4 *>(slot + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
+        }
+        first_segment = false;
+        it += s1 - s0;
+    }
+}
+
+// Adds the partial slots of every tile that stream-K cut between CTAs, in CTA
+// order (deterministic), and writes alpha*sum + beta*C.  blockIdx.x = c-1 for
+// the boundary before stream-K CTA c (the first boundary inside a tile owns
+// it); blockIdx.y = a chunk of kFixupChunk elements of that tile, so every cut
+// tile is spread over many CTAs and the partial loads overlap.
+constexpr int kFixupChunk = 1024;
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) streamk_fixup(const __grid_constant__ KParams p)
+{
+    static_assert(kThreads * 4 == kFixupChunk, "one float4 per thread");
+    const int c = blockIdx.x + 1;                     // boundary before CTA c
+    if (c >= p.ctas) return;
+    const long long W = p.iters;
+    const int G = p.ctas;
+    const long long bpos = sk_begin(W, G, c);
+    if (bpos >= W) return;
+    int pi = 0;
+    while (pi + 1 < p.nprob && bpos >= p.pr[pi + 1].iter0) ++pi;
+    const ProbParams &q = p.pr[pi];
+    const int S = q.kt_total;
+    const long long local = bpos - q.iter0;
+    const long long tile = local / S;
+    const long long tstart = q.iter0 + tile * S, tend = tstart + S;
+    if (bpos == tstart) return;                       // boundary on a tile edge: nothing cut
+    if (sk_begin(W, G, c - 1) > tstart) return;       // an earlier boundary in this tile owns it
+    const int c_lo = c - 1;
+    int c_hi = c;
+    while (c_hi + 1 < G && sk_begin(W, G, c_hi + 1) < tend) ++c_hi;
+
+    // slot offsets of the contributing CTAs, in CTA order (G <= kMaxFixupParts)
+    __shared__ long long slot_off[kMaxFixupParts];
+    const int nparts = min(c_hi - c_lo + 1, kMaxFixupParts);
+    for (int i = threadIdx.x; i < nparts; i += kThreads) {
+        const int cc = c_lo + i;
+        const bool first_is_this = sk_begin(W, G, cc) >= tstart;
+        slot_off[i] = ((long long)cc * 2 + (first_is_this ? 0 : 1)) * (BU * BL);
+    }
+    __syncthreads();
+
+    const int e0 = blockIdx.y * kFixupChunk + threadIdx.x * 4;   // 4 consecutive elements along L
+    const int ur = e0 / BL, lr = e0 % BL;
+    const float *src = p.ws + e0;
+    float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int i = 0;
+    for (; i + 4 <= nparts; i += 4) {          // loads first, adds in CTA order
+        const float4 a = *reinterpret_cast<const float4 *>(src + slot_off[i]);
+        const float4 b = *reinterpret_cast<const float4 *>(src + slot_off[i + 1]);
+        const float4 cv = *reinterpret_cast<const float4 *>(src + slot_off[i + 2]);
+        const float4 d = *reinterpret_cast<const float4 *>(src + slot_off[i + 3]);
+        sum.x += a.x; sum.y += a.y; sum.z += a.z; sum.w += a.w;
+        sum.x += b.x; sum.y += b.y; sum.z += b.z; sum.w += b.w;
+        sum.x += cv.x; sum.y += cv.y; sum.z += cv.z; sum.w += cv.w;
+        sum.x += d.x; sum.y += d.y; sum.z += d.z; sum.w += d.w;
+    }
+    for (; i < nparts; ++i) {
+        const float4 a = *reinterpret_cast<const float4 *>(src + slot_off[i]);
+        sum.x += a.x; sum.y += a.y; sum.z += a.z; sum.w += a.w;
+    }
+
+    const int per_batch = q.tiles_u * q.tiles_l;
+    const int b = (int)(tile / per_batch);
+    const int rem = (int)(tile - (long long)b * per_batch);
+    const int u = (rem / q.tiles_l) * BU + ur;
+    const int l = (rem % q.tiles_l) * BL + lr;
+    if (u >= q.U.rows) return;
+    float *C = q.c_ptr + (long long)b * q.c_bs;
+    const float v[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        if (l + t >= q.L.rows) break;
+        float *dst = C + (long long)u * q.c_su + (long long)(l + t) * q.c_sl;
+        float r = q.alpha * v[t];
+        if (q.beta != 0.0f) r = fmaf(q.beta, *dst, r);
+        *dst = r;
     }
 }
 
@@ -588,6 +729,7 @@ int launch_instance(const KParams &p, dim3 grid, size_t smem, cudaStream_t st)
     return cuda_status(cudaGetLastError());
 }
 
+int launch_fixup(const KParams &p, int boundaries, cudaStream_t st);
 int launch_w8(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
 int launch_w16(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
 int launch_w32(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);

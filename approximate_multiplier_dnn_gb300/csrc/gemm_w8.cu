@@ -4,6 +4,13 @@
 namespace amsim {
 namespace kern {
 
+int launch_fixup(const KParams &p, int boundaries, cudaStream_t st)
+{
+    if (boundaries <= 0) return AMSIM_OK;
+    streamk_fixup<256><<<dim3(boundaries, BU * BL / kFixupChunk), 256, 0, st>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
 int launch_w8(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st)
 {
     return gl ? launch_instance<8, true>(p, grid, smem, st) : launch_instance<8, false>(p, grid, smem, st);

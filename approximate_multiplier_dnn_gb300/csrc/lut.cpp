@@ -50,15 +50,17 @@ int generate(amsim_approx_mul_fn fn, int M, uint32_t *out)
     return AMSIM_OK;
 }
 
-// Narrowest lossless width: entry = narrowed << shift with narrowed < 2^width.
+// Narrowest lossless width.  Entries are < 2^24 (carry bit 23 + mantissa), so
+// 8-bit storage holds bits 16..23 and 16-bit storage bits 8..23: a table
+// narrows when every entry's bits below that are zero (Mitchell for M <= 7
+// and exact for M <= 3 fit 8 bits; exact for M <= 7 fits 16 bits).  The
+// fixed shifts let the kernels rebuild an entry with a constant shift.
 void choose_width(const uint32_t *e, size_t n, int *width, int *shift)
 {
-    uint32_t all_or = 0, maxv = 0;
-    for (size_t i = 0; i < n; ++i) { all_or |= e[i]; if (e[i] > maxv) maxv = e[i]; }
-    int s = 0;
-    if (all_or) while (!((all_or >> s) & 1u)) ++s;
-    if ((maxv >> s) < (1u << 8)) { *width = 8; *shift = s; return; }
-    if ((maxv >> s) < (1u << 16)) { *width = 16; *shift = s; return; }
+    uint32_t all_or = 0;
+    for (size_t i = 0; i < n; ++i) all_or |= e[i];
+    if ((all_or & 0xFFFFu) == 0) { *width = 8; *shift = 16; return; }
+    if ((all_or & 0xFFu) == 0) { *width = 16; *shift = 8; return; }
     *width = 32; *shift = 0;
 }
 

@@ -10,9 +10,10 @@ Dense forward (x, w); preceding-layer gradient (dy, w); weight gradient
 """
 from __future__ import annotations
 
-from . import (ConvDesc, amsim_conv2d_bwd_data, amsim_conv2d_bwd_filter, amsim_conv2d_fwd,
-               amsim_conv2d_out_hw, amsim_conv2d_workspace_size, amsim_gemm, amsim_gemm_strided_batched,
-               amsim_gemm_workspace_size, amsim_softmax_rows, workspace)
+from . import (ConvDesc, GemmProblem, amsim_conv2d_bwd_data, amsim_conv2d_bwd_filter, amsim_conv2d_fwd,
+               amsim_conv2d_out_hw, amsim_conv2d_workspace_size, amsim_gemm, amsim_gemm_grouped,
+               amsim_gemm_grouped_workspace_size, amsim_gemm_strided_batched, amsim_gemm_workspace_size,
+               amsim_softmax_rows, workspace)
 
 
 def _dev(t, device):
@@ -45,11 +46,37 @@ class GemmCall:
                    self.B, max(1, self.B.shape[1]), self.beta, self.C, max(1, self.n), lut, ws=ws,
                    stream=stream)
 
+    def problem(self) -> GemmProblem:
+        return GemmProblem.make(self.tA, self.tB, self.m, self.n, self.k, self.alpha, self.A,
+                                max(1, self.A.shape[1]), self.B, max(1, self.B.shape[1]), self.beta, self.C,
+                                max(1, self.n))
+
+
+class GemmGroup:
+    """Independent GEMMs issued as one grouped launch."""
+
+    def __init__(self, calls):
+        self.calls = list(calls)
+        import ctypes
+        self.arr = (GemmProblem * len(self.calls))(*[c.problem() for c in self.calls])
+
+    @property
+    def macs(self) -> int:
+        return sum(c.macs for c in self.calls)
+
+    def ws_bytes(self, lut) -> int:
+        return amsim_gemm_grouped_workspace_size(self.arr, lut)
+
+    def __call__(self, lut, ws, stream=None):
+        amsim_gemm_grouped(self.arr, lut, ws=ws, stream=stream)
+
 
 class MLPStep:
     """3-layer MLP (784-1000-500-10, batch 256): forward Y_l = X_l W_l, then
     for every layer dX_l = dY_l W_l^T and dW_l = X_l^T dY_l (pure linear
-    layers; X_{l+1} = Y_l; dY_l synthetic per layer)."""
+    layers; X_{l+1} = Y_l; dY_l synthetic per layer).  The nine GEMMs run as
+    three grouped launches ordered by their data dependences:
+    {Y1, dX1, dW1, dX2, dX3}, then {Y2, dW2}, then {Y3, dW3}."""
 
     def __init__(self, data: dict, lut, device="cuda"):
         import torch
@@ -58,24 +85,29 @@ class MLPStep:
         self.inputs = d
         f32 = dict(dtype=torch.float32, device=device)
         X = d["X"]
-        self.Y, self.dX, self.dW, self.calls = [], [], [], []
-        xin = X
+        self.Y, self.dX, self.dW = [], [], []
+        fwd, xin = [], X
         for l in range(3):
             W = d[f"W{l + 1}"]
             Y = torch.empty((X.shape[0], W.shape[1]), **f32)
-            self.calls.append(GemmCall(xin, W, Y))
+            fwd.append(GemmCall(xin, W, Y))
             self.Y.append(Y)
             xin = Y
         xs = [X, self.Y[0], self.Y[1]]
+        dxc, dwc = [], []
         for l in range(3):
             W, dY = d[f"W{l + 1}"], d[f"dY{l + 1}"]
             dX = torch.empty((dY.shape[0], W.shape[0]), **f32)
             dW = torch.empty_like(W)
-            self.calls.append(GemmCall(dY, W, dX, transB=True))
-            self.calls.append(GemmCall(xs[l], dY, dW, transA=True))
+            dxc.append(GemmCall(dY, W, dX, transB=True))
+            dwc.append(GemmCall(xs[l], dY, dW, transA=True))
             self.dX.append(dX)
             self.dW.append(dW)
-        self.ws = workspace(max(c.ws_bytes(lut) for c in self.calls), device)
+        self.calls = fwd + [c for pair in zip(dxc, dwc) for c in pair]
+        self.groups = [("fwd1+dX1+dW1+dX2+dX3", GemmGroup([fwd[0], dxc[0], dwc[0], dxc[1], dxc[2]])),
+                       ("fwd2+dW2", GemmGroup([fwd[1], dwc[1]])),
+                       ("fwd3+dW3", GemmGroup([fwd[2], dwc[2]]))]
+        self.ws = workspace(max(g.ws_bytes(lut) for _, g in self.groups), device)
 
     @property
     def macs(self) -> int:
@@ -86,15 +118,12 @@ class MLPStep:
 
     def parts(self, stream=None):
         """(name, zero-argument launcher, approximate MACs, kernel launches) per ABI call."""
-        names = ["fwd1", "fwd2", "fwd3", "dX1", "dW1", "dX2", "dW2", "dX3", "dW3"]
-        out = []
-        for nm, c in zip(names, self.calls):
-            out.append((nm, (lambda c=c: c(self.lut, self.ws, stream)), c.macs, 1 + (c.ws_bytes(self.lut) > 0)))
-        return out
+        return [(nm, (lambda g=g: g(self.lut, self.ws, stream)), g.macs, 1 + (g.ws_bytes(self.lut) > 0))
+                for nm, g in self.groups]
 
     def run(self, stream=None):
-        for c in self.calls:
-            c(self.lut, self.ws, stream)
+        for _, g in self.groups:
+            g(self.lut, self.ws, stream)
 
 
 class ConvStep:
@@ -199,7 +228,7 @@ class AttentionStep:
         return 2 * self.bh * self.s * self.s * self.d
 
     def outputs(self) -> list:
-        return [self.S, self.P, self.O]
+        return [self.O]
 
     def parts(self, stream=None):
         s, d, bh = self.s, self.d, self.bh

@@ -164,6 +164,36 @@ int amsim_gemm_strided_batched(char transA, char transB, int m, int n, int k, fl
 size_t amsim_gemm_workspace_size(char transA, char transB, int m, int n, int k, int batch,
                                  amsim_lut_t lut);
 
+/*
+ * One GEMM of a group: the arguments of amsim_gemm_strided_batched as a struct
+ * (element strides; transA/transB 'N' or 'T').
+ */
+typedef struct amsim_gemm_problem {
+    const float *A;
+    const float *B;
+    float *C;
+    int64_t strideA, strideB, strideC;
+    int m, n, k, lda, ldb, ldc, batch;
+    float alpha, beta;
+    char transA, transB;
+} amsim_gemm_problem;
+
+/*
+ * `count` independent GEMMs sharing one LUT, scheduled together so that the
+ * work of all of them is spread evenly over the SMs (up to ten per launch;
+ * larger groups run as consecutive launches).  This is how a Dense layer's
+ * forward and both gradients (Sec. VI-C) -- or the independent contractions of
+ * several layers -- fill the GPU when each alone is too small.  No problem may
+ * read another's output or write memory another touches.  `problems` is host
+ * memory, read during the call.  Results equal the separate amsim_gemm calls'
+ * up to fp32 summation order.
+ */
+int amsim_gemm_grouped(int count, const amsim_gemm_problem *problems, amsim_lut_t lut, void *ws,
+                       size_t ws_bytes, amsim_stream_t stream);
+
+/* Bytes of scratch with which amsim_gemm_grouped runs its fastest plan. */
+size_t amsim_gemm_grouped_workspace_size(int count, const amsim_gemm_problem *problems, amsim_lut_t lut);
+
 /* ------------------------------------------------------------------ Conv2D */
 
 /*

@@ -99,3 +99,36 @@ def test_lut_build_from_entries_rejects_wide_entries(L):
     h = ctypes.c_void_p(0)
     assert L.amsim_lut_build_from_entries(e.ctypes.data, 2, ctypes.byref(h)) == am.AMSIM_EUNSUPPORTED
     assert L.amsim_lut_build_from_entries(e.ctypes.data, 0, ctypes.byref(h)) == am.AMSIM_EUNSUPPORTED
+
+
+def test_gemm_problem_struct_layout_matches_header(tmp_path):
+    """The binding's ctypes mirror of amsim_gemm_problem has the C layout."""
+    import os
+    import subprocess
+    src = tmp_path / "layout.c"
+    src.write_text("""
+#include <stdio.h>
+#include <stddef.h>
+#include "amsim.h"
+int main(void) {
+    printf("%zu", sizeof(amsim_gemm_problem));
+#define F(x) printf(" %zu", offsetof(amsim_gemm_problem, x));
+    F(A) F(B) F(C) F(strideA) F(strideB) F(strideC) F(m) F(n) F(k) F(lda) F(ldb) F(ldc) F(batch)
+    F(alpha) F(beta) F(transA) F(transB)
+    printf("\\n");
+    return 0;
+}
+""")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(am.HEADER))
+    subprocess.run(["gcc", "-std=c11", f"-I{inc}", str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    G = am.GemmProblem
+    want = [ctypes.sizeof(G)] + [getattr(G, f).offset for f, _ in G._fields_]
+    assert [int(x) for x in out] == want
+
+
+def test_grouped_rejects_bad_arguments(L):
+    probs = (am.GemmProblem * 1)()
+    assert L.amsim_gemm_grouped(1, probs, None, None, 0, None) == am.AMSIM_EINVAL
+    assert L.amsim_gemm_grouped_workspace_size(1, probs, None) == 0
