@@ -47,6 +47,10 @@ namespace kern {
 #ifndef AMSIM_TN
 #define AMSIM_TN 4
 #endif
+#ifndef AMSIM_KK_UNROLL
+#define AMSIM_KK_UNROLL 1
+#endif
+constexpr int kKkUnroll = AMSIM_KK_UNROLL;   // reduction steps unrolled per loop iteration
 constexpr int NT = AMSIM_NT;       // threads per CTA
 constexpr int BU = AMSIM_BU;       // uniform rows per CTA tile
 constexpr int BL = AMSIM_BL;       // lane columns per CTA tile
@@ -60,7 +64,7 @@ constexpr int LST = BL + 4;        // decoded L row stride (words)
 constexpr int NUE = BU * BK / NT;  // U elements loaded per thread per stage
 constexpr int NLE = BL * BK / NT;  // L elements loaded per thread per stage
 static_assert(TM % 4 == 0 && TN % 4 == 0, "micro-tile");
-static_assert(NT % BU == 0 && NT % BL == 0 && NT % BK == 0, "loader mapping");
+static_assert(NT % BK == 0 && (NT % BU == 0 || BU % NT == 0) && (NT % BL == 0 || BL % NT == 0), "loader mapping");
 static_assert(WU * WL * 32 == NT, "warp layout");
 
 struct RowInfo {
@@ -286,23 +290,35 @@ __device__ __forceinline__ float gather_value(const OperandDesc &d, const float 
 }
 
 // ------------------------------------------------------------------ operand loader
-// R rows per tile, N elements per thread per stage.  "k-fast": thread t owns
-// reduction slot t % BK and rows t/BK + (NT/BK) e; "row-fast": thread t owns
-// row t % R and reduction slots t/R + (NT/R) e.  The host picks the mapping
-// that makes consecutive threads touch consecutive addresses.
+// R rows per tile, N = R*BK/NT elements per thread per stage.  "k-fast":
+// thread t owns reduction slot t % BK and rows t/BK + (NT/BK) e.  "row-fast":
+// thread t owns row t % R (t + NT*j when R > NT) and the reduction slots left
+// over.  The host picks the mapping that makes consecutive threads touch
+// consecutive addresses.
 template <int R, int N>
 struct Loader {
-    int rsub, rstep, ksub0, kstep;
+    static constexpr int RRF = R > NT ? R / NT : 1;    // row repeats per thread (row-fast)
+    static constexpr int KSF = R < NT ? NT / R : 1;    // reduction-slot stride (row-fast)
+    static_assert(R * BK == N * NT, "loader element count");
+    bool kfast;
+    int rsub, ksub0;
     int row0;               // global row of tile row 0
     const float *base;      // operand pointer + batch offset
     KState ks;              // gather state at k = stage*BK + ksub0
     float v[N];
 
-    __device__ __forceinline__ void init(const OperandDesc &d, bool kfast, int tid, int row_tile0, int b,
-                                         int kt_first)
+    __device__ __forceinline__ int row_of(int e) const
     {
-        if (kfast) { rsub = tid / BK; rstep = NT / BK; ksub0 = tid % BK; kstep = 0; }
-        else { rsub = tid % R; rstep = 0; ksub0 = tid / R; kstep = NT / R; }
+        return kfast ? rsub + (NT / BK) * e : rsub + NT * (e % RRF);
+    }
+    __device__ __forceinline__ int k_of(int e) const { return kfast ? ksub0 : ksub0 + KSF * (e / RRF); }
+
+    __device__ __forceinline__ void init(const OperandDesc &d, bool kf, int tid, int row_tile0, int b, int kt_first)
+    {
+        kfast = kf;
+        if (kfast) { rsub = tid / BK; ksub0 = tid % BK; }
+        else if (R <= NT) { rsub = tid % R; ksub0 = tid / R; }
+        else { rsub = tid; ksub0 = 0; }
         row0 = row_tile0;
         base = d.ptr + (long long)b * d.batch_stride;
         if (d.gather) ks = kstate_at(d, kt_first * BK + ksub0);
@@ -310,22 +326,23 @@ struct Loader {
 
     __device__ __forceinline__ void load(const OperandDesc &d, const RowInfo *rowtab, int kt, int K)
     {
-        const int kbase = kt * BK + ksub0;
+        const int kbase = kt * BK;
         if (!d.gather) {
 #pragma unroll
             for (int e = 0; e < N; ++e) {
-                const int r = row0 + rsub + rstep * e;
-                const int k = kbase + kstep * e;
+                const int r = row0 + row_of(e);
+                const int k = kbase + k_of(e);
                 v[e] = (r < d.rows && k < K) ? __ldg(base + (long long)r * d.s_row + (long long)k * d.s_k) : 0.0f;
             }
         } else {
             KState s = ks;
+            int kprev = k_of(0);
 #pragma unroll
             for (int e = 0; e < N; ++e) {
-                const int k = kbase + kstep * e;
-                if (e > 0 && kstep) kstate_advance(d, s, kstep);
-                const RowInfo ri = rowtab[rsub + rstep * e];
-                v[e] = (k < K) ? gather_value(d, base, ri, s) : 0.0f;
+                const int kk = k_of(e);
+                if (kk != kprev) { kstate_advance(d, s, kk - kprev); kprev = kk; }
+                const RowInfo ri = rowtab[row_of(e)];
+                v[e] = (kbase + kk < K) ? gather_value(d, base, ri, s) : 0.0f;
             }
             kstate_advance(d, ks, BK);
         }
@@ -337,8 +354,8 @@ struct Loader {
     {
 #pragma unroll
         for (int e = 0; e < N; ++e) {
-            const int r = rsub + rstep * e;
-            const int k = ksub0 + kstep * e;
+            const int r = row_of(e);
+            const int k = k_of(e);
             uint32_t o;
             float s;
             decode(v[e], M, offshift, o, s, big);
@@ -363,7 +380,7 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
                                               const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
                                               const float *__restrict__ Ls, const uint8_t *lut, int urow, int lcol)
 {
-#pragma unroll 1
+#pragma unroll(kKkUnroll)
     for (int kk = 0; kk < BK; ++kk) {
         uint32_t lo[TN];
         float2 sb[TN];
