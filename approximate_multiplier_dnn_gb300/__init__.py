@@ -95,6 +95,7 @@ def lib():
                                         i64, i32, vp, vp, sz, vp], i32),
         "amsim_gemm_workspace_size": ([ch, ch, i32, i32, i32, i32, vp], sz),
         "amsim_gemm_grouped": ([i32, ctypes.POINTER(GemmProblem), vp, vp, sz, vp], i32),
+        "amsim_gemm_noalloc": ([ch, ch, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp, vp], i32),
         "amsim_gemm_grouped_workspace_size": ([i32, ctypes.POINTER(GemmProblem), vp], sz),
         "amsim_conv2d_out_hw": ([ctypes.POINTER(ConvDesc), ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "amsim_conv2d_fwd": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
@@ -267,6 +268,13 @@ def amsim_gemm_strided_batched(transA, transB, m, n, k, alpha, A, lda, strideA, 
            lib().amsim_gemm_strided_batched(transA.encode(), transB.encode(), m, n, k, float(alpha), _ptr(A), lda,
                                             strideA, _ptr(B), ldb, strideB, float(beta), _ptr(C), ldc, strideC,
                                             batch, _h(lut), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def amsim_gemm_noalloc(transA, transB, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, lut, stream=None):
+    """amsim_gemm with its scratch inside the library (no workspace, no allocation)."""
+    _check("amsim_gemm_noalloc", lib().amsim_gemm_noalloc(transA.encode(), transB.encode(), m, n, k, float(alpha),
+                                                          _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C), ldc,
+                                                          _h(lut), _stream(stream)))
 
 
 def amsim_gemm_workspace_size(transA, transB, m, n, k, batch, lut) -> int:

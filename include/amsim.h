@@ -194,6 +194,29 @@ int amsim_gemm_grouped(int count, const amsim_gemm_problem *problems, amsim_lut_
 /* Bytes of scratch with which amsim_gemm_grouped runs its fastest plan. */
 size_t amsim_gemm_grouped_workspace_size(int count, const amsim_gemm_problem *problems, amsim_lut_t lut);
 
+/*
+ * amsim_gemm without a workspace argument and without any allocation: for
+ * callers that cannot allocate device memory at call time -- a serving loop
+ * that must not allocate after start-up (cudaMalloc can stall the device and
+ * can fail under memory pressure), a plugin host whose own allocator holds the
+ * memory budget, or an interface with nowhere to keep a workspace.  The ApproxTrain
+ * page has no counterpart; this is a library convenience.
+ *
+ * Same arguments and results as amsim_gemm.  The stream-K partial sums go to a
+ * fixed device array of AMSIM_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library reserves until the process exits.  The
+ * first call on a device looks up that array's address (cudaGetSymbolAddress)
+ * with the device current; make that first call before any stream capture.
+ * All calls on a device share the array and leave their partial sums in it;
+ * nothing needs clearing between calls, but calls that may overlap on the GPU
+ * (unordered streams) race on it and must not be made.  A problem whose plan
+ * needs more scratch than the array holds returns AMSIM_EUNSUPPORTED.
+ */
+#define AMSIM_NOALLOC_SCRATCH_BYTES ((size_t)20 << 20)
+int amsim_gemm_noalloc(char transA, char transB, int m, int n, int k, float alpha,
+                       const float *A, int lda, const float *B, int ldb, float beta,
+                       float *C, int ldc, amsim_lut_t lut, amsim_stream_t stream);
+
 /* ------------------------------------------------------------------ Conv2D */
 
 /*
