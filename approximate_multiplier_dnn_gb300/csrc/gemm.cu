@@ -4,7 +4,7 @@
 #include <algorithm>
 #include <atomic>
 
-#include "gemm_kernel.cuh"
+#include "gemm_ws.cuh"
 
 namespace amsim {
 
@@ -66,6 +66,15 @@ Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail)
     return pl;
 }
 
+int launch_ws(int width, const kern::KParams &kp, bool gl, dim3 grid, size_t smem, cudaStream_t st)
+{
+    switch (width) {
+    case 8: return kern::launch_ws_w8(kp, gl, grid, smem, st);
+    case 16: return kern::launch_ws_w16(kp, gl, grid, smem, st);
+    default: return kern::launch_ws_w32(kp, gl, grid, smem, st);
+    }
+}
+
 int launch_w(int width, const kern::KParams &kp, bool gl, dim3 grid, size_t smem, cudaStream_t st)
 {
     switch (width) {
@@ -88,7 +97,10 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
 
 size_t problem_workspace(const Problem &p, amsim_lut_t lut) { return problems_workspace(&p, 1, lut); }
 
-int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
+namespace {
+
+// One launch for problems that all read the same LUT orientation.
+int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (n <= 0) return AMSIM_OK;
     if (n > kern::kMaxProblems) return AMSIM_EINVAL;
@@ -96,8 +108,9 @@ int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_b
     const Plan pl = make_plan(p, n, sms, ws ? ws_bytes : 0);
     if (pl.total_tiles == 0) return AMSIM_OK;
 
+    const size_t fixed = std::max<size_t>(kern::kFixedSmem, kern::kWsFixedSmem);
     const bool gl = lut->narrow_bytes > (size_t)kMaxSmemLut ||
-                    (size_t)kern::kFixedSmem + kern::lut_region_bytes((int)lut->narrow_bytes) > (size_t)kMaxSmemPerCta;
+                    fixed + kern::lut_region_bytes((int)lut->narrow_bytes) > (size_t)kMaxSmemPerCta;
     kern::KParams kp = {};
     int np = 0;
     for (int i = 0; i < n; ++i) {
@@ -131,13 +144,35 @@ int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_b
     kp.wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
     kp.ws = static_cast<float *>(ws);
 
-    const size_t smem = (size_t)kern::kFixedSmem + (gl ? 0 : kern::lut_region_bytes(kp.table_bytes));
-    if (smem > (size_t)kMaxSmemPerCta) return AMSIM_EUNSUPPORTED;
+    const size_t lutb = gl ? 0 : kern::lut_region_bytes(kp.table_bytes);
     const long long blocks = pl.streamk ? pl.ctas : pl.total_tiles;
     if (blocks > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
-    int rc = launch_w(lut->width_bits, kp, gl, dim3((unsigned)blocks), smem, stream);
+    // warp-specialised kernel first; the single-role kernel if its register
+    // split cannot be honoured on this device
+    int rc = launch_ws(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kWsFixedSmem + lutb, stream);
+    if (rc == AMSIM_EUNSUPPORTED)
+        rc = launch_w(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kFixedSmem + lutb, stream);
     if (rc || !pl.streamk) return rc;
     return kern::launch_fixup(kp, pl.ctas - 1, stream);
+}
+
+}  // namespace
+
+int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (n <= 0) return AMSIM_OK;
+    if (n > kern::kMaxProblems) return AMSIM_EINVAL;
+    if (lut->symmetric) return run_same_table(p, n, lut, ws, ws_bytes, stream);
+    // an asymmetric LUT read in both orientations: one launch per orientation
+    Problem part[kern::kMaxProblems];
+    for (int orient = 0; orient < 2; ++orient) {
+        int m = 0;
+        for (int i = 0; i < n; ++i)
+            if ((int)p[i].u_is_first == orient) part[m++] = p[i];
+        int rc = run_same_table(part, m, lut, ws, ws_bytes, stream);
+        if (rc) return rc;
+    }
+    return AMSIM_OK;
 }
 
 int run_problem(const Problem &p, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)

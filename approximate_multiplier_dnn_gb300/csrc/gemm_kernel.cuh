@@ -290,16 +290,16 @@ __device__ __forceinline__ float gather_value(const OperandDesc &d, const float 
 }
 
 // ------------------------------------------------------------------ operand loader
-// R rows per tile, N = R*BK/NT elements per thread per stage.  "k-fast":
-// thread t owns reduction slot t % BK and rows t/BK + (NT/BK) e.  "row-fast":
-// thread t owns row t % R (t + NT*j when R > NT) and the reduction slots left
-// over.  The host picks the mapping that makes consecutive threads touch
+// R rows per tile, N = R*BK/NTH elements per thread per stage (NTH loading
+// threads).  "k-fast": thread t owns reduction slot t % BK and rows
+// t/BK + (NTH/BK) e.  "row-fast": thread t owns row t % R (t + NTH*j when
+// R > NTH) and the reduction slots left over.  The host picks the mapping that makes consecutive threads touch
 // consecutive addresses.
-template <int R, int N>
+template <int R, int N, int NTH = NT>
 struct Loader {
-    static constexpr int RRF = R > NT ? R / NT : 1;    // row repeats per thread (row-fast)
-    static constexpr int KSF = R < NT ? NT / R : 1;    // reduction-slot stride (row-fast)
-    static_assert(R * BK == N * NT, "loader element count");
+    static constexpr int RRF = R > NTH ? R / NTH : 1;    // row repeats per thread (row-fast)
+    static constexpr int KSF = R < NTH ? NTH / R : 1;    // reduction-slot stride (row-fast)
+    static_assert(R * BK == N * NTH, "loader element count");
     bool kfast;
     int rsub, ksub0;
     int row0;               // global row of tile row 0
@@ -309,7 +309,7 @@ struct Loader {
 
     __device__ __forceinline__ int row_of(int e) const
     {
-        return kfast ? rsub + (NT / BK) * e : rsub + NT * (e % RRF);
+        return kfast ? rsub + (NTH / BK) * e : rsub + NTH * (e % RRF);
     }
     __device__ __forceinline__ int k_of(int e) const { return kfast ? ksub0 : ksub0 + KSF * (e / RRF); }
 
@@ -317,7 +317,7 @@ struct Loader {
     {
         kfast = kf;
         if (kfast) { rsub = tid / BK; ksub0 = tid % BK; }
-        else if (R <= NT) { rsub = tid % R; ksub0 = tid / R; }
+        else if (R <= NTH) { rsub = tid % R; ksub0 = tid / R; }
         else { rsub = tid; ksub0 = 0; }
         row0 = row_tile0;
         base = d.ptr + (long long)b * d.batch_stride;
