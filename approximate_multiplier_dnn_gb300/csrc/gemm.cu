@@ -108,9 +108,14 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     const Plan pl = make_plan(p, n, sms, ws ? ws_bytes : 0);
     if (pl.total_tiles == 0) return AMSIM_OK;
 
-    const size_t fixed = std::max<size_t>(kern::kFixedSmem, kern::kWsFixedSmem);
-    const bool gl = lut->narrow_bytes > (size_t)kMaxSmemLut ||
-                    fixed + kern::lut_region_bytes((int)lut->narrow_bytes) > (size_t)kMaxSmemPerCta;
+    // Shared-memory LUT when it fits beside the warp-specialised kernel's
+    // rings; else beside the single-role kernel's stages; else read from global.
+    const size_t lut_smem = kern::lut_region_bytes((int)lut->narrow_bytes);
+    bool use_ws = true, gl = false;
+    if (lut->narrow_bytes > (size_t)kMaxSmemLut) gl = true;
+    else if ((size_t)kern::kWsFixedSmem + lut_smem <= (size_t)kMaxSmemPerCta) gl = false;
+    else if ((size_t)kern::kFixedSmem + lut_smem <= (size_t)kMaxSmemPerCta) use_ws = false;
+    else gl = true;
     kern::KParams kp = {};
     int np = 0;
     for (int i = 0; i < n; ++i) {
@@ -149,7 +154,9 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     if (blocks > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
     // warp-specialised kernel first; the single-role kernel if its register
     // split cannot be honoured on this device
-    int rc = launch_ws(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kWsFixedSmem + lutb, stream);
+    int rc = AMSIM_EUNSUPPORTED;
+    if (use_ws)
+        rc = launch_ws(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kWsFixedSmem + lutb, stream);
     if (rc == AMSIM_EUNSUPPORTED)
         rc = launch_w(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kFixedSmem + lutb, stream);
     if (rc || !pl.streamk) return rc;

@@ -1,4 +1,4 @@
-// Warp-specialised LUT-GEMM: four producer warps stream the operand tiles from
+// Warp-specialised LUT-GEMM: eight producer warps stream the operand tiles from
 // global memory, decode them (LUT byte offset, power-of-two scale) and fill a
 // two-stage shared-memory ring; eight consumer warps only run the LUT lookups
 // and the fp32x2 accumulation (ApproxTrain Sec. V-B Algorithm 2 per product,
@@ -17,22 +17,39 @@
 namespace amsim {
 namespace kern {
 
+#ifndef AMSIM_WS_PWARPS
+#define AMSIM_WS_PWARPS 8
+#endif
 constexpr int kConsumerWarps = WU * WL;                 // 8
-constexpr int kProducerWarps = 4;                       // one warpgroup
+constexpr int kProducerWarps = AMSIM_WS_PWARPS;         // whole warpgroups
 constexpr int kWsThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kProducerThreads = kProducerWarps * 32;
-constexpr int kStages = 2;
-constexpr int kLaunchRegs = 168;                        // 65536 / 384 rounded down to 8
-constexpr int kProducerRegs = 88;
-constexpr int kConsumerRegs = 208;                      // 256*208 + 128*88 == 384*168
+#ifndef AMSIM_WS_STAGES
+#define AMSIM_WS_STAGES 2
+#endif
+constexpr int kStages = AMSIM_WS_STAGES;                // decoded stages in the ring
+// Register budget: the launch gets 65536 / threads (rounded down to 8) per
+// thread; producers release down to kProducerRegs and consumers grow to
+// kConsumerRegs, which must fit in what the launch holds.
+constexpr int kLaunchRegs = (65536 / kWsThreads) & ~7;
+constexpr int kProducerRegs = kProducerWarps == 4 ? 88 : 56;
+constexpr int kConsumerRegs =
+    ((kWsThreads * kLaunchRegs - kProducerThreads * kProducerRegs) / (kConsumerWarps * 32)) & ~7;
 static_assert(kConsumerWarps * 32 * kConsumerRegs + kProducerThreads * kProducerRegs <=
                   kWsThreads * kLaunchRegs, "register split exceeds the launch allocation");
+static_assert(kConsumerRegs <= 256 && kConsumerRegs >= kLaunchRegs, "consumer register count");
+static_assert(kProducerWarps % 4 == 0, "producer warps must form whole warpgroups");
 static_assert(kConsumerWarps % 4 == 0, "consumer warps must form whole warpgroups");
 
 constexpr long long kWaitLimitNs = 2000000000LL;        // 2 s
 
+#ifndef AMSIM_WS_RAW
+#define AMSIM_WS_RAW 2
+#endif
+constexpr int kRawStages = AMSIM_WS_RAW;                // raw (undecoded) stages in flight
 constexpr int kStageBytes = 2 * BK * UST * 4 + 2 * BK * LST * 4;
-constexpr int kWsFixedSmem = kStages * kStageBytes + kRowTabBytes + 128;
+constexpr int kRawBytes = (BU + BL) * BK * 4;           // one raw stage: U then L elements
+constexpr int kWsFixedSmem = kStages * kStageBytes + kRawStages * kRawBytes + kRowTabBytes + 128;
 
 // Set when a bounded wait gave up (one flag per translation unit).
 static __device__ unsigned int g_ws_wait_timeouts;
@@ -108,6 +125,7 @@ __device__ __forceinline__ void producer_bar()
 struct WsSmem {
     uint8_t *lut;
     uint8_t *stage;        // kStages x kStageBytes
+    float *raw;            // kRawStages x (BU + BL) x BK floats, element e of producer t at [e * threads + t]
     RowInfo *rowU, *rowL;
     uint64_t *full, *empty;
     int *flags;            // [kStages][kProducerWarps]: a stage holds |x| >= 2^64
@@ -164,41 +182,223 @@ __device__ __forceinline__ void for_each_segment(const KParams &p, F &&f)
     }
 }
 
+// ------------------------------------------------------------------ producer
+// Element mapping of a producer thread (same scheme as Loader): "k-fast"
+// thread t owns reduction slot t % BK and rows t/BK + (NTH/BK) e; "row-fast"
+// owns row t % R (t + NTH*j when R > NTH) and the reduction slots left over.
+template <int R>
+struct PMap {
+    static constexpr int NTH = kProducerThreads;
+    static constexpr int N = R * BK / NTH;
+    static constexpr int RRF = R > NTH ? R / NTH : 1;
+    static constexpr int KSF = R < NTH ? NTH / R : 1;
+    static constexpr int CH = N < 8 ? N : 8;             // elements per chunk
+    static_assert(R * BK == N * NTH && N % CH == 0, "producer element count");
+    bool kfast;
+    int rsub, ksub0;
+    __device__ __forceinline__ PMap(bool kf, int tid) : kfast(kf)
+    {
+        if (kfast) { rsub = tid / BK; ksub0 = tid % BK; }
+        else if (R <= NTH) { rsub = tid % R; ksub0 = tid / R; }
+        else { rsub = tid; ksub0 = 0; }
+    }
+    __device__ __forceinline__ int row_of(int e) const
+    {
+        return kfast ? rsub + (NTH / BK) * e : rsub + NTH * (e % RRF);
+    }
+    __device__ __forceinline__ int k_of(int e) const { return kfast ? ksub0 : ksub0 + KSF * (e / RRF); }
+};
+
+__device__ __forceinline__ void cp_async4(float *dst, const float *src, bool valid)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Issue-side state of one operand: asynchronous 4-byte copies of this
+// thread's elements of a stage into the raw ring (zero-filled when out of
+// range), with the gather's reduction-index counter carried across stages.
+template <int R>
+struct PIssue {
+    PMap<R> map;
+    int row0;
+    const float *base;
+    KState ks;
+
+    __device__ __forceinline__ PIssue() : map(false, 0) {}
+
+    __device__ __forceinline__ void init(const OperandDesc &d, bool kf, int tid, int row_tile0, int b, int kt)
+    {
+        map = PMap<R>(kf, tid);
+        row0 = row_tile0;
+        base = d.ptr + (long long)b * d.batch_stride;
+        if (d.gather) ks = kstate_at(d, kt * BK + map.ksub0);
+    }
+
+    __device__ __forceinline__ void issue(const OperandDesc &d, const RowInfo *rowtab, int kt, int K, float *raw,
+                                          int tid)
+    {
+        constexpr int N = PMap<R>::N, CH = PMap<R>::CH;
+        const int kbase = kt * BK;
+        if (!d.gather) {
+#pragma unroll 1
+            for (int c = 0; c < N; c += CH) {
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    const int e = c + j;
+                    const int r = row0 + map.row_of(e);
+                    const int k = kbase + map.k_of(e);
+                    const bool ok = r < d.rows && k < K;
+                    const float *src = ok ? base + (long long)r * d.s_row + (long long)k * d.s_k : d.ptr;
+                    cp_async4(raw + e * kProducerThreads + tid, src, ok);
+                }
+            }
+        } else {
+            KState s = ks;
+            int kprev = map.k_of(0);
+#pragma unroll 1
+            for (int c = 0; c < N; c += CH) {
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    const int e = c + j;
+                    const int kk = map.k_of(e);
+                    if (kk != kprev) { kstate_advance(d, s, kk - kprev); kprev = kk; }
+                    const RowInfo ri = rowtab[map.row_of(e)];
+                    int y = ri.y + s.y, x = ri.x + s.x;
+                    bool ok = kbase + kk < K;
+                    if (d.sy > 1) { ok = ok && y >= 0 && y % d.sy == 0; y /= d.sy; }
+                    if (d.sx > 1) { ok = ok && x >= 0 && x % d.sx == 0; x /= d.sx; }
+                    ok = ok && (unsigned)y < (unsigned)d.IH && (unsigned)x < (unsigned)d.IW;
+                    const float *src = ok ? base + ri.b + s.b + ((long long)y * d.IW + x) * d.Cs : d.ptr;
+                    cp_async4(raw + e * kProducerThreads + tid, src, ok);
+                }
+            }
+            kstate_advance(d, ks, BK);
+        }
+    }
+};
+
+// Decode this thread's landed elements of a stage into the consumer layout.
+template <int R, int ST>
+__device__ __forceinline__ void pdecode(const PMap<R> &map, const float *raw, int tid, uint32_t *off, float *scl,
+                                        int M, int offshift, int &big)
+{
+    constexpr int N = PMap<R>::N, CH = PMap<R>::CH;
+#pragma unroll 1
+    for (int c = 0; c < N; c += CH) {
+        float v[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) v[j] = raw[(c + j) * kProducerThreads + tid];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int e = c + j;
+            uint32_t o;
+            float sc;
+            decode(v[j], M, offshift, o, sc, big);
+            off[map.k_of(e) * ST + map.row_of(e)] = o;
+            scl[map.k_of(e) * ST + map.row_of(e)] = sc;
+        }
+    }
+}
+
+// Where iteration `it` of the launch falls: problem, batch, tile origin, stage.
+struct StagePos {
+    int pi, b, u_tile0, l_tile0, kt;
+};
+
+__device__ __forceinline__ StagePos stage_pos(const KParams &p, long long it)
+{
+    StagePos sp;
+    int pi = 0;
+    while (pi + 1 < p.nprob && it >= p.pr[pi + 1].iter0) ++pi;
+    const ProbParams &q = p.pr[pi];
+    const long long local = it - q.iter0;
+    const long long tile = local / q.kt_total;
+    sp.pi = pi;
+    sp.kt = (int)(local - tile * q.kt_total);
+    const int per_batch = q.tiles_u * q.tiles_l;
+    sp.b = (int)(tile / per_batch);
+    const int rem = (int)(tile - (long long)sp.b * per_batch);
+    sp.u_tile0 = (rem / q.tiles_l) * BU;
+    sp.l_tile0 = (rem % q.tiles_l) * BL;
+    return sp;
+}
+
+__device__ __forceinline__ void cta_range(const KParams &p, long long &it, long long &it_end)
+{
+    if (p.streamk) {
+        it = sk_begin(p.iters, p.ctas, blockIdx.x);
+        it_end = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
+    } else {
+        long long t = blockIdx.x;
+        int pi = 0;
+        while (pi + 1 < p.nprob && t >= p.pr[pi].tiles) t -= p.pr[pi++].tiles;
+        it = p.pr[pi].iter0 + t * p.pr[pi].kt_total;
+        it_end = it + p.pr[pi].kt_total;
+    }
+}
+
 template <int W, bool GL>
 __device__ __forceinline__ void ws_producer(const KParams &p, const WsSmem &sm)
 {
     const int ptid = threadIdx.x - kConsumerWarps * 32;
     const int pwarp = ptid >> 5, lane = ptid & 31;
     const int offU = p.M + p.wlog, offL = p.wlog;
+    long long it0, it1;
+    cta_range(p, it0, it1);
+
+    PIssue<BU> isU;
+    PIssue<BL> isL;
+    // Issue the copies of iteration `it` into raw slot `rs`, starting a new
+    // segment (row tables, counters) at a tile's first stage or the CTA's first.
+    auto issue = [&](long long it, int rs) {
+        const StagePos sp = stage_pos(p, it);
+        const ProbParams &q = p.pr[sp.pi];
+        if (it == it0 || sp.kt == 0) {
+            if (q.U.gather || q.L.gather) {
+                producer_bar();     // all producers are done with the previous row tables
+                if (q.U.gather)
+                    for (int r = ptid; r < BU; r += kProducerThreads) sm.rowU[r] = row_info(q.U, sp.u_tile0 + r);
+                if (q.L.gather)
+                    for (int r = ptid; r < BL; r += kProducerThreads) sm.rowL[r] = row_info(q.L, sp.l_tile0 + r);
+                producer_bar();
+            }
+            isU.init(q.U, q.u_kfast, ptid, sp.u_tile0, sp.b, sp.kt);
+            isL.init(q.L, q.l_kfast, ptid, sp.l_tile0, sp.b, sp.kt);
+        }
+        float *raw = sm.raw + (size_t)rs * ((BU + BL) * BK);
+        isU.issue(q.U, sm.rowU, sp.kt, q.K, raw, ptid);
+        isL.issue(q.L, sm.rowL, sp.kt, q.K, raw + BU * BK, ptid);
+    };
+
+    long long iti = it0;
+    for (int r = 0; r < kRawStages - 1; ++r, ++iti) {
+        if (iti < it1) issue(iti, r);
+        cp_async_commit();
+    }
     uint32_t g = 0;
     bool aborted = false;
-    for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool) {
-        if (q.U.gather || q.L.gather) {
-            producer_bar();     // every producer is done reading the previous segment's row tables
-            if (q.U.gather)
-                for (int r = ptid; r < BU; r += kProducerThreads) sm.rowU[r] = row_info(q.U, u_tile0 + r);
-            if (q.L.gather)
-                for (int r = ptid; r < BL; r += kProducerThreads) sm.rowL[r] = row_info(q.L, l_tile0 + r);
-            producer_bar();
-        }
-        Loader<BU, BU * BK / kProducerThreads, kProducerThreads> ldU;
-        Loader<BL, BL * BK / kProducerThreads, kProducerThreads> ldL;
-        ldU.init(q.U, q.u_kfast, ptid, u_tile0, b, s0);
-        ldL.init(q.L, q.l_kfast, ptid, l_tile0, b, s0);
-        for (int kt = s0; kt < s1; ++kt) {
-            ldU.load(q.U, sm.rowU, kt, q.K);
-            ldL.load(q.L, sm.rowL, kt, q.K);
-            const int slot = g % kStages;
-            mbar_wait(&sm.empty[slot], ((g / kStages) & 1) ^ 1, aborted);
-            int big = 0;
-            ldU.template store<UST>(st_Uoff(sm, slot), st_Uscl(sm, slot), p.M, offU, big);
-            ldL.template store<LST>(st_Loff(sm, slot), st_Lscl(sm, slot), p.M, offL, big);
-            const int any = __any_sync(0xFFFFFFFFu, big);
-            if (lane == 0) sm.flags[slot * kProducerWarps + pwarp] = any;
-            mbar_arrive(&sm.full[slot]);
-            ++g;
-        }
-    });
+    for (long long itd = it0; itd < it1; ++itd, ++iti, ++g) {
+        if (iti < it1) issue(iti, (int)((g + kRawStages - 1) % kRawStages));
+        cp_async_commit();
+        cp_async_wait<kRawStages - 1>();        // this thread's copies of stage g have landed
+        const ProbParams &q = p.pr[stage_pos(p, itd).pi];
+        const int slot = g % kStages;
+        mbar_wait(&sm.empty[slot], ((g / kStages) & 1) ^ 1, aborted);
+        const float *raw = sm.raw + (size_t)(g % kRawStages) * ((BU + BL) * BK);
+        int big = 0;
+        pdecode<BU, UST>(PMap<BU>(q.u_kfast, ptid), raw, ptid, st_Uoff(sm, slot), st_Uscl(sm, slot), p.M, offU, big);
+        pdecode<BL, LST>(PMap<BL>(q.l_kfast, ptid), raw + BU * BK, ptid, st_Loff(sm, slot), st_Lscl(sm, slot), p.M,
+                         offL, big);
+        const int any = __any_sync(0xFFFFFFFFu, big);
+        if (lane == 0) sm.flags[slot * kProducerWarps + pwarp] = any;
+        mbar_arrive(&sm.full[slot]);
+    }
+    cp_async_wait<0>();
 }
 
 template <int W, bool GL>
@@ -222,7 +422,10 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
             const int slot = g % kStages;
             mbar_wait(&sm.full[slot], (g / kStages) & 1, aborted);
             const int *fl = sm.flags + slot * kProducerWarps;
-            const bool slow = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
+            int any_big = 0;
+#pragma unroll
+            for (int w = 0; w < kProducerWarps; ++w) any_big |= fl[w];
+            const bool slow = any_big != 0;
             if (slow)
                 compute_stage<W, GL, true>(acc, st_Uoff(sm, slot), st_Uscl(sm, slot), st_Loff(sm, slot),
                                            st_Lscl(sm, slot), lut, urow, lcol);
@@ -259,9 +462,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) lutgemm_ws_kernel(const __grid_
     WsSmem sm;
     sm.lut = smem;
     sm.stage = smem + lut_bytes;
-    sm.rowU = reinterpret_cast<RowInfo *>(smem + lut_bytes + kStages * kStageBytes);
+    sm.raw = reinterpret_cast<float *>(smem + lut_bytes + kStages * kStageBytes);
+    sm.rowU = reinterpret_cast<RowInfo *>(smem + lut_bytes + kStages * kStageBytes + kRawStages * kRawBytes);
     sm.rowL = sm.rowU + BU;
-    uint8_t *tail = smem + lut_bytes + kStages * kStageBytes + kRowTabBytes;
+    uint8_t *tail = smem + lut_bytes + kStages * kStageBytes + kRawStages * kRawBytes + kRowTabBytes;
     sm.full = reinterpret_cast<uint64_t *>(tail);
     sm.empty = sm.full + kStages;
     sm.flags = reinterpret_cast<int *>(sm.empty + kStages);
