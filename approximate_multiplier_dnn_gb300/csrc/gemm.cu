@@ -16,6 +16,10 @@ using kern::BU;
 
 constexpr int kMaxSmemLut = 160 * 1024;   // LUTs up to this size are staged in shared memory
 
+// Stream-K flag values: every launch gets a fresh one, so flags left in
+// scratch by earlier launches never match.
+std::atomic<unsigned long long> g_epoch{0x5EED0001ULL};
+
 int device_sms(int dev)
 {
     static std::atomic<int> cache[64];
@@ -56,7 +60,7 @@ Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail)
         pl.total_tiles += pl.tiles[i];
     }
     pl.ctas = (int)std::min<long long>(std::min(sms, kern::kMaxFixupParts), pl.iters);
-    pl.sk_bytes = (size_t)2 * pl.ctas * BU * BL * sizeof(float);
+    pl.sk_bytes = (size_t)2 * pl.ctas * BU * BL * sizeof(float) + (size_t)pl.ctas * sizeof(unsigned long long);
     // Data parallel (one CTA per tile) when the tiles fill the SMs in nearly
     // whole waves; otherwise stream-K over (tile, stage) iterations.
     const long long waves = (pl.total_tiles + sms - 1) / std::max(1, sms);
@@ -155,10 +159,22 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     // warp-specialised kernel first; the single-role kernel if its register
     // split cannot be honoured on this device
     int rc = AMSIM_EUNSUPPORTED;
-    if (use_ws)
+    if (use_ws) {
+        // stream-K: finish cut tiles inside the kernel when a cooperative
+        // launch is possible, else run the separate fixup kernel afterwards
+        kp.fused = pl.streamk ? 1 : 0;
+        kp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
         rc = launch_ws(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kWsFixedSmem + lutb, stream);
-    if (rc == AMSIM_EUNSUPPORTED)
+        if (rc == kern::AMSIM_ENOTCOOP) {
+            kp.fused = 0;
+            rc = launch_ws(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kWsFixedSmem + lutb, stream);
+        }
+        if (rc == AMSIM_OK && kp.fused) return AMSIM_OK;
+    }
+    if (rc == AMSIM_EUNSUPPORTED) {
+        kp.fused = 0;
         rc = launch_w(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kFixedSmem + lutb, stream);
+    }
     if (rc || !pl.streamk) return rc;
     return kern::launch_fixup(kp, pl.ctas - 1, stream);
 }

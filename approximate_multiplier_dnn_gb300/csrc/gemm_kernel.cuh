@@ -102,7 +102,9 @@ struct KParams {
     int table_bytes;        // bytes staged to shared memory (0 when read from global)
     int M;
     int wlog;               // log2(entry bytes)
-    float *ws;              // stream-K partial slots [G][2][BU*BL]
+    float *ws;              // stream-K partial slots [G][2][BU*BL], then G epoch flags
+    int fused;              // stream-K cut tiles are finished inside the kernel (cooperative launch)
+    unsigned long long epoch;   // this launch's flag value (never reused)
 };
 
 // Shared-memory layout (bytes) after the LUT region.

@@ -42,6 +42,7 @@ static_assert(kProducerWarps % 4 == 0, "producer warps must form whole warpgroup
 static_assert(kConsumerWarps % 4 == 0, "consumer warps must form whole warpgroups");
 
 constexpr long long kWaitLimitNs = 2000000000LL;        // 2 s
+constexpr int AMSIM_ENOTCOOP = -100;                    // internal: cooperative launch refused
 
 #ifndef AMSIM_WS_RAW
 #define AMSIM_WS_RAW 2
@@ -401,6 +402,52 @@ __device__ __forceinline__ void ws_producer(const KParams &p, const WsSmem &sm)
     cp_async_wait<0>();
 }
 
+__device__ __forceinline__ void consumer_bar()
+{
+    asm volatile("bar.sync 2, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long *sk_flags(const KParams &p)
+{
+    return reinterpret_cast<unsigned long long *>(p.ws + (long long)p.ctas * 2 * (BU * BL));
+}
+
+__device__ __forceinline__ void flag_store(unsigned long long *f, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long flag_load(const unsigned long long *f)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Wait until *f == v (another CTA of this cooperative launch raised it).
+__device__ __forceinline__ void flag_wait(const unsigned long long *f, unsigned long long v, bool &aborted)
+{
+    if (aborted) return;
+    if (flag_load(f) == v) return;
+    const unsigned long long t0 = global_ns();
+    while (flag_load(f) != v) {
+        if (global_ns() - t0 > (unsigned long long)kWaitLimitNs) {
+            aborted = true;
+            atomicOr(&g_ws_wait_timeouts, 2u);
+            return;
+        }
+    }
+}
+
+// One past the last launch iteration of the tile with origin (b, u_tile0, l_tile0).
+__device__ __forceinline__ long long stage_tile_end(const KParams &p, const ProbParams &q, int b, int u_tile0,
+                                                    int l_tile0)
+{
+    const long long tile = (long long)b * q.tiles_u * q.tiles_l + (long long)(u_tile0 / BU) * q.tiles_l +
+                           l_tile0 / BL;
+    return q.iter0 + (tile + 1) * q.kt_total;
+}
+
 template <int W, bool GL>
 __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
 {
@@ -437,16 +484,49 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
         }
         const int u0 = u_tile0 + wu * TM;
         const int l0 = l_tile0 + wl * 32 * TN + lane * TN;
+        const int ur = wu * TM, lr = wl * 32 * TN + lane * TN;
         if (s0 == 0 && s1 == q.kt_total) {
             store_tile(q, acc, b, u0, l0);
-        } else {
+        } else if (!p.fused) {
+            // partial tile for the separate fixup kernel
             float *slotp = p.ws + ((long long)blockIdx.x * 2 + (first ? 0 : 1)) * (BU * BL);
-            const int ur = wu * TM, lr = wl * 32 * TN + lane * TN;
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
                 for (int t4 = 0; t4 < TN / 4; ++t4)
                     *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
+        } else if (s0 > 0) {
+            // The tile began in an earlier CTA: this is this CTA's first
+            // segment.  Leave the partial sum in slot 0 and raise this CTA's
+            // flag; the CTA holding the tile's first stages adds it.
+            float *slotp = p.ws + (long long)blockIdx.x * 2 * (BU * BL);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int t4 = 0; t4 < TN / 4; ++t4)
+                    *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
+            __threadfence();            // this thread's slot writes are visible GPU-wide ...
+            consumer_bar();             // ... before any consumer raises the flag
+            if (threadIdx.x == 0) flag_store(sk_flags(p) + blockIdx.x, p.epoch);
+        } else {
+            // This CTA holds the tile's first stages and ends inside it (its
+            // last segment): add the later CTAs' partial sums in CTA order.
+            const long long tend = stage_tile_end(p, q, b, u_tile0, l_tile0);
+            for (int cc = blockIdx.x + 1; cc < p.ctas && sk_begin(p.iters, p.ctas, cc) < tend; ++cc) {
+                flag_wait(sk_flags(p) + cc, p.epoch, aborted);
+                const float *slotp = p.ws + (long long)cc * 2 * (BU * BL);
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int t4 = 0; t4 < TN / 4; ++t4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(slotp + (ur + i) * BL + lr + 4 * t4));
+                        float2 &a0 = acc[i >> 1][4 * t4], &a1 = acc[i >> 1][4 * t4 + 1];
+                        float2 &a2 = acc[i >> 1][4 * t4 + 2], &a3 = acc[i >> 1][4 * t4 + 3];
+                        if (i & 1) { a0.y += v.x; a1.y += v.y; a2.y += v.z; a3.y += v.w; }
+                        else { a0.x += v.x; a1.x += v.y; a2.x += v.z; a3.x += v.w; }
+                    }
+            }
+            store_tile(q, acc, b, u0, l0);
         }
     });
 }
@@ -517,6 +597,15 @@ int launch_ws_instance(const KParams &p, dim3 grid, size_t smem, cudaStream_t st
         }
     }
     if (checked[dev] < 0) return AMSIM_EUNSUPPORTED;
+    if (p.fused) {
+        // every CTA resident at once: a CTA may wait for later CTAs' partial sums
+        void *args[] = {const_cast<KParams *>(&p)};
+        cudaError_t e = cudaLaunchCooperativeKernel((const void *)lutgemm_ws_kernel<W, GL>, grid, dim3(kWsThreads),
+                                                    args, smem, st);
+        if (e == cudaSuccess) return AMSIM_OK;
+        cudaGetLastError();
+        return AMSIM_ENOTCOOP;
+    }
     lutgemm_ws_kernel<W, GL><<<grid, kWsThreads, smem, st>>>(p);
     return cuda_status(cudaGetLastError());
 }

@@ -75,8 +75,9 @@ class MLPStep:
     """3-layer MLP (784-1000-500-10, batch 256): forward Y_l = X_l W_l, then
     for every layer dX_l = dY_l W_l^T and dW_l = X_l^T dY_l (pure linear
     layers; X_{l+1} = Y_l; dY_l synthetic per layer).  The nine GEMMs run as
-    three grouped launches ordered by their data dependences:
-    {Y1, dX1, dW1, dX2, dX3}, then {Y2, dW2}, then {Y3, dW3}."""
+    three grouped launches ordered by their data dependences and sized so
+    that none is tiny: {Y1, dX1, dW1, dX3}, then {Y2, dX2}, then
+    {Y3, dW3, dW2} (dW2 needs only Y1)."""
 
     def __init__(self, data: dict, lut, device="cuda"):
         import torch
@@ -104,9 +105,9 @@ class MLPStep:
             self.dX.append(dX)
             self.dW.append(dW)
         self.calls = fwd + [c for pair in zip(dxc, dwc) for c in pair]
-        self.groups = [("fwd1+dX1+dW1+dX2+dX3", GemmGroup([fwd[0], dxc[0], dwc[0], dxc[1], dxc[2]])),
-                       ("fwd2+dW2", GemmGroup([fwd[1], dwc[1]])),
-                       ("fwd3+dW3", GemmGroup([fwd[2], dwc[2]]))]
+        self.groups = [("fwd1+dX1+dW1+dX3", GemmGroup([fwd[0], dxc[0], dwc[0], dxc[2]])),
+                       ("fwd2+dX2", GemmGroup([fwd[1], dxc[1]])),
+                       ("fwd3+dW3+dW2", GemmGroup([fwd[2], dwc[2], dwc[1]]))]
         self.ws = workspace(max(g.ws_bytes(lut) for _, g in self.groups), device)
 
     @property
