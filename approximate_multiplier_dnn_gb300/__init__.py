@@ -82,6 +82,7 @@ def lib():
                                  ctypes.c_size_t, ctypes.c_char)
     sig = {
         "amsim_status_string": ([i32], ctypes.c_char_p),
+        "amsim_kernel_launches": ([], ctypes.c_ulonglong),
         "amsim_lut_generate": ([i32, i32, vp], i32),
         "amsim_lut_generate_from_fn": ([APPROX_MUL_FN, i32, vp], i32),
         "amsim_lut_build": ([i32, i32, ctypes.POINTER(vp)], i32),
@@ -119,6 +120,11 @@ def header_functions() -> list[str]:
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"\b(amsim_[a-z0-9_]+)\s*\(", text)
     return sorted(set(names))
+
+
+def amsim_kernel_launches() -> int:
+    """Kernels the library has enqueued so far in this process."""
+    return int(lib().amsim_kernel_launches())
 
 
 def status_string(status: int) -> str:

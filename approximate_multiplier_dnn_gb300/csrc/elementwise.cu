@@ -95,5 +95,7 @@ extern "C" int amsim_mul(const float *a, const float *b, float *c, int64_t n, am
         amsim_mul_kernel<32><<<(unsigned)blocks, 256, 0, st>>>(a, b, c, n, lut->d_narrow, lut->M, lut->shift, vec4);
         break;
     }
-    return amsim::cuda_status(cudaGetLastError());
+    rc = amsim::cuda_status(cudaGetLastError());
+    if (rc == AMSIM_OK) amsim::count_launch();
+    return rc;
 }

@@ -188,6 +188,10 @@ __device__ __forceinline__ uint32_t lut_ld(const uint8_t *lut, uint32_t off)
 // (24 - W) for 8/16-bit tables, the entry itself for 32-bit ones) plus the bit
 // pattern of 1.0f.  A shift and an add keep this off the FMA pipes, which
 // carry the scale multiply and the accumulation.
+// v = 2^carry * 1.mantissa as fp32: the canonical entry (narrowed entry <<
+// (24 - W) for 8/16-bit tables, the entry itself for 32-bit ones) plus the bit
+// pattern of 1.0f.  (A shift-and-add or a multiply-add by 2^(24-W) compile to
+// the same instruction.)
 template <int W>
 __device__ __forceinline__ float expand(uint32_t narrowed)
 {
@@ -745,7 +749,9 @@ int launch_instance(const KParams &p, dim3 grid, size_t smem, cudaStream_t st)
         attr_done[dev] = true;
     }
     lutgemm_kernel<W, GL><<<grid, NT, smem, st>>>(p);
-    return cuda_status(cudaGetLastError());
+    const int rc = cuda_status(cudaGetLastError());
+    if (rc == AMSIM_OK) count_launch();
+    return rc;
 }
 
 int launch_fixup(const KParams &p, int boundaries, cudaStream_t st);

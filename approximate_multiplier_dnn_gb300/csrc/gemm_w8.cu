@@ -8,7 +8,9 @@ int launch_fixup(const KParams &p, int boundaries, cudaStream_t st)
 {
     if (boundaries <= 0) return AMSIM_OK;
     streamk_fixup<256><<<dim3(boundaries, BU * BL / kFixupChunk), 256, 0, st>>>(p);
-    return cuda_status(cudaGetLastError());
+    const int rc = cuda_status(cudaGetLastError());
+    if (rc == AMSIM_OK) count_launch();
+    return rc;
 }
 
 int launch_ws_w8(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st)

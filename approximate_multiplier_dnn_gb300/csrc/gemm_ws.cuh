@@ -537,6 +537,9 @@ template <int W, bool GL>
 __global__ void __launch_bounds__(kWsThreads, 1) lutgemm_ws_kernel(const __grid_constant__ KParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
+    // The next launch on the stream may begin its own set-up as our CTAs
+    // retire (it waits for our results before touching global data).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int lut_bytes = GL ? 0 : lut_region_bytes(p.table_bytes);
     WsSmem sm;
@@ -564,6 +567,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) lutgemm_ws_kernel(const __grid_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // Operands, outputs and scratch may belong to the previous launch on the
+    // stream: wait for it to complete before any of them is touched.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (tid >= kConsumerWarps * 32) {
         reg_dealloc<kProducerRegs>();
@@ -597,17 +603,37 @@ int launch_ws_instance(const KParams &p, dim3 grid, size_t smem, cudaStream_t st
         }
     }
     if (checked[dev] < 0) return AMSIM_EUNSUPPORTED;
-    if (p.fused) {
-        // every CTA resident at once: a CTA may wait for later CTAs' partial sums
-        void *args[] = {const_cast<KParams *>(&p)};
-        cudaError_t e = cudaLaunchCooperativeKernel((const void *)lutgemm_ws_kernel<W, GL>, grid, dim3(kWsThreads),
-                                                    args, smem, st);
-        if (e == cudaSuccess) return AMSIM_OK;
+    // Programmatic stream serialisation lets this launch overlap the tail of
+    // the previous one; a cut tile finished inside the kernel needs every CTA
+    // resident (cooperative).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kWsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    for (int pdl = 1; pdl >= 0; --pdl) {
+        int na = 0;
+        if (pdl) {
+            attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attrs[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
+        if (p.fused) {
+            attrs[na].id = cudaLaunchAttributeCooperative;
+            attrs[na].val.cooperative = 1;
+            ++na;
+        }
+        cfg.attrs = attrs;
+        cfg.numAttrs = na;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, lutgemm_ws_kernel<W, GL>, p);
+        if (e == cudaSuccess) {
+            count_launch();
+            return AMSIM_OK;
+        }
         cudaGetLastError();
-        return AMSIM_ENOTCOOP;
     }
-    lutgemm_ws_kernel<W, GL><<<grid, kWsThreads, smem, st>>>(p);
-    return cuda_status(cudaGetLastError());
+    return p.fused ? AMSIM_ENOTCOOP : AMSIM_ECUDA;
 }
 
 int launch_ws_w8(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);

@@ -4,6 +4,7 @@
 #include <new>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <vector>
 
 #include "amsim_internal.h"
@@ -134,6 +135,12 @@ int build_from_entries(const uint32_t *entries, int M, amsim_lut_t *out)
 
 namespace amsim {
 
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 int cuda_status(cudaError_t e)
 {
     if (e == cudaSuccess) return AMSIM_OK;
@@ -207,6 +214,8 @@ int amsim_lut_info(amsim_lut_t lut, int *M, int *width_bits, int *shift)
     if (shift) *shift = lut->shift;
     return AMSIM_OK;
 }
+
+unsigned long long amsim_kernel_launches(void) { return amsim::g_launches.load(std::memory_order_relaxed); }
 
 void amsim_lut_destroy(amsim_lut_t lut)
 {

@@ -37,5 +37,7 @@ extern "C" int amsim_softmax_rows(const float *S, float *P, int64_t rows, int co
     long long blocks = (rows + 7) / 8;
     if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
     softmax_rows_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(S, P, rows, cols);
-    return amsim::cuda_status(cudaGetLastError());
+    const int rc = amsim::cuda_status(cudaGetLastError());
+    if (rc == AMSIM_OK) amsim::count_launch();
+    return rc;
 }

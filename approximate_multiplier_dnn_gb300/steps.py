@@ -10,7 +10,7 @@ Dense forward (x, w); preceding-layer gradient (dy, w); weight gradient
 """
 from __future__ import annotations
 
-from . import (ConvDesc, GemmProblem, amsim_conv2d_bwd_data, amsim_conv2d_bwd_filter, amsim_conv2d_fwd,
+from . import (ConvDesc, GemmProblem, amsim_mul, amsim_conv2d_bwd_data, amsim_conv2d_bwd_filter, amsim_conv2d_fwd,
                amsim_conv2d_out_hw, amsim_conv2d_workspace_size, amsim_gemm, amsim_gemm_grouped,
                amsim_gemm_grouped_workspace_size, amsim_gemm_strided_batched, amsim_gemm_workspace_size,
                amsim_softmax_rows, workspace)
@@ -252,3 +252,28 @@ class AttentionStep:
         amsim_softmax_rows(self.S, self.P, bh * s, s, stream=stream)
         amsim_gemm_strided_batched("N", "N", s, d, s, 1.0, self.P, s, s * s, self.V, d, s * d, 0.0, self.O, d,
                                    s * d, bh, self.lut, ws=self.ws, stream=stream)
+
+
+class MulStep:
+    """Elementwise AMSim products c = AMSim(a, b) over n pairs."""
+
+    def __init__(self, data: dict, lut, device="cuda"):
+        import torch
+        self.lut = lut
+        self.a = _dev(data["a"], device)
+        self.b = _dev(data["b"], device)
+        self.c = torch.empty_like(self.a)
+
+    @property
+    def macs(self) -> int:
+        return self.a.numel()
+
+    def outputs(self) -> list:
+        return [self.c]
+
+    def parts(self, stream=None):
+        return [("mul", lambda: amsim_mul(self.a, self.b, self.c, self.a.numel(), self.lut, stream=stream),
+                 0, 1)]
+
+    def run(self, stream=None):
+        amsim_mul(self.a, self.b, self.c, self.a.numel(), self.lut, stream=stream)

@@ -32,7 +32,17 @@ METRIC = "approx-GMAC/s for LUT-multiplier GEMM/conv at M=7"
 UNIT = "approx-GMAC/s"
 LOOKUPS_PER_CLK_PER_SM = 32     # one 4-byte shared-memory wavefront per clock per SM
 
-WORKLOADS = ("mlp", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "gemm64")
+WORKLOADS = ("mlp", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "gemm64", "mul")
+
+
+def measured_peaks():
+    """Measured peaks of this machine's GPUs, else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
 
 
 def env_int(name, default):
@@ -61,6 +71,10 @@ def make_step(name, lut_for):
     if name == "conv1x1":
         return (steps.ConvStep(wl.conv1x1(), wl.CONV1X1, lut_for("mitchell", 7), passes=(0,)),
                 "conv1x1_nhwc_64x56x56x256_k256_fwd_mitchell_M7")
+    if name == "mul":
+        from approximate_multiplier_dnn_gb300 import steps as st
+        return st.MulStep(wl.elementwise_pairs(1 << 28, seed=5), lut_for("mitchell", 7)), \
+            "elementwise_2^28_pairs_special_mix_mitchell_M7"
     if name == "gemm64":
         from approximate_multiplier_dnn_gb300 import steps as st
         import torch
@@ -186,9 +200,12 @@ def gpu_id_for_smi(torch):
 def recorded_traffic(workload):
     """Per-launch DRAM bytes of the LUT-GEMM kernel from a committed ncu
     summary, if it was taken on the current kernel source; else None."""
-    src = os.path.join(ROOT, "approximate_multiplier_dnn_gb300", "csrc", "gemm_kernel.cuh")
+    csrc = os.path.join(ROOT, "approximate_multiplier_dnn_gb300", "csrc")
     try:
-        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+        h = hashlib.sha1()
+        for f in ("gemm_kernel.cuh", "gemm_ws.cuh"):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+        sha = h.hexdigest()[:12]
         with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             for line in f:
                 kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
@@ -234,7 +251,7 @@ def reference_arm(args, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mlp", choices=WORKLOADS)
@@ -287,7 +304,25 @@ def main():
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
+
+    def timed_loop(nsteps, per_part):
+        """nsteps steps, L2 flushed and the queue pre-filled before each; events
+        around the step (and around every call when per_part)."""
+        nev = len(parts) + 1 if per_part else 2
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(nsteps)]
+        torch.cuda.synchronize()
+        for s in range(nsteps):
+            flush.fill_(float(s))
+            torch.cuda._sleep(sleep_cycles)
+            evs[s][0].record(stream)
+            for i, p in enumerate(parts):
+                p[1]()
+                if per_part:
+                    evs[s][i + 1].record(stream)
+            if not per_part:
+                evs[s][1].record(stream)
+        torch.cuda.synchronize()
+        return evs
 
     sampler = ClockSampler(gpu_id_for_smi(torch))
     sampler.start()
@@ -296,21 +331,20 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for s in range(K):
-        flush.fill_(float(s))
-        torch.cuda._sleep(sleep_cycles)
-        evs[s][0].record(stream)
-        for i, p in enumerate(parts):
-            p[1]()
-            evs[s][i + 1].record(stream)
-    torch.cuda.synchronize()
+    launches0 = am.amsim_kernel_launches()
+    evs = timed_loop(K, per_part=False)
+    launches_timed = am.amsim_kernel_launches() - launches0
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
 
-    step_ms = [evs[s][0].elapsed_time(evs[s][-1]) for s in range(K)]
-    part_ms = [sum(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(K)) / K for i in range(len(parts))]
+    # per-call times (events between calls stop launches from overlapping, so
+    # these come from a separate, shorter pass)
+    P = max(3, min(K, 50))
+    pevs = timed_loop(P, per_part=True)
+    part_ms = [sum(pevs[s][i].elapsed_time(pevs[s][i + 1]) for s in range(P)) / P for i in range(len(parts))]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
@@ -321,14 +355,27 @@ def main():
     ms_per_step = total_ms / K
 
     # dominant kernel: the LUT-GEMM (every part with MACs), lookups = MACs
+    # its time per step = the timed step time x its share of the per-call pass
     lut_parts = [i for i, p in enumerate(parts) if p[2] > 0]
-    lut_ms = sum(part_ms[i] for i in lut_parts)
+    lut_share = sum(part_ms[i] for i in lut_parts) / max(1e-12, sum(part_ms))
+    lut_ms = ms_per_step * lut_share
     lut_macs = sum(parts[i][2] for i in lut_parts)
     launches_lut = sum(1 for _ in lut_parts)
-    achieved = lut_macs / (lut_ms * 1e-3) / 1e9            # Glookup/s
+    achieved = lut_macs / (lut_ms * 1e-3) / 1e9 if lut_ms > 0 else 0.0   # Glookup/s
     mhz = clocks["sm_mhz"] or props.clock_rate / 1e3
     peak = sms * LOOKUPS_PER_CLK_PER_SM * mhz * 1e6 / 1e9   # Glookup/s
     traffic = recorded_traffic(wname)
+    roofline = {"bound": "alu", "pipe": "shared-memory LUT lookups: SMs x 32 per clock x SM clock",
+                "achieved": achieved, "peak": peak, "unit": "Glookup/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": "lutgemm_ws_kernel (stream-K cut tiles finished in-kernel)",
+                "launches_per_step": launches_lut, "lut_share_of_step": round(lut_share, 4), "sms": sms,
+                "sm_mhz": mhz}
+    if args.workload == "mul":
+        # HBM-bound: 12 bytes per product (two operands in, one result out)
+        hbm, src = measured_peaks()
+        gbs = 12.0 * macs / (ms_per_step * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "peak_source": src, "unit": "GB/s",
+                    "frac": gbs / hbm, "traffic": traffic, "kernel": "amsim_mul_kernel"}
 
     # end to end: pinned host inputs -> device, step, outputs -> pinned host
     e2e = None
@@ -336,6 +383,8 @@ def main():
         inputs = step.inputs
     elif hasattr(step, "x"):
         inputs = {k: getattr(step, k) for k in ("x", "w", "dy") if getattr(step, k, None) is not None}
+    elif hasattr(step, "a"):
+        inputs = {"a": step.a, "b": step.b}
     elif hasattr(step, "Q"):
         inputs = {"Q": step.Q, "K": step.K, "V": step.V}
     else:
@@ -372,7 +421,6 @@ def main():
                "sample": f"{m} MACs: round-robin chunks of {cores} output rows over every contraction, "
                          f"{secs:.1f} s wall"}
 
-    launches_per_step = sum(p[3] for p in parts)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -380,13 +428,10 @@ def main():
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": wname, "macs_per_step": macs, "l2": "flushed before every timed step "
                        "(256 MiB write, outside the timed events)", "parallelism": f"replicas{world}"},
-            "roofline": {"bound": "alu", "pipe": "shared-memory LUT lookups: SMs x 32 per clock x SM clock",
-                         "achieved": achieved, "peak": peak, "unit": "Glookup/s", "frac": achieved / peak,
-                         "traffic": traffic, "kernel": "lutgemm_kernel (+ split-K reduce inside the same calls)",
-                         "launches_timed": launches_lut, "sms": sms, "sm_mhz": mhz},
+            "roofline": roofline,
             "parts_ms": {p[0]: round(t, 5) for p, t in zip(parts, part_ms)},
             "e2e": e2e,
-            "gpu_launches": launches_per_step * K,
+            "gpu_launches": launches_timed,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
                        "samples": clocks["samples"]},
             "wall_s": wall,

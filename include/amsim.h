@@ -69,6 +69,10 @@ enum amsim_status {
 /* Human-readable text for a status code (static storage). */
 const char *amsim_status_string(int status);
 
+/* Number of kernels this library has enqueued in the process so far (all
+ * devices, all calls); a diagnostic for counting launches around a region. */
+unsigned long long amsim_kernel_launches(void);
+
 /* ------------------------------------------------------------------ LUTs */
 
 /*
