@@ -51,6 +51,7 @@ struct OperandDesc {
     int64_t rcb[3];
     int ry0, rx0;        // constant offsets added to the row part
     int IH, IW, Cs, sy, sx;
+    int64_t extent;      // gather: elements of the source tensor (dense operands: computed by the planner)
 };
 
 // A contraction as the kernels see it: out[u][l] = sum_k AMSim-product of the
@@ -75,5 +76,9 @@ size_t problem_workspace(const Problem &p, amsim_lut_t lut);
 // Up to ten independent problems in one launch (one LUT for all).
 int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream);
 size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut);
+// The part of the above that the stream-K schedule alone needs.
+size_t problems_workspace_streamk(const Problem *p, int n, amsim_lut_t lut);
+// Workspace of a (batched) GEMM call: the fastest plan's, or the stream-K part only.
+size_t gemm_workspace(char transA, char transB, int m, int n, int k, int batch, amsim_lut_t lut, bool streamk_only);
 
 }  // namespace amsim

@@ -65,6 +65,7 @@ OperandDesc x_im2col(const Geo &g, const float *x)
     d.kD0 = g.C; d.kD1 = g.S;
     d.kcb[0] = 1; d.kcx[1] = g.dw; d.kcy[2] = g.dh;
     d.IH = g.H; d.IW = g.W; d.Cs = g.C;
+    d.extent = (long long)g.N * g.H * g.W * g.C;
     return d;
 }
 
@@ -79,6 +80,7 @@ OperandDesc x_im2col_weight(const Geo &g, const float *x)
     d.kD0 = g.Q; d.kD1 = g.P;
     d.kcx[0] = g.sw; d.kcy[1] = g.sh; d.kcb[2] = (long long)g.H * g.W * g.C;
     d.IH = g.H; d.IW = g.W; d.Cs = g.C;
+    d.extent = (long long)g.N * g.H * g.W * g.C;
     return d;
 }
 
@@ -96,6 +98,7 @@ OperandDesc dy_im2col_plg(const Geo &g, const float *dy)
     d.kcb[0] = 1; d.kcx[1] = -g.dw; d.kcy[2] = -g.dh;
     d.IH = g.P; d.IW = g.Q; d.Cs = g.K;
     d.sy = g.sh; d.sx = g.sw;
+    d.extent = (long long)g.N * g.P * g.Q * g.K;
     return d;
 }
 
@@ -111,6 +114,7 @@ OperandDesc w_transposed(const Geo &g, const float *w)
     d.kD0 = g.K; d.kD1 = g.S;
     d.kcb[0] = 1; d.kcb[1] = (long long)g.C * g.K; d.kcb[2] = (long long)g.S * g.C * g.K;
     d.IH = 1; d.IW = 1; d.Cs = 0;
+    d.extent = (long long)g.R * g.S * g.C * g.K;
     return d;
 }
 
@@ -130,6 +134,32 @@ int build(const amsim_conv_desc *desc, int which, const float *t0, const float *
     Geo g;
     int rc = geometry(desc, &g);
     if (rc) return rc;
+    // A 1x1 filter at stride 1 without padding reads every operand as a plain
+    // matrix (pixels x channels): dense operands, no gather.
+    const bool pointwise = g.R == 1 && g.S == 1 && g.sh == 1 && g.sw == 1 && g.ph == 0 && g.pw == 0;
+    if (pointwise) {
+        const int pix = g.N * g.H * g.W;
+        if (which == 0) {
+            pr->U = dense(t1, g.K, 1, g.K);              // w[c][k]: row k, index c
+            pr->L = dense(t0, pix, g.C, 1);              // x[pixel][c]
+            pr->K = g.C;
+            set_out(pr, out, 1, g.K);
+        } else if (which == 1) {
+            pr->U = dense(t1, g.C, g.K, 1);              // w[c][k]: row c, index k
+            pr->L = dense(t0, pix, g.K, 1);              // dy[pixel][k]
+            pr->K = g.K;
+            set_out(pr, out, 1, g.C);
+        } else {
+            pr->U = dense(t1, g.K, 1, g.K);              // dy[pixel][k]: row k, index pixel
+            pr->L = dense(t0, g.C, 1, g.C);              // x[pixel][c]: row c, index pixel
+            pr->K = pix;
+            set_out(pr, out, 1, g.K);
+        }
+        pr->u_is_first = false;
+        const long long outs = (long long)pr->U.rows * pr->L.rows;
+        if (outs > 0 && (!t0 || !t1 || !out)) return AMSIM_EINVAL;
+        return AMSIM_OK;
+    }
     if (which == 0) {            // y = conv(x, w): first operand x
         pr->U = dense(t1, g.K, 1, g.K);                  // w[(r,s,c)][k]: row k, index rsc
         pr->L = x_im2col(g, t0);
@@ -151,7 +181,6 @@ int build(const amsim_conv_desc *desc, int which, const float *t0, const float *
     }
     const long long outs = (long long)pr->U.rows * pr->L.rows;
     if (outs > 0 && (!t0 || !t1 || !out)) return AMSIM_EINVAL;
-    if (pr->L.rows == 0) return AMSIM_OK;
     return AMSIM_OK;
 }
 
@@ -201,9 +230,11 @@ int amsim_conv2d_bwd_filter(const amsim_conv_desc *desc, const float *x, const f
 size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim_lut_t lut)
 {
     if (!lut || which < 0 || which > 2) return 0;
-    static const float dummy = 0.0f;
+    // distinct dummy addresses keep the operands' planes apart
+    static const float dummy0 = 0.0f, dummy1 = 0.0f;
+    static float dummy_out = 0.0f;
     Problem pr;
-    if (build(desc, which, &dummy, &dummy, const_cast<float *>(&dummy), &pr)) return 0;
+    if (build(desc, which, &dummy0, &dummy1, &dummy_out, &pr)) return 0;
     return amsim::problem_workspace(pr, lut);
 }
 

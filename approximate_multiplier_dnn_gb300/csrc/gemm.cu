@@ -3,8 +3,12 @@
 // (ApproxTrain Sec. VI-D GEMM kernel; Sec. VI-C AMDENSE forward and gradients).
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
-#include "gemm_ws.cuh"
+#include <cudaTypedefs.h>
+
+#include "gemm_tma.cuh"
+#include "predecode.h"
 
 namespace amsim {
 
@@ -88,6 +92,140 @@ int launch_w(int width, const kern::KParams &kp, bool gl, dim3 grid, size_t smem
     }
 }
 
+// ------------------------------------------------------------------ predecoded operands
+// Every dense operand of a launch becomes a plane pair [batch][2][K][rows_pad]
+// in scratch, after the stream-K region and a block of per-plane flags.
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled encode_tiled()
+{
+    static std::once_flag once;
+    static EncodeTiled fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(f);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+constexpr size_t kFlagBlock = 256;   // kMaxDecodeJobs flags of 8 bytes
+
+struct PlaneKey {
+    const float *src;
+    long long bs, s_row, s_k;
+    int rows, K, nb, offshift;
+    bool operator==(const PlaneKey &o) const
+    {
+        return src == o.src && bs == o.bs && s_row == o.s_row && s_k == o.s_k && rows == o.rows && K == o.K &&
+               nb == o.nb && offshift == o.offshift;
+    }
+};
+
+PlaneKey plane_key(const OperandDesc &d, int K, int batch, int offshift)
+{
+    const int nb = (d.batch_stride == 0 || batch <= 1) ? 1 : batch;
+    return PlaneKey{d.ptr, nb > 1 ? (long long)d.batch_stride : 0LL, d.s_row, d.s_k, d.rows, K, nb, offshift};
+}
+
+int rows_pad(int rows) { return (rows + 3) & ~3; }
+
+size_t plane_bytes(const PlaneKey &k) { return align256((size_t)k.nb * 2 * k.K * rows_pad(k.rows) * 4); }
+
+// Distinct planes of problems [0, n) (operand order U0, L0, U1, L1, ...):
+// slot[2i] / slot[2i+1] give the plane index of problem i's U / L operand.
+struct PlaneSet {
+    PlaneKey key[kern::kMaxDecodeJobs];
+    size_t off[kern::kMaxDecodeJobs];    // from the start of the plane region
+    int n;
+    int slot[2 * kern::kMaxProblems];
+    size_t bytes;
+};
+
+// False when some problem cannot take the predecoded path (gather operand,
+// empty reduction).
+bool plan_planes(const Problem *p, int n, const Plan &pl, int M, int wlog, PlaneSet *ps)
+{
+    ps->n = 0;
+    ps->bytes = 0;
+    for (int i = 0; i < n; ++i) {
+        if (pl.tiles[i] == 0) continue;
+        if (p[i].U.gather || p[i].L.gather || p[i].K <= 0) return false;
+        for (int r = 0; r < 2; ++r) {
+            const OperandDesc &d = r == 0 ? p[i].U : p[i].L;
+            const PlaneKey k = plane_key(d, p[i].K, p[i].batch, r == 0 ? M + wlog : wlog);
+            int j = 0;
+            while (j < ps->n && !(ps->key[j] == k)) ++j;
+            if (j == ps->n) {
+                ps->key[j] = k;
+                ps->off[j] = ps->bytes;
+                ps->bytes += plane_bytes(k);
+                ++ps->n;
+            }
+            ps->slot[2 * i + r] = j;
+        }
+    }
+    return true;
+}
+
+// The planes pay for their extra memory traffic (written once, read at least
+// once) when operand elements are reused by several tiles; a large operand
+// read by a single tile row (attention's P in O = P V) is decoded as cheaply
+// inside the GEMM.  Measured on GB300: 0.03 plane bytes per MAC gains, 0.13
+// loses.  Below 64 MB of planes the pass costs microseconds either way.
+bool planes_pay(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
+{
+    if (ps.bytes <= ((size_t)64 << 20)) return true;
+    double macs = 0.0;
+    for (int i = 0; i < n; ++i)
+        if (pl.tiles[i] > 0) macs += (double)p[i].U.rows * p[i].L.rows * (double)p[i].K * p[i].batch;
+    return (double)ps.bytes <= 0.05 * macs;
+}
+
+// Ring depth of the TMA kernel beside a LUT region of lut_bytes (0 if none fits).
+int tma_stages(size_t lut_bytes)
+{
+    const long long room = (long long)kMaxSmemPerCta - kern::tma_smem_bytes((int)lut_bytes, 0);
+    long long s = room / kern::kTmaStageBytes;
+    if (s > kern::kTmaMaxStages) s = kern::kTmaMaxStages;
+    return s >= 2 ? (int)s : 0;
+}
+
+int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_rows)
+{
+    EncodeTiled enc = encode_tiled();
+    if (!enc) return AMSIM_EUNSUPPORTED;
+    const cuuint64_t pitch = (cuuint64_t)rows_pad(k.rows) * 4;
+    const cuuint64_t dims[4] = {(cuuint64_t)k.rows, (cuuint64_t)k.K, 2, (cuuint64_t)k.nb};
+    const cuuint64_t strides[3] = {pitch, pitch * (cuuint64_t)k.K, pitch * (cuuint64_t)k.K * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)box_rows, (cuuint32_t)kern::BK, 2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
+}
+
+int launch_tma(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
+               cudaStream_t st)
+{
+    switch (width) {
+    case 8: return kern::launch_tma_w8(kp, maps, gl, grid, smem, st);
+    case 16: return kern::launch_tma_w16(kp, maps, gl, grid, smem, st);
+    default: return kern::launch_tma_w32(kp, maps, gl, grid, smem, st);
+    }
+}
+
+// Scratch the predecoded path adds after `base` bytes of stream-K scratch.
+size_t tma_extra(size_t base, const PlaneSet &ps) { return align256(base) - base + kFlagBlock + ps.bytes; }
+
 }  // namespace
 
 size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
@@ -96,7 +234,21 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     const int dev = lut ? lut->device : 0;
     const int sms = device_sms(dev);
     Plan pl = make_plan(p, n, sms, (size_t)-1);
-    return pl.ws_bytes;
+    size_t need = pl.ws_bytes;
+    if (lut && encode_tiled()) {
+        const int wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
+        PlaneSet ps;
+        if (plan_planes(p, n, pl, lut->M, wlog, &ps) && ps.n > 0 && planes_pay(p, n, pl, ps))
+            need += tma_extra(pl.ws_bytes, ps);
+    }
+    return need;
+}
+
+size_t problems_workspace_streamk(const Problem *p, int n, amsim_lut_t lut)
+{
+    if (n <= 0 || n > kern::kMaxProblems) return 0;
+    const int dev = lut ? lut->device : 0;
+    return make_plan(p, n, device_sms(dev), (size_t)-1).ws_bytes;
 }
 
 size_t problem_workspace(const Problem &p, amsim_lut_t lut) { return problems_workspace(&p, 1, lut); }
@@ -153,10 +305,82 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     kp.wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
     kp.ws = static_cast<float *>(ws);
 
-    const size_t lutb = gl ? 0 : kern::lut_region_bytes(kp.table_bytes);
     const long long blocks = pl.streamk ? pl.ctas : pl.total_tiles;
     if (blocks > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
-    // warp-specialised kernel first; the single-role kernel if its register
+
+    // Predecoded operands copied by TMA, when every operand is dense and the
+    // scratch holds the planes after the stream-K region.
+    PlaneSet ps;
+    bool tma_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
+    if (!tma_gl && tma_stages(kern::lut_region_bytes((int)lut->narrow_bytes)) == 0) tma_gl = true;
+    const size_t tma_lutb = tma_gl ? 0 : kern::lut_region_bytes((int)lut->narrow_bytes);
+    if (ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0 && encode_tiled() &&
+        plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 && planes_pay(p, n, pl, ps) &&
+        ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps)) {
+        uint8_t *base = static_cast<uint8_t *>(ws);
+        const size_t flags_off = align256(pl.ws_bytes);
+        unsigned long long *flags = reinterpret_cast<unsigned long long *>(base + flags_off);
+        uint8_t *planes = base + flags_off + kFlagBlock;
+        const unsigned long long epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
+        kern::DecodeParams dp = {};
+        dp.M = lut->M;
+        dp.epoch = epoch;
+        long long dtiles = 0;
+        for (int j = 0; j < ps.n; ++j) {
+            const PlaneKey &k = ps.key[j];
+            kern::DecodeJob &d = dp.job[j];
+            d.src = k.src;
+            d.bs = k.bs;
+            d.s_row = k.s_row;
+            d.s_k = k.s_k;
+            d.rows = k.rows;
+            d.K = k.K;
+            d.batch = k.nb;
+            d.rows_pad = rows_pad(k.rows);
+            d.offshift = k.offshift;
+            d.plane = reinterpret_cast<uint32_t *>(planes + ps.off[j]);
+            d.flag = flags + j;
+            d.tiles_r = ceil_div(k.rows, kern::kDecodeTile);
+            d.tiles_k = ceil_div(k.K, kern::kDecodeTile);
+            d.tile0 = dtiles;
+            dtiles += (long long)k.nb * d.tiles_r * d.tiles_k;
+        }
+        dp.njobs = ps.n;
+        dp.tiles = dtiles;
+        kern::TmaMaps maps;
+        int erc = AMSIM_OK;
+        for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
+            if (pl.tiles[i] == 0) continue;
+            const int ju = ps.slot[2 * i], jl = ps.slot[2 * i + 1];
+            erc = encode_plane_map(&maps.u[qi], ps.key[ju], planes + ps.off[ju], BU);
+            if (erc == AMSIM_OK) erc = encode_plane_map(&maps.l[qi], ps.key[jl], planes + ps.off[jl], BL);
+            kern::ProbParams &q = kp.pr[qi++];
+            q.u_big = flags + ju;
+            q.l_big = flags + jl;
+            q.u_bsel = ps.key[ju].nb > 1 ? 1 : 0;
+            q.l_bsel = ps.key[jl].nb > 1 ? 1 : 0;
+        }
+        if (erc == AMSIM_OK) {
+            kern::KParams tp = kp;
+            tp.table_bytes = tma_gl ? 0 : (int)lut->narrow_bytes;
+            tp.stages = tma_stages(tma_lutb);
+            tp.fused = pl.streamk ? 1 : 0;
+            tp.epoch = epoch;
+            const size_t smem = (size_t)kern::tma_smem_bytes((int)tma_lutb, tp.stages);
+            int rc = kern::launch_predecode(dp, sms, stream);
+            if (rc) return rc;
+            rc = launch_tma(lut->width_bits, tp, maps, tma_gl, dim3((unsigned)blocks), smem, stream);
+            if (rc == kern::AMSIM_ENOTCOOP) {
+                tp.fused = 0;
+                rc = launch_tma(lut->width_bits, tp, maps, tma_gl, dim3((unsigned)blocks), smem, stream);
+            }
+            if (rc == AMSIM_OK) return tp.fused || !pl.streamk ? AMSIM_OK : kern::launch_fixup(tp, pl.ctas - 1, stream);
+            if (rc != AMSIM_EUNSUPPORTED) return rc;
+        }
+    }
+
+    const size_t lutb = gl ? 0 : kern::lut_region_bytes(kp.table_bytes);
+    // warp-specialised kernel next; the single-role kernel if its register
     // split cannot be honoured on this device
     int rc = AMSIM_EUNSUPPORTED;
     if (use_ws) {
@@ -273,6 +497,27 @@ int build_gemm(char transA, char transB, int m, int n, int k, float alpha, const
 
 }  // namespace
 
+namespace amsim {
+
+size_t gemm_workspace(char transA, char transB, int m, int n, int k, int batch, amsim_lut_t lut, bool streamk_only)
+{
+    if (!lut) return 0;
+    Problem pr;
+    static const float dummy = 0.0f;
+    float *dc = const_cast<float *>(&dummy);
+    bool ta, tb;
+    if (!trans_flag(transA, &ta) || !trans_flag(transB, &tb) || m < 0 || n < 0 || k < 0 || batch < 1) return 0;
+    // A distinct dummy address per operand keeps the two planes apart, and a
+    // nonzero batch stride sizes one plane per batch (the most a call can need).
+    static const float dummy2 = 0.0f;
+    if (build_gemm(transA, transB, m, n, k, 1.0f, &dummy, std::max(1, ta ? m : k), 1, &dummy2,
+                   std::max(1, tb ? k : n), 1, 0.0f, dc, std::max(1, n), 0, batch, &pr))
+        return 0;
+    return streamk_only ? problems_workspace_streamk(&pr, 1, lut) : problem_workspace(pr, lut);
+}
+
+}  // namespace amsim
+
 extern "C" {
 
 int amsim_gemm_strided_batched(char transA, char transB, int m, int n, int k, float alpha, const float *A, int lda,
@@ -339,16 +584,7 @@ size_t amsim_gemm_grouped_workspace_size(int count, const amsim_gemm_problem *pr
 
 size_t amsim_gemm_workspace_size(char transA, char transB, int m, int n, int k, int batch, amsim_lut_t lut)
 {
-    if (!lut) return 0;
-    Problem pr;
-    static const float dummy = 0.0f;
-    float *dc = const_cast<float *>(&dummy);
-    bool ta, tb;
-    if (!trans_flag(transA, &ta) || !trans_flag(transB, &tb) || m < 0 || n < 0 || k < 0 || batch < 1) return 0;
-    if (build_gemm(transA, transB, m, n, k, 1.0f, &dummy, std::max(1, ta ? m : k), 0, &dummy,
-                   std::max(1, tb ? k : n), 0, 0.0f, dc, std::max(1, n), 0, batch, &pr))
-        return 0;
-    return amsim::problem_workspace(pr, lut);
+    return amsim::gemm_workspace(transA, transB, m, n, k, batch, lut, false);
 }
 
 }  // extern "C"

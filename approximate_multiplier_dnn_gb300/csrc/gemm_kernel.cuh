@@ -87,6 +87,11 @@ struct ProbParams {
     long long c_bs, c_su, c_sl;
     float alpha, beta;
     int u_kfast, l_kfast;
+    // Predecoded operands (TMA kernel only): each plane's "holds an element
+    // with |x| >= 2^64" flag, raised when it equals the launch epoch, and the
+    // batch coordinate factor (0 when one plane serves every batch).
+    const unsigned long long *u_big, *l_big;
+    int u_bsel, l_bsel;
 };
 
 // A launch: the (problem, tile, stage) iterations of all problems laid end to
@@ -104,6 +109,7 @@ struct KParams {
     int wlog;               // log2(entry bytes)
     float *ws;              // stream-K partial slots [G][2][BU*BL], then G epoch flags
     int fused;              // stream-K cut tiles are finished inside the kernel (cooperative launch)
+    int stages;             // TMA kernel: stages in the shared-memory ring
     unsigned long long epoch;   // this launch's flag value (never reused)
 };
 
@@ -381,7 +387,7 @@ __device__ __forceinline__ float accv(const float2 (&acc)[TM / 2][TN], int i, in
 // One stage of BK reduction steps.  acc[p][t] holds rows (2p, 2p+1) of the
 // warp's TM uniform rows for lane column t, so the U scales pair up straight
 // from the vector loads and only the L scale is duplicated (once per column).
-template <int W, bool GL, bool SLOW>
+template <int W, bool GL, bool SLOW, int USTR = UST, int LSTR = LST>
 __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                               const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
                                               const float *__restrict__ Ls, const uint8_t *lut, int urow, int lcol)
@@ -392,8 +398,8 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
         float2 sb[TN];
 #pragma unroll
         for (int t4 = 0; t4 < TN / 4; ++t4) {
-            const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * LST + lcol + 4 * t4);
-            const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * LST + lcol + 4 * t4);
+            const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * LSTR + lcol + 4 * t4);
+            const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * LSTR + lcol + 4 * t4);
             lo[4 * t4 + 0] = o.x; lo[4 * t4 + 1] = o.y; lo[4 * t4 + 2] = o.z; lo[4 * t4 + 3] = o.w;
             sb[4 * t4 + 0] = make_float2(sc.x, sc.x);
             sb[4 * t4 + 1] = make_float2(sc.y, sc.y);
@@ -402,8 +408,8 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
         }
 #pragma unroll
         for (int ig = 0; ig < TM / 4; ++ig) {
-            const uint4 uo = *reinterpret_cast<const uint4 *>(Uo + kk * UST + urow + 4 * ig);
-            const float4 us = *reinterpret_cast<const float4 *>(Us + kk * UST + urow + 4 * ig);
+            const uint4 uo = *reinterpret_cast<const uint4 *>(Uo + kk * USTR + urow + 4 * ig);
+            const float4 us = *reinterpret_cast<const float4 *>(Us + kk * USTR + urow + 4 * ig);
             const uint32_t uov[4] = {uo.x, uo.y, uo.z, uo.w};
             const float2 sa[2] = {make_float2(us.x, us.y), make_float2(us.z, us.w)};
 #pragma unroll

@@ -1,0 +1,241 @@
+// LUT-GEMM over predecoded operands, fed by the Tensor Memory Accelerator.
+//
+// A separate pass (decode.cu) turns every dense operand into two planes once
+// per launch -- the byte offset of the element's LUT row/column and its signed
+// power-of-two scale, laid out [batch][plane][k][row] -- so that a stage of a
+// tile is one 4-D box per operand: BU (or BL) rows x BK reduction steps x both
+// planes.  One thread issues the two bulk tensor copies of a stage and the
+// copies complete on the stage's "full" mbarrier (transaction bytes); eight
+// consumer warps run the LUT lookups exactly as in the warp-specialised kernel
+// (ApproxTrain Sec. V-B Algorithm 2 per product, Sec. VI-D GEMM kernel) and
+// release the stage on its "empty" mbarrier.  Out-of-range rows and reduction
+// steps arrive as zero words, which decode as offset 0 and scale +0.0: the
+// product of +0.0 adds nothing.
+//
+// Every wait is bounded by the global timer (2 s): a thread that gives up
+// records it in a device flag and skips its remaining waits, and the copy
+// thread waits (again bounded) for its copies still in flight before the CTA
+// ends.
+#pragma once
+
+#include <cuda.h>
+
+#include "gemm_ws.cuh"
+
+namespace amsim {
+namespace kern {
+
+constexpr int kTmaConsumerThreads = WU * WL * 32;              // 256
+constexpr int kTmaThreads = kTmaConsumerThreads + 32;          // + one copy warp
+constexpr int kTmaMaxStages = 6;
+constexpr int kTmaUBytes = 2 * BK * BU * 4;                    // offsets then scales, [k][row]
+constexpr int kTmaLBytes = 2 * BK * BL * 4;
+constexpr int kTmaStageBytes = kTmaUBytes + kTmaLBytes;        // 40 KB
+constexpr int kTmaBarBytes = 2 * kTmaMaxStages * 8;
+static_assert(kTmaStageBytes % 128 == 0 && kTmaUBytes % 128 == 0, "stage alignment");
+
+// Shared memory of the TMA kernel for a ring of `stages` and a LUT region of `lut_bytes`.
+__host__ __device__ constexpr int tma_smem_bytes(int lut_bytes, int stages)
+{
+    return 128 + lut_bytes + stages * kTmaStageBytes + kTmaBarBytes;
+}
+
+// Tensor maps of the operand planes of every problem of a launch.
+struct TmaMaps {
+    CUtensorMap u[kMaxProblems];
+    CUtensorMap l[kMaxProblems];
+};
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Box (x, y, z, w) of the 4-D tensor map into shared memory; completes on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// The copy thread: for every iteration of this CTA, wait for the ring slot to
+// be released, announce the stage's bytes and issue the two box copies.
+__device__ __forceinline__ void tma_producer(const KParams &p, const TmaMaps &maps, uint8_t *ring, uint64_t *full,
+                                             uint64_t *empty)
+{
+    long long it0, it1;
+    cta_range(p, it0, it1);
+    const int S = p.stages;
+    int slot = 0;
+    uint32_t phase = 0;
+    bool aborted = false;
+    long long issued = 0;
+    for (long long it = it0; it < it1; ++it) {
+        if (!mbar_wait(&empty[slot], phase ^ 1, aborted)) break;
+        const StagePos sp = stage_pos(p, it);
+        const ProbParams &q = p.pr[sp.pi];
+        uint8_t *st = ring + (size_t)slot * kTmaStageBytes;
+        mbar_expect_tx(&full[slot], kTmaStageBytes);
+        tma_load_4d(st, &maps.u[sp.pi], sp.u_tile0, sp.kt * BK, 0, sp.b * q.u_bsel, &full[slot]);
+        tma_load_4d(st + kTmaUBytes, &maps.l[sp.pi], sp.l_tile0, sp.kt * BK, 0, sp.b * q.l_bsel, &full[slot]);
+        ++issued;
+        if (++slot == S) { slot = 0; phase ^= 1; }
+    }
+    if (aborted) {
+        // copies issued into slots the consumers never waited for may still
+        // be landing: let them finish before the CTA's shared memory goes away
+        bool gave_up = false;
+        const long long n = issued < S ? issued : S;
+        for (long long j = issued - n; j < issued; ++j) {
+            const int sl = (int)(j % S);
+            mbar_wait(&full[sl], (uint32_t)((j / S) & 1), gave_up);
+        }
+    }
+}
+
+template <int W, bool GL>
+__device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lut, const uint8_t *ring,
+                                             uint64_t *full, uint64_t *empty)
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int wu = warp / WL, wl = warp % WL;
+    const int urow = wu * TM;
+    const int lcol = wl * 32 * TN + lane * TN;
+    const int S = p.stages;
+    int slot = 0;
+    uint32_t phase = 0;
+    bool aborted = false;
+    for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
+        // a problem with an operand of magnitude >= 2^64 rounds every product before adding it
+        const bool slow = __ldcg(q.u_big) == p.epoch || __ldcg(q.l_big) == p.epoch;
+        float2 acc[TM / 2][TN];
+#pragma unroll
+        for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+        for (int kt = s0; kt < s1; ++kt) {
+            mbar_wait(&full[slot], phase, aborted);
+            const uint8_t *st = ring + (size_t)slot * kTmaStageBytes;
+            const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
+            const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
+            const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
+            const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
+            if (slow)
+                compute_stage<W, GL, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+            else
+                compute_stage<W, GL, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+            mbar_arrive(&empty[slot]);
+            if (++slot == S) { slot = 0; phase ^= 1; }
+        }
+        segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, aborted);
+    });
+}
+
+// All problems of a launch read the same LUT orientation (staged once).
+template <int W, bool GL>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    lutgemm_tma_kernel(const __grid_constant__ KParams p, const __grid_constant__ TmaMaps maps)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // The next launch on the stream may begin its own set-up as our CTAs retire.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x;
+    uint8_t *smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
+    const int lut_bytes = GL ? 0 : lut_region_bytes(p.table_bytes);
+    uint8_t *ring = smem + lut_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.stages * kTmaStageBytes);
+    uint64_t *empty = full + kTmaMaxStages;
+
+    if constexpr (!GL) {
+        // the table was written when the LUT was built, before any launch
+        const uint4 *src = static_cast<const uint4 *>(p.pr[0].table);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem);
+        const int nvec = (p.table_bytes + 15) >> 4;
+        for (int i = tid; i < nvec; i += kTmaThreads) dst[i] = __ldg(src + i);
+    }
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kTmaConsumerThreads);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid == kTmaConsumerThreads) {
+        for (int i = 0; i < p.nprob; ++i) {
+            tma_prefetch_map(&maps.u[i]);
+            tma_prefetch_map(&maps.l[i]);
+        }
+    }
+    __syncthreads();
+    // Planes, flags, outputs and scratch belong to earlier launches on the
+    // stream: wait for them to complete before any of them is touched.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
+    if (tid >= kTmaConsumerThreads) {
+        if (tid == kTmaConsumerThreads) tma_producer(p, maps, ring, full, empty);
+    } else {
+        tma_consumer<W, GL>(p, lut, ring, full, empty);
+    }
+}
+
+template <int W, bool GL>
+int launch_tma_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t smem, cudaStream_t st)
+{
+    static int checked[64] = {};   // 0 unknown, 1 configured
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AMSIM_ECUDA;
+    if (dev >= 64) return AMSIM_EUNSUPPORTED;
+    if (checked[dev] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(lutgemm_tma_kernel<W, GL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kMaxSmemPerCta);
+        if (e != cudaSuccess) return cuda_status(e);
+        checked[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    for (int pdl = 1; pdl >= 0; --pdl) {
+        int na = 0;
+        if (pdl) {
+            attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attrs[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
+        if (p.fused) {
+            attrs[na].id = cudaLaunchAttributeCooperative;
+            attrs[na].val.cooperative = 1;
+            ++na;
+        }
+        cfg.attrs = attrs;
+        cfg.numAttrs = na;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, lutgemm_tma_kernel<W, GL>, p, maps);
+        if (e == cudaSuccess) {
+            count_launch();
+            return AMSIM_OK;
+        }
+        cudaGetLastError();
+    }
+    return p.fused ? AMSIM_ENOTCOOP : AMSIM_ECUDA;
+}
+
+int launch_tma_w8(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+int launch_tma_w16(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+int launch_tma_w32(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+
+}  // namespace kern
+}  // namespace amsim

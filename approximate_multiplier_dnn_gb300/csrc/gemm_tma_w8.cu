@@ -1,0 +1,14 @@
+// Instances of the TMA-fed LUT-GEMM kernel for 8-bit narrowed LUT entries.
+#include "gemm_tma.cuh"
+
+namespace amsim {
+namespace kern {
+
+int launch_tma_w8(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st)
+{
+    return gl ? launch_tma_instance<8, true>(p, maps, grid, smem, st)
+              : launch_tma_instance<8, false>(p, maps, grid, smem, st);
+}
+
+}  // namespace kern
+}  // namespace amsim

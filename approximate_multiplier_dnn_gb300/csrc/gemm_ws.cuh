@@ -448,6 +448,65 @@ __device__ __forceinline__ long long stage_tile_end(const KParams &p, const Prob
     return q.iter0 + (tile + 1) * q.kt_total;
 }
 
+// Finish a segment of tile (b, u_tile0, l_tile0) covering stages [s0, s1):
+// store a whole tile, leave a partial sum for the separate fixup kernel, or
+// (fused stream-K) hand a partial sum to / collect partial sums from the
+// other CTAs that share the tile.  Called by all consumer threads.
+__device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbParams &q, float2 (&acc)[TM / 2][TN],
+                                                 int b, int u_tile0, int l_tile0, int s0, int s1, bool first,
+                                                 bool &aborted)
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int wu = warp / WL, wl = warp % WL;
+    const int u0 = u_tile0 + wu * TM;
+    const int l0 = l_tile0 + wl * 32 * TN + lane * TN;
+    const int ur = wu * TM, lr = wl * 32 * TN + lane * TN;
+    if (s0 == 0 && s1 == q.kt_total) {
+        store_tile(q, acc, b, u0, l0);
+    } else if (!p.fused) {
+        // partial tile for the separate fixup kernel
+        float *slotp = p.ws + ((long long)blockIdx.x * 2 + (first ? 0 : 1)) * (BU * BL);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int t4 = 0; t4 < TN / 4; ++t4)
+                *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
+    } else if (s0 > 0) {
+        // The tile began in an earlier CTA: this is this CTA's first
+        // segment.  Leave the partial sum in slot 0 and raise this CTA's
+        // flag; the CTA holding the tile's first stages adds it.
+        float *slotp = p.ws + (long long)blockIdx.x * 2 * (BU * BL);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int t4 = 0; t4 < TN / 4; ++t4)
+                *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
+        __threadfence();            // this thread's slot writes are visible GPU-wide ...
+        consumer_bar();             // ... before any consumer raises the flag
+        if (threadIdx.x == 0) flag_store(sk_flags(p) + blockIdx.x, p.epoch);
+    } else {
+        // This CTA holds the tile's first stages and ends inside it (its
+        // last segment): add the later CTAs' partial sums in CTA order.
+        const long long tend = stage_tile_end(p, q, b, u_tile0, l_tile0);
+        for (int cc = blockIdx.x + 1; cc < p.ctas && sk_begin(p.iters, p.ctas, cc) < tend; ++cc) {
+            flag_wait(sk_flags(p) + cc, p.epoch, aborted);
+            const float *slotp = p.ws + (long long)cc * 2 * (BU * BL);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int t4 = 0; t4 < TN / 4; ++t4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(slotp + (ur + i) * BL + lr + 4 * t4));
+                    float2 &a0 = acc[i >> 1][4 * t4], &a1 = acc[i >> 1][4 * t4 + 1];
+                    float2 &a2 = acc[i >> 1][4 * t4 + 2], &a3 = acc[i >> 1][4 * t4 + 3];
+                    if (i & 1) { a0.y += v.x; a1.y += v.y; a2.y += v.z; a3.y += v.w; }
+                    else { a0.x += v.x; a1.x += v.y; a2.x += v.z; a3.x += v.w; }
+                }
+        }
+        store_tile(q, acc, b, u0, l0);
+    }
+}
+
 template <int W, bool GL>
 __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
 {
@@ -482,52 +541,7 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
             mbar_arrive(&sm.empty[slot]);
             ++g;
         }
-        const int u0 = u_tile0 + wu * TM;
-        const int l0 = l_tile0 + wl * 32 * TN + lane * TN;
-        const int ur = wu * TM, lr = wl * 32 * TN + lane * TN;
-        if (s0 == 0 && s1 == q.kt_total) {
-            store_tile(q, acc, b, u0, l0);
-        } else if (!p.fused) {
-            // partial tile for the separate fixup kernel
-            float *slotp = p.ws + ((long long)blockIdx.x * 2 + (first ? 0 : 1)) * (BU * BL);
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int t4 = 0; t4 < TN / 4; ++t4)
-                    *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
-        } else if (s0 > 0) {
-            // The tile began in an earlier CTA: this is this CTA's first
-            // segment.  Leave the partial sum in slot 0 and raise this CTA's
-            // flag; the CTA holding the tile's first stages adds it.
-            float *slotp = p.ws + (long long)blockIdx.x * 2 * (BU * BL);
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int t4 = 0; t4 < TN / 4; ++t4)
-                    *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
-            __threadfence();            // this thread's slot writes are visible GPU-wide ...
-            consumer_bar();             // ... before any consumer raises the flag
-            if (threadIdx.x == 0) flag_store(sk_flags(p) + blockIdx.x, p.epoch);
-        } else {
-            // This CTA holds the tile's first stages and ends inside it (its
-            // last segment): add the later CTAs' partial sums in CTA order.
-            const long long tend = stage_tile_end(p, q, b, u_tile0, l_tile0);
-            for (int cc = blockIdx.x + 1; cc < p.ctas && sk_begin(p.iters, p.ctas, cc) < tend; ++cc) {
-                flag_wait(sk_flags(p) + cc, p.epoch, aborted);
-                const float *slotp = p.ws + (long long)cc * 2 * (BU * BL);
-#pragma unroll
-                for (int i = 0; i < TM; ++i)
-#pragma unroll
-                    for (int t4 = 0; t4 < TN / 4; ++t4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(slotp + (ur + i) * BL + lr + 4 * t4));
-                        float2 &a0 = acc[i >> 1][4 * t4], &a1 = acc[i >> 1][4 * t4 + 1];
-                        float2 &a2 = acc[i >> 1][4 * t4 + 2], &a3 = acc[i >> 1][4 * t4 + 3];
-                        if (i & 1) { a0.y += v.x; a1.y += v.y; a2.y += v.z; a3.y += v.w; }
-                        else { a0.x += v.x; a1.x += v.y; a2.x += v.z; a3.x += v.w; }
-                    }
-            }
-            store_tile(q, acc, b, u0, l0);
-        }
+        segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, aborted);
     });
 }
 

@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = AMSIM_NOALLOC_SCRATCH_BYTES;   // stream-K slots for up to 160 SMs
+constexpr size_t kScratchBytes = AMSIM_NOALLOC_SCRATCH_BYTES;   // stream-K slots for up to 159 SMs
 
 static __device__ __align__(256) unsigned char amsim_noalloc_scratch[kScratchBytes];
 
@@ -56,9 +56,9 @@ extern "C" int amsim_gemm_noalloc(char transA, char transB, int m, int n, int k,
 {
     int rc = amsim::check_lut(lut);
     if (rc) return rc;
-    // Validate and plan exactly as amsim_gemm does; the workspace query gives
-    // the scratch its fastest plan wants.
-    const size_t need = amsim_gemm_workspace_size(transA, transB, m, n, k, 1, lut);
+    // Plan exactly as amsim_gemm does: the stream-K partial sums must fit in
+    // the array (operand planes that do not fit are simply not used).
+    const size_t need = amsim::gemm_workspace(transA, transB, m, n, k, 1, lut, true);
     if (need > kScratchBytes) return AMSIM_EUNSUPPORTED;
     void *scratch = nullptr;
     rc = scratch_on_current_device(&scratch);

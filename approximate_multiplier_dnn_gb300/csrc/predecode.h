@@ -1,0 +1,48 @@
+// Operand predecode pass of the TMA-fed LUT-GEMM (internal).
+//
+// Each job turns one dense operand -- element (b, r, k) at
+// src[b*bs + r*s_row + k*s_k] -- into two planes laid out [b][plane][k][row]
+// with a row pitch of rows_pad words: plane 0 holds the byte offset of the
+// element's LUT row (U operands) or column (L operands), plane 1 its signed
+// power-of-two scale (ApproxTrain Sec. V-B Algorithm 2: the operand half of
+// the product -- sign, biased exponent, top-M fraction bits, with denormals
+// as zero and NaN kept).  A job raises *flag to the launch epoch when an
+// element has |x| >= 2^64, the magnitude above which a product may overflow.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace amsim {
+namespace kern {
+
+constexpr int kMaxDecodeJobs = 20;
+constexpr int kDecodeTile = 32;                  // rows x reduction steps per tile
+
+struct DecodeJob {
+    const float *src;
+    long long bs, s_row, s_k;                    // element strides
+    int rows, K, batch;                          // batch: planes written (1 for a broadcast operand)
+    int rows_pad;                                // row pitch of a plane, multiple of 4
+    int offshift;                                // offset = top-M fraction bits << offshift
+    uint32_t *plane;                             // [batch][2][K][rows_pad]
+    unsigned long long *flag;
+    int tiles_r, tiles_k;                        // 32 x 32 tiles per batch
+    long long tile0;                             // first tile of this job in the launch
+};
+
+struct DecodeParams {
+    DecodeJob job[kMaxDecodeJobs];
+    int njobs;
+    long long tiles;
+    int M;
+    unsigned long long epoch;
+};
+
+// Enqueue the predecode of all jobs (programmatic dependent launch: the kernel
+// waits for the previous launch on the stream before reading any source).
+int launch_predecode(const DecodeParams &p, int sms, cudaStream_t st);
+
+}  // namespace kern
+}  // namespace amsim

@@ -19,6 +19,8 @@ GEOMS = [
     (3, 12, 11, 20, 70, 3, 3, (1, 1), (1, 1), (1, 1)),
     (2, 16, 16, 64, 64, 3, 3, (2, 2), (1, 1), (1, 1)),
     (1, 6, 40, 33, 9, 5, 1, (1, 1), (2, 0), (1, 1)),
+    (2, 20, 17, 40, 300, 1, 1, (1, 1), (0, 0), (1, 1)),   # pointwise: dense operands
+    (1, 9, 9, 8, 12, 1, 1, (2, 2), (0, 0), (1, 1)),       # strided 1x1: gather
 ]
 
 

@@ -237,3 +237,83 @@ def test_stream_k_shapes(amd, orc, luts, shape):
     rows = np.unique(np.random.default_rng(1).integers(0, m, size=min(m, 40)))
     ref, sa = orc.gemm("mitchell", 7, A, B, rows=rows)
     assert_close(g1[rows], ref, sa, f"stream-k {shape}")
+
+
+def _path_ws(amd, lut, path, tA, tB, m, n, k, batch=1):
+    """Scratch selecting one kernel path: 'planes' (the full size: operands
+    predecoded once into planes, copied by TMA), 'in_kernel' (one byte short:
+    operands decoded inside the GEMM, stream-K kept) or 'none'."""
+    full = amd.amsim_gemm_workspace_size(tA, tB, m, n, k, batch, lut)
+    if path == "planes":
+        return amd.workspace(full)
+    if path == "in_kernel":
+        return amd.workspace(max(full - 1, 1))
+    return None
+
+
+PATH_SHAPES = [(33, 65, 129), (257, 10, 500), (300, 500, 2000), (65, 257, 17), (2, 3, 5000)]
+
+
+@pytest.mark.parametrize("path", ["planes", "in_kernel", "none"])
+@pytest.mark.parametrize("shape", PATH_SHAPES)
+def test_each_kernel_path(amd, orc, luts, shape, path):
+    m, n, k = shape
+    rng = np.random.default_rng(31 * m + 7 * n + k)
+    A, B = rnd(rng, (m, k)), rnd(rng, (n, k))
+    lut = luts("mitchell", 7)
+    got = gpu_gemm(amd, lut, A, B, False, True, ws=_path_ws(amd, lut, path, "N", "T", m, n, k))
+    check(orc, "mitchell", 7, A, B, False, True, got, what=f"{shape} path={path}")
+
+
+@pytest.mark.parametrize("path", ["planes", "in_kernel", "none"])
+def test_special_operands_each_path(amd, orc, luts, path):
+    """Zeros, denormals, infinities, NaNs and |x| >= 2^64 through every path;
+    the predecoded path flags the whole problem for the rounding slow path."""
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    rng = np.random.default_rng(12)
+    a, b = wl.special_values_mix(70 * 130 + 130 * 90, seed=13)
+    A = a[:70 * 130].reshape(70, 130).copy()
+    B = b[70 * 130:70 * 130 + 130 * 90].reshape(130, 90).copy()
+    A[:, :] = np.where(rng.random(A.shape) < 0.93, rng.standard_normal(A.shape), A).astype(np.float32)
+    B[:, :] = np.where(rng.random(B.shape) < 0.93, rng.standard_normal(B.shape), B).astype(np.float32)
+    for kind in ("mitchell", "exact"):
+        lut = luts(kind, 7)
+        got = gpu_gemm(amd, lut, A, B, False, False, ws=_path_ws(amd, lut, path, "N", "N", 70, 90, 130))
+        check(orc, kind, 7, A, B, False, False, got, what=f"specials {kind} path={path}")
+
+
+@pytest.mark.parametrize("path", ["planes", "none"])
+def test_batched_broadcast_operand(amd, orc, luts, path):
+    """strideB = 0: one B serves every batch (one plane for all batches)."""
+    import torch
+    rng = np.random.default_rng(14)
+    batch, m, n, k = 5, 70, 90, 150
+    A = rnd(rng, (batch, m, k))
+    B = rnd(rng, (k, n))
+    lut = luts("mitchell", 7)
+    buf, C = guarded((batch, m, n))
+    full = amd.amsim_gemm_workspace_size("N", "N", m, n, k, batch, lut)
+    ws = amd.workspace(full) if path == "planes" else None
+    amd.amsim_gemm_strided_batched("N", "N", m, n, k, 1.0, to_dev(A), k, m * k, to_dev(B), n, 0, 0.0, C, n, m * n,
+                                   batch, lut, ws=ws)
+    torch.cuda.synchronize()
+    assert guards_intact(buf)
+    got = C.cpu().numpy()
+    for b in range(batch):
+        ref, sa = orc.gemm("mitchell", 7, A[b], B)
+        assert_close(got[b], ref, sa, f"batch {b} path={path}")
+
+
+def test_paths_bit_identical_without_stream_k(amd, luts):
+    """A shape that fills whole waves runs data-parallel on every path; the
+    per-element summation order is the same, so the outputs are bit-identical."""
+    import torch
+    rng = np.random.default_rng(15)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    m, n, k = 64 * sms, 200, 100          # one 64 x 256 tile per SM
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    lut = luts("mitchell", 7)
+    outs = [gpu_gemm(amd, lut, A, B, False, False, ws=_path_ws(amd, lut, p, "N", "N", m, n, k))
+            for p in ("planes", "in_kernel", "none")]
+    for o in outs[1:]:
+        assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32))
