@@ -64,7 +64,8 @@ Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail)
         pl.total_tiles += pl.tiles[i];
     }
     pl.ctas = (int)std::min<long long>(std::min(sms, kern::kMaxFixupParts), pl.iters);
-    pl.sk_bytes = (size_t)2 * pl.ctas * BU * BL * sizeof(float) + (size_t)pl.ctas * sizeof(unsigned long long);
+    // two partial-sum slots and two flags per CTA
+    pl.sk_bytes = (size_t)2 * pl.ctas * BU * BL * sizeof(float) + (size_t)2 * pl.ctas * sizeof(unsigned long long);
     // Data parallel (one CTA per tile) when the tiles fill the SMs in nearly
     // whole waves; otherwise stream-K over (tile, stage) iterations.
     const long long waves = (pl.total_tiles + sms - 1) / std::max(1, sms);
@@ -195,7 +196,7 @@ int tma_stages(size_t lut_bytes)
     const long long room = (long long)kMaxSmemPerCta - kern::tma_smem_bytes((int)lut_bytes, 0);
     long long s = room / kern::kTmaStageBytes;
     if (s > kern::kTmaMaxStages) s = kern::kTmaMaxStages;
-    return s >= 2 ? (int)s : 0;
+    return s >= kern::kTmaMinStages ? (int)s : 0;
 }
 
 int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_rows)
@@ -261,6 +262,8 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     if (n <= 0) return AMSIM_OK;
     if (n > kern::kMaxProblems) return AMSIM_EINVAL;
     const int sms = device_sms(lut->device);
+    // scratch that breaks the 256-byte alignment rule is not used
+    if (reinterpret_cast<uintptr_t>(ws) & 255) ws = nullptr;
     const Plan pl = make_plan(p, n, sms, ws ? ws_bytes : 0);
     if (pl.total_tiles == 0) return AMSIM_OK;
 

@@ -107,7 +107,7 @@ struct KParams {
     int table_bytes;        // bytes staged to shared memory (0 when read from global)
     int M;
     int wlog;               // log2(entry bytes)
-    float *ws;              // stream-K partial slots [G][2][BU*BL], then G epoch flags
+    float *ws;              // stream-K partial slots [G][2][BU*BL], then [G][2] epoch flags
     int fused;              // stream-K cut tiles are finished inside the kernel (cooperative launch)
     int stages;             // TMA kernel: stages in the shared-memory ring
     unsigned long long epoch;   // this launch's flag value (never reused)

@@ -25,13 +25,32 @@
 namespace amsim {
 namespace kern {
 
+// The copy thread lives in one extra warp; with AMSIM_TMA_PWARPS=4 it gets a
+// whole warpgroup that gives its registers to the consumers (setmaxnreg).
+#ifndef AMSIM_TMA_PWARPS
+#define AMSIM_TMA_PWARPS 4
+#endif
 constexpr int kTmaConsumerThreads = WU * WL * 32;              // 256
-constexpr int kTmaThreads = kTmaConsumerThreads + 32;          // + one copy warp
+constexpr int kTmaProducerWarps = AMSIM_TMA_PWARPS;
+constexpr int kTmaThreads = kTmaConsumerThreads + 32 * kTmaProducerWarps;
+constexpr int kTmaLaunchRegs = (65536 / kTmaThreads) & ~7;
+constexpr int kTmaProducerRegs = 56;
+constexpr int kTmaConsumerRegs =
+    ((kTmaThreads * kTmaLaunchRegs - 32 * kTmaProducerWarps * kTmaProducerRegs) / kTmaConsumerThreads) & ~7;
+static_assert(kTmaProducerWarps == 1 || kTmaProducerWarps == 4, "one copy warp or one warpgroup");
+static_assert(kTmaProducerWarps == 1 || (kTmaConsumerRegs <= 256 && kTmaConsumerThreads * kTmaConsumerRegs +
+                                         128 * kTmaProducerRegs <= kTmaThreads * kTmaLaunchRegs),
+              "register split exceeds the launch allocation");
 constexpr int kTmaMaxStages = 6;
 constexpr int kTmaUBytes = 2 * BK * BU * 4;                    // offsets then scales, [k][row]
 constexpr int kTmaLBytes = 2 * BK * BL * 4;
 constexpr int kTmaStageBytes = kTmaUBytes + kTmaLBytes;        // 40 KB
-constexpr int kTmaBarBytes = 2 * kTmaMaxStages * 8;
+constexpr int kTmaBarBytes = (2 * kTmaMaxStages + 1) * 8;        // full, empty, reduction
+// the ring doubles as the stream-K reduction buffer: one tile plus 16 bytes
+// per participant (up to 1024)
+constexpr int kRedBytes = (BU * BL + 1024 * 4) * 4;
+constexpr int kTmaMinStages = (kRedBytes + kTmaStageBytes - 1) / kTmaStageBytes < 2
+                                  ? 2 : (kRedBytes + kTmaStageBytes - 1) / kTmaStageBytes;
 static_assert(kTmaStageBytes % 128 == 0 && kTmaUBytes % 128 == 0, "stage alignment");
 
 // Shared memory of the TMA kernel for a ring of `stages` and a LUT region of `lut_bytes`.
@@ -45,12 +64,6 @@ struct TmaMaps {
     CUtensorMap u[kMaxProblems];
     CUtensorMap l[kMaxProblems];
 };
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
 
 // Box (x, y, z, w) of the 4-D tensor map into shared memory; completes on `bar`.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
@@ -104,8 +117,8 @@ __device__ __forceinline__ void tma_producer(const KParams &p, const TmaMaps &ma
 }
 
 template <int W, bool GL>
-__device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lut, const uint8_t *ring,
-                                             uint64_t *full, uint64_t *empty)
+__device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lut, uint8_t *ring, uint64_t *full,
+                                             uint64_t *empty, uint64_t *red)
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -116,6 +129,8 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
     int slot = 0;
     uint32_t phase = 0;
     bool aborted = false;
+    CutTile cut0, cut1;
+    int ncut = 0;
     for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
         // a problem with an operand of magnitude >= 2^64 rounds every product before adding it
         const bool slow = __ldcg(q.u_big) == p.epoch || __ldcg(q.l_big) == p.epoch;
@@ -138,8 +153,10 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
             mbar_arrive(&empty[slot]);
             if (++slot == S) { slot = 0; phase ^= 1; }
         }
-        segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, aborted);
+        segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, cut0, cut1, ncut);
     });
+    // the ring (at least two 40 KB stages) holds the reduction's copies
+    finish_cut_tiles(p, cut0, cut1, ncut, reinterpret_cast<float *>(ring), S * kTmaStageBytes, red, aborted);
 }
 
 // All problems of a launch read the same LUT orientation (staged once).
@@ -169,6 +186,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kTmaConsumerThreads);
         }
+        mbar_init(empty + kTmaMaxStages, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (tid == kTmaConsumerThreads) {
@@ -184,25 +202,38 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
     if (tid >= kTmaConsumerThreads) {
+        if constexpr (kTmaProducerWarps == 4) reg_dealloc<kTmaProducerRegs>();
         if (tid == kTmaConsumerThreads) tma_producer(p, maps, ring, full, empty);
     } else {
-        tma_consumer<W, GL>(p, lut, ring, full, empty);
+        if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
+        tma_consumer<W, GL>(p, lut, ring, full, empty, empty + kTmaMaxStages);
     }
 }
 
 template <int W, bool GL>
 int launch_tma_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t smem, cudaStream_t st)
 {
-    static int checked[64] = {};   // 0 unknown, 1 configured
+    static int checked[64] = {};   // 0 unknown, 1 usable, -1 register split not satisfiable
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return AMSIM_ECUDA;
     if (dev >= 64) return AMSIM_EUNSUPPORTED;
     if (checked[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(lutgemm_tma_kernel<W, GL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kMaxSmemPerCta);
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, lutgemm_tma_kernel<W, GL>);
         if (e != cudaSuccess) return cuda_status(e);
-        checked[dev] = 1;
+        // setmaxnreg.inc waits for registers released from the launch
+        // allocation; only launch when the split provably fits in it
+        if (kTmaProducerWarps == 4 &&
+            fa.numRegs * kTmaThreads < kTmaConsumerThreads * kTmaConsumerRegs + 128 * kTmaProducerRegs) {
+            checked[dev] = -1;
+        } else {
+            e = cudaFuncSetAttribute(lutgemm_tma_kernel<W, GL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kMaxSmemPerCta);
+            if (e != cudaSuccess) return cuda_status(e);
+            checked[dev] = 1;
+        }
     }
+    if (checked[dev] < 0) return AMSIM_EUNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kTmaThreads);

@@ -51,6 +51,10 @@ constexpr int kRawStages = AMSIM_WS_RAW;                // raw (undecoded) stage
 constexpr int kStageBytes = 2 * BK * UST * 4 + 2 * BK * LST * 4;
 constexpr int kRawBytes = (BU + BL) * BK * 4;           // one raw stage: U then L elements
 constexpr int kWsFixedSmem = kStages * kStageBytes + kRawStages * kRawBytes + kRowTabBytes + 128;
+// the decoded and raw rings (contiguous) double as the stream-K reduction buffer
+static_assert(kStages * kStageBytes + kRawStages * kRawBytes >= (BU * BL + 1024 * 4) * 4,
+              "stream-K reduction buffer");
+static_assert(2 * kStages * 8 + 8 + kStages * kProducerWarps * 4 <= 128, "barrier block");
 
 // Set when a bounded wait gave up (one flag per translation unit).
 static __device__ unsigned int g_ws_wait_timeouts;
@@ -68,6 +72,12 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
@@ -129,6 +139,7 @@ struct WsSmem {
     float *raw;            // kRawStages x (BU + BL) x BK floats, element e of producer t at [e * threads + t]
     RowInfo *rowU, *rowL;
     uint64_t *full, *empty;
+    uint64_t *red;         // completion of the stream-K reduction's bulk copies
     int *flags;            // [kStages][kProducerWarps]: a stage holds |x| >= 2^64
 };
 
@@ -448,13 +459,21 @@ __device__ __forceinline__ long long stage_tile_end(const KParams &p, const Prob
     return q.iter0 + (tile + 1) * q.kt_total;
 }
 
+// A tile cut between CTAs (stream-K): its problem, batch and origin, and its
+// first launch iteration.
+struct CutTile {
+    int pi, b, u_tile0, l_tile0;
+    long long tstart;
+};
+
 // Finish a segment of tile (b, u_tile0, l_tile0) covering stages [s0, s1):
-// store a whole tile, leave a partial sum for the separate fixup kernel, or
-// (fused stream-K) hand a partial sum to / collect partial sums from the
-// other CTAs that share the tile.  Called by all consumer threads.
+// store a whole tile, or leave the partial sum of a cut tile in this CTA's
+// slot (0 for its first segment, 1 for its last) -- for the separate fixup
+// kernel, or (fused stream-K) raising the slot's flag and recording the tile
+// in `cut` so that finish_cut_tiles reduces it.  Called by all consumer threads.
 __device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbParams &q, float2 (&acc)[TM / 2][TN],
                                                  int b, int u_tile0, int l_tile0, int s0, int s1, bool first,
-                                                 bool &aborted)
+                                                 CutTile &cut0, CutTile &cut1, int &ncut)
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -464,46 +483,148 @@ __device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbPar
     const int ur = wu * TM, lr = wl * 32 * TN + lane * TN;
     if (s0 == 0 && s1 == q.kt_total) {
         store_tile(q, acc, b, u0, l0);
-    } else if (!p.fused) {
-        // partial tile for the separate fixup kernel
-        float *slotp = p.ws + ((long long)blockIdx.x * 2 + (first ? 0 : 1)) * (BU * BL);
+        return;
+    }
+    const int slot = first ? 0 : 1;
+    float *slotp = p.ws + ((long long)blockIdx.x * 2 + slot) * (BU * BL);
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int t4 = 0; t4 < TN / 4; ++t4)
-                *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
-    } else if (s0 > 0) {
-        // The tile began in an earlier CTA: this is this CTA's first
-        // segment.  Leave the partial sum in slot 0 and raise this CTA's
-        // flag; the CTA holding the tile's first stages adds it.
-        float *slotp = p.ws + (long long)blockIdx.x * 2 * (BU * BL);
-#pragma unroll
-        for (int i = 0; i < TM; ++i)
-#pragma unroll
-            for (int t4 = 0; t4 < TN / 4; ++t4)
-                *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
-        __threadfence();            // this thread's slot writes are visible GPU-wide ...
-        consumer_bar();             // ... before any consumer raises the flag
-        if (threadIdx.x == 0) flag_store(sk_flags(p) + blockIdx.x, p.epoch);
-    } else {
-        // This CTA holds the tile's first stages and ends inside it (its
-        // last segment): add the later CTAs' partial sums in CTA order.
-        const long long tend = stage_tile_end(p, q, b, u_tile0, l_tile0);
-        for (int cc = blockIdx.x + 1; cc < p.ctas && sk_begin(p.iters, p.ctas, cc) < tend; ++cc) {
-            flag_wait(sk_flags(p) + cc, p.epoch, aborted);
-            const float *slotp = p.ws + (long long)cc * 2 * (BU * BL);
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int t4 = 0; t4 < TN / 4; ++t4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(slotp + (ur + i) * BL + lr + 4 * t4));
-                    float2 &a0 = acc[i >> 1][4 * t4], &a1 = acc[i >> 1][4 * t4 + 1];
-                    float2 &a2 = acc[i >> 1][4 * t4 + 2], &a3 = acc[i >> 1][4 * t4 + 3];
-                    if (i & 1) { a0.y += v.x; a1.y += v.y; a2.y += v.z; a3.y += v.w; }
-                    else { a0.x += v.x; a1.x += v.y; a2.x += v.z; a3.x += v.w; }
-                }
+        for (int t4 = 0; t4 < TN / 4; ++t4)
+            *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
+    if (!p.fused) return;
+    // every consumer's slot writes precede the barrier; the release store of
+    // one thread then publishes all of them (release is cumulative)
+    consumer_bar();
+    if (threadIdx.x == 0) flag_store(sk_flags(p) + 2 * blockIdx.x + slot, p.epoch);
+    CutTile c;
+    c.pi = (int)(&q - p.pr);
+    c.b = b;
+    c.u_tile0 = u_tile0;
+    c.l_tile0 = l_tile0;
+    c.tstart = stage_tile_end(p, q, b, u_tile0, l_tile0) - q.kt_total;
+    if (ncut++ == 0) cut0 = c;
+    else cut1 = c;
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Fused stream-K: every CTA that holds part of a cut tile reduces an equal
+// share of the tile's elements once all of them have left their partial sums.
+// One thread pulls the share of every participant's partial into shared
+// memory (`red`, free once the main loop is over) with bulk copies; then the
+// consumers add the partials in CTA order (the order the separate fixup
+// kernel uses), scale by alpha, add beta*C and store.
+struct CutShare {
+    int c_lo, n;        // participants c_lo .. c_lo + n - 1
+    int lo_slot;        // slot of the first participant's partial (the others use slot 0)
+    int e_lo, m;        // this CTA's float4 units of the tile
+};
+
+__device__ __forceinline__ CutShare cut_share(const KParams &p, const CutTile &ct)
+{
+    constexpr int kUnits = BU * BL / 4;
+    const long long W = p.iters;
+    const int G = p.ctas;
+    const long long tstart = ct.tstart, tend = tstart + p.pr[ct.pi].kt_total;
+    int c_lo = blockIdx.x, c_hi = blockIdx.x;
+    while (c_lo > 0 && sk_begin(W, G, c_lo) > tstart) --c_lo;
+    while (c_hi + 1 < G && sk_begin(W, G, c_hi + 1) < tend) ++c_hi;
+    CutShare sh;
+    sh.c_lo = c_lo;
+    sh.n = c_hi - c_lo + 1;
+    // the first participant began before the tile unless it began exactly at
+    // its start (then the tile was its first segment); every later one began
+    // inside the tile, so the tile was its first segment
+    sh.lo_slot = sk_begin(W, G, c_lo) == tstart ? 0 : 1;
+    const int j = blockIdx.x - c_lo;
+    sh.e_lo = (int)((long long)j * kUnits / sh.n);
+    sh.m = (int)((long long)(j + 1) * kUnits / sh.n) - sh.e_lo;
+    return sh;
+}
+
+// Consumer thread i waits for the flags of participants i, i + 256, ...
+__device__ __forceinline__ void wait_participants(const KParams &p, const CutShare &sh, bool &aborted)
+{
+    for (int i = threadIdx.x; i < sh.n; i += kConsumerWarps * 32)
+        flag_wait(sk_flags(p) + 2 * (sh.c_lo + i) + (i == 0 ? sh.lo_slot : 0), p.epoch, aborted);
+}
+
+// One thread: copy every participant's part of this CTA's share into red.
+__device__ __forceinline__ void copy_share(const KParams &p, const CutShare &sh, float *red, uint64_t *bar)
+{
+    for (int i = 0; i < sh.n; ++i) {
+        const float *src = p.ws + ((long long)(sh.c_lo + i) * 2 + (i == 0 ? sh.lo_slot : 0)) * (BU * BL) + 4 * sh.e_lo;
+        bulk_g2s(red + (size_t)4 * sh.m * i, src, (uint32_t)(16 * sh.m), bar);
+    }
+}
+
+__device__ __forceinline__ void store_share(const KParams &p, const CutTile &ct, const CutShare &sh, const float *red)
+{
+    const ProbParams &q = p.pr[ct.pi];
+    float *C = q.c_ptr + (long long)ct.b * q.c_bs;
+    for (int e = (int)threadIdx.x; e < sh.m; e += kConsumerWarps * 32) {
+        const int ur = (4 * (sh.e_lo + e)) / BL, lr = (4 * (sh.e_lo + e)) % BL;
+        const int u = ct.u_tile0 + ur, l = ct.l_tile0 + lr;
+        float4 sum = *reinterpret_cast<const float4 *>(red + 4 * e);
+        for (int i = 1; i < sh.n; ++i) {
+            const float4 v = *reinterpret_cast<const float4 *>(red + (size_t)4 * sh.m * i + 4 * e);
+            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
         }
-        store_tile(q, acc, b, u0, l0);
+        if (u >= q.U.rows) continue;
+        const float v4[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (l + k >= q.L.rows) break;
+            float *dst = C + (long long)u * q.c_su + (long long)(l + k) * q.c_sl;
+            float r = q.alpha * v4[k];
+            if (q.beta != 0.0f) r = fmaf(q.beta, *dst, r);
+            *dst = r;
+        }
+    }
+}
+
+// Reduce this CTA's cut tiles (at most two: its first and its last segment),
+// both in one round of copies when `red_bytes` holds both shares.
+__device__ __forceinline__ void finish_cut_tiles(const KParams &p, const CutTile &cut0, const CutTile &cut1,
+                                                 int ncut, float *red, int red_bytes, uint64_t *bar, bool &aborted)
+{
+    if (ncut == 0) return;
+    const CutShare sh0 = cut_share(p, cut0);
+    CutShare sh1 = sh0;
+    if (ncut > 1) sh1 = cut_share(p, cut1);
+    const int bytes0 = 16 * sh0.m * sh0.n, bytes1 = ncut > 1 ? 16 * sh1.m * sh1.n : 0;
+    const bool together = ncut > 1 && bytes0 + bytes1 <= red_bytes;
+    uint32_t phase = 0;
+    for (int round = 0; round < (ncut > 1 && !together ? 2 : 1); ++round) {
+        const bool first_tile = round == 0;
+        const bool second_tile = round == 1 || together;
+        if (first_tile) wait_participants(p, sh0, aborted);
+        if (second_tile) wait_participants(p, sh1, aborted);
+        consumer_bar();         // every consumer is past the main loop and has seen the flags
+        float *red1 = first_tile ? red + bytes0 / 4 : red;
+        if (threadIdx.x == 0) {
+            asm volatile("fence.proxy.async;" ::: "memory");
+            mbar_expect_tx(bar, (uint32_t)((first_tile ? bytes0 : 0) + (second_tile ? bytes1 : 0)));
+            if (first_tile) copy_share(p, sh0, red, bar);
+            if (second_tile) copy_share(p, sh1, red1, bar);
+        }
+        // wait for the copies even after an earlier wait gave up: they land in
+        // this CTA's shared memory and must complete before it is released
+        bool copies_timed_out = false;
+        mbar_wait(bar, phase, copies_timed_out);
+        if (first_tile) store_share(p, cut0, sh0, red);
+        if (second_tile) store_share(p, cut1, sh1, red1);
+        consumer_bar();         // the shared buffer is free again
+        phase ^= 1;
     }
 }
 
@@ -518,6 +639,8 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : sm.lut;
     uint32_t g = 0;
     bool aborted = false;
+    CutTile cut0, cut1;
+    int ncut = 0;
     for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
         float2 acc[TM / 2][TN];
 #pragma unroll
@@ -541,8 +664,10 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
             mbar_arrive(&sm.empty[slot]);
             ++g;
         }
-        segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, aborted);
+        segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, cut0, cut1, ncut);
     });
+    finish_cut_tiles(p, cut0, cut1, ncut, reinterpret_cast<float *>(sm.stage),
+                     kStages * kStageBytes + kRawStages * kRawBytes, sm.red, aborted);
 }
 
 // All problems of a launch must read the same LUT orientation (the host splits
@@ -565,7 +690,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) lutgemm_ws_kernel(const __grid_
     uint8_t *tail = smem + lut_bytes + kStages * kStageBytes + kRawStages * kRawBytes + kRowTabBytes;
     sm.full = reinterpret_cast<uint64_t *>(tail);
     sm.empty = sm.full + kStages;
-    sm.flags = reinterpret_cast<int *>(sm.empty + kStages);
+    sm.red = sm.empty + kStages;
+    sm.flags = reinterpret_cast<int *>(sm.red + 1);
 
     if constexpr (!GL) {
         const uint4 *src = static_cast<const uint4 *>(p.pr[0].table);
@@ -578,6 +704,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) lutgemm_ws_kernel(const __grid_
             mbar_init(&sm.full[s], kProducerThreads);
             mbar_init(&sm.empty[s], kConsumerWarps * 32);
         }
+        mbar_init(sm.red, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
