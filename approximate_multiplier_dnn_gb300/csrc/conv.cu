@@ -5,7 +5,7 @@
 // no column buffer is materialised.
 #include <algorithm>
 
-#include "amsim_internal.h"
+#include "gemm_kernel.cuh"
 
 namespace {
 
@@ -118,6 +118,145 @@ OperandDesc w_transposed(const Geo &g, const float *w)
     return d;
 }
 
+// ------------------------------------------------------------------ TMA layouts
+// With unit strides a convolution's operands can be predecoded into planes
+// that tensor boxes read directly: the im2col rows of one filter tap are
+// whole rows of the activation shifted by the tap's column offset (one
+// shifted copy per filter column, built by the predecode pass), and the
+// weight gradient's rows are channel runs of the activation in NHWC order.
+
+amsim::TmaPlaneJob dense_job(const float *src, int rows, int K, long long s_row, long long s_k)
+{
+    amsim::TmaPlaneJob j = {};
+    j.src = src;
+    j.s_row = s_row;
+    j.s_k = s_k;
+    j.rdiv = rows;
+    j.rlim = rows;
+    j.kdiv = K;
+    j.rows = rows;
+    j.K = K;
+    j.batch = 1;
+    j.rows_pad = (rows + 3) & ~3;
+    return j;
+}
+
+// [1][2][K][rows_pad] planes read as BU x BK boxes (the U operand).
+amsim::TmaMapSpec plane_map(const amsim::TmaPlaneJob &j)
+{
+    amsim::TmaMapSpec m = {};
+    m.rank = 4;
+    const uint64_t pitch = (uint64_t)j.rows_pad * 4;
+    m.dims[0] = (uint64_t)j.rows; m.dims[1] = (uint64_t)j.K; m.dims[2] = 2; m.dims[3] = (uint64_t)j.batch;
+    m.strides[0] = pitch; m.strides[1] = pitch * j.K; m.strides[2] = pitch * j.K * 2;
+    m.box[0] = amsim::kern::BU; m.box[1] = amsim::kern::BK; m.box[2] = 2; m.box[3] = 1;
+    return m;
+}
+
+// Shifted copies for the forward pass (act = x, out = y) or the data gradient
+// (act = dy, out = dx): copy s holds act[n][y][x + x0 + s*xs][c] at [n][2][c][y][x]
+// for x in [0, OW), zero outside the activation's width AW.
+void shifted_copies(amsim::ConvTma *cv, const float *act, int N, int AH, int AW, int CH, int OW, int S, int x0,
+                    int xs)
+{
+    cv->nl = S;
+    for (int s = 0; s < S; ++s) {
+        amsim::TmaPlaneJob &j = cv->l[s];
+        j = {};
+        j.src = act;
+        j.batch = N;
+        j.bs = (long long)AH * AW * CH;
+        j.rows = AH * OW;
+        j.rdiv = OW;
+        j.s_rhi = (long long)AW * CH;
+        j.roff = x0 + s * xs;
+        j.rlim = AW;
+        j.s_row = CH;
+        j.K = CH;
+        j.kdiv = CH;
+        j.s_k = 1;
+        j.rows_pad = AH * OW;
+        amsim::TmaMapSpec &m = cv->lmap[s];
+        m = {};
+        m.rank = 5;
+        m.dims[0] = (uint64_t)OW; m.dims[1] = (uint64_t)AH; m.dims[2] = (uint64_t)CH; m.dims[3] = 2;
+        m.dims[4] = (uint64_t)N;
+        m.strides[0] = (uint64_t)OW * 4;
+        m.strides[1] = (uint64_t)AH * OW * 4;
+        m.strides[2] = (uint64_t)CH * AH * OW * 4;
+        m.strides[3] = 2ULL * CH * AH * OW * 4;
+        m.box[0] = (uint32_t)OW; m.box[1] = (uint32_t)(amsim::kern::BL / OW); m.box[2] = amsim::kern::BK;
+        m.box[3] = 2; m.box[4] = 1;
+    }
+}
+
+// Fills *cv and returns true when pass `which` of geometry g can use the TMA layouts.
+bool conv_tma(const Geo &g, int which, const float *t0, const float *t1, amsim::ConvTma *cv)
+{
+    using amsim::kern::BL;
+    if (g.sh != 1 || g.sw != 1 || g.S > amsim::kMaxConvCopies) return false;
+    *cv = {};
+    cv->S = g.S;
+    if (which == 0) {
+        // y[n,p,q,k] = sum x[n, p - ph + r dh, q - pw + s dw, c] w[r,s,c,k]
+        if (g.C % 16 || g.Q % 4 || BL % g.Q || g.P % (BL / g.Q)) return false;
+        cv->mode = 1;
+        cv->u = dense_job(t1, g.K, g.R * g.S * g.C, 1, g.K);
+        shifted_copies(cv, t0, g.N, g.H, g.W, g.C, g.Q, g.S, -g.pw, g.dw);
+        cv->ch = g.C;
+        cv->rows_tile = BL / g.Q;
+        cv->tiles_img = g.P / cv->rows_tile;
+        cv->ybase = -g.ph;
+        cv->ystep = g.dh;
+    } else if (which == 1) {
+        // dx[n,h,w,c] = sum dy[n, h + ph - r dh, w + pw - s dw, k] w[r,s,c,k]
+        if (g.K % 16 || g.W % 4 || BL % g.W || g.H % (BL / g.W)) return false;
+        cv->mode = 1;
+        // filter with its channel axes swapped: row c, index (r, s, k)
+        amsim::TmaPlaneJob u = dense_job(t1, g.C, g.R * g.S * g.K, g.K, 1);
+        u.kdiv = g.K;
+        u.s_khi = (long long)g.C * g.K;
+        cv->u = u;
+        shifted_copies(cv, t0, g.N, g.P, g.Q, g.K, g.W, g.S, g.pw, -g.dw);
+        cv->ch = g.K;
+        cv->rows_tile = BL / g.W;
+        cv->tiles_img = g.H / cv->rows_tile;
+        cv->ybase = g.ph;
+        cv->ystep = -g.dh;
+    } else {
+        // dw[r,s,c,k] = sum over (n,p,q) of x[n, p - ph + r dh, q - pw + s dw, c] dy[n,p,q,k]
+        if (g.C % 64 || g.Q % 16) return false;
+        cv->mode = 2;
+        cv->u = dense_job(t1, g.K, g.N * g.P * g.Q, 1, g.K);
+        // x as planes [n][h][2][w][c]: job batch (n, h), row c, index w
+        cv->nl = 1;
+        amsim::TmaPlaneJob j = dense_job(t0, g.C, g.W, 1, g.C);
+        j.batch = g.N * g.H;
+        j.bs = (long long)g.W * g.C;
+        cv->l[0] = j;
+        amsim::TmaMapSpec &m = cv->lmap[0];
+        m.rank = 5;
+        m.dims[0] = (uint64_t)g.C; m.dims[1] = (uint64_t)g.W; m.dims[2] = 2; m.dims[3] = (uint64_t)g.H;
+        m.dims[4] = (uint64_t)g.N;
+        m.strides[0] = (uint64_t)g.C * 4;
+        m.strides[1] = (uint64_t)g.W * g.C * 4;
+        m.strides[2] = 2ULL * g.W * g.C * 4;
+        m.strides[3] = 2ULL * g.H * g.W * g.C * 4;
+        m.box[0] = 64; m.box[1] = amsim::kern::BK; m.box[2] = 2; m.box[3] = 1; m.box[4] = 1;
+        cv->ch = g.C;
+        cv->N = g.N;
+        cv->P = g.P;
+        cv->Q = g.Q;
+        cv->rows = g.R * g.S * g.C;
+        cv->ybase = -g.ph;
+        cv->ystep = g.dh;
+        cv->xbase = -g.pw;
+        cv->xstep = g.dw;
+    }
+    cv->umap = plane_map(cv->u);
+    return true;
+}
+
 void set_out(Problem *pr, float *out, long long c_su, long long c_sl)
 {
     pr->c_ptr = out;
@@ -192,6 +331,11 @@ int run(const amsim_conv_desc *desc, int which, const float *t0, const float *t1
     Problem pr;
     rc = build(desc, which, t0, t1, out, &pr);
     if (rc) return rc;
+    Geo g;
+    geometry(desc, &g);
+    amsim::ConvTma cv;
+    if (pr.U.gather || pr.L.gather)
+        if (conv_tma(g, which, t0, t1, &cv)) pr.tma = &cv;
     return amsim::run_problem(pr, lut, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -235,6 +379,11 @@ size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim
     static float dummy_out = 0.0f;
     Problem pr;
     if (build(desc, which, &dummy0, &dummy1, &dummy_out, &pr)) return 0;
+    Geo g;
+    geometry(desc, &g);
+    amsim::ConvTma cv;
+    if (pr.U.gather || pr.L.gather)
+        if (conv_tma(g, which, &dummy0, &dummy1, &cv)) pr.tma = &cv;
     return amsim::problem_workspace(pr, lut);
 }
 

@@ -34,8 +34,8 @@ __global__ void __launch_bounds__(256) predecode_kernel(const __grid_constant__ 
         uint32_t *po = d.plane + (size_t)b * 2 * d.K * d.rows_pad;
         float *ps = reinterpret_cast<float *>(po + (size_t)d.K * d.rows_pad);
         int big = 0;
-        if (d.s_row == 1) {
-            // row-fast source: lanes walk rows in both the read and the write
+        if (d.s_row == 1 && d.rdiv >= d.rows && d.kdiv >= d.K && d.roff == 0) {
+            // row-fast dense source: lanes walk rows in both the read and the write
             const int r = r0 + tx;
 #pragma unroll
             for (int i = 0; i < kDecodeTile / 8; ++i) {
@@ -51,14 +51,18 @@ __global__ void __launch_bounds__(256) predecode_kernel(const __grid_constant__ 
         } else {
             // lanes walk k in the read, rows in the write
             const int k = k0 + tx;
+            const long long koff = k < d.K ? (long long)(k / d.kdiv) * d.s_khi + (long long)(k % d.kdiv) * d.s_k : 0;
 #pragma unroll
             for (int i = 0; i < kDecodeTile / 8; ++i) {
                 const int rr = ty + 8 * i, r = r0 + rr;
                 uint32_t o = 0;
                 float s = 0.0f;
-                if (r < d.rows && k < d.K)
-                    decode(__ldcs(src + (long long)r * d.s_row + (long long)k * d.s_k), p.M, d.offshift, o, s,
-                           big);
+                if (r < d.rows && k < d.K) {
+                    const int rl = r % d.rdiv + d.roff;
+                    if (rl >= 0 && rl < d.rlim)   // else a zero operand: offset 0, scale +0
+                        decode(__ldcs(src + (long long)(r / d.rdiv) * d.s_rhi + (long long)rl * d.s_row + koff),
+                               p.M, d.offshift, o, s, big);
+                }
                 t_off[tx][rr] = o;
                 t_scl[tx][rr] = s;
             }

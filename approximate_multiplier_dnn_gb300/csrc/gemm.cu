@@ -214,6 +214,60 @@ int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_ro
     return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
 }
 
+int encode_spec_map(CUtensorMap *map, const TmaMapSpec &m, void *base)
+{
+    EncodeTiled enc = encode_tiled();
+    if (!enc) return AMSIM_EUNSUPPORTED;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], estr[5];
+    for (int i = 0; i < m.rank; ++i) {
+        dims[i] = m.dims[i];
+        box[i] = m.box[i];
+        estr[i] = 1;
+        if (i + 1 < m.rank) strides[i] = m.strides[i];
+    }
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, (cuuint32_t)m.rank, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
+}
+
+size_t job_plane_bytes(const TmaPlaneJob &j) { return align256((size_t)j.batch * 2 * j.K * j.rows_pad * 4); }
+
+// Plane bytes of a convolution's operands.
+size_t conv_plane_bytes(const ConvTma &cv)
+{
+    size_t b = job_plane_bytes(cv.u);
+    for (int i = 0; i < cv.nl; ++i) b += job_plane_bytes(cv.l[i]);
+    return b;
+}
+
+void fill_job(kern::DecodeJob &d, const TmaPlaneJob &j, int offshift, void *plane, unsigned long long *flag,
+              long long &tiles)
+{
+    d.src = j.src;
+    d.bs = j.bs;
+    d.s_row = j.s_row;
+    d.s_k = j.s_k;
+    d.s_rhi = j.s_rhi;
+    d.s_khi = j.s_khi;
+    d.rdiv = j.rdiv;
+    d.roff = j.roff;
+    d.rlim = j.rlim;
+    d.kdiv = j.kdiv;
+    d.rows = j.rows;
+    d.K = j.K;
+    d.batch = j.batch;
+    d.rows_pad = j.rows_pad;
+    d.offshift = offshift;
+    d.plane = static_cast<uint32_t *>(plane);
+    d.flag = flag;
+    d.tiles_r = ceil_div(j.rows, kern::kDecodeTile);
+    d.tiles_k = ceil_div(j.K, kern::kDecodeTile);
+    d.tile0 = tiles;
+    tiles += (long long)j.batch * d.tiles_r * d.tiles_k;
+}
+
 int launch_tma(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
                cudaStream_t st)
 {
@@ -236,7 +290,9 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     const int sms = device_sms(dev);
     Plan pl = make_plan(p, n, sms, (size_t)-1);
     size_t need = pl.ws_bytes;
-    if (lut && encode_tiled()) {
+    if (lut && encode_tiled() && n == 1 && p[0].tma) {
+        need += align256(pl.ws_bytes) - pl.ws_bytes + kFlagBlock + conv_plane_bytes(*p[0].tma);
+    } else if (lut && encode_tiled()) {
         const int wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
         PlaneSet ps;
         if (plan_planes(p, n, pl, lut->M, wlog, &ps) && ps.n > 0 && planes_pay(p, n, pl, ps))
@@ -311,13 +367,72 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     const long long blocks = pl.streamk ? pl.ctas : pl.total_tiles;
     if (blocks > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
 
-    // Predecoded operands copied by TMA, when every operand is dense and the
-    // scratch holds the planes after the stream-K region.
+    // Predecoded operands copied by TMA, when every operand is dense (or a
+    // convolution laid out for TMA) and the scratch holds the planes after the
+    // stream-K region.
     PlaneSet ps;
     bool tma_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
     if (!tma_gl && tma_stages(kern::lut_region_bytes((int)lut->narrow_bytes)) == 0) tma_gl = true;
     const size_t tma_lutb = tma_gl ? 0 : kern::lut_region_bytes((int)lut->narrow_bytes);
-    if (ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0 && encode_tiled() &&
+    if (n == 1 && p[0].tma && pl.tiles[0] > 0 && ws && encode_tiled() &&
+        ws_bytes >= align256(pl.ws_bytes) + kFlagBlock + conv_plane_bytes(*p[0].tma)) {
+        const ConvTma &cv = *p[0].tma;
+        uint8_t *base = static_cast<uint8_t *>(ws);
+        const size_t flags_off = align256(pl.ws_bytes);
+        unsigned long long *flags = reinterpret_cast<unsigned long long *>(base + flags_off);
+        uint8_t *plane = base + flags_off + kFlagBlock;
+        const unsigned long long epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
+        kern::DecodeParams dp = {};
+        dp.M = lut->M;
+        dp.epoch = epoch;
+        long long dtiles = 0;
+        kern::TmaMaps maps;
+        int erc = encode_spec_map(&maps.u[0], cv.umap, plane);
+        fill_job(dp.job[0], cv.u, lut->M + kp.wlog, plane, flags, dtiles);
+        plane += job_plane_bytes(cv.u);
+        for (int i = 0; i < cv.nl && erc == AMSIM_OK; ++i) {
+            erc = encode_spec_map(&maps.l[i], cv.lmap[i], plane);
+            fill_job(dp.job[1 + i], cv.l[i], kp.wlog, plane, flags + 1, dtiles);
+            plane += job_plane_bytes(cv.l[i]);
+        }
+        dp.njobs = 1 + cv.nl;
+        dp.tiles = dtiles;
+        if (erc == AMSIM_OK) {
+            kern::KParams tp = kp;
+            kern::ProbParams &q = tp.pr[0];
+            q.u_big = flags;
+            q.l_big = flags + 1;
+            q.u_bsel = q.l_bsel = 0;
+            tp.conv = cv.mode;
+            tp.cv_ch = cv.ch;
+            tp.cv_S = cv.S;
+            tp.cv_tiles_img = cv.tiles_img;
+            tp.cv_rows_tile = cv.rows_tile;
+            tp.cv_ybase = cv.ybase;
+            tp.cv_ystep = cv.ystep;
+            tp.cv_xbase = cv.xbase;
+            tp.cv_xstep = cv.xstep;
+            tp.cv_N = cv.N;
+            tp.cv_P = cv.P;
+            tp.cv_Q = cv.Q;
+            tp.cv_rows = cv.rows;
+            tp.table_bytes = tma_gl ? 0 : (int)lut->narrow_bytes;
+            tp.stages = tma_stages(tma_lutb);
+            tp.fused = pl.streamk ? 1 : 0;
+            tp.epoch = epoch;
+            const size_t smem = (size_t)kern::tma_smem_bytes((int)tma_lutb, tp.stages);
+            int rc = kern::launch_predecode(dp, sms, stream);
+            if (rc) return rc;
+            rc = launch_tma(lut->width_bits, tp, maps, tma_gl, dim3((unsigned)blocks), smem, stream);
+            if (rc == kern::AMSIM_ENOTCOOP) {
+                tp.fused = 0;
+                rc = launch_tma(lut->width_bits, tp, maps, tma_gl, dim3((unsigned)blocks), smem, stream);
+            }
+            if (rc == AMSIM_OK) return tp.fused || !pl.streamk ? AMSIM_OK : kern::launch_fixup(tp, pl.ctas - 1, stream);
+            if (rc != AMSIM_EUNSUPPORTED) return rc;
+        }
+    }
+    if (ws && encode_tiled() &&
         plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 && planes_pay(p, n, pl, ps) &&
         ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps)) {
         uint8_t *base = static_cast<uint8_t *>(ws);
@@ -336,6 +451,12 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             d.bs = k.bs;
             d.s_row = k.s_row;
             d.s_k = k.s_k;
+            d.s_rhi = 0;
+            d.s_khi = 0;
+            d.rdiv = k.rows;
+            d.roff = 0;
+            d.rlim = k.rows;
+            d.kdiv = k.K;
             d.rows = k.rows;
             d.K = k.K;
             d.batch = k.nb;

@@ -1,8 +1,12 @@
 // Operand predecode pass of the TMA-fed LUT-GEMM (internal).
 //
-// Each job turns one dense operand -- element (b, r, k) at
-// src[b*bs + r*s_row + k*s_k] -- into two planes laid out [b][plane][k][row]
-// with a row pitch of rows_pad words: plane 0 holds the byte offset of the
+// Each job turns one operand into two planes laid out [b][plane][k][row] with
+// a row pitch of rows_pad words.  Element (b, r, k) of the operand is
+//   src[b*bs + (r / rdiv)*s_rhi + (r % rdiv + roff)*s_row + (k / kdiv)*s_khi + (k % kdiv)*s_k]
+// and reads as zero when r % rdiv + roff falls outside [0, rlim) -- a dense
+// matrix (rdiv = rows, kdiv = K), a filter read with its channel axes
+// swapped, or an activation shifted along its width for one filter column.
+// Plane 0 holds the byte offset of the
 // element's LUT row (U operands) or column (L operands), plane 1 its signed
 // power-of-two scale (ApproxTrain Sec. V-B Algorithm 2: the operand half of
 // the product -- sign, biased exponent, top-M fraction bits, with denormals
@@ -23,6 +27,8 @@ constexpr int kDecodeTile = 32;                  // rows x reduction steps per t
 struct DecodeJob {
     const float *src;
     long long bs, s_row, s_k;                    // element strides
+    long long s_rhi, s_khi;                      // strides of r / rdiv and k / kdiv
+    int rdiv, roff, rlim, kdiv;
     int rows, K, batch;                          // batch: planes written (1 for a broadcast operand)
     int rows_pad;                                // row pitch of a plane, multiple of 4
     int offshift;                                // offset = top-M fraction bits << offshift
