@@ -262,8 +262,8 @@ void fill_job(kern::DecodeJob &d, const TmaPlaneJob &j, int offshift, void *plan
     d.offshift = offshift;
     d.plane = static_cast<uint32_t *>(plane);
     d.flag = flag;
-    d.tiles_r = ceil_div(j.rows, kern::kDecodeTile);
-    d.tiles_k = ceil_div(j.K, kern::kDecodeTile);
+    d.tiles_r = ceil_div(j.rows, kern::kDecodeTileR);
+    d.tiles_k = ceil_div(j.K, kern::kDecodeTileK);
     d.tile0 = tiles;
     tiles += (long long)j.batch * d.tiles_r * d.tiles_k;
 }
@@ -464,8 +464,8 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             d.offshift = k.offshift;
             d.plane = reinterpret_cast<uint32_t *>(planes + ps.off[j]);
             d.flag = flags + j;
-            d.tiles_r = ceil_div(k.rows, kern::kDecodeTile);
-            d.tiles_k = ceil_div(k.K, kern::kDecodeTile);
+            d.tiles_r = ceil_div(k.rows, kern::kDecodeTileR);
+            d.tiles_k = ceil_div(k.K, kern::kDecodeTileK);
             d.tile0 = dtiles;
             dtiles += (long long)k.nb * d.tiles_r * d.tiles_k;
         }

@@ -194,8 +194,15 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
         for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
             for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+        // a warp whose rows or columns all lie past the problem's edge has nothing to add
+        const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + wl * 32 * TN >= q.L.rows;
         for (int kt = s0; kt < s1; ++kt) {
             mbar_wait(&full[slot], phase, aborted);
+            if (idle) {
+                mbar_arrive(&empty[slot]);
+                if (++slot == S) { slot = 0; phase ^= 1; }
+                continue;
+            }
             const uint8_t *st = ring + (size_t)slot * kTmaStageBytes;
             const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
             const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);

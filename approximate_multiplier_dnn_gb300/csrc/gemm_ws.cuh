@@ -647,9 +647,16 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
         for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
             for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+        // a warp whose rows or columns all lie past the problem's edge has nothing to add
+        const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + wl * 32 * TN >= q.L.rows;
         for (int kt = s0; kt < s1; ++kt) {
             const int slot = g % kStages;
             mbar_wait(&sm.full[slot], (g / kStages) & 1, aborted);
+            if (idle) {
+                mbar_arrive(&sm.empty[slot]);
+                ++g;
+                continue;
+            }
             const int *fl = sm.flags + slot * kProducerWarps;
             int any_big = 0;
 #pragma unroll

@@ -22,7 +22,8 @@ namespace amsim {
 namespace kern {
 
 constexpr int kMaxDecodeJobs = 20;
-constexpr int kDecodeTile = 32;                  // rows x reduction steps per tile
+constexpr int kDecodeTileR = 64;                 // rows per tile
+constexpr int kDecodeTileK = 32;                 // reduction steps per tile
 
 struct DecodeJob {
     const float *src;
@@ -34,7 +35,7 @@ struct DecodeJob {
     int offshift;                                // offset = top-M fraction bits << offshift
     uint32_t *plane;                             // [batch][2][K][rows_pad]
     unsigned long long *flag;
-    int tiles_r, tiles_k;                        // 32 x 32 tiles per batch
+    int tiles_r, tiles_k;                        // 64 x 32 tiles per batch
     long long tile0;                             // first tile of this job in the launch
 };
 
