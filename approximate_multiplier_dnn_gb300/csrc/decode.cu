@@ -13,96 +13,131 @@ namespace kern {
 
 namespace {
 
+// Offset of element (r, k) of a job's batch, and whether it is inside the operand.
+__device__ __forceinline__ bool elem_at(const DecodeJob &d, int rh, int rl, int k, long long &off)
+{
+    const int x = rl + d.roff;
+    off = (long long)rh * d.s_rhi + (long long)x * d.s_row + (long long)(k / d.kdiv) * d.s_khi +
+          (long long)(k % d.kdiv) * d.s_k;
+    return x >= 0 && x < d.rlim;
+}
+
+// Unit of work: 64 rows x 64 reduction steps of one batch of one job (16
+// elements per thread).  Row-fast sources are read and written along rows
+// (4 rows per thread, 16-byte loads and stores where aligned); the others are
+// read along k and transposed through shared memory.
 __global__ void __launch_bounds__(256) predecode_kernel(const __grid_constant__ DecodeParams p)
 {
     // Sources may be outputs of the previous launch on the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    constexpr int TR = kDecodeTileR, TK = kDecodeTileK, PITCH = TR + 1;   // odd pitch: conflict-free columns
+    constexpr int TR = kDecodeTileR, TK = kDecodeTileK, PITCH = TR + 1;
     __shared__ uint32_t t_off[TK][PITCH];
     __shared__ float t_scl[TK][PITCH];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;    // 32 x 8
+    const int tid = threadIdx.x;
+    const int lane4 = (tid & 15) * 4, grp = tid >> 4;          // 16 groups of 16 threads
     for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x) {
         int j = 0;
         while (j + 1 < p.njobs && t >= p.job[j + 1].tile0) ++j;
         const DecodeJob &d = p.job[j];
-        const long long lt = t - d.tile0;
-        const long long per_b = (long long)d.tiles_r * d.tiles_k;
-        const int b = (int)(lt / per_b);
-        const int rem = (int)(lt - (long long)b * per_b);
+        const int lt = (int)(t - d.tile0);
+        const int per_b = d.tiles_r * d.tiles_k;
+        const int b = lt / per_b;
+        const int rem = lt - b * per_b;
         const int r0 = (rem / d.tiles_k) * TR, k0 = (rem % d.tiles_k) * TK;
         const float *src = d.src + (long long)b * d.bs;
         uint32_t *po = d.plane + (size_t)b * 2 * d.K * d.rows_pad;
         float *ps = reinterpret_cast<float *>(po + (size_t)d.K * d.rows_pad);
         int big = 0;
-        if (d.s_row == 1 && d.rdiv >= d.rows && d.kdiv >= d.K && d.roff == 0) {
-            // row-fast dense source: lanes walk rows in both the read and the write
-            float v[TR / 32][TK / 8];
+        if (d.rowfast) {
+            // rows r .. r + 3 at reduction steps k0 + grp + 16 i
+            const int r = r0 + lane4;
+            if (r < d.rows) {
 #pragma unroll
-            for (int h = 0; h < TR / 32; ++h)
+                for (int i = 0; i < TK / 16; ++i) {
+                    const int k = k0 + grp + 16 * i;
+                    if (k >= d.K) break;
+                    const float *a = src + r + (long long)k * d.s_k;
+                    float v[4];
+                    if (d.vec && r + 4 <= d.rows) {
+                        const float4 q = __ldcs(reinterpret_cast<const float4 *>(a));
+                        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+                    } else {
 #pragma unroll
-                for (int i = 0; i < TK / 8; ++i) {
-                    const int r = r0 + tx + 32 * h, k = k0 + ty + 8 * i;
-                    v[h][i] = (r < d.rows && k < d.K) ? __ldcs(src + r + (long long)k * d.s_k) : 0.0f;
+                        for (int e = 0; e < 4; ++e) v[e] = r + e < d.rows ? __ldcs(a + e) : 0.0f;
+                    }
+                    uint4 o4;
+                    float4 s4;
+                    decode(v[0], p.M, d.offshift, o4.x, s4.x, big);
+                    decode(v[1], p.M, d.offshift, o4.y, s4.y, big);
+                    decode(v[2], p.M, d.offshift, o4.z, s4.z, big);
+                    decode(v[3], p.M, d.offshift, o4.w, s4.w, big);
+                    // rows_pad is a multiple of 4: the pad columns of a partial quad may be written
+                    *reinterpret_cast<uint4 *>(po + (size_t)k * d.rows_pad + r) = o4;
+                    *reinterpret_cast<float4 *>(ps + (size_t)k * d.rows_pad + r) = s4;
                 }
+            }
+        } else {
+            // read steps k0 + lane4 .. + 3 of rows r0 + grp + 16 i, transpose, write rows
+            const int k = k0 + lane4;
+            int rr0 = r0 + grp;
+            int rh = rr0 / d.rdiv, rl = rr0 - rh * d.rdiv;
 #pragma unroll
-            for (int h = 0; h < TR / 32; ++h)
+            for (int i = 0; i < TR / 16; ++i) {
+                const int r = rr0 + 16 * i;
+                float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                bool ok[4] = {false, false, false, false};
+                if (r < d.rows) {
+                    long long off;
+                    const bool in = elem_at(d, rh, rl, k < d.K ? k : 0, off);
+                    if (d.vec && k + 4 <= d.K) {
+                        // k .. k + 3 contiguous and 16-byte aligned
+                        if (in) {
+                            const float4 q = __ldcs(reinterpret_cast<const float4 *>(src + off));
+                            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+                        }
+                        ok[0] = ok[1] = ok[2] = ok[3] = in;
+                    } else {
 #pragma unroll
-                for (int i = 0; i < TK / 8; ++i) {
-                    const int r = r0 + tx + 32 * h, k = k0 + ty + 8 * i;
-                    if (r < d.rows && k < d.K) {
-                        uint32_t o;
-                        float s;
-                        decode(v[h][i], p.M, d.offshift, o, s, big);
-                        po[(size_t)k * d.rows_pad + r] = o;
-                        ps[(size_t)k * d.rows_pad + r] = s;
+                        for (int e = 0; e < 4; ++e) {
+                            if (k + e >= d.K) break;
+                            long long oe;
+                            ok[e] = elem_at(d, rh, rl, k + e, oe);
+                            if (ok[e]) v[e] = __ldcs(src + oe);
+                        }
                     }
                 }
-        } else {
-            // lanes walk k in the read (rows ty, ty + 8, ...), rows in the write
-            const int k = k0 + tx;
-            const bool kok = k < d.K;
-            const long long koff = kok ? (long long)(k / d.kdiv) * d.s_khi + (long long)(k % d.kdiv) * d.s_k : 0;
-            int rh = (r0 + ty) / d.rdiv, rl = (r0 + ty) - rh * d.rdiv;     // (r / rdiv, r % rdiv), stepped by 8
-            float v[TR / 8];
-            bool ok[TR / 8];
 #pragma unroll
-            for (int i = 0; i < TR / 8; ++i) {
-                const int r = r0 + ty + 8 * i;
-                const int x = rl + d.roff;
-                ok[i] = kok && r < d.rows && x >= 0 && x < d.rlim;   // else a zero operand: offset 0, scale +0
-                v[i] = ok[i] ? __ldcs(src + (long long)rh * d.s_rhi + (long long)x * d.s_row + koff) : 0.0f;
-                rl += 8;
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t o = 0;
+                    float sc = 0.0f;                 // outside the operand: offset 0, scale +0
+                    if (ok[e]) decode(v[e], p.M, d.offshift, o, sc, big);
+                    t_off[lane4 + e][grp + 16 * i] = o;
+                    t_scl[lane4 + e][grp + 16 * i] = sc;
+                }
+                rl += 16;
                 while (rl >= d.rdiv) { rl -= d.rdiv; ++rh; }
             }
-#pragma unroll
-            for (int i = 0; i < TR / 8; ++i) {
-                uint32_t o = 0;
-                float s = 0.0f;
-                if (ok[i]) decode(v[i], p.M, d.offshift, o, s, big);
-                t_off[tx][ty + 8 * i] = o;
-                t_scl[tx][ty + 8 * i] = s;
-            }
             __syncthreads();
-            // each thread writes 4 consecutive rows of 2 reduction steps, 16-byte stores
-            const int rq = (threadIdx.x & 15) * 4, r = r0 + rq;
+            // each thread writes rows r0 + lane4 .. + 3 of steps k0 + grp + 16 i
+            const int r = r0 + lane4;
+            if (r < d.rows) {
 #pragma unroll
-            for (int h = 0; h < TK / 16; ++h) {
-                const int kk = (threadIdx.x >> 4) + 16 * h, k2 = k0 + kk;
-                if (k2 >= d.K || r >= d.rows) continue;
-                const uint4 o4 = make_uint4(t_off[kk][rq], t_off[kk][rq + 1], t_off[kk][rq + 2], t_off[kk][rq + 3]);
-                const float4 s4 = make_float4(t_scl[kk][rq], t_scl[kk][rq + 1], t_scl[kk][rq + 2], t_scl[kk][rq + 3]);
-                uint32_t *od = po + (size_t)k2 * d.rows_pad + r;
-                float *sd = ps + (size_t)k2 * d.rows_pad + r;
-                if (r + 4 <= d.rows_pad) {      // rows_pad is a multiple of 4: the pad columns may be written
-                    *reinterpret_cast<uint4 *>(od) = o4;
-                    *reinterpret_cast<float4 *>(sd) = s4;
+                for (int i = 0; i < TK / 16; ++i) {
+                    const int kk = grp + 16 * i, k2 = k0 + kk;
+                    if (k2 >= d.K) break;
+                    const uint4 o4 = make_uint4(t_off[kk][lane4], t_off[kk][lane4 + 1], t_off[kk][lane4 + 2],
+                                                t_off[kk][lane4 + 3]);
+                    const float4 s4 = make_float4(t_scl[kk][lane4], t_scl[kk][lane4 + 1], t_scl[kk][lane4 + 2],
+                                                  t_scl[kk][lane4 + 3]);
+                    *reinterpret_cast<uint4 *>(po + (size_t)k2 * d.rows_pad + r) = o4;
+                    *reinterpret_cast<float4 *>(ps + (size_t)k2 * d.rows_pad + r) = s4;
                 }
             }
             __syncthreads();
         }
         // every thread of the warp takes part; one store per warp that saw a large element
-        if (__any_sync(0xFFFFFFFFu, big) && tx == 0) *d.flag = p.epoch;
+        if (__any_sync(0xFFFFFFFFu, big) && (tid & 31) == 0) *d.flag = p.epoch;
     }
 }
 
@@ -111,8 +146,21 @@ __global__ void __launch_bounds__(256) predecode_kernel(const __grid_constant__ 
 int launch_predecode(const DecodeParams &p, int sms, cudaStream_t st)
 {
     if (p.tiles <= 0) return AMSIM_OK;
+    // The GEMM launches around this one run with the largest shared-memory
+    // carve-out; asking for the same one spares the SMs a reconfiguration
+    // between the launches.
+    static bool carveout_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && !carveout_set[dev]) {
+        cudaFuncSetAttribute(predecode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        cudaGetLastError();
+        carveout_set[dev] = true;
+    }
+    // one resident wave (four blocks per SM), so that every block has started,
+    // and the dependent GEMM is launched, while the first blocks still run
     long long blocks = p.tiles;
-    const long long cap = (long long)sms * 8;
+    const long long cap = (long long)sms * 4;
     if (blocks > cap) blocks = cap;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);

@@ -242,6 +242,18 @@ size_t conv_plane_bytes(const ConvTma &cv)
     return b;
 }
 
+// Access-pattern flags of a decode job (see DecodeJob).
+void classify_job(kern::DecodeJob &d)
+{
+    const bool aligned = (reinterpret_cast<uintptr_t>(d.src) & 15) == 0 && (d.batch <= 1 || d.bs % 4 == 0);
+    d.rowfast = d.s_row == 1 && d.rdiv >= d.rows && d.rlim >= d.rows && d.roff == 0 && d.kdiv >= d.K;
+    if (d.rowfast)
+        d.vec = aligned && (d.s_k % 4 == 0 || d.K == 1);
+    else
+        d.vec = aligned && d.s_k == 1 && (d.kdiv >= d.K || d.kdiv % 4 == 0) && d.s_row % 4 == 0 &&
+                d.s_rhi % 4 == 0 && d.s_khi % 4 == 0;
+}
+
 void fill_job(kern::DecodeJob &d, const TmaPlaneJob &j, int offshift, void *plane, unsigned long long *flag,
               long long &tiles)
 {
@@ -266,6 +278,7 @@ void fill_job(kern::DecodeJob &d, const TmaPlaneJob &j, int offshift, void *plan
     d.tiles_k = ceil_div(j.K, kern::kDecodeTileK);
     d.tile0 = tiles;
     tiles += (long long)j.batch * d.tiles_r * d.tiles_k;
+    classify_job(d);
 }
 
 int launch_tma(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
@@ -468,6 +481,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             d.tiles_k = ceil_div(k.K, kern::kDecodeTileK);
             d.tile0 = dtiles;
             dtiles += (long long)k.nb * d.tiles_r * d.tiles_k;
+            classify_job(d);
         }
         dp.njobs = ps.n;
         dp.tiles = dtiles;

@@ -23,7 +23,7 @@ namespace kern {
 
 constexpr int kMaxDecodeJobs = 20;
 constexpr int kDecodeTileR = 64;                 // rows per tile
-constexpr int kDecodeTileK = 32;                 // reduction steps per tile
+constexpr int kDecodeTileK = 64;                 // reduction steps per tile
 
 struct DecodeJob {
     const float *src;
@@ -35,7 +35,11 @@ struct DecodeJob {
     int offshift;                                // offset = top-M fraction bits << offshift
     uint32_t *plane;                             // [batch][2][K][rows_pad]
     unsigned long long *flag;
-    int tiles_r, tiles_k;                        // 64 x 32 tiles per batch
+    int tiles_r, tiles_k;                        // 64 x 64 tiles per batch
+    // row-fast: a dense operand with unit row stride (read and written along
+    // rows); vec: 16-byte loads of 4 consecutive rows (row-fast) or steps
+    // (otherwise) start aligned wherever they lie inside the operand
+    int rowfast, vec;
     long long tile0;                             // first tile of this job in the launch
 };
 

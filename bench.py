@@ -53,7 +53,7 @@ def env_int(name, default):
 
 
 # ---------------------------------------------------------------- workloads
-def make_step(name, lut_for):
+def make_step(name, lut_for, M=7):
     from approximate_multiplier_dnn_gb300 import steps
     from approximate_multiplier_dnn_gb300 import workloads as wl
     if name == "mlp":
@@ -65,7 +65,8 @@ def make_step(name, lut_for):
         return (steps.ConvStep(wl.conv3x3(), wl.CONV3X3, lut_for("exact", 7)),
                 "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_exact_M7")
     if name == "gemm4096":
-        return steps.SquareGemmStep(wl.square_gemm(4096), lut_for("mitchell", 7)), "gemm_4096^3_mitchell_M7"
+        # the mantissa-width sweep runs this workload at M = 4 .. 11
+        return steps.SquareGemmStep(wl.square_gemm(4096), lut_for("mitchell", M)), f"gemm_4096^3_mitchell_M{M}"
     if name == "attention":
         return steps.AttentionStep(wl.attention(), lut_for("mitchell", 7)), "attention_32x16x512x64_mitchell_M7"
     if name == "conv1x1":
@@ -196,16 +197,33 @@ def gpu_id_for_smi(torch):
     return torch.cuda.current_device()
 
 
+def lut_residency(lut):
+    """Where the LUT-GEMM keeps the table: shared memory up to 160 KB of
+    narrowed entries, else global memory read through L2 (then the lookup
+    roofline above is an upper bound, not the bound)."""
+    info = lut.info()
+    nbytes = (1 << (2 * info["M"])) * info["width_bits"] // 8
+    return "shared" if nbytes <= 160 * 1024 else "global (L2 gather)"
+
+
 # ---------------------------------------------------------------- traffic record
+# sources of the LUT-GEMM kernels; a traffic record holds for one version of them
+KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_ws.cuh", "gemm_tma.cuh", "decode.cu")
+
+
+def kernel_sha():
+    csrc = os.path.join(ROOT, "approximate_multiplier_dnn_gb300", "csrc")
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
 def recorded_traffic(workload):
     """Per-launch DRAM bytes of the LUT-GEMM kernel from a committed ncu
     summary, if it was taken on the current kernel source; else None."""
-    csrc = os.path.join(ROOT, "approximate_multiplier_dnn_gb300", "csrc")
     try:
-        h = hashlib.sha1()
-        for f in ("gemm_kernel.cuh", "gemm_ws.cuh"):
-            h.update(open(os.path.join(csrc, f), "rb").read())
-        sha = h.hexdigest()[:12]
+        sha = kernel_sha()
         with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             for line in f:
                 kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
@@ -258,7 +276,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mantissa", type=int, default=7, help="LUT mantissa bits M (gemm4096 only: the M sweep)")
     args = ap.parse_args()
+    if args.mantissa != 7 and args.workload != "gemm4096":
+        ap.error("--mantissa applies to --workload gemm4096 only")
+    if not 1 <= args.mantissa <= 11:
+        ap.error("--mantissa must be in 1..11")
     args.warmup = max(args.warmup, 3)
 
     rank, world = env_int("RANK", 0), env_int("WORLD_SIZE", 1)
@@ -284,7 +307,7 @@ def main():
             luts[(kind, M)] = am.Lut.build(kind, M)
         return luts[(kind, M)]
 
-    step, wname = make_step(args.workload, lut_for)
+    step, wname = make_step(args.workload, lut_for, args.mantissa)
     stream = torch.cuda.current_stream()
     parts = step.parts()
     props = torch.cuda.get_device_properties(local)
@@ -367,8 +390,11 @@ def main():
     traffic = recorded_traffic(wname)
     roofline = {"bound": "alu", "pipe": "shared-memory LUT lookups: SMs x 32 per clock x SM clock",
                 "achieved": achieved, "peak": peak, "unit": "Glookup/s", "frac": achieved / peak,
-                "traffic": traffic, "kernel": "lutgemm_ws_kernel (stream-K cut tiles finished in-kernel)",
-                "launches_per_step": launches_lut, "lut_share_of_step": round(lut_share, 4), "sms": sms,
+                "traffic": traffic,
+                "kernel": "LUT-GEMM calls: predecode + lutgemm_tma_kernel (lutgemm_ws_kernel for gathers)",
+                "calls_per_step": launches_lut, "kernel_launches_per_step": launches_timed / K,
+                "lut_residency": lut_residency(step.lut),
+                "lut_share_of_step": round(lut_share, 4), "sms": sms,
                 "sm_mhz": mhz}
     if args.workload == "mul":
         # HBM-bound: 12 bytes per product (two operands in, one result out)

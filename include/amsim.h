@@ -164,7 +164,15 @@ int amsim_gemm_strided_batched(char transA, char transB, int m, int n, int k, fl
                                amsim_lut_t lut, void *ws, size_t ws_bytes,
                                amsim_stream_t stream);
 
-/* Bytes of scratch with which the GEMM calls above run their fastest plan. */
+/*
+ * Bytes of scratch with which the GEMM calls above run their fastest plan:
+ * the split-K (stream-K) partial sums, when the problem needs them, plus the
+ * operands decoded once into LUT-offset and scale planes (8 bytes per operand
+ * element, per batch unless the batch stride is 0).  Less scratch selects a
+ * plan that decodes operands inside the GEMM; none selects one without
+ * split-K.  All plans give results within the contraction tolerance; a
+ * given scratch size always gives the same plan.
+ */
 size_t amsim_gemm_workspace_size(char transA, char transB, int m, int n, int k, int batch,
                                  amsim_lut_t lut);
 
@@ -267,7 +275,13 @@ int amsim_conv2d_bwd_data(const amsim_conv_desc *desc, const float *dy, const fl
 int amsim_conv2d_bwd_filter(const amsim_conv_desc *desc, const float *x, const float *dy, float *dw,
                             amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);
 
-/* which: 0 forward, 1 bwd_data, 2 bwd_filter. Bytes of scratch for the fastest plan. */
+/*
+ * which: 0 forward, 1 bwd_data, 2 bwd_filter.  Bytes of scratch for the
+ * fastest plan: split-K partial sums plus, for unit strides, the operands
+ * decoded into LUT-offset and scale planes laid out for tensor copies (for the
+ * forward and data-gradient passes one copy of the activation per filter
+ * column).  Less scratch selects the gathering kernel.
+ */
 size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim_lut_t lut);
 
 /* ------------------------------------------------------------------ glue */
