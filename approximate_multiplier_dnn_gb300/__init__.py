@@ -83,6 +83,7 @@ def lib():
     sig = {
         "amsim_status_string": ([i32], ctypes.c_char_p),
         "amsim_kernel_launches": ([], ctypes.c_ulonglong),
+        "amsim_last_path": ([], i32),
         "amsim_lut_generate": ([i32, i32, vp], i32),
         "amsim_lut_generate_from_fn": ([APPROX_MUL_FN, i32, vp], i32),
         "amsim_lut_build": ([i32, i32, ctypes.POINTER(vp)], i32),
@@ -120,6 +121,19 @@ def header_functions() -> list[str]:
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"\b(amsim_[a-z0-9_]+)\s*\(", text)
     return sorted(set(names))
+
+
+AMSIM_PATH_PLANES = 1
+AMSIM_PATH_INKERNEL_DECODE = 4
+AMSIM_PATH_SINGLE_ROLE = 8
+AMSIM_PATH_STREAMK = 16
+AMSIM_PATH_FIXUP = 32
+AMSIM_PATH_CONV_BOXES = 64
+
+
+def amsim_last_path() -> int:
+    """Kernel-path bits (AMSIM_PATH_*) of this thread's most recent GEMM or convolution call."""
+    return int(lib().amsim_last_path())
 
 
 def amsim_kernel_launches() -> int:

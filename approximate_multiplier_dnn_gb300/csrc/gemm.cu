@@ -20,6 +20,9 @@ using kern::BU;
 
 constexpr int kMaxSmemLut = 160 * 1024;   // LUTs up to this size are staged in shared memory
 
+// Paths taken by the calling thread's current (or last) GEMM / conv call.
+thread_local int g_last_path = 0;
+
 // Stream-K flag values: every launch gets a fresh one, so flags left in
 // scratch by earlier launches never match.
 std::atomic<unsigned long long> g_epoch{0x5EED0001ULL};
@@ -117,7 +120,8 @@ EncodeTiled encode_tiled()
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-constexpr size_t kFlagBlock = 256;   // kMaxDecodeJobs flags of 8 bytes
+constexpr size_t kFlagBlock = 256;   // kMaxDecodeJobs plane flags of 8 bytes
+static_assert(kern::kMaxDecodeJobs * 8 <= (int)kFlagBlock, "plane flags fit the block");
 
 struct PlaneKey {
     const float *src;
@@ -291,6 +295,27 @@ int launch_tma(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bo
     }
 }
 
+// The predecode pass, then the TMA LUT-GEMM over its planes: stream-K plans
+// launch cooperatively and finish cut tiles inside the kernel, else (or
+// without a cooperative launch) the separate fixup kernel does.
+int run_tma(int width, kern::KParams &tp, const kern::TmaMaps &maps, const kern::DecodeParams &dp, bool gl,
+            long long blocks, size_t smem, int sms, bool streamk, cudaStream_t stream)
+{
+    const dim3 grid((unsigned)blocks);
+    int rc = kern::launch_predecode(dp, sms, stream);
+    if (rc) return rc;
+    const int base = AMSIM_PATH_PLANES | (streamk ? AMSIM_PATH_STREAMK : 0) | (tp.conv ? AMSIM_PATH_CONV_BOXES : 0);
+    tp.fused = streamk ? 1 : 0;
+    rc = launch_tma(width, tp, maps, gl, grid, smem, stream);
+    if (rc == kern::AMSIM_ENOTCOOP) {
+        tp.fused = 0;
+        rc = launch_tma(width, tp, maps, gl, grid, smem, stream);
+    }
+    if (rc) return rc;
+    g_last_path |= base | (streamk && !tp.fused ? AMSIM_PATH_FIXUP : 0);
+    return streamk && !tp.fused ? kern::launch_fixup(tp, tp.ctas - 1, stream) : AMSIM_OK;
+}
+
 // Scratch the predecoded path adds after `base` bytes of stream-K scratch.
 size_t tma_extra(size_t base, const PlaneSet &ps) { return align256(base) - base + kFlagBlock + ps.bytes; }
 
@@ -431,17 +456,9 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             tp.cv_rows = cv.rows;
             tp.table_bytes = tma_gl ? 0 : (int)lut->narrow_bytes;
             tp.stages = tma_stages(tma_lutb);
-            tp.fused = pl.streamk ? 1 : 0;
             tp.epoch = epoch;
             const size_t smem = (size_t)kern::tma_smem_bytes((int)tma_lutb, tp.stages);
-            int rc = kern::launch_predecode(dp, sms, stream);
-            if (rc) return rc;
-            rc = launch_tma(lut->width_bits, tp, maps, tma_gl, dim3((unsigned)blocks), smem, stream);
-            if (rc == kern::AMSIM_ENOTCOOP) {
-                tp.fused = 0;
-                rc = launch_tma(lut->width_bits, tp, maps, tma_gl, dim3((unsigned)blocks), smem, stream);
-            }
-            if (rc == AMSIM_OK) return tp.fused || !pl.streamk ? AMSIM_OK : kern::launch_fixup(tp, pl.ctas - 1, stream);
+            const int rc = run_tma(lut->width_bits, tp, maps, dp, tma_gl, blocks, smem, sms, pl.streamk, stream);
             if (rc != AMSIM_EUNSUPPORTED) return rc;
         }
     }
@@ -502,17 +519,9 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             kern::KParams tp = kp;
             tp.table_bytes = tma_gl ? 0 : (int)lut->narrow_bytes;
             tp.stages = tma_stages(tma_lutb);
-            tp.fused = pl.streamk ? 1 : 0;
             tp.epoch = epoch;
             const size_t smem = (size_t)kern::tma_smem_bytes((int)tma_lutb, tp.stages);
-            int rc = kern::launch_predecode(dp, sms, stream);
-            if (rc) return rc;
-            rc = launch_tma(lut->width_bits, tp, maps, tma_gl, dim3((unsigned)blocks), smem, stream);
-            if (rc == kern::AMSIM_ENOTCOOP) {
-                tp.fused = 0;
-                rc = launch_tma(lut->width_bits, tp, maps, tma_gl, dim3((unsigned)blocks), smem, stream);
-            }
-            if (rc == AMSIM_OK) return tp.fused || !pl.streamk ? AMSIM_OK : kern::launch_fixup(tp, pl.ctas - 1, stream);
+            const int rc = run_tma(lut->width_bits, tp, maps, dp, tma_gl, blocks, smem, sms, pl.streamk, stream);
             if (rc != AMSIM_EUNSUPPORTED) return rc;
         }
     }
@@ -521,6 +530,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     // warp-specialised kernel next; the single-role kernel if its register
     // split cannot be honoured on this device
     int rc = AMSIM_EUNSUPPORTED;
+    const int sk = pl.streamk ? AMSIM_PATH_STREAMK : 0;
     if (use_ws) {
         // stream-K: finish cut tiles inside the kernel when a cooperative
         // launch is possible, else run the separate fixup kernel afterwards
@@ -531,13 +541,16 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             kp.fused = 0;
             rc = launch_ws(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kWsFixedSmem + lutb, stream);
         }
+        if (rc == AMSIM_OK) g_last_path |= AMSIM_PATH_INKERNEL_DECODE | sk;
         if (rc == AMSIM_OK && kp.fused) return AMSIM_OK;
     }
     if (rc == AMSIM_EUNSUPPORTED) {
         kp.fused = 0;
         rc = launch_w(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kFixedSmem + lutb, stream);
+        if (rc == AMSIM_OK) g_last_path |= AMSIM_PATH_SINGLE_ROLE | sk;
     }
     if (rc || !pl.streamk) return rc;
+    g_last_path |= AMSIM_PATH_FIXUP;
     return kern::launch_fixup(kp, pl.ctas - 1, stream);
 }
 
@@ -545,6 +558,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
 
 int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
+    g_last_path = 0;
     if (n <= 0) return AMSIM_OK;
     if (n > kern::kMaxProblems) return AMSIM_EINVAL;
     if (lut->symmetric) return run_same_table(p, n, lut, ws, ws_bytes, stream);
@@ -657,6 +671,8 @@ size_t gemm_workspace(char transA, char transB, int m, int n, int k, int batch, 
 }  // namespace amsim
 
 extern "C" {
+
+int amsim_last_path(void) { return amsim::g_last_path; }
 
 int amsim_gemm_strided_batched(char transA, char transB, int m, int n, int k, float alpha, const float *A, int lda,
                                int64_t strideA, const float *B, int ldb, int64_t strideB, float beta, float *C,

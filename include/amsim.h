@@ -73,6 +73,18 @@ const char *amsim_status_string(int status);
  * devices, all calls); a diagnostic for counting launches around a region. */
 unsigned long long amsim_kernel_launches(void);
 
+/* Kernel paths of the calling host thread's most recent GEMM or convolution
+ * call (a diagnostic; 0 before any, or when the call enqueued nothing): */
+enum amsim_path {
+    AMSIM_PATH_PLANES = 1,          /* operands decoded once into planes, copied by TMA */
+    AMSIM_PATH_INKERNEL_DECODE = 4, /* operands decoded inside the warp-specialised GEMM */
+    AMSIM_PATH_SINGLE_ROLE = 8,     /* the single-role fallback kernel */
+    AMSIM_PATH_STREAMK = 16,        /* reduction split across CTAs (stream-K) */
+    AMSIM_PATH_FIXUP = 32,          /* cut tiles finished by the separate fixup kernel */
+    AMSIM_PATH_CONV_BOXES = 64      /* convolution operands as shifted or blocked tensor boxes */
+};
+int amsim_last_path(void);
+
 /* ------------------------------------------------------------------ LUTs */
 
 /*

@@ -98,8 +98,8 @@ def test_conv_errors(amd, luts):
 
 def test_tma_layout_is_used_when_scratch_allows(amd, luts):
     """A unit-stride geometry asks for plane scratch on every pass and, given
-    it, runs the predecode pass and the GEMM (two launches); without scratch
-    the gathering kernel runs alone."""
+    it, takes the tensor-box layouts (a predecode launch, then the GEMM);
+    without scratch the gathering kernel runs alone."""
     import torch
     N, H, W, C, K, R, S = 1, 32, 32, 64, 32, 3, 3
     desc = amd.ConvDesc.make(N, H, W, C, K, R, S, (1, 1), (1, 1), (1, 1))
@@ -114,10 +114,17 @@ def test_tma_layout_is_used_when_scratch_allows(amd, luts):
     for which in range(3):
         nb = amd.amsim_conv2d_workspace_size(desc, which, lut)
         assert nb >= 2 * 4 * N * H * W * min(C, K), f"pass {which}: no plane scratch requested"
-        for scratch, launches in ((True, 2), (False, 1)):
+        for scratch in (True, False):
             ws = amd.workspace(nb) if scratch else None
             torch.cuda.synchronize()
             n0 = amd.amsim_kernel_launches()
             fns[which](desc, *args[which], outs[which], lut, ws=ws)
             torch.cuda.synchronize()
-            assert amd.amsim_kernel_launches() - n0 == launches, (which, scratch)
+            path, launches = amd.amsim_last_path(), amd.amsim_kernel_launches() - n0
+            if scratch:
+                assert path & amd.AMSIM_PATH_PLANES and path & amd.AMSIM_PATH_CONV_BOXES, (which, path)
+                # the predecode pass and the GEMM (and the fixup kernel without a cooperative launch)
+                assert launches == (3 if path & amd.AMSIM_PATH_FIXUP else 2), (which, path, launches)
+            else:
+                assert path & amd.AMSIM_PATH_INKERNEL_DECODE and not path & amd.AMSIM_PATH_PLANES, (which, path)
+                assert launches == 1, (which, launches)

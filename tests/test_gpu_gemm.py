@@ -262,6 +262,14 @@ def test_each_kernel_path(amd, orc, luts, shape, path):
     A, B = rnd(rng, (m, k)), rnd(rng, (n, k))
     lut = luts("mitchell", 7)
     got = gpu_gemm(amd, lut, A, B, False, True, ws=_path_ws(amd, lut, path, "N", "T", m, n, k))
+    taken = amd.amsim_last_path()
+    if path == "planes":
+        assert taken & amd.AMSIM_PATH_PLANES, taken
+    else:
+        assert not taken & amd.AMSIM_PATH_PLANES, taken
+        assert taken & (amd.AMSIM_PATH_INKERNEL_DECODE | amd.AMSIM_PATH_SINGLE_ROLE), taken
+    if path == "none":
+        assert not taken & amd.AMSIM_PATH_STREAMK, taken
     check(orc, "mitchell", 7, A, B, False, True, got, what=f"{shape} path={path}")
 
 
