@@ -21,7 +21,6 @@
 #include <cuda.h>
 
 #include "gemm_ws.cuh"
-#include "predecode.h"
 
 namespace amsim {
 namespace kern {
@@ -273,7 +272,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // Planes, flags, outputs and scratch belong to earlier launches on the
     // stream: wait for them to complete before any of them is touched.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-
 
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
     if (tid >= kTmaConsumerThreads) {
