@@ -69,11 +69,14 @@ Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail)
     pl.ctas = (int)std::min<long long>(std::min(sms, kern::kMaxFixupParts), pl.iters);
     // two partial-sum slots and two flags per CTA
     pl.sk_bytes = (size_t)2 * pl.ctas * BU * BL * sizeof(float) + (size_t)2 * pl.ctas * sizeof(unsigned long long);
-    // Data parallel (one CTA per tile) when the tiles fill the SMs in nearly
-    // whole waves; otherwise stream-K over (tile, stage) iterations.
+    // Stream-K over (tile, stage) iterations with one persistent CTA per SM,
+    // unless the tiles fit in one wave that fills the SMs nearly whole (then
+    // one CTA per tile).  Persistent CTAs stage the LUT once and keep the
+    // copy ring full across tile boundaries, so a tile's epilogue overlaps the
+    // next tile's first copies.
     const long long waves = (pl.total_tiles + sms - 1) / std::max(1, sms);
     const double dp_eff = pl.total_tiles > 0 ? (double)pl.total_tiles / (double)(waves * sms) : 1.0;
-    pl.streamk = pl.ctas > 1 && dp_eff < 0.9 && pl.sk_bytes <= ws_avail;
+    pl.streamk = pl.ctas > 1 && (dp_eff < 0.9 || waves > 1) && pl.sk_bytes <= ws_avail;
     pl.ws_bytes = pl.streamk ? pl.sk_bytes : 0;
     return pl;
 }
