@@ -129,6 +129,7 @@ AMSIM_PATH_SINGLE_ROLE = 8
 AMSIM_PATH_STREAMK = 16
 AMSIM_PATH_FIXUP = 32
 AMSIM_PATH_CONV_BOXES = 64
+AMSIM_PATH_RAW_TILES = 128
 
 
 def amsim_last_path() -> int:

@@ -7,7 +7,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "gemm_tma.cuh"
+#include "gemm_raw.cuh"
 #include "predecode.h"
 
 namespace amsim {
@@ -188,13 +188,18 @@ bool plan_planes(const Problem *p, int n, const Plan &pl, int M, int wlog, Plane
 // read by a single tile row (attention's P in O = P V) is decoded as cheaply
 // inside the GEMM.  Measured on GB300: 0.03 plane bytes per MAC gains, 0.13
 // loses.  Below 64 MB of planes the pass costs microseconds either way.
-bool planes_pay(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
+double planes_bytes_per_mac(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
 {
-    if (ps.bytes <= ((size_t)64 << 20)) return true;
     double macs = 0.0;
     for (int i = 0; i < n; ++i)
         if (pl.tiles[i] > 0) macs += (double)p[i].U.rows * p[i].L.rows * (double)p[i].K * p[i].batch;
-    return (double)ps.bytes <= 0.05 * macs;
+    return macs > 0.0 ? (double)ps.bytes / macs : 1e30;
+}
+
+bool planes_pay(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
+{
+    if (ps.bytes <= ((size_t)64 << 20)) return true;
+    return planes_bytes_per_mac(p, n, pl, ps) <= 0.05;
 }
 
 // Ring depth of the TMA kernel beside a LUT region of lut_bytes (0 if none fits).
@@ -319,6 +324,67 @@ int run_tma(int width, kern::KParams &tp, const kern::TmaMaps &maps, const kern:
     return streamk && !tp.fused ? kern::launch_fixup(tp, tp.ctas - 1, stream) : AMSIM_OK;
 }
 
+// ------------------------------------------------------------------ raw tiles
+// A dense operand the copy engine reads in place: unit stride along rows or
+// along k, the other strides multiples of 4 elements, and (when checked) a
+// 16-byte aligned base.
+bool raw_ok(const OperandDesc &d, int K, int batch, bool check_ptr)
+{
+    if (d.gather || d.rows <= 0 || K <= 0) return false;
+    const bool rowfast = d.s_row == 1;
+    if (!rowfast && d.s_k != 1) return false;
+    const long long outer = rowfast ? d.s_k : d.s_row;
+    if (outer <= 0 || outer % 4) return false;
+    if (batch > 1 && d.batch_stride != 0 && d.batch_stride % 4) return false;
+    if (check_ptr && (reinterpret_cast<uintptr_t>(d.ptr) & 15)) return false;
+    return true;
+}
+
+bool all_raw_ok(const Problem *p, int n, const Plan &pl, bool check_ptr)
+{
+    for (int i = 0; i < n; ++i) {
+        if (pl.tiles[i] == 0) continue;
+        if (p[i].tma || !raw_ok(p[i].U, p[i].K, p[i].batch, check_ptr) ||
+            !raw_ok(p[i].L, p[i].K, p[i].batch, check_ptr))
+            return false;
+    }
+    return true;
+}
+
+// 3-D map (rows or k innermost, then the other, then batch) over a raw operand.
+int encode_raw_map(CUtensorMap *map, const OperandDesc &d, int K, int batch, int box_rows)
+{
+    EncodeTiled enc = encode_tiled();
+    if (!enc) return AMSIM_EUNSUPPORTED;
+    const bool rowfast = d.s_row == 1;
+    const cuuint64_t outer = (cuuint64_t)(rowfast ? d.s_k : d.s_row);
+    const cuuint64_t nb = (d.batch_stride == 0 || batch <= 1) ? 1 : (cuuint64_t)batch;
+    const cuuint64_t inner_dim = rowfast ? (cuuint64_t)d.rows : (cuuint64_t)K;
+    const cuuint64_t outer_dim = rowfast ? (cuuint64_t)K : (cuuint64_t)d.rows;
+    const cuuint64_t dims[3] = {inner_dim, outer_dim, nb};
+    // one batch only: any 16-byte multiple covering the operand serves as its stride
+    const cuuint64_t bstride = nb > 1 ? (cuuint64_t)d.batch_stride * 4 : ((outer * outer_dim * 4 + 15) & ~15ULL);
+    const cuuint64_t strides[2] = {outer * 4, bstride};
+    const cuuint32_t box[3] = {rowfast ? (cuuint32_t)box_rows : (cuuint32_t)kern::BK,
+                               rowfast ? (cuuint32_t)kern::BK : (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(d.ptr), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           rowfast ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
+}
+
+int launch_raw(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
+               cudaStream_t st)
+{
+    switch (width) {
+    case 8: return kern::launch_raw_w8(kp, maps, gl, grid, smem, st);
+    case 16: return kern::launch_raw_w16(kp, maps, gl, grid, smem, st);
+    default: return kern::launch_raw_w32(kp, maps, gl, grid, smem, st);
+    }
+}
+
 // Scratch the predecoded path adds after `base` bytes of stream-K scratch.
 size_t tma_extra(size_t base, const PlaneSet &ps) { return align256(base) - base + kFlagBlock + ps.bytes; }
 
@@ -331,7 +397,12 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     const int sms = device_sms(dev);
     Plan pl = make_plan(p, n, sms, (size_t)-1);
     size_t need = pl.ws_bytes;
-    if (lut && encode_tiled() && n == 1 && p[0].tma) {
+    PlaneSet rps;
+    const int rwlog = lut ? (lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2) : 0;
+    if (lut && encode_tiled() && all_raw_ok(p, n, pl, false) &&
+        !(plan_planes(p, n, pl, lut->M, rwlog, &rps) && rps.n > 0 && planes_bytes_per_mac(p, n, pl, rps) < 0.01)) {
+        // operand tiles are copied in place and decoded inside the GEMM
+    } else if (lut && encode_tiled() && n == 1 && p[0].tma) {
         need += align256(pl.ws_bytes) - pl.ws_bytes + kFlagBlock + conv_plane_bytes(*p[0].tma);
     } else if (lut && encode_tiled()) {
         const int wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
@@ -408,10 +479,54 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     const long long blocks = pl.streamk ? pl.ctas : pl.total_tiles;
     if (blocks > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
 
+    // Raw operand tiles copied in place by TMA and decoded in shared memory,
+    // when every operand is dense with copy-engine strides -- unless planes
+    // fit the scratch and are reused so much that decoding each element once
+    // is cheaper than once per tile (measured on GB300: the 4096^3 GEMM, at
+    // 0.004 plane bytes per MAC, runs 5 % faster on planes; attention scores,
+    // at 0.03, 1 % slower; attention's P V 11 % slower).
+    PlaneSet ps;
+    const bool planes_fit = ws && encode_tiled() && plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 &&
+                            ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps);
+    if (encode_tiled() && all_raw_ok(p, n, pl, true) && !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01)) {
+        bool raw_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
+        if (!raw_gl && kern::raw_smem_bytes((int)lut->narrow_bytes) > kMaxSmemPerCta) raw_gl = true;
+        kern::TmaMaps maps;
+        int erc = AMSIM_OK;
+        for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
+            if (pl.tiles[i] == 0) continue;
+            erc = encode_raw_map(&maps.u[qi], p[i].U, p[i].K, p[i].batch, BU);
+            if (erc == AMSIM_OK) erc = encode_raw_map(&maps.l[qi], p[i].L, p[i].K, p[i].batch, BL);
+            kern::ProbParams &q = kp.pr[qi++];
+            q.u_kfast = p[i].U.s_row != 1;
+            q.l_kfast = p[i].L.s_row != 1;
+            q.u_bsel = (p[i].U.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
+            q.l_bsel = (p[i].L.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
+        }
+        if (erc == AMSIM_OK) {
+            kern::KParams tp = kp;
+            tp.table_bytes = raw_gl ? 0 : (int)lut->narrow_bytes;
+            tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
+            tp.fused = pl.streamk ? 1 : 0;
+            const size_t smem = (size_t)kern::raw_smem_bytes(tp.table_bytes);
+            const dim3 grid((unsigned)blocks);
+            int rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
+            if (rc == kern::AMSIM_ENOTCOOP) {
+                tp.fused = 0;
+                rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
+            }
+            if (rc == AMSIM_OK) {
+                const bool fix = pl.streamk && !tp.fused;
+                g_last_path |= AMSIM_PATH_RAW_TILES | (pl.streamk ? AMSIM_PATH_STREAMK : 0) | (fix ? AMSIM_PATH_FIXUP : 0);
+                return fix ? kern::launch_fixup(tp, pl.ctas - 1, stream) : AMSIM_OK;
+            }
+            if (rc != AMSIM_EUNSUPPORTED) return rc;
+        }
+    }
+
     // Predecoded operands copied by TMA, when every operand is dense (or a
     // convolution laid out for TMA) and the scratch holds the planes after the
     // stream-K region.
-    PlaneSet ps;
     bool tma_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
     if (!tma_gl && tma_stages(kern::lut_region_bytes((int)lut->narrow_bytes)) == 0) tma_gl = true;
     const size_t tma_lutb = tma_gl ? 0 : kern::lut_region_bytes((int)lut->narrow_bytes);

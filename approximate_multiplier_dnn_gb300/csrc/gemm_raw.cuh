@@ -1,0 +1,321 @@
+// LUT-GEMM fed with raw operand tiles by the Tensor Memory Accelerator and
+// decoded in shared memory (ApproxTrain Sec. V-B Algorithm 2 per product,
+// Sec. VI-D GEMM kernel).
+//
+// One producer thread copies each stage's fp32 tiles -- BU (or BL) rows x BK
+// reduction steps of each operand, straight from the caller's tensors -- as
+// tensor boxes into a raw ring.  The producer warpgroup (128 threads) then
+// decodes a landed stage into (LUT byte offset, scale) [k][row] arrays, which
+// the eight consumer warps use exactly as in the predecoded kernel.  Operands
+// stored k-fast arrive [row][k] with the copy engine's 64-byte swizzle, so the
+// decoders' transposing reads are free of bank conflicts.  No operand planes
+// and no separate decode launch are needed; each CTA decodes its own tiles.
+//
+// Barriers: raw_full (copy bytes), raw_empty (decoders done with a raw slot),
+// full (decoded stage ready), empty (consumers done).  Every wait is bounded
+// by the global timer; copies still in flight at an abort are waited for.
+#pragma once
+
+#include "gemm_tma.cuh"
+
+namespace amsim {
+namespace kern {
+
+constexpr int kRawDecoders = 128;                       // the producer warpgroup
+constexpr int kRawThreads = kTmaConsumerThreads + kRawDecoders;
+static_assert(kRawThreads == kTmaThreads, "same block shape as the predecoded kernel");
+constexpr int kRawUBytes = BU * BK * 4;                 // raw fp32 tile of U
+constexpr int kRawLBytes = BL * BK * 4;
+constexpr int kRawStageBytes = kRawUBytes + kRawLBytes; // 20 KB
+constexpr int kRawRing = 3;                             // raw stages
+constexpr int kRawDec = 3;                              // decoded stages
+constexpr int kRawBarBytes = 256;                       // barriers and big-operand flags
+static_assert(kRawUBytes % 1024 == 0 && kRawLBytes % 1024 == 0, "swizzled boxes start 1024-byte aligned");
+static_assert((2 * kRawRing + 2 * kRawDec) * 8 + kRawDec * (kRawDecoders / 32) * 4 <= kRawBarBytes, "barrier block");
+static_assert(kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes >= (BU * BL + 1024 * 4) * 4,
+              "the rings hold the stream-K reduction buffer");
+
+__host__ __device__ constexpr int raw_lut_region(int lut_bytes) { return (lut_bytes + 1023) & ~1023; }
+
+// Shared memory of the raw-tile kernel beside a LUT of lut_bytes (1 KB for alignment).
+__host__ __device__ constexpr int raw_smem_bytes(int lut_bytes)
+{
+    return 1024 + raw_lut_region(lut_bytes) + kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes + kRawBarBytes;
+}
+
+// Box (x, y, z) of a 3-D tensor map into shared memory; completes on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Decode a raw R-row tile into off/scl [BK][R].  k-fast tiles are [R][BK]
+// fp32 rows of 64 bytes whose 16-byte chunks the copy engine swizzled as
+// chunk ^ ((row >> 1) & 3); row-fast tiles are [BK][R].
+template <int R>
+__device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint32_t *off, float *scl, int M,
+                                           int offshift, int d, int &big)
+{
+    if (kfast) {
+#pragma unroll 2
+        for (int task = d; task < R * (BK / 4); task += kRawDecoders) {
+            const int r = task % R, c = task / R;
+            const float4 v = *reinterpret_cast<const float4 *>(raw + r * (BK * 4) + ((c ^ ((r >> 1) & 3)) << 4));
+            const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t o;
+                float s;
+                decode(e[i], M, offshift, o, s, big);
+                off[(4 * c + i) * R + r] = o;
+                scl[(4 * c + i) * R + r] = s;
+            }
+        }
+    } else {
+#pragma unroll 2
+        for (int task = d; task < BK * (R / 4); task += kRawDecoders) {
+            const int k = task / (R / 4), r4 = (task % (R / 4)) * 4;
+            const float4 v = *reinterpret_cast<const float4 *>(raw + (k * R + r4) * 4);
+            uint4 o;
+            float4 s;
+            decode(v.x, M, offshift, o.x, s.x, big);
+            decode(v.y, M, offshift, o.y, s.y, big);
+            decode(v.z, M, offshift, o.z, s.z, big);
+            decode(v.w, M, offshift, o.w, s.w, big);
+            *reinterpret_cast<uint4 *>(off + k * R + r4) = o;
+            *reinterpret_cast<float4 *>(scl + k * R + r4) = s;
+        }
+    }
+}
+
+struct RawSmem {
+    uint8_t *dec;          // kRawDec decoded stages of kTmaStageBytes
+    uint8_t *raw;          // kRawRing raw stages of kRawStageBytes
+    uint64_t *raw_full, *raw_empty, *full, *empty;
+    int *flags;            // [kRawDec][decoder warps]: the stage holds |x| >= 2^64
+};
+
+// The producer warpgroup: thread 0 also issues the copies, kRawRing - 1 stages ahead.
+__device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &maps, const RawSmem &sm)
+{
+    const int d = threadIdx.x - kTmaConsumerThreads;
+    const int lane = d & 31, dw = d >> 5;
+    const int offU = p.M + p.wlog, offL = p.wlog;
+    long long it0, it1;
+    cta_range(p, it0, it1);
+    bool aborted = false;
+    long long issued = 0;
+    auto issue = [&](long long it) {
+        const long long g = it - it0;
+        const int rs = (int)(g % kRawRing);
+        if (!mbar_wait(&sm.raw_empty[rs], (uint32_t)(((g / kRawRing) & 1) ^ 1), aborted)) return;
+        const StagePos sp = stage_pos(p, it);
+        const ProbParams &q = p.pr[sp.pi];
+        uint8_t *st = sm.raw + (size_t)rs * kRawStageBytes;
+        mbar_expect_tx(&sm.raw_full[rs], kRawStageBytes);
+        const int k0 = sp.kt * BK;
+        if (q.u_kfast) tma_load_3d(st, &maps.u[sp.pi], k0, sp.u_tile0, sp.b * q.u_bsel, &sm.raw_full[rs]);
+        else tma_load_3d(st, &maps.u[sp.pi], sp.u_tile0, k0, sp.b * q.u_bsel, &sm.raw_full[rs]);
+        if (q.l_kfast) tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], k0, sp.l_tile0, sp.b * q.l_bsel, &sm.raw_full[rs]);
+        else tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], sp.l_tile0, k0, sp.b * q.l_bsel, &sm.raw_full[rs]);
+        ++issued;
+    };
+    if (d == 0)
+        for (long long it = it0; it < it1 && it < it0 + kRawRing - 1; ++it) issue(it);
+    for (long long it = it0; it < it1; ++it) {
+        const long long g = it - it0;
+        if (d == 0 && it + kRawRing - 1 < it1 && !aborted) issue(it + kRawRing - 1);
+        const int rs = (int)(g % kRawRing), ds = (int)(g % kRawDec);
+        mbar_wait(&sm.raw_full[rs], (uint32_t)((g / kRawRing) & 1), aborted);
+        mbar_wait(&sm.empty[ds], (uint32_t)(((g / kRawDec) & 1) ^ 1), aborted);
+        const StagePos sp = stage_pos(p, it);
+        const ProbParams &q = p.pr[sp.pi];
+        const uint8_t *raw = sm.raw + (size_t)rs * kRawStageBytes;
+        uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
+        int big = 0;
+        raw_decode<BU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st), reinterpret_cast<float *>(st + BK * BU * 4),
+                       p.M, offU, d, big);
+        raw_decode<BL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+                       reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
+        mbar_arrive(&sm.raw_empty[rs]);
+        const int any = __any_sync(0xFFFFFFFFu, big);
+        if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;
+        mbar_arrive(&sm.full[ds]);
+    }
+    if (d == 0 && aborted) {
+        // copies issued into raw slots nobody waited for may still be landing
+        bool gave_up = false;
+        const long long n = issued < kRawRing ? issued : kRawRing;
+        for (long long j = issued - n; j < issued; ++j)
+            mbar_wait(&sm.raw_full[j % kRawRing], (uint32_t)((j / kRawRing) & 1), gave_up);
+    }
+}
+
+template <int W, bool GL>
+__device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lut, const RawSmem &sm, int red_bytes)
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int wu = warp / WL, wl = warp % WL;
+    const int urow = wu * TM;
+    const int lcol = wl * 32 * TN + lane * TN;
+    uint32_t g = 0;
+    bool aborted = false;
+    CutTile cut0, cut1;
+    int ncut = 0;
+    for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
+        float2 acc[TM / 2][TN];
+#pragma unroll
+        for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+        const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + wl * 32 * TN >= q.L.rows;
+        for (int kt = s0; kt < s1; ++kt, ++g) {
+            const int ds = g % kRawDec;
+            mbar_wait(&sm.full[ds], (g / kRawDec) & 1, aborted);
+            if (!idle) {
+                const uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
+                const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
+                const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
+                const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
+                const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
+                int any_big = 0;
+#pragma unroll
+                for (int w = 0; w < kRawDecoders / 32; ++w) any_big |= sm.flags[ds * (kRawDecoders / 32) + w];
+                if (any_big)
+                    compute_stage<W, GL, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                else
+                    compute_stage<W, GL, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+            }
+            mbar_arrive(&sm.empty[ds]);
+        }
+        segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, cut0, cut1, ncut);
+    });
+    // the rings (decoded, then raw, contiguous) hold the reduction's copies
+    finish_cut_tiles(p, cut0, cut1, ncut, reinterpret_cast<float *>(sm.dec), red_bytes, sm.raw_full + 2 * kRawRing +
+                     2 * kRawDec, aborted);
+}
+
+// All problems of a launch read the same LUT orientation (staged once).
+template <int W, bool GL>
+__global__ void __launch_bounds__(kRawThreads, 1)
+    lutgemm_raw_kernel(const __grid_constant__ KParams p, const __grid_constant__ TmaMaps maps)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x;
+    // swizzled copies want their boxes 1024-byte aligned: align the base at run time
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const int lut_bytes = GL ? 0 : raw_lut_region(p.table_bytes);
+    RawSmem sm;
+    sm.dec = smem + lut_bytes;
+    sm.raw = sm.dec + kRawDec * kTmaStageBytes;
+    sm.raw_full = reinterpret_cast<uint64_t *>(sm.raw + kRawRing * kRawStageBytes);
+    sm.raw_empty = sm.raw_full + kRawRing;
+    sm.full = sm.raw_empty + kRawRing;
+    sm.empty = sm.full + kRawDec;
+    uint64_t *red = sm.empty + kRawDec;                    // the stream-K reduction's barrier
+    sm.flags = reinterpret_cast<int *>(red + 1);
+
+    if constexpr (!GL) {
+        // the table was written when the LUT was built, before any launch
+        const uint4 *src = static_cast<const uint4 *>(p.pr[0].table);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem);
+        const int nvec = (p.table_bytes + 15) >> 4;
+        for (int i = tid; i < nvec; i += kRawThreads) dst[i] = __ldg(src + i);
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kRawRing; ++s) {
+            mbar_init(&sm.raw_full[s], 1);
+            mbar_init(&sm.raw_empty[s], kRawDecoders);
+        }
+        for (int s = 0; s < kRawDec; ++s) {
+            mbar_init(&sm.full[s], kRawDecoders);
+            mbar_init(&sm.empty[s], kTmaConsumerThreads);
+        }
+        mbar_init(red, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid == kTmaConsumerThreads) {
+        for (int i = 0; i < p.nprob; ++i) {
+            tma_prefetch_map(&maps.u[i]);
+            tma_prefetch_map(&maps.l[i]);
+        }
+    }
+    __syncthreads();
+    // Operands, outputs and scratch may belong to the previous launch on the
+    // stream: wait for it to complete before any of them is touched.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
+    if (tid >= kTmaConsumerThreads) {
+        if constexpr (kTmaProducerWarps == 4) reg_dealloc<kTmaProducerRegs>();
+        raw_producer(p, maps, sm);
+    } else {
+        if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
+        raw_consumer<W, GL>(p, lut, sm, kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes);
+    }
+}
+
+template <int W, bool GL>
+int launch_raw_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t smem, cudaStream_t st)
+{
+    static int checked[64] = {};   // 0 unknown, 1 usable, -1 register split not satisfiable
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AMSIM_ECUDA;
+    if (dev >= 64) return AMSIM_EUNSUPPORTED;
+    if (checked[dev] == 0) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, lutgemm_raw_kernel<W, GL>);
+        if (e != cudaSuccess) return cuda_status(e);
+        if (kTmaProducerWarps == 4 &&
+            fa.numRegs * kRawThreads < kTmaConsumerThreads * kTmaConsumerRegs + 128 * kTmaProducerRegs) {
+            checked[dev] = -1;
+        } else {
+            e = cudaFuncSetAttribute(lutgemm_raw_kernel<W, GL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kMaxSmemPerCta);
+            if (e != cudaSuccess) return cuda_status(e);
+            checked[dev] = 1;
+        }
+    }
+    if (checked[dev] < 0) return AMSIM_EUNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kRawThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    for (int pdl = 1; pdl >= 0; --pdl) {
+        int na = 0;
+        if (pdl) {
+            attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attrs[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
+        if (p.fused) {
+            attrs[na].id = cudaLaunchAttributeCooperative;
+            attrs[na].val.cooperative = 1;
+            ++na;
+        }
+        cfg.attrs = attrs;
+        cfg.numAttrs = na;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, lutgemm_raw_kernel<W, GL>, p, maps);
+        if (e == cudaSuccess) {
+            count_launch();
+            return AMSIM_OK;
+        }
+        cudaGetLastError();
+    }
+    return p.fused ? AMSIM_ENOTCOOP : AMSIM_ECUDA;
+}
+
+int launch_raw_w8(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+int launch_raw_w16(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+int launch_raw_w32(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+
+}  // namespace kern
+}  // namespace amsim

@@ -1,0 +1,14 @@
+// Instances of the raw-tile TMA LUT-GEMM kernel for 16-bit narrowed LUT entries.
+#include "gemm_raw.cuh"
+
+namespace amsim {
+namespace kern {
+
+int launch_raw_w16(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st)
+{
+    return gl ? launch_raw_instance<16, true>(p, maps, grid, smem, st)
+              : launch_raw_instance<16, false>(p, maps, grid, smem, st);
+}
+
+}  // namespace kern
+}  // namespace amsim

@@ -1,0 +1,14 @@
+// Instances of the raw-tile TMA LUT-GEMM kernel for 8-bit narrowed LUT entries.
+#include "gemm_raw.cuh"
+
+namespace amsim {
+namespace kern {
+
+int launch_raw_w8(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st)
+{
+    return gl ? launch_raw_instance<8, true>(p, maps, grid, smem, st)
+              : launch_raw_instance<8, false>(p, maps, grid, smem, st);
+}
+
+}  // namespace kern
+}  // namespace amsim

@@ -81,7 +81,8 @@ enum amsim_path {
     AMSIM_PATH_SINGLE_ROLE = 8,     /* the single-role fallback kernel */
     AMSIM_PATH_STREAMK = 16,        /* reduction split across CTAs (stream-K) */
     AMSIM_PATH_FIXUP = 32,          /* cut tiles finished by the separate fixup kernel */
-    AMSIM_PATH_CONV_BOXES = 64      /* convolution operands as shifted or blocked tensor boxes */
+    AMSIM_PATH_CONV_BOXES = 64,     /* convolution operands as shifted or blocked tensor boxes */
+    AMSIM_PATH_RAW_TILES = 128      /* operand tiles copied in place by TMA, decoded in shared memory */
 };
 int amsim_last_path(void);
 

@@ -263,10 +263,15 @@ def test_each_kernel_path(amd, orc, luts, shape, path):
     lut = luts("mitchell", 7)
     got = gpu_gemm(amd, lut, A, B, False, True, ws=_path_ws(amd, lut, path, "N", "T", m, n, k))
     taken = amd.amsim_last_path()
-    if path == "planes":
+    # operands with copy-engine strides (k a multiple of 4 here) are copied in
+    # place and decoded in shared memory on any scratch; others need planes
+    raw = k % 4 == 0
+    if raw:
+        assert taken & amd.AMSIM_PATH_RAW_TILES, taken
+    elif path == "planes":
         assert taken & amd.AMSIM_PATH_PLANES, taken
     else:
-        assert not taken & amd.AMSIM_PATH_PLANES, taken
+        assert not taken & (amd.AMSIM_PATH_PLANES | amd.AMSIM_PATH_RAW_TILES), taken
         assert taken & (amd.AMSIM_PATH_INKERNEL_DECODE | amd.AMSIM_PATH_SINGLE_ROLE), taken
     if path == "none":
         assert not taken & amd.AMSIM_PATH_STREAMK, taken
@@ -290,12 +295,14 @@ def test_special_operands_each_path(amd, orc, luts, path):
         check(orc, kind, 7, A, B, False, False, got, what=f"specials {kind} path={path}")
 
 
+@pytest.mark.parametrize("k", [150, 152])
 @pytest.mark.parametrize("path", ["planes", "none"])
-def test_batched_broadcast_operand(amd, orc, luts, path):
-    """strideB = 0: one B serves every batch (one plane for all batches)."""
+def test_batched_broadcast_operand(amd, orc, luts, path, k):
+    """strideB = 0: one B serves every batch (one plane, or one copied tensor
+    for k = 152, for all batches)."""
     import torch
     rng = np.random.default_rng(14)
-    batch, m, n, k = 5, 70, 90, 150
+    batch, m, n = 5, 70, 90
     A = rnd(rng, (batch, m, k))
     B = rnd(rng, (k, n))
     lut = luts("mitchell", 7)
@@ -325,3 +332,54 @@ def test_paths_bit_identical_without_stream_k(amd, luts):
             for p in ("planes", "in_kernel", "none")]
     for o in outs[1:]:
         assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32))
+
+
+RAW_SHAPES = [(64, 256, 16), (300, 500, 2000), (130, 520, 40), (257, 10, 500), (5, 7, 4), (700, 90, 332)]
+
+
+@pytest.mark.parametrize("ta", [False, True])
+@pytest.mark.parametrize("tb", [False, True])
+@pytest.mark.parametrize("shape", RAW_SHAPES)
+def test_raw_tile_path(amd, orc, luts, shape, ta, tb):
+    """Operand tiles copied in place (rows or k innermost, so both the plain and
+    the swizzled transposing decode run) and decoded in shared memory; leading
+    dimensions that are multiples of 4 elements select this path."""
+    m, n, k = shape
+    lda, ldb = (m if ta else k), (k if tb else n)
+    if lda % 4 or ldb % 4:
+        pytest.skip("leading dimension not a multiple of 4")
+    rng = np.random.default_rng(7 * m + 5 * n + k + 2 * ta + tb)
+    A = rnd(rng, (k, m) if ta else (m, k))
+    B = rnd(rng, (n, k) if tb else (k, n))
+    lut = luts("mitchell", 7)
+    got = gpu_gemm(amd, lut, A, B, ta, tb)
+    assert amd.amsim_last_path() & amd.AMSIM_PATH_RAW_TILES, amd.amsim_last_path()
+    check(orc, "mitchell", 7, A, B, ta, tb, got, what=f"raw {shape} {ta}{tb}")
+
+
+def test_raw_tile_path_special_operands(amd, orc, luts):
+    """Zeros, denormals, infinities, NaNs and |x| >= 2^64 through the in-place
+    copies (the per-stage large-operand flag selects the rounding path)."""
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    rng = np.random.default_rng(16)
+    a, b = wl.special_values_mix(72 * 128 + 128 * 96, seed=17)
+    A = a[:72 * 128].reshape(72, 128).copy()
+    B = b[72 * 128:72 * 128 + 128 * 96].reshape(128, 96).copy()
+    A[:, :] = np.where(rng.random(A.shape) < 0.93, rng.standard_normal(A.shape), A).astype(np.float32)
+    B[:, :] = np.where(rng.random(B.shape) < 0.93, rng.standard_normal(B.shape), B).astype(np.float32)
+    for kind in ("mitchell", "exact"):
+        got = gpu_gemm(amd, luts(kind, 7), A, B, False, False)
+        assert amd.amsim_last_path() & amd.AMSIM_PATH_RAW_TILES
+        check(orc, kind, 7, A, B, False, False, got, what=f"raw specials {kind}")
+
+
+def test_unaligned_leading_dimension_takes_planes(amd, orc, luts):
+    """A leading dimension that is not a multiple of 4 elements cannot be copied
+    in place: with scratch the operands go through planes instead."""
+    rng = np.random.default_rng(18)
+    A, B = rnd(rng, (70, 129)), rnd(rng, (129, 90))
+    lut = luts("mitchell", 7)
+    got = gpu_gemm(amd, lut, A, B, False, False)
+    taken = amd.amsim_last_path()
+    assert taken & amd.AMSIM_PATH_PLANES and not taken & amd.AMSIM_PATH_RAW_TILES, taken
+    check(orc, "mitchell", 7, A, B, False, False, got, what="unaligned lda")
