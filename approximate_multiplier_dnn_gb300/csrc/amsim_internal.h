@@ -54,36 +54,26 @@ struct OperandDesc {
     int64_t extent;      // gather: elements of the source tensor (dense operands: computed by the planner)
 };
 
-// Operands of a convolution laid out for the TMA-fed kernel (built in
-// conv.cu).  Each operand is one or more predecode jobs -- element (b, r, k)
-// of job j at src[b*bs + (r / rdiv)*s_rhi + (r % rdiv + roff)*s_row +
-// (k / kdiv)*s_khi + (k % kdiv)*s_k], zero when r % rdiv + roff is outside
-// [0, rlim) -- written as planes [batch][2][K][rows_pad], and a tensor map
-// over each job's planes (dims[0] innermost, strides in bytes for dims 1..).
-struct TmaPlaneJob {
-    const float *src;
-    int64_t bs, s_row, s_k, s_rhi, s_khi;
-    int rdiv, roff, rlim, kdiv;
-    int rows, K, batch, rows_pad;
-};
-struct TmaMapSpec {
+// A convolution's operands read in place by the raw-tile TMA kernel (built in
+// conv.cu): a tensor map over each caller tensor (dims[0] innermost, strides
+// in bytes for dims 1.., 64-byte swizzle for boxes that arrive [row][k]).
+struct TmaRawMap {
+    const float *base;
     int rank;
     uint64_t dims[5], strides[4];
     uint32_t box[5];
+    int swizzle64;
 };
-constexpr int kMaxConvCopies = 10;
-struct ConvTma {
-    // 1: the L tile is whole image rows of one image, read from the copy of
-    //    the activation shifted for the current filter column (forward, data
-    //    gradient); 2: the L tile is four 64-channel blocks of filter taps
+struct ConvRaw {
+    // 1: the L tile is whole output rows of one image; a stage is one box of
+    //    16 channels of the activation at the filter tap's offset (forward,
+    //    data gradient); 2: the L tile is four 64-channel blocks of filter taps
     //    over 16 output pixels of one row (filter gradient)
     int mode;
-    TmaPlaneJob u;
-    TmaMapSpec umap;
-    int nl;
-    TmaPlaneJob l[kMaxConvCopies];
-    TmaMapSpec lmap[kMaxConvCopies];
-    // box coordinates (see the TMA kernel's copy thread)
+    TmaRawMap umap, lmap;
+    int u_kfast;     // the U box arrives [row][k]
+    int u_tap;       // U box coordinates (step within the tap, row, tap): the data gradient's filter
+    // box coordinates (see the raw-tile kernel's copy thread)
     int ch, S, tiles_img, rows_tile, ybase, ystep, xbase, xstep, N, P, Q, rows;
 };
 
@@ -100,7 +90,7 @@ struct Problem {
     float *c_ptr;
     int64_t c_bs, c_su, c_sl;
     float alpha, beta;
-    const ConvTma *tma = nullptr;   // convolution operands for the TMA kernel, if it applies
+    const ConvRaw *conv = nullptr;  // convolution operands as tensor boxes, if they qualify
 };
 
 // Launch the LUT-GEMM for a problem.  ws may be null; the stream-K schedule

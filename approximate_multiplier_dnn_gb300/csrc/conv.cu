@@ -118,131 +118,86 @@ OperandDesc w_transposed(const Geo &g, const float *w)
     return d;
 }
 
-// ------------------------------------------------------------------ TMA layouts
-// With unit strides a convolution's operands can be predecoded into planes
-// that tensor boxes read directly: the im2col rows of one filter tap are
-// whole rows of the activation shifted by the tap's column offset (one
-// shifted copy per filter column, built by the predecode pass), and the
-// weight gradient's rows are channel runs of the activation in NHWC order.
+// ------------------------------------------------------------------ tensor boxes
+// With unit strides the raw-tile kernel reads a convolution's operands in
+// place: for filter tap (r, s) the im2col rows of whole output rows are one
+// box of the NHWC activation whose start row and column are the tap's
+// offsets (out-of-range pixels arrive as zeros), and the weight gradient's
+// rows are 64-channel runs of the activation at each tap's input position.
 
-amsim::TmaPlaneJob dense_job(const float *src, int rows, int K, long long s_row, long long s_k)
+amsim::TmaRawMap raw_map(const float *base, int rank, const uint64_t *dims, const uint32_t *box, int swizzle64)
 {
-    amsim::TmaPlaneJob j = {};
-    j.src = src;
-    j.s_row = s_row;
-    j.s_k = s_k;
-    j.rdiv = rows;
-    j.rlim = rows;
-    j.kdiv = K;
-    j.rows = rows;
-    j.K = K;
-    j.batch = 1;
-    j.rows_pad = (rows + 3) & ~3;
-    return j;
-}
-
-// [1][2][K][rows_pad] planes read as BU x BK boxes (the U operand).
-amsim::TmaMapSpec plane_map(const amsim::TmaPlaneJob &j)
-{
-    amsim::TmaMapSpec m = {};
-    m.rank = 4;
-    const uint64_t pitch = (uint64_t)j.rows_pad * 4;
-    m.dims[0] = (uint64_t)j.rows; m.dims[1] = (uint64_t)j.K; m.dims[2] = 2; m.dims[3] = (uint64_t)j.batch;
-    m.strides[0] = pitch; m.strides[1] = pitch * j.K; m.strides[2] = pitch * j.K * 2;
-    m.box[0] = amsim::kern::BU; m.box[1] = amsim::kern::BK; m.box[2] = 2; m.box[3] = 1;
+    amsim::TmaRawMap m = {};
+    m.base = base;
+    m.rank = rank;
+    uint64_t stride = 4;
+    for (int i = 0; i < rank; ++i) {
+        m.dims[i] = dims[i];
+        m.box[i] = box[i];
+        stride *= dims[i];
+        if (i + 1 < rank) m.strides[i] = stride;
+    }
+    m.swizzle64 = swizzle64;
     return m;
 }
 
-// Shifted copies for the forward pass (act = x, out = y) or the data gradient
-// (act = dy, out = dx): copy s holds act[n][y][x + x0 + s*xs][c] at [n][2][c][y][x]
-// for x in [0, OW), zero outside the activation's width AW.
-void shifted_copies(amsim::ConvTma *cv, const float *act, int N, int AH, int AW, int CH, int OW, int S, int x0,
-                    int xs)
+// Fills *cv and returns true when pass `which` of geometry g can use tensor boxes.
+bool conv_raw(const Geo &g, int which, const float *t0, const float *t1, amsim::ConvRaw *cv)
 {
-    cv->nl = S;
-    for (int s = 0; s < S; ++s) {
-        amsim::TmaPlaneJob &j = cv->l[s];
-        j = {};
-        j.src = act;
-        j.batch = N;
-        j.bs = (long long)AH * AW * CH;
-        j.rows = AH * OW;
-        j.rdiv = OW;
-        j.s_rhi = (long long)AW * CH;
-        j.roff = x0 + s * xs;
-        j.rlim = AW;
-        j.s_row = CH;
-        j.K = CH;
-        j.kdiv = CH;
-        j.s_k = 1;
-        j.rows_pad = AH * OW;
-        amsim::TmaMapSpec &m = cv->lmap[s];
-        m = {};
-        m.rank = 5;
-        m.dims[0] = (uint64_t)OW; m.dims[1] = (uint64_t)AH; m.dims[2] = (uint64_t)CH; m.dims[3] = 2;
-        m.dims[4] = (uint64_t)N;
-        m.strides[0] = (uint64_t)OW * 4;
-        m.strides[1] = (uint64_t)AH * OW * 4;
-        m.strides[2] = (uint64_t)CH * AH * OW * 4;
-        m.strides[3] = 2ULL * CH * AH * OW * 4;
-        m.box[0] = (uint32_t)OW; m.box[1] = (uint32_t)(amsim::kern::BL / OW); m.box[2] = amsim::kern::BK;
-        m.box[3] = 2; m.box[4] = 1;
-    }
-}
-
-// Fills *cv and returns true when pass `which` of geometry g can use the TMA layouts.
-bool conv_tma(const Geo &g, int which, const float *t0, const float *t1, amsim::ConvTma *cv)
-{
+    using amsim::kern::BK;
     using amsim::kern::BL;
-    if (g.sh != 1 || g.sw != 1 || g.S > amsim::kMaxConvCopies) return false;
+    using amsim::kern::BU;
+    if (g.sh != 1 || g.sw != 1) return false;
     *cv = {};
     cv->S = g.S;
     if (which == 0) {
         // y[n,p,q,k] = sum x[n, p - ph + r dh, q - pw + s dw, c] w[r,s,c,k]
-        if (g.C % 16 || g.Q % 4 || BL % g.Q || g.P % (BL / g.Q)) return false;
+        if (g.C % 16 || BL % g.Q || g.P % (BL / g.Q)) return false;
         cv->mode = 1;
-        cv->u = dense_job(t1, g.K, g.R * g.S * g.C, 1, g.K);
-        shifted_copies(cv, t0, g.N, g.H, g.W, g.C, g.Q, g.S, -g.pw, g.dw);
+        const uint64_t ud[3] = {(uint64_t)g.K, (uint64_t)g.R * g.S * g.C, 1};
+        const uint32_t ub[3] = {(uint32_t)BU, (uint32_t)BK, 1};
+        cv->umap = raw_map(t1, 3, ud, ub, 0);                  // w[(r,s,c)][k]: rows k innermost
+        const uint64_t ld[4] = {(uint64_t)g.C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.N};
+        const uint32_t lb[4] = {(uint32_t)BK, (uint32_t)g.Q, (uint32_t)(BL / g.Q), 1};
+        cv->lmap = raw_map(t0, 4, ld, lb, 1);                  // x NHWC, [row][channel] boxes
         cv->ch = g.C;
         cv->rows_tile = BL / g.Q;
         cv->tiles_img = g.P / cv->rows_tile;
         cv->ybase = -g.ph;
         cv->ystep = g.dh;
+        cv->xbase = -g.pw;
+        cv->xstep = g.dw;
     } else if (which == 1) {
         // dx[n,h,w,c] = sum dy[n, h + ph - r dh, w + pw - s dw, k] w[r,s,c,k]
-        if (g.K % 16 || g.W % 4 || BL % g.W || g.H % (BL / g.W)) return false;
+        if (g.K % 16 || BL % g.W || g.H % (BL / g.W)) return false;
         cv->mode = 1;
-        // filter with its channel axes swapped: row c, index (r, s, k)
-        amsim::TmaPlaneJob u = dense_job(t1, g.C, g.R * g.S * g.K, g.K, 1);
-        u.kdiv = g.K;
-        u.s_khi = (long long)g.C * g.K;
-        cv->u = u;
-        shifted_copies(cv, t0, g.N, g.P, g.Q, g.K, g.W, g.S, g.pw, -g.dw);
+        // the filter with its channel axes swapped: rows c, steps (r, s, k) -> boxes of
+        // 16 k by 64 c of one tap, [c][k]
+        const uint64_t ud[3] = {(uint64_t)g.K, (uint64_t)g.C, (uint64_t)g.R * g.S};
+        const uint32_t ub[3] = {(uint32_t)BK, (uint32_t)BU, 1};
+        cv->umap = raw_map(t1, 3, ud, ub, 1);
+        cv->u_kfast = 1;
+        cv->u_tap = 1;
+        const uint64_t ld[4] = {(uint64_t)g.K, (uint64_t)g.Q, (uint64_t)g.P, (uint64_t)g.N};
+        const uint32_t lb[4] = {(uint32_t)BK, (uint32_t)g.W, (uint32_t)(BL / g.W), 1};
+        cv->lmap = raw_map(t0, 4, ld, lb, 1);                  // dy NHWC
         cv->ch = g.K;
         cv->rows_tile = BL / g.W;
         cv->tiles_img = g.H / cv->rows_tile;
         cv->ybase = g.ph;
         cv->ystep = -g.dh;
+        cv->xbase = g.pw;
+        cv->xstep = -g.dw;
     } else {
         // dw[r,s,c,k] = sum over (n,p,q) of x[n, p - ph + r dh, q - pw + s dw, c] dy[n,p,q,k]
         if (g.C % 64 || g.Q % 16) return false;
         cv->mode = 2;
-        cv->u = dense_job(t1, g.K, g.N * g.P * g.Q, 1, g.K);
-        // x as planes [n][h][2][w][c]: job batch (n, h), row c, index w
-        cv->nl = 1;
-        amsim::TmaPlaneJob j = dense_job(t0, g.C, g.W, 1, g.C);
-        j.batch = g.N * g.H;
-        j.bs = (long long)g.W * g.C;
-        cv->l[0] = j;
-        amsim::TmaMapSpec &m = cv->lmap[0];
-        m.rank = 5;
-        m.dims[0] = (uint64_t)g.C; m.dims[1] = (uint64_t)g.W; m.dims[2] = 2; m.dims[3] = (uint64_t)g.H;
-        m.dims[4] = (uint64_t)g.N;
-        m.strides[0] = (uint64_t)g.C * 4;
-        m.strides[1] = (uint64_t)g.W * g.C * 4;
-        m.strides[2] = 2ULL * g.W * g.C * 4;
-        m.strides[3] = 2ULL * g.H * g.W * g.C * 4;
-        m.box[0] = 64; m.box[1] = amsim::kern::BK; m.box[2] = 2; m.box[3] = 1; m.box[4] = 1;
+        const uint64_t ud[3] = {(uint64_t)g.K, (uint64_t)g.N * g.P * g.Q, 1};
+        const uint32_t ub[3] = {(uint32_t)BU, (uint32_t)BK, 1};
+        cv->umap = raw_map(t1, 3, ud, ub, 0);                  // dy[(n,p,q)][k]: rows k innermost
+        const uint64_t ld[4] = {(uint64_t)g.C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.N};
+        const uint32_t lb[4] = {64, (uint32_t)BK, 1, 1};
+        cv->lmap = raw_map(t0, 4, ld, lb, 0);                  // x NHWC, [pixel][channel] = [k][row]
         cv->ch = g.C;
         cv->N = g.N;
         cv->P = g.P;
@@ -253,7 +208,6 @@ bool conv_tma(const Geo &g, int which, const float *t0, const float *t1, amsim::
         cv->xbase = -g.pw;
         cv->xstep = g.dw;
     }
-    cv->umap = plane_map(cv->u);
     return true;
 }
 
@@ -333,9 +287,9 @@ int run(const amsim_conv_desc *desc, int which, const float *t0, const float *t1
     if (rc) return rc;
     Geo g;
     geometry(desc, &g);
-    amsim::ConvTma cv;
+    amsim::ConvRaw cv;
     if (pr.U.gather || pr.L.gather)
-        if (conv_tma(g, which, t0, t1, &cv)) pr.tma = &cv;
+        if (conv_raw(g, which, t0, t1, &cv)) pr.conv = &cv;
     return amsim::run_problem(pr, lut, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -381,9 +335,9 @@ size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim
     if (build(desc, which, &dummy0, &dummy1, &dummy_out, &pr)) return 0;
     Geo g;
     geometry(desc, &g);
-    amsim::ConvTma cv;
+    amsim::ConvRaw cv;
     if (pr.U.gather || pr.L.gather)
-        if (conv_tma(g, which, &dummy0, &dummy1, &cv)) pr.tma = &cv;
+        if (conv_raw(g, which, &dummy0, &dummy1, &cv)) pr.conv = &cv;
     return amsim::problem_workspace(pr, lut);
 }
 

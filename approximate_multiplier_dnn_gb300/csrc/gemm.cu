@@ -226,34 +226,6 @@ int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_ro
     return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
 }
 
-int encode_spec_map(CUtensorMap *map, const TmaMapSpec &m, void *base)
-{
-    EncodeTiled enc = encode_tiled();
-    if (!enc) return AMSIM_EUNSUPPORTED;
-    cuuint64_t dims[5], strides[4];
-    cuuint32_t box[5], estr[5];
-    for (int i = 0; i < m.rank; ++i) {
-        dims[i] = m.dims[i];
-        box[i] = m.box[i];
-        estr[i] = 1;
-        if (i + 1 < m.rank) strides[i] = m.strides[i];
-    }
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, (cuuint32_t)m.rank, base, dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
-}
-
-size_t job_plane_bytes(const TmaPlaneJob &j) { return align256((size_t)j.batch * 2 * j.K * j.rows_pad * 4); }
-
-// Plane bytes of a convolution's operands.
-size_t conv_plane_bytes(const ConvTma &cv)
-{
-    size_t b = job_plane_bytes(cv.u);
-    for (int i = 0; i < cv.nl; ++i) b += job_plane_bytes(cv.l[i]);
-    return b;
-}
-
 // Access-pattern flags of a decode job (see DecodeJob).
 void classify_job(kern::DecodeJob &d)
 {
@@ -266,31 +238,24 @@ void classify_job(kern::DecodeJob &d)
                 d.s_rhi % 4 == 0 && d.s_khi % 4 == 0;
 }
 
-void fill_job(kern::DecodeJob &d, const TmaPlaneJob &j, int offshift, void *plane, unsigned long long *flag,
-              long long &tiles)
+int encode_raw_spec(CUtensorMap *map, const TmaRawMap &m)
 {
-    d.src = j.src;
-    d.bs = j.bs;
-    d.s_row = j.s_row;
-    d.s_k = j.s_k;
-    d.s_rhi = j.s_rhi;
-    d.s_khi = j.s_khi;
-    d.rdiv = j.rdiv;
-    d.roff = j.roff;
-    d.rlim = j.rlim;
-    d.kdiv = j.kdiv;
-    d.rows = j.rows;
-    d.K = j.K;
-    d.batch = j.batch;
-    d.rows_pad = j.rows_pad;
-    d.offshift = offshift;
-    d.plane = static_cast<uint32_t *>(plane);
-    d.flag = flag;
-    d.tiles_r = ceil_div(j.rows, kern::kDecodeTileR);
-    d.tiles_k = ceil_div(j.K, kern::kDecodeTileK);
-    d.tile0 = tiles;
-    tiles += (long long)j.batch * d.tiles_r * d.tiles_k;
-    classify_job(d);
+    EncodeTiled enc = encode_tiled();
+    if (!enc) return AMSIM_EUNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(m.base) & 15) return AMSIM_EUNSUPPORTED;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], estr[5];
+    for (int i = 0; i < m.rank; ++i) {
+        dims[i] = m.dims[i];
+        box[i] = m.box[i];
+        estr[i] = 1;
+        if (i + 1 < m.rank) strides[i] = m.strides[i];
+    }
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)m.rank, const_cast<float *>(m.base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           m.swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
 }
 
 int launch_tma(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
@@ -312,7 +277,7 @@ int run_tma(int width, kern::KParams &tp, const kern::TmaMaps &maps, const kern:
     const dim3 grid((unsigned)blocks);
     int rc = kern::launch_predecode(dp, sms, stream);
     if (rc) return rc;
-    const int base = AMSIM_PATH_PLANES | (streamk ? AMSIM_PATH_STREAMK : 0) | (tp.conv ? AMSIM_PATH_CONV_BOXES : 0);
+    const int base = AMSIM_PATH_PLANES | (streamk ? AMSIM_PATH_STREAMK : 0);
     tp.fused = streamk ? 1 : 0;
     rc = launch_tma(width, tp, maps, gl, grid, smem, stream);
     if (rc == kern::AMSIM_ENOTCOOP) {
@@ -344,7 +309,7 @@ bool all_raw_ok(const Problem *p, int n, const Plan &pl, bool check_ptr)
 {
     for (int i = 0; i < n; ++i) {
         if (pl.tiles[i] == 0) continue;
-        if (p[i].tma || !raw_ok(p[i].U, p[i].K, p[i].batch, check_ptr) ||
+        if (p[i].conv || !raw_ok(p[i].U, p[i].K, p[i].batch, check_ptr) ||
             !raw_ok(p[i].L, p[i].K, p[i].batch, check_ptr))
             return false;
     }
@@ -402,8 +367,8 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     if (lut && encode_tiled() && all_raw_ok(p, n, pl, false) &&
         !(plan_planes(p, n, pl, lut->M, rwlog, &rps) && rps.n > 0 && planes_bytes_per_mac(p, n, pl, rps) < 0.01)) {
         // operand tiles are copied in place and decoded inside the GEMM
-    } else if (lut && encode_tiled() && n == 1 && p[0].tma) {
-        need += align256(pl.ws_bytes) - pl.ws_bytes + kFlagBlock + conv_plane_bytes(*p[0].tma);
+    } else if (lut && encode_tiled() && n == 1 && p[0].conv) {
+        // convolution tiles are copied in place as tensor boxes
     } else if (lut && encode_tiled()) {
         const int wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
         PlaneSet ps;
@@ -488,78 +453,24 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     PlaneSet ps;
     const bool planes_fit = ws && encode_tiled() && plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 &&
                             ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps);
-    if (encode_tiled() && all_raw_ok(p, n, pl, true) && !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01)) {
+    const bool conv_raw = n == 1 && p[0].conv && pl.tiles[0] > 0 && encode_tiled();
+    if (conv_raw || (encode_tiled() && all_raw_ok(p, n, pl, true) &&
+                     !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01))) {
         bool raw_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
         if (!raw_gl && kern::raw_smem_bytes((int)lut->narrow_bytes) > kMaxSmemPerCta) raw_gl = true;
         kern::TmaMaps maps;
+        kern::KParams tp = kp;
         int erc = AMSIM_OK;
-        for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
-            if (pl.tiles[i] == 0) continue;
-            erc = encode_raw_map(&maps.u[qi], p[i].U, p[i].K, p[i].batch, BU);
-            if (erc == AMSIM_OK) erc = encode_raw_map(&maps.l[qi], p[i].L, p[i].K, p[i].batch, BL);
-            kern::ProbParams &q = kp.pr[qi++];
-            q.u_kfast = p[i].U.s_row != 1;
-            q.l_kfast = p[i].L.s_row != 1;
-            q.u_bsel = (p[i].U.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
-            q.l_bsel = (p[i].L.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
-        }
-        if (erc == AMSIM_OK) {
-            kern::KParams tp = kp;
-            tp.table_bytes = raw_gl ? 0 : (int)lut->narrow_bytes;
-            tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
-            tp.fused = pl.streamk ? 1 : 0;
-            const size_t smem = (size_t)kern::raw_smem_bytes(tp.table_bytes);
-            const dim3 grid((unsigned)blocks);
-            int rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
-            if (rc == kern::AMSIM_ENOTCOOP) {
-                tp.fused = 0;
-                rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
-            }
-            if (rc == AMSIM_OK) {
-                const bool fix = pl.streamk && !tp.fused;
-                g_last_path |= AMSIM_PATH_RAW_TILES | (pl.streamk ? AMSIM_PATH_STREAMK : 0) | (fix ? AMSIM_PATH_FIXUP : 0);
-                return fix ? kern::launch_fixup(tp, pl.ctas - 1, stream) : AMSIM_OK;
-            }
-            if (rc != AMSIM_EUNSUPPORTED) return rc;
-        }
-    }
-
-    // Predecoded operands copied by TMA, when every operand is dense (or a
-    // convolution laid out for TMA) and the scratch holds the planes after the
-    // stream-K region.
-    bool tma_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
-    if (!tma_gl && tma_stages(kern::lut_region_bytes((int)lut->narrow_bytes)) == 0) tma_gl = true;
-    const size_t tma_lutb = tma_gl ? 0 : kern::lut_region_bytes((int)lut->narrow_bytes);
-    if (n == 1 && p[0].tma && pl.tiles[0] > 0 && ws && encode_tiled() &&
-        ws_bytes >= align256(pl.ws_bytes) + kFlagBlock + conv_plane_bytes(*p[0].tma)) {
-        const ConvTma &cv = *p[0].tma;
-        uint8_t *base = static_cast<uint8_t *>(ws);
-        const size_t flags_off = align256(pl.ws_bytes);
-        unsigned long long *flags = reinterpret_cast<unsigned long long *>(base + flags_off);
-        uint8_t *plane = base + flags_off + kFlagBlock;
-        const unsigned long long epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
-        kern::DecodeParams dp = {};
-        dp.M = lut->M;
-        dp.epoch = epoch;
-        long long dtiles = 0;
-        kern::TmaMaps maps;
-        int erc = encode_spec_map(&maps.u[0], cv.umap, plane);
-        fill_job(dp.job[0], cv.u, lut->M + kp.wlog, plane, flags, dtiles);
-        plane += job_plane_bytes(cv.u);
-        for (int i = 0; i < cv.nl && erc == AMSIM_OK; ++i) {
-            erc = encode_spec_map(&maps.l[i], cv.lmap[i], plane);
-            fill_job(dp.job[1 + i], cv.l[i], kp.wlog, plane, flags + 1, dtiles);
-            plane += job_plane_bytes(cv.l[i]);
-        }
-        dp.njobs = 1 + cv.nl;
-        dp.tiles = dtiles;
-        if (erc == AMSIM_OK) {
-            kern::KParams tp = kp;
+        if (conv_raw) {
+            const ConvRaw &cv = *p[0].conv;
+            erc = encode_raw_spec(&maps.u[0], cv.umap);
+            if (erc == AMSIM_OK) erc = encode_raw_spec(&maps.l[0], cv.lmap);
             kern::ProbParams &q = tp.pr[0];
-            q.u_big = flags;
-            q.l_big = flags + 1;
+            q.u_kfast = cv.u_kfast;
+            q.l_kfast = cv.mode == 1 ? 1 : 0;
             q.u_bsel = q.l_bsel = 0;
             tp.conv = cv.mode;
+            tp.cv_u_tap = cv.u_tap;
             tp.cv_ch = cv.ch;
             tp.cv_S = cv.S;
             tp.cv_tiles_img = cv.tiles_img;
@@ -572,14 +483,45 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             tp.cv_P = cv.P;
             tp.cv_Q = cv.Q;
             tp.cv_rows = cv.rows;
-            tp.table_bytes = tma_gl ? 0 : (int)lut->narrow_bytes;
-            tp.stages = tma_stages(tma_lutb);
-            tp.epoch = epoch;
-            const size_t smem = (size_t)kern::tma_smem_bytes((int)tma_lutb, tp.stages);
-            const int rc = run_tma(lut->width_bits, tp, maps, dp, tma_gl, blocks, smem, sms, pl.streamk, stream);
+        } else {
+            for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
+                if (pl.tiles[i] == 0) continue;
+                erc = encode_raw_map(&maps.u[qi], p[i].U, p[i].K, p[i].batch, BU);
+                if (erc == AMSIM_OK) erc = encode_raw_map(&maps.l[qi], p[i].L, p[i].K, p[i].batch, BL);
+                kern::ProbParams &q = tp.pr[qi++];
+                q.u_kfast = p[i].U.s_row != 1;
+                q.l_kfast = p[i].L.s_row != 1;
+                q.u_bsel = (p[i].U.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
+                q.l_bsel = (p[i].L.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
+            }
+        }
+        if (erc == AMSIM_OK) {
+            tp.table_bytes = raw_gl ? 0 : (int)lut->narrow_bytes;
+            tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
+            tp.fused = pl.streamk ? 1 : 0;
+            const size_t smem = (size_t)kern::raw_smem_bytes(tp.table_bytes);
+            const dim3 grid((unsigned)blocks);
+            int rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
+            if (rc == kern::AMSIM_ENOTCOOP) {
+                tp.fused = 0;
+                rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
+            }
+            if (rc == AMSIM_OK) {
+                const bool fix = pl.streamk && !tp.fused;
+                g_last_path |= AMSIM_PATH_RAW_TILES | (pl.streamk ? AMSIM_PATH_STREAMK : 0) |
+                               (fix ? AMSIM_PATH_FIXUP : 0) | (tp.conv ? AMSIM_PATH_CONV_BOXES : 0);
+                return fix ? kern::launch_fixup(tp, pl.ctas - 1, stream) : AMSIM_OK;
+            }
             if (rc != AMSIM_EUNSUPPORTED) return rc;
         }
     }
+
+    // Predecoded operands copied by TMA, when every operand is dense (or a
+    // convolution laid out for TMA) and the scratch holds the planes after the
+    // stream-K region.
+    bool tma_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
+    if (!tma_gl && tma_stages(kern::lut_region_bytes((int)lut->narrow_bytes)) == 0) tma_gl = true;
+    const size_t tma_lutb = tma_gl ? 0 : kern::lut_region_bytes((int)lut->narrow_bytes);
     if (ws && encode_tiled() &&
         plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 && planes_pay(p, n, pl, ps) &&
         ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps)) {

@@ -111,9 +111,10 @@ struct KParams {
     int fused;              // stream-K cut tiles are finished inside the kernel (cooperative launch)
     int stages;             // TMA kernel: stages in the shared-memory ring
     unsigned long long epoch;   // this launch's flag value (never reused)
-    // TMA kernel, convolution operands (one problem): conv 0 plain operands,
-    // 1 shifted-row L boxes, 2 blocked-channel L boxes (see ConvTma)
-    int conv;
+    // Raw-tile kernel, convolution operands (one problem): conv 0 plain
+    // operands, 1 whole-row L boxes per filter tap, 2 blocked-channel L boxes
+    // (see ConvRaw); cv_u_tap: U boxes addressed (step in tap, row, tap)
+    int conv, cv_u_tap;
     int cv_ch, cv_S, cv_tiles_img, cv_rows_tile, cv_ybase, cv_ystep, cv_xbase, cv_xstep, cv_N, cv_P, cv_Q, cv_rows;
 };
 

@@ -4,7 +4,11 @@
 //
 // One producer thread copies each stage's fp32 tiles -- BU (or BL) rows x BK
 // reduction steps of each operand, straight from the caller's tensors -- as
-// tensor boxes into a raw ring.  The producer warpgroup (128 threads) then
+// tensor boxes into a raw ring.  Unit-stride convolutions read their im2col
+// tiles the same way: a box of 16 channels of the NHWC activation at the
+// stage's filter tap covers whole output rows (the tap's row and column
+// offsets are box coordinates; out-of-range pixels arrive as zeros), and the
+// filter gradient's tile is four boxes of 64 channels.  The producer warpgroup (128 threads) then
 // decodes a landed stage into (LUT byte offset, scale) [k][row] arrays, which
 // the eight consumer warps use exactly as in the predecoded kernel.  Operands
 // stored k-fast arrive [row][k] with the copy engine's 64-byte swizzle, so the
@@ -31,6 +35,7 @@ constexpr int kRawRing = 3;                             // raw stages
 constexpr int kRawDec = 3;                              // decoded stages
 constexpr int kRawBarBytes = 256;                       // barriers and big-operand flags
 static_assert(kRawUBytes % 1024 == 0 && kRawLBytes % 1024 == 0, "swizzled boxes start 1024-byte aligned");
+static_assert(BL % 64 == 0 && (BL / 64) * BK * 64 * 4 == kRawLBytes, "blocked L boxes fill the L stage");
 static_assert((2 * kRawRing + 2 * kRawDec) * 8 + kRawDec * (kRawDecoders / 32) * 4 <= kRawBarBytes, "barrier block");
 static_assert(kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes >= (BU * BL + 1024 * 4) * 4,
               "the rings hold the stream-K reduction buffer");
@@ -92,6 +97,74 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
     }
 }
 
+// Decode four row-fast 64-row blocks ([BK][64] each, the filter gradient's
+// L tile) into columns 64 b .. 64 b + 63 of off/scl [BK][BL].
+__device__ __forceinline__ void raw_decode_blocks(const uint8_t *raw, uint32_t *off, float *scl, int M,
+                                                  int offshift, int d, int &big)
+{
+#pragma unroll 2
+    for (int task = d; task < (BL / 64) * BK * 16; task += kRawDecoders) {
+        const int b = task / (BK * 16), rem = task % (BK * 16);
+        const int k = rem / 16, r4 = (rem % 16) * 4;
+        const float4 v = *reinterpret_cast<const float4 *>(raw + ((b * BK + k) * 64 + r4) * 4);
+        uint4 o;
+        float4 s;
+        decode(v.x, M, offshift, o.x, s.x, big);
+        decode(v.y, M, offshift, o.y, s.y, big);
+        decode(v.z, M, offshift, o.z, s.z, big);
+        decode(v.w, M, offshift, o.w, s.w, big);
+        *reinterpret_cast<uint4 *>(off + k * BL + 64 * b + r4) = o;
+        *reinterpret_cast<float4 *>(scl + k * BL + 64 * b + r4) = s;
+    }
+}
+
+// Convolution boxes of stage kt (see ConvRaw): U from the filter or dy, L from
+// the activation at the stage's filter tap.
+__device__ __forceinline__ void conv_raw_boxes(const KParams &p, const TmaMaps &maps, const ProbParams &q,
+                                               int u_tile0, int l_tile0, int kt, uint8_t *st, uint64_t *bar)
+{
+    const int k0 = kt * BK;
+    if (p.cv_u_tap) {
+        const int rs = k0 / p.cv_ch;
+        tma_load_3d(st, &maps.u[0], k0 - rs * p.cv_ch, u_tile0, rs, bar);
+    } else if (q.u_kfast) {
+        tma_load_3d(st, &maps.u[0], k0, u_tile0, 0, bar);
+    } else {
+        tma_load_3d(st, &maps.u[0], u_tile0, k0, 0, bar);
+    }
+    uint8_t *dl = st + kRawUBytes;
+    if (p.conv == 1) {
+        // whole output rows y0 .. of image n; channels ch0 .. ch0 + 15 of tap (r, s)
+        const int t = l_tile0 / BL;
+        const int n = t / p.cv_tiles_img, y0 = (t - n * p.cv_tiles_img) * p.cv_rows_tile;
+        const int rs = k0 / p.cv_ch, ch0 = k0 - rs * p.cv_ch;
+        const int r = rs / p.cv_S, s = rs - r * p.cv_S;
+        tma_load_4d(dl, &maps.l[0], ch0, p.cv_xbase + s * p.cv_xstep, y0 + p.cv_ybase + r * p.cv_ystep, n, bar);
+    } else {
+        // 16 output pixels (n, pp, q0 ..) of one row; four blocks of 64 rows
+        // (tap, channel), each 64 channels at the tap's input position; rows
+        // past the end get a box wholly outside the tensor (zeros), so every
+        // stage carries the same bytes
+        const int pq = p.cv_P * p.cv_Q;
+        const int n = k0 / pq, rem = k0 - n * pq;
+        const int pp = rem / p.cv_Q, q0 = rem - pp * p.cv_Q;
+#pragma unroll
+        for (int blk = 0; blk < BL / 64; ++blk) {
+            const int row = l_tile0 + 64 * blk;
+            int c0 = 0, h = 0, w = 0, nn = p.cv_N;
+            if (row < p.cv_rows) {
+                const int rs = row / p.cv_ch;
+                const int r = rs / p.cv_S, s = rs - r * p.cv_S;
+                c0 = row - rs * p.cv_ch;
+                h = pp + p.cv_ybase + r * p.cv_ystep;
+                w = q0 + p.cv_xbase + s * p.cv_xstep;
+                nn = n;
+            }
+            tma_load_4d(dl + blk * (BK * 64 * 4), &maps.l[0], c0, w, h, nn, bar);
+        }
+    }
+}
+
 struct RawSmem {
     uint8_t *dec;          // kRawDec decoded stages of kTmaStageBytes
     uint8_t *raw;          // kRawRing raw stages of kRawStageBytes
@@ -118,10 +191,16 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
         uint8_t *st = sm.raw + (size_t)rs * kRawStageBytes;
         mbar_expect_tx(&sm.raw_full[rs], kRawStageBytes);
         const int k0 = sp.kt * BK;
-        if (q.u_kfast) tma_load_3d(st, &maps.u[sp.pi], k0, sp.u_tile0, sp.b * q.u_bsel, &sm.raw_full[rs]);
-        else tma_load_3d(st, &maps.u[sp.pi], sp.u_tile0, k0, sp.b * q.u_bsel, &sm.raw_full[rs]);
-        if (q.l_kfast) tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], k0, sp.l_tile0, sp.b * q.l_bsel, &sm.raw_full[rs]);
-        else tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], sp.l_tile0, k0, sp.b * q.l_bsel, &sm.raw_full[rs]);
+        if (p.conv) {
+            conv_raw_boxes(p, maps, q, sp.u_tile0, sp.l_tile0, sp.kt, st, &sm.raw_full[rs]);
+        } else {
+            if (q.u_kfast) tma_load_3d(st, &maps.u[sp.pi], k0, sp.u_tile0, sp.b * q.u_bsel, &sm.raw_full[rs]);
+            else tma_load_3d(st, &maps.u[sp.pi], sp.u_tile0, k0, sp.b * q.u_bsel, &sm.raw_full[rs]);
+            if (q.l_kfast)
+                tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], k0, sp.l_tile0, sp.b * q.l_bsel, &sm.raw_full[rs]);
+            else
+                tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], sp.l_tile0, k0, sp.b * q.l_bsel, &sm.raw_full[rs]);
+        }
         ++issued;
     };
     if (d == 0)
@@ -139,8 +218,12 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
         int big = 0;
         raw_decode<BU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st), reinterpret_cast<float *>(st + BK * BU * 4),
                        p.M, offU, d, big);
-        raw_decode<BL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
-                       reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
+        if (p.conv == 2)
+            raw_decode_blocks(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+                              reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
+        else
+            raw_decode<BL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+                           reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         mbar_arrive(&sm.raw_empty[rs]);
         const int any = __any_sync(0xFFFFFFFFu, big);
         if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;

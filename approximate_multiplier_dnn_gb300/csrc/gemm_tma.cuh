@@ -52,8 +52,6 @@ constexpr int kRedBytes = (BU * BL + 1024 * 4) * 4;
 constexpr int kTmaMinStages = (kRedBytes + kTmaStageBytes - 1) / kTmaStageBytes < 2
                                   ? 2 : (kRedBytes + kTmaStageBytes - 1) / kTmaStageBytes;
 static_assert(kTmaStageBytes % 128 == 0 && kTmaUBytes % 128 == 0, "stage alignment");
-static_assert(BL % 64 == 0 && 64 % TN == 0, "blocked L layout: a thread's columns lie in one 64-row block");
-static_assert(BK * 64 * 4 * 2 * (BL / 64) == kTmaLBytes, "blocked L boxes fill the L stage");
 
 // Shared memory of the TMA kernel for a ring of `stages` and a LUT region of `lut_bytes`.
 __host__ __device__ constexpr int tma_smem_bytes(int lut_bytes, int stages)
@@ -76,56 +74,6 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
         : "memory");
-}
-
-// Box (c0 .. c4) of a 5-D tensor map into shared memory; completes on `bar`.
-__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
-                                            int c4, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Convolution L boxes of stage kt of L tile l_tile0 into `dst` (see ConvTma).
-__device__ __forceinline__ void conv_l_boxes(const KParams &p, const TmaMaps &maps, int l_tile0, int kt,
-                                             uint8_t *dst, uint64_t *bar)
-{
-    if (p.conv == 1) {
-        // whole image rows y0 .. y0 + rows_tile - 1 of image n, channels
-        // ch0 .. ch0 + 15 of filter tap (r, s), from the copy for column s
-        const int t = l_tile0 / BL;
-        const int n = t / p.cv_tiles_img, y0 = (t - n * p.cv_tiles_img) * p.cv_rows_tile;
-        const int k0 = kt * BK;
-        const int rs = k0 / p.cv_ch, ch0 = k0 - rs * p.cv_ch;
-        const int r = rs / p.cv_S, s = rs - r * p.cv_S;
-        tma_load_5d(dst, &maps.l[s], 0, y0 + p.cv_ybase + r * p.cv_ystep, ch0, 0, n, bar);
-    } else {
-        // 16 output pixels (n, pp, q0 ..) of one row; four blocks of 64 rows
-        // (filter tap, channel), each a box of channels c0 .. c0 + 63 at the
-        // input position the tap reads; rows past the end get a box wholly
-        // outside the tensor (zeros), so every stage carries the same bytes
-        const int pix0 = kt * BK;
-        const int pq = p.cv_P * p.cv_Q;
-        const int n = pix0 / pq, rem = pix0 - n * pq;
-        const int pp = rem / p.cv_Q, q0 = rem - pp * p.cv_Q;
-#pragma unroll
-        for (int blk = 0; blk < BL / 64; ++blk) {
-            const int row = l_tile0 + 64 * blk;
-            int c0 = 0, h = 0, w = 0, nn = p.cv_N;
-            if (row < p.cv_rows) {
-                const int rs = row / p.cv_ch;
-                const int r = rs / p.cv_S, s = rs - r * p.cv_S;
-                c0 = row - rs * p.cv_ch;
-                h = pp + p.cv_ybase + r * p.cv_ystep;
-                w = q0 + p.cv_xbase + s * p.cv_xstep;
-                nn = n;
-            }
-            tma_load_5d(dst + blk * (2 * BK * 64 * 4), &maps.l[0], c0, w, 0, h, nn, bar);
-        }
-    }
 }
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
@@ -152,10 +100,7 @@ __device__ __forceinline__ void tma_producer(const KParams &p, const TmaMaps &ma
         uint8_t *st = ring + (size_t)slot * kTmaStageBytes;
         mbar_expect_tx(&full[slot], kTmaStageBytes);
         tma_load_4d(st, &maps.u[sp.pi], sp.u_tile0, sp.kt * BK, 0, sp.b * q.u_bsel, &full[slot]);
-        if (p.conv == 0)
-            tma_load_4d(st + kTmaUBytes, &maps.l[sp.pi], sp.l_tile0, sp.kt * BK, 0, sp.b * q.l_bsel, &full[slot]);
-        else
-            conv_l_boxes(p, maps, sp.l_tile0, sp.kt, st + kTmaUBytes, &full[slot]);
+        tma_load_4d(st + kTmaUBytes, &maps.l[sp.pi], sp.l_tile0, sp.kt * BK, 0, sp.b * q.l_bsel, &full[slot]);
         ++issued;
         if (++slot == S) { slot = 0; phase ^= 1; }
     }
@@ -206,24 +151,12 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
             const uint8_t *st = ring + (size_t)slot * kTmaStageBytes;
             const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
             const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
-            if (p.conv != 2) {
-                const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
-                const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
-                if (slow)
-                    compute_stage<W, GL, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-                else
-                    compute_stage<W, GL, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-            } else {
-                // blocked L: 64-row blocks of [offsets 16 x 64][scales 16 x 64];
-                // a thread's TN columns lie in one block
-                const uint8_t *blk = st + kTmaUBytes + (lcol / 64) * (2 * BK * 64 * 4);
-                const uint32_t *Lo = reinterpret_cast<const uint32_t *>(blk);
-                const float *Ls = reinterpret_cast<const float *>(blk + BK * 64 * 4);
-                if (slow)
-                    compute_stage<W, GL, true, BU, 64>(acc, Uo, Us, Lo, Ls, lut, urow, lcol % 64);
-                else
-                    compute_stage<W, GL, false, BU, 64>(acc, Uo, Us, Lo, Ls, lut, urow, lcol % 64);
-            }
+            const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
+            const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
+            if (slow)
+                compute_stage<W, GL, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+            else
+                compute_stage<W, GL, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
             mbar_arrive(&empty[slot]);
             if (++slot == S) { slot = 0; phase ^= 1; }
         }
@@ -264,9 +197,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (tid == kTmaConsumerThreads) {
-        for (int i = 0; i < p.nprob; ++i) tma_prefetch_map(&maps.u[i]);
-        const int nl = p.conv == 1 ? p.cv_S : p.nprob;
-        for (int i = 0; i < nl; ++i) tma_prefetch_map(&maps.l[i]);
+        for (int i = 0; i < p.nprob; ++i) {
+            tma_prefetch_map(&maps.u[i]);
+            tma_prefetch_map(&maps.l[i]);
+        }
     }
     __syncthreads();
     // Planes, flags, outputs and scratch belong to earlier launches on the

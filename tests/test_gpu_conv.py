@@ -23,9 +23,9 @@ GEOMS = [
     (1, 9, 9, 8, 12, 1, 1, (2, 2), (0, 0), (1, 1)),       # strided 1x1: gather
 ]
 
-# Unit-stride geometries whose passes take the tensor-box layouts (shifted
-# activation copies for the forward and data-gradient passes, 64-channel
-# blocks for the filter gradient) when the scratch holds the planes.
+# Unit-stride geometries whose passes read their operands in place as tensor
+# boxes (whole output rows of the activation at each filter tap for the
+# forward and data-gradient passes, 64-channel blocks for the filter gradient).
 TMA_GEOMS = [
     (1, 32, 32, 64, 32, 3, 3, (1, 1), (1, 1), (1, 1)),    # all three passes
     (2, 16, 16, 32, 48, 3, 3, (1, 1), (1, 1), (1, 1)),    # forward and data gradient
@@ -55,7 +55,7 @@ def test_conv_three_passes(amd, orc, luts, g, kind):
 
 @pytest.mark.parametrize("g", TMA_GEOMS)
 def test_conv_three_passes_without_scratch(amd, orc, luts, g):
-    """The same geometries through the gathering kernel (no scratch for planes)."""
+    """The same geometries without scratch: no split reduction."""
     check_three_passes(amd, orc, luts, g, "mitchell", False)
 
 
@@ -96,35 +96,47 @@ def test_conv_errors(amd, luts):
         amd.amsim_conv2d_bwd_data(amd.ConvDesc.make(1, 4, 4, 1, 1, 3, 3), None, x, x, lut)
 
 
-def test_tma_layout_is_used_when_scratch_allows(amd, luts):
-    """A unit-stride geometry asks for plane scratch on every pass and, given
-    it, takes the tensor-box layouts (a predecode launch, then the GEMM);
-    without scratch the gathering kernel runs alone."""
+def test_tensor_boxes_and_gather_fallback(amd, orc, luts):
+    """A unit-stride geometry reads its operands in place as tensor boxes, with
+    or without scratch (one launch, or a fixup kernel after a non-cooperative
+    split); operands that are not 16-byte aligned fall back to the gathering
+    kernel.  Both match the oracle."""
     import torch
     N, H, W, C, K, R, S = 1, 32, 32, 64, 32, 3, 3
     desc = amd.ConvDesc.make(N, H, W, C, K, R, S, (1, 1), (1, 1), (1, 1))
+    odesc = orc.conv_desc(N, H, W, C, K, R, S, (1, 1), (1, 1), (1, 1))
     lut = luts("mitchell", 7)
-    x = torch.zeros((N, H, W, C), device="cuda")
-    w = torch.zeros((R, S, C, K), device="cuda")
-    dy = torch.zeros((N, H, W, K), device="cuda")
-    outs = [torch.empty((N, H, W, K), device="cuda"), torch.empty((N, H, W, C), device="cuda"),
-            torch.empty((R, S, C, K), device="cuda")]
-    args = [(x, w), (dy, w), (x, dy)]
+    rng = np.random.default_rng(99)
+    x = rng.standard_normal((N, H, W, C)).astype(np.float32)
+    w = rng.standard_normal((R, S, C, K)).astype(np.float32)
+    dy = rng.standard_normal((N, H, W, K)).astype(np.float32)
     fns = (amd.amsim_conv2d_fwd, amd.amsim_conv2d_bwd_data, amd.amsim_conv2d_bwd_filter)
+    refs = (orc.conv2d_fwd, orc.conv2d_bwd_data, orc.conv2d_bwd_filter)
+    args = [(x, w), (dy, w), (x, dy)]
+    shapes = [(N, H, W, K), (N, H, W, C), (R, S, C, K)]
+
+    def dev(a, shift):
+        # a device copy starting `shift` floats into its buffer (shift 1: 4-byte aligned only)
+        buf = torch.empty(a.size + 4, dtype=torch.float32, device="cuda")
+        view = buf[shift:shift + a.size].view(*a.shape)
+        view.copy_(torch.from_numpy(a).cuda())
+        return view
+
     for which in range(3):
         nb = amd.amsim_conv2d_workspace_size(desc, which, lut)
-        assert nb >= 2 * 4 * N * H * W * min(C, K), f"pass {which}: no plane scratch requested"
-        for scratch in (True, False):
+        ref, sa = refs[which]("mitchell", 7, odesc, *args[which], np.arange(int(np.prod(shapes[which]))))
+        for shift, scratch in ((0, True), (0, False), (1, True)):
+            a0, a1 = dev(args[which][0], shift), dev(args[which][1], shift)
+            out = torch.empty(shapes[which], dtype=torch.float32, device="cuda")
             ws = amd.workspace(nb) if scratch else None
             torch.cuda.synchronize()
             n0 = amd.amsim_kernel_launches()
-            fns[which](desc, *args[which], outs[which], lut, ws=ws)
+            fns[which](desc, a0, a1, out, lut, ws=ws)
             torch.cuda.synchronize()
             path, launches = amd.amsim_last_path(), amd.amsim_kernel_launches() - n0
-            if scratch:
-                assert path & amd.AMSIM_PATH_PLANES and path & amd.AMSIM_PATH_CONV_BOXES, (which, path)
-                # the predecode pass and the GEMM (and the fixup kernel without a cooperative launch)
-                assert launches == (3 if path & amd.AMSIM_PATH_FIXUP else 2), (which, path, launches)
+            if shift == 0:
+                assert path & amd.AMSIM_PATH_RAW_TILES and path & amd.AMSIM_PATH_CONV_BOXES, (which, path)
+                assert launches == (2 if path & amd.AMSIM_PATH_FIXUP else 1), (which, path, launches)
             else:
-                assert path & amd.AMSIM_PATH_INKERNEL_DECODE and not path & amd.AMSIM_PATH_PLANES, (which, path)
-                assert launches == 1, (which, launches)
+                assert path & amd.AMSIM_PATH_INKERNEL_DECODE and not path & amd.AMSIM_PATH_CONV_BOXES, (which, path)
+            assert_close(out.cpu().numpy().reshape(-1), ref, sa, f"pass {which} shift {shift} scratch {scratch}")
