@@ -209,7 +209,7 @@ def lut_residency(lut):
 # ---------------------------------------------------------------- traffic record
 # sources of the LUT-GEMM kernels (the kernel the traffic records measure);
 # a record holds for one version of them
-KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_ws.cuh", "gemm_tma.cuh")
+KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_ws.cuh", "gemm_tma.cuh", "gemm_raw.cuh")
 
 
 def kernel_sha():
@@ -392,7 +392,8 @@ def main():
     roofline = {"bound": "alu", "pipe": "shared-memory LUT lookups: SMs x 32 per clock x SM clock",
                 "achieved": achieved, "peak": peak, "unit": "Glookup/s", "frac": achieved / peak,
                 "traffic": traffic,
-                "kernel": "LUT-GEMM calls: predecode + lutgemm_tma_kernel (lutgemm_ws_kernel for gathers)",
+                "kernel": "LUT-GEMM calls: lutgemm_raw_kernel, or predecode + lutgemm_tma_kernel "
+                          "(lutgemm_ws_kernel for gathers); see amsim_last_path",
                 "calls_per_step": launches_lut, "kernel_launches_per_step": launches_timed / K,
                 "lut_residency": lut_residency(step.lut),
                 "lut_share_of_step": round(lut_share, 4), "sms": sms,
