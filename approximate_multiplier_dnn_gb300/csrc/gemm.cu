@@ -305,15 +305,25 @@ bool raw_ok(const OperandDesc &d, int K, int batch, bool check_ptr)
     return true;
 }
 
+// Elements of operands the raw-tile kernel would read with plain loads above
+// which the launch prefers planes (plain loads serve small operands, such as
+// a 10-wide layer's, without a predecode launch).
+constexpr double kDirectElems = 256.0 * 1024;
+
+// Every operand dense; each either copy-engine-strided or, in total, small
+// enough for plain loads.
 bool all_raw_ok(const Problem *p, int n, const Plan &pl, bool check_ptr)
 {
+    double direct = 0.0;
     for (int i = 0; i < n; ++i) {
         if (pl.tiles[i] == 0) continue;
-        if (p[i].conv || !raw_ok(p[i].U, p[i].K, p[i].batch, check_ptr) ||
-            !raw_ok(p[i].L, p[i].K, p[i].batch, check_ptr))
-            return false;
+        if (p[i].conv || p[i].U.gather || p[i].L.gather || p[i].K <= 0) return false;
+        if (!raw_ok(p[i].U, p[i].K, p[i].batch, check_ptr))
+            direct += (double)p[i].U.rows * p[i].K * (p[i].U.batch_stride ? p[i].batch : 1);
+        if (!raw_ok(p[i].L, p[i].K, p[i].batch, check_ptr))
+            direct += (double)p[i].L.rows * p[i].K * (p[i].L.batch_stride ? p[i].batch : 1);
     }
-    return true;
+    return direct <= kDirectElems;
 }
 
 // 3-D map (rows or k innermost, then the other, then batch) over a raw operand.
@@ -486,9 +496,13 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
         } else {
             for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
                 if (pl.tiles[i] == 0) continue;
-                erc = encode_raw_map(&maps.u[qi], p[i].U, p[i].K, p[i].batch, BU);
-                if (erc == AMSIM_OK) erc = encode_raw_map(&maps.l[qi], p[i].L, p[i].K, p[i].batch, BL);
-                kern::ProbParams &q = tp.pr[qi++];
+                kern::ProbParams &q = tp.pr[qi];
+                q.u_direct = !raw_ok(p[i].U, p[i].K, p[i].batch, true);
+                q.l_direct = !raw_ok(p[i].L, p[i].K, p[i].batch, true);
+                if (q.u_direct || q.l_direct) tp.direct = 1;
+                if (!q.u_direct) erc = encode_raw_map(&maps.u[qi], p[i].U, p[i].K, p[i].batch, BU);
+                if (erc == AMSIM_OK && !q.l_direct) erc = encode_raw_map(&maps.l[qi], p[i].L, p[i].K, p[i].batch, BL);
+                ++qi;
                 q.u_kfast = p[i].U.s_row != 1;
                 q.l_kfast = p[i].L.s_row != 1;
                 q.u_bsel = (p[i].U.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;

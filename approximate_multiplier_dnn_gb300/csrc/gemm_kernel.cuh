@@ -92,6 +92,9 @@ struct ProbParams {
     // batch coordinate factor (0 when one plane serves every batch).
     const unsigned long long *u_big, *l_big;
     int u_bsel, l_bsel;
+    // Raw-tile kernel: the operand is read with plain loads by the decoders
+    // (strides the copy engine cannot take) instead of a tensor box.
+    int u_direct, l_direct;
 };
 
 // A launch: the (problem, tile, stage) iterations of all problems laid end to
@@ -115,6 +118,7 @@ struct KParams {
     // operands, 1 whole-row L boxes per filter tap, 2 blocked-channel L boxes
     // (see ConvRaw); cv_u_tap: U boxes addressed (step in tap, row, tap)
     int conv, cv_u_tap;
+    int direct;             // raw-tile kernel: some operand is read with plain loads
     int cv_ch, cv_S, cv_tiles_img, cv_rows_tile, cv_ybase, cv_ystep, cv_xbase, cv_xstep, cv_N, cv_P, cv_Q, cv_rows;
 };
 

@@ -165,6 +165,90 @@ __device__ __forceinline__ void conv_raw_boxes(const KParams &p, const TmaMaps &
     }
 }
 
+// Decode an R-row tile of an operand read with plain loads (rows row0 ..,
+// steps k0 .., batch b; zeros outside the operand) into off/scl [BK][R].
+// Lanes walk the operand's unit-stride dimension when it has one.
+// Operands whose strides the copy engine cannot take (a leading dimension that
+// is not a multiple of 4 elements, or a base address off a 16-byte boundary)
+// are read with plain loads.  Only the tile's in-range elements are loaded,
+// spread over all decoders so that each issues as few dependent loads as
+// possible; the rest of the tile is the decode of zero.
+struct DirectTile {
+    const float *base;
+    long long sr, sk;         // element strides of rows and steps
+    int vr, vk;               // in-range rows and steps of the tile
+    bool rows_fast;           // consecutive tasks walk rows (unit row stride, or neither stride unit)
+};
+
+__device__ __forceinline__ DirectTile direct_tile(const OperandDesc &od, int K, int b, int bsel, int row0, int k0,
+                                                  int R)
+{
+    DirectTile t;
+    t.sr = od.s_row;
+    t.sk = od.s_k;
+    t.base = od.ptr + (long long)b * bsel * od.batch_stride + (long long)row0 * t.sr + (long long)k0 * t.sk;
+    t.vr = max(0, min(R, od.rows - row0));
+    t.vk = max(0, min(BK, K - k0));
+    t.rows_fast = od.s_row == 1 || od.s_k != 1;
+    return t;
+}
+
+__device__ __forceinline__ void direct_task(const DirectTile &t, int task, int &rr, int &kk)
+{
+    if (t.rows_fast) {
+        kk = task / t.vr;
+        rr = task - kk * t.vr;
+    } else {
+        rr = task / t.vk;
+        kk = task - rr * t.vk;
+    }
+}
+
+// Pull a later stage's in-range elements toward L2 (no destination, no wait).
+template <int R>
+__device__ __forceinline__ void direct_prefetch(const OperandDesc &od, int K, int b, int bsel, int row0, int k0, int d)
+{
+    const DirectTile t = direct_tile(od, K, b, bsel, row0, k0, R);
+    const int n = t.vr * t.vk;
+#pragma unroll 1
+    for (int task = d; task < n; task += kRawDecoders) {
+        int rr, kk;
+        direct_task(t, task, rr, kk);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(t.base + rr * t.sr + kk * t.sk));
+    }
+}
+
+// Copy a tile of a plainly-read operand into its raw slot with asynchronous
+// 4-byte copies (every copy of the tile in flight at once; zero-filled out of
+// range), in the layout a tensor copy would have produced: [k][row] for an
+// operand with unit row stride, otherwise the swizzled [row][k] boxes.  The
+// caller waits for the copies and syncs the decoders before decoding.
+template <int R>
+__device__ __forceinline__ void direct_copy(const OperandDesc &od, int K, int b, int bsel, int row0, int k0,
+                                            uint8_t *raw, int d)
+{
+    const DirectTile t = direct_tile(od, K, b, bsel, row0, k0, R);
+    float *dst = reinterpret_cast<float *>(raw);
+    if (od.s_row == 1) {
+#pragma unroll 1
+        for (int task = d; task < R * BK; task += kRawDecoders) {
+            const int rr = task % R, kk = task / R;
+            const bool ok = rr < t.vr && kk < t.vk;
+            cp_async4(dst + kk * R + rr, ok ? t.base + rr + kk * t.sk : od.ptr, ok);
+        }
+    } else {
+#pragma unroll 1
+        for (int task = d; task < R * BK; task += kRawDecoders) {
+            const int kk = task % BK, rr = task / BK;
+            const bool ok = rr < t.vr && kk < t.vk;
+            float *e = reinterpret_cast<float *>(raw + rr * (BK * 4) + ((((kk >> 2) ^ ((rr >> 1) & 3))) << 4)) + (kk & 3);
+            cp_async4(e, ok ? t.base + rr * t.sr + kk * t.sk : od.ptr, ok);
+        }
+    }
+}
+
+__device__ __forceinline__ void decoder_bar() { asm volatile("bar.sync 3, %0;" ::"n"(kRawDecoders) : "memory"); }
+
 struct RawSmem {
     uint8_t *dec;          // kRawDec decoded stages of kTmaStageBytes
     uint8_t *raw;          // kRawRing raw stages of kRawStageBytes
@@ -189,17 +273,28 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
         const StagePos sp = stage_pos(p, it);
         const ProbParams &q = p.pr[sp.pi];
         uint8_t *st = sm.raw + (size_t)rs * kRawStageBytes;
-        mbar_expect_tx(&sm.raw_full[rs], kRawStageBytes);
         const int k0 = sp.kt * BK;
         if (p.conv) {
+            mbar_expect_tx(&sm.raw_full[rs], kRawStageBytes);
             conv_raw_boxes(p, maps, q, sp.u_tile0, sp.l_tile0, sp.kt, st, &sm.raw_full[rs]);
         } else {
-            if (q.u_kfast) tma_load_3d(st, &maps.u[sp.pi], k0, sp.u_tile0, sp.b * q.u_bsel, &sm.raw_full[rs]);
-            else tma_load_3d(st, &maps.u[sp.pi], sp.u_tile0, k0, sp.b * q.u_bsel, &sm.raw_full[rs]);
-            if (q.l_kfast)
+            // operands read with plain loads contribute no copy bytes (an all-plain
+            // stage is a bare arrival)
+            const uint32_t bytes = (q.u_direct ? 0 : kRawUBytes) + (q.l_direct ? 0 : kRawLBytes);
+            if (bytes) mbar_expect_tx(&sm.raw_full[rs], bytes);
+            else mbar_arrive(&sm.raw_full[rs]);
+            if (q.u_direct) {
+            } else if (q.u_kfast) {
+                tma_load_3d(st, &maps.u[sp.pi], k0, sp.u_tile0, sp.b * q.u_bsel, &sm.raw_full[rs]);
+            } else {
+                tma_load_3d(st, &maps.u[sp.pi], sp.u_tile0, k0, sp.b * q.u_bsel, &sm.raw_full[rs]);
+            }
+            if (q.l_direct) {
+            } else if (q.l_kfast) {
                 tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], k0, sp.l_tile0, sp.b * q.l_bsel, &sm.raw_full[rs]);
-            else
+            } else {
                 tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], sp.l_tile0, k0, sp.b * q.l_bsel, &sm.raw_full[rs]);
+            }
         }
         ++issued;
     };
@@ -216,8 +311,16 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
         const uint8_t *raw = sm.raw + (size_t)rs * kRawStageBytes;
         uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
         int big = 0;
-        raw_decode<BU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st), reinterpret_cast<float *>(st + BK * BU * 4),
-                       p.M, offU, d, big);
+        if (q.u_direct || q.l_direct) {
+            uint8_t *rw = sm.raw + (size_t)rs * kRawStageBytes;
+            if (q.u_direct) direct_copy<BU>(q.U, q.K, sp.b, q.u_bsel, sp.u_tile0, sp.kt * BK, rw, d);
+            if (q.l_direct) direct_copy<BL>(q.L, q.K, sp.b, q.l_bsel, sp.l_tile0, sp.kt * BK, rw + kRawUBytes, d);
+            cp_async_commit();
+            cp_async_wait<0>();
+            decoder_bar();          // every decoder's copies have landed
+        }
+        raw_decode<BU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st),
+                       reinterpret_cast<float *>(st + BK * BU * 4), p.M, offU, d, big);
         if (p.conv == 2)
             raw_decode_blocks(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                               reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
@@ -228,6 +331,12 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
         const int any = __any_sync(0xFFFFFFFFu, big);
         if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;
         mbar_arrive(&sm.full[ds]);
+        if (p.direct && it + kRawRing < it1) {
+            const StagePos np = stage_pos(p, it + kRawRing);
+            const ProbParams &nq = p.pr[np.pi];
+            if (nq.u_direct) direct_prefetch<BU>(nq.U, nq.K, np.b, nq.u_bsel, np.u_tile0, np.kt * BK, d);
+            if (nq.l_direct) direct_prefetch<BL>(nq.L, nq.K, np.b, nq.l_bsel, np.l_tile0, np.kt * BK, d);
+        }
     }
     if (d == 0 && aborted) {
         // copies issued into raw slots nobody waited for may still be landing

@@ -75,11 +75,13 @@ class MLPStep:
     """3-layer MLP (784-1000-500-10, batch 256): forward Y_l = X_l W_l, then
     for every layer dX_l = dY_l W_l^T and dW_l = X_l^T dY_l (pure linear
     layers; X_{l+1} = Y_l; dY_l synthetic per layer).  The nine GEMMs run as
-    three grouped calls ordered by their data dependences: {Y1, dX1, dW1},
-    then {Y2, dX2}, then {Y3, dW3, dW2, dX3} (dW2 needs only Y1).  The four
-    GEMMs of the 10-wide layer (leading dimension 10, not a multiple of 4
-    elements) share the last call, the one whose operands go through planes;
-    the first two copy their operand tiles in place."""
+    three grouped calls ordered by their data dependences: {Y1, dX1, dX2},
+    then {Y2, dW1, dW2} (dW2 needs Y1), then {Y3, dW3, dX3} (both need Y2).
+    The first two calls carry about the same work; the three small GEMMs of
+    the 10-wide layer share the last one, so that their one-stage tiles do
+    not lengthen the large calls.  Every call copies its operand tiles in
+    place (the 10-wide operands, whose leading dimension is not a multiple of
+    4 elements, with plain asynchronous loads)."""
 
     def __init__(self, data: dict, lut, device="cuda"):
         import torch
@@ -107,9 +109,9 @@ class MLPStep:
             self.dX.append(dX)
             self.dW.append(dW)
         self.calls = fwd + [c for pair in zip(dxc, dwc) for c in pair]
-        self.groups = [("fwd1+dX1+dW1", GemmGroup([fwd[0], dxc[0], dwc[0]])),
-                       ("fwd2+dX2", GemmGroup([fwd[1], dxc[1]])),
-                       ("fwd3+dW3+dW2+dX3", GemmGroup([fwd[2], dwc[2], dwc[1], dxc[2]]))]
+        self.groups = [("fwd1+dX1+dX2", GemmGroup([fwd[0], dxc[0], dxc[1]])),
+                       ("fwd2+dW1+dW2", GemmGroup([fwd[1], dwc[0], dwc[1]])),
+                       ("fwd3+dW3+dX3", GemmGroup([fwd[2], dwc[2], dxc[2]]))]
         self.ws = workspace(max(g.ws_bytes(lut) for _, g in self.groups), device)
 
     @property

@@ -251,7 +251,11 @@ def _path_ws(amd, lut, path, tA, tB, m, n, k, batch=1):
     return None
 
 
-PATH_SHAPES = [(33, 65, 129), (257, 10, 500), (300, 500, 2000), (65, 257, 17), (2, 3, 5000)]
+PATH_SHAPES = [(33, 65, 129), (257, 10, 500), (300, 500, 2000), (65, 257, 17), (2, 3, 5000), (513, 600, 999)]
+
+# elements of unaligned operands the raw-tile kernel loads plainly (above it a
+# launch uses planes or the in-kernel decode)
+DIRECT_ELEMS = 256 * 1024
 
 
 @pytest.mark.parametrize("path", ["planes", "in_kernel", "none"])
@@ -264,8 +268,9 @@ def test_each_kernel_path(amd, orc, luts, shape, path):
     got = gpu_gemm(amd, lut, A, B, False, True, ws=_path_ws(amd, lut, path, "N", "T", m, n, k))
     taken = amd.amsim_last_path()
     # operands with copy-engine strides (k a multiple of 4 here) are copied in
-    # place and decoded in shared memory on any scratch; others need planes
-    raw = k % 4 == 0
+    # place and decoded in shared memory on any scratch, and so are small
+    # unaligned ones (loaded plainly); larger unaligned ones need planes
+    raw = k % 4 == 0 or (m + n) * k <= DIRECT_ELEMS
     if raw:
         assert taken & amd.AMSIM_PATH_RAW_TILES, taken
     elif path == "planes":
@@ -298,8 +303,8 @@ def test_special_operands_each_path(amd, orc, luts, path):
 @pytest.mark.parametrize("k", [150, 152])
 @pytest.mark.parametrize("path", ["planes", "none"])
 def test_batched_broadcast_operand(amd, orc, luts, path, k):
-    """strideB = 0: one B serves every batch (one plane, or one copied tensor
-    for k = 152, for all batches)."""
+    """strideB = 0: one B serves every batch (one plane, one copied tensor for
+    k = 152, or plain loads of one tensor for k = 150, for all batches)."""
     import torch
     rng = np.random.default_rng(14)
     batch, m, n = 5, 70, 90
@@ -373,11 +378,65 @@ def test_raw_tile_path_special_operands(amd, orc, luts):
         check(orc, kind, 7, A, B, False, False, got, what=f"raw specials {kind}")
 
 
-def test_unaligned_leading_dimension_takes_planes(amd, orc, luts):
-    """A leading dimension that is not a multiple of 4 elements cannot be copied
-    in place: with scratch the operands go through planes instead."""
+@pytest.mark.parametrize("ta", [False, True])
+@pytest.mark.parametrize("tb", [False, True])
+@pytest.mark.parametrize("shape", [(70, 90, 129), (64, 10, 500), (10, 256, 1000), (33, 7, 3)])
+def test_unaligned_small_operands_load_plainly(amd, orc, luts, shape, ta, tb):
+    """Small operands whose leading dimension is not a multiple of 4 elements
+    (a 10-wide layer) are read by the raw-tile kernel with plain loads, alone
+    or beside an operand copied in place, with no predecode launch."""
+    m, n, k = shape
+    rng = np.random.default_rng(19 * m + 3 * n + k + 2 * ta + tb)
+    A = rnd(rng, (k, m) if ta else (m, k))
+    B = rnd(rng, (n, k) if tb else (k, n))
+    for kind in ("mitchell", "exact"):
+        got = gpu_gemm(amd, luts(kind, 7), A, B, ta, tb)
+        taken = amd.amsim_last_path()
+        assert taken & amd.AMSIM_PATH_RAW_TILES and not taken & amd.AMSIM_PATH_PLANES, taken
+        check(orc, kind, 7, A, B, ta, tb, got, what=f"plain loads {shape} {ta}{tb} {kind}")
+
+
+def test_unaligned_special_operands_load_plainly(amd, orc, luts):
+    """Zeros, denormals, infinities, NaNs and |x| >= 2^64 through the plain
+    loads of the raw-tile kernel."""
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    rng = np.random.default_rng(20)
+    a, b = wl.special_values_mix(70 * 130 + 130 * 90, seed=21)
+    A = a[:70 * 130].reshape(70, 130).copy()
+    B = b[70 * 130:70 * 130 + 130 * 90].reshape(130, 90).copy()
+    A[:, :] = np.where(rng.random(A.shape) < 0.93, rng.standard_normal(A.shape), A).astype(np.float32)
+    B[:, :] = np.where(rng.random(B.shape) < 0.93, rng.standard_normal(B.shape), B).astype(np.float32)
+    for kind in ("mitchell", "exact"):
+        got = gpu_gemm(amd, luts(kind, 7), A, B, False, False)
+        assert amd.amsim_last_path() & amd.AMSIM_PATH_RAW_TILES
+        check(orc, kind, 7, A, B, False, False, got, what=f"plain-load specials {kind}")
+
+
+def test_misaligned_base_address_loads_plainly(amd, orc, luts):
+    """An operand with a leading dimension that is a multiple of 4 elements
+    but a base address off a 16-byte boundary is read with plain loads; the
+    other operand is still copied in place."""
+    import torch
+    rng = np.random.default_rng(22)
+    m, n, k = 96, 80, 200
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    lut = luts("mitchell", 7)
+    store = torch.zeros(m * k + 1, dtype=torch.float32, device="cuda")
+    dA = store[1:].view(m, k)
+    dA.copy_(to_dev(A))
+    buf, C = guarded((m, n))
+    amd.amsim_gemm("N", "N", m, n, k, 1.0, dA, k, to_dev(B), n, 0.0, C, n, lut)
+    torch.cuda.synchronize()
+    assert guards_intact(buf)
+    assert amd.amsim_last_path() & amd.AMSIM_PATH_RAW_TILES, amd.amsim_last_path()
+    check(orc, "mitchell", 7, A, B, False, False, C.cpu().numpy(), what="misaligned base")
+
+
+def test_unaligned_large_operands_take_planes(amd, orc, luts):
+    """Larger operands whose leading dimension is not a multiple of 4 elements
+    cannot be copied in place: with scratch they go through planes instead."""
     rng = np.random.default_rng(18)
-    A, B = rnd(rng, (70, 129)), rnd(rng, (129, 90))
+    A, B = rnd(rng, (600, 999)), rnd(rng, (999, 700))
     lut = luts("mitchell", 7)
     got = gpu_gemm(amd, lut, A, B, False, False)
     taken = amd.amsim_last_path()
