@@ -99,6 +99,10 @@ def lib():
         "amsim_gemm_grouped": ([i32, ctypes.POINTER(GemmProblem), vp, vp, sz, vp], i32),
         "amsim_gemm_noalloc": ([ch, ch, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp, vp], i32),
         "amsim_gemm_grouped_workspace_size": ([i32, ctypes.POINTER(GemmProblem), vp], sz),
+        "amsim_gemm_phased": ([i32, ctypes.POINTER(GemmProblem), i32, ctypes.POINTER(i32), ctypes.POINTER(i32), vp,
+                               vp, sz, vp], i32),
+        "amsim_gemm_phased_workspace_size": ([i32, ctypes.POINTER(GemmProblem), i32, ctypes.POINTER(i32),
+                                              ctypes.POINTER(i32), vp], sz),
         "amsim_conv2d_out_hw": ([ctypes.POINTER(ConvDesc), ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "amsim_conv2d_fwd": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
         "amsim_conv2d_bwd_data": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
@@ -130,6 +134,7 @@ AMSIM_PATH_STREAMK = 16
 AMSIM_PATH_FIXUP = 32
 AMSIM_PATH_CONV_BOXES = 64
 AMSIM_PATH_RAW_TILES = 128
+AMSIM_PATH_PHASED = 256
 
 
 def amsim_last_path() -> int:
@@ -317,6 +322,30 @@ def amsim_gemm_grouped(problems, lut, ws=None, ws_bytes=None, stream=None):
     ws_bytes = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check("amsim_gemm_grouped", lib().amsim_gemm_grouped(len(arr), arr, _h(lut), _ptr(ws), ws_bytes,
                                                           _stream(stream)))
+
+
+def _phase_arrays(phase_first, phase_after):
+    n = len(phase_first)
+    if len(phase_after) != n:
+        raise ValueError("phase_first and phase_after differ in length")
+    return n, (ctypes.c_int32 * n)(*phase_first), (ctypes.c_int32 * n)(*phase_after)
+
+
+def amsim_gemm_phased(problems, phase_first, phase_after, lut, ws=None, ws_bytes=None, stream=None):
+    """Ordered phases of GEMMs (sequences of GemmProblem): phase ph is
+    problems[phase_first[ph]:phase_first[ph + 1]] and reads outputs of phases
+    before phase_after[ph] only."""
+    arr = _problem_array(problems)
+    nph, first, after = _phase_arrays(phase_first, phase_after)
+    ws_bytes = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("amsim_gemm_phased", lib().amsim_gemm_phased(len(arr), arr, nph, first, after, _h(lut), _ptr(ws),
+                                                        ws_bytes, _stream(stream)))
+
+
+def amsim_gemm_phased_workspace_size(problems, phase_first, phase_after, lut) -> int:
+    arr = _problem_array(problems)
+    nph, first, after = _phase_arrays(phase_first, phase_after)
+    return int(lib().amsim_gemm_phased_workspace_size(len(arr), arr, nph, first, after, _h(lut)))
 
 
 def amsim_gemm_grouped_workspace_size(problems, lut) -> int:

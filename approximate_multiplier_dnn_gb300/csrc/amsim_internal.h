@@ -100,6 +100,10 @@ size_t problem_workspace(const Problem &p, amsim_lut_t lut);
 // Up to ten independent problems in one launch (one LUT for all).
 int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream);
 size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut);
+// Ordered phases of problems in one launch (see amsim_gemm_phased); n <= kMaxProblems.
+int run_phased(const Problem *p, int n, int nphase, const int *first, const int *after, amsim_lut_t lut, void *ws,
+               size_t ws_bytes, cudaStream_t stream);
+size_t phased_workspace(const Problem *p, int n, int nphase, const int *first, amsim_lut_t lut);
 // The part of the above that the stream-K schedule alone needs.
 size_t problems_workspace_streamk(const Problem *p, int n, amsim_lut_t lut);
 // Workspace of a (batched) GEMM call: the fastest plan's, or the stream-K part only.

@@ -374,7 +374,7 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     size_t need = pl.ws_bytes;
     PlaneSet rps;
     const int rwlog = lut ? (lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2) : 0;
-    if (lut && encode_tiled() && all_raw_ok(p, n, pl, false) &&
+    if (lut && encode_tiled() && pl.iters < 0x7FFFFFFFLL && all_raw_ok(p, n, pl, false) &&
         !(plan_planes(p, n, pl, lut->M, rwlog, &rps) && rps.n > 0 && planes_bytes_per_mac(p, n, pl, rps) < 0.01)) {
         // operand tiles are copied in place and decoded inside the GEMM
     } else if (lut && encode_tiled() && n == 1 && p[0].conv) {
@@ -399,26 +399,9 @@ size_t problem_workspace(const Problem &p, amsim_lut_t lut) { return problems_wo
 
 namespace {
 
-// One launch for problems that all read the same LUT orientation.
-int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
+// Launch parameters of the problems that have tiles (in launch order).
+void fill_params(const Problem *p, int n, const Plan &pl, amsim_lut_t lut, kern::KParams &kp)
 {
-    if (n <= 0) return AMSIM_OK;
-    if (n > kern::kMaxProblems) return AMSIM_EINVAL;
-    const int sms = device_sms(lut->device);
-    // scratch that breaks the 256-byte alignment rule is not used
-    if (reinterpret_cast<uintptr_t>(ws) & 255) ws = nullptr;
-    const Plan pl = make_plan(p, n, sms, ws ? ws_bytes : 0);
-    if (pl.total_tiles == 0) return AMSIM_OK;
-
-    // Shared-memory LUT when it fits beside the warp-specialised kernel's
-    // rings; else beside the single-role kernel's stages; else read from global.
-    const size_t lut_smem = kern::lut_region_bytes((int)lut->narrow_bytes);
-    bool use_ws = true, gl = false;
-    if (lut->narrow_bytes > (size_t)kMaxSmemLut) gl = true;
-    else if ((size_t)kern::kWsFixedSmem + lut_smem <= (size_t)kMaxSmemPerCta) gl = false;
-    else if ((size_t)kern::kFixedSmem + lut_smem <= (size_t)kMaxSmemPerCta) use_ws = false;
-    else gl = true;
-    kern::KParams kp = {};
     int np = 0;
     for (int i = 0; i < n; ++i) {
         if (pl.tiles[i] == 0) continue;
@@ -446,9 +429,63 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     kp.streamk = pl.streamk ? 1 : 0;
     kp.iters = pl.iters;
     kp.ctas = pl.ctas;
-    kp.table_bytes = gl ? 0 : (int)lut->narrow_bytes;
     kp.M = lut->M;
     kp.wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
+}
+
+// Raw-tile operands of dense problems: a tensor map per copy-engine-strided
+// operand, plain loads for the rest.
+int encode_raw_problems(const Problem *p, int n, const Plan &pl, kern::KParams &tp, kern::TmaMaps &maps)
+{
+    int erc = AMSIM_OK;
+    for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
+        if (pl.tiles[i] == 0) continue;
+        kern::ProbParams &q = tp.pr[qi];
+        q.u_direct = !raw_ok(p[i].U, p[i].K, p[i].batch, true);
+        q.l_direct = !raw_ok(p[i].L, p[i].K, p[i].batch, true);
+        if (q.u_direct || q.l_direct) tp.direct = 1;
+        if (!q.u_direct) erc = encode_raw_map(&maps.u[qi], p[i].U, p[i].K, p[i].batch, BU);
+        if (erc == AMSIM_OK && !q.l_direct) erc = encode_raw_map(&maps.l[qi], p[i].L, p[i].K, p[i].batch, BL);
+        ++qi;
+        q.u_kfast = p[i].U.s_row != 1;
+        q.l_kfast = p[i].L.s_row != 1;
+        q.u_bsel = (p[i].U.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
+        q.l_bsel = (p[i].L.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
+    }
+    return erc;
+}
+
+// Shared memory of the raw-tile kernel and whether its LUT is read from global.
+size_t raw_smem(amsim_lut_t lut, bool *gl)
+{
+    bool raw_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
+    if (!raw_gl && kern::raw_smem_bytes((int)lut->narrow_bytes) > kMaxSmemPerCta) raw_gl = true;
+    *gl = raw_gl;
+    return (size_t)kern::raw_smem_bytes(raw_gl ? 0 : (int)lut->narrow_bytes);
+}
+
+// One launch for problems that all read the same LUT orientation.
+int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (n <= 0) return AMSIM_OK;
+    if (n > kern::kMaxProblems) return AMSIM_EINVAL;
+    const int sms = device_sms(lut->device);
+    // scratch that breaks the 256-byte alignment rule is not used
+    if (reinterpret_cast<uintptr_t>(ws) & 255) ws = nullptr;
+    const Plan pl = make_plan(p, n, sms, ws ? ws_bytes : 0);
+    if (pl.total_tiles == 0) return AMSIM_OK;
+
+    // Shared-memory LUT when it fits beside the warp-specialised kernel's
+    // rings; else beside the single-role kernel's stages; else read from global.
+    const size_t lut_smem = kern::lut_region_bytes((int)lut->narrow_bytes);
+    bool use_ws = true, gl = false;
+    if (lut->narrow_bytes > (size_t)kMaxSmemLut) gl = true;
+    else if ((size_t)kern::kWsFixedSmem + lut_smem <= (size_t)kMaxSmemPerCta) gl = false;
+    else if ((size_t)kern::kFixedSmem + lut_smem <= (size_t)kMaxSmemPerCta) use_ws = false;
+    else gl = true;
+    kern::KParams kp = {};
+    fill_params(p, n, pl, lut, kp);
+    kp.table_bytes = gl ? 0 : (int)lut->narrow_bytes;
     kp.ws = static_cast<float *>(ws);
 
     const long long blocks = pl.streamk ? pl.ctas : pl.total_tiles;
@@ -463,12 +500,14 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     PlaneSet ps;
     const bool planes_fit = ws && encode_tiled() && plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 &&
                             ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps);
-    const bool conv_raw = n == 1 && p[0].conv && pl.tiles[0] > 0 && encode_tiled();
-    if (conv_raw || (encode_tiled() && all_raw_ok(p, n, pl, true) &&
+    // (the raw-tile kernel counts a launch's iterations in 32 bits)
+    const bool raw_fits = pl.iters < 0x7FFFFFFFLL;
+    const bool conv_raw = raw_fits && n == 1 && p[0].conv && pl.tiles[0] > 0 && encode_tiled();
+    if (conv_raw || (raw_fits && encode_tiled() && all_raw_ok(p, n, pl, true) &&
                      !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01))) {
-        bool raw_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
-        if (!raw_gl && kern::raw_smem_bytes((int)lut->narrow_bytes) > kMaxSmemPerCta) raw_gl = true;
-        kern::TmaMaps maps;
+        bool raw_gl = false;
+        const size_t smem = raw_smem(lut, &raw_gl);
+        kern::TmaMaps maps = {};
         kern::KParams tp = kp;
         int erc = AMSIM_OK;
         if (conv_raw) {
@@ -494,26 +533,12 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             tp.cv_Q = cv.Q;
             tp.cv_rows = cv.rows;
         } else {
-            for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
-                if (pl.tiles[i] == 0) continue;
-                kern::ProbParams &q = tp.pr[qi];
-                q.u_direct = !raw_ok(p[i].U, p[i].K, p[i].batch, true);
-                q.l_direct = !raw_ok(p[i].L, p[i].K, p[i].batch, true);
-                if (q.u_direct || q.l_direct) tp.direct = 1;
-                if (!q.u_direct) erc = encode_raw_map(&maps.u[qi], p[i].U, p[i].K, p[i].batch, BU);
-                if (erc == AMSIM_OK && !q.l_direct) erc = encode_raw_map(&maps.l[qi], p[i].L, p[i].K, p[i].batch, BL);
-                ++qi;
-                q.u_kfast = p[i].U.s_row != 1;
-                q.l_kfast = p[i].L.s_row != 1;
-                q.u_bsel = (p[i].U.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
-                q.l_bsel = (p[i].L.batch_stride != 0 && p[i].batch > 1) ? 1 : 0;
-            }
+            erc = encode_raw_problems(p, n, pl, tp, maps);
         }
         if (erc == AMSIM_OK) {
             tp.table_bytes = raw_gl ? 0 : (int)lut->narrow_bytes;
             tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
             tp.fused = pl.streamk ? 1 : 0;
-            const size_t smem = (size_t)kern::raw_smem_bytes(tp.table_bytes);
             const dim3 grid((unsigned)blocks);
             int rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
             if (rc == kern::AMSIM_ENOTCOOP) {
@@ -576,7 +601,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
         }
         dp.njobs = ps.n;
         dp.tiles = dtiles;
-        kern::TmaMaps maps;
+        kern::TmaMaps maps = {};
         int erc = AMSIM_OK;
         for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
             if (pl.tiles[i] == 0) continue;
@@ -651,6 +676,115 @@ int run_problems(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws_b
 int run_problem(const Problem &p, amsim_lut_t lut, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     return run_problems(&p, 1, lut, ws, ws_bytes, stream);
+}
+
+namespace {
+
+// Scratch of a phased launch: per phase and CTA a completion flag and a flag
+// for the stored last part of a cut tile (the other parts are added in C).
+size_t phased_sk_bytes(int nphase, int G)
+{
+    return (size_t)2 * nphase * G * sizeof(unsigned long long);
+}
+
+// Problems [first[ph], first[ph + 1]) of phase ph (the last ends at n).
+void phase_bounds(const int *first, int nphase, int n, int ph, int *lo, int *hi)
+{
+    *lo = first[ph];
+    *hi = ph + 1 < nphase ? first[ph + 1] : n;
+}
+
+// One launch can run all phases: dense operands for the raw-tile kernel,
+// one LUT orientation, at most kMaxPhases phases and kMaxProblems problems.
+bool phased_ok(const Problem *p, int n, int nphase, const Plan &pl, amsim_lut_t lut, bool check_ptr)
+{
+    if (nphase < 2 || nphase > kern::kMaxPhases || n > kern::kMaxProblems || pl.ctas < 2) return false;
+    if (pl.iters >= 0x7FFFFFFFLL) return false;     // the raw-tile kernel counts iterations in 32 bits
+    if (!encode_tiled()) return false;
+    bool gl = false;
+    raw_smem(lut, &gl);
+    if (gl) return false;                           // phased launches stage the LUT in shared memory
+    for (int i = 1; i < n; ++i)
+        if (!lut->symmetric && p[i].u_is_first != p[0].u_is_first) return false;
+    return all_raw_ok(p, n, pl, check_ptr);
+}
+
+}  // namespace
+
+int run_phased(const Problem *p, int n, int nphase, const int *first, const int *after, amsim_lut_t lut, void *ws,
+               size_t ws_bytes, cudaStream_t stream)
+{
+    g_last_path = 0;
+    if (n <= 0) return AMSIM_OK;
+    if (reinterpret_cast<uintptr_t>(ws) & 255) ws = nullptr;
+    const int sms = device_sms(lut->device);
+    Plan pl = make_plan(p, std::min(n, kern::kMaxProblems), sms, (size_t)-1);
+    if (pl.total_tiles == 0 && n <= kern::kMaxProblems) return AMSIM_OK;
+    if (ws && phased_ok(p, n, nphase, pl, lut, true) && ws_bytes >= phased_sk_bytes(nphase, pl.ctas)) {
+        pl.streamk = true;
+        kern::KParams tp = {};
+        fill_params(p, n, pl, lut, tp);
+        bool gl = false;
+        const size_t smem = raw_smem(lut, &gl);
+        tp.table_bytes = gl ? 0 : (int)lut->narrow_bytes;
+        tp.ws = static_cast<float *>(ws);
+        tp.nphase = nphase;
+        for (int ph = 0; ph < nphase; ++ph) {
+            int lo, hi;
+            phase_bounds(first, nphase, n, ph, &lo, &hi);
+            tp.ph_iter0[ph] = lo < n ? pl.iter0[lo] : pl.iters;
+            tp.ph_after[ph] = after[ph];
+        }
+        tp.ph_iter0[nphase] = pl.iters;
+        // every CTA with a share of a phase gets at least one iteration of it
+        // (a reduction waits for every CTA whose share starts inside a tile)
+        for (int ph = 0; ph < nphase; ++ph) {
+            const long long w = tp.ph_iter0[ph + 1] - tp.ph_iter0[ph];
+            tp.ph_split[ph] = w >= 2LL * pl.ctas ? kern::kSplitBalanced : w >= pl.ctas ? kern::kSplitEven
+                                                                                       : kern::kSplitLeading;
+        }
+        kern::TmaMaps maps = {};
+        int rc = encode_raw_problems(p, n, pl, tp, maps);
+        if (rc == AMSIM_OK) {
+            tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
+            tp.fused = 1;
+            rc = launch_raw(lut->width_bits, tp, maps, gl, dim3((unsigned)pl.ctas), smem, stream);
+            if (rc == AMSIM_OK) {
+                g_last_path = AMSIM_PATH_RAW_TILES | AMSIM_PATH_STREAMK | AMSIM_PATH_PHASED;
+                return AMSIM_OK;
+            }
+            if (rc != kern::AMSIM_ENOTCOOP && rc != AMSIM_EUNSUPPORTED) return rc;
+        }
+    }
+    // one grouped launch (or more) per phase, in order on the stream
+    int path = 0;
+    for (int ph = 0; ph < nphase; ++ph) {
+        int lo, hi;
+        phase_bounds(first, nphase, n, ph, &lo, &hi);
+        for (int base = lo; base < hi; base += kern::kMaxProblems) {
+            const int rc = run_problems(p + base, std::min(hi - base, kern::kMaxProblems), lut, ws, ws_bytes, stream);
+            path |= g_last_path;
+            if (rc) return rc;
+        }
+    }
+    g_last_path = path;
+    return AMSIM_OK;
+}
+
+size_t phased_workspace(const Problem *p, int n, int nphase, const int *first, amsim_lut_t lut)
+{
+    size_t best = 0;
+    for (int ph = 0; ph < nphase; ++ph) {
+        int lo, hi;
+        phase_bounds(first, nphase, n, ph, &lo, &hi);
+        for (int base = lo; base < hi; base += kern::kMaxProblems)
+            best = std::max(best, problems_workspace(p + base, std::min(hi - base, kern::kMaxProblems), lut));
+    }
+    if (n <= kern::kMaxProblems) {
+        const Plan pl = make_plan(p, n, device_sms(lut->device), (size_t)-1);
+        if (phased_ok(p, n, nphase, pl, lut, false)) best = std::max(best, phased_sk_bytes(nphase, pl.ctas));
+    }
+    return best;
 }
 
 }  // namespace amsim
@@ -794,6 +928,67 @@ int amsim_gemm_grouped(int count, const amsim_gemm_problem *problems, amsim_lut_
         if (rc) return rc;
     }
     return AMSIM_OK;
+}
+
+namespace {
+
+// Phases of a phased call: phase_first[0] == 0, non-decreasing, within
+// [0, count]; phase_after[ph] in [0, ph].
+bool phases_valid(int count, int nphase, const int *phase_first, const int *phase_after)
+{
+    if (nphase < 1 || !phase_first || !phase_after || phase_first[0] != 0) return false;
+    for (int ph = 0; ph < nphase; ++ph) {
+        if (phase_first[ph] < 0 || phase_first[ph] > count) return false;
+        if (ph > 0 && phase_first[ph] < phase_first[ph - 1]) return false;
+        if (phase_after[ph] < 0 || phase_after[ph] > ph) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+int amsim_gemm_phased(int count, const amsim_gemm_problem *problems, int nphase, const int *phase_first,
+                      const int *phase_after, amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream)
+{
+    int rc = amsim::check_lut(lut);
+    if (rc) return rc;
+    if (count < 0 || (count > 0 && !problems)) return AMSIM_EINVAL;
+    if (!phases_valid(count, nphase, phase_first, phase_after)) return AMSIM_EINVAL;
+    Problem pr[amsim::kern::kMaxProblems];
+    for (int i = 0; i < count; ++i) {           // validate everything before enqueuing anything
+        rc = grouped_build(&problems[i], &pr[0]);
+        if (rc) return rc;
+    }
+    if (count <= amsim::kern::kMaxProblems) {
+        for (int i = 0; i < count; ++i) grouped_build(&problems[i], &pr[i]);
+        return amsim::run_phased(pr, count, nphase, phase_first, phase_after, lut, ws, ws_bytes,
+                                 static_cast<cudaStream_t>(stream));
+    }
+    // more problems than one launch holds: the phases one after another
+    for (int ph = 0; ph < nphase; ++ph) {
+        const int lo = phase_first[ph], hi = ph + 1 < nphase ? phase_first[ph + 1] : count;
+        rc = amsim_gemm_grouped(hi - lo, problems + lo, lut, ws, ws_bytes, stream);
+        if (rc) return rc;
+    }
+    return AMSIM_OK;
+}
+
+size_t amsim_gemm_phased_workspace_size(int count, const amsim_gemm_problem *problems, int nphase,
+                                        const int *phase_first, const int *phase_after, amsim_lut_t lut)
+{
+    if (!lut || count <= 0 || !problems || !phases_valid(count, nphase, phase_first, phase_after)) return 0;
+    if (count > amsim::kern::kMaxProblems) {
+        size_t best = 0;
+        for (int ph = 0; ph < nphase; ++ph) {
+            const int lo = phase_first[ph], hi = ph + 1 < nphase ? phase_first[ph + 1] : count;
+            if (hi > lo) best = std::max(best, amsim_gemm_grouped_workspace_size(hi - lo, problems + lo, lut));
+        }
+        return best;
+    }
+    Problem pr[amsim::kern::kMaxProblems];
+    for (int i = 0; i < count; ++i)
+        if (grouped_build(&problems[i], &pr[i])) return 0;
+    return amsim::phased_workspace(pr, count, nphase, phase_first, lut);
 }
 
 size_t amsim_gemm_grouped_workspace_size(int count, const amsim_gemm_problem *problems, amsim_lut_t lut)

@@ -36,7 +36,7 @@ constexpr int kRawDec = 3;                              // decoded stages
 constexpr int kRawBarBytes = 256;                       // barriers and big-operand flags
 static_assert(kRawUBytes % 1024 == 0 && kRawLBytes % 1024 == 0, "swizzled boxes start 1024-byte aligned");
 static_assert(BL % 64 == 0 && (BL / 64) * BK * 64 * 4 == kRawLBytes, "blocked L boxes fill the L stage");
-static_assert((2 * kRawRing + 2 * kRawDec) * 8 + kRawDec * (kRawDecoders / 32) * 4 <= kRawBarBytes, "barrier block");
+static_assert((2 * kRawRing + 2 * kRawDec + 1) * 8 + kRawDec * (kRawDecoders / 32) * 4 <= kRawBarBytes, "barrier block");
 static_assert(kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes >= (BU * BL + 1024 * 4) * 4,
               "the rings hold the stream-K reduction buffer");
 
@@ -392,11 +392,311 @@ __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lu
                      2 * kRawDec, aborted);
 }
 
-// All problems of a launch read the same LUT orientation (staged once).
-template <int W, bool GL>
+// Scratch of a phased launch: completion flags [phase][cta], then flags
+// [phase][cta] raised once the CTA has stored the last part of the cut tile
+// its share starts in.
+__device__ __forceinline__ unsigned long long *phase_done(const KParams &p)
+{
+    return reinterpret_cast<unsigned long long *>(p.ws);
+}
+
+__device__ __forceinline__ unsigned long long *phase_stored(const KParams &p)
+{
+    return phase_done(p) + (long long)n_phases(p) * p.ctas;
+}
+
+// This CTA's launch iterations in order: its share of every phase (or, data
+// parallel, its one tile).  `it` runs through [it, end) of phase `ph`, then
+// moves to the next phase with a non-empty share.
+struct IterCursor {
+    int ph;
+    int it, end;               // the raw-tile kernel runs launches of fewer than 2^31 iterations
+};
+
+__device__ __forceinline__ void cursor_settle(const KParams &p, IterCursor &c)
+{
+    const int nph = n_phases(p);
+    while (c.it >= c.end && c.ph + 1 < nph) {
+        ++c.ph;
+        c.it = (int)ph_begin(p, c.ph, blockIdx.x);
+        c.end = (int)ph_begin(p, c.ph, blockIdx.x + 1);
+    }
+}
+
+__device__ __forceinline__ IterCursor cursor_start(const KParams &p)
+{
+    IterCursor c;
+    c.ph = 0;
+    if (p.streamk) {
+        c.it = (int)ph_begin(p, 0, blockIdx.x);
+        c.end = (int)ph_begin(p, 0, blockIdx.x + 1);
+        cursor_settle(p, c);
+    } else {
+        long long it, end;
+        cta_range(p, it, end);
+        c.it = (int)it;
+        c.end = (int)end;
+    }
+    return c;
+}
+
+__device__ __forceinline__ void cursor_next(const KParams &p, IterCursor &c)
+{
+    ++c.it;
+    cursor_settle(p, c);
+}
+
+// Before the first copy of a phase that reads earlier phases' outputs: every
+// decoder waits for a part of the completion flags of phases 0 .. nreq - 1
+// (one per CTA and phase), then they sync, so that the copies issued or made
+// after this see those outputs.
+__device__ __forceinline__ void wait_phases(const KParams &p, int nreq, int d, bool &aborted)
+{
+    const unsigned long long *done = phase_done(p);
+    for (int i = d; i < nreq * p.ctas; i += kRawDecoders) flag_wait(done + i, p.epoch, aborted);
+    decoder_bar();
+}
+
+// The producer warpgroup of a phased launch: thread 0 also issues the copies;
+// every decoder tracks the issue position, so that they can wait for a
+// phase's inputs together.
+__device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaMaps &maps, const RawSmem &sm)
+{
+    const int d = threadIdx.x - kTmaConsumerThreads;
+    const int lane = d & 31, dw = d >> 5;
+    const int offU = p.M + p.wlog, offL = p.wlog;
+    IterCursor cur = cursor_start(p), iss = cur;
+    bool aborted = false;
+    int issued = 0, gi = 0;    // stages copied, stages passed by the issue position
+    int waited_ph = 0;          // phases up to this one have had their inputs awaited
+    auto issue = [&]() {
+        if (p.nphase > 1 && iss.ph > waited_ph) {
+            waited_ph = iss.ph;
+            if (p.ph_after[iss.ph] > 0) {
+                wait_phases(p, p.ph_after[iss.ph], d, aborted);
+                // outputs written through the generic proxy, read by tensor copies
+                if (d == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+        }
+        const int it = iss.it;
+        const int g = gi++;
+        cursor_next(p, iss);
+        if (d != 0 || aborted) return;
+        const int rs = g % kRawRing;
+        if (!mbar_wait(&sm.raw_empty[rs], (uint32_t)(((g / kRawRing) & 1) ^ 1), aborted)) return;
+        const StagePos sp = stage_pos(p, it);
+        const ProbParams &q = p.pr[sp.pi];
+        uint8_t *st = sm.raw + (size_t)rs * kRawStageBytes;
+        const int k0 = sp.kt * BK;
+        if (p.conv) {
+            mbar_expect_tx(&sm.raw_full[rs], kRawStageBytes);
+            conv_raw_boxes(p, maps, q, sp.u_tile0, sp.l_tile0, sp.kt, st, &sm.raw_full[rs]);
+        } else {
+            // operands read with plain loads contribute no copy bytes (an all-plain
+            // stage is a bare arrival)
+            const uint32_t bytes = (q.u_direct ? 0 : kRawUBytes) + (q.l_direct ? 0 : kRawLBytes);
+            if (bytes) mbar_expect_tx(&sm.raw_full[rs], bytes);
+            else mbar_arrive(&sm.raw_full[rs]);
+            if (q.u_direct) {
+            } else if (q.u_kfast) {
+                tma_load_3d(st, &maps.u[sp.pi], k0, sp.u_tile0, sp.b * q.u_bsel, &sm.raw_full[rs]);
+            } else {
+                tma_load_3d(st, &maps.u[sp.pi], sp.u_tile0, k0, sp.b * q.u_bsel, &sm.raw_full[rs]);
+            }
+            if (q.l_direct) {
+            } else if (q.l_kfast) {
+                tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], k0, sp.l_tile0, sp.b * q.l_bsel, &sm.raw_full[rs]);
+            } else {
+                tma_load_3d(st + kRawUBytes, &maps.l[sp.pi], sp.l_tile0, k0, sp.b * q.l_bsel, &sm.raw_full[rs]);
+            }
+        }
+        ++issued;
+    };
+    // Copies run up to kRawRing stages ahead of the decode, except into a
+    // phase that reads earlier phases: its first copy waits until every
+    // earlier stage of this CTA is decoded, so that the wait for other CTAs
+    // never holds back this CTA's own part of the phases it waits for.
+    auto may_issue = [&](int g) {
+        if (iss.it >= iss.end || gi >= g + kRawRing) return false;
+        return !(iss.ph > waited_ph && cur.ph < iss.ph && p.ph_after[iss.ph] > 0);
+    };
+    for (int g = 0; cur.it < cur.end; cursor_next(p, cur), ++g) {
+        while (may_issue(g)) issue();
+        const int rs = g % kRawRing, ds = g % kRawDec;
+        mbar_wait(&sm.raw_full[rs], (uint32_t)((g / kRawRing) & 1), aborted);
+        mbar_wait(&sm.empty[ds], (uint32_t)(((g / kRawDec) & 1) ^ 1), aborted);
+        const StagePos sp = stage_pos(p, cur.it);
+        const ProbParams &q = p.pr[sp.pi];
+        const uint8_t *raw = sm.raw + (size_t)rs * kRawStageBytes;
+        uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
+        int big = 0;
+        if (q.u_direct || q.l_direct) {
+            uint8_t *rw = sm.raw + (size_t)rs * kRawStageBytes;
+            if (q.u_direct) direct_copy<BU>(q.U, q.K, sp.b, q.u_bsel, sp.u_tile0, sp.kt * BK, rw, d);
+            if (q.l_direct) direct_copy<BL>(q.L, q.K, sp.b, q.l_bsel, sp.l_tile0, sp.kt * BK, rw + kRawUBytes, d);
+            cp_async_commit();
+            cp_async_wait<0>();
+            decoder_bar();          // every decoder's copies have landed
+        }
+        raw_decode<BU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st),
+                       reinterpret_cast<float *>(st + BK * BU * 4), p.M, offU, d, big);
+        if (p.conv == 2)
+            raw_decode_blocks(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+                              reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
+        else
+            raw_decode<BL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+                           reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
+        mbar_arrive(&sm.raw_empty[rs]);
+        const int any = __any_sync(0xFFFFFFFFu, big);
+        if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;
+        mbar_arrive(&sm.full[ds]);
+        // the tile after the issue position is the next to be copied: pull its
+        // plainly-read operands toward L2 (its phase's inputs may not be ready
+        // yet; a prefetch only warms the cache)
+        if (p.direct && iss.it < iss.end) {
+            const StagePos np = stage_pos(p, iss.it);
+            const ProbParams &nq = p.pr[np.pi];
+            if (nq.u_direct) direct_prefetch<BU>(nq.U, nq.K, np.b, nq.u_bsel, np.u_tile0, np.kt * BK, d);
+            if (nq.l_direct) direct_prefetch<BL>(nq.L, nq.K, np.b, nq.l_bsel, np.l_tile0, np.kt * BK, d);
+        }
+    }
+    if (d == 0 && aborted) {
+        // copies issued into raw slots nobody waited for may still be landing
+        bool gave_up = false;
+        const int n = issued < kRawRing ? issued : kRawRing;
+        for (int j = issued - n; j < issued; ++j)
+            mbar_wait(&sm.raw_full[j % kRawRing], (uint32_t)((j / kRawRing) & 1), gave_up);
+    }
+}
+
+// Vector and scalar reductions into global memory (the sum lands in L2).
+__device__ __forceinline__ void red_add4(float *dst, float4 v)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void red_add1(float *dst, float v)
+{
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(v) : "memory");
+}
+
+// Add alpha * acc of one consumer's block into C (a cut tile of a phased
+// launch, after its last part has been stored).
+__device__ __forceinline__ void add_tile(const ProbParams &q, const float2 (&acc)[TM / 2][TN], int b, int u0, int l0)
+{
+    const int nU = q.U.rows, nL = q.L.rows;
+    float *C = q.c_ptr + (long long)b * q.c_bs;
+    const float alpha = q.alpha;
+    const bool vec_l = (reinterpret_cast<uintptr_t>(C) & 15) == 0 && q.c_sl == 1 && (q.c_su & 3) == 0;
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int u = u0 + i;
+        if (u >= nU) break;
+        if (vec_l && l0 + TN <= nL) {
+#pragma unroll
+            for (int t4 = 0; t4 < TN / 4; ++t4) {
+                const float4 a = acc4(acc, i, 4 * t4);
+                red_add4(C + (long long)u * q.c_su + l0 + 4 * t4,
+                         make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w));
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < TN; ++t) {
+                const int l = l0 + t;
+                if (l >= nL) break;
+                red_add1(C + (long long)u * q.c_su + (long long)l * q.c_sl, alpha * accv(acc, i, t));
+            }
+        }
+    }
+}
+
+// Wait until the CTA whose share of phase ph holds iteration `it` (the last
+// stage of a cut tile) has stored its part of the tile.
+static __device__ __noinline__ void wait_stored(const KParams &p, int ph, long long it, bool &aborted)
+{
+    int c = blockIdx.x;
+    while (c + 1 < p.ctas && ph_begin(p, ph, c + 1) <= it) ++c;
+    flag_wait(phase_stored(p) + (long long)ph * p.ctas + c, p.epoch, aborted);
+}
+
+// The consumers of a phased launch (LUT in shared memory).  A tile that the
+// share boundaries cut is summed in C: the CTA whose share holds the tile's
+// last stages -- the first to finish its part, at the start of its share --
+// stores alpha * part + beta * C and raises a flag; every other part is added
+// with floating-point reductions after a check of that flag (normally long
+// raised), so that no CTA waits for the others at a phase's end.  The
+// summation order of cut tiles therefore varies from run to run.
+template <int W>
+__device__ __forceinline__ void raw_consumer_phased(const KParams &p, const uint8_t *lut, const RawSmem &sm)
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int wu = warp / WL, wl = warp % WL;
+    const int urow = wu * TM;
+    const int lcol = wl * 32 * TN + lane * TN;
+    uint32_t g = 0;
+    bool aborted = false;
+    const int nph = n_phases(p);
+    for (int ph = 0; ph < nph; ++ph) {
+        const long long it0 = ph_begin(p, ph, blockIdx.x), it1 = ph_begin(p, ph, blockIdx.x + 1);
+        walk_segments(p, it0, it1,
+                      [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool) {
+            float2 acc[TM / 2][TN];
+#pragma unroll
+            for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+            const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + wl * 32 * TN >= q.L.rows;
+            for (int kt = s0; kt < s1; ++kt, ++g) {
+                const int ds = g % kRawDec;
+                mbar_wait(&sm.full[ds], (g / kRawDec) & 1, aborted);
+                if (!idle) {
+                    const uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
+                    const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
+                    const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
+                    const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
+                    const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
+                    int any_big = 0;
+#pragma unroll
+                    for (int w = 0; w < kRawDecoders / 32; ++w) any_big |= sm.flags[ds * (kRawDecoders / 32) + w];
+                    if (any_big)
+                        compute_stage<W, false, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                    else
+                        compute_stage<W, false, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                }
+                mbar_arrive(&sm.empty[ds]);
+            }
+            if (s1 == q.kt_total) {
+                // a whole tile, or the last part of a cut one (this share's first segment)
+                store_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
+                if (s0 > 0) {
+                    consumer_bar();
+                    if (tid == 0) flag_store(phase_stored(p) + (long long)ph * p.ctas + blockIdx.x, p.epoch);
+                }
+            } else {
+                const long long tend = q.iter0 + ((long long)b * q.tiles_u * q.tiles_l +
+                                                  (long long)(u_tile0 / BU) * q.tiles_l + l_tile0 / BL + 1) *
+                                                     q.kt_total;
+                wait_stored(p, ph, tend - 1, aborted);
+                add_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
+            }
+        });
+        // every consumer's stores and reductions of the phase precede the flag
+        consumer_bar();
+        if (tid == 0) flag_store(phase_done(p) + (long long)ph * p.ctas + blockIdx.x, p.epoch);
+    }
+}
+
+// All problems of a launch read the same LUT orientation (staged once).  PH:
+// a phased launch (its own instance, so that plain launches keep the lean
+// single-range loops; the LUT is then in shared memory).
+template <int W, bool GL, bool PH>
 __global__ void __launch_bounds__(kRawThreads, 1)
     lutgemm_raw_kernel(const __grid_constant__ KParams p, const __grid_constant__ TmaMaps maps)
 {
+    static_assert(!(PH && GL), "phased launches stage the LUT in shared memory");
     extern __shared__ __align__(128) uint8_t smem_raw[];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
@@ -434,8 +734,9 @@ __global__ void __launch_bounds__(kRawThreads, 1)
     }
     if (tid == kTmaConsumerThreads) {
         for (int i = 0; i < p.nprob; ++i) {
-            tma_prefetch_map(&maps.u[i]);
-            tma_prefetch_map(&maps.l[i]);
+            // operands read with plain loads have no tensor map
+            if (!p.pr[i].u_direct) tma_prefetch_map(&maps.u[i]);
+            if (!p.pr[i].l_direct) tma_prefetch_map(&maps.l[i]);
         }
     }
     __syncthreads();
@@ -446,14 +747,16 @@ __global__ void __launch_bounds__(kRawThreads, 1)
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
     if (tid >= kTmaConsumerThreads) {
         if constexpr (kTmaProducerWarps == 4) reg_dealloc<kTmaProducerRegs>();
-        raw_producer(p, maps, sm);
+        if constexpr (PH) raw_producer_phased(p, maps, sm);
+        else raw_producer(p, maps, sm);
     } else {
         if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
-        raw_consumer<W, GL>(p, lut, sm, kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes);
+        if constexpr (PH) raw_consumer_phased<W>(p, lut, sm);
+        else raw_consumer<W, GL>(p, lut, sm, kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes);
     }
 }
 
-template <int W, bool GL>
+template <int W, bool GL, bool PH = false>
 int launch_raw_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t smem, cudaStream_t st)
 {
     static int checked[64] = {};   // 0 unknown, 1 usable, -1 register split not satisfiable
@@ -462,13 +765,13 @@ int launch_raw_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t
     if (dev >= 64) return AMSIM_EUNSUPPORTED;
     if (checked[dev] == 0) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, lutgemm_raw_kernel<W, GL>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, lutgemm_raw_kernel<W, GL, PH>);
         if (e != cudaSuccess) return cuda_status(e);
         if (kTmaProducerWarps == 4 &&
             fa.numRegs * kRawThreads < kTmaConsumerThreads * kTmaConsumerRegs + 128 * kTmaProducerRegs) {
             checked[dev] = -1;
         } else {
-            e = cudaFuncSetAttribute(lutgemm_raw_kernel<W, GL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(lutgemm_raw_kernel<W, GL, PH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kMaxSmemPerCta);
             if (e != cudaSuccess) return cuda_status(e);
             checked[dev] = 1;
@@ -495,7 +798,7 @@ int launch_raw_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t
         }
         cfg.attrs = attrs;
         cfg.numAttrs = na;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, lutgemm_raw_kernel<W, GL>, p, maps);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, lutgemm_raw_kernel<W, GL, PH>, p, maps);
         if (e == cudaSuccess) {
             count_launch();
             return AMSIM_OK;

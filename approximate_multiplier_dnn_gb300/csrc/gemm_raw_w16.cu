@@ -6,6 +6,7 @@ namespace kern {
 
 int launch_raw_w16(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st)
 {
+    if (p.nphase > 1) return gl ? AMSIM_EUNSUPPORTED : launch_raw_instance<16, false, true>(p, maps, grid, smem, st);
     return gl ? launch_raw_instance<16, true>(p, maps, grid, smem, st)
               : launch_raw_instance<16, false>(p, maps, grid, smem, st);
 }

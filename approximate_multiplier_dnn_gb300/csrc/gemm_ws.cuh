@@ -160,21 +160,11 @@ __device__ __forceinline__ float *st_Lscl(const WsSmem &s, int slot)
     return reinterpret_cast<float *>(s.stage + slot * kStageBytes + 2 * BK * UST * 4 + BK * LST * 4);
 }
 
-// Segment walk shared by both roles: calls f(q, b, u_tile0, l_tile0, s0, s1, first).
+// Segment walk of launch iterations [it, it_end): calls
+// f(q, b, u_tile0, l_tile0, s0, s1, first) per tile segment.
 template <typename F>
-__device__ __forceinline__ void for_each_segment(const KParams &p, F &&f)
+__device__ __forceinline__ void walk_segments(const KParams &p, long long it, long long it_end, F &&f)
 {
-    long long it, it_end;
-    if (p.streamk) {
-        it = sk_begin(p.iters, p.ctas, blockIdx.x);
-        it_end = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
-    } else {
-        long long t = blockIdx.x;
-        int pi = 0;
-        while (pi + 1 < p.nprob && t >= p.pr[pi].tiles) t -= p.pr[pi++].tiles;
-        it = p.pr[pi].iter0 + t * p.pr[pi].kt_total;
-        it_end = it + p.pr[pi].kt_total;
-    }
     bool first = true;
     while (it < it_end) {
         int pi = 0;
@@ -192,6 +182,24 @@ __device__ __forceinline__ void for_each_segment(const KParams &p, F &&f)
         first = false;
         it += s1 - s0;
     }
+}
+
+// Segment walk of this CTA's iterations, shared by both roles.
+template <typename F>
+__device__ __forceinline__ void for_each_segment(const KParams &p, F &&f)
+{
+    long long it, it_end;
+    if (p.streamk) {
+        it = sk_begin(p.iters, p.ctas, blockIdx.x);
+        it_end = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
+    } else {
+        long long t = blockIdx.x;
+        int pi = 0;
+        while (pi + 1 < p.nprob && t >= p.pr[pi].tiles) t -= p.pr[pi++].tiles;
+        it = p.pr[pi].iter0 + t * p.pr[pi].kt_total;
+        it_end = it + p.pr[pi].kt_total;
+    }
+    walk_segments(p, it, it_end, f);
 }
 
 // ------------------------------------------------------------------ producer

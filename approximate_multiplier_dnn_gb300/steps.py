@@ -12,7 +12,8 @@ from __future__ import annotations
 
 from . import (ConvDesc, GemmProblem, amsim_mul, amsim_conv2d_bwd_data, amsim_conv2d_bwd_filter, amsim_conv2d_fwd,
                amsim_conv2d_out_hw, amsim_conv2d_workspace_size, amsim_gemm, amsim_gemm_grouped,
-               amsim_gemm_grouped_workspace_size, amsim_gemm_strided_batched, amsim_gemm_workspace_size,
+               amsim_gemm_grouped_workspace_size, amsim_gemm_phased, amsim_gemm_phased_workspace_size,
+               amsim_gemm_strided_batched, amsim_gemm_workspace_size,
                amsim_softmax_rows, workspace)
 
 
@@ -71,17 +72,41 @@ class GemmGroup:
         amsim_gemm_grouped(self.arr, lut, ws=ws, stream=stream)
 
 
+class PhasedGemms:
+    """Ordered phases of GEMMs issued as one phased call: phase i reads
+    outputs of phases before after[i] only."""
+
+    def __init__(self, phases):
+        self.names = [nm for nm, _, _ in phases]
+        self.calls = [c for _, cl, _ in phases for c in cl]
+        self.first, n = [], 0
+        for _, cl, _ in phases:
+            self.first.append(n)
+            n += len(cl)
+        self.after = [a for _, _, a in phases]
+        self.arr = (GemmProblem * len(self.calls))(*[c.problem() for c in self.calls])
+
+    @property
+    def macs(self) -> int:
+        return sum(c.macs for c in self.calls)
+
+    def ws_bytes(self, lut) -> int:
+        return amsim_gemm_phased_workspace_size(self.arr, self.first, self.after, lut)
+
+    def __call__(self, lut, ws, stream=None):
+        amsim_gemm_phased(self.arr, self.first, self.after, lut, ws=ws, stream=stream)
+
+
 class MLPStep:
     """3-layer MLP (784-1000-500-10, batch 256): forward Y_l = X_l W_l, then
     for every layer dX_l = dY_l W_l^T and dW_l = X_l^T dY_l (pure linear
     layers; X_{l+1} = Y_l; dY_l synthetic per layer).  The nine GEMMs run as
-    three grouped calls ordered by their data dependences: {Y1, dX1, dX2},
-    then {Y2, dW1, dW2} (dW2 needs Y1), then {Y3, dW3, dX3} (both need Y2).
-    The first two calls carry about the same work; the three small GEMMs of
-    the 10-wide layer share the last one, so that their one-stage tiles do
-    not lengthen the large calls.  Every call copies its operand tiles in
-    place (the 10-wide operands, whose leading dimension is not a multiple of
-    4 elements, with plain asynchronous loads)."""
+    one phased call (one launch) whose three phases follow the data
+    dependences and carry about the same work in the first two:
+    {Y1, dX1, dX2}, then {Y2, dW1, dW2} (Y2 and dW2 read Y1), then
+    {Y3, dW3, dX3} (Y3 and dW3 read Y2).  Every phase copies its operand tiles
+    in place (the 10-wide operands, whose leading dimension is not a multiple
+    of 4 elements, with plain asynchronous loads)."""
 
     def __init__(self, data: dict, lut, device="cuda"):
         import torch
@@ -109,10 +134,11 @@ class MLPStep:
             self.dX.append(dX)
             self.dW.append(dW)
         self.calls = fwd + [c for pair in zip(dxc, dwc) for c in pair]
-        self.groups = [("fwd1+dX1+dX2", GemmGroup([fwd[0], dxc[0], dxc[1]])),
-                       ("fwd2+dW1+dW2", GemmGroup([fwd[1], dwc[0], dwc[1]])),
-                       ("fwd3+dW3+dX3", GemmGroup([fwd[2], dwc[2], dxc[2]]))]
-        self.ws = workspace(max(g.ws_bytes(lut) for _, g in self.groups), device)
+        # (name, calls, number of leading phases that must be complete first)
+        self.phased = PhasedGemms([("fwd1+dX1+dX2", [fwd[0], dxc[0], dxc[1]], 0),
+                                   ("fwd2+dW1+dW2", [fwd[1], dwc[0], dwc[1]], 1),
+                                   ("fwd3+dW3+dX3", [fwd[2], dwc[2], dxc[2]], 2)])
+        self.ws = workspace(self.phased.ws_bytes(lut), device)
 
     @property
     def macs(self) -> int:
@@ -123,12 +149,10 @@ class MLPStep:
 
     def parts(self, stream=None):
         """(name, zero-argument launcher, approximate MACs, kernel launches) per ABI call."""
-        return [(nm, (lambda g=g: g(self.lut, self.ws, stream)), g.macs, 1 + (g.ws_bytes(self.lut) > 0))
-                for nm, g in self.groups]
+        return [("+".join(self.phased.names), lambda: self.phased(self.lut, self.ws, stream), self.phased.macs, 1)]
 
     def run(self, stream=None):
-        for _, g in self.groups:
-            g(self.lut, self.ws, stream)
+        self.phased(self.lut, self.ws, stream)
 
 
 class ConvStep:

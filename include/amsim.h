@@ -82,7 +82,8 @@ enum amsim_path {
     AMSIM_PATH_STREAMK = 16,        /* reduction split across CTAs (stream-K) */
     AMSIM_PATH_FIXUP = 32,          /* cut tiles finished by the separate fixup kernel */
     AMSIM_PATH_CONV_BOXES = 64,     /* convolution operands as shifted or blocked tensor boxes */
-    AMSIM_PATH_RAW_TILES = 128      /* operand tiles copied in place by TMA, decoded in shared memory */
+    AMSIM_PATH_RAW_TILES = 128,     /* operand tiles copied in place by TMA, decoded in shared memory */
+    AMSIM_PATH_PHASED = 256         /* every phase of amsim_gemm_phased in one launch */
 };
 int amsim_last_path(void);
 
@@ -218,6 +219,43 @@ int amsim_gemm_grouped(int count, const amsim_gemm_problem *problems, amsim_lut_
 
 /* Bytes of scratch with which amsim_gemm_grouped runs its fastest plan. */
 size_t amsim_gemm_grouped_workspace_size(int count, const amsim_gemm_problem *problems, amsim_lut_t lut);
+
+/*
+ * Ordered phases of GEMMs sharing one LUT -- for example the forward and
+ * backward contractions of a stack of Dense layers (Sec. VI-C), where a
+ * layer's forward GEMM reads the previous layer's output.  Problems
+ * problems[phase_first[ph]] .. problems[phase_first[ph + 1] - 1] form phase ph
+ * (the last phase ends at `count`); phase_first[0] == 0 and phase_first is
+ * non-decreasing (a phase may be empty).  The result equals that of
+ * amsim_gemm_grouped called on each phase in turn on `stream`, up to fp32
+ * summation order, provided that:
+ *   - phase ph reads (as A or B) outputs of phases 0 .. phase_after[ph] - 1
+ *     only, 0 <= phase_after[ph] <= ph;
+ *   - no problem's C is read or written by any other problem of the call
+ *     except as just allowed (in particular, C with beta != 0 is not another
+ *     problem's output);
+ *   - within a phase, the rules of amsim_gemm_grouped hold.
+ * Phases that need nothing of the phase just before them let the SMs carry
+ * straight on from one phase to the next: with up to ten problems, six
+ * phases, operands the raw-tile path reads, one LUT orientation, a LUT that
+ * fits shared memory and at least amsim_gemm_phased_workspace_size bytes of
+ * 256-byte-aligned scratch, every phase runs in one cooperative launch
+ * (AMSIM_PATH_PHASED): each SM takes a share of every phase in order and
+ * waits, before it loads a phase's operands, until every SM has finished
+ * phases 0 .. phase_after[ph] - 1.  Tiles that the shares cut are summed in C
+ * with floating-point reductions, so their last bits may differ from run to
+ * run (within the contraction tolerance).  Otherwise the phases run as
+ * consecutive grouped launches.  Host arrays are read during the call.
+ * Errors: AMSIM_EINVAL for an invalid phase layout or problem, as
+ * amsim_gemm_grouped otherwise.
+ */
+int amsim_gemm_phased(int count, const amsim_gemm_problem *problems, int nphase, const int *phase_first,
+                      const int *phase_after, amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);
+
+/* Bytes of scratch with which amsim_gemm_phased runs its fastest plan (0 for
+ * an invalid phase layout). */
+size_t amsim_gemm_phased_workspace_size(int count, const amsim_gemm_problem *problems, int nphase,
+                                        const int *phase_first, const int *phase_after, amsim_lut_t lut);
 
 /*
  * amsim_gemm without a workspace argument and without any allocation: for
