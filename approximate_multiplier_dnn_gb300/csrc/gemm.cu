@@ -351,12 +351,12 @@ int encode_raw_map(CUtensorMap *map, const OperandDesc &d, int K, int batch, int
 }
 
 int launch_raw(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
-               cudaStream_t st)
+               cudaStream_t st, const kern::PhaseTable *pt = nullptr)
 {
     switch (width) {
-    case 8: return kern::launch_raw_w8(kp, maps, gl, grid, smem, st);
-    case 16: return kern::launch_raw_w16(kp, maps, gl, grid, smem, st);
-    default: return kern::launch_raw_w32(kp, maps, gl, grid, smem, st);
+    case 8: return kern::launch_raw_w8(kp, maps, pt, gl, grid, smem, st);
+    case 16: return kern::launch_raw_w16(kp, maps, pt, gl, grid, smem, st);
+    default: return kern::launch_raw_w32(kp, maps, pt, gl, grid, smem, st);
     }
 }
 
@@ -699,6 +699,7 @@ void phase_bounds(const int *first, int nphase, int n, int ph, int *lo, int *hi)
 bool phased_ok(const Problem *p, int n, int nphase, const Plan &pl, amsim_lut_t lut, bool check_ptr)
 {
     if (nphase < 2 || nphase > kern::kMaxPhases || n > kern::kMaxProblems || pl.ctas < 2) return false;
+    if (pl.ctas > kern::kMaxPhasedCtas) return false;
     if (pl.iters >= 0x7FFFFFFFLL) return false;     // the raw-tile kernel counts iterations in 32 bits
     if (!encode_tiled()) return false;
     bool gl = false;
@@ -707,6 +708,55 @@ bool phased_ok(const Problem *p, int n, int nphase, const Plan &pl, amsim_lut_t 
     for (int i = 1; i < n; ++i)
         if (!lut->symmetric && p[i].u_is_first != p[0].u_is_first) return false;
     return all_raw_ok(p, n, pl, check_ptr);
+}
+
+// Relative time of one stage of a tile: consumer warps whose rows or columns
+// all lie past the operands' edges skip their lookups, and such stages run
+// faster (measured on GB300: a tile with a quarter of its warps busy takes
+// about 0.73 of a full stage), so shares are cut by this cost, not by count.
+double stage_cost(const Problem &p, int ut, int lt)
+{
+    constexpr int WUn = BU / kern::TM, WLn = BL / (32 * kern::TN);
+    int busy = 0;
+    for (int wu = 0; wu < WUn; ++wu)
+        for (int wl = 0; wl < WLn; ++wl)
+            busy += (ut * BU + wu * kern::TM < p.U.rows && lt * BL + wl * 32 * kern::TN < p.L.rows) ? 1 : 0;
+    return 0.64 + 0.36 * busy / (WUn * WLn);
+}
+
+// Share boundaries of one phase: CTA c's share starts where the phase's
+// cumulative stage cost reaches c / G of its total (rounded to a stage).
+void phase_bounds_by_cost(const Problem *p, const Plan &pl, int lo, int hi, int G, int *bound)
+{
+    double total = 0.0;
+    for (int i = lo; i < hi; ++i) {
+        if (pl.tiles[i] == 0) continue;
+        for (int ut = 0; ut < pl.tiles_u[i]; ++ut)
+            for (int lt = 0; lt < pl.tiles_l[i]; ++lt)
+                total += (double)p[i].batch * pl.kt[i] * stage_cost(p[i], ut, lt);
+    }
+    long long it = 0;
+    double cum = 0.0;
+    int c = 1;
+    bound[0] = 0;
+    for (int i = lo; i < hi && c < G; ++i) {
+        if (pl.tiles[i] == 0) continue;
+        for (int b = 0; b < p[i].batch && c < G; ++b)
+            for (int ut = 0; ut < pl.tiles_u[i] && c < G; ++ut)
+                for (int lt = 0; lt < pl.tiles_l[i] && c < G; ++lt) {
+                    const double w = stage_cost(p[i], ut, lt), tc = w * pl.kt[i];
+                    while (c < G && cum + tc >= total * c / G) {
+                        const long long k = std::llround((total * c / G - cum) / w);
+                        bound[c++] = (int)(it + std::min<long long>(std::max<long long>(k, 0), pl.kt[i]));
+                    }
+                    cum += tc;
+                    it += pl.kt[i];
+                }
+    }
+    long long w_all = 0;
+    for (int i = lo; i < hi; ++i) w_all += pl.tiles[i] * pl.kt[i];
+    while (c <= G) bound[c++] = (int)w_all;
+    for (int k = 1; k <= G; ++k) bound[k] = std::min(std::max(bound[k], bound[k - 1]), (int)w_all);
 }
 
 }  // namespace
@@ -736,19 +786,18 @@ int run_phased(const Problem *p, int n, int nphase, const int *first, const int 
             tp.ph_after[ph] = after[ph];
         }
         tp.ph_iter0[nphase] = pl.iters;
-        // every CTA with a share of a phase gets at least one iteration of it
-        // (a reduction waits for every CTA whose share starts inside a tile)
+        kern::PhaseTable pt;
         for (int ph = 0; ph < nphase; ++ph) {
-            const long long w = tp.ph_iter0[ph + 1] - tp.ph_iter0[ph];
-            tp.ph_split[ph] = w >= 2LL * pl.ctas ? kern::kSplitBalanced : w >= pl.ctas ? kern::kSplitEven
-                                                                                       : kern::kSplitLeading;
+            int lo, hi;
+            phase_bounds(first, nphase, n, ph, &lo, &hi);
+            phase_bounds_by_cost(p, pl, lo, hi, pl.ctas, pt.bound[ph]);
         }
         kern::TmaMaps maps = {};
         int rc = encode_raw_problems(p, n, pl, tp, maps);
         if (rc == AMSIM_OK) {
             tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
             tp.fused = 1;
-            rc = launch_raw(lut->width_bits, tp, maps, gl, dim3((unsigned)pl.ctas), smem, stream);
+            rc = launch_raw(lut->width_bits, tp, maps, gl, dim3((unsigned)pl.ctas), smem, stream, &pt);
             if (rc == AMSIM_OK) {
                 g_last_path = AMSIM_PATH_RAW_TILES | AMSIM_PATH_STREAMK | AMSIM_PATH_PHASED;
                 return AMSIM_OK;

@@ -75,11 +75,7 @@ struct RowInfo {
 constexpr int kMaxProblems = 10;     // contractions fused into one launch
 constexpr int kMaxFixupParts = 1024;  // stream-K CTAs per launch (at most one per SM)
 constexpr int kMaxPhases = 6;        // ordered phases of one launch (raw-tile kernel)
-// How a phase's iterations are shared among the CTAs; every CTA with a share
-// gets at least one iteration, so that no empty share lies inside a tile.
-constexpr int kSplitEven = 0;        // W * c / G (W >= G)
-constexpr int kSplitBalanced = 1;    // from the running total over the phases so far (W >= 2 G)
-constexpr int kSplitLeading = 2;     // one iteration to each of the first W CTAs (W < G)
+constexpr int kMaxPhasedCtas = 160;  // CTAs of a phased launch
 
 // One contraction of a launch (see Problem in amsim_internal.h).
 struct ProbParams {
@@ -127,14 +123,12 @@ struct KParams {
     int direct;             // raw-tile kernel: some operand is read with plain loads
     // Phases (raw-tile kernel, fused stream-K): phase ph holds launch
     // iterations [ph_iter0[ph], ph_iter0[ph + 1]) -- whole problems; every CTA
-    // takes a share of every phase, in phase order, and loads nothing of
-    // phase ph before phases 0 .. ph_after[ph] - 1 are complete on every CTA.
-    // ph_split[ph] says how the phase is shared (see ph_begin).  nphase 0 or
-    // 1: one phase of p.iters iterations, split evenly.
+    // takes a share of every phase (PhaseTable), in phase order, and loads
+    // nothing of phase ph before phases 0 .. ph_after[ph] - 1 are complete on
+    // every CTA.  nphase 0 or 1: an ordinary launch.
     int nphase;
     long long ph_iter0[kMaxPhases + 1];
     int ph_after[kMaxPhases];
-    int ph_split[kMaxPhases];
     int cv_ch, cv_S, cv_tiles_img, cv_rows_tile, cv_ybase, cv_ystep, cv_xbase, cv_xstep, cv_N, cv_P, cv_Q, cv_rows;
 };
 
@@ -593,22 +587,12 @@ __device__ __forceinline__ long long sk_begin(long long W, int G, int c) { retur
 
 __device__ __forceinline__ int n_phases(const KParams &p) { return p.nphase > 1 ? p.nphase : 1; }
 
-// First launch iteration of stream-K CTA c's share of phase ph (c = ctas: the
-// phase's end).  Balanced phases take the CTA boundaries of the running total
-// through this phase minus those through the previous one, so that per-CTA
-// totals stay within one iteration of each other however many phases there
-// are; each share then differs from W / G by less than 2, so W >= 2 G keeps
-// every share non-empty.
-__device__ __forceinline__ long long ph_begin(const KParams &p, int ph, int c)
-{
-    if (p.nphase <= 1) return sk_begin(p.iters, p.ctas, c);
-    const long long a = p.ph_iter0[ph], b = p.ph_iter0[ph + 1];
-    switch (p.ph_split[ph]) {
-    case kSplitBalanced: return a + (b * c / p.ctas - a * c / p.ctas);
-    case kSplitLeading: return a + min((long long)c, b - a);
-    default: return a + (b - a) * c / p.ctas;
-    }
-}
+// Share boundaries of a phased launch: CTA c takes iterations
+// [bound[ph][c], bound[ph][c + 1]) of phase ph, counted from the phase's first
+// iteration (computed by the host from a cost model of the phase's tiles).
+struct PhaseTable {
+    int bound[kMaxPhases][kMaxPhasedCtas + 1];
+};
 
 template <int W, bool GL>
 __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ KParams p)

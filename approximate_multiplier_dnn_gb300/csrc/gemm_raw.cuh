@@ -405,45 +405,44 @@ __device__ __forceinline__ unsigned long long *phase_stored(const KParams &p)
     return phase_done(p) + (long long)n_phases(p) * p.ctas;
 }
 
-// This CTA's launch iterations in order: its share of every phase (or, data
-// parallel, its one tile).  `it` runs through [it, end) of phase `ph`, then
-// moves to the next phase with a non-empty share.
+// First launch iteration of CTA c's share of phase ph (c = ctas: the phase's end).
+__device__ __forceinline__ long long ph_begin(const KParams &p, const PhaseTable &pt, int ph, int c)
+{
+    return p.ph_iter0[ph] + pt.bound[ph][c];
+}
+
+// This CTA's launch iterations in order: its share of every phase.  `it` runs
+// through [it, end) of phase `ph`, then moves to the next phase with a
+// non-empty share.
 struct IterCursor {
     int ph;
     int it, end;               // the raw-tile kernel runs launches of fewer than 2^31 iterations
 };
 
-__device__ __forceinline__ void cursor_settle(const KParams &p, IterCursor &c)
+__device__ __forceinline__ void cursor_settle(const KParams &p, const PhaseTable &pt, IterCursor &c)
 {
     const int nph = n_phases(p);
     while (c.it >= c.end && c.ph + 1 < nph) {
         ++c.ph;
-        c.it = (int)ph_begin(p, c.ph, blockIdx.x);
-        c.end = (int)ph_begin(p, c.ph, blockIdx.x + 1);
+        c.it = (int)ph_begin(p, pt, c.ph, blockIdx.x);
+        c.end = (int)ph_begin(p, pt, c.ph, blockIdx.x + 1);
     }
 }
 
-__device__ __forceinline__ IterCursor cursor_start(const KParams &p)
+__device__ __forceinline__ IterCursor cursor_start(const KParams &p, const PhaseTable &pt)
 {
     IterCursor c;
     c.ph = 0;
-    if (p.streamk) {
-        c.it = (int)ph_begin(p, 0, blockIdx.x);
-        c.end = (int)ph_begin(p, 0, blockIdx.x + 1);
-        cursor_settle(p, c);
-    } else {
-        long long it, end;
-        cta_range(p, it, end);
-        c.it = (int)it;
-        c.end = (int)end;
-    }
+    c.it = (int)ph_begin(p, pt, 0, blockIdx.x);
+    c.end = (int)ph_begin(p, pt, 0, blockIdx.x + 1);
+    cursor_settle(p, pt, c);
     return c;
 }
 
-__device__ __forceinline__ void cursor_next(const KParams &p, IterCursor &c)
+__device__ __forceinline__ void cursor_next(const KParams &p, const PhaseTable &pt, IterCursor &c)
 {
     ++c.it;
-    cursor_settle(p, c);
+    cursor_settle(p, pt, c);
 }
 
 // Before the first copy of a phase that reads earlier phases' outputs: every
@@ -460,12 +459,13 @@ __device__ __forceinline__ void wait_phases(const KParams &p, int nreq, int d, b
 // The producer warpgroup of a phased launch: thread 0 also issues the copies;
 // every decoder tracks the issue position, so that they can wait for a
 // phase's inputs together.
-__device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaMaps &maps, const RawSmem &sm)
+__device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaMaps &maps, const PhaseTable &pt,
+                                                   const RawSmem &sm)
 {
     const int d = threadIdx.x - kTmaConsumerThreads;
     const int lane = d & 31, dw = d >> 5;
     const int offU = p.M + p.wlog, offL = p.wlog;
-    IterCursor cur = cursor_start(p), iss = cur;
+    IterCursor cur = cursor_start(p, pt), iss = cur;
     bool aborted = false;
     int issued = 0, gi = 0;    // stages copied, stages passed by the issue position
     int waited_ph = 0;          // phases up to this one have had their inputs awaited
@@ -480,7 +480,7 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
         }
         const int it = iss.it;
         const int g = gi++;
-        cursor_next(p, iss);
+        cursor_next(p, pt, iss);
         if (d != 0 || aborted) return;
         const int rs = g % kRawRing;
         if (!mbar_wait(&sm.raw_empty[rs], (uint32_t)(((g / kRawRing) & 1) ^ 1), aborted)) return;
@@ -520,7 +520,7 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
         if (iss.it >= iss.end || gi >= g + kRawRing) return false;
         return !(iss.ph > waited_ph && cur.ph < iss.ph && p.ph_after[iss.ph] > 0);
     };
-    for (int g = 0; cur.it < cur.end; cursor_next(p, cur), ++g) {
+    for (int g = 0; cur.it < cur.end; cursor_next(p, pt, cur), ++g) {
         while (may_issue(g)) issue();
         const int rs = g % kRawRing, ds = g % kRawDec;
         mbar_wait(&sm.raw_full[rs], (uint32_t)((g / kRawRing) & 1), aborted);
@@ -614,10 +614,11 @@ __device__ __forceinline__ void add_tile(const ProbParams &q, const float2 (&acc
 
 // Wait until the CTA whose share of phase ph holds iteration `it` (the last
 // stage of a cut tile) has stored its part of the tile.
-static __device__ __noinline__ void wait_stored(const KParams &p, int ph, long long it, bool &aborted)
+static __device__ __noinline__ void wait_stored(const KParams &p, const PhaseTable &pt, int ph, long long it,
+                                                bool &aborted)
 {
     int c = blockIdx.x;
-    while (c + 1 < p.ctas && ph_begin(p, ph, c + 1) <= it) ++c;
+    while (c + 1 < p.ctas && ph_begin(p, pt, ph, c + 1) <= it) ++c;
     flag_wait(phase_stored(p) + (long long)ph * p.ctas + c, p.epoch, aborted);
 }
 
@@ -629,7 +630,8 @@ static __device__ __noinline__ void wait_stored(const KParams &p, int ph, long l
 // raised), so that no CTA waits for the others at a phase's end.  The
 // summation order of cut tiles therefore varies from run to run.
 template <int W>
-__device__ __forceinline__ void raw_consumer_phased(const KParams &p, const uint8_t *lut, const RawSmem &sm)
+__device__ __forceinline__ void raw_consumer_phased(const KParams &p, const PhaseTable &pt, const uint8_t *lut,
+                                                   const RawSmem &sm)
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -640,7 +642,7 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const uint
     bool aborted = false;
     const int nph = n_phases(p);
     for (int ph = 0; ph < nph; ++ph) {
-        const long long it0 = ph_begin(p, ph, blockIdx.x), it1 = ph_begin(p, ph, blockIdx.x + 1);
+        const long long it0 = ph_begin(p, pt, ph, blockIdx.x), it1 = ph_begin(p, pt, ph, blockIdx.x + 1);
         walk_segments(p, it0, it1,
                       [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool) {
             float2 acc[TM / 2][TN];
@@ -679,7 +681,7 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const uint
                 const long long tend = q.iter0 + ((long long)b * q.tiles_u * q.tiles_l +
                                                   (long long)(u_tile0 / BU) * q.tiles_l + l_tile0 / BL + 1) *
                                                      q.kt_total;
-                wait_stored(p, ph, tend - 1, aborted);
+                wait_stored(p, pt, ph, tend - 1, aborted);
                 add_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
             }
         });
@@ -690,11 +692,11 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const uint
 }
 
 // All problems of a launch read the same LUT orientation (staged once).  PH:
-// a phased launch (its own instance, so that plain launches keep the lean
-// single-range loops; the LUT is then in shared memory).
+// a phased launch (its own kernel, so that plain launches keep the lean
+// single-range loops and their parameter size; the LUT is then in shared
+// memory).
 template <int W, bool GL, bool PH>
-__global__ void __launch_bounds__(kRawThreads, 1)
-    lutgemm_raw_kernel(const __grid_constant__ KParams p, const __grid_constant__ TmaMaps maps)
+__device__ __forceinline__ void raw_kernel_body(const KParams &p, const TmaMaps &maps, const PhaseTable *pt)
 {
     static_assert(!(PH && GL), "phased launches stage the LUT in shared memory");
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -747,31 +749,51 @@ __global__ void __launch_bounds__(kRawThreads, 1)
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
     if (tid >= kTmaConsumerThreads) {
         if constexpr (kTmaProducerWarps == 4) reg_dealloc<kTmaProducerRegs>();
-        if constexpr (PH) raw_producer_phased(p, maps, sm);
+        if constexpr (PH) raw_producer_phased(p, maps, *pt, sm);
         else raw_producer(p, maps, sm);
     } else {
         if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
-        if constexpr (PH) raw_consumer_phased<W>(p, lut, sm);
+        if constexpr (PH) raw_consumer_phased<W>(p, *pt, lut, sm);
         else raw_consumer<W, GL>(p, lut, sm, kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes);
     }
 }
 
-template <int W, bool GL, bool PH = false>
-int launch_raw_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t smem, cudaStream_t st)
+template <int W, bool GL>
+__global__ void __launch_bounds__(kRawThreads, 1)
+    lutgemm_raw_kernel(const __grid_constant__ KParams p, const __grid_constant__ TmaMaps maps)
 {
+    raw_kernel_body<W, GL, false>(p, maps, nullptr);
+}
+
+template <int W>
+__global__ void __launch_bounds__(kRawThreads, 1)
+    lutgemm_raw_phased_kernel(const __grid_constant__ KParams p, const __grid_constant__ TmaMaps maps,
+                              const __grid_constant__ PhaseTable pt)
+{
+    raw_kernel_body<W, false, true>(p, maps, &pt);
+}
+
+template <int W, bool GL, bool PH = false>
+int launch_raw_instance(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, dim3 grid, size_t smem,
+                        cudaStream_t st)
+{
+    auto kernel = [] {
+        if constexpr (PH) return lutgemm_raw_phased_kernel<W>;
+        else return lutgemm_raw_kernel<W, GL>;
+    }();
     static int checked[64] = {};   // 0 unknown, 1 usable, -1 register split not satisfiable
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return AMSIM_ECUDA;
     if (dev >= 64) return AMSIM_EUNSUPPORTED;
     if (checked[dev] == 0) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, lutgemm_raw_kernel<W, GL, PH>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return cuda_status(e);
         if (kTmaProducerWarps == 4 &&
             fa.numRegs * kRawThreads < kTmaConsumerThreads * kTmaConsumerRegs + 128 * kTmaProducerRegs) {
             checked[dev] = -1;
         } else {
-            e = cudaFuncSetAttribute(lutgemm_raw_kernel<W, GL, PH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kMaxSmemPerCta);
             if (e != cudaSuccess) return cuda_status(e);
             checked[dev] = 1;
@@ -798,7 +820,9 @@ int launch_raw_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t
         }
         cfg.attrs = attrs;
         cfg.numAttrs = na;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, lutgemm_raw_kernel<W, GL, PH>, p, maps);
+        cudaError_t e;
+        if constexpr (PH) e = cudaLaunchKernelEx(&cfg, kernel, p, maps, *pt);
+        else e = cudaLaunchKernelEx(&cfg, kernel, p, maps);
         if (e == cudaSuccess) {
             count_launch();
             return AMSIM_OK;
@@ -808,9 +832,13 @@ int launch_raw_instance(const KParams &p, const TmaMaps &maps, dim3 grid, size_t
     return p.fused ? AMSIM_ENOTCOOP : AMSIM_ECUDA;
 }
 
-int launch_raw_w8(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
-int launch_raw_w16(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
-int launch_raw_w32(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
+// pt: the share boundaries of a phased launch (p.nphase > 1), else null.
+int launch_raw_w8(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, bool gl, dim3 grid, size_t smem,
+                  cudaStream_t st);
+int launch_raw_w16(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, bool gl, dim3 grid, size_t smem,
+                   cudaStream_t st);
+int launch_raw_w32(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, bool gl, dim3 grid, size_t smem,
+                   cudaStream_t st);
 
 }  // namespace kern
 }  // namespace amsim

@@ -4,11 +4,13 @@
 namespace amsim {
 namespace kern {
 
-int launch_raw_w32(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st)
+int launch_raw_w32(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, bool gl, dim3 grid, size_t smem,
+                  cudaStream_t st)
 {
-    if (p.nphase > 1) return gl ? AMSIM_EUNSUPPORTED : launch_raw_instance<32, false, true>(p, maps, grid, smem, st);
-    return gl ? launch_raw_instance<32, true>(p, maps, grid, smem, st)
-              : launch_raw_instance<32, false>(p, maps, grid, smem, st);
+    if (p.nphase > 1)
+        return gl || !pt ? AMSIM_EUNSUPPORTED : launch_raw_instance<32, false, true>(p, maps, pt, grid, smem, st);
+    return gl ? launch_raw_instance<32, true>(p, maps, nullptr, grid, smem, st)
+              : launch_raw_instance<32, false>(p, maps, nullptr, grid, smem, st);
 }
 
 }  // namespace kern

@@ -101,9 +101,10 @@ class MLPStep:
     """3-layer MLP (784-1000-500-10, batch 256): forward Y_l = X_l W_l, then
     for every layer dX_l = dY_l W_l^T and dW_l = X_l^T dY_l (pure linear
     layers; X_{l+1} = Y_l; dY_l synthetic per layer).  The nine GEMMs run as
-    one phased call (one launch) whose three phases follow the data
-    dependences and carry about the same work in the first two:
-    {Y1, dX1, dX2}, then {Y2, dW1, dW2} (Y2 and dW2 read Y1), then
+    one phased call (one launch) whose five phases follow the data
+    dependences, with independent work between each forward GEMM and the
+    GEMMs that read its output, so that no SM waits at a phase boundary:
+    {Y1}, {dX1, dX2}, {Y2} (reads Y1), {dW1, dW2} (dW2 reads Y1),
     {Y3, dW3, dX3} (Y3 and dW3 read Y2).  Every phase copies its operand tiles
     in place (the 10-wide operands, whose leading dimension is not a multiple
     of 4 elements, with plain asynchronous loads)."""
@@ -135,9 +136,11 @@ class MLPStep:
             self.dW.append(dW)
         self.calls = fwd + [c for pair in zip(dxc, dwc) for c in pair]
         # (name, calls, number of leading phases that must be complete first)
-        self.phased = PhasedGemms([("fwd1+dX1+dX2", [fwd[0], dxc[0], dxc[1]], 0),
-                                   ("fwd2+dW1+dW2", [fwd[1], dwc[0], dwc[1]], 1),
-                                   ("fwd3+dW3+dX3", [fwd[2], dwc[2], dxc[2]], 2)])
+        self.phased = PhasedGemms([("fwd1", [fwd[0]], 0),
+                                   ("dX1+dX2", [dxc[0], dxc[1]], 0),
+                                   ("fwd2", [fwd[1]], 1),
+                                   ("dW1+dW2", [dwc[0], dwc[1]], 1),
+                                   ("fwd3+dW3+dX3", [fwd[2], dwc[2], dxc[2]], 3)])
         self.ws = workspace(self.phased.ws_bytes(lut), device)
 
     @property
