@@ -2,6 +2,7 @@
 // operand roles), the deterministic split-K reduction, and the GEMM ABI
 // (ApproxTrain Sec. VI-D GEMM kernel; Sec. VI-C AMDENSE forward and gradients).
 #include <algorithm>
+#include <vector>
 #include <atomic>
 #include <mutex>
 
@@ -403,9 +404,12 @@ namespace {
 void fill_params(const Problem *p, int n, const Plan &pl, amsim_lut_t lut, kern::KParams &kp)
 {
     int np = 0;
+    long long tile0 = 0;
     for (int i = 0; i < n; ++i) {
         if (pl.tiles[i] == 0) continue;
         kern::ProbParams &q = kp.pr[np++];
+        q.tile0 = tile0;
+        tile0 += pl.tiles[i];
         q.U = p[i].U;
         q.L = p[i].L;
         q.K = p[i].K;
@@ -680,11 +684,12 @@ int run_problem(const Problem &p, amsim_lut_t lut, void *ws, size_t ws_bytes, cu
 
 namespace {
 
-// Scratch of a phased launch: per phase and CTA a completion flag and a flag
-// for the stored last part of a cut tile (the other parts are added in C).
-size_t phased_sk_bytes(int nphase, int G)
+// Scratch of a phased launch: a completion flag per phase and CTA, then per
+// tile an arrival ticket and a flag for its first stored part (the other
+// parts of a cut tile are added in C).
+size_t phased_sk_bytes(int nphase, int G, long long tiles)
 {
-    return (size_t)2 * nphase * G * sizeof(unsigned long long);
+    return ((size_t)nphase * G + 2 * (size_t)tiles) * sizeof(unsigned long long);
 }
 
 // Problems [first[ph], first[ph + 1]) of phase ph (the last ends at n).
@@ -712,8 +717,9 @@ bool phased_ok(const Problem *p, int n, int nphase, const Plan &pl, amsim_lut_t 
 
 // Relative time of one stage of a tile: consumer warps whose rows or columns
 // all lie past the operands' edges skip their lookups, and such stages run
-// faster (measured on GB300: a tile with a quarter of its warps busy takes
-// about 0.73 of a full stage), so shares are cut by this cost, not by count.
+// faster -- measured on GB300 from per-CTA timelines of phased launches, a
+// stage with a fraction f of its warps busy takes about 0.47 + 0.53 f of a
+// full stage (0.6 at f = 1/4) -- so shares are cut by this cost, not by count.
 double stage_cost(const Problem &p, int ut, int lt)
 {
     constexpr int WUn = BU / kern::TM, WLn = BL / (32 * kern::TN);
@@ -721,42 +727,68 @@ double stage_cost(const Problem &p, int ut, int lt)
     for (int wu = 0; wu < WUn; ++wu)
         for (int wl = 0; wl < WLn; ++wl)
             busy += (ut * BU + wu * kern::TM < p.U.rows && lt * BL + wl * 32 * kern::TN < p.L.rows) ? 1 : 0;
-    return 0.64 + 0.36 * busy / (WUn * WLn);
+    return 0.47 + 0.53 * busy / (WUn * WLn);
 }
 
-// Share boundaries of one phase: CTA c's share starts where the phase's
-// cumulative stage cost reaches c / G of its total (rounded to a stage).
-void phase_bounds_by_cost(const Problem *p, const Plan &pl, int lo, int hi, int G, int *bound)
+// Share boundaries of every phase.  CTAs 0 .. c-1 together get, through
+// phase ph, the cumulative stage cost c / G of phases 0 .. ph (rounded to a
+// stage): each phase's boundary for CTA c is where the phase's running cost
+// reaches that target minus what the earlier phases actually gave those
+// CTAs, so the rounding of one phase is made up in the next and per-CTA
+// totals stay within about a stage of each other however many phases there
+// are.
+void phased_bounds_by_cost(const Problem *p, const Plan &pl, const int *first, int nphase, int n, int G,
+                           kern::PhaseTable *pt)
 {
-    double total = 0.0;
-    for (int i = lo; i < hi; ++i) {
-        if (pl.tiles[i] == 0) continue;
-        for (int ut = 0; ut < pl.tiles_u[i]; ++ut)
-            for (int lt = 0; lt < pl.tiles_l[i]; ++lt)
-                total += (double)p[i].batch * pl.kt[i] * stage_cost(p[i], ut, lt);
-    }
-    long long it = 0;
-    double cum = 0.0;
-    int c = 1;
-    bound[0] = 0;
-    for (int i = lo; i < hi && c < G; ++i) {
-        if (pl.tiles[i] == 0) continue;
-        for (int b = 0; b < p[i].batch && c < G; ++b)
-            for (int ut = 0; ut < pl.tiles_u[i] && c < G; ++ut)
-                for (int lt = 0; lt < pl.tiles_l[i] && c < G; ++lt) {
-                    const double w = stage_cost(p[i], ut, lt), tc = w * pl.kt[i];
-                    while (c < G && cum + tc >= total * c / G) {
-                        const long long k = std::llround((total * c / G - cum) / w);
-                        bound[c++] = (int)(it + std::min<long long>(std::max<long long>(k, 0), pl.kt[i]));
+    std::vector<double> prev(G + 1, 0.0), target(G + 1), actual(G + 1);
+    double V = 0.0;
+    for (int ph = 0; ph < nphase; ++ph) {
+        int lo, hi;
+        phase_bounds(first, nphase, n, ph, &lo, &hi);
+        struct Run { int kt; double w; };
+        std::vector<Run> runs;                  // tiles in iteration order
+        double C = 0.0;
+        long long W = 0;
+        for (int i = lo; i < hi; ++i) {
+            if (pl.tiles[i] == 0) continue;
+            for (int b = 0; b < p[i].batch; ++b)
+                for (int ut = 0; ut < pl.tiles_u[i]; ++ut)
+                    for (int lt = 0; lt < pl.tiles_l[i]; ++lt) {
+                        const double w = stage_cost(p[i], ut, lt);
+                        runs.push_back({pl.kt[i], w});
+                        C += w * pl.kt[i];
+                        W += pl.kt[i];
                     }
-                    cum += tc;
-                    it += pl.kt[i];
-                }
+        }
+        V += C;
+        target[0] = 0.0;
+        for (int c = 1; c < G; ++c)
+            target[c] = std::min(std::max(V * c / G - prev[c], target[c - 1]), C);
+        target[G] = C;
+        int *bound = pt->bound[ph];
+        bound[0] = 0;
+        actual[0] = 0.0;
+        int c = 1;
+        long long it = 0;
+        double cum = 0.0;
+        for (const Run &r : runs) {
+            const double tc = r.w * r.kt;
+            while (c < G && cum + tc >= target[c]) {
+                const long long k =
+                    std::min<long long>(std::max<long long>(std::llround((target[c] - cum) / r.w), 0), r.kt);
+                bound[c] = (int)(it + k);
+                actual[c] = cum + k * r.w;
+                ++c;
+            }
+            cum += tc;
+            it += r.kt;
+        }
+        for (; c <= G; ++c) {
+            bound[c] = (int)W;
+            actual[c] = C;
+        }
+        for (int k = 1; k <= G; ++k) prev[k] += actual[k];
     }
-    long long w_all = 0;
-    for (int i = lo; i < hi; ++i) w_all += pl.tiles[i] * pl.kt[i];
-    while (c <= G) bound[c++] = (int)w_all;
-    for (int k = 1; k <= G; ++k) bound[k] = std::min(std::max(bound[k], bound[k - 1]), (int)w_all);
 }
 
 }  // namespace
@@ -770,7 +802,8 @@ int run_phased(const Problem *p, int n, int nphase, const int *first, const int 
     const int sms = device_sms(lut->device);
     Plan pl = make_plan(p, std::min(n, kern::kMaxProblems), sms, (size_t)-1);
     if (pl.total_tiles == 0 && n <= kern::kMaxProblems) return AMSIM_OK;
-    if (ws && phased_ok(p, n, nphase, pl, lut, true) && ws_bytes >= phased_sk_bytes(nphase, pl.ctas)) {
+    if (ws && phased_ok(p, n, nphase, pl, lut, true) &&
+        ws_bytes >= phased_sk_bytes(nphase, pl.ctas, pl.total_tiles)) {
         pl.streamk = true;
         kern::KParams tp = {};
         fill_params(p, n, pl, lut, tp);
@@ -787,11 +820,7 @@ int run_phased(const Problem *p, int n, int nphase, const int *first, const int 
         }
         tp.ph_iter0[nphase] = pl.iters;
         kern::PhaseTable pt;
-        for (int ph = 0; ph < nphase; ++ph) {
-            int lo, hi;
-            phase_bounds(first, nphase, n, ph, &lo, &hi);
-            phase_bounds_by_cost(p, pl, lo, hi, pl.ctas, pt.bound[ph]);
-        }
+        phased_bounds_by_cost(p, pl, first, nphase, n, pl.ctas, &pt);
         kern::TmaMaps maps = {};
         int rc = encode_raw_problems(p, n, pl, tp, maps);
         if (rc == AMSIM_OK) {
@@ -831,7 +860,8 @@ size_t phased_workspace(const Problem *p, int n, int nphase, const int *first, a
     }
     if (n <= kern::kMaxProblems) {
         const Plan pl = make_plan(p, n, device_sms(lut->device), (size_t)-1);
-        if (phased_ok(p, n, nphase, pl, lut, false)) best = std::max(best, phased_sk_bytes(nphase, pl.ctas));
+        if (phased_ok(p, n, nphase, pl, lut, false))
+            best = std::max(best, phased_sk_bytes(nphase, pl.ctas, pl.total_tiles));
     }
     return best;
 }

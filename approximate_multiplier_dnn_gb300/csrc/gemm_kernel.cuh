@@ -84,6 +84,7 @@ struct ProbParams {
     int tiles_u, tiles_l, kt_total;
     long long tiles;        // tiles_u * tiles_l * batch
     long long iter0;        // first iteration of this problem in the launch's iteration space
+    long long tile0;        // first tile of this problem among the launch's tiles
     const void *table;      // LUT oriented [U mantissa][L mantissa]
     float *c_ptr;
     long long c_bs, c_su, c_sl;

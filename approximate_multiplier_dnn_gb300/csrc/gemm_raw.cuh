@@ -36,7 +36,8 @@ constexpr int kRawDec = 3;                              // decoded stages
 constexpr int kRawBarBytes = 256;                       // barriers and big-operand flags
 static_assert(kRawUBytes % 1024 == 0 && kRawLBytes % 1024 == 0, "swizzled boxes start 1024-byte aligned");
 static_assert(BL % 64 == 0 && (BL / 64) * BK * 64 * 4 == kRawLBytes, "blocked L boxes fill the L stage");
-static_assert((2 * kRawRing + 2 * kRawDec + 1) * 8 + kRawDec * (kRawDecoders / 32) * 4 <= kRawBarBytes, "barrier block");
+static_assert((2 * kRawRing + 2 * kRawDec + 2) * 8 + (kRawDec * (kRawDecoders / 32) + 1) * 4 <= kRawBarBytes,
+              "barrier block");
 static_assert(kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes >= (BU * BL + 1024 * 4) * 4,
               "the rings hold the stream-K reduction buffer");
 
@@ -392,17 +393,31 @@ __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lu
                      2 * kRawDec, aborted);
 }
 
-// Scratch of a phased launch: completion flags [phase][cta], then flags
-// [phase][cta] raised once the CTA has stored the last part of the cut tile
-// its share starts in.
+// Scratch of a phased launch: completion flags [phase][cta], then per tile of
+// the launch an arrival ticket (launch epoch in the high half, parts arrived
+// in the low half) and a flag raised once its first arrived part is stored.
 __device__ __forceinline__ unsigned long long *phase_done(const KParams &p)
 {
     return reinterpret_cast<unsigned long long *>(p.ws);
 }
 
-__device__ __forceinline__ unsigned long long *phase_stored(const KParams &p)
+__device__ __forceinline__ unsigned long long *tile_ticket(const KParams &p, long long tile)
 {
-    return phase_done(p) + (long long)n_phases(p) * p.ctas;
+    return phase_done(p) + (long long)n_phases(p) * p.ctas + 2 * tile;
+}
+
+// Count this part's arrival at a cut tile; true for the first part of this launch.
+__device__ __forceinline__ bool first_arrival(const KParams &p, long long tile)
+{
+    unsigned long long *t = tile_ticket(p, tile);
+    const unsigned long long ep = (p.epoch & 0xFFFFFFFFull) << 32;
+    unsigned long long v = *reinterpret_cast<volatile unsigned long long *>(t);
+    for (;;) {
+        const unsigned long long nv = (v & 0xFFFFFFFF00000000ull) == ep ? v + 1 : ep | 1ull;
+        const unsigned long long old = atomicCAS(t, v, nv);
+        if (old == v) return (nv & 0xFFFFFFFFull) == 1;
+        v = old;
+    }
 }
 
 // First launch iteration of CTA c's share of phase ph (c = ctas: the phase's end).
@@ -612,27 +627,18 @@ __device__ __forceinline__ void add_tile(const ProbParams &q, const float2 (&acc
     }
 }
 
-// Wait until the CTA whose share of phase ph holds iteration `it` (the last
-// stage of a cut tile) has stored its part of the tile.
-static __device__ __noinline__ void wait_stored(const KParams &p, const PhaseTable &pt, int ph, long long it,
-                                                bool &aborted)
-{
-    int c = blockIdx.x;
-    while (c + 1 < p.ctas && ph_begin(p, pt, ph, c + 1) <= it) ++c;
-    flag_wait(phase_stored(p) + (long long)ph * p.ctas + c, p.epoch, aborted);
-}
-
 // The consumers of a phased launch (LUT in shared memory).  A tile that the
-// share boundaries cut is summed in C: the CTA whose share holds the tile's
-// last stages -- the first to finish its part, at the start of its share --
-// stores alpha * part + beta * C and raises a flag; every other part is added
-// with floating-point reductions after a check of that flag (normally long
-// raised), so that no CTA waits for the others at a phase's end.  The
-// summation order of cut tiles therefore varies from run to run.
+// share boundaries cut is summed in C: the first of its parts to be done (an
+// arrival ticket per tile decides) is stored as alpha * part + beta * C, and a
+// flag is raised; every other part is added with floating-point reductions
+// after that flag -- no CTA waits for another CTA's compute, at a phase's end
+// or anywhere else.  The summation order of cut tiles therefore varies from
+// run to run.
 template <int W>
 __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const PhaseTable &pt, const uint8_t *lut,
                                                    const RawSmem &sm)
 {
+    volatile int *first_flag = sm.flags + kRawDec * (kRawDecoders / 32);   // the ticket's verdict
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
@@ -670,19 +676,24 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const Phas
                 }
                 mbar_arrive(&sm.empty[ds]);
             }
-            if (s1 == q.kt_total) {
-                // a whole tile, or the last part of a cut one (this share's first segment)
+            if (s0 == 0 && s1 == q.kt_total) {
                 store_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
-                if (s0 > 0) {
-                    consumer_bar();
-                    if (tid == 0) flag_store(phase_stored(p) + (long long)ph * p.ctas + blockIdx.x, p.epoch);
-                }
             } else {
-                const long long tend = q.iter0 + ((long long)b * q.tiles_u * q.tiles_l +
-                                                  (long long)(u_tile0 / BU) * q.tiles_l + l_tile0 / BL + 1) *
-                                                     q.kt_total;
-                wait_stored(p, pt, ph, tend - 1, aborted);
-                add_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
+                const long long tile = q.tile0 + (long long)b * q.tiles_u * q.tiles_l +
+                                       (long long)(u_tile0 / BU) * q.tiles_l + l_tile0 / BL;
+                unsigned long long *stored = tile_ticket(p, tile) + 1;
+                if (tid == 0) *first_flag = first_arrival(p, tile) ? 1 : 0;
+                consumer_bar();
+                const bool first = *first_flag != 0;
+                consumer_bar();         // everyone has read the ticket's verdict
+                if (first) {
+                    store_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
+                    consumer_bar();
+                    if (tid == 0) flag_store(stored, p.epoch);
+                } else {
+                    flag_wait(stored, p.epoch, aborted);
+                    add_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
+                }
             }
         });
         // every consumer's stores and reductions of the phase precede the flag
@@ -713,15 +724,9 @@ __device__ __forceinline__ void raw_kernel_body(const KParams &p, const TmaMaps 
     sm.full = sm.raw_empty + kRawRing;
     sm.empty = sm.full + kRawDec;
     uint64_t *red = sm.empty + kRawDec;                    // the stream-K reduction's barrier
-    sm.flags = reinterpret_cast<int *>(red + 1);
+    uint64_t *lut_bar = red + 1;                           // the LUT's copy into shared memory
+    sm.flags = reinterpret_cast<int *>(red + 2);
 
-    if constexpr (!GL) {
-        // the table was written when the LUT was built, before any launch
-        const uint4 *src = static_cast<const uint4 *>(p.pr[0].table);
-        uint4 *dst = reinterpret_cast<uint4 *>(smem);
-        const int nvec = (p.table_bytes + 15) >> 4;
-        for (int i = tid; i < nvec; i += kRawThreads) dst[i] = __ldg(src + i);
-    }
     if (tid == 0) {
         for (int s = 0; s < kRawRing; ++s) {
             mbar_init(&sm.raw_full[s], 1);
@@ -732,7 +737,16 @@ __device__ __forceinline__ void raw_kernel_body(const KParams &p, const TmaMaps 
             mbar_init(&sm.empty[s], kTmaConsumerThreads);
         }
         mbar_init(red, 1);
+        mbar_init(lut_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if constexpr (!GL) {
+            // one bulk copy of the table (written when the LUT was built, before
+            // any launch; its allocation is padded to 256 bytes), overlapping the
+            // first tile copies; the consumers wait for it before their first stage
+            const uint32_t bytes = (uint32_t)((p.table_bytes + 15) & ~15);
+            mbar_expect_tx(lut_bar, bytes);
+            bulk_g2s(smem, p.pr[0].table, bytes, lut_bar);
+        }
     }
     if (tid == kTmaConsumerThreads) {
         for (int i = 0; i < p.nprob; ++i) {
@@ -753,6 +767,10 @@ __device__ __forceinline__ void raw_kernel_body(const KParams &p, const TmaMaps 
         else raw_producer(p, maps, sm);
     } else {
         if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
+        if constexpr (!GL) {
+            bool gave_up = false;
+            mbar_wait(lut_bar, 0, gave_up);
+        }
         if constexpr (PH) raw_consumer_phased<W>(p, *pt, lut, sm);
         else raw_consumer<W, GL>(p, lut, sm, kRawDec * kTmaStageBytes + kRawRing * kRawStageBytes);
     }
