@@ -405,39 +405,87 @@ def main():
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "peak_source": src, "unit": "GB/s",
                     "frac": gbs / hbm, "traffic": traffic, "kernel": "amsim_mul_kernel"}
 
-    # end to end: pinned host inputs -> device, step, outputs -> pinned host
-    e2e = None
-    if hasattr(step, "inputs"):
-        inputs = step.inputs
-    elif hasattr(step, "x"):
-        inputs = {k: getattr(step, k) for k in ("x", "w", "dy") if getattr(step, k, None) is not None}
-    elif hasattr(step, "a"):
-        inputs = {"a": step.a, "b": step.b}
-    elif hasattr(step, "Q"):
-        inputs = {"Q": step.Q, "K": step.K, "V": step.V}
-    else:
-        inputs = {"A": step.A, "B": step.B}
-    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu()) for k, v in inputs.items()}
-    outs = step.outputs()
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    # end to end through the library's calls with host buffers: every step's
+    # inputs go from pinned host memory to the device and its outputs come back,
+    # inside the timed region.  E steps run back to back as a stream of batches:
+    # two step instances alternate, step s's inputs go up on one copy stream
+    # while step s-1 computes and step s-1's outputs come down on another, so
+    # the throughput is that of the slowest of the three.  A serial pass (copy
+    # in, compute, copy out, one step at a time) is reported beside it.
+    def step_inputs(st):
+        if hasattr(st, "inputs"):
+            return st.inputs
+        if hasattr(st, "x"):
+            return {k: getattr(st, k) for k in ("x", "w", "dy") if getattr(st, k, None) is not None}
+        if hasattr(st, "a"):
+            return {"a": st.a, "b": st.b}
+        if hasattr(st, "Q"):
+            return {"Q": st.Q, "K": st.K, "V": st.V}
+        return {"A": st.A, "B": st.B}
+
+    pair = [step, make_step(args.workload, lut_for, args.mantissa)[0]]
+    for _ in range(args.warmup):
+        pair[1].run()
+    ins = [step_inputs(st) for st in pair]
+    outs = [st.outputs() for st in pair]
+    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu()) for k, v in ins[0].items()}
+    host_out = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs[j]] for j in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs)
-    E = max(1, min(args.e2e_steps, K))
-    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E)]
+    d2h = sum(o.numel() * o.element_size() for o in outs[0])
+    E = max(3, min(args.e2e_steps, K))
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_down = [torch.cuda.Event() for _ in range(2)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    t_start.record(stream)
+    up.wait_event(t_start)
+    down.wait_event(t_start)
     for s in range(E):
+        j = s % 2
+        if s >= 2:
+            up.wait_event(ev_comp[j])           # step s-2 is done reading instance j's inputs
+        with torch.cuda.stream(up):
+            for k, v in ins[j].items():
+                v.copy_(host_in[k], non_blocking=True)
+        ev_up[j].record(up)
+        stream.wait_event(ev_up[j])
+        if s >= 2:
+            stream.wait_event(ev_down[j])       # step s-2's outputs are on the host
+        pair[j].run(stream)
+        ev_comp[j].record(stream)
+        down.wait_event(ev_comp[j])
+        with torch.cuda.stream(down):
+            for o, h in zip(outs[j], host_out[j]):
+                h.copy_(o, non_blocking=True)
+        ev_down[j].record(down)
+    for j in range(2):
+        stream.wait_event(ev_down[j])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = t_start.elapsed_time(t_end) / E
+
+    # serial: one step at a time, its copies and compute in sequence
+    ES = max(1, min(10, E))
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ES)]
+    torch.cuda.synchronize()
+    for s in range(ES):
         torch.cuda._sleep(sleep_cycles * 2)
         e_ev[s][0].record(stream)
-        for k, v in inputs.items():
+        for k, v in ins[0].items():
             v.copy_(host_in[k], non_blocking=True)
         step.run()
-        for o, h in zip(outs, host_out):
+        for o, h in zip(outs[0], host_out[0]):
             h.copy_(o, non_blocking=True)
         e_ev[s][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e_ev) / E
+    serial_ms = sum(a.elapsed_time(b) for a, b in e_ev) / ES
     e2e = {"value": world * macs / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": E,
+           "pipeline": "two step instances alternate; inputs up and outputs down on two copy streams",
+           "serial_ms_per_step": serial_ms,
+           "serial_value": world * macs / (serial_ms * 1e-3) / 1e9}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("mlp", "gemm4096"):
