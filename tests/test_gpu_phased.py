@@ -7,7 +7,7 @@ NaN so that a read before the producing phase finished would show."""
 import numpy as np
 import pytest
 
-from gpu_helpers import assert_close, guarded, guards_intact, to_dev
+from gpu_helpers import REL, assert_close, guarded, guards_intact, to_dev
 from approximate_multiplier_dnn_gb300 import GemmProblem
 
 pytestmark = pytest.mark.gpu
@@ -180,3 +180,64 @@ def test_phased_rejects_bad_layouts(amd, luts):
         with pytest.raises(amd.AmsimError):
             amd.amsim_gemm_phased(probs, first, after, lut)
         assert amd.amsim_gemm_phased_workspace_size(probs, first, after, lut) == 0
+
+
+@pytest.mark.parametrize("kind", ["mitchell", "exact"])
+def test_phased_alpha_beta_and_transposes(amd, orc, luts, kind):
+    """alpha and beta != 0 on cut tiles (the first-arriving part carries
+    beta * C, the others add alpha * part), all four transpose pairs, and a
+    phase that reads a transposed output of an earlier one."""
+    rng = np.random.default_rng(45)
+    lut = luts(kind, 7)
+    m, n, k = 300, 520, 700
+    A, B = rnd(rng, (k, m)), rnd(rng, (n, k))                  # op(A) = A^T, op(B) = B^T
+    C0 = rnd(rng, (m, n))
+    Cb, C = guarded((m, n), C0)
+    E, F = rnd(rng, (m, 260)), rnd(rng, (260, 400))            # N, N
+    G0 = rnd(rng, (m, 400))
+    Gb, Gt = guarded((m, 400), G0)
+    H = rnd(rng, (n, 96))                                      # phase 2 reads C^T
+    Ob, O = guarded((n, 96), np.full((n, 96), np.nan, np.float32))
+    Wt = rnd(rng, (96, m))                                     # O = C^T (n x m) . Wt^T (m x 96)
+    dev = [to_dev(x) for x in (A, B, E, F, Wt)]
+    probs = [problem(dev[0], dev[1], C, ta=True, tb=True, alpha=0.75, beta=-1.25),
+             problem(dev[2], dev[3], Gt, alpha=2.0, beta=0.5),
+             problem(C, dev[4], O, ta=True, tb=True)]
+    path = run_phased(amd, lut, probs, [0, 1, 2], [0, 0, 1])
+    assert path & amd.AMSIM_PATH_PHASED, path
+    for buf in (Cb, Gb, Ob):
+        assert guards_intact(buf)
+    ref, sa = orc.gemm(kind, 7, A, B, transA=True, transB=True, alpha=0.75, beta=-1.25, C0=C0)
+    # beta * C is rounded once and then each added part rounds at its magnitude:
+    # allow 16 ulps of it beside the products' own bound
+    assert_close(host(C), ref, 0.75 * sa + 1.25 * np.abs(C0.astype(np.float64)) / REL * 2.0 ** -20, "C")
+    ref, sa = orc.gemm(kind, 7, E, F, alpha=2.0, beta=0.5, C0=G0)
+    assert_close(host(Gt), ref, 2.0 * sa + 0.5 * np.abs(G0.astype(np.float64)) / REL * 2.0 ** -20, "G")
+    ref, sa = orc.gemm(kind, 7, host(C), Wt, transA=True, transB=True)
+    assert_close(host(O), ref, sa, "O")
+
+
+def test_phased_batched_problems(amd, orc, luts):
+    """Strided-batched problems (one with a broadcast operand) across phases."""
+    rng = np.random.default_rng(46)
+    lut = luts("mitchell", 7)
+    batch, m, n, k = 6, 128, 200, 96
+    A = rnd(rng, (batch, m, k))
+    B = rnd(rng, (k, n))                                       # broadcast: strideB = 0
+    Yb, Y = guarded((batch, m, n), np.full((batch, m, n), np.nan, np.float32))
+    V = rnd(rng, (batch, n, 64))
+    Zb, Z = guarded((batch, m, 64), np.full((batch, m, 64), np.nan, np.float32))
+    dA, dB, dV = to_dev(A), to_dev(B), to_dev(V)
+    probs = [GemmProblem.make("N", "N", m, n, k, 1.0, dA, k, dB, n, 0.0, Y, n, strideA=m * k, strideB=0,
+                              strideC=m * n, batch=batch),
+             GemmProblem.make("N", "N", m, 64, n, 1.0, Y, n, dV, 64, 0.0, Z, 64, strideA=m * n, strideB=n * 64,
+                              strideC=m * 64, batch=batch)]
+    path = run_phased(amd, lut, probs, [0, 1], [0, 1])
+    assert path & amd.AMSIM_PATH_PHASED, path
+    assert guards_intact(Yb) and guards_intact(Zb)
+    y = host(Y)
+    for b in range(batch):
+        ref, sa = orc.gemm("mitchell", 7, A[b], B)
+        assert_close(y[b], ref, sa, f"Y[{b}]")
+        ref, sa = orc.gemm("mitchell", 7, y[b], V[b])
+        assert_close(host(Z)[b], ref, sa, f"Z[{b}]")
