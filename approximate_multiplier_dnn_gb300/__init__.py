@@ -109,6 +109,7 @@ def lib():
         "amsim_conv2d_bwd_filter": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
         "amsim_conv2d_workspace_size": ([ctypes.POINTER(ConvDesc), i32, vp], sz),
         "amsim_softmax_rows": ([vp, vp, i64, i32, vp], i32),
+        "amsim_softmax_rows_backward": ([vp, vp, vp, i64, i32, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -379,6 +380,11 @@ def amsim_conv2d_bwd_filter(desc, x, dy, dw, lut, ws=None, ws_bytes=None, stream
 
 def amsim_conv2d_workspace_size(desc, which: int, lut) -> int:
     return int(lib().amsim_conv2d_workspace_size(ctypes.byref(desc), int(which), _h(lut)))
+
+
+def amsim_softmax_rows_backward(P, dP, dS, rows, cols, stream=None):
+    _check("amsim_softmax_rows_backward",
+           lib().amsim_softmax_rows_backward(_ptr(P), _ptr(dP), _ptr(dS), int(rows), int(cols), _stream(stream)))
 
 
 def amsim_softmax_rows(S, P, rows, cols, stream=None):

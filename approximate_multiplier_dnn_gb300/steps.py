@@ -47,6 +47,14 @@ class GemmCall:
                    self.B, max(1, self.B.shape[1]), self.beta, self.C, max(1, self.n), lut, ws=ws,
                    stream=stream)
 
+    def native(self):
+        """The same contraction with torch fp32 (cuBLAS) into a scratch output."""
+        import torch
+        a = self.A.t() if self.tA == "T" else self.A
+        b = self.B.t() if self.tB == "T" else self.B
+        out = torch.empty((self.m, self.n), dtype=torch.float32, device=self.A.device)
+        return lambda: torch.matmul(a, b, out=out)
+
     def problem(self) -> GemmProblem:
         return GemmProblem.make(self.tA, self.tB, self.m, self.n, self.k, self.alpha, self.A,
                                 max(1, self.A.shape[1]), self.B, max(1, self.B.shape[1]), self.beta, self.C,
@@ -157,6 +165,65 @@ class MLPStep:
     def run(self, stream=None):
         self.phased(self.lut, self.ws, stream)
 
+    def native(self):
+        fns = [c.native() for c in self.calls]
+        return lambda: [f() for f in fns]
+
+
+class LayersMLPStep:
+    """The MLP 784-1000-500-10 (batch 256) through the autograd layers: three
+    approximate Dense layers (no bias) run forward and backward by torch's
+    autograd -- nine separate approximate GEMM calls, the backward chained
+    through the layers (a layer's dY is the next layer's dX), from a
+    synthetic dY3.  Same MAC count as MLPStep; the gradients accumulate into
+    buffers that are cleared each step."""
+
+    def __init__(self, data: dict, lut, device="cuda"):
+        import torch
+        self.lut = lut
+        d = {k: _dev(v, device) for k, v in data.items()}
+        self.inputs = {k: d[k] for k in ("X", "W1", "W2", "W3", "dY3")}
+        self.X = d["X"].requires_grad_()
+        self.W = [d[f"W{l + 1}"].requires_grad_() for l in range(3)]
+        self.dY = d["dY3"]
+        for t in [self.X] + self.W:
+            t.grad = torch.zeros_like(t)
+        self.Y = None
+
+    @property
+    def macs(self) -> int:
+        n, dims = self.X.shape[0], [self.X.shape[1]] + [w.shape[1] for w in self.W]
+        return 3 * sum(n * dims[i] * dims[i + 1] for i in range(3))
+
+    def outputs(self) -> list:
+        return [self.X.grad] + [w.grad for w in self.W]
+
+    def run(self, stream=None):
+        import torch
+        from .layers import am_dense
+        ctx = torch.cuda.stream(stream) if stream is not None else torch.cuda.stream(torch.cuda.current_stream())
+        with ctx:
+            for t in [self.X] + self.W:
+                t.grad.zero_()
+            h = self.X
+            for w in self.W:
+                h = am_dense(h, w, self.lut)
+            h.backward(self.dY)
+
+    def parts(self, stream=None):
+        return [("fwd+bwd through AMDense layers", lambda: self.run(stream), self.macs, 9)]
+
+    def native(self):
+        import torch
+        X, W = self.X.detach().clone().requires_grad_(), [w.detach().clone().requires_grad_() for w in self.W]
+
+        def f():
+            h = X
+            for w in W:
+                h = h @ w
+            h.backward(self.dY)
+        return f
+
 
 class ConvStep:
     """Conv2D forward, preceding-layer gradient and weight gradient of one
@@ -200,6 +267,25 @@ class ConvStep:
         return [(fns[p][0], fns[p][1], per, 1 + (amsim_conv2d_workspace_size(self.desc, p, self.lut) > 0))
                 for p in self.passes]
 
+    def native(self):
+        """The same passes with torch fp32 (cuDNN): NHWC tensors as channels-last views."""
+        import torch
+        import torch.nn.functional as F
+        from torch.nn import grad as nng
+        g = self.g
+        st, pd, dl = (g["stride"][0], g["stride"][1]), (g["pad"][0], g["pad"][1]), (g["dil"][0], g["dil"][1])
+        x = self.x.permute(0, 3, 1, 2)                       # N C H W view of NHWC
+        w = self.w.permute(3, 2, 0, 1).contiguous()          # K C R S from R S C K
+        dy = self.dy.permute(0, 3, 1, 2) if self.dy is not None else None
+        fns = []
+        if 0 in self.passes:
+            fns.append(lambda: F.conv2d(x, w, stride=st, padding=pd, dilation=dl))
+        if 1 in self.passes:
+            fns.append(lambda: nng.conv2d_input(x.shape, w, dy, stride=st, padding=pd, dilation=dl))
+        if 2 in self.passes:
+            fns.append(lambda: nng.conv2d_weight(x, w.shape, dy, stride=st, padding=pd, dilation=dl))
+        return lambda: [f() for f in fns]
+
     def run(self, stream=None):
         if 0 in self.passes:
             amsim_conv2d_fwd(self.desc, self.x, self.w, self.y, self.lut, ws=self.ws, stream=stream)
@@ -232,6 +318,9 @@ class SquareGemmStep:
 
     def run(self, stream=None):
         self.call(self.lut, self.ws, stream)
+
+    def native(self):
+        return self.call.native()
 
 
 class AttentionStep:
@@ -284,6 +373,17 @@ class AttentionStep:
         amsim_gemm_strided_batched("N", "N", s, d, s, 1.0, self.P, s, s * s, self.V, d, s * d, 0.0, self.O, d,
                                    s * d, bh, self.lut, ws=self.ws, stream=stream)
 
+    def native(self):
+        """S = Q K^T / sqrt(d), row softmax, O = P V with torch fp32 (cuBLAS)."""
+        import torch
+        b, h, s, d = self.Q.shape
+        q, k, v = (t.reshape(b * h, s, d) for t in (self.Q, self.K, self.V))
+
+        def f():
+            sc = torch.bmm(q, k.transpose(1, 2)) * self.scale
+            return torch.bmm(torch.softmax(sc, dim=-1), v)
+        return f
+
 
 class MulStep:
     """Elementwise AMSim products c = AMSim(a, b) over n pairs."""
@@ -308,3 +408,8 @@ class MulStep:
 
     def run(self, stream=None):
         amsim_mul(self.a, self.b, self.c, self.a.numel(), self.lut, stream=stream)
+
+    def native(self):
+        import torch
+        c = torch.empty_like(self.c)
+        return lambda: torch.mul(self.a, self.b, out=c)

@@ -32,7 +32,7 @@ METRIC = "approx-GMAC/s for LUT-multiplier GEMM/conv at M=7"
 UNIT = "approx-GMAC/s"
 LOOKUPS_PER_CLK_PER_SM = 32     # one 4-byte shared-memory wavefront per clock per SM
 
-WORKLOADS = ("mlp", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "gemm64", "mul")
+WORKLOADS = ("mlp", "mlp_layers", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "gemm64", "mul")
 
 
 def measured_peaks():
@@ -58,6 +58,9 @@ def make_step(name, lut_for, M=7):
     from approximate_multiplier_dnn_gb300 import workloads as wl
     if name == "mlp":
         return steps.MLPStep(wl.mlp(), lut_for("mitchell", 7)), "mlp_784-1000-500-10_b256_fwd+dX+dW_mitchell_M7"
+    if name == "mlp_layers":
+        return (steps.LayersMLPStep(wl.mlp(), lut_for("mitchell", 7)),
+                "mlp_784-1000-500-10_b256_autograd_AMDense_layers_mitchell_M7")
     if name == "conv3x3":
         return (steps.ConvStep(wl.conv3x3(), wl.CONV3X3, lut_for("mitchell", 7)),
                 "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_mitchell_M7")
@@ -405,6 +408,30 @@ def main():
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "peak_source": src, "unit": "GB/s",
                     "frac": gbs / hbm, "traffic": traffic, "kernel": "amsim_mul_kernel"}
 
+    # native fp32 on the same shapes (TF32 off), timed the same way: the pages
+    # put the simulated GEMM beside the native one (ApproxTrain Sec. V-C)
+    native = None
+    if hasattr(step, "native"):
+        torch.backends.cuda.matmul.allow_tf32 = False
+        torch.backends.cudnn.allow_tf32 = False
+        nf = step.native()
+        for _ in range(3):
+            nf()
+        NN = max(3, min(50, K))
+        nev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(NN)]
+        torch.cuda.synchronize()
+        for s in range(NN):
+            flush.fill_(float(s))
+            torch.cuda._sleep(sleep_cycles)
+            nev[s][0].record(stream)
+            nf()
+            nev[s][1].record(stream)
+        torch.cuda.synchronize()
+        native_ms = sum(a.elapsed_time(b) for a, b in nev) / NN
+        native = {"impl": "torch fp32 (cuBLAS / cuDNN), TF32 off, same shapes, L2 flushed before each step",
+                  "ms_per_step": native_ms, "value": macs / (native_ms * 1e-3) / 1e9, "unit": "GMAC/s",
+                  "approx_time_over_native": ms_per_step / native_ms}
+
     # end to end through the library's calls with host buffers: every step's
     # inputs go from pinned host memory to the device and its outputs come back,
     # inside the timed region.  E steps run back to back as a stream of batches:
@@ -446,7 +473,7 @@ def main():
         j = s % 2
         if s >= 2:
             up.wait_event(ev_comp[j])           # step s-2 is done reading instance j's inputs
-        with torch.cuda.stream(up):
+        with torch.cuda.stream(up), torch.no_grad():
             for k, v in ins[j].items():
                 v.copy_(host_in[k], non_blocking=True)
         ev_up[j].record(up)
@@ -473,8 +500,9 @@ def main():
     for s in range(ES):
         torch.cuda._sleep(sleep_cycles * 2)
         e_ev[s][0].record(stream)
-        for k, v in ins[0].items():
-            v.copy_(host_in[k], non_blocking=True)
+        with torch.no_grad():
+            for k, v in ins[0].items():
+                v.copy_(host_in[k], non_blocking=True)
         step.run()
         for o, h in zip(outs[0], host_out[0]):
             h.copy_(o, non_blocking=True)
@@ -512,6 +540,7 @@ def main():
             "roofline": roofline,
             "parts_ms": {p[0]: round(t, 5) for p, t in zip(parts, part_ms)},
             "e2e": e2e,
+            "native_fp32": native,
             "gpu_launches": launches_timed,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
                        "samples": clocks["samples"]},

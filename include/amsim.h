@@ -344,6 +344,15 @@ size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim
  */
 int amsim_softmax_rows(const float *S, float *P, int64_t rows, int cols, amsim_stream_t stream);
 
+/*
+ * Gradient of amsim_softmax_rows: dS[r,c] = P[r,c] * (dP[r,c] - sum_j P[r,j] dP[r,j])
+ * for `rows` rows of `cols` contiguous values, in exact fp32 (the backward of
+ * attention's softmax, between its approximate gradient contractions).  dS may
+ * alias dP.  Device pointers; asynchronous on `stream`.
+ */
+int amsim_softmax_rows_backward(const float *P, const float *dP, float *dS, int64_t rows, int cols,
+                                amsim_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -221,6 +221,14 @@ def softmax_rows(S) -> np.ndarray:
     return e / e.sum(axis=-1, keepdims=True)
 
 
+def softmax_rows_backward(P, dP) -> np.ndarray:
+    """Gradient of the row softmax: dS = P * (dP - sum_c P dP) per row (the
+    softmax Jacobian diag(P) - P P^T applied to dP), in double."""
+    P = np.asarray(P, dtype=np.float64)
+    dP = np.asarray(dP, dtype=np.float64)
+    return P * (dP - (P * dP).sum(axis=-1, keepdims=True))
+
+
 def attention_scores(kind, M, Q, K, scale, rows=None, nthreads=None):
     """S = scale * Q K^T for one (batch, head) slice, AMSim products (q, k)."""
     return gemm(kind, M, Q, K, transB=True, alpha=scale, rows=rows, nthreads=nthreads)

@@ -169,3 +169,24 @@ def test_attention_scores_scale_exact(orc):
     S, sa = orc.attention_scores("exact", 11, Qm, Km, 0.125)
     ref = 0.125 * (Qm.astype(np.float64) @ Km.astype(np.float64).T)
     assert close(S, ref, 0.125 * sa)
+
+
+def test_softmax_backward_matches_finite_differences():
+    """The softmax gradient reference equals the derivative of the softmax,
+    taken by central differences of the double softmax."""
+    import oracle as orc
+    rng = np.random.default_rng(71)
+    S = rng.standard_normal((5, 9))
+    dP = rng.standard_normal((5, 9))
+    dS = orc.softmax_rows_backward(orc.softmax_rows(S), dP)
+    h = 1e-6
+    num = np.empty_like(S)
+    for r in range(S.shape[0]):
+        for c in range(S.shape[1]):
+            Sp, Sm = S.copy(), S.copy()
+            Sp[r, c] += h
+            Sm[r, c] -= h
+            num[r, c] = ((orc.softmax_rows(Sp) - orc.softmax_rows(Sm))[r] * dP[r]).sum() / (2 * h)
+    assert np.allclose(dS, num, rtol=1e-6, atol=1e-9)
+    # rows of dS sum to zero (the softmax's outputs sum to one)
+    assert np.allclose(dS.sum(axis=1), 0.0, atol=1e-12)
