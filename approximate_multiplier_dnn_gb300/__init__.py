@@ -90,6 +90,7 @@ def lib():
         "amsim_lut_build_from_entries": ([vp, i32, ctypes.POINTER(vp)], i32),
         "amsim_lut_entries": ([vp, vp], i32),
         "amsim_lut_info": ([vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
+        "amsim_lut_set_closed_form": ([vp, i32], i32),
         "amsim_lut_destroy": ([vp], None),
         "amsim_mul": ([vp, vp, vp, i64, vp, vp], i32),
         "amsim_gemm": ([ch, ch, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp, vp, sz, vp], i32),
@@ -136,6 +137,7 @@ AMSIM_PATH_FIXUP = 32
 AMSIM_PATH_CONV_BOXES = 64
 AMSIM_PATH_RAW_TILES = 128
 AMSIM_PATH_PHASED = 256
+AMSIM_PATH_CLOSED_FORM = 512
 
 
 def amsim_last_path() -> int:
@@ -210,6 +212,10 @@ class Lut:
     def entries(self):
         return amsim_lut_entries(self.handle, self.M)
 
+    def set_closed_form(self, on: bool = True) -> "Lut":
+        amsim_lut_set_closed_form(self.handle, on)
+        return self
+
     def close(self):
         if self.handle:
             lib().amsim_lut_destroy(self.handle)
@@ -260,6 +266,10 @@ def amsim_lut_entries(lut, M: int):
     out = np.zeros(1 << (2 * M), dtype=np.uint32)
     _check("amsim_lut_entries", lib().amsim_lut_entries(_h(lut), out.ctypes.data))
     return out
+
+
+def amsim_lut_set_closed_form(lut, on: bool = True) -> None:
+    _check("amsim_lut_set_closed_form", lib().amsim_lut_set_closed_form(_h(lut), 1 if on else 0))
 
 
 def amsim_lut_info(lut):

@@ -19,6 +19,8 @@ struct amsim_lut_s {
     const void *d_narrow = nullptr;      // narrowed, index [first operand][second operand]
     const void *d_narrow_t = nullptr;    // narrowed, index [second operand][first operand]
     size_t narrow_bytes = 0;
+    int kind = -1;              // AMSIM_EXACT / AMSIM_MITCHELL when built from a kind, else -1
+    bool closed_form = false;   // raw-tile launches compute products in registers (kinds only)
 };
 
 namespace amsim {

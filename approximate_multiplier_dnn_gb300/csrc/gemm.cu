@@ -351,9 +351,17 @@ int encode_raw_map(CUtensorMap *map, const OperandDesc &d, int K, int batch, int
     return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
 }
 
+// Closed-form product code of the raw-tile kernel for a handle (0: the table).
+int alu_code(amsim_lut_t lut)
+{
+    if (!lut || !lut->closed_form) return 0;
+    return lut->kind == AMSIM_MITCHELL ? 1 : 2;
+}
+
 int launch_raw(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
                cudaStream_t st, const kern::PhaseTable *pt = nullptr)
 {
+    if (kp.alu) return kern::launch_raw_alu(kp, maps, pt, grid, smem, st);
     switch (width) {
     case 8: return kern::launch_raw_w8(kp, maps, pt, gl, grid, smem, st);
     case 16: return kern::launch_raw_w16(kp, maps, pt, gl, grid, smem, st);
@@ -376,7 +384,8 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     PlaneSet rps;
     const int rwlog = lut ? (lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2) : 0;
     if (lut && encode_tiled() && pl.iters < 0x7FFFFFFFLL && all_raw_ok(p, n, pl, false) &&
-        !(plan_planes(p, n, pl, lut->M, rwlog, &rps) && rps.n > 0 && planes_bytes_per_mac(p, n, pl, rps) < 0.01)) {
+        (alu_code(lut) ||
+         !(plan_planes(p, n, pl, lut->M, rwlog, &rps) && rps.n > 0 && planes_bytes_per_mac(p, n, pl, rps) < 0.01))) {
         // operand tiles are copied in place and decoded inside the GEMM
     } else if (lut && encode_tiled() && n == 1 && p[0].conv) {
         // convolution tiles are copied in place as tensor boxes
@@ -459,9 +468,14 @@ int encode_raw_problems(const Problem *p, int n, const Plan &pl, kern::KParams &
     return erc;
 }
 
-// Shared memory of the raw-tile kernel and whether its LUT is read from global.
+// Shared memory of the raw-tile kernel and whether its LUT is read from global
+// (closed-form launches stage no table).
 size_t raw_smem(amsim_lut_t lut, bool *gl)
 {
+    if (alu_code(lut)) {
+        *gl = false;
+        return (size_t)kern::raw_smem_bytes(0);
+    }
     bool raw_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
     if (!raw_gl && kern::raw_smem_bytes((int)lut->narrow_bytes) > kMaxSmemPerCta) raw_gl = true;
     *gl = raw_gl;
@@ -507,8 +521,11 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     // (the raw-tile kernel counts a launch's iterations in 32 bits)
     const bool raw_fits = pl.iters < 0x7FFFFFFFLL;
     const bool conv_raw = raw_fits && n == 1 && p[0].conv && pl.tiles[0] > 0 && encode_tiled();
+    // Closed-form products exist only in the raw-tile kernel, which then takes
+    // every problem it can read.
+    const int alu = alu_code(lut);
     if (conv_raw || (raw_fits && encode_tiled() && all_raw_ok(p, n, pl, true) &&
-                     !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01))) {
+                     (alu || !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01)))) {
         bool raw_gl = false;
         const size_t smem = raw_smem(lut, &raw_gl);
         kern::TmaMaps maps = {};
@@ -540,7 +557,8 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             erc = encode_raw_problems(p, n, pl, tp, maps);
         }
         if (erc == AMSIM_OK) {
-            tp.table_bytes = raw_gl ? 0 : (int)lut->narrow_bytes;
+            tp.alu = alu;
+            tp.table_bytes = (raw_gl || alu) ? 0 : (int)lut->narrow_bytes;
             tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
             tp.fused = pl.streamk ? 1 : 0;
             const dim3 grid((unsigned)blocks);
@@ -552,7 +570,8 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             if (rc == AMSIM_OK) {
                 const bool fix = pl.streamk && !tp.fused;
                 g_last_path |= AMSIM_PATH_RAW_TILES | (pl.streamk ? AMSIM_PATH_STREAMK : 0) |
-                               (fix ? AMSIM_PATH_FIXUP : 0) | (tp.conv ? AMSIM_PATH_CONV_BOXES : 0);
+                               (fix ? AMSIM_PATH_FIXUP : 0) | (tp.conv ? AMSIM_PATH_CONV_BOXES : 0) |
+                               (alu ? AMSIM_PATH_CLOSED_FORM : 0);
                 return fix ? kern::launch_fixup(tp, pl.ctas - 1, stream) : AMSIM_OK;
             }
             if (rc != AMSIM_EUNSUPPORTED) return rc;
@@ -809,7 +828,8 @@ int run_phased(const Problem *p, int n, int nphase, const int *first, const int 
         fill_params(p, n, pl, lut, tp);
         bool gl = false;
         const size_t smem = raw_smem(lut, &gl);
-        tp.table_bytes = gl ? 0 : (int)lut->narrow_bytes;
+        tp.alu = alu_code(lut);
+        tp.table_bytes = (gl || tp.alu) ? 0 : (int)lut->narrow_bytes;
         tp.ws = static_cast<float *>(ws);
         tp.nphase = nphase;
         for (int ph = 0; ph < nphase; ++ph) {
@@ -828,7 +848,8 @@ int run_phased(const Problem *p, int n, int nphase, const int *first, const int 
             tp.fused = 1;
             rc = launch_raw(lut->width_bits, tp, maps, gl, dim3((unsigned)pl.ctas), smem, stream, &pt);
             if (rc == AMSIM_OK) {
-                g_last_path = AMSIM_PATH_RAW_TILES | AMSIM_PATH_STREAMK | AMSIM_PATH_PHASED;
+                g_last_path = AMSIM_PATH_RAW_TILES | AMSIM_PATH_STREAMK | AMSIM_PATH_PHASED |
+                              (tp.alu ? AMSIM_PATH_CLOSED_FORM : 0);
                 return AMSIM_OK;
             }
             if (rc != kern::AMSIM_ENOTCOOP && rc != AMSIM_EUNSUPPORTED) return rc;

@@ -122,6 +122,7 @@ struct KParams {
     // (see ConvRaw); cv_u_tap: U boxes addressed (step in tap, row, tap)
     int conv, cv_u_tap;
     int direct;             // raw-tile kernel: some operand is read with plain loads
+    int alu;                // raw-tile kernel: closed-form products, no table (1 Mitchell, 2 exact)
     // Phases (raw-tile kernel, fused stream-K): phase ph holds launch
     // iterations [ph_iter0[ph], ph_iter0[ph + 1]) -- whole problems; every CTA
     // takes a share of every phase (PhaseTable), in phase order, and loads

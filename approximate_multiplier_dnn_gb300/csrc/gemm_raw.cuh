@@ -59,12 +59,44 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Closed-form operand decode (no table): off is the operand truncated to M
+// fraction bits (keep masks them) with its sign and exponent -- zeros and
+// denormals as signed zero -- or, with FRAC, the truncated fraction field
+// alone; s is decode()'s signed power-of-two scale.  flag marks values the
+// fast closed-form stages must not see: those decode() flags (|x| >= 2^64,
+// infinities, NaN) and nonzero |x| < 2^-63, whose products with each other
+// can fall below the smallest normal, where the table path's scale product
+// flushes them to zero.
+template <bool FRAC>
+__device__ __forceinline__ void decode_alu(float v, uint32_t keep, uint32_t &off, float &s, int &flag)
+{
+    const uint32_t x = __float_as_uint(v);
+    const uint32_t e = (x >> 23) & 0xFFu;
+    const uint32_t f = x & 0x7FFFFFu;
+    if constexpr (FRAC) off = f & keep;
+    else off = e ? (x & (0xFF800000u | keep)) : (x & 0x80000000u);
+    uint32_t sb = x & 0xFF800000u;
+    if (e == 255u && f) sb = 0x7FC00000u;
+    s = __uint_as_float(sb);
+    flag |= (e >= 191u) | (e - 1u < 63u);
+}
+
+// Decode mode DM: 0 the table's (offset, scale), 1 the closed-form truncated
+// value, 2 the closed-form truncated fraction; aux is the table offset's shift
+// (DM 0) or the mask of the kept fraction bits.
+template <int DM>
+__device__ __forceinline__ void decode_as(float v, int M, uint32_t aux, uint32_t &off, float &s, int &flag)
+{
+    if constexpr (DM == 0) decode(v, M, (int)aux, off, s, flag);
+    else decode_alu<DM == 2>(v, aux, off, s, flag);
+}
+
 // Decode a raw R-row tile into off/scl [BK][R].  k-fast tiles are [R][BK]
 // fp32 rows of 64 bytes whose 16-byte chunks the copy engine swizzled as
 // chunk ^ ((row >> 1) & 3); row-fast tiles are [BK][R].
-template <int R>
+template <int R, int DM>
 __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint32_t *off, float *scl, int M,
-                                           int offshift, int d, int &big)
+                                           uint32_t aux, int d, int &big)
 {
     if (kfast) {
 #pragma unroll 2
@@ -76,7 +108,7 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
             for (int i = 0; i < 4; ++i) {
                 uint32_t o;
                 float s;
-                decode(e[i], M, offshift, o, s, big);
+                decode_as<DM>(e[i], M, aux, o, s, big);
                 off[(4 * c + i) * R + r] = o;
                 scl[(4 * c + i) * R + r] = s;
             }
@@ -88,10 +120,10 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
             const float4 v = *reinterpret_cast<const float4 *>(raw + (k * R + r4) * 4);
             uint4 o;
             float4 s;
-            decode(v.x, M, offshift, o.x, s.x, big);
-            decode(v.y, M, offshift, o.y, s.y, big);
-            decode(v.z, M, offshift, o.z, s.z, big);
-            decode(v.w, M, offshift, o.w, s.w, big);
+            decode_as<DM>(v.x, M, aux, o.x, s.x, big);
+            decode_as<DM>(v.y, M, aux, o.y, s.y, big);
+            decode_as<DM>(v.z, M, aux, o.z, s.z, big);
+            decode_as<DM>(v.w, M, aux, o.w, s.w, big);
             *reinterpret_cast<uint4 *>(off + k * R + r4) = o;
             *reinterpret_cast<float4 *>(scl + k * R + r4) = s;
         }
@@ -100,8 +132,9 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
 
 // Decode four row-fast 64-row blocks ([BK][64] each, the filter gradient's
 // L tile) into columns 64 b .. 64 b + 63 of off/scl [BK][BL].
+template <int DM>
 __device__ __forceinline__ void raw_decode_blocks(const uint8_t *raw, uint32_t *off, float *scl, int M,
-                                                  int offshift, int d, int &big)
+                                                  uint32_t aux, int d, int &big)
 {
 #pragma unroll 2
     for (int task = d; task < (BL / 64) * BK * 16; task += kRawDecoders) {
@@ -110,10 +143,10 @@ __device__ __forceinline__ void raw_decode_blocks(const uint8_t *raw, uint32_t *
         const float4 v = *reinterpret_cast<const float4 *>(raw + ((b * BK + k) * 64 + r4) * 4);
         uint4 o;
         float4 s;
-        decode(v.x, M, offshift, o.x, s.x, big);
-        decode(v.y, M, offshift, o.y, s.y, big);
-        decode(v.z, M, offshift, o.z, s.z, big);
-        decode(v.w, M, offshift, o.w, s.w, big);
+        decode_as<DM>(v.x, M, aux, o.x, s.x, big);
+        decode_as<DM>(v.y, M, aux, o.y, s.y, big);
+        decode_as<DM>(v.z, M, aux, o.z, s.z, big);
+        decode_as<DM>(v.w, M, aux, o.w, s.w, big);
         *reinterpret_cast<uint4 *>(off + k * BL + 64 * b + r4) = o;
         *reinterpret_cast<float4 *>(scl + k * BL + 64 * b + r4) = s;
     }
@@ -257,12 +290,106 @@ struct RawSmem {
     int *flags;            // [kRawDec][decoder warps]: the stage holds |x| >= 2^64
 };
 
-// The producer warpgroup: thread 0 also issues the copies, kRawRing - 1 stages ahead.
+// One decoded stage with closed-form products (KIND 1 Mitchell, 2 exact),
+// same accumulator layout and summation order as compute_stage, so that the
+// sums equal the table path's bit for bit.  Uo holds truncated values
+// (sign | exponent | M fraction bits), Lo truncated values (exact) or
+// fractions in place (Mitchell).
+//  - Fast stages (every nonzero operand in [2^-63, 2^64)): Mitchell's product
+//    is the float whose bits are a's truncated value plus b's fraction --
+//    a's scale times Mitchell's factor, the fraction carry landing in the
+//    exponent exactly when the 2 (x + y) branch applies -- times b's scale;
+//    a zero a gives a denormal, which the multiply flushes to a signed zero.
+//    The exact product is the fp32 FMA of the two truncated values.  Each
+//    is exact and normal (exponent sum >= 1), as the table path's v * s is.
+//  - Other stages rebuild the table path's (v, s) and round the product
+//    before adding it, as compute_stage's slow stages do.
+template <int KIND, bool SLOW>
+__device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
+                                                  const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
+                                                  const float *__restrict__ Ls, int urow, int lcol)
+{
+#pragma unroll(kKkUnroll)
+    for (int kk = 0; kk < BK; ++kk) {
+        uint32_t lo[TN];
+        float2 sb[TN];
+#pragma unroll
+        for (int t4 = 0; t4 < TN / 4; ++t4) {
+            const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * BL + lcol + 4 * t4);
+            lo[4 * t4 + 0] = o.x; lo[4 * t4 + 1] = o.y; lo[4 * t4 + 2] = o.z; lo[4 * t4 + 3] = o.w;
+            if constexpr (SLOW || KIND == 1) {
+                const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * BL + lcol + 4 * t4);
+                sb[4 * t4 + 0] = make_float2(sc.x, sc.x);
+                sb[4 * t4 + 1] = make_float2(sc.y, sc.y);
+                sb[4 * t4 + 2] = make_float2(sc.z, sc.z);
+                sb[4 * t4 + 3] = make_float2(sc.w, sc.w);
+            }
+        }
+#pragma unroll
+        for (int ig = 0; ig < TM / 4; ++ig) {
+            const uint4 uo = *reinterpret_cast<const uint4 *>(Uo + kk * BU + urow + 4 * ig);
+            const uint32_t uov[4] = {uo.x, uo.y, uo.z, uo.w};
+            float2 sa[2];
+            if constexpr (SLOW) {
+                const float4 us = *reinterpret_cast<const float4 *>(Us + kk * BU + urow + 4 * ig);
+                sa[0] = make_float2(us.x, us.y);
+                sa[1] = make_float2(us.z, us.w);
+            }
+#pragma unroll
+            for (int ip = 0; ip < 2; ++ip) {
+#pragma unroll
+                for (int t = 0; t < TN; ++t) {
+                    float2 &a = acc[2 * ig + ip][t];
+                    const uint32_t u0 = uov[2 * ip], u1 = uov[2 * ip + 1];
+                    if constexpr (SLOW) {
+                        float2 v;
+                        if constexpr (KIND == 1) {
+                            v = make_float2(__uint_as_float(0x3F800000u + (u0 & 0x7FFFFFu) + lo[t]),
+                                            __uint_as_float(0x3F800000u + (u1 & 0x7FFFFFu) + lo[t]));
+                        } else {
+                            const float vb = __uint_as_float(0x3F800000u | (lo[t] & 0x7FFFFFu));
+                            v = make_float2(__fmul_rn(__uint_as_float(0x3F800000u | (u0 & 0x7FFFFFu)), vb),
+                                            __fmul_rn(__uint_as_float(0x3F800000u | (u1 & 0x7FFFFFu)), vb));
+                        }
+                        const float2 s = fmul2_ftz(sa[ip], sb[t]);
+                        a.x = __fadd_rn(a.x, __fmul_rn(v.x, s.x));
+                        a.y = __fadd_rn(a.y, __fmul_rn(v.y, s.y));
+                    } else if constexpr (KIND == 1) {
+                        const float2 w = make_float2(__uint_as_float(u0 + lo[t]), __uint_as_float(u1 + lo[t]));
+                        a = fadd2(a, fmul2_ftz(w, sb[t]));
+                    } else {
+                        const float b = __uint_as_float(lo[t]);
+                        a = ffma2(make_float2(__uint_as_float(u0), __uint_as_float(u1)), make_float2(b, b), a);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// A decoded stage of the raw-tile kernel: table entries (W = 8, 16, 32) or
+// closed forms (W = 1 Mitchell, 2 exact).
+template <int W, bool GL, bool SLOW>
+__device__ __forceinline__ void raw_stage(float2 (&acc)[TM / 2][TN], const uint32_t *Uo, const float *Us,
+                                          const uint32_t *Lo, const float *Ls, const uint8_t *lut, int urow,
+                                          int lcol)
+{
+    if constexpr (W <= 2) compute_stage_alu<W, SLOW>(acc, Uo, Us, Lo, Ls, urow, lcol);
+    else compute_stage<W, GL, SLOW, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+}
+
+// The producer warpgroup: thread 0 also issues the copies, kRawRing - 1 stages
+// ahead.  ALU: 0 table offsets, 1 / 2 Mitchell's / the exact closed form.
+template <int ALU>
 __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &maps, const RawSmem &sm)
 {
     const int d = threadIdx.x - kTmaConsumerThreads;
     const int lane = d & 31, dw = d >> 5;
-    const int offU = p.M + p.wlog, offL = p.wlog;
+    // decode modes and their shift / fraction mask (closed forms: U keeps its
+    // sign and exponent; L keeps them for the exact product, not for Mitchell's)
+    constexpr int DU = ALU ? 1 : 0, DL = ALU == 1 ? 2 : ALU ? 1 : 0;
+    const uint32_t keep = ((1u << p.M) - 1u) << (23 - p.M);
+    const uint32_t offU = ALU ? keep : (uint32_t)(p.M + p.wlog), offL = ALU ? keep : (uint32_t)p.wlog;
     long long it0, it1;
     cta_range(p, it0, it1);
     bool aborted = false;
@@ -320,13 +447,13 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
             cp_async_wait<0>();
             decoder_bar();          // every decoder's copies have landed
         }
-        raw_decode<BU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st),
+        raw_decode<BU, DU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st),
                        reinterpret_cast<float *>(st + BK * BU * 4), p.M, offU, d, big);
         if (p.conv == 2)
-            raw_decode_blocks(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+            raw_decode_blocks<DL>(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                               reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         else
-            raw_decode<BL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+            raw_decode<BL, DL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                            reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         mbar_arrive(&sm.raw_empty[rs]);
         const int any = __any_sync(0xFFFFFFFFu, big);
@@ -380,9 +507,9 @@ __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lu
 #pragma unroll
                 for (int w = 0; w < kRawDecoders / 32; ++w) any_big |= sm.flags[ds * (kRawDecoders / 32) + w];
                 if (any_big)
-                    compute_stage<W, GL, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                    raw_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
                 else
-                    compute_stage<W, GL, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                    raw_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
             }
             mbar_arrive(&sm.empty[ds]);
         }
@@ -474,12 +601,17 @@ __device__ __forceinline__ void wait_phases(const KParams &p, int nreq, int d, b
 // The producer warpgroup of a phased launch: thread 0 also issues the copies;
 // every decoder tracks the issue position, so that they can wait for a
 // phase's inputs together.
+template <int ALU>
 __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaMaps &maps, const PhaseTable &pt,
                                                    const RawSmem &sm)
 {
     const int d = threadIdx.x - kTmaConsumerThreads;
     const int lane = d & 31, dw = d >> 5;
-    const int offU = p.M + p.wlog, offL = p.wlog;
+    // decode modes and their shift / fraction mask (closed forms: U keeps its
+    // sign and exponent; L keeps them for the exact product, not for Mitchell's)
+    constexpr int DU = ALU ? 1 : 0, DL = ALU == 1 ? 2 : ALU ? 1 : 0;
+    const uint32_t keep = ((1u << p.M) - 1u) << (23 - p.M);
+    const uint32_t offU = ALU ? keep : (uint32_t)(p.M + p.wlog), offL = ALU ? keep : (uint32_t)p.wlog;
     IterCursor cur = cursor_start(p, pt), iss = cur;
     bool aborted = false;
     int issued = 0, gi = 0;    // stages copied, stages passed by the issue position
@@ -553,13 +685,13 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
             cp_async_wait<0>();
             decoder_bar();          // every decoder's copies have landed
         }
-        raw_decode<BU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st),
+        raw_decode<BU, DU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st),
                        reinterpret_cast<float *>(st + BK * BU * 4), p.M, offU, d, big);
         if (p.conv == 2)
-            raw_decode_blocks(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+            raw_decode_blocks<DL>(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                               reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         else
-            raw_decode<BL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+            raw_decode<BL, DL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                            reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         mbar_arrive(&sm.raw_empty[rs]);
         const int any = __any_sync(0xFFFFFFFFu, big);
@@ -670,9 +802,9 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const Phas
 #pragma unroll
                     for (int w = 0; w < kRawDecoders / 32; ++w) any_big |= sm.flags[ds * (kRawDecoders / 32) + w];
                     if (any_big)
-                        compute_stage<W, false, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                        raw_stage<W, false, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
                     else
-                        compute_stage<W, false, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                        raw_stage<W, false, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
                 }
                 mbar_arrive(&sm.empty[ds]);
             }
@@ -739,7 +871,7 @@ __device__ __forceinline__ void raw_kernel_body(const KParams &p, const TmaMaps 
         mbar_init(red, 1);
         mbar_init(lut_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if constexpr (!GL) {
+        if (!GL && p.table_bytes > 0) {
             // one bulk copy of the table (written when the LUT was built, before
             // any launch; its allocation is padded to 256 bytes), overlapping the
             // first tile copies; the consumers wait for it before their first stage
@@ -763,11 +895,12 @@ __device__ __forceinline__ void raw_kernel_body(const KParams &p, const TmaMaps 
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
     if (tid >= kTmaConsumerThreads) {
         if constexpr (kTmaProducerWarps == 4) reg_dealloc<kTmaProducerRegs>();
-        if constexpr (PH) raw_producer_phased(p, maps, *pt, sm);
-        else raw_producer(p, maps, sm);
+        constexpr int ALU = W <= 2 ? W : 0;
+        if constexpr (PH) raw_producer_phased<ALU>(p, maps, *pt, sm);
+        else raw_producer<ALU>(p, maps, sm);
     } else {
         if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
-        if constexpr (!GL) {
+        if (!GL && p.table_bytes > 0) {
             bool gave_up = false;
             mbar_wait(lut_bar, 0, gave_up);
         }
@@ -856,6 +989,9 @@ int launch_raw_w8(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, b
 int launch_raw_w16(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, bool gl, dim3 grid, size_t smem,
                    cudaStream_t st);
 int launch_raw_w32(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, bool gl, dim3 grid, size_t smem,
+                   cudaStream_t st);
+// Closed-form products (p.alu: 1 Mitchell, 2 exact), no table.
+int launch_raw_alu(const KParams &p, const TmaMaps &maps, const PhaseTable *pt, dim3 grid, size_t smem,
                    cudaStream_t st);
 
 }  // namespace kern

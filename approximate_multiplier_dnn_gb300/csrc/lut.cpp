@@ -191,7 +191,17 @@ int amsim_lut_build(int kind, int M, amsim_lut_t *out)
     std::vector<uint32_t> e(size_t(1) << (2 * M));
     int rc = amsim_lut_generate(kind, M, e.data());
     if (rc) return rc;
-    return build_from_entries(e.data(), M, out);
+    rc = build_from_entries(e.data(), M, out);
+    if (rc == AMSIM_OK) (*out)->kind = kind;
+    return rc;
+}
+
+int amsim_lut_set_closed_form(amsim_lut_t lut, int on)
+{
+    if (!lut) return AMSIM_EINVAL;
+    if (on && lut->kind != AMSIM_EXACT && lut->kind != AMSIM_MITCHELL) return AMSIM_EUNSUPPORTED;
+    lut->closed_form = on != 0;
+    return AMSIM_OK;
 }
 
 int amsim_lut_build_from_entries(const uint32_t *host_entries, int M, amsim_lut_t *out)

@@ -31,6 +31,11 @@ if ROOT not in sys.path:
 METRIC = "approx-GMAC/s for LUT-multiplier GEMM/conv at M=7"
 UNIT = "approx-GMAC/s"
 LOOKUPS_PER_CLK_PER_SM = 32     # one 4-byte shared-memory wavefront per clock per SM
+# Closed-form products per clock per SM (no table): Mitchell's costs an integer
+# add, half a paired fp32 multiply and half a paired fp32 add -- two issue
+# slots of the SM's four warp instructions per clock -> 64; the exact one half
+# a paired FMA on the 128 fp32 lanes -> 128.
+CLOSED_FORM_PER_CLK_PER_SM = {"mitchell": 64, "exact": 128}
 
 WORKLOADS = ("mlp", "mlp_layers", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "gemm64", "mul")
 
@@ -53,7 +58,7 @@ def env_int(name, default):
 
 
 # ---------------------------------------------------------------- workloads
-def make_step(name, lut_for, M=7):
+def make_step(name, lut_for, M=7, kind="mitchell"):
     from approximate_multiplier_dnn_gb300 import steps
     from approximate_multiplier_dnn_gb300 import workloads as wl
     if name == "mlp":
@@ -69,7 +74,7 @@ def make_step(name, lut_for, M=7):
                 "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_exact_M7")
     if name == "gemm4096":
         # the mantissa-width sweep runs this workload at M = 4 .. 11
-        return steps.SquareGemmStep(wl.square_gemm(4096), lut_for("mitchell", M)), f"gemm_4096^3_mitchell_M{M}"
+        return steps.SquareGemmStep(wl.square_gemm(4096), lut_for(kind, M)), f"gemm_4096^3_{kind}_M{M}"
     if name == "attention":
         return steps.AttentionStep(wl.attention(), lut_for("mitchell", 7)), "attention_32x16x512x64_mitchell_M7"
     if name == "conv1x1":
@@ -281,9 +286,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mantissa", type=int, default=7, help="LUT mantissa bits M (gemm4096 only: the M sweep)")
+    ap.add_argument("--kind", default="mitchell", choices=["mitchell", "exact"], help="multiplier (gemm4096 only)")
+    ap.add_argument("--closed-form", action="store_true",
+                    help="compute the built-in multipliers' products in registers instead of reading the LUT")
     args = ap.parse_args()
-    if args.mantissa != 7 and args.workload != "gemm4096":
-        ap.error("--mantissa applies to --workload gemm4096 only")
+    if (args.mantissa != 7 or args.kind != "mitchell") and args.workload != "gemm4096":
+        ap.error("--mantissa and --kind apply to --workload gemm4096 only")
+    if args.closed_form and args.workload == "mul":
+        ap.error("--closed-form applies to the contractions")
     if not 1 <= args.mantissa <= 11:
         ap.error("--mantissa must be in 1..11")
     args.warmup = max(args.warmup, 3)
@@ -308,10 +318,12 @@ def main():
 
     def lut_for(kind, M):
         if (kind, M) not in luts:
-            luts[(kind, M)] = am.Lut.build(kind, M)
+            luts[(kind, M)] = am.Lut.build(kind, M).set_closed_form(args.closed_form)
         return luts[(kind, M)]
 
-    step, wname = make_step(args.workload, lut_for, args.mantissa)
+    step, wname = make_step(args.workload, lut_for, args.mantissa, args.kind)
+    if args.closed_form:
+        wname += "_closed_form"
     stream = torch.cuda.current_stream()
     parts = step.parts()
     props = torch.cuda.get_device_properties(local)
@@ -401,6 +413,15 @@ def main():
                 "lut_residency": lut_residency(step.lut),
                 "lut_share_of_step": round(lut_share, 4), "sms": sms,
                 "sm_mhz": mhz}
+    if args.closed_form:
+        kinds = sorted({k for k, _ in luts})
+        per_clk = min(CLOSED_FORM_PER_CLK_PER_SM[k] for k in kinds)
+        cpeak = sms * per_clk * mhz * 1e6 / 1e9
+        roofline = dict(roofline, pipe=f"closed-form {'/'.join(kinds)} products: SMs x {per_clk} per clock x "
+                        "SM clock (issue slots / fp32 lanes)", peak=cpeak, unit="Gproduct/s",
+                        frac=achieved / cpeak, lookup_roofline_frac=achieved / peak,
+                        kernel="lutgemm_raw_kernel<1|2> (closed forms, no table); see amsim_last_path")
+        roofline.pop("lut_residency", None)
     if args.workload == "mul":
         # HBM-bound: 12 bytes per product (two operands in, one result out)
         hbm, src = measured_peaks()
@@ -450,7 +471,7 @@ def main():
             return {"Q": st.Q, "K": st.K, "V": st.V}
         return {"A": st.A, "B": st.B}
 
-    pair = [step, make_step(args.workload, lut_for, args.mantissa)[0]]
+    pair = [step, make_step(args.workload, lut_for, args.mantissa, args.kind)[0]]
     for _ in range(args.warmup):
         pair[1].run()
     ins = [step_inputs(st) for st in pair]

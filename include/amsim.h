@@ -83,7 +83,8 @@ enum amsim_path {
     AMSIM_PATH_FIXUP = 32,          /* cut tiles finished by the separate fixup kernel */
     AMSIM_PATH_CONV_BOXES = 64,     /* convolution operands as shifted or blocked tensor boxes */
     AMSIM_PATH_RAW_TILES = 128,     /* operand tiles copied in place by TMA, decoded in shared memory */
-    AMSIM_PATH_PHASED = 256         /* every phase of amsim_gemm_phased in one launch */
+    AMSIM_PATH_PHASED = 256,        /* every phase of amsim_gemm_phased in one launch */
+    AMSIM_PATH_CLOSED_FORM = 512    /* products computed in registers (amsim_lut_set_closed_form) */
 };
 int amsim_last_path(void);
 
@@ -135,6 +136,26 @@ int amsim_lut_entries(amsim_lut_t lut, uint32_t *host_dst);
 
 /* M, narrowed entry width in bits, and the left shift that restores an entry. */
 int amsim_lut_info(amsim_lut_t lut, int *M, int *width_bits, int *shift);
+
+/*
+ * Closed-form products for a handle built by amsim_lut_build (on != 0), or
+ * the table again (on == 0).  With it on, GEMM and convolution launches that
+ * take the raw-tile kernel (AMSIM_PATH_RAW_TILES, including phased launches)
+ * compute each product's mantissa factor in registers instead of reading the
+ * table -- the direct simulation the ApproxTrain page compares its LUT with
+ * (Sec. VII, Fig. 6):
+ *   AMSIM_MITCHELL: the fp32 whose bits are 1.0f + (qa + qb) << (23 - M),
+ *                   qa, qb the operands' truncated M-bit fractions (the sum's
+ *                   carry into the exponent is Mitchell's 2(x+y) branch);
+ *   AMSIM_EXACT:    (1 + qa/2^M) * (1 + qb/2^M) rounded to fp32 (exact, M <= 11).
+ * Both equal the table's entries bit for bit, so results are identical to the
+ * table's for the same plan; launches on other kernel paths keep reading the
+ * table.  Such launches add AMSIM_PATH_CLOSED_FORM to the path bits.  The
+ * setting belongs to the handle: calls enqueued after it changes see the new
+ * setting.  Errors: AMSIM_EINVAL for a null handle; AMSIM_EUNSUPPORTED when
+ * on != 0 and the handle was built from entries or a function.
+ */
+int amsim_lut_set_closed_form(amsim_lut_t lut, int on);
 
 /* Free the handle's device memory.  NULL is ignored. */
 void amsim_lut_destroy(amsim_lut_t lut);

@@ -132,3 +132,8 @@ def test_grouped_rejects_bad_arguments(L):
     probs = (am.GemmProblem * 1)()
     assert L.amsim_gemm_grouped(1, probs, None, None, 0, None) == am.AMSIM_EINVAL
     assert L.amsim_gemm_grouped_workspace_size(1, probs, None) == 0
+
+
+def test_closed_form_switch_rejects_null(L):
+    assert L.amsim_lut_set_closed_form(None, 1) == am.AMSIM_EINVAL
+    assert L.amsim_lut_set_closed_form(None, 0) == am.AMSIM_EINVAL

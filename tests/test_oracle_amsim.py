@@ -214,3 +214,21 @@ def test_nan_and_inf_propagation(orc):
         inf = orc.mul(kind, 7, np.full(1000, np.inf, np.float32), x)
         assert np.all(np.isinf(inf))
         assert np.array_equal(np.signbit(inf), np.signbit(x))
+
+
+@pytest.mark.parametrize("M", list(range(1, 12)))
+def test_closed_forms_equal_oracle_tables(orc, M):
+    """The register-only product values the raw-tile kernel computes for the
+    two built-in kinds equal the oracle's expanded table entries (entry +
+    1.0f's bits) for every index: Mitchell's is the float with bits
+    1.0f + (qa + qb) << (23 - M), the exact one the fp32 product of 1.qa and
+    1.qb."""
+    q = np.arange(1 << M, dtype=np.uint32)
+    qa, qb = np.meshgrid(q, q, indexing="ij")
+    one = np.uint32(0x3F800000)
+    mitchell = one + ((qa + qb) << np.uint32(23 - M))
+    fa = (one + (qa << np.uint32(23 - M))).view(np.float32)
+    fb = (one + (qb << np.uint32(23 - M))).view(np.float32)
+    exact = (fa * fb).view(np.uint32)
+    assert np.array_equal(mitchell.reshape(-1), orc.lut("mitchell", M) + one)
+    assert np.array_equal(exact.reshape(-1), orc.lut("exact", M) + one)
