@@ -59,36 +59,59 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// Closed-form operand decode (no table): off is the operand truncated to M
-// fraction bits (keep masks them) with its sign and exponent -- zeros and
-// denormals as signed zero -- or, with FRAC, the truncated fraction field
-// alone; s is decode()'s signed power-of-two scale.  flag marks values the
-// fast closed-form stages must not see: those decode() flags (|x| >= 2^64,
-// infinities, NaN) and nonzero |x| < 2^-63, whose products with each other
-// can fall below the smallest normal, where the table path's scale product
-// flushes them to zero.
-template <bool FRAC>
-__device__ __forceinline__ void decode_alu(float v, uint32_t keep, uint32_t &off, float &s, int &flag)
+// What a decoder thread saw in a stage that the fast stage computations must
+// not see: the table decode's flag (|x| >= 2^64, infinities, NaN), and for
+// closed forms the largest magnitude and the smallest nonzero magnitude
+// (minus one) as bit patterns.  Closed forms send to the slow computation the
+// values the table's does (magnitudes of 2^64 and up, infinities, NaN) and
+// nonzero magnitudes below 2^-63, whose products with each other can fall
+// below the smallest normal, where the table path's scale product flushes them.
+struct StageFlags {
+    int big = 0;
+    uint32_t amax = 0u, aminm1 = 0xFFFFFFFFu;
+    __device__ __forceinline__ int any() const
+    {
+        return big | (amax >= 0x5F800000u) | (aminm1 < 0x1FFFFFFFu);
+    }
+};
+
+// v * 1 with denormals flushed to signed zero (NaN stays NaN with its
+// fraction's top bit set).
+__device__ __forceinline__ uint32_t ftz_bits(float v)
 {
-    const uint32_t x = __float_as_uint(v);
-    const uint32_t e = (x >> 23) & 0xFFu;
-    const uint32_t f = x & 0x7FFFFFu;
-    if constexpr (FRAC) off = f & keep;
-    else off = e ? (x & (0xFF800000u | keep)) : (x & 0x80000000u);
-    uint32_t sb = x & 0xFF800000u;
-    if (e == 255u && f) sb = 0x7FC00000u;
-    s = __uint_as_float(sb);
-    flag |= (e >= 191u) | (e - 1u < 63u);
+    float r;
+    asm("mul.rn.ftz.f32 %0, %1, 0f3F800000;" : "=f"(r) : "f"(v));
+    return __float_as_uint(r);
+}
+
+// Closed-form operand decode (no table): without FRAC, off is the operand
+// truncated to the M fraction bits keep masks, sign and exponent kept and
+// denormals as signed zero (no scale is stored: the slow computation takes it
+// from off); with FRAC, off is that truncated fraction field alone and s the
+// signed power-of-two scale.
+template <bool FRAC>
+__device__ __forceinline__ void decode_alu(float v, uint32_t keep, uint32_t &off, float &s, StageFlags &fl)
+{
+    const uint32_t y = ftz_bits(v);
+    const uint32_t ax = y & 0x7FFFFFFFu;
+    fl.amax = max(fl.amax, ax);
+    fl.aminm1 = min(fl.aminm1, ax - 1u);
+    if constexpr (FRAC) {
+        off = y & keep;
+        s = __uint_as_float(y & 0xFF800000u);
+    } else {
+        off = y & (0xFF800000u | keep);
+    }
 }
 
 // Decode mode DM: 0 the table's (offset, scale), 1 the closed-form truncated
-// value, 2 the closed-form truncated fraction; aux is the table offset's shift
-// (DM 0) or the mask of the kept fraction bits.
+// value (no scale), 2 the closed-form truncated fraction and scale; aux is the
+// table offset's shift (DM 0) or the mask of the kept fraction bits.
 template <int DM>
-__device__ __forceinline__ void decode_as(float v, int M, uint32_t aux, uint32_t &off, float &s, int &flag)
+__device__ __forceinline__ void decode_as(float v, int M, uint32_t aux, uint32_t &off, float &s, StageFlags &fl)
 {
-    if constexpr (DM == 0) decode(v, M, (int)aux, off, s, flag);
-    else decode_alu<DM == 2>(v, aux, off, s, flag);
+    if constexpr (DM == 0) decode(v, M, (int)aux, off, s, fl.big);
+    else decode_alu<DM == 2>(v, aux, off, s, fl);
 }
 
 // Decode a raw R-row tile into off/scl [BK][R].  k-fast tiles are [R][BK]
@@ -96,7 +119,7 @@ __device__ __forceinline__ void decode_as(float v, int M, uint32_t aux, uint32_t
 // chunk ^ ((row >> 1) & 3); row-fast tiles are [BK][R].
 template <int R, int DM>
 __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint32_t *off, float *scl, int M,
-                                           uint32_t aux, int d, int &big)
+                                           uint32_t aux, int d, StageFlags &fl)
 {
     if (kfast) {
 #pragma unroll 2
@@ -108,9 +131,9 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
             for (int i = 0; i < 4; ++i) {
                 uint32_t o;
                 float s;
-                decode_as<DM>(e[i], M, aux, o, s, big);
+                decode_as<DM>(e[i], M, aux, o, s, fl);
                 off[(4 * c + i) * R + r] = o;
-                scl[(4 * c + i) * R + r] = s;
+                if constexpr (DM != 1) scl[(4 * c + i) * R + r] = s;
             }
         }
     } else {
@@ -120,12 +143,12 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
             const float4 v = *reinterpret_cast<const float4 *>(raw + (k * R + r4) * 4);
             uint4 o;
             float4 s;
-            decode_as<DM>(v.x, M, aux, o.x, s.x, big);
-            decode_as<DM>(v.y, M, aux, o.y, s.y, big);
-            decode_as<DM>(v.z, M, aux, o.z, s.z, big);
-            decode_as<DM>(v.w, M, aux, o.w, s.w, big);
+            decode_as<DM>(v.x, M, aux, o.x, s.x, fl);
+            decode_as<DM>(v.y, M, aux, o.y, s.y, fl);
+            decode_as<DM>(v.z, M, aux, o.z, s.z, fl);
+            decode_as<DM>(v.w, M, aux, o.w, s.w, fl);
             *reinterpret_cast<uint4 *>(off + k * R + r4) = o;
-            *reinterpret_cast<float4 *>(scl + k * R + r4) = s;
+            if constexpr (DM != 1) *reinterpret_cast<float4 *>(scl + k * R + r4) = s;
         }
     }
 }
@@ -134,7 +157,7 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
 // L tile) into columns 64 b .. 64 b + 63 of off/scl [BK][BL].
 template <int DM>
 __device__ __forceinline__ void raw_decode_blocks(const uint8_t *raw, uint32_t *off, float *scl, int M,
-                                                  uint32_t aux, int d, int &big)
+                                                  uint32_t aux, int d, StageFlags &fl)
 {
 #pragma unroll 2
     for (int task = d; task < (BL / 64) * BK * 16; task += kRawDecoders) {
@@ -143,12 +166,12 @@ __device__ __forceinline__ void raw_decode_blocks(const uint8_t *raw, uint32_t *
         const float4 v = *reinterpret_cast<const float4 *>(raw + ((b * BK + k) * 64 + r4) * 4);
         uint4 o;
         float4 s;
-        decode_as<DM>(v.x, M, aux, o.x, s.x, big);
-        decode_as<DM>(v.y, M, aux, o.y, s.y, big);
-        decode_as<DM>(v.z, M, aux, o.z, s.z, big);
-        decode_as<DM>(v.w, M, aux, o.w, s.w, big);
+        decode_as<DM>(v.x, M, aux, o.x, s.x, fl);
+        decode_as<DM>(v.y, M, aux, o.y, s.y, fl);
+        decode_as<DM>(v.z, M, aux, o.z, s.z, fl);
+        decode_as<DM>(v.w, M, aux, o.w, s.w, fl);
         *reinterpret_cast<uint4 *>(off + k * BL + 64 * b + r4) = o;
-        *reinterpret_cast<float4 *>(scl + k * BL + 64 * b + r4) = s;
+        if constexpr (DM != 1) *reinterpret_cast<float4 *>(scl + k * BL + 64 * b + r4) = s;
     }
 }
 
@@ -287,8 +310,15 @@ struct RawSmem {
     uint8_t *dec;          // kRawDec decoded stages of kTmaStageBytes
     uint8_t *raw;          // kRawRing raw stages of kRawStageBytes
     uint64_t *raw_full, *raw_empty, *full, *empty;
-    int *flags;            // [kRawDec][decoder warps]: the stage holds |x| >= 2^64
+    int *flags;            // [kRawDec][decoder warps]: the stage needs the slow computation (StageFlags)
 };
+
+// Signed power-of-two scale of a truncated value (sign | exponent | fraction
+// bits): zero for a zero, infinity for an infinity, NaN for a NaN.
+__device__ __forceinline__ float trunc_scale(uint32_t t)
+{
+    return __uint_as_float((t & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : (t & 0xFF800000u));
+}
 
 // One decoded stage with closed-form products (KIND 1 Mitchell, 2 exact),
 // same accumulator layout and summation order as compute_stage, so that the
@@ -317,12 +347,22 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
         for (int t4 = 0; t4 < TN / 4; ++t4) {
             const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * BL + lcol + 4 * t4);
             lo[4 * t4 + 0] = o.x; lo[4 * t4 + 1] = o.y; lo[4 * t4 + 2] = o.z; lo[4 * t4 + 3] = o.w;
-            if constexpr (SLOW || KIND == 1) {
+            if constexpr (KIND == 1) {
                 const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * BL + lcol + 4 * t4);
                 sb[4 * t4 + 0] = make_float2(sc.x, sc.x);
                 sb[4 * t4 + 1] = make_float2(sc.y, sc.y);
                 sb[4 * t4 + 2] = make_float2(sc.z, sc.z);
                 sb[4 * t4 + 3] = make_float2(sc.w, sc.w);
+            }
+            if constexpr (SLOW) {
+                // the scales, NaN included, from the truncated values (Mitchell's
+                // L scale and fraction together make one)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = 4 * t4 + i;
+                    const float b = KIND == 1 ? trunc_scale(__float_as_uint(sb[t].x) | lo[t]) : trunc_scale(lo[t]);
+                    sb[t] = make_float2(b, b);
+                }
             }
         }
 #pragma unroll
@@ -331,9 +371,8 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
             const uint32_t uov[4] = {uo.x, uo.y, uo.z, uo.w};
             float2 sa[2];
             if constexpr (SLOW) {
-                const float4 us = *reinterpret_cast<const float4 *>(Us + kk * BU + urow + 4 * ig);
-                sa[0] = make_float2(us.x, us.y);
-                sa[1] = make_float2(us.z, us.w);
+                sa[0] = make_float2(trunc_scale(uo.x), trunc_scale(uo.y));
+                sa[1] = make_float2(trunc_scale(uo.z), trunc_scale(uo.w));
             }
 #pragma unroll
             for (int ip = 0; ip < 2; ++ip) {
@@ -438,7 +477,7 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
         const ProbParams &q = p.pr[sp.pi];
         const uint8_t *raw = sm.raw + (size_t)rs * kRawStageBytes;
         uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
-        int big = 0;
+        StageFlags big;
         if (q.u_direct || q.l_direct) {
             uint8_t *rw = sm.raw + (size_t)rs * kRawStageBytes;
             if (q.u_direct) direct_copy<BU>(q.U, q.K, sp.b, q.u_bsel, sp.u_tile0, sp.kt * BK, rw, d);
@@ -456,7 +495,7 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
             raw_decode<BL, DL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                            reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         mbar_arrive(&sm.raw_empty[rs]);
-        const int any = __any_sync(0xFFFFFFFFu, big);
+        const int any = __any_sync(0xFFFFFFFFu, big.any());
         if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;
         mbar_arrive(&sm.full[ds]);
         if (p.direct && it + kRawRing < it1) {
@@ -676,7 +715,7 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
         const ProbParams &q = p.pr[sp.pi];
         const uint8_t *raw = sm.raw + (size_t)rs * kRawStageBytes;
         uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
-        int big = 0;
+        StageFlags big;
         if (q.u_direct || q.l_direct) {
             uint8_t *rw = sm.raw + (size_t)rs * kRawStageBytes;
             if (q.u_direct) direct_copy<BU>(q.U, q.K, sp.b, q.u_bsel, sp.u_tile0, sp.kt * BK, rw, d);
@@ -694,7 +733,7 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
             raw_decode<BL, DL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                            reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         mbar_arrive(&sm.raw_empty[rs]);
-        const int any = __any_sync(0xFFFFFFFFu, big);
+        const int any = __any_sync(0xFFFFFFFFu, big.any());
         if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;
         mbar_arrive(&sm.full[ds]);
         // the tile after the issue position is the next to be copied: pull its

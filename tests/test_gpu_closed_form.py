@@ -112,6 +112,16 @@ def test_closed_form_special_values(amd, orc, luts, cf, kind):
     A[40, 1] = np.float32(3e19)                     # >= 2^64
     B[1, 30] = np.float32(-2e19)                    # product overflows to -inf
     B[2, :] = np.float32(1e-39)
+    # magnitudes at the fast stages' lower edge: 2^-63 x 2^-63 products are the
+    # smallest normals; 2^-64 x 2^-64 ones fall below and are zero
+    j = np.arange(k, dtype=np.float32)
+    A[50, :] = np.ldexp(1.0 + (j % 8) / 8.0, -63).astype(np.float32)
+    B[:, 60] = np.ldexp(1.0 + (j % 5) / 4.0, -63).astype(np.float32)
+    A[60, :] = np.ldexp(1.0 + (j % 3) / 2.0, -64).astype(np.float32)
+    B[:, 70] = np.float32(2.0 ** -64)
+    # NaN with payloads (signalling, and negative quiet)
+    A[70, 9] = np.array([0x7F800001], np.uint32).view(np.float32)[0]
+    B[10, 80] = np.array([0xFFC00001], np.uint32).view(np.float32)[0]
     Ad, Bd = to_dev(A), to_dev(B)
     got_t, _ = gemm(amd, luts(kind, 7), Ad, Bd, m, n, k)
     got_c, path = gemm(amd, cf(kind, 7), Ad, Bd, m, n, k)
@@ -119,6 +129,8 @@ def test_closed_form_special_values(amd, orc, luts, cf, kind):
     same_bits(got_c, got_t, "C")
     ref, sa = orc.gemm(kind, 7, A, B)
     assert_close(got_c, ref, sa, "C")
+    assert got_c[60, 70] == 0.0 and 0.0 < abs(got_c[50, 60]) < 1e-33
+    assert np.isnan(got_c[70]).all() and np.isnan(got_c[:, 80]).all()
 
 
 @pytest.mark.parametrize("kind", ["mitchell", "exact"])
