@@ -8,7 +8,8 @@ attention reference (scaled QK^T, softmax in double, PV).
 
 Page followed: "ApproxTrain: Fast Simulation of Approximate Multipliers for
 DNN Training and Inference", Sec. V-A (Algorithm 1), Sec. V-B (Algorithm 2),
-Sec. VI-B (Algorithms 3 and 4, Fig. 8).
+Sec. VI-B (Algorithms 3 and 4, Fig. 8); depthwise convolution from Sec. III's
+Table I, written as the grouped case of those sums.
 
 Parity unpinned: nothing.  Every function here has a pin in
 ``tests/test_oracle_*.py`` (see the module docstrings there).
@@ -71,7 +72,8 @@ def lib():
                                         f64, vp, i64, vp, i32, vp, vp, i32]
             L.orc_gemm_rows.restype = i32
             for name in ("orc_conv2d_fwd_points", "orc_conv2d_bwd_data_points",
-                         "orc_conv2d_bwd_filter_points"):
+                         "orc_conv2d_bwd_filter_points", "orc_dwconv2d_fwd_points",
+                         "orc_dwconv2d_bwd_data_points", "orc_dwconv2d_bwd_filter_points"):
                 fn = getattr(L, name)
                 fn.argtypes = [i32, i32, vp, vp, vp, vp, i64, vp, vp, i32]
                 fn.restype = i32
@@ -210,6 +212,22 @@ def conv2d_bwd_data(kind, M, desc, dy, w, pts, nthreads=None):
 def conv2d_bwd_filter(kind, M, desc, x, dy, pts, nthreads=None):
     """dW (RSCK) at flat indices pts: sum over (n,p,q) of AMSim(x, dy)."""
     return _conv("orc_conv2d_bwd_filter_points", kind, M, desc, x, dy, pts, nthreads)
+
+
+def dwconv2d_fwd(kind, M, desc, x, w, pts, nthreads=None):
+    """Depthwise Y (NPQK, K = C*D) at flat indices pts: sum over (r,s) of
+    AMSim(x[..., c], w[r,s,c,d]) for output channel k = c*D + d; w is RSCD."""
+    return _conv("orc_dwconv2d_fwd_points", kind, M, desc, x, w, pts, nthreads)
+
+
+def dwconv2d_bwd_data(kind, M, desc, dy, w, pts, nthreads=None):
+    """Depthwise dX (NHWC) at flat indices pts: sum over (r,s,d) of AMSim(dy, w)."""
+    return _conv("orc_dwconv2d_bwd_data_points", kind, M, desc, dy, w, pts, nthreads)
+
+
+def dwconv2d_bwd_filter(kind, M, desc, x, dy, pts, nthreads=None):
+    """Depthwise dW (RSCD) at flat indices pts: sum over (n,p,q) of AMSim(x, dy)."""
+    return _conv("orc_dwconv2d_bwd_filter_points", kind, M, desc, x, dy, pts, nthreads)
 
 
 # ---------------------------------------------------------------- attention

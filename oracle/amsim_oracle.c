@@ -420,3 +420,127 @@ int orc_conv2d_out_hw(const int *desc, int *P, int *Q)
     *P = c.P; *Q = c.Q;
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Depthwise Conv2D (Sec. III, Table I lists it beside Conv2D; it is the
+ * convolution with one input channel per filter group).  Same descriptor,
+ * K = C * D output channels for a channel multiplier D; the filter is
+ * R x S x C x D and output channel k = c*D + d reads input channel c only:
+ *   Y[n,p,q,c*D+d]  = sum_{r,s}   X[n, p*sh-ph+r*dh, q*sw-pw+s*dw, c] * W[r,s,c,d]
+ *   dX[n,h,w,c]     = sum_{r,s,d} dY[n,p,q,c*D+d] * W[r,s,c,d]
+ *                     over p = (h+ph-r*dh)/sh, q = (w+pw-s*dw)/sw integral, in range
+ *   dW[r,s,c,d]     = sum_{n,p,q} X[n, p*sh-ph+r*dh, q*sw-pw+s*dw, c] * dY[n,p,q,c*D+d]
+ * Operand order as for Conv2D: (x, w), (dy, w), (x, dy). */
+
+static void orc_dw_fwd_pt(void *vctx, int64_t t)
+{
+    orc_conv_ctx *g = (orc_conv_ctx *)vctx;
+    const orc_conv *c = &g->c;
+    const int D = c->K / c->C;
+    int64_t idx = g->pts[t];
+    int k = (int)(idx % c->K); idx /= c->K;
+    int q = (int)(idx % c->Q); idx /= c->Q;
+    int p = (int)(idx % c->P); idx /= c->P;
+    int n = (int)idx;
+    int ch = k / D, d = k % D;
+    double s = 0.0, sa = 0.0;
+    for (int r = 0; r < c->R; ++r)
+        for (int ss = 0; ss < c->S; ++ss) {
+            float a = x_at(c, g->x, n, p * c->sh - c->ph + r * c->dh, q * c->sw - c->pw + ss * c->dw, ch);
+            float b = g->w[(((int64_t)r * c->S + ss) * c->C + ch) * D + d];
+            float pr = orc_amsim(g->kind, g->M, a, b);
+            s += (double)pr; sa += fabs((double)pr);
+        }
+    g->out[t] = (float)s;
+    if (g->sumabs) g->sumabs[t] = sa;
+}
+
+static void orc_dw_bwd_data_pt(void *vctx, int64_t t)
+{
+    orc_conv_ctx *g = (orc_conv_ctx *)vctx;
+    const orc_conv *c = &g->c;
+    const int D = c->K / c->C;
+    int64_t idx = g->pts[t];
+    int ch = (int)(idx % c->C); idx /= c->C;
+    int w = (int)(idx % c->W); idx /= c->W;
+    int h = (int)(idx % c->H); idx /= c->H;
+    int n = (int)idx;
+    double s = 0.0, sa = 0.0;
+    for (int r = 0; r < c->R; ++r)
+        for (int ss = 0; ss < c->S; ++ss)
+            for (int d = 0; d < D; ++d) {
+                int hp = h + c->ph - r * c->dh, wq = w + c->pw - ss * c->dw;
+                float a = 0.0f;
+                if (hp >= 0 && wq >= 0 && hp % c->sh == 0 && wq % c->sw == 0) {
+                    int p = hp / c->sh, q = wq / c->sw;
+                    if (p < c->P && q < c->Q)
+                        a = g->dy[(((int64_t)n * c->P + p) * c->Q + q) * c->K + ch * D + d];
+                }
+                float b = g->w[(((int64_t)r * c->S + ss) * c->C + ch) * D + d];
+                float pr = orc_amsim(g->kind, g->M, a, b);
+                s += (double)pr; sa += fabs((double)pr);
+            }
+    g->out[t] = (float)s;
+    if (g->sumabs) g->sumabs[t] = sa;
+}
+
+static void orc_dw_bwd_filter_pt(void *vctx, int64_t t)
+{
+    orc_conv_ctx *g = (orc_conv_ctx *)vctx;
+    const orc_conv *c = &g->c;
+    const int D = c->K / c->C;
+    int64_t idx = g->pts[t];
+    int d = (int)(idx % D); idx /= D;
+    int ch = (int)(idx % c->C); idx /= c->C;
+    int ss = (int)(idx % c->S); idx /= c->S;
+    int r = (int)idx;
+    double s = 0.0, sa = 0.0;
+    for (int n = 0; n < c->N; ++n)
+        for (int p = 0; p < c->P; ++p)
+            for (int q = 0; q < c->Q; ++q) {
+                float a = x_at(c, g->x, n, p * c->sh - c->ph + r * c->dh, q * c->sw - c->pw + ss * c->dw, ch);
+                float b = g->dy[(((int64_t)n * c->P + p) * c->Q + q) * c->K + ch * D + d];
+                float pr = orc_amsim(g->kind, g->M, a, b);
+                s += (double)pr; sa += fabs((double)pr);
+            }
+    g->out[t] = (float)s;
+    if (g->sumabs) g->sumabs[t] = sa;
+}
+
+static int orc_dw_run(int which, int kind, int M, const int *desc,
+                      const float *x, const float *w, const float *dy,
+                      const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
+{
+    orc_conv_ctx g;
+    if (M < 1 || M > 11) return ORC_EINVAL;
+    if (orc_conv_init(desc, &g.c)) return ORC_EINVAL;
+    if (g.c.K % g.c.C) return ORC_EINVAL;
+    int64_t total;
+    if (which == 0) total = (int64_t)g.c.N * g.c.P * g.c.Q * g.c.K;
+    else if (which == 1) total = (int64_t)g.c.N * g.c.H * g.c.W * g.c.C;
+    else total = (int64_t)g.c.R * g.c.S * g.c.K;
+    for (int64_t t = 0; t < npts; ++t)
+        if (pts[t] < 0 || pts[t] >= total) return ORC_EINVAL;
+    g.kind = kind; g.M = M; g.x = x; g.w = w; g.dy = dy; g.pts = pts; g.out = out; g.sumabs = sumabs;
+    orc_parallel(which == 0 ? orc_dw_fwd_pt : which == 1 ? orc_dw_bwd_data_pt : orc_dw_bwd_filter_pt,
+                 &g, npts, nthreads);
+    return ORC_OK;
+}
+
+int orc_dwconv2d_fwd_points(int kind, int M, const int *desc, const float *x, const float *w,
+                            const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
+{
+    return orc_dw_run(0, kind, M, desc, x, w, NULL, pts, npts, out, sumabs, nthreads);
+}
+
+int orc_dwconv2d_bwd_data_points(int kind, int M, const int *desc, const float *dy, const float *w,
+                                 const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
+{
+    return orc_dw_run(1, kind, M, desc, NULL, w, dy, pts, npts, out, sumabs, nthreads);
+}
+
+int orc_dwconv2d_bwd_filter_points(int kind, int M, const int *desc, const float *x, const float *dy,
+                                   const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
+{
+    return orc_dw_run(2, kind, M, desc, x, NULL, dy, pts, npts, out, sumabs, nthreads);
+}

@@ -190,3 +190,91 @@ def test_softmax_backward_matches_finite_differences():
     assert np.allclose(dS, num, rtol=1e-6, atol=1e-9)
     # rows of dS sum to zero (the softmax's outputs sum to one)
     assert np.allclose(dS.sum(axis=1), 0.0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ depthwise conv
+DW_GEOMS = [
+    # N, H, W, C, D, R, S, stride, pad, dil
+    (2, 7, 6, 3, 1, 3, 3, (1, 1), (1, 1), (1, 1)),
+    (1, 9, 8, 2, 3, 3, 2, (2, 1), (1, 0), (1, 1)),
+    (2, 8, 9, 4, 2, 3, 3, (1, 2), (2, 2), (2, 1)),
+    (1, 10, 7, 3, 1, 5, 3, (3, 2), (2, 2), (1, 2)),
+    (1, 5, 5, 5, 1, 1, 1, (1, 1), (0, 0), (1, 1)),
+]
+
+
+@pytest.mark.parametrize("g", DW_GEOMS)
+def test_dwconv_exact_kind_equals_torch_grouped_float64(orc, g):
+    """Depthwise = torch's grouped convolution with one group per input channel
+    (weight [C*D, 1, R, S], output channel c*D + d reads channel c)."""
+    torch = _torch()
+    import torch.nn.functional as F
+    N, H, W, C, D, R, S, st, pd, dl = g
+    K = C * D
+    rng = np.random.default_rng(100 + sum(g[:7]))
+    desc = orc.conv_desc(N, H, W, C, K, R, S, st, pd, dl)
+    P, Q = orc.conv_out_hw(desc)
+    x = short_mantissa((N, H, W, C), rng)
+    w = short_mantissa((R, S, C, D), rng)
+    dy = short_mantissa((N, P, Q, K), rng)
+    xt = torch.from_numpy(x.astype(np.float64)).permute(0, 3, 1, 2)
+    wt = torch.from_numpy(w.astype(np.float64)).reshape(R, S, K).permute(2, 0, 1).unsqueeze(1)  # K 1 R S
+    dyt = torch.from_numpy(dy.astype(np.float64)).permute(0, 3, 1, 2)
+
+    yref = F.conv2d(xt, wt, stride=st, padding=pd, dilation=dl, groups=C).permute(0, 2, 3, 1).numpy()
+    assert yref.shape == (N, P, Q, K)
+    y, sa = orc.dwconv2d_fwd("exact", 11, desc, x, w, np.arange(yref.size))
+    assert close(y, yref.reshape(-1), sa)
+
+    dxref = torch.nn.grad.conv2d_input((N, C, H, W), wt, dyt, stride=st, padding=pd, dilation=dl,
+                                       groups=C).permute(0, 2, 3, 1).numpy()
+    dx, sa = orc.dwconv2d_bwd_data("exact", 11, desc, dy, w, np.arange(dxref.size))
+    assert close(dx, dxref.reshape(-1), sa)
+
+    dwref = torch.nn.grad.conv2d_weight(xt, (K, 1, R, S), dyt, stride=st, padding=pd, dilation=dl,
+                                        groups=C)                                           # K 1 R S
+    dwref = dwref[:, 0].permute(1, 2, 0).numpy()                                            # R S K = R S C D
+    dw, sa = orc.dwconv2d_bwd_filter("exact", 11, desc, x, dy, np.arange(dwref.size))
+    assert close(dw, dwref.reshape(-1), sa)
+
+
+def test_dwconv_single_channel_equals_conv(orc):
+    """With one input channel the depthwise sums are the ordinary Conv2D sums
+    (K = D output channels), Mitchell products included."""
+    rng = np.random.default_rng(41)
+    N, H, W, D, R, S = 2, 6, 5, 3, 3, 2
+    desc = orc.conv_desc(N, H, W, 1, D, R, S, (2, 1), (1, 1), (1, 2))
+    P, Q = orc.conv_out_hw(desc)
+    x = rng.standard_normal((N, H, W, 1)).astype(np.float32)
+    w = rng.standard_normal((R, S, 1, D)).astype(np.float32)
+    dy = rng.standard_normal((N, P, Q, D)).astype(np.float32)
+    for dwf, cf, a, b, size in ((orc.dwconv2d_fwd, orc.conv2d_fwd, x, w, N * P * Q * D),
+                                (orc.dwconv2d_bwd_data, orc.conv2d_bwd_data, dy, w, N * H * W),
+                                (orc.dwconv2d_bwd_filter, orc.conv2d_bwd_filter, x, dy, R * S * D)):
+        got, sa = dwf("mitchell", 7, desc, a, b, np.arange(size))
+        ref, sr = cf("mitchell", 7, desc, a, b, np.arange(size))
+        assert np.array_equal(got, ref) and np.array_equal(sa, sr)
+
+
+def test_dwconv_channels_are_independent(orc):
+    """Each output channel of a depthwise convolution equals a one-channel
+    convolution of its own input channel with its own filter slice."""
+    rng = np.random.default_rng(42)
+    N, H, W, C, D, R, S = 1, 5, 6, 3, 2, 3, 3
+    desc = orc.conv_desc(N, H, W, C, C * D, R, S, (1, 1), (1, 1), (1, 1))
+    P, Q = orc.conv_out_hw(desc)
+    x = rng.standard_normal((N, H, W, C)).astype(np.float32)
+    w = rng.standard_normal((R, S, C, D)).astype(np.float32)
+    y, _ = orc.dwconv2d_fwd("mitchell", 7, desc, x, w, np.arange(N * P * Q * C * D))
+    y = y.reshape(N, P, Q, C, D)
+    d1 = orc.conv_desc(N, H, W, 1, D, R, S, (1, 1), (1, 1), (1, 1))
+    for c in range(C):
+        ref, _ = orc.conv2d_fwd("mitchell", 7, d1, x[..., c:c + 1], w[:, :, c:c + 1, :], np.arange(N * P * Q * D))
+        assert np.array_equal(y[..., c, :].reshape(-1), ref)
+
+
+def test_dwconv_rejects_channels_not_dividing(orc):
+    desc = orc.conv_desc(1, 4, 4, 3, 4, 3, 3, (1, 1), (1, 1), (1, 1))
+    with pytest.raises(ValueError):
+        orc.dwconv2d_fwd("exact", 7, desc, np.zeros((1, 4, 4, 3), np.float32),
+                         np.zeros((3, 3, 3, 1), np.float32), np.arange(4))
