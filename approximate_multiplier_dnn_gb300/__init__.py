@@ -109,6 +109,10 @@ def lib():
         "amsim_conv2d_bwd_data": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
         "amsim_conv2d_bwd_filter": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
         "amsim_conv2d_workspace_size": ([ctypes.POINTER(ConvDesc), i32, vp], sz),
+        "amsim_dwconv2d_fwd": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
+        "amsim_dwconv2d_bwd_data": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
+        "amsim_dwconv2d_bwd_filter": ([ctypes.POINTER(ConvDesc), vp, vp, vp, vp, vp, sz, vp], i32),
+        "amsim_dwconv2d_workspace_size": ([ctypes.POINTER(ConvDesc), i32, vp], sz),
         "amsim_softmax_rows": ([vp, vp, i64, i32, vp], i32),
         "amsim_softmax_rows_backward": ([vp, vp, vp, i64, i32, vp], i32),
     }
@@ -138,6 +142,8 @@ AMSIM_PATH_CONV_BOXES = 64
 AMSIM_PATH_RAW_TILES = 128
 AMSIM_PATH_PHASED = 256
 AMSIM_PATH_CLOSED_FORM = 512
+AMSIM_PATH_DW_TILES = 1024
+AMSIM_PATH_DW_DIRECT = 2048
 
 
 def amsim_last_path() -> int:
@@ -390,6 +396,23 @@ def amsim_conv2d_bwd_filter(desc, x, dy, dw, lut, ws=None, ws_bytes=None, stream
 
 def amsim_conv2d_workspace_size(desc, which: int, lut) -> int:
     return int(lib().amsim_conv2d_workspace_size(ctypes.byref(desc), int(which), _h(lut)))
+
+
+def amsim_dwconv2d_fwd(desc, x, w, y, lut, ws=None, ws_bytes=None, stream=None):
+    """Depthwise forward; desc.K = C * D, w is R x S x C x D."""
+    _conv("amsim_dwconv2d_fwd", desc, x, w, y, lut, ws, ws_bytes, stream)
+
+
+def amsim_dwconv2d_bwd_data(desc, dy, w, dx, lut, ws=None, ws_bytes=None, stream=None):
+    _conv("amsim_dwconv2d_bwd_data", desc, dy, w, dx, lut, ws, ws_bytes, stream)
+
+
+def amsim_dwconv2d_bwd_filter(desc, x, dy, dw, lut, ws=None, ws_bytes=None, stream=None):
+    _conv("amsim_dwconv2d_bwd_filter", desc, x, dy, dw, lut, ws, ws_bytes, stream)
+
+
+def amsim_dwconv2d_workspace_size(desc, which: int, lut) -> int:
+    return int(lib().amsim_dwconv2d_workspace_size(ctypes.byref(desc), int(which), _h(lut)))
 
 
 def amsim_softmax_rows_backward(P, dP, dS, rows, cols, stream=None):

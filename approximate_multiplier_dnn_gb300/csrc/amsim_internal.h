@@ -31,6 +31,7 @@ constexpr int kMaxSmemPerCta = 227 * 1024;
 int check_lut(amsim_lut_t lut);   // AMSIM_OK if usable on the current device
 void count_launch();              // one kernel enqueued by the library
 int cuda_status(cudaError_t e);   // maps to AMSIM_OK / AMSIM_ECUDA / AMSIM_ENOMEM
+void set_last_path(int bits);     // the calling thread's amsim_last_path() value
 
 // One GEMM operand in the kernel's terms: element (row r, reduction index k).
 // Dense: value at ptr[batch*batch_stride + r*s_row + k*s_k].

@@ -976,6 +976,8 @@ size_t gemm_workspace(char transA, char transB, int m, int n, int k, int batch, 
     return streamk_only ? problems_workspace_streamk(&pr, 1, lut) : problem_workspace(pr, lut);
 }
 
+void set_last_path(int bits) { g_last_path = bits; }
+
 }  // namespace amsim
 
 extern "C" {

@@ -14,6 +14,7 @@ from . import (ConvDesc, GemmProblem, amsim_mul, amsim_conv2d_bwd_data, amsim_co
                amsim_conv2d_out_hw, amsim_conv2d_workspace_size, amsim_gemm, amsim_gemm_grouped,
                amsim_gemm_grouped_workspace_size, amsim_gemm_phased, amsim_gemm_phased_workspace_size,
                amsim_gemm_strided_batched, amsim_gemm_workspace_size,
+               amsim_dwconv2d_bwd_data, amsim_dwconv2d_bwd_filter, amsim_dwconv2d_fwd, amsim_dwconv2d_workspace_size,
                amsim_softmax_rows, workspace)
 
 
@@ -293,6 +294,97 @@ class ConvStep:
             amsim_conv2d_bwd_data(self.desc, self.dy, self.w, self.dx, self.lut, ws=self.ws, stream=stream)
         if 2 in self.passes:
             amsim_conv2d_bwd_filter(self.desc, self.x, self.dy, self.dw, self.lut, ws=self.ws, stream=stream)
+
+
+class DwConvStep:
+    """Depthwise Conv2D forward, preceding-layer gradient and weight gradient
+    of one NHWC layer with a channel multiplier D (K = C*D output channels)."""
+
+    def __init__(self, data: dict, geom: dict, lut, device="cuda", passes=(0, 1, 2)):
+        import torch
+        self.lut = lut
+        g = geom
+        self.desc = ConvDesc.make(g["N"], g["H"], g["W"], g["C"], g["C"] * g["D"], g["R"], g["S"], g["stride"],
+                                  g["pad"], g["dil"])
+        self.P, self.Q = amsim_conv2d_out_hw(self.desc)
+        self.x = _dev(data["x"], device)
+        self.w = _dev(data["w"], device)
+        self.dy = _dev(data["dy"], device) if "dy" in data else None
+        self.passes = tuple(passes)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.y = torch.empty((g["N"], self.P, self.Q, g["C"] * g["D"]), **f32) if 0 in self.passes else None
+        self.dx = torch.empty_like(self.x) if 1 in self.passes else None
+        self.dw = torch.empty_like(self.w) if 2 in self.passes else None
+        self.g = g
+        self.ws = workspace(max(amsim_dwconv2d_workspace_size(self.desc, p, lut) for p in self.passes), device)
+
+    @property
+    def per_pass(self) -> int:
+        g = self.g
+        return g["N"] * self.P * self.Q * g["C"] * g["D"] * g["R"] * g["S"]
+
+    @property
+    def macs(self) -> int:
+        return len(self.passes) * self.per_pass
+
+    def pass_bytes(self, p) -> int:
+        """Compulsory DRAM bytes of pass p: it reads its two operands once and
+        writes its output once (4 bytes per element); the three passes touch
+        the same three tensors (x, w, y) or their gradients."""
+        g = self.g
+        nx = g["N"] * g["H"] * g["W"] * g["C"]
+        ny = g["N"] * self.P * self.Q * g["C"] * g["D"]
+        nw = g["R"] * g["S"] * g["C"] * g["D"]
+        return 4 * (nx + ny + nw)
+
+    @property
+    def tiled(self) -> bool:
+        """Whether the geometry takes the tiled kernel (3x3, unit stride and
+        dilation, one filter per channel, channels a multiple of 4)."""
+        g = self.g
+        return (g["D"] == 1 and g["R"] == 3 and g["S"] == 3 and tuple(g["stride"]) == (1, 1)
+                and tuple(g["dil"]) == (1, 1) and g["C"] % 4 == 0)
+
+    def outputs(self) -> list:
+        return [t for t in (self.y, self.dx, self.dw) if t is not None]
+
+    def _call(self, p, stream):
+        if p == 0:
+            amsim_dwconv2d_fwd(self.desc, self.x, self.w, self.y, self.lut, ws=self.ws, stream=stream)
+        elif p == 1:
+            amsim_dwconv2d_bwd_data(self.desc, self.dy, self.w, self.dx, self.lut, ws=self.ws, stream=stream)
+        else:
+            amsim_dwconv2d_bwd_filter(self.desc, self.x, self.dy, self.dw, self.lut, ws=self.ws, stream=stream)
+
+    def parts(self, stream=None):
+        names = {0: "fwd", 1: "bwd_data", 2: "bwd_filter"}
+        return [(names[p], (lambda p=p: self._call(p, stream)), self.per_pass,
+                 1 + (amsim_dwconv2d_workspace_size(self.desc, p, self.lut) > 0)) for p in self.passes]
+
+    def run(self, stream=None):
+        for p in self.passes:
+            self._call(p, stream)
+
+    def native(self):
+        """The same passes with torch fp32 (cuDNN grouped convolution, one group
+        per input channel) on channels-last views."""
+        import torch.nn.functional as F
+        from torch.nn import grad as nng
+        g = self.g
+        st, pd, dl = tuple(g["stride"]), tuple(g["pad"]), tuple(g["dil"])
+        K = g["C"] * g["D"]
+        x = self.x.permute(0, 3, 1, 2)                                   # N C H W view of NHWC
+        w = self.w.reshape(g["R"], g["S"], K).permute(2, 0, 1).unsqueeze(1).contiguous()   # K 1 R S
+        dy = self.dy.permute(0, 3, 1, 2) if self.dy is not None else None
+        fns = []
+        if 0 in self.passes:
+            fns.append(lambda: F.conv2d(x, w, stride=st, padding=pd, dilation=dl, groups=g["C"]))
+        if 1 in self.passes:
+            fns.append(lambda: nng.conv2d_input(x.shape, w, dy, stride=st, padding=pd, dilation=dl, groups=g["C"]))
+        if 2 in self.passes:
+            fns.append(lambda: nng.conv2d_weight(x, w.shape, dy, stride=st, padding=pd, dilation=dl,
+                                                 groups=g["C"]))
+        return lambda: [f() for f in fns]
 
 
 class SquareGemmStep:

@@ -120,3 +120,15 @@ CONV1X1 = dict(N=64, H=56, W=56, C=256, K=256, R=1, S=1, stride=(1, 1), pad=(0, 
 
 def conv1x1(N=64, H=56, W=56, C=256, K=256, seed=0):
     return {"x": normal((N, H, W, C), 1.0, seed), "w": he_normal((1, 1, C, K), C, seed + 1)}
+
+
+# MobileNet-style depthwise 3x3 layer (depthwise convolution: ApproxTrain Table I)
+DWCONV3X3 = dict(N=64, H=56, W=56, C=128, D=1, R=3, S=3, stride=(1, 1), pad=(1, 1), dil=(1, 1))
+
+
+def dwconv3x3(N=64, H=56, W=56, C=128, D=1, seed=0):
+    """NHWC input ~ N(0,1), 3x3 depthwise filter (R, S, C, D) He-normal over
+    its 9 taps, NPQK dY ~ N(0, 0.01^2)."""
+    return {"x": normal((N, H, W, C), 1.0, seed),
+            "w": he_normal((3, 3, C, D), 9, seed + 1),
+            "dy": normal((N, H, W, C * D), 0.01, seed + 2)}

@@ -37,7 +37,8 @@ LOOKUPS_PER_CLK_PER_SM = 32     # one 4-byte shared-memory wavefront per clock p
 # a paired FMA on the 128 fp32 lanes -> 128.
 CLOSED_FORM_PER_CLK_PER_SM = {"mitchell": 64, "exact": 128}
 
-WORKLOADS = ("mlp", "mlp_layers", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "gemm64", "mul")
+WORKLOADS = ("mlp", "mlp_layers", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "dwconv3x3",
+             "gemm64", "mul")
 
 
 def measured_peaks():
@@ -80,6 +81,9 @@ def make_step(name, lut_for, M=7, kind="mitchell"):
     if name == "conv1x1":
         return (steps.ConvStep(wl.conv1x1(), wl.CONV1X1, lut_for("mitchell", 7), passes=(0,)),
                 "conv1x1_nhwc_64x56x56x256_k256_fwd_mitchell_M7")
+    if name == "dwconv3x3":
+        return (steps.DwConvStep(wl.dwconv3x3(), wl.DWCONV3X3, lut_for("mitchell", 7)),
+                "dwconv3x3_nhwc_64x56x56x128_d1_fwd+bwd_data+bwd_filter_mitchell_M7")
     if name == "mul":
         from approximate_multiplier_dnn_gb300 import steps as st
         return st.MulStep(wl.elementwise_pairs(1 << 28, seed=5), lut_for("mitchell", 7)), \
@@ -118,6 +122,28 @@ def oracle_parts(name):
     if name == "gemm4096":
         d = wl.square_gemm(4096)
         return [(lambda rows: oracle.gemm("mitchell", 7, d["A"], d["B"], rows=rows), 4096, 4096 * 4096)]
+    if name == "dwconv3x3":
+        # a "row" is a block of 64 consecutive outputs (forward, data gradient)
+        # or one filter-gradient element (a sum over every N*P*Q pixel)
+        d, g = wl.dwconv3x3(), wl.DWCONV3X3
+        desc = oracle.conv_desc(g["N"], g["H"], g["W"], g["C"], g["C"] * g["D"], g["R"], g["S"], g["stride"],
+                                g["pad"], g["dil"])
+        P, Q = oracle.conv_out_hw(desc)
+        ny = g["N"] * P * Q * g["C"] * g["D"]
+        nx = g["N"] * g["H"] * g["W"] * g["C"]
+        taps = g["R"] * g["S"]
+
+        def blocks(rows):
+            return (rows.astype(np.int64)[:, None] * 64 + np.arange(64)).reshape(-1)
+
+        out.append((lambda rows: oracle.dwconv2d_fwd("mitchell", 7, desc, d["x"], d["w"], blocks(rows)),
+                    ny // 64, 64 * taps))
+        out.append((lambda rows: oracle.dwconv2d_bwd_data("mitchell", 7, desc, d["dy"], d["w"], blocks(rows)),
+                    nx // 64, 64 * taps * g["D"]))
+        out.append((lambda rows: oracle.dwconv2d_bwd_filter("mitchell", 7, desc, d["x"], d["dy"],
+                                                            rows.astype(np.int64)),
+                    taps * g["C"] * g["D"], g["N"] * P * Q))
+        return out
     raise SystemExit(f"no oracle sampler for workload {name}")
 
 
@@ -218,21 +244,22 @@ def lut_residency(lut):
 # sources of the LUT-GEMM kernels (the kernel the traffic records measure);
 # a record holds for one version of them
 KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_ws.cuh", "gemm_tma.cuh", "gemm_raw.cuh")
+DW_KERNEL_SOURCES = ("gemm_kernel.cuh", "dwconv.cu")
 
 
-def kernel_sha():
+def kernel_sha(sources=KERNEL_SOURCES):
     csrc = os.path.join(ROOT, "approximate_multiplier_dnn_gb300", "csrc")
     h = hashlib.sha1()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:12]
 
 
-def recorded_traffic(workload):
-    """Per-launch DRAM bytes of the LUT-GEMM kernel from a committed ncu
+def recorded_traffic(workload, sources=KERNEL_SOURCES):
+    """Per-launch DRAM bytes of the dominant kernel from a committed ncu
     summary, if it was taken on the current kernel source; else None."""
     try:
-        sha = kernel_sha()
+        sha = kernel_sha(sources)
         with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             for line in f:
                 kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
@@ -422,6 +449,34 @@ def main():
                         frac=achieved / cpeak, lookup_roofline_frac=achieved / peak,
                         kernel="lutgemm_raw_kernel<1|2> (closed forms, no table); see amsim_last_path")
         roofline.pop("lut_residency", None)
+    if args.workload == "dwconv3x3":
+        # a stencil: each pass reads its operands once and writes its output
+        # once, with 9 products per output element.  Every pass's two lower
+        # bounds (compulsory DRAM bytes at the measured copy bandwidth, lookups
+        # at the shared-memory pipe's rate) are reported; the roofline is that
+        # of the pass that takes longest, against the larger of its bounds.
+        hbm, src = measured_peaks()
+        per = {}
+        for i, p in enumerate(parts):
+            t_ms = ms_per_step * part_ms[i] / max(1e-12, sum(part_ms))
+            nbytes = step.pass_bytes(step.passes[i])
+            per[p[0]] = {"ms": t_ms, "bytes": nbytes, "macs": p[2],
+                         "hbm_gbs": nbytes / (t_ms * 1e-3) / 1e9, "hbm_frac": nbytes / (t_ms * 1e-3) / 1e9 / hbm,
+                         "glookups": p[2] / (t_ms * 1e-3) / 1e9,
+                         "lookup_frac": p[2] / (t_ms * 1e-3) / 1e9 / peak,
+                         "bound": "hbm" if nbytes / (hbm * 1e9) >= p[2] / (peak * 1e9) else "alu"}
+        dom = max(per, key=lambda k: per[k]["ms"])
+        d = per[dom]
+        kern = "dw_tile_kernel" if step.tiled else "dw_direct_kernel"
+        if d["bound"] == "hbm":
+            roofline = {"bound": "hbm", "achieved": d["hbm_gbs"], "peak": hbm, "peak_source": src, "unit": "GB/s",
+                        "frac": d["hbm_frac"], "lookup_frac": d["lookup_frac"]}
+        else:
+            roofline = {"bound": "alu", "pipe": "shared-memory LUT lookups: SMs x 32 per clock x SM clock",
+                        "achieved": d["glookups"], "peak": peak, "unit": "Glookup/s", "frac": d["lookup_frac"],
+                        "hbm_frac": d["hbm_frac"]}
+        roofline.update({"traffic": recorded_traffic(f"{wname}:{dom}", DW_KERNEL_SOURCES),
+                         "kernel": f"{kern} ({dom} pass)", "passes": per, "sms": sms, "sm_mhz": mhz})
     if args.workload == "mul":
         # HBM-bound: 12 bytes per product (two operands in, one result out)
         hbm, src = measured_peaks()
@@ -542,7 +597,7 @@ def main():
            "serial_value": world * macs / (serial_ms * 1e-3) / 1e9}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("mlp", "gemm4096"):
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("mlp", "gemm4096", "dwconv3x3"):
         import oracle
         oracle.build()
         cores = os.cpu_count() or 1

@@ -74,7 +74,7 @@ const char *amsim_status_string(int status);
 unsigned long long amsim_kernel_launches(void);
 
 /* Kernel paths of the calling host thread's most recent GEMM or convolution
- * call (a diagnostic; 0 before any, or when the call enqueued nothing): */
+ * (ordinary or depthwise) call (a diagnostic; 0 before any, or when the call enqueued nothing): */
 enum amsim_path {
     AMSIM_PATH_PLANES = 1,          /* operands decoded once into planes, copied by TMA */
     AMSIM_PATH_INKERNEL_DECODE = 4, /* operands decoded inside the warp-specialised GEMM */
@@ -84,7 +84,9 @@ enum amsim_path {
     AMSIM_PATH_CONV_BOXES = 64,     /* convolution operands as shifted or blocked tensor boxes */
     AMSIM_PATH_RAW_TILES = 128,     /* operand tiles copied in place by TMA, decoded in shared memory */
     AMSIM_PATH_PHASED = 256,        /* every phase of amsim_gemm_phased in one launch */
-    AMSIM_PATH_CLOSED_FORM = 512    /* products computed in registers (amsim_lut_set_closed_form) */
+    AMSIM_PATH_CLOSED_FORM = 512,   /* products computed in registers (amsim_lut_set_closed_form) */
+    AMSIM_PATH_DW_TILES = 1024,     /* depthwise: halo tiles in shared memory, one channel per warp */
+    AMSIM_PATH_DW_DIRECT = 2048     /* depthwise: one lane per output element, operands read directly */
 };
 int amsim_last_path(void);
 
@@ -355,6 +357,59 @@ int amsim_conv2d_bwd_filter(const amsim_conv_desc *desc, const float *x, const f
  * column).  Less scratch selects the gathering kernel.
  */
 size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim_lut_t lut);
+
+/* ------------------------------------------------------------------ depthwise Conv2D */
+
+/*
+ * Depthwise convolution (Sec. III, Table I: depthwise Conv2D is one of the
+ * layer types ApproxTrain simulates), every product an AMSim product, fp32
+ * accumulation.  The descriptor is the Conv2D one with K = C * D output
+ * channels for a channel multiplier D >= 1 (K not a multiple of C is
+ * AMSIM_EINVAL).  The filter is w[r][s][c][d] (R*S*C*D floats, TF's
+ * depthwise HWC-multiplier layout) and output channel k = c*D + d reads input
+ * channel c only:
+ *   y[n,p,q,c*D+d] = sum_{r,s} AMSim(x[n, p*sh - ph + r*dh, q*sw - pw + s*dw, c], w[r,s,c,d]).
+ * x: N*H*W*C, w: R*S*C*D, y: N*P*Q*K (written).  Padded taps are zero
+ * operands.  3x3 filters with unit stride and dilation, D = 1, C a multiple of
+ * 4, 16-byte aligned x and y and an 8- or 16-bit narrowed LUT of at most
+ * 64 KB take the tiled kernel (AMSIM_PATH_DW_TILES); everything else the
+ * direct kernel (AMSIM_PATH_DW_DIRECT).  Scratch is not used.
+ */
+int amsim_dwconv2d_fwd(const amsim_conv_desc *desc, const float *x, const float *w, float *y,
+                       amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);
+
+/*
+ * Preceding-layer gradient of the depthwise convolution (Algorithm 4's
+ * IM2COL_PLG / TransposeAndReverse reading, per channel):
+ *   dx[n,h,w,c] = sum_{r,s,d} AMSim(dy[n,p,q,c*D+d], w[r,s,c,d]),
+ *   p = (h + ph - r*dh)/sh, q = (w + pw - s*dw)/sw where integral and in range
+ *   (zero operands elsewhere).
+ * dy: N*P*Q*K, w: R*S*C*D, dx: N*H*W*C (written).  Kernel choice as for the
+ * forward pass (dy and dx 16-byte aligned).  Scratch is not used.
+ */
+int amsim_dwconv2d_bwd_data(const amsim_conv_desc *desc, const float *dy, const float *w, float *dx,
+                            amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);
+
+/*
+ * Weight gradient of the depthwise convolution:
+ *   dw[r,s,c,d] = sum_{n,p,q} AMSim(x[n, p*sh - ph + r*dh, q*sw - pw + s*dw, c], dy[n,p,q,c*D+d]).
+ * x: N*H*W*C, dy: N*P*Q*K, dw: R*S*C*D (written; all +0 when N == 0).  The
+ * reduction over N*P*Q is split into shares when scratch allows
+ * (amsim_dwconv2d_workspace_size), whose partial sums a second kernel adds in
+ * share order (AMSIM_PATH_STREAMK is then set); without scratch one share per
+ * channel block runs, more slowly.  Results are deterministic for a given
+ * scratch size.  Kernel choice as for the forward pass (x and dy 16-byte
+ * aligned).
+ */
+int amsim_dwconv2d_bwd_filter(const amsim_conv_desc *desc, const float *x, const float *dy, float *dw,
+                              amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);
+
+/*
+ * which: 0 forward, 1 bwd_data, 2 bwd_filter.  Bytes of scratch with which the
+ * call splits its reduction over every SM (0 for the first two passes, and
+ * for an invalid descriptor).
+ */
+size_t amsim_dwconv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim_lut_t lut);
 
 /* ------------------------------------------------------------------ glue */
 

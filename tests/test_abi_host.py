@@ -86,6 +86,9 @@ def test_calls_reject_null_lut_without_device_work(L):
     assert L.amsim_conv2d_fwd(ctypes.byref(d), None, None, None, None, None, 0, None) == am.AMSIM_EINVAL
     assert L.amsim_gemm_workspace_size(b"N", b"N", 8, 8, 8, 1, None) == 0
     assert L.amsim_conv2d_workspace_size(ctypes.byref(d), 0, None) == 0
+    for fn in ("amsim_dwconv2d_fwd", "amsim_dwconv2d_bwd_data", "amsim_dwconv2d_bwd_filter"):
+        assert getattr(L, fn)(ctypes.byref(d), None, None, None, None, None, 0, None) == am.AMSIM_EINVAL
+    assert L.amsim_dwconv2d_workspace_size(ctypes.byref(d), 2, None) == 0
     L.amsim_lut_destroy(vp(None))     # NULL is ignored
     assert L.amsim_lut_info(None, None, None, None) == am.AMSIM_EINVAL
     assert L.amsim_lut_entries(None, None) == am.AMSIM_EINVAL
