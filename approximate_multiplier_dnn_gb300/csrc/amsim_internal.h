@@ -8,6 +8,8 @@
 
 #include "amsim.h"
 
+struct CUtensorMap_st;   // cuda.h's tensor map (CUtensorMap)
+
 struct amsim_lut_s {
     int M = 0;
     int device = -1;
@@ -67,6 +69,9 @@ struct TmaRawMap {
     uint32_t box[5];
     int swizzle64;
 };
+// Encode a tiled fp32 tensor map (zero fill out of bounds) into `map` (a
+// CUtensorMap); AMSIM_EUNSUPPORTED when the driver refuses it.
+int encode_tensor_map(::CUtensorMap_st *map, const TmaRawMap &m);
 struct ConvRaw {
     // 1: the L tile is whole output rows of one image; a stage is one box of
     //    16 channels of the activation at the filter tap's offset (forward,

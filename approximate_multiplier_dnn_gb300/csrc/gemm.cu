@@ -978,6 +978,8 @@ size_t gemm_workspace(char transA, char transB, int m, int n, int k, int batch, 
 
 void set_last_path(int bits) { g_last_path = bits; }
 
+int encode_tensor_map(CUtensorMap_st *map, const TmaRawMap &m) { return encode_raw_spec(map, m); }
+
 }  // namespace amsim
 
 extern "C" {
