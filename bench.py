@@ -244,7 +244,7 @@ def lut_residency(lut):
 # sources of the LUT-GEMM kernels (the kernel the traffic records measure);
 # a record holds for one version of them
 KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_ws.cuh", "gemm_tma.cuh", "gemm_raw.cuh")
-DW_KERNEL_SOURCES = ("gemm_kernel.cuh", "dwconv.cu")
+DW_KERNEL_SOURCES = ("gemm_kernel.cuh", "dwconv_kernel.cuh", "dwconv.cu")
 
 
 def kernel_sha(sources=KERNEL_SOURCES):
@@ -477,6 +477,8 @@ def main():
                         "hbm_frac": d["hbm_frac"]}
         roofline.update({"traffic": recorded_traffic(f"{wname}:{dom}", DW_KERNEL_SOURCES),
                          "kernel": f"{kern} ({dom} pass)", "passes": per, "sms": sms, "sm_mhz": mhz})
+        if args.closed_form:
+            roofline["products"] = "closed form in registers (no table lookups): lookup_frac is lookups avoided"
     if args.workload == "mul":
         # HBM-bound: 12 bytes per product (two operands in, one result out)
         hbm, src = measured_peaks()

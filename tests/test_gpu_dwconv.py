@@ -240,3 +240,39 @@ def test_dwconv_mobilenet_layer_full_size(amd, orc, luts):
     pts = np.unique(np.concatenate([rng.integers(0, dw.size, 96), [0, dw.size - 1]]))
     ref, sa = orc.dwconv2d_bwd_filter("mitchell", 7, desc, data["x"], data["dy"], pts)
     assert_close(dw[pts], ref, sa, "full-size bwd_filter")
+
+
+@pytest.mark.parametrize("kind", ["mitchell", "exact"])
+def test_dwconv_closed_form_equals_table(amd, orc, kind):
+    """Closed-form products (amsim_lut_set_closed_form) in the tiled kernel
+    give the table path's results bit for bit, on ordinary operands and on
+    tiles with special or tiny (nonzero, below 2^-63) values, which take the
+    slow computation; and they stay within the oracle's tolerance."""
+    lut_t = amd.Lut.build(kind, 7)
+    lut_c = amd.Lut.build(kind, 7).set_closed_form(True)
+    try:
+        for g in (TILED[0], TILED[1], TILED[4]):
+            for specials in (False, True):
+                rng = np.random.default_rng(11 + sum(g[:7]) + specials)
+                x, w, dy = operands(orc, g, rng)
+                if specials:
+                    x, w, dy = sprinkle(x, rng), sprinkle(w, rng, 0.05), sprinkle(dy, rng)
+                    x.reshape(-1)[::97] = np.float32(3e-20)
+                    dy.reshape(-1)[::89] = np.float32(-5e-21)
+                desc, P, Q = dims(orc, g)
+                args = ((x, w), (dy, w), (x, dy))
+                for which in range(3):
+                    shape = out_shape(g, P, Q, which)
+                    a, pa = run_dw(amd, lut_t, which, g, *args[which], shape)
+                    b, pb = run_dw(amd, lut_c, which, g, *args[which], shape)
+                    assert pa & amd.AMSIM_PATH_DW_TILES and not pa & amd.AMSIM_PATH_CLOSED_FORM, pa
+                    assert pb & amd.AMSIM_PATH_DW_TILES and pb & amd.AMSIM_PATH_CLOSED_FORM, pb
+                    ba, bb = bits(a), bits(b)
+                    both_nan = np.isnan(a) & np.isnan(b)
+                    assert np.array_equal(ba[~both_nan], bb[~both_nan]), (kind, g, specials, PASSES[which])
+                    assert np.array_equal(np.isnan(a), np.isnan(b))
+                    ref, sa = oracle_pass(orc, kind, 7, which, desc, *args[which], b.size)
+                    assert_close(b.reshape(-1), ref, sa, f"closed form {kind} {PASSES[which]} {g}")
+    finally:
+        lut_t.close()
+        lut_c.close()
