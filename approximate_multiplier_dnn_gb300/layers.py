@@ -9,12 +9,13 @@ additions are ordinary (exact) torch additions, as they are not products.
 
 Layouts: Dense weights are [in, out] (y = x w); Conv2D tensors are NHWC with
 RSCK filters (TF's HWIO), stride/padding/dilation as in ApproxTrain's Conv2D;
+depthwise filters are R x S x C x D (TF's depthwise layout, multiplier D);
 attention takes Q, K, V as [batch, heads, seq, dim].
 
 Operand order of every contraction (which operand indexes the LUT's rows;
 it matters only for an asymmetric user LUT): Dense forward (x, w), input
 gradient (dy, w), weight gradient (x, dy); Conv2D likewise (x, w), (dy, w),
-(x, dy); attention S = (q, k), O = (p, v), dV = (p, dO), dP = (dO, v),
+(x, dy), and the same for depthwise; attention S = (q, k), O = (p, v), dV = (p, dO), dP = (dO, v),
 dQ = (dS, k), dK = (dS, q).
 """
 from __future__ import annotations
@@ -24,7 +25,8 @@ import math
 import torch
 
 from . import (ConvDesc, amsim_conv2d_bwd_data, amsim_conv2d_bwd_filter, amsim_conv2d_fwd, amsim_conv2d_out_hw,
-               amsim_conv2d_workspace_size, amsim_gemm, amsim_gemm_strided_batched, amsim_gemm_workspace_size,
+               amsim_conv2d_workspace_size, amsim_dwconv2d_bwd_data, amsim_dwconv2d_bwd_filter, amsim_dwconv2d_fwd,
+               amsim_dwconv2d_workspace_size, amsim_gemm, amsim_gemm_strided_batched, amsim_gemm_workspace_size,
                amsim_softmax_rows, amsim_softmax_rows_backward, workspace)
 
 
@@ -159,6 +161,69 @@ class AMConv2d(torch.nn.Module):
 
     def forward(self, x):
         y = _Conv2dFn.apply(x, self.weight, self.lut, self.stride, self.padding, self.dilation)
+        return y + self.bias if self.bias is not None else y
+
+
+# ------------------------------------------------------------------ depthwise Conv2D
+class _DepthwiseConv2dFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, w, lut, stride, padding, dilation):
+        x, w = _f32(x), _f32(w)
+        N, H, W, C = x.shape
+        R, S, C2, D = w.shape
+        if C2 != C:
+            raise ValueError("filter channels differ from the input's")
+        desc = ConvDesc.make(N, H, W, C, C * D, R, S, stride, padding, dilation)
+        P, Q = amsim_conv2d_out_hw(desc)
+        y = torch.empty((N, P, Q, C * D), dtype=torch.float32, device=x.device)
+        amsim_dwconv2d_fwd(desc, x, w, y, lut)
+        ctx.save_for_backward(x, w)
+        ctx.lut, ctx.desc = lut, desc
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, w = ctx.saved_tensors
+        dy = _f32(dy)
+        desc, lut = ctx.desc, ctx.lut
+        dx = dw = None
+        if ctx.needs_input_grad[0]:
+            dx = torch.empty_like(x)
+            amsim_dwconv2d_bwd_data(desc, dy, w, dx, lut)
+        if ctx.needs_input_grad[1]:
+            dw = torch.empty_like(w)
+            amsim_dwconv2d_bwd_filter(desc, x, dy, dw, lut,
+                                      ws=workspace(amsim_dwconv2d_workspace_size(desc, 2, lut), x.device))
+        return dx, dw, None, None, None, None
+
+
+def am_depthwise_conv2d(x, w, lut, stride=1, padding=0, dilation=1):
+    """Depthwise y = conv2d(x, w) per channel with approximate products (x NHWC,
+    w R x S x C x D for a channel multiplier D, y NPQ(C*D), output channel
+    c*D + d from input channel c)."""
+    return _DepthwiseConv2dFn.apply(x, w, lut, _pair(stride), _pair(padding), _pair(dilation))
+
+
+class AMDepthwiseConv2d(torch.nn.Module):
+    """Depthwise 2-D convolution (one filter group per input channel, channel
+    multiplier D) whose forward pass and both gradients use the approximate
+    multiplier; depthwise convolution is one of the layer types ApproxTrain
+    simulates (Sec. III, Table I).  NHWC input, R x S x C x D filters."""
+
+    def __init__(self, channels: int, kernel_size, lut, depth_multiplier: int = 1, stride=1, padding=0,
+                 dilation=1, bias: bool = True, device="cuda", generator: torch.Generator | None = None):
+        super().__init__()
+        self.lut = lut
+        R, S = _pair(kernel_size)
+        self.stride, self.padding, self.dilation = _pair(stride), _pair(padding), _pair(dilation)
+        std = math.sqrt(2.0 / (R * S))                                  # He normal over a channel's taps
+        w = torch.randn((R, S, channels, depth_multiplier), generator=generator) * std
+        self.weight = torch.nn.Parameter(w.to(device))
+        self.bias = (torch.nn.Parameter(torch.zeros(channels * depth_multiplier, device=device)) if bias
+                     else None)
+
+    def forward(self, x):
+        y = _DepthwiseConv2dFn.apply(x, self.weight, self.lut, self.stride, self.padding, self.dilation)
         return y + self.bias if self.bias is not None else y
 
 

@@ -88,6 +88,42 @@ def test_am_conv2d_forward_and_gradients(amd, orc, luts, geom):
     assert_close(host(layer.weight.grad).reshape(-1), ref, sa, "dW")
 
 
+@pytest.mark.parametrize("geom", [
+    dict(N=2, H=9, W=70, C=20, D=1, R=3, S=3, stride=1, pad=1, dil=1),    # tiled kernel
+    dict(N=2, H=10, W=9, C=6, D=2, R=3, S=3, stride=2, pad=1, dil=1),     # direct kernel, multiplier 2
+])
+def test_am_depthwise_conv2d_forward_and_gradients(amd, orc, luts, geom):
+    """AMDepthwiseConv2d: output and both autograd gradients against the
+    oracle's depthwise sums; the bias is added exactly."""
+    import torch
+    from approximate_multiplier_dnn_gb300.layers import AMDepthwiseConv2d, am_depthwise_conv2d
+    g = torch.Generator().manual_seed(6)
+    lut = luts("mitchell", 7)
+    G = geom
+    layer = AMDepthwiseConv2d(G["C"], (G["R"], G["S"]), lut, depth_multiplier=G["D"], stride=G["stride"],
+                              padding=G["pad"], dilation=G["dil"], bias=True, generator=g)
+    with torch.no_grad():
+        layer.bias.copy_(torch.randn(layer.bias.shape, generator=g).cuda())
+    X = torch.randn((G["N"], G["H"], G["W"], G["C"]), generator=g).cuda().requires_grad_()
+    y = layer(X)
+    dy = torch.randn(tuple(y.shape), generator=g).cuda() * 0.01
+    y.backward(dy)
+    torch.cuda.synchronize()
+    st, pd, dl = (G["stride"],) * 2, (G["pad"],) * 2, (G["dil"],) * 2
+    K = G["C"] * G["D"]
+    desc = orc.conv_desc(G["N"], G["H"], G["W"], G["C"], K, G["R"], G["S"], st, pd, dl)
+    x, w, d = host(X), host(layer.weight), host(dy)
+    y0 = am_depthwise_conv2d(X.detach(), layer.weight.detach(), lut, G["stride"], G["pad"], G["dil"])
+    assert torch.equal(y.detach(), y0 + layer.bias.detach())
+    ref, sa = orc.dwconv2d_fwd("mitchell", 7, desc, x, w, np.arange(y.numel()))
+    assert_close(host(y0).reshape(-1), ref, sa, "y")
+    ref, sa = orc.dwconv2d_bwd_data("mitchell", 7, desc, d, w, np.arange(X.numel()))
+    assert_close(host(X.grad).reshape(-1), ref, sa, "dX")
+    ref, sa = orc.dwconv2d_bwd_filter("mitchell", 7, desc, x, d, np.arange(w.size))
+    assert_close(host(layer.weight.grad).reshape(-1), ref, sa, "dW")
+    assert np.allclose(host(layer.bias.grad), d.reshape(-1, K).sum(0), rtol=1e-5, atol=1e-6)
+
+
 def test_softmax_rows_backward_kernel(amd, orc):
     import torch
     rng = np.random.default_rng(8)
