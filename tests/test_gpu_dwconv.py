@@ -20,6 +20,8 @@ TILED = [
     (2, 8, 8, 8, 1, 3, 3, (1, 1), (2, 2), (1, 1)),      # padding 2
     (1, 5, 12, 4, 1, 3, 3, (1, 1), (3, 1), (1, 1)),     # padding beyond the filter reach
     (3, 17, 65, 48, 1, 3, 3, (1, 1), (1, 1), (1, 1)),   # 65 columns: a one-column second tile
+    (3, 1, 1, 8, 1, 3, 3, (1, 1), (1, 1), (1, 1)),      # 1x1 image: only the centre tap meets data
+    (2, 3, 130, 4, 1, 3, 3, (1, 1), (0, 0), (1, 1)),    # one output row, exactly two 64-column tiles
 ]
 DIRECT = [
     (2, 7, 6, 3, 1, 3, 3, (1, 1), (1, 1), (1, 1)),      # 3 channels: not a multiple of 4
