@@ -468,9 +468,9 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
     bool aborted = false;
     for (int t = t_begin; t < t_end; t += t_step) {
         const DwTile tl = tile_at(t);
-        __syncthreads();                    // the previous tile's shared-memory reads are done
         mbar_wait(bar, phase, aborted);
         phase ^= 1;
+        // also orders the previous tile's shared-memory reads before this tile's packing
         if (__syncthreads_or(aborted)) break;
         bool big = false;
         const int a_shift = MODE == 2 ? hi_shift : lo_shift;

@@ -270,6 +270,24 @@ def recorded_traffic(workload, sources=KERNEL_SOURCES):
     return None
 
 
+# ---------------------------------------------------------------- replicas
+def slowest_rank_ms(total_ms, world, device):
+    """The job's timed total: the largest of the ranks' totals (every rank runs
+    one replica of the workload on its own GPU; the slowest sets the time)."""
+    if world <= 1:
+        return total_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(macs_per_step, steps, total_ms, world):
+    """Whole-job approx-GMAC/s: the MACs every rank processed over the job time."""
+    return world * macs_per_step * steps / (total_ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- reference arm
 def reference_arm(args, rank):
     if rank != 0:
@@ -411,13 +429,9 @@ def main():
     P = max(3, min(K, 50))
     pevs = timed_loop(P, per_part=True)
     part_ms = [sum(pevs[s][i].elapsed_time(pevs[s][i + 1]) for s in range(P)) / P for i in range(len(parts))]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(sum(step_ms), world, "cuda")
     macs = step.macs
-    value = world * macs * K / (total_ms * 1e-3) / 1e9
+    value = job_throughput(macs, K, total_ms, world)
     ms_per_step = total_ms / K
 
     # dominant kernel: the LUT-GEMM (every part with MACs), lookups = MACs
