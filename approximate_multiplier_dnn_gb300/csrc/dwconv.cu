@@ -300,14 +300,40 @@ int dw_tile_ctas_per_sm(const amsim_lut_t lut, int which)
     return std::max(1, std::min(2, (228 * 1024) / per));
 }
 
+// Tile shape of the tiled kernel for an OH x OW output grid: LQ lanes across
+// (2 columns each) by 32 / LQ blocks of 8 rows.  The shape that computes the
+// fewest outputs past the grid's edges wins; ties go to the smaller halo,
+// then to the wider tile.
+struct DwShape {
+    int lq_shift, tp, tq, th, tw;
+};
+
+DwShape dw_shape(int OH, int OW)
+{
+    DwShape best{};
+    long long best_cost = -1, best_halo = 0;
+    for (int ls = 5; ls >= 2; --ls) {
+        const int tq = 2 << ls, tp = kDwRB * (32 >> ls);
+        const long long cost = (long long)((OH + tp - 1) / tp) * tp * ((OW + tq - 1) / tq) * tq;
+        const long long halo = (long long)(tp + 2) * (tq + 2);
+        if (best_cost < 0 || cost < best_cost || (cost == best_cost && halo < best_halo)) {
+            best = DwShape{ls, tp, tq, tp + 2, tq + 2};
+            best_cost = cost;
+            best_halo = halo;
+        }
+    }
+    return best;
+}
+
 DwFilterPlan filter_plan(const DwGeo &g, bool tiled, int sms, const amsim_lut_t lut)
 {
     DwFilterPlan f{};
     f.tiled = tiled;
     f.outs = (long long)g.R * g.S * g.K;
     if (tiled) {
-        f.tiles_p = (g.P + kDwTP - 1) / kDwTP;
-        f.tiles_q = (g.Q + kDwTQ - 1) / kDwTQ;
+        const DwShape sh = dw_shape(g.P, g.Q);
+        f.tiles_p = (g.P + sh.tp - 1) / sh.tp;
+        f.tiles_q = (g.Q + sh.tq - 1) / sh.tq;
         f.cblocks = (g.C + dw_channel_block(2) - 1) / dw_channel_block(2);
         f.tiles = g.N * f.tiles_p * f.tiles_q;
         const int slots = dw_tile_ctas_per_sm(lut, 2) * sms;
@@ -369,27 +395,36 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         tp.C = g.C;
         tp.a = t0;
         tp.expand_mul = 1u << (24 - width);
+        // output grid: y (forward), dx (data gradient), dy (weight gradient)
+        const DwShape sh = which == 1 ? dw_shape(g.H, g.W) : dw_shape(g.P, g.Q);
+        tp.lq_shift = sh.lq_shift;
+        tp.tp = sh.tp;
+        tp.tq = sh.tq;
+        tp.tq_shift = sh.lq_shift + 1;
+        tp.th = sh.th;
+        tp.tw = sh.tw;
+        tp.raw_a_bytes = sh.th * sh.tw * dw_channel_block(which) * 4;
         bool mapped;
         if (which == 0) {
             tp.IH = g.H; tp.IW = g.W;
             tp.b = t1; tp.out = out;
             tp.OH = g.P; tp.OW = g.Q;
             tp.oy = -g.ph; tp.ox = -g.pw;
-            mapped = dw_map(&tp.amap, t0, g.N, g.H, g.W, g.C, dw_channel_block(0), kDwTW, kDwTH);
+            mapped = dw_map(&tp.amap, t0, g.N, g.H, g.W, g.C, dw_channel_block(0), sh.tw, sh.th);
         } else if (which == 1) {
             // dx[h][w] = sum_{r',s'} dy[h + ph - 2 + r'][w + pw - 2 + s'] * w[2 - r'][2 - s']
             tp.IH = g.P; tp.IW = g.Q;
             tp.b = t1; tp.out = out;
             tp.OH = g.H; tp.OW = g.W;
             tp.oy = g.ph - 2; tp.ox = g.pw - 2;
-            mapped = dw_map(&tp.amap, t0, g.N, g.P, g.Q, g.C, dw_channel_block(1), kDwTW, kDwTH);
+            mapped = dw_map(&tp.amap, t0, g.N, g.P, g.Q, g.C, dw_channel_block(1), sh.tw, sh.th);
         } else {
             tp.IH = g.H; tp.IW = g.W;
             tp.b = t1;
             tp.OH = g.P; tp.OW = g.Q;
             tp.oy = -g.ph; tp.ox = -g.pw;
-            mapped = dw_map(&tp.amap, t0, g.N, g.H, g.W, g.C, dw_channel_block(2), kDwTW, kDwTH) &&
-                     dw_map(&tp.bmap, t1, g.N, g.P, g.Q, g.C, dw_channel_block(2), kDwTQ, kDwTP);
+            mapped = dw_map(&tp.amap, t0, g.N, g.H, g.W, g.C, dw_channel_block(2), sh.tw, sh.th) &&
+                     dw_map(&tp.bmap, t1, g.N, g.P, g.Q, g.C, dw_channel_block(2), sh.tq, sh.tp);
         }
         if (!mapped) {               // the driver refused a tensor map: the direct kernel
             tiled = false;
@@ -397,8 +432,8 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         }
     }
     if (tiled) {
-        tp.tiles_p = (tp.OH + kDwTP - 1) / kDwTP;
-        tp.tiles_q = (tp.OW + kDwTQ - 1) / kDwTQ;
+        tp.tiles_p = (tp.OH + tp.tp - 1) / tp.tp;
+        tp.tiles_q = (tp.OW + tp.tq - 1) / tp.tq;
         tp.cblocks = (g.C + dw_channel_block(which) - 1) / dw_channel_block(which);
         tp.tiles = g.N * tp.tiles_p * tp.tiles_q;
         const size_t smem = (size_t)dw_tile_smem(dw_staged_lut(lut), which);

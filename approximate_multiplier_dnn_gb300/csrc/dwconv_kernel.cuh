@@ -66,14 +66,18 @@ __device__ __forceinline__ float fmul_ftz(float a, float b)
 
 // ------------------------------------------------------------------ tiled kernel
 constexpr int kDwThreads = 256;       // 8 warps
-constexpr int kDwTP = 8;              // output rows per tile
-constexpr int kDwTQ = 64;             // output columns per tile (2 per lane)
-constexpr int kDwTH = kDwTP + 2;      // halo rows (3x3 filter)
-constexpr int kDwTW = kDwTQ + 2;      // halo columns
+// Tile shapes: a lane owns 2 adjacent output columns of an 8-row block; a
+// warp's 32 lanes are LQ = 32, 16, 8 or 4 lanes across by 32 / LQ row blocks,
+// so a tile is (256 / LQ) rows x 2 LQ columns = 512 outputs per channel and
+// its halo (rows + 2) x (columns + 2) is at most 660 positions.  The host
+// picks LQ per launch to waste the fewest computed outputs past the edges.
+constexpr int kDwRB = 8;              // output rows per lane
+constexpr int kDwTileOut = 512;       // outputs per tile and channel
+constexpr int kDwHaloMax = 660;       // halo positions of the widest and tallest shapes
 constexpr int kDwCP = 666;            // packed halo words per channel: >= 660, = 2 mod 8 (conflict-free packing)
 constexpr int kDwOP = 514;            // packed output-gradient / output-tile words per channel: >= 512, = 2 mod 8
-static_assert(kDwTH * kDwTW <= kDwCP && kDwTP * kDwTQ <= kDwOP, "tile pitches");
-static_assert(kDwCP % 2 == 0 && kDwOP % 2 == 0 && kDwTW % 2 == 0, "8-byte aligned lane pairs");
+static_assert(kDwHaloMax <= kDwCP && kDwTileOut <= kDwOP, "tile pitches");
+static_assert(kDwCP % 2 == 0 && kDwOP % 2 == 0, "8-byte aligned lane pairs");
 
 __host__ __device__ constexpr int dw_lut_region(int table_bytes) { return (table_bytes + 127) & ~127; }
 
@@ -84,8 +88,8 @@ template <int MODE>
 struct DwCfg {
     static constexpr int CB = MODE == 2 ? 8 : 16;
     static constexpr int CPW = CB / 8;                        // channels per warp
-    static constexpr int RawA = kDwTH * kDwTW * CB * 4;       // raw halo box as the tensor copy lands: [row][col][c]
-    static constexpr int RawB = kDwTP * kDwTQ * CB * 4;       // raw output-gradient box (weight gradient)
+    static constexpr int RawA = kDwHaloMax * CB * 4;          // raw halo box as the tensor copy lands: [row][col][c]
+    static constexpr int RawB = kDwTileOut * CB * 4;          // raw output-gradient box (weight gradient)
     static constexpr int Halo = (CB * kDwCP * 4 + 127) & ~127;   // packed halo [c][pos]
     static constexpr int Out = (CB * kDwOP * 4 + 127) & ~127;    // packed dy (weight gradient) / output tile
     static constexpr int WB = (3 * CB * 9 * 4 + 127) & ~127;     // filter taps: offsets, scales, closed forms
@@ -108,8 +112,8 @@ __host__ __device__ constexpr int dw_tile_smem(int table_bytes, int mode)
 __host__ __device__ constexpr int dw_channel_block(int mode) { return mode == 2 ? DwCfg<2>::CB : DwCfg<0>::CB; }
 
 struct DwTileParams {
-    CUtensorMap amap;      // activation: dims (C, IW, IH, N), box (16, kDwTW, kDwTH, 1)
-    CUtensorMap bmap;      // weight gradient's dy: dims (C, OW, OH, N), box (16, kDwTQ, kDwTP, 1)
+    CUtensorMap amap;      // activation: dims (C, IW, IH, N), box (CB, tw, th, 1)
+    CUtensorMap bmap;      // weight gradient's dy: dims (C, OW, OH, N), box (CB, tq, tp, 1)
     const float *a;        // activation (for re-packing a tile with special values)
     const float *b;        // w [3][3][C] (modes 0, 1), dy (mode 2)
     float *out;            // y / dx (NHWC), or the weight gradient's shares [G][9][C]
@@ -121,6 +125,10 @@ struct DwTileParams {
     int OH, OW;            // output (modes 0, 1) or dy (mode 2) height and width
     int oy, ox;            // activation row/column of output (0, 0) at tap (0, 0)
     int tiles_p, tiles_q, cblocks;
+    int lq_shift;          // log2 of the lanes across a row block (5, 4, 3, 2)
+    int tp, tq, tq_shift;  // tile rows, tile columns (2 LQ) and log2(tq)
+    int th, tw;            // halo rows and columns (tp + 2, tq + 2)
+    int raw_a_bytes;       // bytes of one raw halo box (th * tw * CB * 4)
     int tiles;             // N * tiles_p * tiles_q spatial tiles
     int G;                 // mode 2: shares of the spatial tiles
 };
@@ -182,7 +190,7 @@ __device__ __forceinline__ void dw_issue(const DwTileParams &p, const DwTile &t,
 {
     using amsim::kern::mbar_expect_tx;
     using amsim::kern::tma_load_4d;
-    mbar_expect_tx(bar, MODE == 2 ? DwCfg<2>::RawA + DwCfg<2>::RawB : DwCfg<MODE>::RawA);
+    mbar_expect_tx(bar, MODE == 2 ? p.raw_a_bytes + DwCfg<2>::RawB : p.raw_a_bytes);
     tma_load_4d(rawA, &p.amap, t.c0, t.q0 + p.ox, t.p0 + p.oy, t.n, bar);
     if constexpr (MODE == 2) tma_load_4d(rawB, &p.bmap, t.c0, t.q0, t.p0, t.n, bar);
 }
@@ -190,15 +198,15 @@ __device__ __forceinline__ void dw_issue(const DwTileParams &p, const DwTile &t,
 // Forward / data-gradient compute of one channel for one lane: acc[i] holds
 // output row i at tile columns 2*lane (.x) and 2*lane + 1 (.y).
 template <int W, bool SLOW, bool GL = false>
-__device__ __forceinline__ void dw_taps_channel(float2 (&acc)[kDwTP], const uint32_t *xr, const uint8_t *lut,
+__device__ __forceinline__ void dw_taps_channel(float2 (&acc)[kDwRB], const uint32_t *xr, int tw, const uint8_t *lut,
                                                 const uint32_t (&woff)[9], const float (&wsc)[9], uint32_t mul)
 {
 #pragma unroll
-    for (int i = 0; i < kDwTP; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    for (int i = 0; i < kDwRB; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int hh = 0; hh < kDwTH; ++hh) {
-        const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + hh * kDwTW);
-        const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + hh * kDwTW + 2);
+    for (int hh = 0; hh < kDwRB + 2; ++hh) {
+        const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + hh * tw);
+        const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + hh * tw + 2);
         const uint32_t px[4] = {a01.x, a01.y, a23.x, a23.y};
         uint32_t sb[4];
         float sx[4];
@@ -210,7 +218,7 @@ __device__ __forceinline__ void dw_taps_channel(float2 (&acc)[kDwTP], const uint
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
             const int i = hh - r;
-            if (i < 0 || i >= kDwTP) continue;
+            if (i < 0 || i >= kDwRB) continue;
 #pragma unroll
             for (int s = 0; s < 3; ++s) {
                 const int t = r * 3 + s;
@@ -237,20 +245,21 @@ __device__ __forceinline__ void dw_taps_channel(float2 (&acc)[kDwTP], const uint
 // gradient (past P or Q) are skipped, so an infinite activation there cannot
 // meet a zero-filled gradient.
 template <int W, bool SLOW, bool GL = false>
-__device__ __forceinline__ void dw_filter_channel(float2 (&acc)[9], const uint32_t *xr, const uint32_t *dr,
-                                                  const uint8_t *lut, int rows_ok, bool ok0, bool ok1, uint32_t mul)
+__device__ __forceinline__ void dw_filter_channel(float2 (&acc)[9], const uint32_t *xr, int tw, const uint32_t *dr,
+                                                  int tq, const uint8_t *lut, int rows_ok, bool ok0, bool ok1,
+                                                  uint32_t mul)
 {
 #pragma unroll
-    for (int i = 0; i < kDwTP; ++i) {
-        const uint2 d01 = *reinterpret_cast<const uint2 *>(dr + i * kDwTQ);
+    for (int i = 0; i < kDwRB; ++i) {
+        const uint2 d01 = *reinterpret_cast<const uint2 *>(dr + i * tq);
         const uint32_t db0 = dw_scale_bits(d01.x), db1 = dw_scale_bits(d01.y);
         const uint32_t od0 = d01.x - db0, od1 = d01.y - db1;
         const float2 sd = make_float2(__uint_as_float(db0), __uint_as_float(db1));
         const bool row_ok = i < rows_ok;
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
-            const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + (i + r) * kDwTW);
-            const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + (i + r) * kDwTW + 2);
+            const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + (i + r) * tw);
+            const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + (i + r) * tw + 2);
             const uint32_t px[4] = {a01.x, a01.y, a23.x, a23.y};
             uint32_t sb[4];
             float sx[4];
@@ -321,14 +330,14 @@ __device__ __forceinline__ void dw_pack_box_alu(const float *raw, uint32_t *dst,
 //  Both products are exact and equal the table path's v * s, and the
 //  accumulation order is the table path's: results are bit-identical.
 template <int ALU>
-__device__ __forceinline__ void dw_taps_alu(float2 (&acc)[kDwTP], const uint32_t *xr, const uint32_t (&wv)[9])
+__device__ __forceinline__ void dw_taps_alu(float2 (&acc)[kDwRB], const uint32_t *xr, int tw, const uint32_t (&wv)[9])
 {
 #pragma unroll
-    for (int i = 0; i < kDwTP; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    for (int i = 0; i < kDwRB; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int hh = 0; hh < kDwTH; ++hh) {
-        const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + hh * kDwTW);
-        const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + hh * kDwTW + 2);
+    for (int hh = 0; hh < kDwRB + 2; ++hh) {
+        const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + hh * tw);
+        const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + hh * tw + 2);
         const uint32_t px[4] = {a01.x, a01.y, a23.x, a23.y};
         uint32_t sb[4];
 #pragma unroll
@@ -336,7 +345,7 @@ __device__ __forceinline__ void dw_taps_alu(float2 (&acc)[kDwTP], const uint32_t
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
             const int i = hh - r;
-            if (i < 0 || i >= kDwTP) continue;
+            if (i < 0 || i >= kDwRB) continue;
 #pragma unroll
             for (int s = 0; s < 3; ++s) {
                 const int t = r * 3 + s;
@@ -358,19 +367,19 @@ __device__ __forceinline__ void dw_taps_alu(float2 (&acc)[kDwTP], const uint32_t
 // Weight-gradient products in closed form for one channel and lane (x the
 // value operand, dy the fraction-and-scale operand for Mitchell).
 template <int ALU>
-__device__ __forceinline__ void dw_filter_alu(float2 (&acc)[9], const uint32_t *xr, const uint32_t *dr)
+__device__ __forceinline__ void dw_filter_alu(float2 (&acc)[9], const uint32_t *xr, int tw, const uint32_t *dr, int tq)
 {
 #pragma unroll
-    for (int i = 0; i < kDwTP; ++i) {
-        const uint2 d01 = *reinterpret_cast<const uint2 *>(dr + i * kDwTQ);
+    for (int i = 0; i < kDwRB; ++i) {
+        const uint2 d01 = *reinterpret_cast<const uint2 *>(dr + i * tq);
         const uint32_t db0 = d01.x & 0xFF800000u, db1 = d01.y & 0xFF800000u;
         const uint32_t od0 = d01.x - db0, od1 = d01.y - db1;
         const float2 sd = make_float2(__uint_as_float(db0), __uint_as_float(db1));
         const float2 dv = make_float2(__uint_as_float(d01.x), __uint_as_float(d01.y));
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
-            const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + (i + r) * kDwTW);
-            const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + (i + r) * kDwTW + 2);
+            const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + (i + r) * tw);
+            const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + (i + r) * tw + 2);
             const uint32_t px[4] = {a01.x, a01.y, a23.x, a23.y};
 #pragma unroll
             for (int s = 0; s < 3; ++s) {
@@ -394,7 +403,7 @@ __device__ __forceinline__ void dw_filter_alu(float2 (&acc)[9], const uint32_t *
 // Thread 0 copies the next tile's raw boxes while the CTA computes the
 // current one; every wait on the copy is bounded (a timeout is recorded and
 // the CTA leaves its remaining tiles).
-template <int W, int MODE, int ALU>
+template <int W, int MODE, int ALU, bool WIDE>
 __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_constant__ DwTileParams p)
 {
     using amsim::kern::mbar_init;
@@ -403,6 +412,9 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
     using Cfg = DwCfg<MODE>;
     constexpr int CB = Cfg::CB, CPW = Cfg::CPW;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // tile shape: compile-time for the widest (8 x 64) tiles, else from the launch
+    const int lq_shift = WIDE ? 5 : p.lq_shift, tq_shift = WIDE ? 6 : p.tq_shift;
+    const int tq = WIDE ? 64 : p.tq, tw = WIDE ? 66 : p.tw, th = WIDE ? 10 : p.th, tpr = WIDE ? 8 : p.tp;
     uint8_t *lut = smem;
     const uint8_t *glut = static_cast<const uint8_t *>(p.table);         // slow closed-form tiles
     float *rawA = reinterpret_cast<float *>(smem + (ALU ? 0 : dw_lut_region(p.table_bytes)));
@@ -435,11 +447,11 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
             cb = t % p.cblocks;
             rest = t / p.cblocks;
         }
-        const int tq = rest % p.tiles_q;
+        const int tqi = rest % p.tiles_q;
         rest /= p.tiles_q;
-        d.p0 = (rest % p.tiles_p) * kDwTP;
+        d.p0 = (rest % p.tiles_p) * tpr;
         d.n = rest / p.tiles_p;
-        d.q0 = tq * kDwTQ;
+        d.q0 = tqi * tq;
         d.c0 = cb * CB;
         return d;
     };
@@ -476,13 +488,13 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
         const int a_shift = MODE == 2 ? hi_shift : lo_shift;
         const uint32_t keep = ((1u << p.M) - 1u) << (23 - p.M);
         if constexpr (ALU != 0) {
-            dw_pack_box_alu<CB>(rawA, xt, kDwTH * kDwTW, kDwCP, keep, tid, big);
-            if constexpr (MODE == 2) dw_pack_box_alu<CB>(rawB, dyt, kDwTP * kDwTQ, kDwOP, keep, tid, big);
+            dw_pack_box_alu<CB>(rawA, xt, th * tw, kDwCP, keep, tid, big);
+            if constexpr (MODE == 2) dw_pack_box_alu<CB>(rawB, dyt, kDwTileOut, kDwOP, keep, tid, big);
         } else {
-            dw_pack_box<CB>(rawA, xt, kDwTH * kDwTW, kDwCP, 23 - p.M - a_shift, ((1u << p.M) - 1u) << a_shift, tid,
+            dw_pack_box<CB>(rawA, xt, th * tw, kDwCP, 23 - p.M - a_shift, ((1u << p.M) - 1u) << a_shift, tid,
                             big);
             if constexpr (MODE == 2)
-                dw_pack_box<CB>(rawB, dyt, kDwTP * kDwTQ, kDwOP, 23 - p.M - lo_shift, ((1u << p.M) - 1u) << lo_shift,
+                dw_pack_box<CB>(rawB, dyt, kDwTileOut, kDwOP, 23 - p.M - lo_shift, ((1u << p.M) - 1u) << lo_shift,
                                 tid, big);
         }
         if (MODE != 2 && tid < CB * 9) {
@@ -505,35 +517,38 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
             // a tile with |x| >= 2^64, infinities or NaN (closed forms: also
             // nonzero |x| < 2^-63): pack it again exactly for the table (NaN
             // kept as NaN) from global memory, then take the slow products
-            dw_repack<CB>(p.a, xt, kDwCP, tl.n, p.IH, p.IW, p.C, tl.p0 + p.oy, tl.q0 + p.ox, tl.c0, kDwTH, kDwTW, p.M,
+            dw_repack<CB>(p.a, xt, kDwCP, tl.n, p.IH, p.IW, p.C, tl.p0 + p.oy, tl.q0 + p.ox, tl.c0, th, tw, p.M,
                       a_shift, tid);
             if constexpr (MODE == 2)
-                dw_repack<CB>(p.b, dyt, kDwOP, tl.n, p.OH, p.OW, p.C, tl.p0, tl.q0, tl.c0, kDwTP, kDwTQ, p.M, lo_shift,
+                dw_repack<CB>(p.b, dyt, kDwOP, tl.n, p.OH, p.OW, p.C, tl.p0, tl.q0, tl.c0, tpr, tq, p.M, lo_shift,
                           tid);
             __syncthreads();
         }
 
+        // lane -> (row block rb of 8 output rows, column pair lc) of the tile
+        const int rb = lane >> lq_shift, lc = lane & ((1 << lq_shift) - 1);
         if constexpr (MODE == 2) {
-            const int rows_ok = p.OH - tl.p0;
-            const bool ok0 = tl.q0 + 2 * lane < p.OW, ok1 = tl.q0 + 2 * lane + 1 < p.OW;
+            const int rows_ok = p.OH - (tl.p0 + rb * kDwRB);
+            const bool ok0 = tl.q0 + 2 * lc < p.OW, ok1 = tl.q0 + 2 * lc + 1 < p.OW;
 #pragma unroll
             for (int ci = 0; ci < CPW; ++ci) {
                 const int c = warp + 8 * ci;
-                const uint32_t *xr = xt + c * kDwCP + 2 * lane;
-                const uint32_t *dr = dyt + c * kDwOP + 2 * lane;
+                const uint32_t *xr = xt + c * kDwCP + rb * kDwRB * tw + 2 * lc;
+                const uint32_t *dr = dyt + c * kDwOP + rb * kDwRB * tq + 2 * lc;
                 if (slow) {
                     if constexpr (ALU != 0)
-                        dw_filter_channel<W, true, true>(facc[ci], xr, dr, glut, rows_ok, ok0, ok1, p.expand_mul);
+                        dw_filter_channel<W, true, true>(facc[ci], xr, tw, dr, tq, glut, rows_ok, ok0, ok1,
+                                                         p.expand_mul);
                     else
-                        dw_filter_channel<W, true>(facc[ci], xr, dr, lut, rows_ok, ok0, ok1, p.expand_mul);
+                        dw_filter_channel<W, true>(facc[ci], xr, tw, dr, tq, lut, rows_ok, ok0, ok1, p.expand_mul);
                 } else if constexpr (ALU != 0) {
-                    dw_filter_alu<ALU>(facc[ci], xr, dr);
+                    dw_filter_alu<ALU>(facc[ci], xr, tw, dr, tq);
                 } else {
-                    dw_filter_channel<W, false>(facc[ci], xr, dr, lut, rows_ok, ok0, ok1, p.expand_mul);
+                    dw_filter_channel<W, false>(facc[ci], xr, tw, dr, tq, lut, rows_ok, ok0, ok1, p.expand_mul);
                 }
             }
         } else {
-            float2 acc[CPW][kDwTP];
+            float2 acc[CPW][kDwRB];
 #pragma unroll
             for (int ci = 0; ci < CPW; ++ci) {
                 const int c = warp + 8 * ci;
@@ -544,35 +559,35 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
                     woff[k] = wt_off[c * 9 + k];
                     wsc[k] = wt_scl[c * 9 + k];
                 }
-                const uint32_t *xr = xt + c * kDwCP + 2 * lane;
+                const uint32_t *xr = xt + c * kDwCP + rb * kDwRB * tw + 2 * lc;
                 if (slow) {
                     if constexpr (ALU != 0)
-                        dw_taps_channel<W, true, true>(acc[ci], xr, glut, woff, wsc, p.expand_mul);
+                        dw_taps_channel<W, true, true>(acc[ci], xr, tw, glut, woff, wsc, p.expand_mul);
                     else
-                        dw_taps_channel<W, true>(acc[ci], xr, lut, woff, wsc, p.expand_mul);
+                        dw_taps_channel<W, true>(acc[ci], xr, tw, lut, woff, wsc, p.expand_mul);
                 } else if constexpr (ALU != 0) {
                     uint32_t wv[9];
 #pragma unroll
                     for (int k = 0; k < 9; ++k) wv[k] = wt_val[c * 9 + k];
-                    dw_taps_alu<ALU>(acc[ci], xr, wv);
+                    dw_taps_alu<ALU>(acc[ci], xr, tw, wv);
                 } else {
-                    dw_taps_channel<W, false>(acc[ci], xr, lut, woff, wsc, p.expand_mul);
+                    dw_taps_channel<W, false>(acc[ci], xr, tw, lut, woff, wsc, p.expand_mul);
                 }
             }
             __syncthreads();                // every warp is done with the packed halo
             float *ot = reinterpret_cast<float *>(xt);
 #pragma unroll
             for (int ci = 0; ci < CPW; ++ci) {
-                float *o = ot + (warp + 8 * ci) * kDwOP + 2 * lane;
+                float *o = ot + (warp + 8 * ci) * kDwOP + rb * kDwRB * tq + 2 * lc;
 #pragma unroll
-                for (int i = 0; i < kDwTP; ++i) *reinterpret_cast<float2 *>(o + i * kDwTQ) = acc[ci][i];
+                for (int i = 0; i < kDwRB; ++i) *reinterpret_cast<float2 *>(o + i * tq) = acc[ci][i];
             }
             __syncthreads();
             float *dst = p.out + (long long)tl.n * p.OH * p.OW * p.C;
 #pragma unroll 4
-            for (int e = tid; e < kDwTP * kDwTQ * 4; e += kDwThreads) {
+            for (int e = tid; e < kDwTileOut * 4; e += kDwThreads) {
                 const int c4 = e & 3, pos = e >> 2;
-                const int i = pos / kDwTQ, j = pos % kDwTQ;
+                const int i = pos >> tq_shift, j = pos & (tq - 1);
                 const int pp = tl.p0 + i, qq = tl.q0 + j, c = tl.c0 + 4 * c4;
                 if (pp < p.OH && qq < p.OW && c < p.C) {
                     const float *src = ot + 4 * c4 * kDwOP + pos;
@@ -603,7 +618,9 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
 template <int MODE, int ALU>
 int launch_tile(int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
 {
-    auto kfn = width == 8 ? dw_tile_kernel<8, MODE, ALU> : dw_tile_kernel<16, MODE, ALU>;
+    const bool wide = tp.lq_shift == 5;
+    auto kfn = width == 8 ? (wide ? dw_tile_kernel<8, MODE, ALU, true> : dw_tile_kernel<8, MODE, ALU, false>)
+                          : (wide ? dw_tile_kernel<16, MODE, ALU, true> : dw_tile_kernel<16, MODE, ALU, false>);
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return amsim::cuda_status(e);
     kfn<<<grid, kDwThreads, smem, st>>>(tp);

@@ -22,6 +22,10 @@ TILED = [
     (3, 17, 65, 48, 1, 3, 3, (1, 1), (1, 1), (1, 1)),   # 65 columns: a one-column second tile
     (3, 1, 1, 8, 1, 3, 3, (1, 1), (1, 1), (1, 1)),      # 1x1 image: only the centre tap meets data
     (2, 3, 130, 4, 1, 3, 3, (1, 1), (0, 0), (1, 1)),    # one output row, exactly two 64-column tiles
+    (2, 14, 14, 32, 1, 3, 3, (1, 1), (1, 1), (1, 1)),   # 16 x 32 tiles (two 8-row blocks per warp)
+    (1, 32, 16, 8, 1, 3, 3, (1, 1), (1, 1), (1, 1)),    # 32 x 16 tiles
+    (1, 64, 8, 4, 1, 3, 3, (1, 1), (1, 1), (1, 1)),     # 64 x 8 tiles
+    (2, 7, 7, 16, 1, 3, 3, (1, 1), (1, 1), (1, 1)),     # 7 x 7: the last MobileNet resolution
 ]
 DIRECT = [
     (2, 7, 6, 3, 1, 3, 3, (1, 1), (1, 1), (1, 1)),      # 3 channels: not a multiple of 4
