@@ -78,8 +78,9 @@ struct DwDirectParams {
     float *out;
     const void *table;     // narrowed LUT, [first operand][second operand] of the pass
     int M, wlog;
-    long long items;       // mode 0/1: output channels x 32-position chunks; mode 2: R*S*K outputs x G shares
-    long long chunks;      // mode 0/1: 32-position chunks per channel
+    long long items;       // mode 0/1: pixels x channel groups; mode 2: taps x shares x channel groups
+    int groups;            // 32-channel groups of the lanes' channel dimension
+    int table_bytes;       // staged table bytes (0: read through the cache)
     int G;                 // mode 2: shares of the N*P*Q reduction
 };
 
@@ -91,92 +92,143 @@ __device__ __forceinline__ float dw_scale(uint32_t x)
     return __uint_as_float(nan ? 0x7FC00000u : (x & 0xFF800000u));
 }
 
-// AMSim product of two fp32 values (first operand = high index bits) from a
-// narrowed table, rounded to fp32 before it is added (infinity on overflow).
-template <int W>
-__device__ __forceinline__ float dw_product(float first, float second, const void *table, int M, int wlog)
+// Whether v = u * s for an integer u in [0, lim) (u returned); s >= 1.
+__device__ __forceinline__ bool dw_on_grid(int v, int s, int lim, int &u)
+{
+    if (v < 0) return false;
+    if (s == 1) u = v;
+    else if (s == 2) { if (v & 1) return false; u = v >> 1; }
+    else { u = v / s; if (u * s != v) return false; }
+    return u < lim;
+}
+
+// AMSim product from the staged (GL false) or global (GL true) narrowed table
+// [first][second], rounded to fp32 before it is added.
+template <int W, bool GL>
+__device__ __forceinline__ float dw_product_t(float first, float second, const uint8_t *lut, int M, int wlog)
 {
     const uint32_t xa = __float_as_uint(first), xb = __float_as_uint(second);
     const uint32_t idx = ((((xa & 0x7FFFFFu) >> (23 - M)) << M) | ((xb & 0x7FFFFFu) >> (23 - M))) << wlog;
-    const float v = expand<W>(lut_ld<W, true>(static_cast<const uint8_t *>(table), idx));
+    const float v = expand<W>(lut_ld<W, GL>(lut, idx));
     return __fmul_rn(v, fmul_ftz(dw_scale(xa), dw_scale(xb)));
 }
 
-template <int W, int MODE>
+// Direct kernel: a warp takes one pixel (or, for the weight gradient, one
+// filter tap and one share of the pixels) and 32 consecutive channels, so both
+// operands are read as coalesced rows; the table sits in shared memory unless
+// it is wider than 16 bits or larger than 64 KB (then the read-only cache).
+template <int W, int MODE, bool GL>
 __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ DwDirectParams p)
 {
+    extern __shared__ __align__(16) uint8_t dsmem[];
     const DwGeo &g = p.g;
     const int lane = threadIdx.x & 31;
-    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-    for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < p.items; it += warps) {
-        if constexpr (MODE == 0) {
-            // warp: output channel k (uniform filter tap), lanes: 32 consecutive output pixels
-            const int k = (int)(it / p.chunks);
-            const long long pix = (it % p.chunks) * 32 + lane;
-            if (pix >= (long long)g.N * g.P * g.Q) continue;
-            const int q = (int)(pix % g.Q);
-            const int pp = (int)((pix / g.Q) % g.P);
-            const int n = (int)(pix / ((long long)g.P * g.Q));
-            const int c = k / g.D, d = k % g.D;
-            float acc = 0.0f;
-            for (int r = 0; r < g.R; ++r)
-                for (int s = 0; s < g.S; ++s) {
-                    const int h = pp * g.sh - g.ph + r * g.dh, w = q * g.sw - g.pw + s * g.dw;
-                    float xv = 0.0f;
-                    if ((unsigned)h < (unsigned)g.H && (unsigned)w < (unsigned)g.W)
-                        xv = __ldg(p.a + (((long long)n * g.H + h) * g.W + w) * g.C + c);
-                    const float wv = __ldg(p.b + ((long long)(r * g.S + s) * g.C + c) * g.D + d);
-                    acc = __fadd_rn(acc, dw_product<W>(xv, wv, p.table, p.M, p.wlog));
-                }
-            p.out[pix * g.K + k] = acc;
-        } else if constexpr (MODE == 1) {
-            // warp: input channel c, lanes: 32 consecutive input pixels
-            const int c = (int)(it / p.chunks);
-            const long long pix = (it % p.chunks) * 32 + lane;
-            if (pix >= (long long)g.N * g.H * g.W) continue;
-            const int w = (int)(pix % g.W);
-            const int h = (int)((pix / g.W) % g.H);
-            const int n = (int)(pix / ((long long)g.H * g.W));
-            float acc = 0.0f;
-            for (int r = 0; r < g.R; ++r)
-                for (int s = 0; s < g.S; ++s) {
-                    const int hp = h + g.ph - r * g.dh, wq = w + g.pw - s * g.dw;
-                    const bool in = hp >= 0 && wq >= 0 && hp % g.sh == 0 && wq % g.sw == 0 && hp / g.sh < g.P &&
-                                    wq / g.sw < g.Q;
-                    const long long base = in ? (((long long)n * g.P + hp / g.sh) * g.Q + wq / g.sw) * g.K : 0;
-                    for (int d = 0; d < g.D; ++d) {
-                        const float dyv = in ? __ldg(p.a + base + (long long)c * g.D + d) : 0.0f;
+    const uint8_t *lut = static_cast<const uint8_t *>(p.table);
+    if constexpr (!GL) {
+        const uint4 *src = static_cast<const uint4 *>(p.table);
+        uint4 *dst = reinterpret_cast<uint4 *>(dsmem);
+        for (int i = threadIdx.x; i < (p.table_bytes + 15) >> 4; i += blockDim.x) dst[i] = __ldg(src + i);
+        __syncthreads();
+        lut = dsmem;
+    }
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    const int warp0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if constexpr (MODE == 0) {
+        // a warp takes output pixels warp0, warp0 + warps, ... (32-bit: N*P*Q < 2^30),
+        // each for every 32-channel group; consecutive warps take neighbouring pixels
+        const int npix = g.N * g.P * g.Q;
+        for (int pix = warp0; pix < npix; pix += warps) {
+            const int q = pix % g.Q, t = pix / g.Q;
+            const int pp = t % g.P, n = t / g.P;
+            for (int kg = 0; kg < p.groups; ++kg) {
+                const int k = kg * 32 + lane;
+                if (k >= g.K) continue;
+                const int c = k / g.D, d = k - c * g.D;
+                const float *xn = p.a + (long long)n * g.H * g.W * g.C + c;
+                float acc = 0.0f;
+                for (int r = 0; r < g.R; ++r) {
+                    const int h = pp * g.sh - g.ph + r * g.dh;
+                    const bool hin = (unsigned)h < (unsigned)g.H;
+                    for (int s = 0; s < g.S; ++s) {
+                        const int w = q * g.sw - g.pw + s * g.dw;
                         const float wv = __ldg(p.b + ((long long)(r * g.S + s) * g.C + c) * g.D + d);
-                        acc = __fadd_rn(acc, dw_product<W>(dyv, wv, p.table, p.M, p.wlog));
+                        const bool in = hin && (unsigned)w < (unsigned)g.W;
+                        // a padded tap multiplies a zero operand: a signed zero, which leaves
+                        // the sum unchanged, unless the weight is infinite or NaN (then NaN)
+                        if (!in && isfinite(wv)) continue;
+                        const float xv = in ? __ldg(xn + ((long long)h * g.W + w) * g.C) : 0.0f;
+                        acc = __fadd_rn(acc, dw_product_t<W, GL>(xv, wv, lut, p.M, p.wlog));
                     }
                 }
-            p.out[pix * g.C + c] = acc;
-        } else {
-            // warp: one filter element (r,s,c,d) over one share of the N*P*Q pixels
-            const long long RSK = (long long)g.R * g.S * g.K;
-            const int share = (int)(it / RSK);
-            const long long o = it % RSK;
-            const int k = (int)(o % g.K);
-            const int s = (int)((o / g.K) % g.S);
-            const int r = (int)(o / ((long long)g.K * g.S));
+                p.out[(long long)pix * g.K + k] = acc;
+            }
+        }
+    } else if constexpr (MODE == 1) {
+        // a warp takes input pixels warp0, warp0 + warps, ..., each for every 32-channel group
+        const int npix = g.N * g.H * g.W;
+        for (int pix = warp0; pix < npix; pix += warps) {
+            const int w = pix % g.W, t = pix / g.W;
+            const int h = t % g.H, n = t / g.H;
+            for (int cg = 0; cg < p.groups; ++cg) {
+                const int c = cg * 32 + lane;
+                if (c >= g.C) continue;
+                const float *dyn = p.a + (long long)n * g.P * g.Q * g.K + (long long)c * g.D;
+                float acc = 0.0f;
+                for (int r = 0; r < g.R; ++r) {
+                    int pr = 0;
+                    const bool rin = dw_on_grid(h + g.ph - r * g.dh, g.sh, g.P, pr);
+                    for (int s = 0; s < g.S; ++s) {
+                        int qs = 0;
+                        const bool in = rin && dw_on_grid(w + g.pw - s * g.dw, g.sw, g.Q, qs);
+                        const float *dyp = dyn + ((long long)pr * g.Q + qs) * g.K;
+                        for (int d = 0; d < g.D; ++d) {
+                            const float wv = __ldg(p.b + ((long long)(r * g.S + s) * g.C + c) * g.D + d);
+                            // a tap between stride positions or past the edge multiplies a zero
+                            // operand: a signed zero, which leaves the sum unchanged, unless the
+                            // weight is infinite or NaN (then NaN)
+                            if (!in && isfinite(wv)) continue;
+                            const float dyv = in ? __ldg(dyp + d) : 0.0f;
+                            acc = __fadd_rn(acc, dw_product_t<W, GL>(dyv, wv, lut, p.M, p.wlog));
+                        }
+                    }
+                }
+                p.out[(long long)pix * g.C + c] = acc;
+            }
+        }
+    } else {
+        for (long long it = warp0; it < p.items; it += warps) {
+            // item: (filter tap, share of the N*P*Q pixels, 32-channel group); each lane
+            // sums its channel over the share's pixels in order
+            const int kg = (int)(it % p.groups);
+            long long rest = it / p.groups;
+            const int share = (int)(rest % p.G);
+            const int tap = (int)(rest / p.G);
+            const int r = tap / g.S, s = tap - r * g.S;
+            const int k = kg * 32 + lane;
+            if (k >= g.K) continue;
             const int c = k / g.D;
             const long long npq = (long long)g.N * g.P * g.Q;
             const long long b0 = npq * share / p.G, b1 = npq * (share + 1) / p.G;
             float acc = 0.0f;
-            for (long long pix = b0 + lane; pix < b1; pix += 32) {
-                const int q = (int)(pix % g.Q);
-                const int pp = (int)((pix / g.Q) % g.P);
-                const int n = (int)(pix / ((long long)g.P * g.Q));
-                const int h = pp * g.sh - g.ph + r * g.dh, w = q * g.sw - g.pw + s * g.dw;
-                float xv = 0.0f;
-                if ((unsigned)h < (unsigned)g.H && (unsigned)w < (unsigned)g.W)
-                    xv = __ldg(p.a + (((long long)n * g.H + h) * g.W + w) * g.C + c);
-                const float dyv = __ldg(p.b + pix * g.K + k);
-                acc = __fadd_rn(acc, dw_product<W>(xv, dyv, p.table, p.M, p.wlog));
+            if (b0 < b1) {
+                int q = (int)(b0 % g.Q);
+                const long long t = b0 / g.Q;
+                int pp = (int)(t % g.P), n = (int)(t / g.P);
+                for (long long pix = b0; pix < b1; ++pix) {
+                    const int h = pp * g.sh - g.ph + r * g.dh, w = q * g.sw - g.pw + s * g.dw;
+                    const float dyv = __ldg(p.b + pix * g.K + k);
+                    const bool in = (unsigned)h < (unsigned)g.H && (unsigned)w < (unsigned)g.W;
+                    if (in || !isfinite(dyv)) {
+                        const float xv = in ? __ldg(p.a + (((long long)n * g.H + h) * g.W + w) * g.C + c) : 0.0f;
+                        acc = __fadd_rn(acc, dw_product_t<W, GL>(xv, dyv, lut, p.M, p.wlog));
+                    }
+                    if (++q == g.Q) {
+                        q = 0;
+                        if (++pp == g.P) { pp = 0; ++n; }
+                    }
+                }
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-            if (lane == 0) p.out[(long long)share * RSK + o] = acc;
+            p.out[((long long)share * g.R * g.S + tap) * g.K + k] = acc;
         }
     }
 }
@@ -261,12 +313,22 @@ int launch_tile_any(int alu, int width, const DwTileParams &tp, int grid, size_t
     return launch_tile<MODE, 0>(width, tp, grid, smem, st);
 }
 
+constexpr int kDwDirectMaxLut = 64 * 1024;   // tables the direct kernel stages in shared memory
+
 template <int MODE>
 int launch_direct(int width, const DwDirectParams &dp, int grid, cudaStream_t st)
 {
-    if (width == 8) dw_direct_kernel<8, MODE><<<grid, 256, 0, st>>>(dp);
-    else if (width == 16) dw_direct_kernel<16, MODE><<<grid, 256, 0, st>>>(dp);
-    else dw_direct_kernel<32, MODE><<<grid, 256, 0, st>>>(dp);
+    const size_t smem = (size_t)((dp.table_bytes + 15) & ~15);
+    if (dp.table_bytes > 0) {
+        auto kfn = width == 8 ? dw_direct_kernel<8, MODE, false> : dw_direct_kernel<16, MODE, false>;
+        cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return amsim::cuda_status(e);
+        kfn<<<grid, 256, smem, st>>>(dp);
+    } else {
+        if (width == 8) dw_direct_kernel<8, MODE, true><<<grid, 256, 0, st>>>(dp);
+        else if (width == 16) dw_direct_kernel<16, MODE, true><<<grid, 256, 0, st>>>(dp);
+        else dw_direct_kernel<32, MODE, true><<<grid, 256, 0, st>>>(dp);
+    }
     return amsim::cuda_status(cudaGetLastError());
 }
 
@@ -341,8 +403,9 @@ DwFilterPlan filter_plan(const DwGeo &g, bool tiled, int sms, const amsim_lut_t 
         f.G_want = std::max(1, std::min(want, f.tiles));
     } else {
         const long long npq = (long long)g.N * g.P * g.Q;
-        const long long want = (64LL * sms + f.outs - 1) / f.outs;            // about 64 warps per SM
-        const long long cap = std::max(1LL, npq / 256);                       // at least 256 pixels a share
+        const long long items = (long long)g.R * g.S * ((g.K + 31) / 32);     // warps per share
+        const long long want = (64LL * sms + items - 1) / items;              // about 64 warps per SM
+        const long long cap = std::max(1LL, npq / 64);                        // at least 64 pixels a share
         f.G_want = (int)std::max(1LL, std::min(std::min(want, cap), 4096LL));
     }
     return f;
@@ -471,21 +534,24 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         dp.M = lut->M;
         dp.wlog = wlog;
         dp.G = 1;
+        dp.table_bytes = (width <= 16 && (int)lut->narrow_bytes <= kDwDirectMaxLut) ? (int)lut->narrow_bytes : 0;
         if (which == 0) {
-            dp.chunks = ((long long)g.N * g.P * g.Q + 31) / 32;
-            dp.items = dp.chunks * g.K;
+            dp.groups = (g.K + 31) / 32;
+            dp.items = (long long)g.N * g.P * g.Q * dp.groups;
             dp.out = out;
         } else if (which == 1) {
-            dp.chunks = ((long long)g.N * g.H * g.W + 31) / 32;
-            dp.items = dp.chunks * g.C;
+            dp.groups = (g.C + 31) / 32;
+            dp.items = (long long)g.N * g.H * g.W * dp.groups;
             dp.out = out;
         } else {
             const DwFilterPlan f = filter_plan(g, false, sms, lut);
             dp.G = shares_for(f, ws_bytes);
-            dp.items = f.outs * dp.G;
+            dp.groups = (g.K + 31) / 32;
+            dp.items = (long long)g.R * g.S * dp.G * dp.groups;
             dp.out = dp.G > 1 ? static_cast<float *>(ws) : out;
         }
-        const int grid = (int)std::max<long long>(1, std::min<long long>((dp.items + 7) / 8, 16LL * sms));
+        // persistent CTAs: each stages the table once
+        const int grid = (int)std::max<long long>(1, std::min<long long>((dp.items + 7) / 8, 8LL * sms));
         rc = which == 0 ? launch_direct<0>(width, dp, grid, st)
            : which == 1 ? launch_direct<1>(width, dp, grid, st)
                         : launch_direct<2>(width, dp, grid, st);

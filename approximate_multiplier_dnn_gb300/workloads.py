@@ -132,3 +132,15 @@ def dwconv3x3(N=64, H=56, W=56, C=128, D=1, seed=0):
     return {"x": normal((N, H, W, C), 1.0, seed),
             "w": he_normal((3, 3, C, D), 9, seed + 1),
             "dy": normal((N, H, W, C * D), 0.01, seed + 2)}
+
+
+# MobileNet-style strided depthwise layer: 112x112x64 -> 56x56x64
+DWCONV3X3_S2 = dict(N=64, H=112, W=112, C=64, D=1, R=3, S=3, stride=(2, 2), pad=(1, 1), dil=(1, 1))
+
+
+def dwconv3x3_s2(N=64, H=112, W=112, C=64, seed=0):
+    """As dwconv3x3 for the stride-2 layer: dY is the 56x56 output's gradient."""
+    P = (H + 2 - 3) // 2 + 1
+    return {"x": normal((N, H, W, C), 1.0, seed),
+            "w": he_normal((3, 3, C, 1), 9, seed + 1),
+            "dy": normal((N, P, P, C), 0.01, seed + 2)}

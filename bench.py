@@ -38,7 +38,7 @@ LOOKUPS_PER_CLK_PER_SM = 32     # one 4-byte shared-memory wavefront per clock p
 CLOSED_FORM_PER_CLK_PER_SM = {"mitchell": 64, "exact": 128}
 
 WORKLOADS = ("mlp", "mlp_layers", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "dwconv3x3",
-             "gemm64", "mul")
+             "dwconv3x3_s2", "gemm64", "mul")
 
 
 def measured_peaks():
@@ -84,6 +84,9 @@ def make_step(name, lut_for, M=7, kind="mitchell"):
     if name == "dwconv3x3":
         return (steps.DwConvStep(wl.dwconv3x3(), wl.DWCONV3X3, lut_for("mitchell", 7)),
                 "dwconv3x3_nhwc_64x56x56x128_d1_fwd+bwd_data+bwd_filter_mitchell_M7")
+    if name == "dwconv3x3_s2":
+        return (steps.DwConvStep(wl.dwconv3x3_s2(), wl.DWCONV3X3_S2, lut_for("mitchell", 7)),
+                "dwconv3x3_stride2_nhwc_64x112x112x64_d1_fwd+bwd_data+bwd_filter_mitchell_M7")
     if name == "mul":
         from approximate_multiplier_dnn_gb300 import steps as st
         return st.MulStep(wl.elementwise_pairs(1 << 28, seed=5), lut_for("mitchell", 7)), \
@@ -463,7 +466,7 @@ def main():
                         frac=achieved / cpeak, lookup_roofline_frac=achieved / peak,
                         kernel="lutgemm_raw_kernel<1|2> (closed forms, no table); see amsim_last_path")
         roofline.pop("lut_residency", None)
-    if args.workload == "dwconv3x3":
+    if args.workload in ("dwconv3x3", "dwconv3x3_s2"):
         # a stencil: each pass reads its operands once and writes its output
         # once, with 9 products per output element.  Every pass's two lower
         # bounds (compulsory DRAM bytes at the measured copy bandwidth, lookups
