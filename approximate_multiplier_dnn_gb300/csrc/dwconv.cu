@@ -81,6 +81,7 @@ struct DwDirectParams {
     long long items;       // mode 0/1: pixels x channel groups; mode 2: taps x shares x channel groups
     int groups;            // 32-channel groups of the lanes' channel dimension
     int table_bytes;       // staged table bytes (0: read through the cache)
+    int grid_taps;         // data gradient: unit dilation, so the taps on the stride grid can be enumerated
     int G;                 // mode 2: shares of the N*P*Q reduction
 };
 
@@ -128,9 +129,22 @@ __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ 
         const uint4 *src = static_cast<const uint4 *>(p.table);
         uint4 *dst = reinterpret_cast<uint4 *>(dsmem);
         for (int i = threadIdx.x; i < (p.table_bytes + 15) >> 4; i += blockDim.x) dst[i] = __ldg(src + i);
-        __syncthreads();
         lut = dsmem;
     }
+    // data gradient: per input channel, whether all its filter taps are finite
+    // (then taps off the stride grid, whose products are signed zeros, need no visit)
+    uint8_t *finite = dsmem + ((p.table_bytes + 15) & ~15);
+    if constexpr (MODE == 1) {
+        for (int c = threadIdx.x; c < g.C; c += blockDim.x) {
+            bool ok = true;
+            for (int t = 0; t < g.R * g.S * g.D; ++t) {
+                const int tap = t / g.D, d = t - tap * g.D;
+                ok = ok && isfinite(__ldg(p.b + ((long long)tap * g.C + c) * g.D + d));
+            }
+            finite[c] = ok;
+        }
+    }
+    __syncthreads();
     const int warps = gridDim.x * (blockDim.x >> 5);
     const int warp0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if constexpr (MODE == 0) {
@@ -174,6 +188,26 @@ __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ 
                 if (c >= g.C) continue;
                 const float *dyn = p.a + (long long)n * g.P * g.Q * g.K + (long long)c * g.D;
                 float acc = 0.0f;
+                if (p.grid_taps && finite[c]) {
+                    // unit dilation: the taps on the stride grid are r = r0, r0 + sh, ... with
+                    // r0 = (h + ph) mod sh, and likewise s; the others add signed zeros
+                    const int r0 = (h + g.ph) % g.sh, s0 = (w + g.pw) % g.sw;
+                    for (int r = r0; r < g.R; r += g.sh) {
+                        const int pr = (h + g.ph - r) / g.sh;
+                        if (pr < 0 || pr >= g.P) continue;
+                        for (int s = s0; s < g.S; s += g.sw) {
+                            const int qs = (w + g.pw - s) / g.sw;
+                            if (qs < 0 || qs >= g.Q) continue;
+                            const float *dyp = dyn + ((long long)pr * g.Q + qs) * g.K;
+                            const float *wp = p.b + ((long long)(r * g.S + s) * g.C + c) * g.D;
+                            for (int d = 0; d < g.D; ++d)
+                                acc = __fadd_rn(acc, dw_product_t<W, GL>(__ldg(dyp + d), __ldg(wp + d), lut, p.M,
+                                                                         p.wlog));
+                        }
+                    }
+                    p.out[(long long)pix * g.C + c] = acc;
+                    continue;
+                }
                 for (int r = 0; r < g.R; ++r) {
                     int pr = 0;
                     const bool rin = dw_on_grid(h + g.ph - r * g.dh, g.sh, g.P, pr);
@@ -318,17 +352,17 @@ constexpr int kDwDirectMaxLut = 64 * 1024;   // tables the direct kernel stages 
 template <int MODE>
 int launch_direct(int width, const DwDirectParams &dp, int grid, cudaStream_t st)
 {
-    const size_t smem = (size_t)((dp.table_bytes + 15) & ~15);
-    if (dp.table_bytes > 0) {
-        auto kfn = width == 8 ? dw_direct_kernel<8, MODE, false> : dw_direct_kernel<16, MODE, false>;
+    // the staged table, then (data gradient) one flag byte per input channel
+    const size_t smem = (size_t)((dp.table_bytes + 15) & ~15) + (MODE == 1 ? (size_t)dp.g.C : 0);
+    auto kfn = dp.table_bytes > 0 ? (width == 8 ? dw_direct_kernel<8, MODE, false> : dw_direct_kernel<16, MODE, false>)
+             : width == 8          ? dw_direct_kernel<8, MODE, true>
+             : width == 16         ? dw_direct_kernel<16, MODE, true>
+                                   : dw_direct_kernel<32, MODE, true>;
+    if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return amsim::cuda_status(e);
-        kfn<<<grid, 256, smem, st>>>(dp);
-    } else {
-        if (width == 8) dw_direct_kernel<8, MODE, true><<<grid, 256, 0, st>>>(dp);
-        else if (width == 16) dw_direct_kernel<16, MODE, true><<<grid, 256, 0, st>>>(dp);
-        else dw_direct_kernel<32, MODE, true><<<grid, 256, 0, st>>>(dp);
     }
+    kfn<<<grid, 256, smem, st>>>(dp);
     return amsim::cuda_status(cudaGetLastError());
 }
 
@@ -535,6 +569,9 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         dp.wlog = wlog;
         dp.G = 1;
         dp.table_bytes = (width <= 16 && (int)lut->narrow_bytes <= kDwDirectMaxLut) ? (int)lut->narrow_bytes : 0;
+        dp.grid_taps = g.dh == 1 && g.dw == 1;
+        if (which == 1 && (size_t)g.C + 16 + (size_t)dp.table_bytes > (size_t)amsim::kMaxSmemPerCta)
+            return AMSIM_EUNSUPPORTED;     // the channel flags do not fit shared memory
         if (which == 0) {
             dp.groups = (g.K + 31) / 32;
             dp.items = (long long)g.N * g.P * g.Q * dp.groups;
