@@ -467,6 +467,9 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
         const int nvec = (p.table_bytes + 15) >> 4;
         for (int i = tid; i < nvec; i += kDwThreads) dst[i] = __ldg(src + i);
     }
+    // the barrier's initialisation (thread 0) and the staged table are visible to
+    // every thread before any of them waits on the barrier or reads the table
+    __syncthreads();
     const int hi_shift = p.M + p.wlog, lo_shift = p.wlog;
 
     float2 facc[CPW][9];                    // mode 2: per-tap sums of this CTA's share

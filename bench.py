@@ -247,7 +247,7 @@ def lut_residency(lut):
 # sources of the LUT-GEMM kernels (the kernel the traffic records measure);
 # a record holds for one version of them
 KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_ws.cuh", "gemm_tma.cuh", "gemm_raw.cuh")
-DW_KERNEL_SOURCES = ("gemm_kernel.cuh", "dwconv_kernel.cuh", "dwconv.cu")
+DW_KERNEL_SOURCES = ("gemm_kernel.cuh", "dwconv_kernel.cuh")   # the tiled kernel's own sources
 
 
 def kernel_sha(sources=KERNEL_SOURCES):
