@@ -325,10 +325,12 @@ bool dw_map(CUtensorMap *map, const float *base, int N, int H, int W, int C, int
     return amsim::encode_tensor_map(map, m) == AMSIM_OK;
 }
 
-// The closed-form variants are compiled in dwconv_alu.cu.
+// The closed-form variants are compiled in dwconv_alu.cu, the stride-2 kernel in dwconv_s2.cu.
 }  // namespace
 namespace amsim {
 namespace dw {
+int launch_s2(int mode, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st);
+size_t s2_smem_bytes(int table_bytes, int mode);
 extern template int launch_tile<0, 1>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<1, 1>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<2, 1>(int, const DwTileParams &, int, size_t, cudaStream_t);
@@ -370,6 +372,27 @@ int wlog_of(int width_bits) { return width_bits == 8 ? 0 : width_bits == 16 ? 1 
 
 // Shares of the weight gradient's reduction: the count that fills the GPU,
 // and the count that fits `ws_bytes` of scratch (at least 1: no scratch).
+// The stride-2 tiled kernel covers 3x3 filters at stride 2 and unit dilation
+// with one filter per channel, for the forward pass and the weight gradient,
+// on the same conditions as the stride-1 kernel.
+bool dw_s2_ok(const DwGeo &g, const amsim_lut_t lut, int which, const float *t0, const float *t1,
+              const float *out)
+{
+    if (which == 1 || g.D != 1 || g.R != 3 || g.S != 3 || g.sh != 2 || g.sw != 2 || g.dh != 1 || g.dw != 1)
+        return false;
+    if (g.C % 4 || lut->width_bits == 32 || (int)lut->narrow_bytes > kDwMaxTileLut) return false;
+    if (!aligned16(t0) || (which == 0 && !aligned16(out)) || (which == 2 && !aligned16(t1))) return false;
+    return true;
+}
+
+int s2_ctas_per_sm(const amsim_lut_t lut, int which)
+{
+    const int per = (int)amsim::dw::s2_smem_bytes((int)lut->narrow_bytes, which) + 1024;
+    return std::max(1, std::min(2, (228 * 1024) / per));
+}
+
+constexpr int kS2Rows = 4, kS2Cols = 64, kS2Ch = 8;   // the stride-2 kernel's tile
+
 struct DwFilterPlan {
     bool tiled;
     int tiles_p, tiles_q, cblocks, tiles;
@@ -421,12 +444,20 @@ DwShape dw_shape(int OH, int OW)
     return best;
 }
 
-DwFilterPlan filter_plan(const DwGeo &g, bool tiled, int sms, const amsim_lut_t lut)
+// kind: 0 direct kernel, 1 tiled kernel, 2 stride-2 tiled kernel.
+DwFilterPlan filter_plan(const DwGeo &g, int kind, int sms, const amsim_lut_t lut)
 {
     DwFilterPlan f{};
-    f.tiled = tiled;
+    f.tiled = kind != 0;
     f.outs = (long long)g.R * g.S * g.K;
-    if (tiled) {
+    if (kind == 2) {
+        f.tiles_p = (g.P + kS2Rows - 1) / kS2Rows;
+        f.tiles_q = (g.Q + kS2Cols - 1) / kS2Cols;
+        f.cblocks = (g.C + kS2Ch - 1) / kS2Ch;
+        f.tiles = g.N * f.tiles_p * f.tiles_q;
+        const int slots = s2_ctas_per_sm(lut, 2) * sms;
+        f.G_want = std::max(1, std::min((slots + f.cblocks - 1) / f.cblocks, f.tiles));
+    } else if (kind == 1) {
         const DwShape sh = dw_shape(g.P, g.Q);
         f.tiles_p = (g.P + sh.tp - 1) / sh.tp;
         f.tiles_q = (g.Q + sh.tq - 1) / sh.tq;
@@ -480,6 +511,56 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         rc = amsim::cuda_status(cudaMemsetAsync(out, 0, (size_t)n_out * 4, st));
         if (rc == AMSIM_OK) amsim::set_last_path(path);
         return rc;
+    }
+
+    if (!tiled && dw_s2_ok(g, lut, which, t0, t1, out)) {
+        // stride 2: forward or weight gradient on the stride-2 tiled kernel
+        DwTileParams sp{};
+        sp.table = tab_tiled;
+        sp.table_bytes = (int)lut->narrow_bytes;
+        sp.M = lut->M;
+        sp.wlog = wlog;
+        sp.N = g.N;
+        sp.C = g.C;
+        sp.a = t0;
+        sp.b = t1;
+        sp.expand_mul = 1u << (24 - width);
+        sp.IH = g.H; sp.IW = g.W; sp.OH = g.P; sp.OW = g.Q;
+        sp.oy = -g.ph; sp.ox = -g.pw;
+        sp.tiles_p = (g.P + kS2Rows - 1) / kS2Rows;
+        sp.tiles_q = (g.Q + kS2Cols - 1) / kS2Cols;
+        sp.cblocks = (g.C + kS2Ch - 1) / kS2Ch;
+        sp.tiles = g.N * sp.tiles_p * sp.tiles_q;
+        const bool mapped = dw_map(&sp.amap, t0, g.N, g.H, g.W, g.C, kS2Ch, 2 * kS2Cols + 1, 2 * kS2Rows + 1) &&
+                            (which == 0 || dw_map(&sp.bmap, t1, g.N, g.P, g.Q, g.C, kS2Ch, kS2Cols, kS2Rows));
+        if (mapped) {
+            const size_t smem = amsim::dw::s2_smem_bytes((int)lut->narrow_bytes, which);
+            path = AMSIM_PATH_DW_TILES;
+            if (which == 0) {
+                sp.out = out;
+                sp.G = 1;
+                const long long total = (long long)sp.tiles * sp.cblocks;
+                if (total > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
+                const int grid = (int)std::min<long long>(total, (long long)s2_ctas_per_sm(lut, 0) * sms);
+                rc = amsim::dw::launch_s2(0, width, sp, grid, smem, st);
+                if (rc == AMSIM_OK) amsim::count_launch();
+            } else {
+                const DwFilterPlan f = filter_plan(g, 2, sms, lut);
+                sp.G = shares_for(f, ws_bytes);
+                sp.out = sp.G > 1 ? static_cast<float *>(ws) : out;
+                rc = amsim::dw::launch_s2(2, width, sp, sp.cblocks * sp.G, smem, st);
+                if (rc == AMSIM_OK) amsim::count_launch();
+                if (rc == AMSIM_OK && sp.G > 1) {
+                    const int blocks = (int)std::min<long long>((n_out + 255) / 256, 4LL * sms);
+                    dw_sum_kernel<<<blocks, 256, 0, st>>>(static_cast<const float *>(ws), out, n_out, sp.G);
+                    rc = amsim::cuda_status(cudaGetLastError());
+                    if (rc == AMSIM_OK) amsim::count_launch();
+                    path |= AMSIM_PATH_STREAMK;
+                }
+            }
+            if (rc == AMSIM_OK) amsim::set_last_path(path);
+            return rc;
+        }
     }
 
     DwTileParams tp{};
@@ -545,7 +626,7 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
                             : launch_tile_any<1>(alu, width, tp, grid, smem, st);
             if (rc == AMSIM_OK) amsim::count_launch();
         } else {
-            const DwFilterPlan f = filter_plan(g, true, sms, lut);
+            const DwFilterPlan f = filter_plan(g, 1, sms, lut);
             tp.G = shares_for(f, ws_bytes);
             tp.out = tp.G > 1 ? static_cast<float *>(ws) : out;
             const int grid = tp.cblocks * tp.G;
@@ -581,7 +662,7 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
             dp.items = (long long)g.N * g.H * g.W * dp.groups;
             dp.out = out;
         } else {
-            const DwFilterPlan f = filter_plan(g, false, sms, lut);
+            const DwFilterPlan f = filter_plan(g, 0, sms, lut);
             dp.G = shares_for(f, ws_bytes);
             dp.groups = (g.K + 31) / 32;
             dp.items = (long long)g.R * g.S * dp.G * dp.groups;
@@ -632,8 +713,10 @@ size_t amsim_dwconv2d_workspace_size(const amsim_conv_desc *desc, int which, ams
     DwGeo g;
     if (which != 2 || !lut || dw_geometry(desc, &g) != AMSIM_OK) return 0;
     const int dev = lut->device;
-    const bool tiled = dw_tile_ok(g, lut, 2, nullptr, nullptr, nullptr);
-    const DwFilterPlan f = filter_plan(g, tiled, sm_count(dev), lut);
+    const int kind = dw_tile_ok(g, lut, 2, nullptr, nullptr, nullptr)  ? 1
+                   : dw_s2_ok(g, lut, 2, nullptr, nullptr, nullptr) ? 2
+                                                                     : 0;
+    const DwFilterPlan f = filter_plan(g, kind, sm_count(dev), lut);
     if (f.G_want <= 1) return 0;
     return (size_t)f.G_want * (size_t)f.outs * 4;
 }

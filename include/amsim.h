@@ -370,9 +370,9 @@ size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim
  * channel c only:
  *   y[n,p,q,c*D+d] = sum_{r,s} AMSim(x[n, p*sh - ph + r*dh, q*sw - pw + s*dw, c], w[r,s,c,d]).
  * x: N*H*W*C, w: R*S*C*D, y: N*P*Q*K (written).  Padded taps are zero
- * operands.  3x3 filters with unit stride and dilation, D = 1, C a multiple of
- * 4, 16-byte aligned x and y and an 8- or 16-bit narrowed LUT of at most
- * 64 KB take the tiled kernel (AMSIM_PATH_DW_TILES); everything else the
+ * operands.  3x3 filters with unit dilation at stride 1 or 2, D = 1, C a
+ * multiple of 4, 16-byte aligned x and y and an 8- or 16-bit narrowed LUT of
+ * at most 64 KB take a tiled kernel (AMSIM_PATH_DW_TILES); everything else the
  * direct kernel (AMSIM_PATH_DW_DIRECT).  Scratch is not used.
  */
 int amsim_dwconv2d_fwd(const amsim_conv_desc *desc, const float *x, const float *w, float *y,
@@ -385,7 +385,8 @@ int amsim_dwconv2d_fwd(const amsim_conv_desc *desc, const float *x, const float 
  *   p = (h + ph - r*dh)/sh, q = (w + pw - s*dw)/sw where integral and in range
  *   (zero operands elsewhere).
  * dy: N*P*Q*K, w: R*S*C*D, dx: N*H*W*C (written).  Kernel choice as for the
- * forward pass (dy and dx 16-byte aligned).  Scratch is not used.
+ * forward pass at stride 1 (dy and dx 16-byte aligned); strided layers take
+ * the direct kernel.  Scratch is not used.
  */
 int amsim_dwconv2d_bwd_data(const amsim_conv_desc *desc, const float *dy, const float *w, float *dx,
                             amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);

@@ -33,8 +33,16 @@ DIRECT = [
     (2, 8, 9, 4, 2, 3, 3, (1, 2), (2, 2), (2, 1)),      # multiplier 2, dilation
     (1, 10, 7, 3, 1, 5, 3, (3, 2), (2, 2), (1, 2)),
     (1, 5, 5, 5, 1, 1, 1, (1, 1), (0, 0), (1, 1)),      # pointwise
-    (2, 16, 16, 32, 1, 3, 3, (2, 2), (1, 1), (1, 1)),   # the stride-2 MobileNet layer shape
     (1, 12, 40, 8, 4, 3, 3, (1, 1), (1, 1), (1, 1)),    # 3x3 unit stride with multiplier 4
+]
+
+# 3x3 stride 2: the stride-2 tiled kernel for the forward pass and the weight
+# gradient, the direct kernel for the data gradient
+STRIDE2 = [
+    (2, 16, 16, 32, 1, 3, 3, (2, 2), (1, 1), (1, 1)),   # the stride-2 MobileNet layer shape
+    (1, 33, 130, 16, 1, 3, 3, (2, 2), (1, 1), (1, 1)),  # 17 x 65 outputs: ragged row and column tiles
+    (2, 14, 14, 12, 1, 3, 3, (2, 2), (1, 1), (1, 1)),   # 12 channels: a half channel block
+    (1, 17, 17, 8, 1, 3, 3, (2, 2), (0, 0), (1, 1)),    # no padding
 ]
 
 PASSES = ("fwd", "bwd_data", "bwd_filter")
@@ -83,12 +91,14 @@ def oracle_pass(orc, kind, M, which, desc, t0, t1, n):
 
 
 def check_passes(amd, orc, lut, kind, M, g, x, w, dy, expect_path, scratch=True):
+    """expect_path: one AMSIM_PATH_* bit for every pass, or a bit per pass."""
     desc, P, Q = dims(orc, g)
     args = ((x, w), (dy, w), (x, dy))
+    expect = tuple(expect_path) if isinstance(expect_path, (tuple, list)) else (expect_path,) * 3
     for which in range(3):
         shape = out_shape(g, P, Q, which)
         got, path = run_dw(amd, lut, which, g, *args[which], shape, scratch)
-        assert path & expect_path, (PASSES[which], g, path)
+        assert path & expect[which], (PASSES[which], g, path)
         ref, sa = oracle_pass(orc, kind, M, which, desc, *args[which], got.size)
         assert_close(got.reshape(-1), ref, sa, f"{PASSES[which]} {g} {kind} M={M}")
 
@@ -107,6 +117,15 @@ def test_dwconv_direct_kernel(amd, orc, luts, g, kind):
     rng = np.random.default_rng(3 + sum(g[:7]) + 7 * (kind == "exact"))
     x, w, dy = operands(orc, g, rng)
     check_passes(amd, orc, luts(kind, 7), kind, 7, g, x, w, dy, amd.AMSIM_PATH_DW_DIRECT)
+
+
+@pytest.mark.parametrize("kind", ["mitchell", "exact"])
+@pytest.mark.parametrize("g", STRIDE2)
+def test_dwconv_stride2_kernel(amd, orc, luts, g, kind):
+    rng = np.random.default_rng(5 + sum(g[:7]) + 7 * (kind == "exact"))
+    x, w, dy = operands(orc, g, rng)
+    t, d = amd.AMSIM_PATH_DW_TILES, amd.AMSIM_PATH_DW_DIRECT
+    check_passes(amd, orc, luts(kind, 7), kind, 7, g, x, w, dy, (t, d, t))
 
 
 @pytest.mark.parametrize("M,path", [(1, "tiles"), (4, "tiles"), (8, "direct"), (11, "direct")])
@@ -133,7 +152,7 @@ def sprinkle(a, rng, frac=0.03):
     return flat.view(np.float32).reshape(a.shape)
 
 
-@pytest.mark.parametrize("g", [TILED[0], TILED[1], DIRECT[1], DIRECT[5]])
+@pytest.mark.parametrize("g", [TILED[0], TILED[1], DIRECT[1], STRIDE2[0], STRIDE2[3]])
 def test_dwconv_special_operands(amd, orc, luts, g):
     """Zeros, denormals, infinities, NaN and overflowing products in every
     operand: the NaN pattern and infinities match exactly, the rest within the
@@ -146,7 +165,8 @@ def test_dwconv_special_operands(amd, orc, luts, g):
     if g[8] == (0, 0):
         x[0, 3, -1, :] = np.inf
         x[0, 4, -2, 1] = -np.inf
-    bit = amd.AMSIM_PATH_DW_TILES if g in TILED else amd.AMSIM_PATH_DW_DIRECT
+    t, d = amd.AMSIM_PATH_DW_TILES, amd.AMSIM_PATH_DW_DIRECT
+    bit = t if g in TILED else (t, d, t) if g in STRIDE2 else d
     check_passes(amd, orc, luts("mitchell", 7), "mitchell", 7, g, x, w, dy, bit)
 
 
