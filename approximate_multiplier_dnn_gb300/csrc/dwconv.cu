@@ -331,6 +331,8 @@ namespace amsim {
 namespace dw {
 int launch_s2(int mode, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st);
 size_t s2_smem_bytes(int table_bytes, int mode);
+int launch_s2d(int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st);
+size_t s2d_smem_bytes(int table_bytes);
 extern template int launch_tile<0, 1>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<1, 1>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<2, 1>(int, const DwTileParams &, int, size_t, cudaStream_t);
@@ -378,10 +380,12 @@ int wlog_of(int width_bits) { return width_bits == 8 ? 0 : width_bits == 16 ? 1 
 bool dw_s2_ok(const DwGeo &g, const amsim_lut_t lut, int which, const float *t0, const float *t1,
               const float *out)
 {
-    if (which == 1 || g.D != 1 || g.R != 3 || g.S != 3 || g.sh != 2 || g.sw != 2 || g.dh != 1 || g.dw != 1)
-        return false;
+    if (g.D != 1 || g.R != 3 || g.S != 3 || g.sh != 2 || g.sw != 2 || g.dh != 1 || g.dw != 1) return false;
+    // the data gradient's kernel is written for padding 1 (each output parity
+    // class then has fixed taps)
+    if (which == 1 && (g.ph != 1 || g.pw != 1)) return false;
     if (g.C % 4 || lut->width_bits == 32 || (int)lut->narrow_bytes > kDwMaxTileLut) return false;
-    if (!aligned16(t0) || (which == 0 && !aligned16(out)) || (which == 2 && !aligned16(t1))) return false;
+    if (!aligned16(t0) || (which != 2 && !aligned16(out)) || (which == 2 && !aligned16(t1))) return false;
     return true;
 }
 
@@ -531,7 +535,30 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         sp.tiles_q = (g.Q + kS2Cols - 1) / kS2Cols;
         sp.cblocks = (g.C + kS2Ch - 1) / kS2Ch;
         sp.tiles = g.N * sp.tiles_p * sp.tiles_q;
-        const bool mapped = dw_map(&sp.amap, t0, g.N, g.H, g.W, g.C, kS2Ch, 2 * kS2Cols + 1, 2 * kS2Rows + 1) &&
+        if (which == 1) {
+            // data gradient: 8 x 64 dx tiles of 16 channels over 5 x 33 dy windows
+            sp.IH = g.P; sp.IW = g.Q; sp.OH = g.H; sp.OW = g.W;
+            sp.out = out;
+            sp.tiles_p = (g.H + 7) / 8;
+            sp.tiles_q = (g.W + 63) / 64;
+            sp.cblocks = (g.C + 15) / 16;
+            sp.tiles = g.N * sp.tiles_p * sp.tiles_q;
+            if (dw_map(&sp.amap, t0, g.N, g.P, g.Q, g.C, 16, 33, 5)) {
+                const long long total = (long long)sp.tiles * sp.cblocks;
+                if (total > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
+                const size_t smem = amsim::dw::s2d_smem_bytes((int)lut->narrow_bytes);
+                const int per_sm = std::max(1, std::min(2, (int)((228 * 1024) / (smem + 1024))));
+                const int grid = (int)std::min<long long>(total, (long long)per_sm * sms);
+                rc = amsim::dw::launch_s2d(width, sp, grid, smem, st);
+                if (rc == AMSIM_OK) {
+                    amsim::count_launch();
+                    amsim::set_last_path(AMSIM_PATH_DW_TILES);
+                }
+                return rc;
+            }
+        }
+        const bool mapped = which != 1 &&
+                            dw_map(&sp.amap, t0, g.N, g.H, g.W, g.C, kS2Ch, 2 * kS2Cols + 1, 2 * kS2Rows + 1) &&
                             (which == 0 || dw_map(&sp.bmap, t1, g.N, g.P, g.Q, g.C, kS2Ch, kS2Cols, kS2Rows));
         if (mapped) {
             const size_t smem = amsim::dw::s2_smem_bytes((int)lut->narrow_bytes, which);

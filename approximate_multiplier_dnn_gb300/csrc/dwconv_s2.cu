@@ -356,6 +356,216 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_const
     }
 }
 
+// ------------------------------------------------------------------ data gradient
+// Stride 2, padding 1: dx(2I + a, 2J + b) = sum over the taps whose parity fits:
+//   rows: a = 0 -> tap row 1 at dy row I; a = 1 -> tap rows 0 and 2 at dy rows I + 1 and I
+//   columns likewise (b = 0 -> tap column 1 at dy column J; b = 1 -> tap columns 0 and 2
+//   at dy columns J + 1 and J).
+// A tile is 8 dx rows x 64 dx columns x 16 channels (two per warp); a lane owns
+// dx columns 2J, 2J + 1 (J = lane) of all 8 rows and reads dy columns J, J + 1
+// of the tile's 5 x 33 dy window.  The tap is warp-uniform, so lookups read one
+// table row.  Tiles with |x| >= 2^64, infinities or NaN take a slow computation
+// that visits all nine taps of every output (off-parity taps as zero operands,
+// as the page's zero-operand rule has them).
+constexpr int kSdRows = 8, kSdCols = 64, kSdCB = 16;
+constexpr int kSdWR = kSdRows / 2 + 1;        // dy window rows
+constexpr int kSdWC = kSdCols / 2 + 1;        // dy window columns
+constexpr int kSdPW = kSdWC;                  // packed window row pitch (scalar loads)
+constexpr int kSdCP = 170;                    // words per channel: >= 5 x 33, = 2 mod 8
+static_assert(kSdWR * kSdPW <= kSdCP, "window pitch");
+constexpr int kSdRaw = (kSdWR * kSdWC * kSdCB * 4 + 127) & ~127;
+constexpr int kSdWin = (kSdCB * kSdCP * 4 + 127) & ~127;
+constexpr int kSdOut = (kSdCB * kDwOP * 4 + 127) & ~127;
+constexpr int kSdWB = (2 * kSdCB * 9 * 4 + 127) & ~127;
+
+__host__ __device__ constexpr int sd_smem(int table_bytes)
+{
+    return dw_lut_region(table_bytes) + kSdRaw + kSdWin + kSdOut + kSdWB + 128;
+}
+
+template <int W, bool SLOW>
+__device__ __forceinline__ void sd_channel(float2 (&acc)[kSdRows], const uint32_t *wr, const uint8_t *lut,
+                                           const uint32_t (&woff)[9], const float (&wsc)[9], uint32_t mul)
+{
+#pragma unroll
+    for (int i = 0; i < kSdRows; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    if constexpr (!SLOW) {
+#pragma unroll
+        for (int ww = 0; ww < kSdWR; ++ww) {
+            const uint32_t d0 = wr[ww * kSdPW], d1 = wr[ww * kSdPW + 1];
+            const uint32_t b0 = dw_scale_bits(d0), b1 = dw_scale_bits(d1);
+            const float2 sd = make_float2(__uint_as_float(b0), __uint_as_float(b1));
+            // (dx row, tap row) pairs this window row feeds
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const int row = k == 0 ? 2 * ww : k == 1 ? 2 * ww - 1 : 2 * ww + 1;   // dx row of the lane
+                const int r = k == 0 ? 1 : k == 1 ? 0 : 2;
+                if (row < 0 || row >= kSdRows) continue;
+                // column pair: dx 2J (tap column 1, dy J) and 2J + 1 (tap column 0, dy J + 1)
+                const int t1 = r * 3 + 1, t0 = r * 3 + 0, t2 = r * 3 + 2;
+                const uint32_t i0 = d0 - b0 + woff[t1], i1 = d1 - b1 + woff[t0];
+                const float2 v = make_float2(dw_expand(lut_ld<W, false>(lut, i0), mul),
+                                             dw_expand(lut_ld<W, false>(lut, i1), mul));
+                const float2 sc = fmul2_ftz(make_float2(wsc[t1], wsc[t0]), sd);
+                acc[row] = ffma2(v, sc, acc[row]);
+                // dx 2J + 1 again: tap column 2 at dy J
+                const float v2 = dw_expand(lut_ld<W, false>(lut, d0 - b0 + woff[t2]), mul);
+                acc[row].y = fmaf(v2, fmul_ftz(wsc[t2], sd.x), acc[row].y);
+            }
+        }
+    } else {
+        // all nine taps of each output, products rounded before the add
+#pragma unroll
+        for (int row = 0; row < kSdRows; ++row)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float a = 0.0f;
+#pragma unroll
+                for (int r = 0; r < 3; ++r)
+#pragma unroll
+                    for (int s = 0; s < 3; ++s) {
+                        const int ry = row + 1 - r, cx = b + 1 - s;   // twice the window offsets
+                        const bool on = (ry & 1) == 0 && (cx & 1) == 0 && ry >= 0;
+                        // cx >= -1: cx even means 0 or 2, i.e. dy column J or J + 1
+                        const uint32_t d = on ? wr[(ry >> 1) * kSdPW + (cx >> 1)] : 0u;
+                        const uint32_t sb = dw_scale_bits(d);
+                        const int t = r * 3 + s;
+                        const float v = dw_expand(lut_ld<W, false>(lut, d - sb + woff[t]), mul);
+                        a = __fadd_rn(a, __fmul_rn(v, fmul_ftz(wsc[t], __uint_as_float(sb))));
+                    }
+                if (b == 0) acc[row].x = a;
+                else acc[row].y = a;
+            }
+    }
+}
+
+template <int W>
+__global__ void __launch_bounds__(kDwThreads, 2) dw_s2d_kernel(const __grid_constant__ DwTileParams p)
+{
+    using amsim::kern::mbar_expect_tx;
+    using amsim::kern::mbar_init;
+    using amsim::kern::mbar_wait;
+    using amsim::kern::tma_load_4d;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint8_t *lut = smem;
+    float *raw = reinterpret_cast<float *>(smem + dw_lut_region(p.table_bytes));
+    uint32_t *win = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(raw) + kSdRaw);
+    float *ot = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(win) + kSdWin);
+    uint32_t *wt_off = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(ot) + kSdOut);
+    float *wt_scl = reinterpret_cast<float *>(wt_off + kSdCB * 9);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(wt_off) + kSdWB);
+
+    const int total = p.tiles * p.cblocks;
+    auto tile_at = [&](int t) {
+        DwTile d;
+        const int cb = t % p.cblocks;
+        int rest = t / p.cblocks;
+        const int tqi = rest % p.tiles_q;
+        rest /= p.tiles_q;
+        d.p0 = (rest % p.tiles_p) * kSdRows;     // first dx row
+        d.n = rest / p.tiles_p;
+        d.q0 = tqi * kSdCols;                    // first dx column
+        d.c0 = cb * kSdCB;
+        return d;
+    };
+    auto issue = [&](const DwTile &t) {
+        mbar_expect_tx(bar, kSdWR * kSdWC * kSdCB * 4);
+        tma_load_4d(raw, &p.amap, t.c0, t.q0 / 2, t.p0 / 2, t.n, bar);
+    };
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if ((int)blockIdx.x < total) issue(tile_at(blockIdx.x));
+    }
+    {
+        const uint4 *src = static_cast<const uint4 *>(p.table);
+        uint4 *dst = reinterpret_cast<uint4 *>(lut);
+        const int nvec = (p.table_bytes + 15) >> 4;
+        for (int i = tid; i < nvec; i += kDwThreads) dst[i] = __ldg(src + i);
+    }
+    // the barrier's initialisation and the staged table are visible to every
+    // thread before any of them waits on the barrier or reads the table
+    __syncthreads();
+    const int hi_shift = p.M + p.wlog, lo_shift = p.wlog;
+    uint32_t phase = 0;
+    bool aborted = false;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const DwTile tl = tile_at(t);
+        mbar_wait(bar, phase, aborted);
+        phase ^= 1;
+        // also orders the previous tile's shared-memory reads before this tile's packing
+        if (__syncthreads_or(aborted)) break;
+        bool big = false;
+        dw_pack_box<kSdCB>(raw, win, kSdWR * kSdWC, kSdCP, 23 - p.M - lo_shift, ((1u << p.M) - 1u) << lo_shift, tid,
+                           big);
+        if (tid < kSdCB * 9) {
+            const int c = tid / 9, tap = tid % 9;
+            const float v = tl.c0 + c < p.C ? __ldg(p.b + (long long)tap * p.C + tl.c0 + c) : 0.0f;
+            int wbig = 0;
+            const uint32_t pk = dw_pack(v, p.M, hi_shift, wbig);
+            big |= wbig != 0;
+            wt_off[tid] = pk - dw_scale_bits(pk);
+            wt_scl[tid] = __uint_as_float(dw_scale_bits(pk));
+        }
+        const bool slow = __syncthreads_or(big);   // the raw window is consumed
+        if (tid == 0 && t + (int)gridDim.x < total) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(tile_at(t + gridDim.x));
+        }
+        if (slow) {
+            dw_repack<kSdCB>(p.a, win, kSdCP, tl.n, p.IH, p.IW, p.C, tl.p0 / 2, tl.q0 / 2, tl.c0, kSdWR, kSdWC, p.M,
+                             lo_shift, tid);
+            __syncthreads();
+        }
+        float2 acc[2][kSdRows];
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci) {
+            const int c = warp + 8 * ci;
+            uint32_t woff[9];
+            float wsc[9];
+#pragma unroll
+            for (int k = 0; k < 9; ++k) {
+                woff[k] = wt_off[c * 9 + k];
+                wsc[k] = wt_scl[c * 9 + k];
+            }
+            const uint32_t *wr = win + c * kSdCP + lane;
+            if (slow) sd_channel<W, true>(acc[ci], wr, lut, woff, wsc, p.expand_mul);
+            else sd_channel<W, false>(acc[ci], wr, lut, woff, wsc, p.expand_mul);
+        }
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci) {
+            float *o = ot + (warp + 8 * ci) * kDwOP + 2 * lane;
+#pragma unroll
+            for (int i = 0; i < kSdRows; ++i) *reinterpret_cast<float2 *>(o + i * kSdCols) = acc[ci][i];
+        }
+        __syncthreads();
+        float *dst = p.out + (long long)tl.n * p.OH * p.OW * p.C;
+#pragma unroll 4
+        for (int e = tid; e < kSdRows * kSdCols * 4; e += kDwThreads) {
+            const int c4 = e & 3, pos = e >> 2;
+            const int i = pos / kSdCols, j = pos % kSdCols;
+            const int hh = tl.p0 + i, wq = tl.q0 + j, c = tl.c0 + 4 * c4;
+            if (hh < p.OH && wq < p.OW && c < p.C) {
+                const float *src = ot + 4 * c4 * kDwOP + pos;
+                const float4 v = make_float4(src[0], src[kDwOP], src[2 * kDwOP], src[3 * kDwOP]);
+                __stcs(reinterpret_cast<float4 *>(dst + ((long long)hh * p.OW + wq) * p.C + c), v);
+            }
+        }
+    }
+}
+
+int launch_s2d(int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
+{
+    auto kfn = width == 8 ? dw_s2d_kernel<8> : dw_s2d_kernel<16>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return amsim::cuda_status(e);
+    kfn<<<grid, kDwThreads, smem, st>>>(tp);
+    return amsim::cuda_status(cudaGetLastError());
+}
+
+size_t s2d_smem_bytes(int table_bytes) { return (size_t)sd_smem(table_bytes); }
+
 // Launch for a narrowed table of `width` bits (8 or 16); mode 0 or 2.
 int launch_s2(int mode, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
 {

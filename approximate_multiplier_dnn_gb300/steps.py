@@ -337,13 +337,19 @@ class DwConvStep:
         nw = g["R"] * g["S"] * g["C"] * g["D"]
         return 4 * (nx + ny + nw)
 
-    @property
-    def tiled(self) -> bool:
-        """Whether the geometry takes the tiled kernel (3x3, unit stride and
-        dilation, one filter per channel, channels a multiple of 4)."""
+    def kernel_name(self, p) -> str:
+        """The library kernel pass p takes for this geometry (for labelling
+        measurements; the library decides, see amsim_last_path)."""
         g = self.g
-        return (g["D"] == 1 and g["R"] == 3 and g["S"] == 3 and tuple(g["stride"]) == (1, 1)
-                and tuple(g["dil"]) == (1, 1) and g["C"] % 4 == 0)
+        base = (g["D"] == 1 and g["R"] == 3 and g["S"] == 3 and tuple(g["dil"]) == (1, 1) and g["C"] % 4 == 0)
+        if base and tuple(g["stride"]) == (1, 1):
+            return "dw_tile_kernel"
+        if base and tuple(g["stride"]) == (2, 2):
+            if p != 1:
+                return "dw_s2_kernel"
+            if tuple(g["pad"]) == (1, 1):
+                return "dw_s2d_kernel"
+        return "dw_direct_kernel"
 
     def outputs(self) -> list:
         return [t for t in (self.y, self.dx, self.dw) if t is not None]

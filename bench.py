@@ -484,7 +484,7 @@ def main():
                          "bound": "hbm" if nbytes / (hbm * 1e9) >= p[2] / (peak * 1e9) else "alu"}
         dom = max(per, key=lambda k: per[k]["ms"])
         d = per[dom]
-        kern = "dw_tile_kernel" if step.tiled else "dw_direct_kernel"
+        kern = step.kernel_name(step.passes[list(per).index(dom)])
         if d["bound"] == "hbm":
             roofline = {"bound": "hbm", "achieved": d["hbm_gbs"], "peak": hbm, "peak_source": src, "unit": "GB/s",
                         "frac": d["hbm_frac"], "lookup_frac": d["lookup_frac"]}

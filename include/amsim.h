@@ -385,8 +385,8 @@ int amsim_dwconv2d_fwd(const amsim_conv_desc *desc, const float *x, const float 
  *   p = (h + ph - r*dh)/sh, q = (w + pw - s*dw)/sw where integral and in range
  *   (zero operands elsewhere).
  * dy: N*P*Q*K, w: R*S*C*D, dx: N*H*W*C (written).  Kernel choice as for the
- * forward pass at stride 1 (dy and dx 16-byte aligned); strided layers take
- * the direct kernel.  Scratch is not used.
+ * forward pass (dy and dx 16-byte aligned), at stride 2 for padding 1 only.
+ * Scratch is not used.
  */
 int amsim_dwconv2d_bwd_data(const amsim_conv_desc *desc, const float *dy, const float *w, float *dx,
                             amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);

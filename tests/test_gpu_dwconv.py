@@ -36,13 +36,14 @@ DIRECT = [
     (1, 12, 40, 8, 4, 3, 3, (1, 1), (1, 1), (1, 1)),    # 3x3 unit stride with multiplier 4
 ]
 
-# 3x3 stride 2: the stride-2 tiled kernel for the forward pass and the weight
-# gradient, the direct kernel for the data gradient
+# 3x3 stride 2: the stride-2 tiled kernels (the data gradient's for padding 1
+# only; other paddings take the direct kernel for that pass)
 STRIDE2 = [
     (2, 16, 16, 32, 1, 3, 3, (2, 2), (1, 1), (1, 1)),   # the stride-2 MobileNet layer shape
     (1, 33, 130, 16, 1, 3, 3, (2, 2), (1, 1), (1, 1)),  # 17 x 65 outputs: ragged row and column tiles
     (2, 14, 14, 12, 1, 3, 3, (2, 2), (1, 1), (1, 1)),   # 12 channels: a half channel block
     (1, 17, 17, 8, 1, 3, 3, (2, 2), (0, 0), (1, 1)),    # no padding
+    (1, 18, 130, 20, 1, 3, 3, (2, 2), (1, 1), (1, 1)),  # even height, 130 columns, 20 channels
 ]
 
 PASSES = ("fwd", "bwd_data", "bwd_filter")
@@ -124,8 +125,12 @@ def test_dwconv_direct_kernel(amd, orc, luts, g, kind):
 def test_dwconv_stride2_kernel(amd, orc, luts, g, kind):
     rng = np.random.default_rng(5 + sum(g[:7]) + 7 * (kind == "exact"))
     x, w, dy = operands(orc, g, rng)
+    check_passes(amd, orc, luts(kind, 7), kind, 7, g, x, w, dy, stride2_paths(amd, g))
+
+
+def stride2_paths(amd, g):
     t, d = amd.AMSIM_PATH_DW_TILES, amd.AMSIM_PATH_DW_DIRECT
-    check_passes(amd, orc, luts(kind, 7), kind, 7, g, x, w, dy, (t, d, t))
+    return (t, t if g[8] == (1, 1) else d, t)
 
 
 @pytest.mark.parametrize("M,path", [(1, "tiles"), (4, "tiles"), (8, "direct"), (11, "direct")])
@@ -166,7 +171,7 @@ def test_dwconv_special_operands(amd, orc, luts, g):
         x[0, 3, -1, :] = np.inf
         x[0, 4, -2, 1] = -np.inf
     t, d = amd.AMSIM_PATH_DW_TILES, amd.AMSIM_PATH_DW_DIRECT
-    bit = t if g in TILED else (t, d, t) if g in STRIDE2 else d
+    bit = t if g in TILED else stride2_paths(amd, g) if g in STRIDE2 else d
     check_passes(amd, orc, luts("mitchell", 7), "mitchell", 7, g, x, w, dy, bit)
 
 
