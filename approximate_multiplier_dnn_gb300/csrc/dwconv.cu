@@ -267,13 +267,22 @@ __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ 
     }
 }
 
-// out[i] = sum over shares g = 0 .. G-1 of part[g*n + i], in share order.
+// out[i] = sum over shares g = 0 .. G-1 of part[g*n + i], in share order (the
+// loads of eight shares are issued together, the adds stay in order).
 __global__ void __launch_bounds__(256) dw_sum_kernel(const float *__restrict__ part, float *__restrict__ out,
                                                      long long n, int G)
 {
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
         float v = part[i];
-        for (int g = 1; g < G; ++g) v += part[(long long)g * n + i];
+        int g = 1;
+        for (; g + 8 <= G; g += 8) {
+            float t[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) t[u] = __ldg(part + (long long)(g + u) * n + i);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v += t[u];
+        }
+        for (; g < G; ++g) v += __ldg(part + (long long)g * n + i);
         out[i] = v;
     }
 }

@@ -248,6 +248,7 @@ def lut_residency(lut):
 # a record holds for one version of them
 KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_ws.cuh", "gemm_tma.cuh", "gemm_raw.cuh")
 DW_KERNEL_SOURCES = ("gemm_kernel.cuh", "dwconv_kernel.cuh")   # the tiled kernel's own sources
+DW_S2_KERNEL_SOURCES = ("gemm_kernel.cuh", "dwconv_kernel.cuh", "dwconv_s2.cu")
 
 
 def kernel_sha(sources=KERNEL_SOURCES):
@@ -492,7 +493,8 @@ def main():
             roofline = {"bound": "alu", "pipe": "shared-memory LUT lookups: SMs x 32 per clock x SM clock",
                         "achieved": d["glookups"], "peak": peak, "unit": "Glookup/s", "frac": d["lookup_frac"],
                         "hbm_frac": d["hbm_frac"]}
-        roofline.update({"traffic": recorded_traffic(f"{wname}:{dom}", DW_KERNEL_SOURCES),
+        srcs = DW_S2_KERNEL_SOURCES if args.workload == "dwconv3x3_s2" else DW_KERNEL_SOURCES
+        roofline.update({"traffic": recorded_traffic(f"{wname}:{dom}", srcs),
                          "kernel": f"{kern} ({dom} pass)", "passes": per, "sms": sms, "sm_mhz": mhz})
         if args.closed_form:
             roofline["products"] = "closed form in registers (no table lookups): lookup_frac is lookups avoided"
