@@ -11,10 +11,11 @@
 // Operand order (first operand = high LUT index bits): (x, w), (dy, w), (x, dy).
 //
 // An output sums only R*S (or R*S*D) products, so this is a stencil, not a
-// GEMM, and there is no contraction to tile for the tensor cores.  Two kernels:
-//  * dw_tile_kernel (3x3 filter, unit stride and dilation, D = 1, channels a
-//    multiple of 4): a CTA stages a halo tile of 16 channels of the activation
-//    (10 x 66 positions for an 8 x 64 output tile) in shared memory, each
+// GEMM, and there is no contraction to tile for the tensor cores.  Kernels:
+//  * dw_tile_kernel (dwconv_kernel.cuh; 3x3 filter, unit stride and dilation,
+//    D = 1, channels a multiple of 4): a CTA stages a halo tile of 16 channels
+//    of the activation (10 x 66 positions for an 8 x 64 output tile; narrower
+//    layers take taller tiles of the same 512 outputs) in shared memory, each
 //    element packed once into one word: sign and exponent bits (the signed
 //    power-of-two scale, NaN kept as NaN), the rest the LUT byte offset of its
 //    truncated mantissa.  In the forward and data-gradient passes a warp works
@@ -28,10 +29,13 @@
 //    accumulates the 9 taps per lane across all tiles of its share; its
 //    products have no uniform operand, so its lookups meet bank conflicts.
 //    Thread 0 copies the next tile's raw boxes with a tensor copy (zero fill
-//    outside the tensor) while the CTA computes the current tile.
-//  * dw_direct_kernel (every other geometry): one lane per output element,
-//    operands loaded and decoded per product, the LUT read through the
-//    read-only cache; the weight is still warp-uniform in the first two passes.
+//    outside the tensor) while the CTA computes the current tile.  Closed-form
+//    variants (dwconv_alu.cu) compute the built-in multipliers in registers.
+//  * dw_s2_kernel and dw_s2d_kernel (dwconv_s2.cu): the same scheme for 3x3
+//    filters at stride 2 (the data gradient for padding 1).
+//  * dw_direct_kernel (every other geometry): a warp takes one pixel and 32
+//    consecutive channels, operands read as coalesced rows and decoded per
+//    product, the LUT staged in shared memory when it fits.
 // The weight gradient's reduction over N*P*Q is split into G shares written to
 // scratch and added in share order by dw_sum_kernel, so results are
 // deterministic for a given scratch size.
