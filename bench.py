@@ -59,44 +59,53 @@ def env_int(name, default):
 
 
 # ---------------------------------------------------------------- workloads
+def workload_name(name, M=7, kind="mitchell"):
+    """The descriptive name both arms print as config.workload."""
+    names = {
+        "mlp": "mlp_784-1000-500-10_b256_fwd+dX+dW_mitchell_M7",
+        "mlp_layers": "mlp_784-1000-500-10_b256_autograd_AMDense_layers_mitchell_M7",
+        "conv3x3": "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_mitchell_M7",
+        "conv3x3_exact": "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_exact_M7",
+        "gemm4096": f"gemm_4096^3_{kind}_M{M}",
+        "attention": "attention_32x16x512x64_mitchell_M7",
+        "conv1x1": "conv1x1_nhwc_64x56x56x256_k256_fwd_mitchell_M7",
+        "dwconv3x3": "dwconv3x3_nhwc_64x56x56x128_d1_fwd+bwd_data+bwd_filter_mitchell_M7",
+        "dwconv3x3_s2": "dwconv3x3_stride2_nhwc_64x112x112x64_d1_fwd+bwd_data+bwd_filter_mitchell_M7",
+        "mul": "elementwise_2^28_pairs_special_mix_mitchell_M7",
+        "gemm64": "gemm_64x128x64_mitchell_M7",
+    }
+    if name not in names:
+        raise SystemExit(f"unknown workload {name}")
+    return names[name]
+
+
 def make_step(name, lut_for, M=7, kind="mitchell"):
     from approximate_multiplier_dnn_gb300 import steps
     from approximate_multiplier_dnn_gb300 import workloads as wl
+    wname = workload_name(name, M, kind)
     if name == "mlp":
-        return steps.MLPStep(wl.mlp(), lut_for("mitchell", 7)), "mlp_784-1000-500-10_b256_fwd+dX+dW_mitchell_M7"
+        return steps.MLPStep(wl.mlp(), lut_for("mitchell", 7)), wname
     if name == "mlp_layers":
-        return (steps.LayersMLPStep(wl.mlp(), lut_for("mitchell", 7)),
-                "mlp_784-1000-500-10_b256_autograd_AMDense_layers_mitchell_M7")
+        return steps.LayersMLPStep(wl.mlp(), lut_for("mitchell", 7)), wname
     if name == "conv3x3":
-        return (steps.ConvStep(wl.conv3x3(), wl.CONV3X3, lut_for("mitchell", 7)),
-                "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_mitchell_M7")
+        return steps.ConvStep(wl.conv3x3(), wl.CONV3X3, lut_for("mitchell", 7)), wname
     if name == "conv3x3_exact":
-        return (steps.ConvStep(wl.conv3x3(), wl.CONV3X3, lut_for("exact", 7)),
-                "conv3x3_nhwc_128x32x32x64_k64_fwd+bwd_data+bwd_filter_exact_M7")
+        return steps.ConvStep(wl.conv3x3(), wl.CONV3X3, lut_for("exact", 7)), wname
     if name == "gemm4096":
         # the mantissa-width sweep runs this workload at M = 4 .. 11
-        return steps.SquareGemmStep(wl.square_gemm(4096), lut_for(kind, M)), f"gemm_4096^3_{kind}_M{M}"
+        return steps.SquareGemmStep(wl.square_gemm(4096), lut_for(kind, M)), wname
     if name == "attention":
-        return steps.AttentionStep(wl.attention(), lut_for("mitchell", 7)), "attention_32x16x512x64_mitchell_M7"
+        return steps.AttentionStep(wl.attention(), lut_for("mitchell", 7)), wname
     if name == "conv1x1":
-        return (steps.ConvStep(wl.conv1x1(), wl.CONV1X1, lut_for("mitchell", 7), passes=(0,)),
-                "conv1x1_nhwc_64x56x56x256_k256_fwd_mitchell_M7")
+        return steps.ConvStep(wl.conv1x1(), wl.CONV1X1, lut_for("mitchell", 7), passes=(0,)), wname
     if name == "dwconv3x3":
-        return (steps.DwConvStep(wl.dwconv3x3(), wl.DWCONV3X3, lut_for("mitchell", 7)),
-                "dwconv3x3_nhwc_64x56x56x128_d1_fwd+bwd_data+bwd_filter_mitchell_M7")
+        return steps.DwConvStep(wl.dwconv3x3(), wl.DWCONV3X3, lut_for("mitchell", 7)), wname
     if name == "dwconv3x3_s2":
-        return (steps.DwConvStep(wl.dwconv3x3_s2(), wl.DWCONV3X3_S2, lut_for("mitchell", 7)),
-                "dwconv3x3_stride2_nhwc_64x112x112x64_d1_fwd+bwd_data+bwd_filter_mitchell_M7")
+        return steps.DwConvStep(wl.dwconv3x3_s2(), wl.DWCONV3X3_S2, lut_for("mitchell", 7)), wname
     if name == "mul":
-        from approximate_multiplier_dnn_gb300 import steps as st
-        return st.MulStep(wl.elementwise_pairs(1 << 28, seed=5), lut_for("mitchell", 7)), \
-            "elementwise_2^28_pairs_special_mix_mitchell_M7"
+        return steps.MulStep(wl.elementwise_pairs(1 << 28, seed=5), lut_for("mitchell", 7)), wname
     if name == "gemm64":
-        from approximate_multiplier_dnn_gb300 import steps as st
-        import torch
-        d = wl.gemm_small()
-        s = st.SquareGemmStep(d, lut_for("mitchell", 7))
-        return s, "gemm_64x128x64_mitchell_M7"
+        return steps.SquareGemmStep(wl.gemm_small(), lut_for("mitchell", 7)), wname
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -315,7 +324,8 @@ def reference_arm(args, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate",
         "data": "synthetic",
-        "config": {"workload": args.workload, "sample": f"{cores} rows of each contraction per step"},
+        "config": {"workload": workload_name(args.workload, args.mantissa, args.kind),
+                   "sample": f"{cores} rows of each contraction per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{cores} output rows of each contraction per step, {args.steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
