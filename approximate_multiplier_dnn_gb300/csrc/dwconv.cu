@@ -303,13 +303,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 constexpr int kDwMaxTileLut = 64 * 1024;   // tables staged by the tiled kernel
 
-// The tiled kernel covers 3x3 filters at unit stride and dilation with one
-// filter per channel, channels a multiple of 4, 16-byte aligned tensors and a
-// narrowed 8- or 16-bit LUT of at most 64 KB.
+// The tiled kernel covers 3x3 and 5x5 filters at unit stride and dilation
+// with one filter per channel, channels a multiple of 4, 16-byte aligned
+// tensors and a narrowed 8- or 16-bit LUT of at most 64 KB.
 bool dw_tile_ok(const DwGeo &g, const amsim_lut_t lut, int which, const float *t0, const float *t1,
                 const float *out)
 {
-    if (g.D != 1 || g.R != 3 || g.S != 3 || g.sh != 1 || g.sw != 1 || g.dh != 1 || g.dw != 1) return false;
+    if (g.D != 1 || g.R != g.S || (g.R != 3 && g.R != 5) || g.sh != 1 || g.sw != 1 || g.dh != 1 || g.dw != 1)
+        return false;
     if (g.C % 4 || lut->width_bits == 32 || (int)lut->narrow_bytes > kDwMaxTileLut) return false;
     if (!aligned16(t0) || !aligned16(out)) return false;
     if (which == 2 && !aligned16(t1)) return false;
@@ -338,7 +339,8 @@ bool dw_map(CUtensorMap *map, const float *base, int N, int H, int W, int C, int
     return amsim::encode_tensor_map(map, m) == AMSIM_OK;
 }
 
-// The closed-form variants are compiled in dwconv_alu.cu, the stride-2 kernel in dwconv_s2.cu.
+// The closed-form variants are compiled in dwconv_alu.cu, the 5x5 variants in
+// dwconv_k5.cu, the stride-2 kernels in dwconv_s2.cu.
 }  // namespace
 namespace amsim {
 namespace dw {
@@ -352,13 +354,17 @@ extern template int launch_tile<2, 1>(int, const DwTileParams &, int, size_t, cu
 extern template int launch_tile<0, 2>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<1, 2>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<2, 2>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<0, 0, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<1, 0, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<2, 0, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
 }  // namespace dw
 }  // namespace amsim
 namespace {
 
 template <int MODE>
-int launch_tile_any(int alu, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
+int launch_tile_any(int alu, int ks, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
 {
+    if (ks == 5) return launch_tile<MODE, 0, 5>(width, tp, grid, smem, st);
     if (alu == 1) return launch_tile<MODE, 1>(width, tp, grid, smem, st);
     if (alu == 2) return launch_tile<MODE, 2>(width, tp, grid, smem, st);
     return launch_tile<MODE, 0>(width, tp, grid, smem, st);
@@ -419,20 +425,21 @@ struct DwFilterPlan {
 
 // Resident CTAs of the tiled kernel per SM, from its shared memory (each
 // CTA also holds 1 KB of the SM's 228 KB for the system).
-// Closed-form variant of the tiled kernel a handle selects: 0 the table, 1
-// Mitchell, 2 exact (amsim_lut_set_closed_form on a built-in kind).
-int dw_alu(const amsim_lut_t lut)
+// Closed-form variant of the tiled kernel a handle selects for a ks x ks
+// filter: 0 the table, 1 Mitchell, 2 exact (amsim_lut_set_closed_form on a
+// built-in kind; closed forms are built for 3x3 filters, 5x5 take the table).
+int dw_alu(const amsim_lut_t lut, int ks)
 {
-    if (!lut->closed_form) return 0;
+    if (!lut->closed_form || ks != 3) return 0;
     return lut->kind == AMSIM_MITCHELL ? 1 : 2;
 }
 
 // Bytes of the LUT the tiled kernel stages (closed forms stage none).
-int dw_staged_lut(const amsim_lut_t lut) { return dw_alu(lut) ? 0 : (int)lut->narrow_bytes; }
+int dw_staged_lut(const amsim_lut_t lut, int ks) { return dw_alu(lut, ks) ? 0 : (int)lut->narrow_bytes; }
 
-int dw_tile_ctas_per_sm(const amsim_lut_t lut, int which)
+int dw_tile_ctas_per_sm(const amsim_lut_t lut, int which, int ks)
 {
-    const int per = dw_tile_smem(dw_staged_lut(lut), which) + 1024;
+    const int per = dw_tile_smem(dw_staged_lut(lut, ks), which, ks) + 1024;
     return std::max(1, std::min(2, (228 * 1024) / per));
 }
 
@@ -444,16 +451,16 @@ struct DwShape {
     int lq_shift, tp, tq, th, tw;
 };
 
-DwShape dw_shape(int OH, int OW)
+DwShape dw_shape(int OH, int OW, int ks)
 {
     DwShape best{};
     long long best_cost = -1, best_halo = 0;
     for (int ls = 5; ls >= 2; --ls) {
         const int tq = 2 << ls, tp = kDwRB * (32 >> ls);
         const long long cost = (long long)((OH + tp - 1) / tp) * tp * ((OW + tq - 1) / tq) * tq;
-        const long long halo = (long long)(tp + 2) * (tq + 2);
+        const long long halo = (long long)(tp + ks - 1) * (tq + ks - 1);
         if (best_cost < 0 || cost < best_cost || (cost == best_cost && halo < best_halo)) {
-            best = DwShape{ls, tp, tq, tp + 2, tq + 2};
+            best = DwShape{ls, tp, tq, tp + ks - 1, tq + ks - 1};
             best_cost = cost;
             best_halo = halo;
         }
@@ -475,12 +482,12 @@ DwFilterPlan filter_plan(const DwGeo &g, int kind, int sms, const amsim_lut_t lu
         const int slots = s2_ctas_per_sm(lut, 2) * sms;
         f.G_want = std::max(1, std::min((slots + f.cblocks - 1) / f.cblocks, f.tiles));
     } else if (kind == 1) {
-        const DwShape sh = dw_shape(g.P, g.Q);
+        const DwShape sh = dw_shape(g.P, g.Q, g.R);
         f.tiles_p = (g.P + sh.tp - 1) / sh.tp;
         f.tiles_q = (g.Q + sh.tq - 1) / sh.tq;
-        f.cblocks = (g.C + dw_channel_block(2) - 1) / dw_channel_block(2);
+        f.cblocks = (g.C + dw_channel_block(2, g.R) - 1) / dw_channel_block(2, g.R);
         f.tiles = g.N * f.tiles_p * f.tiles_q;
-        const int slots = dw_tile_ctas_per_sm(lut, 2) * sms;
+        const int slots = dw_tile_ctas_per_sm(lut, 2, g.R) * sms;
         const int want = (slots + f.cblocks - 1) / f.cblocks;
         f.G_want = std::max(1, std::min(want, f.tiles));
     } else {
@@ -614,35 +621,37 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         tp.a = t0;
         tp.expand_mul = 1u << (24 - width);
         // output grid: y (forward), dx (data gradient), dy (weight gradient)
-        const DwShape sh = which == 1 ? dw_shape(g.H, g.W) : dw_shape(g.P, g.Q);
+        const int ks = g.R;
+        const int cbk = dw_channel_block(which, ks);
+        const DwShape sh = which == 1 ? dw_shape(g.H, g.W, ks) : dw_shape(g.P, g.Q, ks);
         tp.lq_shift = sh.lq_shift;
         tp.tp = sh.tp;
         tp.tq = sh.tq;
         tp.tq_shift = sh.lq_shift + 1;
         tp.th = sh.th;
         tp.tw = sh.tw;
-        tp.raw_a_bytes = sh.th * sh.tw * dw_channel_block(which) * 4;
+        tp.raw_a_bytes = sh.th * sh.tw * cbk * 4;
         bool mapped;
         if (which == 0) {
             tp.IH = g.H; tp.IW = g.W;
             tp.b = t1; tp.out = out;
             tp.OH = g.P; tp.OW = g.Q;
             tp.oy = -g.ph; tp.ox = -g.pw;
-            mapped = dw_map(&tp.amap, t0, g.N, g.H, g.W, g.C, dw_channel_block(0), sh.tw, sh.th);
+            mapped = dw_map(&tp.amap, t0, g.N, g.H, g.W, g.C, cbk, sh.tw, sh.th);
         } else if (which == 1) {
-            // dx[h][w] = sum_{r',s'} dy[h + ph - 2 + r'][w + pw - 2 + s'] * w[2 - r'][2 - s']
+            // dx[h][w] = sum_{r',s'} dy[h + ph - (ks-1) + r'][w + pw - (ks-1) + s'] * w[ks-1 - r'][ks-1 - s']
             tp.IH = g.P; tp.IW = g.Q;
             tp.b = t1; tp.out = out;
             tp.OH = g.H; tp.OW = g.W;
-            tp.oy = g.ph - 2; tp.ox = g.pw - 2;
-            mapped = dw_map(&tp.amap, t0, g.N, g.P, g.Q, g.C, dw_channel_block(1), sh.tw, sh.th);
+            tp.oy = g.ph - (ks - 1); tp.ox = g.pw - (ks - 1);
+            mapped = dw_map(&tp.amap, t0, g.N, g.P, g.Q, g.C, cbk, sh.tw, sh.th);
         } else {
             tp.IH = g.H; tp.IW = g.W;
             tp.b = t1;
             tp.OH = g.P; tp.OW = g.Q;
             tp.oy = -g.ph; tp.ox = -g.pw;
-            mapped = dw_map(&tp.amap, t0, g.N, g.H, g.W, g.C, dw_channel_block(2), sh.tw, sh.th) &&
-                     dw_map(&tp.bmap, t1, g.N, g.P, g.Q, g.C, dw_channel_block(2), sh.tq, sh.tp);
+            mapped = dw_map(&tp.amap, t0, g.N, g.H, g.W, g.C, cbk, sh.tw, sh.th) &&
+                     dw_map(&tp.bmap, t1, g.N, g.P, g.Q, g.C, cbk, sh.tq, sh.tp);
         }
         if (!mapped) {               // the driver refused a tensor map: the direct kernel
             tiled = false;
@@ -652,25 +661,25 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
     if (tiled) {
         tp.tiles_p = (tp.OH + tp.tp - 1) / tp.tp;
         tp.tiles_q = (tp.OW + tp.tq - 1) / tp.tq;
-        tp.cblocks = (g.C + dw_channel_block(which) - 1) / dw_channel_block(which);
+        tp.cblocks = (g.C + dw_channel_block(which, g.R) - 1) / dw_channel_block(which, g.R);
         tp.tiles = g.N * tp.tiles_p * tp.tiles_q;
-        const size_t smem = (size_t)dw_tile_smem(dw_staged_lut(lut), which);
-        const int alu = dw_alu(lut);
+        const size_t smem = (size_t)dw_tile_smem(dw_staged_lut(lut, g.R), which, g.R);
+        const int alu = dw_alu(lut, g.R);
         if (alu) path |= AMSIM_PATH_CLOSED_FORM;
         if (which < 2) {
             const long long total = (long long)tp.tiles * tp.cblocks;
             if (total > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
-            const int grid = (int)std::min<long long>(total, (long long)dw_tile_ctas_per_sm(lut, which) * sms);
+            const int grid = (int)std::min<long long>(total, (long long)dw_tile_ctas_per_sm(lut, which, g.R) * sms);
             tp.G = 1;
-            rc = which == 0 ? launch_tile_any<0>(alu, width, tp, grid, smem, st)
-                            : launch_tile_any<1>(alu, width, tp, grid, smem, st);
+            rc = which == 0 ? launch_tile_any<0>(alu, g.R, width, tp, grid, smem, st)
+                            : launch_tile_any<1>(alu, g.R, width, tp, grid, smem, st);
             if (rc == AMSIM_OK) amsim::count_launch();
         } else {
             const DwFilterPlan f = filter_plan(g, 1, sms, lut);
             tp.G = shares_for(f, ws_bytes);
             tp.out = tp.G > 1 ? static_cast<float *>(ws) : out;
             const int grid = tp.cblocks * tp.G;
-            rc = launch_tile_any<2>(alu, width, tp, grid, smem, st);
+            rc = launch_tile_any<2>(alu, g.R, width, tp, grid, smem, st);
             if (rc == AMSIM_OK) amsim::count_launch();
             if (rc == AMSIM_OK && tp.G > 1) {
                 const int blocks = (int)std::min<long long>((n_out + 255) / 256, 4LL * sms);

@@ -69,30 +69,35 @@ constexpr int kDwThreads = 256;       // 8 warps
 // Tile shapes: a lane owns 2 adjacent output columns of an 8-row block; a
 // warp's 32 lanes are LQ = 32, 16, 8 or 4 lanes across by 32 / LQ row blocks,
 // so a tile is (256 / LQ) rows x 2 LQ columns = 512 outputs per channel and
-// its halo (rows + 2) x (columns + 2) is at most 660 positions.  The host
-// picks LQ per launch to waste the fewest computed outputs past the edges.
+// its halo, for a KS x KS filter (KS = 3 or 5), (rows + KS - 1) x (columns +
+// KS - 1), is at most 660 (KS = 3) or 816 (KS = 5) positions.  The host picks
+// LQ per launch to waste the fewest computed outputs past the edges.
 constexpr int kDwRB = 8;              // output rows per lane
 constexpr int kDwTileOut = 512;       // outputs per tile and channel
-constexpr int kDwHaloMax = 660;       // halo positions of the widest and tallest shapes
-constexpr int kDwCP = 666;            // packed halo words per channel: >= 660, = 2 mod 8 (conflict-free packing)
 constexpr int kDwOP = 514;            // packed output-gradient / output-tile words per channel: >= 512, = 2 mod 8
-static_assert(kDwHaloMax <= kDwCP && kDwTileOut <= kDwOP, "tile pitches");
-static_assert(kDwCP % 2 == 0 && kDwOP % 2 == 0, "8-byte aligned lane pairs");
+__host__ __device__ constexpr int dw_halo_max(int ks) { return ks == 3 ? 660 : 816; }
+// packed halo words per channel: >= the halo, = 2 mod 8 (conflict-free packing)
+__host__ __device__ constexpr int dw_cp(int ks) { return ks == 3 ? 666 : 818; }
+static_assert(dw_halo_max(3) <= dw_cp(3) && dw_halo_max(5) <= dw_cp(5) && kDwTileOut <= kDwOP, "tile pitches");
+static_assert(dw_cp(3) % 8 == 2 && dw_cp(5) % 8 == 2 && kDwOP % 2 == 0, "pitches");
 
 __host__ __device__ constexpr int dw_lut_region(int table_bytes) { return (table_bytes + 127) & ~127; }
 
 // Channels per tile: 16 (two per warp) in the forward and data-gradient
-// passes; 8 (one per warp) in the weight gradient, whose two raw boxes and two
-// packed tiles would otherwise leave room for one CTA per SM.
-template <int MODE>
+// passes of 3x3 filters; 8 (one per warp) in the weight gradient, whose two
+// raw boxes and two packed tiles would otherwise leave room for one CTA per
+// SM, and for 5x5 filters, whose halos are larger.
+template <int MODE, int KS = 3>
 struct DwCfg {
-    static constexpr int CB = MODE == 2 ? 8 : 16;
+    static constexpr int CB = (MODE == 2 || KS == 5) ? 8 : 16;
     static constexpr int CPW = CB / 8;                        // channels per warp
-    static constexpr int RawA = kDwHaloMax * CB * 4;          // raw halo box as the tensor copy lands: [row][col][c]
+    static constexpr int KK = KS * KS;                        // filter taps
+    static constexpr int CP = dw_cp(KS);
+    static constexpr int RawA = (dw_halo_max(KS) * CB * 4 + 127) & ~127;   // raw halo box as it lands: [row][col][c]
     static constexpr int RawB = kDwTileOut * CB * 4;          // raw output-gradient box (weight gradient)
-    static constexpr int Halo = (CB * kDwCP * 4 + 127) & ~127;   // packed halo [c][pos]
+    static constexpr int Halo = (CB * CP * 4 + 127) & ~127;   // packed halo [c][pos]
     static constexpr int Out = (CB * kDwOP * 4 + 127) & ~127;    // packed dy (weight gradient) / output tile
-    static constexpr int WB = (3 * CB * 9 * 4 + 127) & ~127;     // filter taps: offsets, scales, closed forms
+    static constexpr int WB = (3 * CB * KK * 4 + 127) & ~127;    // filter taps: offsets, scales, closed forms
     static constexpr int Tail = MODE == 2 ? RawB + Out : WB;
     static_assert(Out <= Halo, "the output tile reuses the halo region");
     static_assert(RawA % 128 == 0 && RawB % 128 == 0 && Halo % 128 == 0 && Out % 128 == 0 && WB % 128 == 0,
@@ -101,22 +106,27 @@ struct DwCfg {
 
 // Shared memory of the tiled kernel: LUT, raw box(es), packed tiles, weights
 // (forward / data gradient), one mbarrier.
-__host__ __device__ constexpr int dw_tile_smem(int table_bytes, int mode)
+__host__ __device__ constexpr int dw_tile_smem(int table_bytes, int mode, int ks = 3)
 {
     // table_bytes: the staged LUT (0 for closed forms, which read it only in slow tiles)
     return dw_lut_region(table_bytes) +
-           (mode == 2 ? DwCfg<2>::RawA + DwCfg<2>::Halo + DwCfg<2>::Tail
-                      : DwCfg<0>::RawA + DwCfg<0>::Halo + DwCfg<0>::Tail) + 128;
+           (ks == 5 ? (mode == 2 ? DwCfg<2, 5>::RawA + DwCfg<2, 5>::Halo + DwCfg<2, 5>::Tail
+                                 : DwCfg<0, 5>::RawA + DwCfg<0, 5>::Halo + DwCfg<0, 5>::Tail)
+                    : (mode == 2 ? DwCfg<2>::RawA + DwCfg<2>::Halo + DwCfg<2>::Tail
+                                 : DwCfg<0>::RawA + DwCfg<0>::Halo + DwCfg<0>::Tail)) + 128;
 }
 
-__host__ __device__ constexpr int dw_channel_block(int mode) { return mode == 2 ? DwCfg<2>::CB : DwCfg<0>::CB; }
+__host__ __device__ constexpr int dw_channel_block(int mode, int ks = 3)
+{
+    return ks == 5 ? 8 : mode == 2 ? DwCfg<2>::CB : DwCfg<0>::CB;
+}
 
 struct DwTileParams {
     CUtensorMap amap;      // activation: dims (C, IW, IH, N), box (CB, tw, th, 1)
     CUtensorMap bmap;      // weight gradient's dy: dims (C, OW, OH, N), box (CB, tq, tp, 1)
     const float *a;        // activation (for re-packing a tile with special values)
     const float *b;        // w [3][3][C] (modes 0, 1), dy (mode 2)
-    float *out;            // y / dx (NHWC), or the weight gradient's shares [G][9][C]
+    float *out;            // y / dx (NHWC), or the weight gradient's shares [G][R*S][C]
     uint32_t expand_mul;   // 2^(24 - entry width)
     int IH, IW;            // activation height and width
     const void *table;     // narrowed LUT: [w][activation] (modes 0, 1), [x][dy] (mode 2)
@@ -197,31 +207,44 @@ __device__ __forceinline__ void dw_issue(const DwTileParams &p, const DwTile &t,
 
 // Forward / data-gradient compute of one channel for one lane: acc[i] holds
 // output row i at tile columns 2*lane (.x) and 2*lane + 1 (.y).
-template <int W, bool SLOW, bool GL = false>
+// Load the lane's KS + 1 packed words of one halo row (two output columns
+// and the KS - 1 columns past them) as 8-byte pairs.
+template <int KS>
+__device__ __forceinline__ void dw_row(const uint32_t *p, uint32_t (&px)[KS + 1])
+{
+#pragma unroll
+    for (int k = 0; k < (KS + 1) / 2; ++k) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p + 2 * k);
+        px[2 * k] = v.x;
+        px[2 * k + 1] = v.y;
+    }
+}
+
+template <int W, bool SLOW, bool GL = false, int KS = 3>
 __device__ __forceinline__ void dw_taps_channel(float2 (&acc)[kDwRB], const uint32_t *xr, int tw, const uint8_t *lut,
-                                                const uint32_t (&woff)[9], const float (&wsc)[9], uint32_t mul)
+                                                const uint32_t (&woff)[KS * KS], const float (&wsc)[KS * KS],
+                                                uint32_t mul)
 {
 #pragma unroll
     for (int i = 0; i < kDwRB; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int hh = 0; hh < kDwRB + 2; ++hh) {
-        const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + hh * tw);
-        const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + hh * tw + 2);
-        const uint32_t px[4] = {a01.x, a01.y, a23.x, a23.y};
-        uint32_t sb[4];
-        float sx[4];
+    for (int hh = 0; hh < kDwRB + KS - 1; ++hh) {
+        uint32_t px[KS + 1];
+        dw_row<KS>(xr + hh * tw, px);
+        uint32_t sb[KS + 1];
+        float sx[KS + 1];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < KS + 1; ++k) {
             sb[k] = dw_scale_bits(px[k]);
             sx[k] = __uint_as_float(sb[k]);
         }
 #pragma unroll
-        for (int r = 0; r < 3; ++r) {
+        for (int r = 0; r < KS; ++r) {
             const int i = hh - r;
             if (i < 0 || i >= kDwRB) continue;
 #pragma unroll
-            for (int s = 0; s < 3; ++s) {
-                const int t = r * 3 + s;
+            for (int s = 0; s < KS; ++s) {
+                const int t = r * KS + s;
                 const uint32_t i0 = px[s] - sb[s] + woff[t];
                 const uint32_t i1 = px[s + 1] - sb[s + 1] + woff[t];
                 const float2 v = make_float2(dw_expand(lut_ld<W, GL>(lut, i0), mul),
@@ -244,10 +267,10 @@ __device__ __forceinline__ void dw_taps_channel(float2 (&acc)[kDwRB], const uint
 // and 2*lane + 1 (.y).  In the slow form, positions outside the output
 // gradient (past P or Q) are skipped, so an infinite activation there cannot
 // meet a zero-filled gradient.
-template <int W, bool SLOW, bool GL = false>
-__device__ __forceinline__ void dw_filter_channel(float2 (&acc)[9], const uint32_t *xr, int tw, const uint32_t *dr,
-                                                  int tq, const uint8_t *lut, int rows_ok, bool ok0, bool ok1,
-                                                  uint32_t mul)
+template <int W, bool SLOW, bool GL = false, int KS = 3>
+__device__ __forceinline__ void dw_filter_channel(float2 (&acc)[KS * KS], const uint32_t *xr, int tw,
+                                                  const uint32_t *dr, int tq, const uint8_t *lut, int rows_ok,
+                                                  bool ok0, bool ok1, uint32_t mul)
 {
 #pragma unroll
     for (int i = 0; i < kDwRB; ++i) {
@@ -257,20 +280,19 @@ __device__ __forceinline__ void dw_filter_channel(float2 (&acc)[9], const uint32
         const float2 sd = make_float2(__uint_as_float(db0), __uint_as_float(db1));
         const bool row_ok = i < rows_ok;
 #pragma unroll
-        for (int r = 0; r < 3; ++r) {
-            const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + (i + r) * tw);
-            const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + (i + r) * tw + 2);
-            const uint32_t px[4] = {a01.x, a01.y, a23.x, a23.y};
-            uint32_t sb[4];
-            float sx[4];
+        for (int r = 0; r < KS; ++r) {
+            uint32_t px[KS + 1];
+            dw_row<KS>(xr + (i + r) * tw, px);
+            uint32_t sb[KS + 1];
+            float sx[KS + 1];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < KS + 1; ++k) {
                 sb[k] = dw_scale_bits(px[k]);
                 sx[k] = __uint_as_float(sb[k]);
             }
 #pragma unroll
-            for (int s = 0; s < 3; ++s) {
-                const int t = r * 3 + s;
+            for (int s = 0; s < KS; ++s) {
+                const int t = r * KS + s;
                 const uint32_t i0 = px[s] - sb[s] + od0;
                 const uint32_t i1 = px[s + 1] - sb[s + 1] + od1;
                 const float2 v = make_float2(dw_expand(lut_ld<W, GL>(lut, i0), mul),
@@ -403,18 +425,20 @@ __device__ __forceinline__ void dw_filter_alu(float2 (&acc)[9], const uint32_t *
 // Thread 0 copies the next tile's raw boxes while the CTA computes the
 // current one; every wait on the copy is bounded (a timeout is recorded and
 // the CTA leaves its remaining tiles).
-template <int W, int MODE, int ALU, bool WIDE>
+template <int W, int MODE, int ALU, bool WIDE, int KS = 3>
 __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_constant__ DwTileParams p)
 {
     using amsim::kern::mbar_init;
     using amsim::kern::mbar_wait;
     extern __shared__ __align__(128) uint8_t smem[];
-    using Cfg = DwCfg<MODE>;
-    constexpr int CB = Cfg::CB, CPW = Cfg::CPW;
+    using Cfg = DwCfg<MODE, KS>;
+    constexpr int CB = Cfg::CB, CPW = Cfg::CPW, KK = Cfg::KK, CP = Cfg::CP;
+    static_assert(KS == 3 || ALU == 0, "closed forms are built for 3x3 filters");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // tile shape: compile-time for the widest (8 x 64) tiles, else from the launch
     const int lq_shift = WIDE ? 5 : p.lq_shift, tq_shift = WIDE ? 6 : p.tq_shift;
-    const int tq = WIDE ? 64 : p.tq, tw = WIDE ? 66 : p.tw, th = WIDE ? 10 : p.th, tpr = WIDE ? 8 : p.tp;
+    const int tq = WIDE ? 64 : p.tq, tw = WIDE ? 64 + KS - 1 : p.tw, th = WIDE ? 8 + KS - 1 : p.th;
+    const int tpr = WIDE ? 8 : p.tp;
     uint8_t *lut = smem;
     const uint8_t *glut = static_cast<const uint8_t *>(p.table);         // slow closed-form tiles
     float *rawA = reinterpret_cast<float *>(smem + (ALU ? 0 : dw_lut_region(p.table_bytes)));
@@ -423,8 +447,8 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
     float *rawB = reinterpret_cast<float *>(after);                       // mode 2
     uint32_t *dyt = reinterpret_cast<uint32_t *>(after + Cfg::RawB);      // mode 2
     uint32_t *wt_off = reinterpret_cast<uint32_t *>(after);               // modes 0, 1
-    float *wt_scl = reinterpret_cast<float *>(after + CB * 9 * 4);
-    uint32_t *wt_val = reinterpret_cast<uint32_t *>(after + 2 * CB * 9 * 4);   // closed forms
+    float *wt_scl = reinterpret_cast<float *>(after + CB * KK * 4);
+    uint32_t *wt_val = reinterpret_cast<uint32_t *>(after + 2 * CB * KK * 4);   // closed forms
     uint64_t *bar = reinterpret_cast<uint64_t *>(after + Cfg::Tail);
 
     // this CTA's tiles: [t_begin, t_end) step t_step of the launch's tile list
@@ -472,12 +496,12 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
     __syncthreads();
     const int hi_shift = p.M + p.wlog, lo_shift = p.wlog;
 
-    float2 facc[CPW][9];                    // mode 2: per-tap sums of this CTA's share
+    float2 facc[CPW][MODE == 2 ? KK : 1];   // mode 2: per-tap sums of this CTA's share
     if constexpr (MODE == 2) {
 #pragma unroll
         for (int ci = 0; ci < CPW; ++ci)
 #pragma unroll
-            for (int t = 0; t < 9; ++t) facc[ci][t] = make_float2(0.0f, 0.0f);
+            for (int t = 0; t < KK; ++t) facc[ci][t] = make_float2(0.0f, 0.0f);
     }
     uint32_t phase = 0;
     bool aborted = false;
@@ -491,18 +515,18 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
         const int a_shift = MODE == 2 ? hi_shift : lo_shift;
         const uint32_t keep = ((1u << p.M) - 1u) << (23 - p.M);
         if constexpr (ALU != 0) {
-            dw_pack_box_alu<CB>(rawA, xt, th * tw, kDwCP, keep, tid, big);
+            dw_pack_box_alu<CB>(rawA, xt, th * tw, CP, keep, tid, big);
             if constexpr (MODE == 2) dw_pack_box_alu<CB>(rawB, dyt, kDwTileOut, kDwOP, keep, tid, big);
         } else {
-            dw_pack_box<CB>(rawA, xt, th * tw, kDwCP, 23 - p.M - a_shift, ((1u << p.M) - 1u) << a_shift, tid,
+            dw_pack_box<CB>(rawA, xt, th * tw, CP, 23 - p.M - a_shift, ((1u << p.M) - 1u) << a_shift, tid,
                             big);
             if constexpr (MODE == 2)
                 dw_pack_box<CB>(rawB, dyt, kDwTileOut, kDwOP, 23 - p.M - lo_shift, ((1u << p.M) - 1u) << lo_shift,
                                 tid, big);
         }
-        if (MODE != 2 && tid < CB * 9) {
-            const int c = tid / 9, tap = tid % 9;
-            const int src_t = MODE == 0 ? tap : 8 - tap;   // the data gradient reads the filter rotated by 180 degrees
+        if (MODE != 2 && tid < CB * KK) {
+            const int c = tid / KK, tap = tid % KK;
+            const int src_t = MODE == 0 ? tap : KK - 1 - tap;   // the data gradient reads the filter rotated by 180 degrees
             const float v = tl.c0 + c < p.C ? __ldg(p.b + (long long)src_t * p.C + tl.c0 + c) : 0.0f;
             int wbig = 0;
             const uint32_t pk = dw_pack(v, p.M, hi_shift, wbig);
@@ -520,7 +544,7 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
             // a tile with |x| >= 2^64, infinities or NaN (closed forms: also
             // nonzero |x| < 2^-63): pack it again exactly for the table (NaN
             // kept as NaN) from global memory, then take the slow products
-            dw_repack<CB>(p.a, xt, kDwCP, tl.n, p.IH, p.IW, p.C, tl.p0 + p.oy, tl.q0 + p.ox, tl.c0, th, tw, p.M,
+            dw_repack<CB>(p.a, xt, CP, tl.n, p.IH, p.IW, p.C, tl.p0 + p.oy, tl.q0 + p.ox, tl.c0, th, tw, p.M,
                       a_shift, tid);
             if constexpr (MODE == 2)
                 dw_repack<CB>(p.b, dyt, kDwOP, tl.n, p.OH, p.OW, p.C, tl.p0, tl.q0, tl.c0, tpr, tq, p.M, lo_shift,
@@ -536,18 +560,21 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
 #pragma unroll
             for (int ci = 0; ci < CPW; ++ci) {
                 const int c = warp + 8 * ci;
-                const uint32_t *xr = xt + c * kDwCP + rb * kDwRB * tw + 2 * lc;
+                const uint32_t *xr = xt + c * CP + rb * kDwRB * tw + 2 * lc;
                 const uint32_t *dr = dyt + c * kDwOP + rb * kDwRB * tq + 2 * lc;
-                if (slow) {
-                    if constexpr (ALU != 0)
+                if constexpr (ALU != 0) {
+                    if (slow)
                         dw_filter_channel<W, true, true>(facc[ci], xr, tw, dr, tq, glut, rows_ok, ok0, ok1,
                                                          p.expand_mul);
                     else
-                        dw_filter_channel<W, true>(facc[ci], xr, tw, dr, tq, lut, rows_ok, ok0, ok1, p.expand_mul);
-                } else if constexpr (ALU != 0) {
-                    dw_filter_alu<ALU>(facc[ci], xr, tw, dr, tq);
+                        dw_filter_alu<ALU>(facc[ci], xr, tw, dr, tq);
                 } else {
-                    dw_filter_channel<W, false>(facc[ci], xr, tw, dr, tq, lut, rows_ok, ok0, ok1, p.expand_mul);
+                    if (slow)
+                        dw_filter_channel<W, true, false, KS>(facc[ci], xr, tw, dr, tq, lut, rows_ok, ok0, ok1,
+                                                              p.expand_mul);
+                    else
+                        dw_filter_channel<W, false, false, KS>(facc[ci], xr, tw, dr, tq, lut, rows_ok, ok0, ok1,
+                                                               p.expand_mul);
                 }
             }
         } else {
@@ -555,26 +582,28 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
 #pragma unroll
             for (int ci = 0; ci < CPW; ++ci) {
                 const int c = warp + 8 * ci;
-                uint32_t woff[9];
-                float wsc[9];
+                uint32_t woff[KK];
+                float wsc[KK];
 #pragma unroll
-                for (int k = 0; k < 9; ++k) {
-                    woff[k] = wt_off[c * 9 + k];
-                    wsc[k] = wt_scl[c * 9 + k];
+                for (int k = 0; k < KK; ++k) {
+                    woff[k] = wt_off[c * KK + k];
+                    wsc[k] = wt_scl[c * KK + k];
                 }
-                const uint32_t *xr = xt + c * kDwCP + rb * kDwRB * tw + 2 * lc;
-                if (slow) {
-                    if constexpr (ALU != 0)
+                const uint32_t *xr = xt + c * CP + rb * kDwRB * tw + 2 * lc;
+                if constexpr (ALU != 0) {
+                    if (slow) {
                         dw_taps_channel<W, true, true>(acc[ci], xr, tw, glut, woff, wsc, p.expand_mul);
-                    else
-                        dw_taps_channel<W, true>(acc[ci], xr, tw, lut, woff, wsc, p.expand_mul);
-                } else if constexpr (ALU != 0) {
-                    uint32_t wv[9];
+                    } else {
+                        uint32_t wv[9];
 #pragma unroll
-                    for (int k = 0; k < 9; ++k) wv[k] = wt_val[c * 9 + k];
-                    dw_taps_alu<ALU>(acc[ci], xr, tw, wv);
+                        for (int k = 0; k < 9; ++k) wv[k] = wt_val[c * 9 + k];
+                        dw_taps_alu<ALU>(acc[ci], xr, tw, wv);
+                    }
                 } else {
-                    dw_taps_channel<W, false>(acc[ci], xr, tw, lut, woff, wsc, p.expand_mul);
+                    if (slow)
+                        dw_taps_channel<W, true, false, KS>(acc[ci], xr, tw, lut, woff, wsc, p.expand_mul);
+                    else
+                        dw_taps_channel<W, false, false, KS>(acc[ci], xr, tw, lut, woff, wsc, p.expand_mul);
                 }
             }
             __syncthreads();                // every warp is done with the packed halo
@@ -587,9 +616,10 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
             }
             __syncthreads();
             float *dst = p.out + (long long)tl.n * p.OH * p.OW * p.C;
+            constexpr int G4 = CB / 4;      // 4-channel groups of the tile
 #pragma unroll 4
-            for (int e = tid; e < kDwTileOut * 4; e += kDwThreads) {
-                const int c4 = e & 3, pos = e >> 2;
+            for (int e = tid; e < kDwTileOut * G4; e += kDwThreads) {
+                const int c4 = e % G4, pos = e / G4;
                 const int i = pos >> tq_shift, j = pos & (tq - 1);
                 const int pp = tl.p0 + i, qq = tl.q0 + j, c = tl.c0 + 4 * c4;
                 if (pp < p.OH && qq < p.OW && c < p.C) {
@@ -607,23 +637,24 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
         for (int ci = 0; ci < CPW; ++ci) {
             const int c = c0 + warp + 8 * ci;
 #pragma unroll
-            for (int k = 0; k < 9; ++k) {
+            for (int k = 0; k < KK; ++k) {
                 float v = facc[ci][k].x + facc[ci][k].y;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                if (lane == 0 && c < p.C) p.out[((long long)g * 9 + k) * p.C + c] = v;
+                if (lane == 0 && c < p.C) p.out[((long long)g * KK + k) * p.C + c] = v;
             }
         }
     }
 }
 
 // Launch the tiled kernel for a narrowed table of `width` bits (8 or 16).
-template <int MODE, int ALU>
+template <int MODE, int ALU, int KS = 3>
 int launch_tile(int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
 {
     const bool wide = tp.lq_shift == 5;
-    auto kfn = width == 8 ? (wide ? dw_tile_kernel<8, MODE, ALU, true> : dw_tile_kernel<8, MODE, ALU, false>)
-                          : (wide ? dw_tile_kernel<16, MODE, ALU, true> : dw_tile_kernel<16, MODE, ALU, false>);
+    auto kfn = width == 8 ? (wide ? dw_tile_kernel<8, MODE, ALU, true, KS> : dw_tile_kernel<8, MODE, ALU, false, KS>)
+                          : (wide ? dw_tile_kernel<16, MODE, ALU, true, KS>
+                                  : dw_tile_kernel<16, MODE, ALU, false, KS>);
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return amsim::cuda_status(e);
     kfn<<<grid, kDwThreads, smem, st>>>(tp);

@@ -370,10 +370,11 @@ size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim
  * channel c only:
  *   y[n,p,q,c*D+d] = sum_{r,s} AMSim(x[n, p*sh - ph + r*dh, q*sw - pw + s*dw, c], w[r,s,c,d]).
  * x: N*H*W*C, w: R*S*C*D, y: N*P*Q*K (written).  Padded taps are zero
- * operands.  3x3 filters with unit dilation at stride 1 or 2, D = 1, C a
- * multiple of 4, 16-byte aligned x and y and an 8- or 16-bit narrowed LUT of
- * at most 64 KB take a tiled kernel (AMSIM_PATH_DW_TILES); everything else the
- * direct kernel (AMSIM_PATH_DW_DIRECT).  Scratch is not used.
+ * operands.  3x3 filters with unit dilation at stride 1 or 2 and 5x5 filters
+ * at stride 1, D = 1, C a multiple of 4, 16-byte aligned x and y and an 8- or
+ * 16-bit narrowed LUT of at most 64 KB take a tiled kernel
+ * (AMSIM_PATH_DW_TILES); everything else the direct kernel
+ * (AMSIM_PATH_DW_DIRECT).  Scratch is not used.
  */
 int amsim_dwconv2d_fwd(const amsim_conv_desc *desc, const float *x, const float *w, float *y,
                        amsim_lut_t lut, void *ws, size_t ws_bytes, amsim_stream_t stream);

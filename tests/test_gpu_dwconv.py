@@ -27,6 +27,14 @@ TILED = [
     (1, 64, 8, 4, 1, 3, 3, (1, 1), (1, 1), (1, 1)),     # 64 x 8 tiles
     (2, 7, 7, 16, 1, 3, 3, (1, 1), (1, 1), (1, 1)),     # 7 x 7: the last MobileNet resolution
 ]
+# 5x5 filters at unit stride: the tiled kernel with 8-channel tiles
+TILED5 = [
+    (2, 12, 70, 16, 1, 5, 5, (1, 1), (2, 2), (1, 1)),   # ragged row and column tiles
+    (1, 14, 14, 8, 1, 5, 5, (1, 1), (2, 2), (1, 1)),    # 16 x 32 tiles
+    (2, 9, 9, 12, 1, 5, 5, (1, 1), (0, 0), (1, 1)),     # no padding, 12 channels
+    (1, 7, 40, 20, 1, 5, 5, (1, 1), (4, 1), (1, 1)),    # padding past the filter's reach in rows
+]
+
 DIRECT = [
     (2, 7, 6, 3, 1, 3, 3, (1, 1), (1, 1), (1, 1)),      # 3 channels: not a multiple of 4
     (1, 9, 8, 2, 3, 3, 2, (2, 1), (1, 0), (1, 1)),      # multiplier 3, stride 2
@@ -113,6 +121,14 @@ def test_dwconv_tiled_kernel(amd, orc, luts, g, kind):
 
 
 @pytest.mark.parametrize("kind", ["mitchell", "exact"])
+@pytest.mark.parametrize("g", TILED5)
+def test_dwconv_tiled_kernel_5x5(amd, orc, luts, g, kind):
+    rng = np.random.default_rng(31 + sum(g[:7]) + 7 * (kind == "exact"))
+    x, w, dy = operands(orc, g, rng)
+    check_passes(amd, orc, luts(kind, 7), kind, 7, g, x, w, dy, amd.AMSIM_PATH_DW_TILES)
+
+
+@pytest.mark.parametrize("kind", ["mitchell", "exact"])
 @pytest.mark.parametrize("g", DIRECT)
 def test_dwconv_direct_kernel(amd, orc, luts, g, kind):
     rng = np.random.default_rng(3 + sum(g[:7]) + 7 * (kind == "exact"))
@@ -157,7 +173,7 @@ def sprinkle(a, rng, frac=0.03):
     return flat.view(np.float32).reshape(a.shape)
 
 
-@pytest.mark.parametrize("g", [TILED[0], TILED[1], DIRECT[1], STRIDE2[0], STRIDE2[3]])
+@pytest.mark.parametrize("g", [TILED[0], TILED[1], TILED5[0], TILED5[2], DIRECT[1], STRIDE2[0], STRIDE2[3]])
 def test_dwconv_special_operands(amd, orc, luts, g):
     """Zeros, denormals, infinities, NaN and overflowing products in every
     operand: the NaN pattern and infinities match exactly, the rest within the
@@ -171,7 +187,7 @@ def test_dwconv_special_operands(amd, orc, luts, g):
         x[0, 3, -1, :] = np.inf
         x[0, 4, -2, 1] = -np.inf
     t, d = amd.AMSIM_PATH_DW_TILES, amd.AMSIM_PATH_DW_DIRECT
-    bit = t if g in TILED else stride2_paths(amd, g) if g in STRIDE2 else d
+    bit = t if (g in TILED or g in TILED5) else stride2_paths(amd, g) if g in STRIDE2 else d
     check_passes(amd, orc, luts("mitchell", 7), "mitchell", 7, g, x, w, dy, bit)
 
 
@@ -304,6 +320,15 @@ def test_dwconv_closed_form_equals_table(amd, orc, kind):
                     assert np.array_equal(np.isnan(a), np.isnan(b))
                     ref, sa = oracle_pass(orc, kind, 7, which, desc, *args[which], b.size)
                     assert_close(b.reshape(-1), ref, sa, f"closed form {kind} {PASSES[which]} {g}")
+        # 5x5 filters have no closed-form variant: the table path runs, with the same results
+        g = TILED5[0]
+        rng = np.random.default_rng(12)
+        x, w, dy = operands(orc, g, rng)
+        desc, P, Q = dims(orc, g)
+        a, pa = run_dw(amd, lut_t, 0, g, x, w, out_shape(g, P, Q, 0))
+        b, pb = run_dw(amd, lut_c, 0, g, x, w, out_shape(g, P, Q, 0))
+        assert pb & amd.AMSIM_PATH_DW_TILES and not pb & amd.AMSIM_PATH_CLOSED_FORM, pb
+        assert np.array_equal(bits(a), bits(b))
     finally:
         lut_t.close()
         lut_c.close()
