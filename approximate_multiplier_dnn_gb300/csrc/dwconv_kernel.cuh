@@ -1,6 +1,7 @@
-// Depthwise Conv2D tiled kernel (internal header): the 3x3 unit-stride
-// kernel of dwconv.cu, shared with dwconv_alu.cu, which instantiates its
-// closed-form variants.  See dwconv.cu for the operation and the design.
+// Depthwise Conv2D tiled kernel (internal header): the unit-stride kernel for
+// 3x3 and 5x5 filters, shared by dwconv.cu (3x3 table variants),
+// dwconv_alu.cu (3x3 closed forms), dwconv_k5.cu (5x5) and dwconv_s2.cu (its
+// packing helpers).  See dwconv.cu for the operation and the design.
 #pragma once
 
 #include "gemm_tma.cuh"

@@ -342,7 +342,8 @@ class DwConvStep:
         measurements; the library decides, see amsim_last_path)."""
         g = self.g
         base = (g["D"] == 1 and g["R"] == 3 and g["S"] == 3 and tuple(g["dil"]) == (1, 1) and g["C"] % 4 == 0)
-        if base and tuple(g["stride"]) == (1, 1):
+        five = (g["D"] == 1 and g["R"] == 5 and g["S"] == 5 and tuple(g["dil"]) == (1, 1) and g["C"] % 4 == 0)
+        if (base or five) and tuple(g["stride"]) == (1, 1):
             return "dw_tile_kernel"
         if base and tuple(g["stride"]) == (2, 2):
             if p != 1:

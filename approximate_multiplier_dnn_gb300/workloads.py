@@ -144,3 +144,15 @@ def dwconv3x3_s2(N=64, H=112, W=112, C=64, seed=0):
     return {"x": normal((N, H, W, C), 1.0, seed),
             "w": he_normal((3, 3, C, 1), 9, seed + 1),
             "dy": normal((N, P, P, C), 0.01, seed + 2)}
+
+
+# EfficientNet-style 5x5 depthwise layer: 28x28x240, padding 2
+DWCONV5X5 = dict(N=64, H=28, W=28, C=240, D=1, R=5, S=5, stride=(1, 1), pad=(2, 2), dil=(1, 1))
+
+
+def dwconv5x5(N=64, H=28, W=28, C=240, seed=0):
+    """As dwconv3x3 for a 5x5 filter (He-normal over its 25 taps)."""
+    return {"x": normal((N, H, W, C), 1.0, seed),
+            "w": he_normal((5, 5, C, 1), 25, seed + 1),
+            "dy": normal((N, H, W, C), 0.01, seed + 2)}
+

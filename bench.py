@@ -38,7 +38,7 @@ LOOKUPS_PER_CLK_PER_SM = 32     # one 4-byte shared-memory wavefront per clock p
 CLOSED_FORM_PER_CLK_PER_SM = {"mitchell": 64, "exact": 128}
 
 WORKLOADS = ("mlp", "mlp_layers", "conv3x3", "conv3x3_exact", "gemm4096", "attention", "conv1x1", "dwconv3x3",
-             "dwconv3x3_s2", "gemm64", "mul")
+             "dwconv3x3_s2", "dwconv5x5", "gemm64", "mul")
 
 
 def measured_peaks():
@@ -71,6 +71,7 @@ def workload_name(name, M=7, kind="mitchell"):
         "conv1x1": "conv1x1_nhwc_64x56x56x256_k256_fwd_mitchell_M7",
         "dwconv3x3": "dwconv3x3_nhwc_64x56x56x128_d1_fwd+bwd_data+bwd_filter_mitchell_M7",
         "dwconv3x3_s2": "dwconv3x3_stride2_nhwc_64x112x112x64_d1_fwd+bwd_data+bwd_filter_mitchell_M7",
+        "dwconv5x5": "dwconv5x5_nhwc_64x28x28x240_d1_fwd+bwd_data+bwd_filter_mitchell_M7",
         "mul": "elementwise_2^28_pairs_special_mix_mitchell_M7",
         "gemm64": "gemm_64x128x64_mitchell_M7",
     }
@@ -102,6 +103,8 @@ def make_step(name, lut_for, M=7, kind="mitchell"):
         return steps.DwConvStep(wl.dwconv3x3(), wl.DWCONV3X3, lut_for("mitchell", 7)), wname
     if name == "dwconv3x3_s2":
         return steps.DwConvStep(wl.dwconv3x3_s2(), wl.DWCONV3X3_S2, lut_for("mitchell", 7)), wname
+    if name == "dwconv5x5":
+        return steps.DwConvStep(wl.dwconv5x5(), wl.DWCONV5X5, lut_for("mitchell", 7)), wname
     if name == "mul":
         return steps.MulStep(wl.elementwise_pairs(1 << 28, seed=5), lut_for("mitchell", 7)), wname
     if name == "gemm64":
@@ -477,7 +480,7 @@ def main():
                         frac=achieved / cpeak, lookup_roofline_frac=achieved / peak,
                         kernel="lutgemm_raw_kernel<1|2> (closed forms, no table); see amsim_last_path")
         roofline.pop("lut_residency", None)
-    if args.workload in ("dwconv3x3", "dwconv3x3_s2"):
+    if args.workload in ("dwconv3x3", "dwconv3x3_s2", "dwconv5x5"):
         # a stencil: each pass reads its operands once and writes its output
         # once, with 9 products per output element.  Every pass's two lower
         # bounds (compulsory DRAM bytes at the measured copy bandwidth, lookups
