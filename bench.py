@@ -137,10 +137,12 @@ def oracle_parts(name):
     if name == "gemm4096":
         d = wl.square_gemm(4096)
         return [(lambda rows: oracle.gemm("mitchell", 7, d["A"], d["B"], rows=rows), 4096, 4096 * 4096)]
-    if name == "dwconv3x3":
+    if name in ("dwconv3x3", "dwconv3x3_s2", "dwconv5x5"):
         # a "row" is a block of 64 consecutive outputs (forward, data gradient)
         # or one filter-gradient element (a sum over every N*P*Q pixel)
-        d, g = wl.dwconv3x3(), wl.DWCONV3X3
+        d, g = {"dwconv3x3": (wl.dwconv3x3, wl.DWCONV3X3), "dwconv3x3_s2": (wl.dwconv3x3_s2, wl.DWCONV3X3_S2),
+                "dwconv5x5": (wl.dwconv5x5, wl.DWCONV5X5)}[name]
+        d = d()
         desc = oracle.conv_desc(g["N"], g["H"], g["W"], g["C"], g["C"] * g["D"], g["R"], g["S"], g["stride"],
                                 g["pad"], g["dil"])
         P, Q = oracle.conv_out_hw(desc)
@@ -153,8 +155,9 @@ def oracle_parts(name):
 
         out.append((lambda rows: oracle.dwconv2d_fwd("mitchell", 7, desc, d["x"], d["w"], blocks(rows)),
                     ny // 64, 64 * taps))
+        # the pass's useful MACs (those the GPU step counts) spread over its dx blocks
         out.append((lambda rows: oracle.dwconv2d_bwd_data("mitchell", 7, desc, d["dy"], d["w"], blocks(rows)),
-                    nx // 64, 64 * taps * g["D"]))
+                    nx // 64, int(round(64 * taps * ny / nx))))
         out.append((lambda rows: oracle.dwconv2d_bwd_filter("mitchell", 7, desc, d["x"], d["dy"],
                                                             rows.astype(np.int64)),
                     taps * g["C"] * g["D"], g["N"] * P * Q))
@@ -631,7 +634,8 @@ def main():
            "serial_value": world * macs / (serial_ms * 1e-3) / 1e9}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("mlp", "gemm4096", "dwconv3x3"):
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("mlp", "gemm4096", "dwconv3x3", "dwconv3x3_s2",
+                                                                            "dwconv5x5"):
         import oracle
         oracle.build()
         cores = os.cpu_count() or 1
