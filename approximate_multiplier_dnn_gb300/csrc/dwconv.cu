@@ -344,9 +344,9 @@ bool dw_map(CUtensorMap *map, const float *base, int N, int H, int W, int C, int
 }  // namespace
 namespace amsim {
 namespace dw {
-int launch_s2(int mode, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st);
+int launch_s2(int alu, int mode, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st);
 size_t s2_smem_bytes(int table_bytes, int mode);
-int launch_s2d(int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st);
+int launch_s2d(int alu, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st);
 size_t s2d_smem_bytes(int table_bytes);
 extern template int launch_tile<0, 1>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<1, 1>(int, const DwTileParams &, int, size_t, cudaStream_t);
@@ -408,9 +408,11 @@ bool dw_s2_ok(const DwGeo &g, const amsim_lut_t lut, int which, const float *t0,
     return true;
 }
 
+int dw_staged_lut(const amsim_lut_t lut, int ks);
+
 int s2_ctas_per_sm(const amsim_lut_t lut, int which)
 {
-    const int per = (int)amsim::dw::s2_smem_bytes((int)lut->narrow_bytes, which) + 1024;
+    const int per = (int)amsim::dw::s2_smem_bytes(dw_staged_lut(lut, 3), which) + 1024;
     return std::max(1, std::min(2, (228 * 1024) / per));
 }
 
@@ -555,6 +557,8 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         sp.tiles_q = (g.Q + kS2Cols - 1) / kS2Cols;
         sp.cblocks = (g.C + kS2Ch - 1) / kS2Ch;
         sp.tiles = g.N * sp.tiles_p * sp.tiles_q;
+        const int alu = dw_alu(lut, 3);
+        const int staged = dw_staged_lut(lut, 3);
         if (which == 1) {
             // data gradient: 8 x 64 dx tiles of 16 channels over 5 x 33 dy windows
             sp.IH = g.P; sp.IW = g.Q; sp.OH = g.H; sp.OW = g.W;
@@ -566,13 +570,13 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
             if (dw_map(&sp.amap, t0, g.N, g.P, g.Q, g.C, 16, 33, 5)) {
                 const long long total = (long long)sp.tiles * sp.cblocks;
                 if (total > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
-                const size_t smem = amsim::dw::s2d_smem_bytes((int)lut->narrow_bytes);
+                const size_t smem = amsim::dw::s2d_smem_bytes(staged);
                 const int per_sm = std::max(1, std::min(2, (int)((228 * 1024) / (smem + 1024))));
                 const int grid = (int)std::min<long long>(total, (long long)per_sm * sms);
-                rc = amsim::dw::launch_s2d(width, sp, grid, smem, st);
+                rc = amsim::dw::launch_s2d(alu, width, sp, grid, smem, st);
                 if (rc == AMSIM_OK) {
                     amsim::count_launch();
-                    amsim::set_last_path(AMSIM_PATH_DW_TILES);
+                    amsim::set_last_path(AMSIM_PATH_DW_TILES | (alu ? AMSIM_PATH_CLOSED_FORM : 0));
                 }
                 return rc;
             }
@@ -581,21 +585,21 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
                             dw_map(&sp.amap, t0, g.N, g.H, g.W, g.C, kS2Ch, 2 * kS2Cols + 1, 2 * kS2Rows + 1) &&
                             (which == 0 || dw_map(&sp.bmap, t1, g.N, g.P, g.Q, g.C, kS2Ch, kS2Cols, kS2Rows));
         if (mapped) {
-            const size_t smem = amsim::dw::s2_smem_bytes((int)lut->narrow_bytes, which);
-            path = AMSIM_PATH_DW_TILES;
+            const size_t smem = amsim::dw::s2_smem_bytes(staged, which);
+            path = AMSIM_PATH_DW_TILES | (alu ? AMSIM_PATH_CLOSED_FORM : 0);
             if (which == 0) {
                 sp.out = out;
                 sp.G = 1;
                 const long long total = (long long)sp.tiles * sp.cblocks;
                 if (total > 0x7FFFFFFFLL) return AMSIM_EUNSUPPORTED;
                 const int grid = (int)std::min<long long>(total, (long long)s2_ctas_per_sm(lut, 0) * sms);
-                rc = amsim::dw::launch_s2(0, width, sp, grid, smem, st);
+                rc = amsim::dw::launch_s2(alu, 0, width, sp, grid, smem, st);
                 if (rc == AMSIM_OK) amsim::count_launch();
             } else {
                 const DwFilterPlan f = filter_plan(g, 2, sms, lut);
                 sp.G = shares_for(f, ws_bytes);
                 sp.out = sp.G > 1 ? static_cast<float *>(ws) : out;
-                rc = amsim::dw::launch_s2(2, width, sp, sp.cblocks * sp.G, smem, st);
+                rc = amsim::dw::launch_s2(alu, 2, width, sp, sp.cblocks * sp.G, smem, st);
                 if (rc == AMSIM_OK) amsim::count_launch();
                 if (rc == AMSIM_OK && sp.G > 1) {
                     const int blocks = (int)std::min<long long>((n_out + 255) / 256, 4LL * sms);

@@ -33,7 +33,7 @@ constexpr int kS2RawA = (kS2HR * kS2HC * kS2CB * 4 + 127) & ~127;
 constexpr int kS2RawB = kS2TP * kS2TQ * kS2CB * 4;
 constexpr int kS2Halo = (kS2CB * kS2CP * 4 + 127) & ~127;
 constexpr int kS2Out = (kS2CB * kS2OP * 4 + 127) & ~127;
-constexpr int kS2WB = (2 * kS2CB * 9 * 4 + 127) & ~127;
+constexpr int kS2WB = (3 * kS2CB * 9 * 4 + 127) & ~127;   // tap offsets, scales, closed-form values
 static_assert(kS2Out <= kS2Halo, "the output tile reuses the packed window");
 static_assert(s2_plane_off(1, 1) + 4 * kS2PW == kS2CP, "plane layout");
 
@@ -88,7 +88,7 @@ __device__ __forceinline__ void s2_repack_window(const float *x, uint32_t *xt, i
 
 // Forward products of one channel for one lane (xc: the channel's planes,
 // offset by the lane's column pair).
-template <int W, bool SLOW>
+template <int W, bool SLOW, bool GL = false>
 __device__ __forceinline__ void s2_taps(float2 (&acc)[kS2TP], const uint32_t *xc, const uint8_t *lut,
                                         const uint32_t (&woff)[9], const float (&wsc)[9], uint32_t mul)
 {
@@ -121,8 +121,8 @@ __device__ __forceinline__ void s2_taps(float2 (&acc)[kS2TP], const uint32_t *xc
                         const int t = r * 3 + s;
                         const uint32_t i0 = px[so] - sb[so] + woff[t];
                         const uint32_t i1 = px[so + 1] - sb[so + 1] + woff[t];
-                        const float2 v = make_float2(dw_expand(lut_ld<W, false>(lut, i0), mul),
-                                                     dw_expand(lut_ld<W, false>(lut, i1), mul));
+                        const float2 v = make_float2(dw_expand(lut_ld<W, GL>(lut, i0), mul),
+                                                     dw_expand(lut_ld<W, GL>(lut, i1), mul));
                         const float2 sc = fmul2_ftz(make_float2(wsc[t], wsc[t]), make_float2(sx[so], sx[so + 1]));
                         if constexpr (SLOW) {
                             acc[i].x = __fadd_rn(acc[i].x, __fmul_rn(v.x, sc.x));
@@ -138,7 +138,7 @@ __device__ __forceinline__ void s2_taps(float2 (&acc)[kS2TP], const uint32_t *xc
 // Weight-gradient products of one channel for one lane over one tile (dr: the
 // channel's dy tile at the lane's column pair).  In the slow form, positions
 // past the output gradient's edge are skipped.
-template <int W, bool SLOW>
+template <int W, bool SLOW, bool GL = false>
 __device__ __forceinline__ void s2_filter(float2 (&acc)[9], const uint32_t *xc, const uint32_t *dr,
                                           const uint8_t *lut, int rows_ok, bool ok0, bool ok1, uint32_t mul)
 {
@@ -180,8 +180,8 @@ __device__ __forceinline__ void s2_filter(float2 (&acc)[9], const uint32_t *xc, 
                         const int t = r * 3 + s;
                         const uint32_t i0 = px[so] - sb[so] + od[i][0];
                         const uint32_t i1 = px[so + 1] - sb[so + 1] + od[i][1];
-                        const float2 v = make_float2(dw_expand(lut_ld<W, false>(lut, i0), mul),
-                                                     dw_expand(lut_ld<W, false>(lut, i1), mul));
+                        const float2 v = make_float2(dw_expand(lut_ld<W, GL>(lut, i0), mul),
+                                                     dw_expand(lut_ld<W, GL>(lut, i1), mul));
                         const float2 sc = fmul2_ftz(make_float2(sx[so], sx[so + 1]), sd[i]);
                         if constexpr (SLOW) {
                             if (row_ok && ok0) acc[t].x = __fadd_rn(acc[t].x, __fmul_rn(v.x, sc.x));
@@ -194,10 +194,120 @@ __device__ __forceinline__ void s2_filter(float2 (&acc)[9], const uint32_t *xc, 
             }
 }
 
+// ------------------------------------------------------------------ closed forms
+// Closed-form products (amsim_lut_set_closed_form; ALU 1 Mitchell, 2 exact) on
+// words packed by dw_pack_alu (the truncated value itself), as in the
+// stride-1 kernel: Mitchell adds the other operand's fraction field to the
+// truncated value's bits and multiplies by its scale; exact takes one FMA of
+// the two truncated values.  Same products and accumulation order as the
+// table path, so results are bit-identical.
+__device__ __forceinline__ void s2_pack_window_alu(const float *raw, uint32_t *xt, uint32_t keep, int tid, bool &big)
+{
+#pragma unroll 4
+    for (int e = tid; e < kS2HR * kS2HC * 2; e += kDwThreads) {
+        const int c4 = e & 1, pos = e >> 1;
+        const int row = pos / kS2HC, col = pos - row * kS2HC;
+        const float4 v = *reinterpret_cast<const float4 *>(raw + pos * kS2CB + 4 * c4);
+        uint32_t *d = xt + 4 * c4 * kS2CP + s2_index(row, col);
+        d[0] = dw_pack_alu(v.x, keep, big);
+        d[kS2CP] = dw_pack_alu(v.y, keep, big);
+        d[2 * kS2CP] = dw_pack_alu(v.z, keep, big);
+        d[3 * kS2CP] = dw_pack_alu(v.w, keep, big);
+    }
+}
+
+template <int ALU>
+__device__ __forceinline__ void s2_taps_alu(float2 (&acc)[kS2TP], const uint32_t *xc, const uint32_t (&wv)[9])
+{
+#pragma unroll
+    for (int i = 0; i < kS2TP; ++i) acc[i] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int pr = 0; pr < 5 - a; ++pr) {
+                const uint32_t *row = xc + s2_plane_off(a, b) + pr * kS2PW;
+                const uint2 a01 = *reinterpret_cast<const uint2 *>(row);
+                const uint32_t px[3] = {a01.x, a01.y, b == 0 ? row[2] : 0u};
+                uint32_t sb[3];
+#pragma unroll
+                for (int k = 0; k < 3; ++k) sb[k] = px[k] & 0xFF800000u;
+#pragma unroll
+                for (int ro = 0; ro < 2; ++ro) {
+                    const int r = 2 * ro + a, i = pr - ro;
+                    if (r > 2 || i < 0 || i >= kS2TP) continue;
+#pragma unroll
+                    for (int so = 0; so < 2; ++so) {
+                        const int s = 2 * so + b;
+                        if (s > 2) continue;
+                        const int t = r * 3 + s;
+                        if constexpr (ALU == 1) {
+                            const float2 w = make_float2(__uint_as_float(wv[t] + px[so] - sb[so]),
+                                                         __uint_as_float(wv[t] + px[so + 1] - sb[so + 1]));
+                            acc[i] = fadd2(acc[i], fmul2_ftz(w, make_float2(__uint_as_float(sb[so]),
+                                                                            __uint_as_float(sb[so + 1]))));
+                        } else {
+                            const float wf = __uint_as_float(wv[t]);
+                            acc[i] = ffma2(make_float2(__uint_as_float(px[so]), __uint_as_float(px[so + 1])),
+                                           make_float2(wf, wf), acc[i]);
+                        }
+                    }
+                }
+            }
+}
+
+template <int ALU>
+__device__ __forceinline__ void s2_filter_alu(float2 (&acc)[9], const uint32_t *xc, const uint32_t *dr)
+{
+    uint32_t od[kS2TP][2];
+    float2 sd[kS2TP], dv[kS2TP];
+#pragma unroll
+    for (int i = 0; i < kS2TP; ++i) {
+        const uint2 d01 = *reinterpret_cast<const uint2 *>(dr + i * kS2TQ);
+        const uint32_t db0 = d01.x & 0xFF800000u, db1 = d01.y & 0xFF800000u;
+        od[i][0] = d01.x - db0;
+        od[i][1] = d01.y - db1;
+        sd[i] = make_float2(__uint_as_float(db0), __uint_as_float(db1));
+        dv[i] = make_float2(__uint_as_float(d01.x), __uint_as_float(d01.y));
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int pr = 0; pr < 5 - a; ++pr) {
+                const uint32_t *row = xc + s2_plane_off(a, b) + pr * kS2PW;
+                const uint2 a01 = *reinterpret_cast<const uint2 *>(row);
+                const uint32_t px[3] = {a01.x, a01.y, b == 0 ? row[2] : 0u};
+#pragma unroll
+                for (int ro = 0; ro < 2; ++ro) {
+                    const int r = 2 * ro + a, i = pr - ro;
+                    if (r > 2 || i < 0 || i >= kS2TP) continue;
+#pragma unroll
+                    for (int so = 0; so < 2; ++so) {
+                        const int s = 2 * so + b;
+                        if (s > 2) continue;
+                        const int t = r * 3 + s;
+                        if constexpr (ALU == 1) {
+                            const float2 w = make_float2(__uint_as_float(px[so] + od[i][0]),
+                                                         __uint_as_float(px[so + 1] + od[i][1]));
+                            acc[t] = fadd2(acc[t], fmul2_ftz(w, sd[i]));
+                        } else {
+                            acc[t] = ffma2(make_float2(__uint_as_float(px[so]), __uint_as_float(px[so + 1])), dv[i],
+                                           acc[t]);
+                        }
+                    }
+                }
+            }
+}
+
 // MODE 0: forward (grid-stride over the tiles); 2: weight gradient (CTA =
-// (channel block, share of the spatial tiles)).  p.tiles_p / p.tiles_q count
+// (channel block, share of the spatial tiles)).  ALU 0: table products from
+// the staged LUT; 1 / 2: closed forms (the LUT read from global memory only by
+// slow tiles).  p.tiles_p / p.tiles_q count
 // 4-row / 64-column tiles of the output (or dy) grid.
-template <int W, int MODE>
+template <int W, int MODE, int ALU>
 __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_constant__ DwTileParams p)
 {
     using amsim::kern::mbar_expect_tx;
@@ -207,13 +317,15 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_const
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint8_t *lut = smem;
-    float *rawA = reinterpret_cast<float *>(smem + dw_lut_region(p.table_bytes));
+    const uint8_t *glut = static_cast<const uint8_t *>(p.table);         // slow closed-form tiles
+    float *rawA = reinterpret_cast<float *>(smem + (ALU ? 0 : dw_lut_region(p.table_bytes)));
     uint32_t *xt = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(rawA) + kS2RawA);
     uint8_t *after = reinterpret_cast<uint8_t *>(xt) + kS2Halo;
     float *rawB = reinterpret_cast<float *>(after);                      // mode 2
     uint32_t *dyt = reinterpret_cast<uint32_t *>(after + kS2RawB);       // mode 2
     uint32_t *wt_off = reinterpret_cast<uint32_t *>(after);              // mode 0
     float *wt_scl = reinterpret_cast<float *>(after + kS2CB * 9 * 4);
+    uint32_t *wt_val = reinterpret_cast<uint32_t *>(after + 2 * kS2CB * 9 * 4);   // closed forms
     uint64_t *bar = reinterpret_cast<uint64_t *>(after + (MODE == 2 ? kS2RawB + kS2Out : kS2WB));
 
     int t_begin, t_end, t_step, cb_fixed = 0, g = 0;
@@ -254,7 +366,7 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_const
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (t_begin < t_end) issue(tile_at(t_begin));
     }
-    {   // LUT -> shared memory (the device table is padded to 256 bytes)
+    if constexpr (ALU == 0) {   // LUT -> shared memory (the device table is padded to 256 bytes)
         const uint4 *src = static_cast<const uint4 *>(p.table);
         uint4 *dst = reinterpret_cast<uint4 *>(lut);
         const int nvec = (p.table_bytes + 15) >> 4;
@@ -278,11 +390,17 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_const
         if (__syncthreads_or(aborted)) break;
         bool big = false;
         const int a_shift = MODE == 2 ? hi_shift : lo_shift;
-        s2_pack_window(rawA, xt, 23 - p.M - a_shift, ((1u << p.M) - 1u) << a_shift, tid, big);
-        if constexpr (MODE == 2) {
-            dw_pack_box<kS2CB>(rawB, dyt, kS2TP * kS2TQ, kS2OP, 23 - p.M - lo_shift, ((1u << p.M) - 1u) << lo_shift,
-                               tid, big);
-        } else if (tid < kS2CB * 9) {
+        const uint32_t keep = ((1u << p.M) - 1u) << (23 - p.M);
+        if constexpr (ALU != 0) {
+            s2_pack_window_alu(rawA, xt, keep, tid, big);
+            if constexpr (MODE == 2) dw_pack_box_alu<kS2CB>(rawB, dyt, kS2TP * kS2TQ, kS2OP, keep, tid, big);
+        } else {
+            s2_pack_window(rawA, xt, 23 - p.M - a_shift, ((1u << p.M) - 1u) << a_shift, tid, big);
+            if constexpr (MODE == 2)
+                dw_pack_box<kS2CB>(rawB, dyt, kS2TP * kS2TQ, kS2OP, 23 - p.M - lo_shift,
+                                   ((1u << p.M) - 1u) << lo_shift, tid, big);
+        }
+        if (MODE != 2 && tid < kS2CB * 9) {
             const int c = tid / 9, tap = tid % 9;
             const float v = tl.c0 + c < p.C ? __ldg(p.b + (long long)tap * p.C + tl.c0 + c) : 0.0f;
             int wbig = 0;
@@ -290,6 +408,7 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_const
             big |= wbig != 0;
             wt_off[tid] = pk - dw_scale_bits(pk);
             wt_scl[tid] = __uint_as_float(dw_scale_bits(pk));
+            if constexpr (ALU != 0) wt_val[tid] = dw_pack_alu(v, keep, big);
         }
         const bool slow = __syncthreads_or(big);   // the raw boxes are consumed
         if (tid == 0 && t + t_step < t_end) {
@@ -310,8 +429,13 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_const
             const int rows_ok = p.OH - tl.p0;
             const bool ok0 = tl.q0 + 2 * lane < p.OW, ok1 = tl.q0 + 2 * lane + 1 < p.OW;
             const uint32_t *dr = dyt + warp * kS2OP + 2 * lane;
-            if (slow) s2_filter<W, true>(facc, xc, dr, lut, rows_ok, ok0, ok1, p.expand_mul);
-            else s2_filter<W, false>(facc, xc, dr, lut, rows_ok, ok0, ok1, p.expand_mul);
+            if constexpr (ALU != 0) {
+                if (slow) s2_filter<W, true, true>(facc, xc, dr, glut, rows_ok, ok0, ok1, p.expand_mul);
+                else s2_filter_alu<ALU>(facc, xc, dr);
+            } else {
+                if (slow) s2_filter<W, true>(facc, xc, dr, lut, rows_ok, ok0, ok1, p.expand_mul);
+                else s2_filter<W, false>(facc, xc, dr, lut, rows_ok, ok0, ok1, p.expand_mul);
+            }
         } else {
             uint32_t woff[9];
             float wsc[9];
@@ -321,8 +445,19 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_const
                 wsc[k] = wt_scl[warp * 9 + k];
             }
             float2 acc[kS2TP];
-            if (slow) s2_taps<W, true>(acc, xc, lut, woff, wsc, p.expand_mul);
-            else s2_taps<W, false>(acc, xc, lut, woff, wsc, p.expand_mul);
+            if constexpr (ALU != 0) {
+                if (slow) {
+                    s2_taps<W, true, true>(acc, xc, glut, woff, wsc, p.expand_mul);
+                } else {
+                    uint32_t wv[9];
+#pragma unroll
+                    for (int k = 0; k < 9; ++k) wv[k] = wt_val[warp * 9 + k];
+                    s2_taps_alu<ALU>(acc, xc, wv);
+                }
+            } else {
+                if (slow) s2_taps<W, true>(acc, xc, lut, woff, wsc, p.expand_mul);
+                else s2_taps<W, false>(acc, xc, lut, woff, wsc, p.expand_mul);
+            }
             __syncthreads();                // every warp is done with the packed window
             float *ot = reinterpret_cast<float *>(xt);
             float *o = ot + warp * kS2OP + 2 * lane;
@@ -376,14 +511,14 @@ static_assert(kSdWR * kSdPW <= kSdCP, "window pitch");
 constexpr int kSdRaw = (kSdWR * kSdWC * kSdCB * 4 + 127) & ~127;
 constexpr int kSdWin = (kSdCB * kSdCP * 4 + 127) & ~127;
 constexpr int kSdOut = (kSdCB * kDwOP * 4 + 127) & ~127;
-constexpr int kSdWB = (2 * kSdCB * 9 * 4 + 127) & ~127;
+constexpr int kSdWB = (3 * kSdCB * 9 * 4 + 127) & ~127;
 
 __host__ __device__ constexpr int sd_smem(int table_bytes)
 {
     return dw_lut_region(table_bytes) + kSdRaw + kSdWin + kSdOut + kSdWB + 128;
 }
 
-template <int W, bool SLOW>
+template <int W, bool SLOW, bool GL = false>
 __device__ __forceinline__ void sd_channel(float2 (&acc)[kSdRows], const uint32_t *wr, const uint8_t *lut,
                                            const uint32_t (&woff)[9], const float (&wsc)[9], uint32_t mul)
 {
@@ -404,12 +539,12 @@ __device__ __forceinline__ void sd_channel(float2 (&acc)[kSdRows], const uint32_
                 // column pair: dx 2J (tap column 1, dy J) and 2J + 1 (tap column 0, dy J + 1)
                 const int t1 = r * 3 + 1, t0 = r * 3 + 0, t2 = r * 3 + 2;
                 const uint32_t i0 = d0 - b0 + woff[t1], i1 = d1 - b1 + woff[t0];
-                const float2 v = make_float2(dw_expand(lut_ld<W, false>(lut, i0), mul),
-                                             dw_expand(lut_ld<W, false>(lut, i1), mul));
+                const float2 v = make_float2(dw_expand(lut_ld<W, GL>(lut, i0), mul),
+                                             dw_expand(lut_ld<W, GL>(lut, i1), mul));
                 const float2 sc = fmul2_ftz(make_float2(wsc[t1], wsc[t0]), sd);
                 acc[row] = ffma2(v, sc, acc[row]);
                 // dx 2J + 1 again: tap column 2 at dy J
-                const float v2 = dw_expand(lut_ld<W, false>(lut, d0 - b0 + woff[t2]), mul);
+                const float v2 = dw_expand(lut_ld<W, GL>(lut, d0 - b0 + woff[t2]), mul);
                 acc[row].y = fmaf(v2, fmul_ftz(wsc[t2], sd.x), acc[row].y);
             }
         }
@@ -430,7 +565,7 @@ __device__ __forceinline__ void sd_channel(float2 (&acc)[kSdRows], const uint32_
                         const uint32_t d = on ? wr[(ry >> 1) * kSdPW + (cx >> 1)] : 0u;
                         const uint32_t sb = dw_scale_bits(d);
                         const int t = r * 3 + s;
-                        const float v = dw_expand(lut_ld<W, false>(lut, d - sb + woff[t]), mul);
+                        const float v = dw_expand(lut_ld<W, GL>(lut, d - sb + woff[t]), mul);
                         a = __fadd_rn(a, __fmul_rn(v, fmul_ftz(wsc[t], __uint_as_float(sb))));
                     }
                 if (b == 0) acc[row].x = a;
@@ -439,7 +574,38 @@ __device__ __forceinline__ void sd_channel(float2 (&acc)[kSdRows], const uint32_
     }
 }
 
-template <int W>
+// The fast branch of sd_channel in closed form (ALU 1 Mitchell, 2 exact), same
+// pairing and order; wv: the channel's nine truncated tap values.
+template <int ALU>
+__device__ __forceinline__ void sd_channel_alu(float2 (&acc)[kSdRows], const uint32_t *wr, const uint32_t (&wv)[9])
+{
+#pragma unroll
+    for (int i = 0; i < kSdRows; ++i) acc[i] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int ww = 0; ww < kSdWR; ++ww) {
+        const uint32_t d0 = wr[ww * kSdPW], d1 = wr[ww * kSdPW + 1];
+        const uint32_t b0 = d0 & 0xFF800000u, b1 = d1 & 0xFF800000u;
+        const float2 sd = make_float2(__uint_as_float(b0), __uint_as_float(b1));
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int row = k == 0 ? 2 * ww : k == 1 ? 2 * ww - 1 : 2 * ww + 1;
+            const int r = k == 0 ? 1 : k == 1 ? 0 : 2;
+            if (row < 0 || row >= kSdRows) continue;
+            const int t1 = r * 3 + 1, t0 = r * 3 + 0, t2 = r * 3 + 2;
+            if constexpr (ALU == 1) {
+                const float2 w = make_float2(__uint_as_float(wv[t1] + d0 - b0), __uint_as_float(wv[t0] + d1 - b1));
+                acc[row] = fadd2(acc[row], fmul2_ftz(w, sd));
+                acc[row].y = __fadd_rn(acc[row].y, fmul_ftz(__uint_as_float(wv[t2] + d0 - b0), sd.x));
+            } else {
+                acc[row] = ffma2(make_float2(__uint_as_float(d0), __uint_as_float(d1)),
+                                 make_float2(__uint_as_float(wv[t1]), __uint_as_float(wv[t0])), acc[row]);
+                acc[row].y = fmaf(__uint_as_float(d0), __uint_as_float(wv[t2]), acc[row].y);
+            }
+        }
+    }
+}
+
+template <int W, int ALU>
 __global__ void __launch_bounds__(kDwThreads, 2) dw_s2d_kernel(const __grid_constant__ DwTileParams p)
 {
     using amsim::kern::mbar_expect_tx;
@@ -449,11 +615,13 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2d_kernel(const __grid_cons
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint8_t *lut = smem;
-    float *raw = reinterpret_cast<float *>(smem + dw_lut_region(p.table_bytes));
+    const uint8_t *glut = static_cast<const uint8_t *>(p.table);         // slow closed-form tiles
+    float *raw = reinterpret_cast<float *>(smem + (ALU ? 0 : dw_lut_region(p.table_bytes)));
     uint32_t *win = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(raw) + kSdRaw);
     float *ot = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(win) + kSdWin);
     uint32_t *wt_off = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(ot) + kSdOut);
     float *wt_scl = reinterpret_cast<float *>(wt_off + kSdCB * 9);
+    uint32_t *wt_val = wt_off + 2 * kSdCB * 9;   // closed forms
     uint64_t *bar = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(wt_off) + kSdWB);
 
     const int total = p.tiles * p.cblocks;
@@ -478,7 +646,7 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2d_kernel(const __grid_cons
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if ((int)blockIdx.x < total) issue(tile_at(blockIdx.x));
     }
-    {
+    if constexpr (ALU == 0) {
         const uint4 *src = static_cast<const uint4 *>(p.table);
         uint4 *dst = reinterpret_cast<uint4 *>(lut);
         const int nvec = (p.table_bytes + 15) >> 4;
@@ -497,8 +665,12 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2d_kernel(const __grid_cons
         // also orders the previous tile's shared-memory reads before this tile's packing
         if (__syncthreads_or(aborted)) break;
         bool big = false;
-        dw_pack_box<kSdCB>(raw, win, kSdWR * kSdWC, kSdCP, 23 - p.M - lo_shift, ((1u << p.M) - 1u) << lo_shift, tid,
-                           big);
+        const uint32_t keep = ((1u << p.M) - 1u) << (23 - p.M);
+        if constexpr (ALU != 0)
+            dw_pack_box_alu<kSdCB>(raw, win, kSdWR * kSdWC, kSdCP, keep, tid, big);
+        else
+            dw_pack_box<kSdCB>(raw, win, kSdWR * kSdWC, kSdCP, 23 - p.M - lo_shift, ((1u << p.M) - 1u) << lo_shift,
+                               tid, big);
         if (tid < kSdCB * 9) {
             const int c = tid / 9, tap = tid % 9;
             const float v = tl.c0 + c < p.C ? __ldg(p.b + (long long)tap * p.C + tl.c0 + c) : 0.0f;
@@ -507,6 +679,7 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2d_kernel(const __grid_cons
             big |= wbig != 0;
             wt_off[tid] = pk - dw_scale_bits(pk);
             wt_scl[tid] = __uint_as_float(dw_scale_bits(pk));
+            if constexpr (ALU != 0) wt_val[tid] = dw_pack_alu(v, keep, big);
         }
         const bool slow = __syncthreads_or(big);   // the raw window is consumed
         if (tid == 0 && t + (int)gridDim.x < total) {
@@ -530,8 +703,19 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2d_kernel(const __grid_cons
                 wsc[k] = wt_scl[c * 9 + k];
             }
             const uint32_t *wr = win + c * kSdCP + lane;
-            if (slow) sd_channel<W, true>(acc[ci], wr, lut, woff, wsc, p.expand_mul);
-            else sd_channel<W, false>(acc[ci], wr, lut, woff, wsc, p.expand_mul);
+            if constexpr (ALU != 0) {
+                if (slow) {
+                    sd_channel<W, true, true>(acc[ci], wr, glut, woff, wsc, p.expand_mul);
+                } else {
+                    uint32_t wv[9];
+#pragma unroll
+                    for (int k = 0; k < 9; ++k) wv[k] = wt_val[c * 9 + k];
+                    sd_channel_alu<ALU>(acc[ci], wr, wv);
+                }
+            } else {
+                if (slow) sd_channel<W, true>(acc[ci], wr, lut, woff, wsc, p.expand_mul);
+                else sd_channel<W, false>(acc[ci], wr, lut, woff, wsc, p.expand_mul);
+            }
         }
 #pragma unroll
         for (int ci = 0; ci < 2; ++ci) {
@@ -555,22 +739,35 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2d_kernel(const __grid_cons
     }
 }
 
-int launch_s2d(int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
+// alu 0: table products (narrowed width 8 or 16); 1 / 2: closed forms.
+int launch_s2d(int alu, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
 {
-    auto kfn = width == 8 ? dw_s2d_kernel<8> : dw_s2d_kernel<16>;
+    void (*kfn)(DwTileParams);
+    if (alu == 1) kfn = width == 8 ? dw_s2d_kernel<8, 1> : dw_s2d_kernel<16, 1>;
+    else if (alu == 2) kfn = width == 8 ? dw_s2d_kernel<8, 2> : dw_s2d_kernel<16, 2>;
+    else kfn = width == 8 ? dw_s2d_kernel<8, 0> : dw_s2d_kernel<16, 0>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return amsim::cuda_status(e);
     kfn<<<grid, kDwThreads, smem, st>>>(tp);
     return amsim::cuda_status(cudaGetLastError());
 }
 
+// table_bytes: the staged table's size, 0 for closed forms.
 size_t s2d_smem_bytes(int table_bytes) { return (size_t)sd_smem(table_bytes); }
 
-// Launch for a narrowed table of `width` bits (8 or 16); mode 0 or 2.
-int launch_s2(int mode, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
+// Launch for mode 0 or 2; alu and width as for launch_s2d.
+int launch_s2(int alu, int mode, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
 {
-    auto kfn = mode == 0 ? (width == 8 ? dw_s2_kernel<8, 0> : dw_s2_kernel<16, 0>)
-                         : (width == 8 ? dw_s2_kernel<8, 2> : dw_s2_kernel<16, 2>);
+    void (*kfn)(DwTileParams);
+    if (alu == 1)
+        kfn = mode == 0 ? (width == 8 ? dw_s2_kernel<8, 0, 1> : dw_s2_kernel<16, 0, 1>)
+                        : (width == 8 ? dw_s2_kernel<8, 2, 1> : dw_s2_kernel<16, 2, 1>);
+    else if (alu == 2)
+        kfn = mode == 0 ? (width == 8 ? dw_s2_kernel<8, 0, 2> : dw_s2_kernel<16, 0, 2>)
+                        : (width == 8 ? dw_s2_kernel<8, 2, 2> : dw_s2_kernel<16, 2, 2>);
+    else
+        kfn = mode == 0 ? (width == 8 ? dw_s2_kernel<8, 0, 0> : dw_s2_kernel<16, 0, 0>)
+                        : (width == 8 ? dw_s2_kernel<8, 2, 0> : dw_s2_kernel<16, 2, 0>);
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return amsim::cuda_status(e);
     kfn<<<grid, kDwThreads, smem, st>>>(tp);

@@ -291,14 +291,15 @@ def test_dwconv_mobilenet_layer_full_size(amd, orc, luts):
 
 @pytest.mark.parametrize("kind", ["mitchell", "exact"])
 def test_dwconv_closed_form_equals_table(amd, orc, kind):
-    """Closed-form products (amsim_lut_set_closed_form) in the tiled kernel
-    give the table path's results bit for bit, on ordinary operands and on
-    tiles with special or tiny (nonzero, below 2^-63) values, which take the
-    slow computation; and they stay within the oracle's tolerance."""
+    """Closed-form products (amsim_lut_set_closed_form) in the tiled kernels
+    (3x3 at stride 1, and the three stride-2 kernels) give the table path's
+    results bit for bit, on ordinary operands and on tiles with special or
+    tiny (nonzero, below 2^-63) values, which take the slow computation; and
+    they stay within the oracle's tolerance."""
     lut_t = amd.Lut.build(kind, 7)
     lut_c = amd.Lut.build(kind, 7).set_closed_form(True)
     try:
-        for g in (TILED[0], TILED[1], TILED[4]):
+        for g in (TILED[0], TILED[1], TILED[4], STRIDE2[0], STRIDE2[1], STRIDE2[4]):
             for specials in (False, True):
                 rng = np.random.default_rng(11 + sum(g[:7]) + specials)
                 x, w, dy = operands(orc, g, rng)
