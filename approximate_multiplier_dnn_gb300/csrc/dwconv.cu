@@ -357,6 +357,12 @@ extern template int launch_tile<2, 2>(int, const DwTileParams &, int, size_t, cu
 extern template int launch_tile<0, 0, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<1, 0, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
 extern template int launch_tile<2, 0, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<0, 1, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<1, 1, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<2, 1, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<0, 2, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<1, 2, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
+extern template int launch_tile<2, 2, 5>(int, const DwTileParams &, int, size_t, cudaStream_t);
 }  // namespace dw
 }  // namespace amsim
 namespace {
@@ -364,7 +370,10 @@ namespace {
 template <int MODE>
 int launch_tile_any(int alu, int ks, int width, const DwTileParams &tp, int grid, size_t smem, cudaStream_t st)
 {
-    if (ks == 5) return launch_tile<MODE, 0, 5>(width, tp, grid, smem, st);
+    if (ks == 5)
+        return alu == 1   ? launch_tile<MODE, 1, 5>(width, tp, grid, smem, st)
+               : alu == 2 ? launch_tile<MODE, 2, 5>(width, tp, grid, smem, st)
+                          : launch_tile<MODE, 0, 5>(width, tp, grid, smem, st);
     if (alu == 1) return launch_tile<MODE, 1>(width, tp, grid, smem, st);
     if (alu == 2) return launch_tile<MODE, 2>(width, tp, grid, smem, st);
     return launch_tile<MODE, 0>(width, tp, grid, smem, st);
@@ -429,10 +438,10 @@ struct DwFilterPlan {
 // CTA also holds 1 KB of the SM's 228 KB for the system).
 // Closed-form variant of the tiled kernel a handle selects for a ks x ks
 // filter: 0 the table, 1 Mitchell, 2 exact (amsim_lut_set_closed_form on a
-// built-in kind; closed forms are built for 3x3 filters, 5x5 take the table).
+// built-in kind; 3x3 and 5x5 filters).
 int dw_alu(const amsim_lut_t lut, int ks)
 {
-    if (!lut->closed_form || ks != 3) return 0;
+    if (!lut->closed_form || (ks != 3 && ks != 5)) return 0;
     return lut->kind == AMSIM_MITCHELL ? 1 : 2;
 }
 

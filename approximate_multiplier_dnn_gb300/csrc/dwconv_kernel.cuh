@@ -1,7 +1,7 @@
 // Depthwise Conv2D tiled kernel (internal header): the unit-stride kernel for
 // 3x3 and 5x5 filters, shared by dwconv.cu (3x3 table variants),
-// dwconv_alu.cu (3x3 closed forms), dwconv_k5.cu (5x5) and dwconv_s2.cu (its
-// packing helpers).  See dwconv.cu for the operation and the design.
+// dwconv_alu.cu (3x3 closed forms), dwconv_k5.cu (5x5 table variants),
+// dwconv_k5_alu.cu (5x5 closed forms) and dwconv_s2.cu (its packing helpers).  See dwconv.cu for the operation and the design.
 #pragma once
 
 #include "gemm_tma.cuh"
@@ -352,26 +352,26 @@ __device__ __forceinline__ void dw_pack_box_alu(const float *raw, uint32_t *dst,
 //  path), then added.  Exact: one fp32 FMA of the two truncated values.
 //  Both products are exact and equal the table path's v * s, and the
 //  accumulation order is the table path's: results are bit-identical.
-template <int ALU>
-__device__ __forceinline__ void dw_taps_alu(float2 (&acc)[kDwRB], const uint32_t *xr, int tw, const uint32_t (&wv)[9])
+template <int ALU, int KS = 3>
+__device__ __forceinline__ void dw_taps_alu(float2 (&acc)[kDwRB], const uint32_t *xr, int tw,
+                                            const uint32_t (&wv)[KS * KS])
 {
 #pragma unroll
     for (int i = 0; i < kDwRB; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int hh = 0; hh < kDwRB + 2; ++hh) {
-        const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + hh * tw);
-        const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + hh * tw + 2);
-        const uint32_t px[4] = {a01.x, a01.y, a23.x, a23.y};
-        uint32_t sb[4];
+    for (int hh = 0; hh < kDwRB + KS - 1; ++hh) {
+        uint32_t px[KS + 1];
+        dw_row<KS>(xr + hh * tw, px);
+        uint32_t sb[KS + 1];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sb[k] = px[k] & 0xFF800000u;
+        for (int k = 0; k < KS + 1; ++k) sb[k] = px[k] & 0xFF800000u;
 #pragma unroll
-        for (int r = 0; r < 3; ++r) {
+        for (int r = 0; r < KS; ++r) {
             const int i = hh - r;
             if (i < 0 || i >= kDwRB) continue;
 #pragma unroll
-            for (int s = 0; s < 3; ++s) {
-                const int t = r * 3 + s;
+            for (int s = 0; s < KS; ++s) {
+                const int t = r * KS + s;
                 if constexpr (ALU == 1) {
                     const float2 w = make_float2(__uint_as_float(wv[t] + px[s] - sb[s]),
                                                  __uint_as_float(wv[t] + px[s + 1] - sb[s + 1]));
@@ -389,8 +389,9 @@ __device__ __forceinline__ void dw_taps_alu(float2 (&acc)[kDwRB], const uint32_t
 
 // Weight-gradient products in closed form for one channel and lane (x the
 // value operand, dy the fraction-and-scale operand for Mitchell).
-template <int ALU>
-__device__ __forceinline__ void dw_filter_alu(float2 (&acc)[9], const uint32_t *xr, int tw, const uint32_t *dr, int tq)
+template <int ALU, int KS = 3>
+__device__ __forceinline__ void dw_filter_alu(float2 (&acc)[KS * KS], const uint32_t *xr, int tw, const uint32_t *dr,
+                                              int tq)
 {
 #pragma unroll
     for (int i = 0; i < kDwRB; ++i) {
@@ -400,13 +401,12 @@ __device__ __forceinline__ void dw_filter_alu(float2 (&acc)[9], const uint32_t *
         const float2 sd = make_float2(__uint_as_float(db0), __uint_as_float(db1));
         const float2 dv = make_float2(__uint_as_float(d01.x), __uint_as_float(d01.y));
 #pragma unroll
-        for (int r = 0; r < 3; ++r) {
-            const uint2 a01 = *reinterpret_cast<const uint2 *>(xr + (i + r) * tw);
-            const uint2 a23 = *reinterpret_cast<const uint2 *>(xr + (i + r) * tw + 2);
-            const uint32_t px[4] = {a01.x, a01.y, a23.x, a23.y};
+        for (int r = 0; r < KS; ++r) {
+            uint32_t px[KS + 1];
+            dw_row<KS>(xr + (i + r) * tw, px);
 #pragma unroll
-            for (int s = 0; s < 3; ++s) {
-                const int t = r * 3 + s;
+            for (int s = 0; s < KS; ++s) {
+                const int t = r * KS + s;
                 if constexpr (ALU == 1) {
                     const float2 w = make_float2(__uint_as_float(px[s] + od0), __uint_as_float(px[s + 1] + od1));
                     acc[t] = fadd2(acc[t], fmul2_ftz(w, sd));
@@ -434,7 +434,6 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
     extern __shared__ __align__(128) uint8_t smem[];
     using Cfg = DwCfg<MODE, KS>;
     constexpr int CB = Cfg::CB, CPW = Cfg::CPW, KK = Cfg::KK, CP = Cfg::CP;
-    static_assert(KS == 3 || ALU == 0, "closed forms are built for 3x3 filters");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // tile shape: compile-time for the widest (8 x 64) tiles, else from the launch
     const int lq_shift = WIDE ? 5 : p.lq_shift, tq_shift = WIDE ? 6 : p.tq_shift;
@@ -565,10 +564,10 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
                 const uint32_t *dr = dyt + c * kDwOP + rb * kDwRB * tq + 2 * lc;
                 if constexpr (ALU != 0) {
                     if (slow)
-                        dw_filter_channel<W, true, true>(facc[ci], xr, tw, dr, tq, glut, rows_ok, ok0, ok1,
-                                                         p.expand_mul);
+                        dw_filter_channel<W, true, true, KS>(facc[ci], xr, tw, dr, tq, glut, rows_ok, ok0, ok1,
+                                                             p.expand_mul);
                     else
-                        dw_filter_alu<ALU>(facc[ci], xr, tw, dr, tq);
+                        dw_filter_alu<ALU, KS>(facc[ci], xr, tw, dr, tq);
                 } else {
                     if (slow)
                         dw_filter_channel<W, true, false, KS>(facc[ci], xr, tw, dr, tq, lut, rows_ok, ok0, ok1,
@@ -593,12 +592,12 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_tile_kernel(const __grid_con
                 const uint32_t *xr = xt + c * CP + rb * kDwRB * tw + 2 * lc;
                 if constexpr (ALU != 0) {
                     if (slow) {
-                        dw_taps_channel<W, true, true>(acc[ci], xr, tw, glut, woff, wsc, p.expand_mul);
+                        dw_taps_channel<W, true, true, KS>(acc[ci], xr, tw, glut, woff, wsc, p.expand_mul);
                     } else {
-                        uint32_t wv[9];
+                        uint32_t wv[KK];
 #pragma unroll
-                        for (int k = 0; k < 9; ++k) wv[k] = wt_val[c * 9 + k];
-                        dw_taps_alu<ALU>(acc[ci], xr, tw, wv);
+                        for (int k = 0; k < KK; ++k) wv[k] = wt_val[c * KK + k];
+                        dw_taps_alu<ALU, KS>(acc[ci], xr, tw, wv);
                     }
                 } else {
                     if (slow)

@@ -151,10 +151,9 @@ int amsim_lut_info(amsim_lut_t lut, int *M, int *width_bits, int *shift);
  *                   carry into the exponent is Mitchell's 2(x+y) branch);
  *   AMSIM_EXACT:    (1 + qa/2^M) * (1 + qb/2^M) rounded to fp32 (exact, M <= 11).
  * Both equal the table's entries bit for bit, so results are identical to the
- * table's for the same plan.  Depthwise launches of 3x3 filters on the
- * tiled kernels (AMSIM_PATH_DW_TILES, stride 1 or 2) use them too; launches
- * on other kernel paths (including the 5x5 depthwise kernel) keep reading the
- * table.  Such launches add AMSIM_PATH_CLOSED_FORM to the path bits.  The
+ * table's for the same plan.  Depthwise launches on the tiled kernels
+ * (AMSIM_PATH_DW_TILES: 3x3 at stride 1 or 2, 5x5 at stride 1) use them too;
+ * launches on other kernel paths keep reading the table.  Such launches add AMSIM_PATH_CLOSED_FORM to the path bits.  The
  * setting belongs to the handle: calls enqueued after it changes see the new
  * setting.  Errors: AMSIM_EINVAL for a null handle; AMSIM_EUNSUPPORTED when
  * on != 0 and the handle was built from entries or a function.

@@ -292,14 +292,14 @@ def test_dwconv_mobilenet_layer_full_size(amd, orc, luts):
 @pytest.mark.parametrize("kind", ["mitchell", "exact"])
 def test_dwconv_closed_form_equals_table(amd, orc, kind):
     """Closed-form products (amsim_lut_set_closed_form) in the tiled kernels
-    (3x3 at stride 1, and the three stride-2 kernels) give the table path's
+    (3x3 and 5x5 at stride 1, and the three stride-2 kernels) give the table path's
     results bit for bit, on ordinary operands and on tiles with special or
     tiny (nonzero, below 2^-63) values, which take the slow computation; and
     they stay within the oracle's tolerance."""
     lut_t = amd.Lut.build(kind, 7)
     lut_c = amd.Lut.build(kind, 7).set_closed_form(True)
     try:
-        for g in (TILED[0], TILED[1], TILED[4], STRIDE2[0], STRIDE2[1], STRIDE2[4]):
+        for g in (TILED[0], TILED[1], TILED[4], TILED5[0], TILED5[1], STRIDE2[0], STRIDE2[1], STRIDE2[4]):
             for specials in (False, True):
                 rng = np.random.default_rng(11 + sum(g[:7]) + specials)
                 x, w, dy = operands(orc, g, rng)
@@ -319,17 +319,13 @@ def test_dwconv_closed_form_equals_table(amd, orc, kind):
                     both_nan = np.isnan(a) & np.isnan(b)
                     assert np.array_equal(ba[~both_nan], bb[~both_nan]), (kind, g, specials, PASSES[which])
                     assert np.array_equal(np.isnan(a), np.isnan(b))
+                    if specials and g[5] == 5:
+                        # 25 products near the top of the fp32 range: a partial sum may overflow to an
+                        # infinity in one summation order and not in another, then meet the opposite
+                        # infinity (a NaN in one order only); the bit-identity above is the check here
+                        continue
                     ref, sa = oracle_pass(orc, kind, 7, which, desc, *args[which], b.size)
                     assert_close(b.reshape(-1), ref, sa, f"closed form {kind} {PASSES[which]} {g}")
-        # 5x5 filters have no closed-form variant: the table path runs, with the same results
-        g = TILED5[0]
-        rng = np.random.default_rng(12)
-        x, w, dy = operands(orc, g, rng)
-        desc, P, Q = dims(orc, g)
-        a, pa = run_dw(amd, lut_t, 0, g, x, w, out_shape(g, P, Q, 0))
-        b, pb = run_dw(amd, lut_c, 0, g, x, w, out_shape(g, P, Q, 0))
-        assert pb & amd.AMSIM_PATH_DW_TILES and not pb & amd.AMSIM_PATH_CLOSED_FORM, pb
-        assert np.array_equal(bits(a), bits(b))
     finally:
         lut_t.close()
         lut_c.close()
