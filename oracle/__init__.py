@@ -11,6 +11,12 @@ DNN Training and Inference", Sec. V-A (Algorithm 1), Sec. V-B (Algorithm 2),
 Sec. VI-B (Algorithms 3 and 4, Fig. 8); depthwise convolution from Sec. III's
 Table I, written as the grouped case of those sums.
 
+A multiplier is named by ``kind`` -- "exact", "mitchell", or a numpy array of
+2^(2M) uint32 table entries (carry << 23 | mantissa, first operand's mantissa
+in the high index bits), e.g. from ``lut_from_fn`` over a user's approx_mul --
+plus ``M`` and the exponent width ``ebits`` (1..8, default 8 = fp32's) of the
+simulated (1, e, M) format (Sec. V-B, last paragraph).
+
 Parity unpinned: nothing.  Every function here has a pin in
 ``tests/test_oracle_*.py`` (see the module docstrings there).
 """
@@ -25,6 +31,7 @@ import numpy as np
 
 EXACT = 0
 MITCHELL = 1
+TABLE = 2
 KINDS = {"exact": EXACT, "mitchell": MITCHELL}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +40,13 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libamsim_oracle.so")
 _lock = threading.Lock()
 _lib = None
+
+USER_FN = ctypes.CFUNCTYPE(ctypes.c_float, ctypes.c_float, ctypes.c_float)
+
+
+class _Mult(ctypes.Structure):
+    """orc_mult: kind, M, exponent bits, table pointer."""
+    _fields_ = [("kind", ctypes.c_int), ("M", ctypes.c_int), ("E", ctypes.c_int), ("table", ctypes.c_void_p)]
 
 
 def build(force: bool = False) -> str:
@@ -66,16 +80,21 @@ def lib():
             L.orc_lut.restype = i32
             L.orc_amsim_bits.argtypes = [i32, i32, u32, u32]
             L.orc_amsim_bits.restype = u32
-            L.orc_mul.argtypes = [i32, i32, vp, vp, vp, i64]
-            L.orc_mul.restype = None
-            L.orc_gemm_rows.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, vp, i64, vp, i64,
+            L.orc_lut_from_fn.argtypes = [USER_FN, i32, vp]
+            L.orc_lut_from_fn.restype = i32
+            mp = ctypes.POINTER(_Mult)
+            L.orc_amsim_mult_bits.argtypes = [mp, u32, u32]
+            L.orc_amsim_mult_bits.restype = u32
+            L.orc_mul.argtypes = [mp, vp, vp, vp, i64]
+            L.orc_mul.restype = i32
+            L.orc_gemm_rows.argtypes = [mp, i32, i32, i32, i32, i32, f64, vp, i64, vp, i64,
                                         f64, vp, i64, vp, i32, vp, vp, i32]
             L.orc_gemm_rows.restype = i32
             for name in ("orc_conv2d_fwd_points", "orc_conv2d_bwd_data_points",
                          "orc_conv2d_bwd_filter_points", "orc_dwconv2d_fwd_points",
                          "orc_dwconv2d_bwd_data_points", "orc_dwconv2d_bwd_filter_points"):
                 fn = getattr(L, name)
-                fn.argtypes = [i32, i32, vp, vp, vp, vp, i64, vp, vp, i32]
+                fn.argtypes = [mp, vp, vp, vp, vp, i64, vp, vp, i32]
                 fn.restype = i32
             L.orc_conv2d_out_hw.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             L.orc_conv2d_out_hw.restype = i32
@@ -85,6 +104,19 @@ def lib():
 
 def _kind(kind) -> int:
     return KINDS[kind] if isinstance(kind, str) else int(kind)
+
+
+def mult(kind, M: int, ebits: int = 8):
+    """The orc_mult for a closed-form kind or a table of entries (kept alive by
+    the returned struct)."""
+    if isinstance(kind, np.ndarray):
+        table = np.ascontiguousarray(kind, dtype=np.uint32)
+        if table.size != 1 << (2 * M):
+            raise ValueError(f"a table for M={M} has {1 << (2 * M)} entries, not {table.size}")
+        mu = _Mult(TABLE, M, ebits, table.ctypes.data)
+        mu._table = table
+        return mu
+    return _Mult(_kind(kind), M, ebits, None)
 
 
 def _f32(a) -> np.ndarray:
@@ -123,23 +155,37 @@ def lut(kind, M: int) -> np.ndarray:
     return out
 
 
-def amsim_bits(kind, M: int, a_bits: int, b_bits: int) -> int:
-    return int(lib().orc_amsim_bits(_kind(kind), M, a_bits & 0xFFFFFFFF, b_bits & 0xFFFFFFFF))
+def lut_from_fn(approx_mul, M: int) -> np.ndarray:
+    """Algorithm 1 over a user's approx_mul(A, B) -> C (a Python callable on
+    fp32 values, called through a C function pointer): 2^(2M) u32 entries."""
+    out = np.zeros(1 << (2 * M) if 1 <= M <= 11 else 1, dtype=np.uint32)
+    cb = USER_FN(approx_mul)
+    rc = lib().orc_lut_from_fn(cb, M, _ptr(out))
+    if rc:
+        raise ValueError(f"orc_lut_from_fn rc={rc}")
+    return out
 
 
-def mul(kind, M: int, a, b) -> np.ndarray:
+def amsim_bits(kind, M: int, a_bits: int, b_bits: int, ebits: int = 8) -> int:
+    return int(lib().orc_amsim_mult_bits(ctypes.byref(mult(kind, M, ebits)), a_bits & 0xFFFFFFFF,
+                                         b_bits & 0xFFFFFFFF))
+
+
+def mul(kind, M: int, a, b, ebits: int = 8) -> np.ndarray:
     """Elementwise AMSim products (bit patterns exactly as Algorithm 2 gives)."""
     a = _f32(a)
     b = _f32(b)
     assert a.shape == b.shape
     c = np.empty_like(a)
-    lib().orc_mul(_kind(kind), M, _ptr(a), _ptr(b), _ptr(c), a.size)
+    mu = mult(kind, M, ebits)
+    if lib().orc_mul(ctypes.byref(mu), _ptr(a), _ptr(b), _ptr(c), a.size):
+        raise ValueError("orc_mul: invalid multiplier")
     return c
 
 
 # ---------------------------------------------------------------- contractions
 def gemm(kind, M: int, A, B, *, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None,
-         rows=None, nthreads=None):
+         rows=None, nthreads=None, ebits: int = 8):
     """Row-major C = alpha*op(A)op(B) + beta*C0 for the listed rows.
 
     Returns (out[nrows, n] float32, sumabs[nrows, n] float64) where sumabs is
@@ -162,7 +208,8 @@ def gemm(kind, M: int, A, B, *, transA=False, transB=False, alpha=1.0, beta=0.0,
     else:
         ldc, c0p = 0, None
         assert beta == 0.0
-    rc = lib().orc_gemm_rows(_kind(kind), M, int(transA), int(transB), m, n, k, float(alpha),
+    mu = mult(kind, M, ebits)
+    rc = lib().orc_gemm_rows(ctypes.byref(mu), int(transA), int(transB), m, n, k, float(alpha),
                              _ptr(A), A.shape[1], _ptr(B), B.shape[1], float(beta), c0p, ldc,
                              _ptr(rows), rows.size, _ptr(out), _ptr(sa),
                              nthreads or default_threads())
@@ -185,49 +232,50 @@ def conv_out_hw(desc) -> tuple[int, int]:
     return P.value, Q.value
 
 
-def _conv(fn_name, kind, M, desc, t0, t1, pts, nthreads):
+def _conv(fn_name, kind, M, desc, t0, t1, pts, nthreads, ebits=8):
     desc = np.ascontiguousarray(desc, dtype=np.int32)
     t0 = _f32(t0)
     t1 = _f32(t1)
     pts = np.ascontiguousarray(pts, dtype=np.int64)
     out = np.empty(pts.size, dtype=np.float32)
     sa = np.empty(pts.size, dtype=np.float64)
-    rc = getattr(lib(), fn_name)(_kind(kind), M, _ptr(desc), _ptr(t0), _ptr(t1), _ptr(pts), pts.size,
+    mu = mult(kind, M, ebits)
+    rc = getattr(lib(), fn_name)(ctypes.byref(mu), _ptr(desc), _ptr(t0), _ptr(t1), _ptr(pts), pts.size,
                                  _ptr(out), _ptr(sa), nthreads or default_threads())
     if rc:
         raise ValueError(f"{fn_name} rc={rc}")
     return out, sa
 
 
-def conv2d_fwd(kind, M, desc, x, w, pts, nthreads=None):
+def conv2d_fwd(kind, M, desc, x, w, pts, nthreads=None, ebits=8):
     """Y (NPQK) at flat indices pts: sum over (r,s,c) of AMSim(x, w)."""
-    return _conv("orc_conv2d_fwd_points", kind, M, desc, x, w, pts, nthreads)
+    return _conv("orc_conv2d_fwd_points", kind, M, desc, x, w, pts, nthreads, ebits)
 
 
-def conv2d_bwd_data(kind, M, desc, dy, w, pts, nthreads=None):
+def conv2d_bwd_data(kind, M, desc, dy, w, pts, nthreads=None, ebits=8):
     """dX (NHWC) at flat indices pts: sum over (r,s,k) of AMSim(dy, w)."""
-    return _conv("orc_conv2d_bwd_data_points", kind, M, desc, dy, w, pts, nthreads)
+    return _conv("orc_conv2d_bwd_data_points", kind, M, desc, dy, w, pts, nthreads, ebits)
 
 
-def conv2d_bwd_filter(kind, M, desc, x, dy, pts, nthreads=None):
+def conv2d_bwd_filter(kind, M, desc, x, dy, pts, nthreads=None, ebits=8):
     """dW (RSCK) at flat indices pts: sum over (n,p,q) of AMSim(x, dy)."""
-    return _conv("orc_conv2d_bwd_filter_points", kind, M, desc, x, dy, pts, nthreads)
+    return _conv("orc_conv2d_bwd_filter_points", kind, M, desc, x, dy, pts, nthreads, ebits)
 
 
-def dwconv2d_fwd(kind, M, desc, x, w, pts, nthreads=None):
+def dwconv2d_fwd(kind, M, desc, x, w, pts, nthreads=None, ebits=8):
     """Depthwise Y (NPQK, K = C*D) at flat indices pts: sum over (r,s) of
     AMSim(x[..., c], w[r,s,c,d]) for output channel k = c*D + d; w is RSCD."""
-    return _conv("orc_dwconv2d_fwd_points", kind, M, desc, x, w, pts, nthreads)
+    return _conv("orc_dwconv2d_fwd_points", kind, M, desc, x, w, pts, nthreads, ebits)
 
 
-def dwconv2d_bwd_data(kind, M, desc, dy, w, pts, nthreads=None):
+def dwconv2d_bwd_data(kind, M, desc, dy, w, pts, nthreads=None, ebits=8):
     """Depthwise dX (NHWC) at flat indices pts: sum over (r,s,d) of AMSim(dy, w)."""
-    return _conv("orc_dwconv2d_bwd_data_points", kind, M, desc, dy, w, pts, nthreads)
+    return _conv("orc_dwconv2d_bwd_data_points", kind, M, desc, dy, w, pts, nthreads, ebits)
 
 
-def dwconv2d_bwd_filter(kind, M, desc, x, dy, pts, nthreads=None):
+def dwconv2d_bwd_filter(kind, M, desc, x, dy, pts, nthreads=None, ebits=8):
     """Depthwise dW (RSCD) at flat indices pts: sum over (n,p,q) of AMSim(x, dy)."""
-    return _conv("orc_dwconv2d_bwd_filter_points", kind, M, desc, x, dy, pts, nthreads)
+    return _conv("orc_dwconv2d_bwd_filter_points", kind, M, desc, x, dy, pts, nthreads, ebits)
 
 
 # ---------------------------------------------------------------- attention
@@ -247,11 +295,11 @@ def softmax_rows_backward(P, dP) -> np.ndarray:
     return P * (dP - (P * dP).sum(axis=-1, keepdims=True))
 
 
-def attention_scores(kind, M, Q, K, scale, rows=None, nthreads=None):
+def attention_scores(kind, M, Q, K, scale, rows=None, nthreads=None, ebits=8):
     """S = scale * Q K^T for one (batch, head) slice, AMSim products (q, k)."""
-    return gemm(kind, M, Q, K, transB=True, alpha=scale, rows=rows, nthreads=nthreads)
+    return gemm(kind, M, Q, K, transB=True, alpha=scale, rows=rows, nthreads=nthreads, ebits=ebits)
 
 
-def attention_output(kind, M, P, V, rows=None, nthreads=None):
+def attention_output(kind, M, P, V, rows=None, nthreads=None, ebits=8):
     """O = P V for one (batch, head) slice, AMSim products (p, v)."""
-    return gemm(kind, M, P, V, rows=rows, nthreads=nthreads)
+    return gemm(kind, M, P, V, rows=rows, nthreads=nthreads, ebits=ebits)

@@ -30,11 +30,28 @@
  *   23 bits.  Contractions sum the fp32 products in double in natural k order
  *   and round once; padding / non-integral taps are zero operands.
  *
+ * A multiplier is described by an orc_mult: one of the two closed-form
+ * kinds, or a table of 2^(2M) entries (carry << 23 | mantissa) that a user's
+ * approx_mul produced through Algorithm 1 (Sec. V-A: the designer supplies
+ * the C function; Sec. VI: LUTs are loaded at run time), plus the number E of
+ * exponent bits of the simulated (1, E, M) format (Sec. V-B, last paragraph:
+ * E from 1 to 8 given an exponent casting function).  Reading taken for the
+ * casting function: an fp32 operand's exponent is re-biased to the E-bit
+ * format's bias 2^(E-1) - 1 (IEEE convention: biased 0 is zero, all ones is
+ * Inf/NaN); an operand below the format's smallest normal becomes a signed
+ * zero and one above its largest binade a signed infinity; Algorithm 2 then
+ * runs with that bias and that all-ones exponent, and the product's exponent
+ * is re-biased back to fp32's.  E = 8 is fp32 itself (no change).
+ *
  * Parity pins (tests/test_oracle_*.py): LUT byte sizes printed on the page;
  * exact kind == IEEE fp32 product of truncated operands; Mitchell hand values
  * and its log-domain definition; special-value invariants; brute force over
  * all mantissa pairs; GEMM/conv against numpy / torch-CPU float64 routines
- * on inputs where the exact kind is exact.
+ * on inputs where the exact kind is exact; user models through Algorithm 1
+ * (a model computing the exact product gives the exact kind's table and
+ * products bit for bit; an asymmetric model's hand-worked values); E-bit
+ * formats (E = 5 against IEEE half ranges, hand-worked boundaries at E = 4,
+ * the degenerate E = 1).
  */
 #include <math.h>
 #include <pthread.h>
@@ -44,6 +61,16 @@
 
 #define ORC_EXACT 0
 #define ORC_MITCHELL 1
+#define ORC_TABLE 2
+
+/* A simulated multiplier: closed-form kind or stored table, mantissa bits M
+ * (1..11) and exponent bits E (1..8; 8 = fp32's own exponent). */
+typedef struct {
+    int kind;               /* ORC_EXACT, ORC_MITCHELL or ORC_TABLE */
+    int M;
+    int E;
+    const uint32_t *table;  /* ORC_TABLE: entry of (p, q) at index p << M | q */
+} orc_mult;
 
 #define ORC_OK 0
 #define ORC_EINVAL 1
@@ -86,23 +113,47 @@ float orc_approx_mul(int kind, int M, float a, float b)
     return (float)c;
 }
 
+/* A multiplier model in Algorithm 1's terms: approx_mul(A, B) -> C. */
+typedef float (*orc_model_fn)(const void *ctx, float A, float B);
+
+typedef struct { int kind, M; } orc_kind_ctx;
+
+static float kind_model(const void *ctx, float A, float B)
+{
+    const orc_kind_ctx *k = (const orc_kind_ctx *)ctx;
+    return orc_approx_mul(k->kind, k->M, A, B);
+}
+
+/* A user's C function float approx_mul(float, float), as Sec. V-A has it. */
+typedef float (*orc_user_fn)(float, float);
+typedef struct { orc_user_fn fn; } orc_user_ctx;
+
+static float user_model(const void *ctx, float A, float B)
+{
+    return ((const orc_user_ctx *)ctx)->fn(A, B);
+}
+
 /*
  * Algorithm 1 for one mantissa pair (p, q): build A = 1.p and B = 1.q with a
  * non-special exponent (biased 127 for both, so neither the operands nor the
  * product are special), call approx_mul, and detect the carry by comparing the
  * product's real biased exponent with the unnormalised one, eA + eB - 127.
  * Entry = carry << 23 | 23-bit mantissa of C.  Returns ORC_EINVAL when the
- * model's exponent moves by anything other than 0 or +1.
+ * model's exponent moves by anything other than 0 or +1, or when the model
+ * returns a negative product of two positive operands (the sign is Algorithm
+ * 2's XOR, never the table's).
  */
-int orc_lut_entry(int kind, int M, uint32_t p, uint32_t q, uint32_t *entry)
+static int algorithm1_entry(orc_model_fn approx_mul, const void *ctx, int M, uint32_t p, uint32_t q,
+                            uint32_t *entry)
 {
-    if (M < 1 || M > 11 || (kind != ORC_EXACT && kind != ORC_MITCHELL)) return ORC_EINVAL;
+    if (M < 1 || M > 11) return ORC_EINVAL;
     if (p >= (1u << M) || q >= (1u << M)) return ORC_EINVAL;
     uint32_t ea = 127, eb = 127;
     float A = u2f((ea << 23) | (p << (23 - M)));
     float B = u2f((eb << 23) | (q << (23 - M)));
-    float C = orc_approx_mul(kind, M, A, B);
+    float C = approx_mul(ctx, A, B);
     uint32_t uc = f2u(C);
+    if (sign_of(uc)) return ORC_EINVAL;
     int un_normalized_exp = (int)ea + (int)eb - 127;
     int real_exp = (int)bexp_of(uc);
     int carry;
@@ -113,52 +164,139 @@ int orc_lut_entry(int kind, int M, uint32_t p, uint32_t q, uint32_t *entry)
     return ORC_OK;
 }
 
-/* All 2^(2M) entries, row index p (first operand) high, q low. */
-int orc_lut(int kind, int M, uint32_t *out)
+/* All 2^(2M) entries of a model, row index p (first operand) high, q low. */
+static int algorithm1_table(orc_model_fn approx_mul, const void *ctx, int M, uint32_t *out)
 {
     if (M < 1 || M > 11) return ORC_EINVAL;
     uint32_t n = 1u << M;
     for (uint32_t p = 0; p < n; ++p)
         for (uint32_t q = 0; q < n; ++q) {
-            int rc = orc_lut_entry(kind, M, p, q, &out[(p << M) | q]);
+            int rc = algorithm1_entry(approx_mul, ctx, M, p, q, &out[(p << M) | q]);
             if (rc) return rc;
         }
     return ORC_OK;
 }
 
+int orc_lut_entry(int kind, int M, uint32_t p, uint32_t q, uint32_t *entry)
+{
+    if (kind != ORC_EXACT && kind != ORC_MITCHELL) return ORC_EINVAL;
+    orc_kind_ctx k = {kind, M};
+    return algorithm1_entry(kind_model, &k, M, p, q, entry);
+}
+
+int orc_lut(int kind, int M, uint32_t *out)
+{
+    if (kind != ORC_EXACT && kind != ORC_MITCHELL) return ORC_EINVAL;
+    orc_kind_ctx k = {kind, M};
+    return algorithm1_table(kind_model, &k, M, out);
+}
+
+/* Algorithm 1 over a user's approx_mul (the page's LUT-generation script). */
+int orc_lut_from_fn(orc_user_fn approx_mul, int M, uint32_t *out)
+{
+    if (!approx_mul || !out) return ORC_EINVAL;
+    orc_user_ctx u = {approx_mul};
+    return algorithm1_table(user_model, &u, M, out);
+}
+
+static int mult_valid(const orc_mult *mu)
+{
+    if (!mu || mu->M < 1 || mu->M > 11 || mu->E < 1 || mu->E > 8) return 0;
+    if (mu->kind == ORC_TABLE) return mu->table != NULL;
+    return mu->kind == ORC_EXACT || mu->kind == ORC_MITCHELL;
+}
+
+/* The LUT entry of mantissa pair (qa, qb): read from the stored table, or
+ * formed from the closed form through Algorithm 1. */
+static int mult_entry(const orc_mult *mu, uint32_t qa, uint32_t qb, uint32_t *entry)
+{
+    if (mu->kind == ORC_TABLE) {
+        *entry = mu->table[(qa << mu->M) | qb];
+        return (*entry >> 24) ? ORC_EINVAL : ORC_OK;
+    }
+    return orc_lut_entry(mu->kind, mu->M, qa, qb, entry);
+}
+
+/* Operand classes after the exponent cast to the E-bit format. */
+enum { CL_ZERO, CL_NORMAL, CL_INF, CL_NAN };
+
 /*
- * Algorithm 2 (AMSim) on fp32 bit patterns, with the entry taken from the
- * closed form through Algorithm 1 instead of a stored table.
+ * The exponent casting function (reading stated in the header): fp32 operand
+ * -> class and biased exponent of the (1, E, M) format with bias 2^(E-1) - 1.
+ * Zero and denormal fp32 inputs are zero; fp32 Inf/NaN stay Inf/NaN; a normal
+ * input whose re-biased exponent is not above zero is zero, one that reaches
+ * the all-ones exponent 2^E - 1 is Inf.
  */
-uint32_t orc_amsim_bits(int kind, int M, uint32_t a, uint32_t b)
+static int cast_operand(uint32_t x, int E, int *cexp)
+{
+    const int bias = (1 << (E - 1)) - 1;
+    const int all_ones = (1 << E) - 1;
+    uint32_t ex = bexp_of(x);
+    if (ex == 255) return frac_of(x) ? CL_NAN : CL_INF;
+    if (ex == 0) return CL_ZERO;
+    int c = (int)ex - 127 + bias;
+    if (c <= 0) return CL_ZERO;
+    if (c >= all_ones) return CL_INF;
+    *cexp = c;
+    return CL_NORMAL;
+}
+
+/*
+ * Algorithm 2 (AMSim) on fp32 bit patterns for a (1, E, M) multiplier:
+ * sign XOR; index from the concatenated top-M mantissas; carry and mantissa
+ * from the entry; e0 = eA + eB - bias; zero if e0 <= 0 or an input is zero;
+ * Inf if e0 >= 2^E - 1; otherwise e = e0 + carry (Inf again if that reaches
+ * 2^E - 1); the exponent is re-biased to fp32's for the result.
+ */
+static uint32_t algorithm2(const orc_mult *mu, uint32_t a, uint32_t b)
 {
     const uint32_t QNAN = 0x7FC00000u;
+    const int M = mu->M;
+    const int bias = (1 << (mu->E - 1)) - 1;
+    const int all_ones = (1 << mu->E) - 1;
     uint32_t s = sign_of(a) ^ sign_of(b);
-    uint32_t ea = bexp_of(a), eb = bexp_of(b);
-    int nan_a = (ea == 255 && frac_of(a) != 0), nan_b = (eb == 255 && frac_of(b) != 0);
-    int inf_a = (ea == 255 && frac_of(a) == 0), inf_b = (eb == 255 && frac_of(b) == 0);
-    int zero_a = (ea == 0), zero_b = (eb == 0); /* zero or denormal */
+    int ea = 0, eb = 0;
+    int ca = cast_operand(a, mu->E, &ea), cb = cast_operand(b, mu->E, &eb);
 
-    if (nan_a || nan_b) return QNAN;
-    if (inf_a || inf_b) {
-        if (zero_a || zero_b) return QNAN;
+    if (ca == CL_NAN || cb == CL_NAN) return QNAN;
+    if (ca == CL_INF || cb == CL_INF) {
+        if (ca == CL_ZERO || cb == CL_ZERO) return QNAN;
         return (s << 31) | 0x7F800000u;
     }
-    if (zero_a || zero_b) return s << 31;
+    if (ca == CL_ZERO || cb == CL_ZERO) return s << 31;
 
     /* Alg. 2: extract the top-M mantissas, concatenate into an index, fetch. */
     uint32_t qa = top_bits(a, M), qb = top_bits(b, M);
     uint32_t entry;
-    if (orc_lut_entry(kind, M, qa, qb, &entry) != ORC_OK) return QNAN;
+    if (mult_entry(mu, qa, qb, &entry) != ORC_OK) return QNAN;
     uint32_t carry = entry >> 23;
     uint32_t mant = entry & 0x7FFFFFu;
 
-    int e0 = (int)ea + (int)eb - 127;
-    if (e0 <= 0) return s << 31;                         /* underflow -> zero */
-    if (e0 >= 255) return (s << 31) | 0x7F800000u;       /* overflow -> Inf  */
-    int e = e0 + (int)carry;                             /* normal case      */
-    if (e >= 255) return (s << 31) | 0x7F800000u;
-    return (s << 31) | ((uint32_t)e << 23) | mant;
+    int e0 = ea + eb - bias;
+    if (e0 <= 0) return s << 31;                              /* underflow -> zero */
+    if (e0 >= all_ones) return (s << 31) | 0x7F800000u;       /* overflow -> Inf  */
+    int e = e0 + (int)carry;                                  /* normal case      */
+    if (e >= all_ones) return (s << 31) | 0x7F800000u;
+    return (s << 31) | ((uint32_t)(e - bias + 127) << 23) | mant;
+}
+
+/* AMSim for a closed-form kind with fp32's 8-bit exponent. */
+uint32_t orc_amsim_bits(int kind, int M, uint32_t a, uint32_t b)
+{
+    orc_mult mu = {kind, M, 8, NULL};
+    if (!mult_valid(&mu)) return 0x7FC00000u;
+    return algorithm2(&mu, a, b);
+}
+
+uint32_t orc_amsim_mult_bits(const orc_mult *mu, uint32_t a, uint32_t b)
+{
+    if (!mult_valid(mu)) return 0x7FC00000u;
+    return algorithm2(mu, a, b);
+}
+
+static float amsim(const orc_mult *mu, float a, float b)
+{
+    return u2f(algorithm2(mu, f2u(a), f2u(b)));
 }
 
 float orc_amsim(int kind, int M, float a, float b)
@@ -166,9 +304,11 @@ float orc_amsim(int kind, int M, float a, float b)
     return u2f(orc_amsim_bits(kind, M, f2u(a), f2u(b)));
 }
 
-void orc_mul(int kind, int M, const float *a, const float *b, float *c, int64_t n)
+int orc_mul(const orc_mult *mu, const float *a, const float *b, float *c, int64_t n)
 {
-    for (int64_t i = 0; i < n; ++i) c[i] = orc_amsim(kind, M, a[i], b[i]);
+    if (!mult_valid(mu)) return ORC_EINVAL;
+    for (int64_t i = 0; i < n; ++i) c[i] = amsim(mu, a[i], b[i]);
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -213,12 +353,12 @@ static void orc_parallel(orc_item_fn fn, void *ctx, int64_t n, int nthreads)
 
 /* ------------------------------------------------------------------------ */
 /* GEMM (row-major): C = alpha * op(A) op(B) + beta * C0, every product an
- * AMSim product with A's element as the first operand.  Only the listed rows
+ * AMSim product of the multiplier `mu` with A's element as the first operand.  Only the listed rows
  * of C are produced: out[r*n + j] for r < nrows, plus sumabs = alpha-free
  * sum over k of |product|.  transA: A is stored k x m; transB: B is n x k.  */
 
 typedef struct {
-    int kind, M;
+    orc_mult mu;
     int ta, tb, m, n, k;
     double alpha, beta;
     const float *A; int64_t lda;
@@ -237,7 +377,7 @@ static void orc_gemm_row(void *vctx, int64_t r)
         for (int kk = 0; kk < g->k; ++kk) {
             float a = g->ta ? g->A[(int64_t)kk * g->lda + i] : g->A[(int64_t)i * g->lda + kk];
             float b = g->tb ? g->B[(int64_t)j * g->ldb + kk] : g->B[(int64_t)kk * g->ldb + j];
-            float p = orc_amsim(g->kind, g->M, a, b);
+            float p = amsim(&g->mu, a, b);
             s += (double)p;
             sa += fabs((double)p);
         }
@@ -248,15 +388,15 @@ static void orc_gemm_row(void *vctx, int64_t r)
     }
 }
 
-int orc_gemm_rows(int kind, int M, int transA, int transB, int m, int n, int k,
+int orc_gemm_rows(const orc_mult *mu, int transA, int transB, int m, int n, int k,
                   double alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
                   double beta, const float *C0, int64_t ldc,
                   const int *rows, int nrows, float *out, double *sumabs, int nthreads)
 {
-    if (M < 1 || M > 11 || m < 0 || n < 0 || k < 0 || nrows < 0) return ORC_EINVAL;
+    if (!mult_valid(mu) || m < 0 || n < 0 || k < 0 || nrows < 0) return ORC_EINVAL;
     for (int r = 0; r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= m) return ORC_EINVAL;
-    orc_gemm_ctx g = {kind, M, transA, transB, m, n, k, alpha, beta,
+    orc_gemm_ctx g = {*mu, transA, transB, m, n, k, alpha, beta,
                       A, lda, B, ldb, C0, ldc, rows, out, sumabs};
     orc_parallel(orc_gemm_row, &g, nrows, nthreads);
     return ORC_OK;
@@ -287,7 +427,7 @@ static int orc_conv_init(const int *d, orc_conv *c)
 }
 
 typedef struct {
-    int kind, M;
+    orc_mult mu;
     orc_conv c;
     const float *x, *w, *dy;
     const int64_t *pts;
@@ -316,7 +456,7 @@ static void orc_fwd_pt(void *vctx, int64_t t)
             for (int ch = 0; ch < c->C; ++ch) {
                 float a = x_at(c, g->x, n, p * c->sh - c->ph + r * c->dh, q * c->sw - c->pw + ss * c->dw, ch);
                 float b = g->w[(((int64_t)r * c->S + ss) * c->C + ch) * c->K + k];
-                float pr = orc_amsim(g->kind, g->M, a, b);
+                float pr = amsim(&g->mu, a, b);
                 s += (double)pr; sa += fabs((double)pr);
             }
     g->out[t] = (float)s;
@@ -346,7 +486,7 @@ static void orc_bwd_data_pt(void *vctx, int64_t t)
                         a = g->dy[(((int64_t)n * c->P + p) * c->Q + q) * c->K + k];
                 }
                 float b = g->w[(((int64_t)r * c->S + ss) * c->C + ch) * c->K + k];
-                float pr = orc_amsim(g->kind, g->M, a, b);
+                float pr = amsim(&g->mu, a, b);
                 s += (double)pr; sa += fabs((double)pr);
             }
     g->out[t] = (float)s;
@@ -369,19 +509,19 @@ static void orc_bwd_filter_pt(void *vctx, int64_t t)
             for (int q = 0; q < c->Q; ++q) {
                 float a = x_at(c, g->x, n, p * c->sh - c->ph + r * c->dh, q * c->sw - c->pw + ss * c->dw, ch);
                 float b = g->dy[(((int64_t)n * c->P + p) * c->Q + q) * c->K + k];
-                float pr = orc_amsim(g->kind, g->M, a, b);
+                float pr = amsim(&g->mu, a, b);
                 s += (double)pr; sa += fabs((double)pr);
             }
     g->out[t] = (float)s;
     if (g->sumabs) g->sumabs[t] = sa;
 }
 
-static int orc_conv_run(int which, int kind, int M, const int *desc,
+static int orc_conv_run(int which, const orc_mult *mu, const int *desc,
                         const float *x, const float *w, const float *dy,
                         const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
 {
     orc_conv_ctx g;
-    if (M < 1 || M > 11) return ORC_EINVAL;
+    if (!mult_valid(mu)) return ORC_EINVAL;
     if (orc_conv_init(desc, &g.c)) return ORC_EINVAL;
     int64_t total;
     if (which == 0) total = (int64_t)g.c.N * g.c.P * g.c.Q * g.c.K;
@@ -389,28 +529,28 @@ static int orc_conv_run(int which, int kind, int M, const int *desc,
     else total = (int64_t)g.c.R * g.c.S * g.c.C * g.c.K;
     for (int64_t t = 0; t < npts; ++t)
         if (pts[t] < 0 || pts[t] >= total) return ORC_EINVAL;
-    g.kind = kind; g.M = M; g.x = x; g.w = w; g.dy = dy; g.pts = pts; g.out = out; g.sumabs = sumabs;
+    g.mu = *mu; g.x = x; g.w = w; g.dy = dy; g.pts = pts; g.out = out; g.sumabs = sumabs;
     orc_parallel(which == 0 ? orc_fwd_pt : which == 1 ? orc_bwd_data_pt : orc_bwd_filter_pt,
                  &g, npts, nthreads);
     return ORC_OK;
 }
 
-int orc_conv2d_fwd_points(int kind, int M, const int *desc, const float *x, const float *w,
+int orc_conv2d_fwd_points(const orc_mult *mu, const int *desc, const float *x, const float *w,
                           const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
 {
-    return orc_conv_run(0, kind, M, desc, x, w, NULL, pts, npts, out, sumabs, nthreads);
+    return orc_conv_run(0, mu, desc, x, w, NULL, pts, npts, out, sumabs, nthreads);
 }
 
-int orc_conv2d_bwd_data_points(int kind, int M, const int *desc, const float *dy, const float *w,
+int orc_conv2d_bwd_data_points(const orc_mult *mu, const int *desc, const float *dy, const float *w,
                                const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
 {
-    return orc_conv_run(1, kind, M, desc, NULL, w, dy, pts, npts, out, sumabs, nthreads);
+    return orc_conv_run(1, mu, desc, NULL, w, dy, pts, npts, out, sumabs, nthreads);
 }
 
-int orc_conv2d_bwd_filter_points(int kind, int M, const int *desc, const float *x, const float *dy,
+int orc_conv2d_bwd_filter_points(const orc_mult *mu, const int *desc, const float *x, const float *dy,
                                  const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
 {
-    return orc_conv_run(2, kind, M, desc, x, NULL, dy, pts, npts, out, sumabs, nthreads);
+    return orc_conv_run(2, mu, desc, x, NULL, dy, pts, npts, out, sumabs, nthreads);
 }
 
 int orc_conv2d_out_hw(const int *desc, int *P, int *Q)
@@ -448,7 +588,7 @@ static void orc_dw_fwd_pt(void *vctx, int64_t t)
         for (int ss = 0; ss < c->S; ++ss) {
             float a = x_at(c, g->x, n, p * c->sh - c->ph + r * c->dh, q * c->sw - c->pw + ss * c->dw, ch);
             float b = g->w[(((int64_t)r * c->S + ss) * c->C + ch) * D + d];
-            float pr = orc_amsim(g->kind, g->M, a, b);
+            float pr = amsim(&g->mu, a, b);
             s += (double)pr; sa += fabs((double)pr);
         }
     g->out[t] = (float)s;
@@ -477,7 +617,7 @@ static void orc_dw_bwd_data_pt(void *vctx, int64_t t)
                         a = g->dy[(((int64_t)n * c->P + p) * c->Q + q) * c->K + ch * D + d];
                 }
                 float b = g->w[(((int64_t)r * c->S + ss) * c->C + ch) * D + d];
-                float pr = orc_amsim(g->kind, g->M, a, b);
+                float pr = amsim(&g->mu, a, b);
                 s += (double)pr; sa += fabs((double)pr);
             }
     g->out[t] = (float)s;
@@ -500,19 +640,19 @@ static void orc_dw_bwd_filter_pt(void *vctx, int64_t t)
             for (int q = 0; q < c->Q; ++q) {
                 float a = x_at(c, g->x, n, p * c->sh - c->ph + r * c->dh, q * c->sw - c->pw + ss * c->dw, ch);
                 float b = g->dy[(((int64_t)n * c->P + p) * c->Q + q) * c->K + ch * D + d];
-                float pr = orc_amsim(g->kind, g->M, a, b);
+                float pr = amsim(&g->mu, a, b);
                 s += (double)pr; sa += fabs((double)pr);
             }
     g->out[t] = (float)s;
     if (g->sumabs) g->sumabs[t] = sa;
 }
 
-static int orc_dw_run(int which, int kind, int M, const int *desc,
+static int orc_dw_run(int which, const orc_mult *mu, const int *desc,
                       const float *x, const float *w, const float *dy,
                       const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
 {
     orc_conv_ctx g;
-    if (M < 1 || M > 11) return ORC_EINVAL;
+    if (!mult_valid(mu)) return ORC_EINVAL;
     if (orc_conv_init(desc, &g.c)) return ORC_EINVAL;
     if (g.c.K % g.c.C) return ORC_EINVAL;
     int64_t total;
@@ -521,26 +661,26 @@ static int orc_dw_run(int which, int kind, int M, const int *desc,
     else total = (int64_t)g.c.R * g.c.S * g.c.K;
     for (int64_t t = 0; t < npts; ++t)
         if (pts[t] < 0 || pts[t] >= total) return ORC_EINVAL;
-    g.kind = kind; g.M = M; g.x = x; g.w = w; g.dy = dy; g.pts = pts; g.out = out; g.sumabs = sumabs;
+    g.mu = *mu; g.x = x; g.w = w; g.dy = dy; g.pts = pts; g.out = out; g.sumabs = sumabs;
     orc_parallel(which == 0 ? orc_dw_fwd_pt : which == 1 ? orc_dw_bwd_data_pt : orc_dw_bwd_filter_pt,
                  &g, npts, nthreads);
     return ORC_OK;
 }
 
-int orc_dwconv2d_fwd_points(int kind, int M, const int *desc, const float *x, const float *w,
+int orc_dwconv2d_fwd_points(const orc_mult *mu, const int *desc, const float *x, const float *w,
                             const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
 {
-    return orc_dw_run(0, kind, M, desc, x, w, NULL, pts, npts, out, sumabs, nthreads);
+    return orc_dw_run(0, mu, desc, x, w, NULL, pts, npts, out, sumabs, nthreads);
 }
 
-int orc_dwconv2d_bwd_data_points(int kind, int M, const int *desc, const float *dy, const float *w,
+int orc_dwconv2d_bwd_data_points(const orc_mult *mu, const int *desc, const float *dy, const float *w,
                                  const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
 {
-    return orc_dw_run(1, kind, M, desc, NULL, w, dy, pts, npts, out, sumabs, nthreads);
+    return orc_dw_run(1, mu, desc, NULL, w, dy, pts, npts, out, sumabs, nthreads);
 }
 
-int orc_dwconv2d_bwd_filter_points(int kind, int M, const int *desc, const float *x, const float *dy,
+int orc_dwconv2d_bwd_filter_points(const orc_mult *mu, const int *desc, const float *x, const float *dy,
                                    const int64_t *pts, int64_t npts, float *out, double *sumabs, int nthreads)
 {
-    return orc_dw_run(2, kind, M, desc, x, NULL, dy, pts, npts, out, sumabs, nthreads);
+    return orc_dw_run(2, mu, desc, x, NULL, dy, pts, npts, out, sumabs, nthreads);
 }

@@ -8,8 +8,9 @@ mistakes are the kinds a restatement of Algorithms 1-2 (ApproxTrain Sec. V-A,
 V-B) and of the convolution sums (Sec. VI-B, Algorithms 3-4; depthwise from
 Sec. III, Table I) is likely to contain: an exponent bias, a dropped carry, the
 zero test's boundary, Mitchell's branch, truncation vs rounding, denormals,
-transposes, dilation and flip indices, channel-multiplier indexing, and the
-tolerance scale.
+transposes, dilation and flip indices, channel-multiplier indexing, the
+tolerance scale, a user table's index order and carry, Algorithm 1's carry
+detection over a user model, and the exponent cast of (1, e, m) formats.
 """
 import importlib.util
 import os
@@ -32,6 +33,8 @@ def _load_test_module(name):
 
 T_AMSIM = _load_test_module("test_oracle_amsim")
 T_CONTR = _load_test_module("test_oracle_contractions")
+T_USER = _load_test_module("test_oracle_usermodels")
+T_FMT = _load_test_module("test_oracle_formats")
 
 
 def _function_span(src, fname):
@@ -66,16 +69,16 @@ def _dw_geom(i):
 
 # name: (function, old text, new text, pins that should catch it)
 MUTANTS = {
-    "exponent_bias": ("orc_amsim_bits", "int e0 = (int)ea + (int)eb - 127;", "int e0 = (int)ea + (int)eb - 126;",
+    "exponent_bias": ("algorithm2", "int e0 = ea + eb - bias;", "int e0 = ea + eb - bias + 1;",
                       [T_AMSIM.test_special_values_hand_worked, T_AMSIM.test_mitchell_scaling_in_normal_range]),
-    "dropped_carry": ("orc_amsim_bits", "int e = e0 + (int)carry;", "int e = e0;",
+    "dropped_carry": ("algorithm2", "int e = e0 + (int)carry;", "int e = e0;",
                       [T_AMSIM.test_mitchell_hand_values, T_AMSIM.test_mitchell_scaling_in_normal_range]),
-    "zero_test_boundary": ("orc_amsim_bits", "if (e0 <= 0) return s << 31;", "if (e0 < 0) return s << 31;",
+    "zero_test_boundary": ("algorithm2", "if (e0 <= 0) return s << 31;", "if (e0 < 0) return s << 31;",
                            [T_AMSIM.test_special_values_hand_worked]),
-    "zero_test_after_carry": ("orc_amsim_bits", "if (e0 <= 0) return s << 31;",
+    "zero_test_after_carry": ("algorithm2", "if (e0 <= 0) return s << 31;",
                               "if (e0 + (int)carry <= 0) return s << 31;",
                               [T_AMSIM.test_special_values_hand_worked]),
-    "overflow_via_carry": ("orc_amsim_bits", "if (e >= 255) return (s << 31) | 0x7F800000u;", "",
+    "overflow_via_carry": ("algorithm2", "if (e >= all_ones) return (s << 31) | 0x7F800000u;", "",
                            [T_AMSIM.test_special_values_hand_worked]),
     "mitchell_branch": ("orc_approx_mul", "(x + y < 1.0)", "(x + y < 2.0)",
                         [lambda o: T_AMSIM.test_mitchell_lut_is_log_domain_construction(o, 3)]),
@@ -83,12 +86,12 @@ MUTANTS = {
                          [T_AMSIM.test_mitchell_hand_values]),
     "exact_operand": ("orc_approx_mul", "p = (1.0 + x) * (1.0 + y);", "p = (1.0 + x) * (1.0 + x);",
                       [lambda o: T_AMSIM.test_exact_equals_ieee_product_all_mantissa_pairs(o, 5)]),
-    "index_rounds": ("orc_amsim_bits", "uint32_t qa = top_bits(a, M), qb = top_bits(b, M);",
+    "index_rounds": ("algorithm2", "uint32_t qa = top_bits(a, M), qb = top_bits(b, M);",
                      "uint32_t qa = top_bits(a + (1u << (22 - M)), M), qb = top_bits(b + (1u << (22 - M)), M);",
                      [lambda o: T_AMSIM.test_exact_equals_ieee_product_sampled(o, 9)]),
-    "sign_dropped": ("orc_amsim_bits", "uint32_t s = sign_of(a) ^ sign_of(b);", "uint32_t s = sign_of(a);",
+    "sign_dropped": ("algorithm2", "uint32_t s = sign_of(a) ^ sign_of(b);", "uint32_t s = sign_of(a);",
                      [T_AMSIM.test_mitchell_scaling_in_normal_range]),
-    "denormal_not_zero": ("orc_amsim_bits", "int zero_a = (ea == 0)", "int zero_a = (ea == 0 && frac_of(a) == 0)",
+    "denormal_not_zero": ("cast_operand", "if (ex == 0) return CL_ZERO;", "if (ex == 0) return CL_NORMAL;",
                           [T_AMSIM.test_zero_sign_and_denormals]),
     "gemm_transposed_a": ("orc_gemm_row", "g->ta ? g->A[(int64_t)kk * g->lda + i]",
                           "g->ta ? g->A[(int64_t)i * g->lda + kk]",
@@ -111,11 +114,35 @@ MUTANTS = {
     "dw_bwd_filter_index_order": ("orc_dw_bwd_filter_pt", "int d = (int)(idx % D); idx /= D;\n    int ch = (int)(idx % c->C); idx /= c->C;",
                                   "int ch = (int)(idx % c->C); idx /= c->C;\n    int d = (int)(idx % D); idx /= D;",
                                   [lambda o: T_CONTR.test_dwconv_exact_kind_equals_torch_grouped_float64(o, _dw_geom(1))]),
+    # user models (Algorithm 1 over a caller's approx_mul, Algorithm 2 over a stored table)
+    "table_index_swapped": ("mult_entry", "mu->table[(qa << mu->M) | qb]", "mu->table[(qb << mu->M) | qa]",
+                            [T_USER.test_asymmetric_model_hand_worked]),
+    "table_carry_ignored": ("mult_entry", "*entry = mu->table[(qa << mu->M) | qb];",
+                            "*entry = mu->table[(qa << mu->M) | qb] & 0x7FFFFFu;",
+                            [T_USER.test_table_products_brute_force]),
+    "user_carry_detection": ("algorithm1_entry", "else if (real_exp == un_normalized_exp + 1) carry = 1;",
+                             "else if (real_exp == un_normalized_exp + 1) carry = 0;",
+                             [lambda o: T_USER.test_exact_model_callback_gives_exact_kind(o, 4),
+                              lambda o: T_AMSIM.test_exact_lut_is_integer_normalisation(o, 4)]),
+    "user_negative_allowed": ("algorithm1_entry", "if (sign_of(uc)) return ORC_EINVAL;", "",
+                              [T_USER.test_algorithm1_rejects_models_outside_its_range]),
+    # (1, E, M) formats: the exponent cast and the re-biased Algorithm 2
+    "cast_bias": ("cast_operand", "const int bias = (1 << (E - 1)) - 1;", "const int bias = (1 << (E - 1));",
+                  [T_FMT.test_format_hand_worked]),
+    "cast_underflow_boundary": ("cast_operand", "if (c <= 0) return CL_ZERO;", "if (c < 0) return CL_ZERO;",
+                                [T_FMT.test_format_hand_worked]),
+    "cast_overflow_boundary": ("cast_operand", "if (c >= all_ones) return CL_INF;", "if (c > all_ones) return CL_INF;",
+                               [T_FMT.test_format_hand_worked]),
+    "format_overflow_threshold": ("algorithm2", "const int all_ones = (1 << mu->E) - 1;",
+                                  "const int all_ones = (1 << mu->E);",
+                                  [lambda o: T_FMT.test_half_format_matches_ieee_half_ranges(o, "exact")]),
+    "format_result_not_rebiased": ("algorithm2", "((uint32_t)(e - bias + 127) << 23)", "((uint32_t)e << 23)",
+                                   [lambda o: T_FMT.test_half_format_matches_ieee_half_ranges(o, "exact")]),
 }
 
 
 def test_unmutated_oracle_passes_the_chosen_pins(tmp_path):
-    o = _mutant_oracle(tmp_path, "orc_amsim_bits", "uint32_t s = sign_of(a) ^ sign_of(b);",
+    o = _mutant_oracle(tmp_path, "algorithm2", "uint32_t s = sign_of(a) ^ sign_of(b);",
                        "uint32_t s = sign_of(a) ^ sign_of(b);")
     for _, _, _, pins in MUTANTS.values():
         for pin in pins:
@@ -130,6 +157,6 @@ def test_planted_mistake_fails_a_pin(tmp_path, name):
     for pin in pins:
         try:
             pin(o)
-        except (AssertionError, ValueError):
+        except (AssertionError, ValueError, pytest.fail.Exception):
             failed += 1
     assert failed > 0, f"no pin caught the planted mistake {name}"
