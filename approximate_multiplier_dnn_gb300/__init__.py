@@ -88,6 +88,7 @@ def lib():
         "amsim_lut_generate_from_fn": ([APPROX_MUL_FN, i32, vp], i32),
         "amsim_lut_build": ([i32, i32, ctypes.POINTER(vp)], i32),
         "amsim_lut_build_from_entries": ([vp, i32, ctypes.POINTER(vp)], i32),
+        "amsim_lut_build_from_fn": ([APPROX_MUL_FN, i32, ctypes.POINTER(vp)], i32),
         "amsim_lut_entries": ([vp, vp], i32),
         "amsim_lut_info": ([vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "amsim_lut_set_closed_form": ([vp, i32], i32),
@@ -212,6 +213,10 @@ class Lut:
     def from_entries(cls, entries, M: int) -> "Lut":
         return cls(amsim_lut_build_from_entries(entries, M), M)
 
+    @classmethod
+    def from_fn(cls, approx_mul, M: int) -> "Lut":
+        return cls(amsim_lut_build_from_fn(approx_mul, M), M)
+
     def info(self):
         return amsim_lut_info(self.handle)
 
@@ -264,6 +269,15 @@ def amsim_lut_build_from_entries(entries, M: int) -> int:
     e = np.ascontiguousarray(entries, dtype=np.uint32)
     h = ctypes.c_void_p(0)
     _check("amsim_lut_build_from_entries", lib().amsim_lut_build_from_entries(e.ctypes.data, M, ctypes.byref(h)))
+    return h.value
+
+
+def amsim_lut_build_from_fn(approx_mul, M: int) -> int:
+    """approx_mul: a Python callable (float, float) -> float, called through a C
+    function pointer during the call."""
+    cb = APPROX_MUL_FN(approx_mul)
+    h = ctypes.c_void_p(0)
+    _check("amsim_lut_build_from_fn", lib().amsim_lut_build_from_fn(cb, M, ctypes.byref(h)))
     return h.value
 
 

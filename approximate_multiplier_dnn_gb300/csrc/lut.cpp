@@ -209,6 +209,16 @@ int amsim_lut_build_from_entries(const uint32_t *host_entries, int M, amsim_lut_
     return build_from_entries(host_entries, M, out);
 }
 
+int amsim_lut_build_from_fn(amsim_approx_mul_fn approx_mul, int M, amsim_lut_t *out)
+{
+    if (!out || !approx_mul) return AMSIM_EINVAL;
+    if (M < 1 || M > 11) return AMSIM_EUNSUPPORTED;
+    std::vector<uint32_t> e(size_t(1) << (2 * M));
+    int rc = generate(approx_mul, M, e.data());
+    if (rc) return rc;
+    return build_from_entries(e.data(), M, out);
+}
+
 int amsim_lut_entries(amsim_lut_t lut, uint32_t *host_dst)
 {
     if (!lut || !host_dst) return AMSIM_EINVAL;

@@ -1,10 +1,11 @@
 #!/usr/bin/env python
 """Benchmark of the LUT-multiplier contractions on one GB300 (or N replicas).
 
-Default workload: the 3-layer MLP 784-1000-500-10 at batch 256, forward
-Y = XW plus backward dX = dY W^T and dW = X^T dY for every layer, all products
-through the Mitchell M=7 LUT (989,952,000 approximate MACs per step).  Other
-workloads (--workload) exist for the design tables; they print the same line.
+Default workload: the square GEMM C = A B with A, B 4096 x 4096 ~ U[-1, 1],
+every product through the Mitchell M=7 LUT (68,719,476,736 approximate MACs
+per step), the largest single-GPU configuration of the path.  Other workloads
+(--workload: the MLP step, convolutions, attention, depthwise layers, the
+elementwise product; --mantissa for the M sweep) print the same line.
 
 Prints one JSON line (rank 0).  Timing: W warm-up steps, then K steps, each
 bracketed by CUDA events on the launching stream; before each timed step the
@@ -112,9 +113,10 @@ def make_step(name, lut_for, M=7, kind="mitchell"):
     raise SystemExit(f"unknown workload {name}")
 
 
-def oracle_parts(name):
+def oracle_parts(name, kind="mitchell", M=7):
     """(oracle callable over a row subset, rows, MACs per row) for the reference
-    leg: the same contractions the GPU step runs, one row range at a time."""
+    leg: the same contractions the GPU step runs, one row range at a time
+    (kind and M apply to the gemm4096 sweep)."""
     import numpy as np
     import oracle
     from approximate_multiplier_dnn_gb300 import workloads as wl
@@ -136,7 +138,7 @@ def oracle_parts(name):
         return out
     if name == "gemm4096":
         d = wl.square_gemm(4096)
-        return [(lambda rows: oracle.gemm("mitchell", 7, d["A"], d["B"], rows=rows), 4096, 4096 * 4096)]
+        return [(lambda rows: oracle.gemm(kind, M, d["A"], d["B"], rows=rows), 4096, 4096 * 4096)]
     if name in ("dwconv3x3", "dwconv3x3_s2", "dwconv5x5"):
         # a "row" is a block of 64 consecutive outputs (forward, data gradient)
         # or one filter-gradient element (a sum over every N*P*Q pixel)
@@ -185,9 +187,11 @@ def run_oracle_sample(parts, target_s, nthreads, start=0):
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi samples every 50 ms; stop() keeps those stamped inside the
+    window passed to it (the timed region) when there are any."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_id):
         self.gpu_id = gpu_id
@@ -197,7 +201,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", str(self.gpu_id)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -209,7 +213,17 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    @staticmethod
+    def _stamp(text):
+        from datetime import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.strptime(text.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, window=None):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
@@ -218,12 +232,16 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
+        rows = [[x.strip() for x in ln.split(",")] for ln in self.lines]
+        rows = [f for f in rows if len(f) >= 10]
+        scope = "whole sampling period"
+        if window:
+            inside = [f for f in rows if (t := self._stamp(f[9])) is not None and window[0] <= t <= window[1]]
+            if inside:
+                rows, scope = inside, "timed region"
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
+        for f in rows:
             try:
                 sm.append(float(f[1]))
                 smax.append(float(f[2]))
@@ -233,7 +251,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "scope": scope}
 
 
 def gpu_id_for_smi(torch):
@@ -313,7 +331,7 @@ def reference_arm(args, rank):
         return
     import oracle
     oracle.build()
-    parts = oracle_parts(args.workload)
+    parts = oracle_parts(args.workload, args.kind, args.mantissa)
     cores = os.cpu_count() or 1
     # warm-up then K bounded steps: each step one row chunk per contraction
     for w in range(args.warmup):
@@ -346,7 +364,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="mlp", choices=WORKLOADS)
+    ap.add_argument("--workload", default="gemm4096", choices=WORKLOADS)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -435,13 +453,15 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    epoch0 = time.time()
     launches0 = am.amsim_kernel_launches()
     evs = timed_loop(K, per_part=False)
     launches_timed = am.amsim_kernel_launches() - launches0
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
+    time.sleep(0.1)
+    clocks = sampler.stop(window=(epoch0, epoch0 + wall))
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
 
     # per-call times (events between calls stop launches from overlapping, so
@@ -634,8 +654,30 @@ def main():
            "serial_value": world * macs / (serial_ms * 1e-3) / 1e9}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("mlp", "gemm4096", "dwconv3x3", "dwconv3x3_s2",
-                                                                            "dwconv5x5"):
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "gemm4096":
+        # the oracle on a seeded sample of 64 output rows (all 4096 columns,
+        # all of k): its time, and the GPU's rows checked against it
+        import numpy as np
+        import oracle
+        oracle.build()
+        cores = os.cpu_count() or 1
+        rows = np.sort(np.random.default_rng(0).choice(4096, size=64, replace=False)).astype(np.int32)
+        A, B = step.A.cpu().numpy(), step.B.cpu().numpy()
+        step.run()
+        torch.cuda.synchronize()
+        got = step.C.cpu().numpy()[rows].astype(np.float64)
+        t0 = time.perf_counter()
+        ref, sa = oracle.gemm(args.kind, args.mantissa, A, B, rows=rows, nthreads=cores)
+        secs = time.perf_counter() - t0
+        m = rows.size * 4096 * 4096
+        ratio = np.abs(got - ref) / np.maximum(1e-5 * sa, 1e-300)
+        cpu = {"value": m / secs / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"64 seeded output rows (numpy default_rng(0)) x 4096 columns x k = 4096: {m} MACs, "
+                         f"{secs:.1f} s wall",
+               "parity": {"rows": int(rows.size), "max_err_over_tol": float(ratio.max()),
+                          "tol": "1e-5 * sum_k |AMSim product| per element", "ok": bool(ratio.max() <= 1.0)}}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("mlp", "dwconv3x3",
+                                                                                    "dwconv3x3_s2", "dwconv5x5"):
         import oracle
         oracle.build()
         cores = os.cpu_count() or 1
@@ -657,7 +699,7 @@ def main():
             "native_fp32": native,
             "gpu_launches": launches_timed,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
-                       "samples": clocks["samples"]},
+                       "samples": clocks["samples"], "scope": clocks.get("scope")},
             "wall_s": wall,
         }
         if cpu:

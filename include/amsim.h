@@ -127,11 +127,27 @@ int amsim_lut_build(int kind, int M, amsim_lut_t *out);
 /*
  * Same as amsim_lut_build for an arbitrary table of 2^(2M) canonical entries
  * (carry << 23 | mantissa, carry in {0,1}), e.g. produced by
- * amsim_lut_generate_from_fn or loaded from a file at run time (Sec. VI,
- * "LUTs are loaded into the operator library at run time").  The table need
+ * amsim_lut_generate_from_fn or loaded from a file at run time (Sec. VI, Fig. 5:
+ * generated tables are handed to the operator library when the program
+ * runs, not compiled into it).  The table need
  * not be symmetric.  Errors: AMSIM_EUNSUPPORTED if an entry has bits above 23.
  */
 int amsim_lut_build_from_entries(const uint32_t *host_entries, int M, amsim_lut_t *out);
+
+/*
+ * Algorithm 1 over a user's approx_mul and the device upload in one call: the
+ * page's flow in which the designer writes the multiplier as a C/C++ function
+ * and its generated table is handed to the operator library when the program
+ * runs (Sec. V-A, Algorithm 1; Sec. VI, Figs. 5 and 7).
+ * Equivalent to amsim_lut_generate_from_fn followed by
+ * amsim_lut_build_from_entries: `approx_mul` is called 2^(2M) times on the
+ * host, with normal operands 1.p and 1.q in [1,2), and must return a positive
+ * normal product in [1,4).  The handle belongs to the current device.
+ * Errors: AMSIM_EINVAL for a null function or output, AMSIM_EUNSUPPORTED for
+ * M outside [1,11] or a product whose exponent moves by anything but 0 or +1
+ * (or that is negative), AMSIM_ENOMEM / AMSIM_ECUDA from the upload.
+ */
+int amsim_lut_build_from_fn(amsim_approx_mul_fn approx_mul, int M, amsim_lut_t *out);
 
 /* Copy the 2^(2M) canonical entries of a handle back to host memory (synchronous). */
 int amsim_lut_entries(amsim_lut_t lut, uint32_t *host_dst);

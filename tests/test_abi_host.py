@@ -140,3 +140,17 @@ def test_grouped_rejects_bad_arguments(L):
 def test_closed_form_switch_rejects_null(L):
     assert L.amsim_lut_set_closed_form(None, 1) == am.AMSIM_EINVAL
     assert L.amsim_lut_set_closed_form(None, 0) == am.AMSIM_EINVAL
+
+
+def test_lut_build_from_fn_rejects_before_device_work(L):
+    """amsim_lut_build_from_fn runs Algorithm 1 on the host before it touches a
+    device: argument and model errors come back without a GPU."""
+    h = ctypes.c_void_p(0)
+    cb = am.APPROX_MUL_FN(lambda a, b: a * b)
+    assert L.amsim_lut_build_from_fn(am.APPROX_MUL_FN(), 3, ctypes.byref(h)) == am.AMSIM_EINVAL
+    assert L.amsim_lut_build_from_fn(cb, 3, None) == am.AMSIM_EINVAL
+    assert L.amsim_lut_build_from_fn(cb, 0, ctypes.byref(h)) == am.AMSIM_EUNSUPPORTED
+    assert L.amsim_lut_build_from_fn(cb, 12, ctypes.byref(h)) == am.AMSIM_EUNSUPPORTED
+    bad = am.APPROX_MUL_FN(lambda a, b: 0.25 * a * b)
+    assert L.amsim_lut_build_from_fn(bad, 3, ctypes.byref(h)) == am.AMSIM_EUNSUPPORTED
+    assert h.value is None

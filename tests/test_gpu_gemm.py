@@ -340,19 +340,18 @@ def test_paths_bit_identical_without_stream_k(amd, luts):
 
 
 RAW_SHAPES = [(64, 256, 16), (300, 500, 2000), (130, 520, 40), (257, 10, 500), (5, 7, 4), (700, 90, 332)]
+# (shape, transA, transB) whose leading dimensions are multiples of 4 elements
+# (what selects this path): lda = m for a transposed A, else k; ldb = k for a
+# transposed B, else n.
+RAW_CASES = [(s, ta, tb) for s in RAW_SHAPES for ta in (False, True) for tb in (False, True)
+             if (s[0] if ta else s[2]) % 4 == 0 and (s[2] if tb else s[1]) % 4 == 0]
 
 
-@pytest.mark.parametrize("ta", [False, True])
-@pytest.mark.parametrize("tb", [False, True])
-@pytest.mark.parametrize("shape", RAW_SHAPES)
+@pytest.mark.parametrize("shape,ta,tb", RAW_CASES)
 def test_raw_tile_path(amd, orc, luts, shape, ta, tb):
     """Operand tiles copied in place (rows or k innermost, so both the plain and
-    the swizzled transposing decode run) and decoded in shared memory; leading
-    dimensions that are multiples of 4 elements select this path."""
+    the swizzled transposing decode run) and decoded in shared memory."""
     m, n, k = shape
-    lda, ldb = (m if ta else k), (k if tb else n)
-    if lda % 4 or ldb % 4:
-        pytest.skip("leading dimension not a multiple of 4")
     rng = np.random.default_rng(7 * m + 5 * n + k + 2 * ta + tb)
     A = rnd(rng, (k, m) if ta else (m, k))
     B = rnd(rng, (n, k) if tb else (k, n))

@@ -3,7 +3,13 @@ device memory at call time (no workspace argument; its stream-K partial sums
 go to a fixed array inside the library).  Checked through the C ABI against
 amsim_gemm with a caller workspace, on two calls in a row so the second call
 runs over the array contents the first one left, within the contraction
-tolerance the other tests use (1e-5 * sum_k |AMSim product| per element)."""
+tolerance the other tests use (1e-5 * sum_k |AMSim product| per element).
+
+The first shape splits its reduction across CTAs (stream-K), so its partial
+sums really go through the library's array; the test asserts that path.  The
+array holds one stream-K slot pair per SM for up to 159 SMs, so on this GPU no
+problem's plan exceeds it and the over-size rejection (AMSIM_EUNSUPPORTED) is
+never reached; a large multi-wave problem is run to show that it is not."""
 import ctypes
 
 import numpy as np
@@ -43,6 +49,8 @@ def test_noalloc_gemm_matches_workspace_gemm_twice(amd, orc, luts, kind):
                                       ctypes.c_float(0.0), out.data_ptr(), n, lut.handle,
                                       torch.cuda.current_stream().cuda_stream)
             assert rc == amd.AMSIM_OK, amd.status_string(rc)
+            if (m, n, k) == (300, 500, 2000):
+                assert amd.amsim_last_path() & amd.AMSIM_PATH_STREAMK, amd.amsim_last_path()
             torch.cuda.synchronize()
             got = out.cpu().numpy()
             assert_close(got, want, 2.0 * bound, f"noalloc vs workspace {m}x{n}x{k} call {call}")
@@ -63,3 +71,29 @@ def test_noalloc_rejects_bad_arguments(amd, luts):
     rc = L.amsim_gemm_noalloc(b"N", b"N", 4, 4, 4, ctypes.c_float(1.0), x.data_ptr(), 4, x.data_ptr(), 4,
                               ctypes.c_float(0.0), x.data_ptr(), 4, None, None)
     assert rc == amd.AMSIM_EINVAL
+
+
+def test_noalloc_large_multi_wave_problem_fits_the_array(amd, orc, luts):
+    """A 2048 x 2048 x 256 GEMM has 256 tiles, more than one wave on any GPU of
+    this family: stream-K over every SM, the largest plan the array must hold."""
+    import torch
+    L = amd.lib()
+    lut = luts("mitchell", 7)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sms <= 159, "the array holds stream-K slots for up to 159 SMs"
+    m = n = 2048
+    k = 256
+    rng = np.random.default_rng(5)
+    A = rng.standard_normal((m, k)).astype(np.float32)
+    B = rng.standard_normal((k, n)).astype(np.float32)
+    dA, dB = to_dev(A), to_dev(B)     # kept alive until the kernel has read them
+    out = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    rc = L.amsim_gemm_noalloc(b"N", b"N", m, n, k, ctypes.c_float(1.0), dA.data_ptr(), k, dB.data_ptr(), n,
+                              ctypes.c_float(0.0), out.data_ptr(), n, lut.handle,
+                              torch.cuda.current_stream().cuda_stream)
+    assert rc == amd.AMSIM_OK, amd.status_string(rc)
+    assert amd.amsim_last_path() & amd.AMSIM_PATH_STREAMK, amd.amsim_last_path()
+    torch.cuda.synchronize()
+    rows = np.array([0, 1000, m - 1])
+    ref, sa = orc.gemm("mitchell", 7, A, B, rows=rows)
+    assert_close(out.cpu().numpy()[rows], ref, sa, "noalloc 2048x2048x256")
