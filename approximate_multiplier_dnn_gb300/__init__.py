@@ -27,6 +27,10 @@ AMSIM_EINVAL = 1
 AMSIM_EUNSUPPORTED = 2
 AMSIM_ENOMEM = 3
 AMSIM_ECUDA = 4
+AMSIM_ETIMEOUT = 5
+AMSIM_WAIT_COPY = 1
+AMSIM_WAIT_PARTIAL = 2
+AMSIM_WAIT_PHASE = 4
 
 _lib = None
 
@@ -84,6 +88,8 @@ def lib():
         "amsim_status_string": ([i32], ctypes.c_char_p),
         "amsim_kernel_launches": ([], ctypes.c_ulonglong),
         "amsim_last_path": ([], i32),
+        "amsim_device_errors": ([ctypes.POINTER(ctypes.c_uint), i32], i32),
+        "amsim_set_flag_wait_limit": ([ctypes.c_longlong], i32),
         "amsim_lut_generate": ([i32, i32, vp], i32),
         "amsim_lut_generate_from_fn": ([APPROX_MUL_FN, i32, vp], i32),
         "amsim_lut_build": ([i32, i32, ctypes.POINTER(vp)], i32),
@@ -155,6 +161,20 @@ def amsim_last_path() -> int:
 def amsim_kernel_launches() -> int:
     """Kernels the library has enqueued so far in this process."""
     return int(lib().amsim_kernel_launches())
+
+
+def amsim_device_errors(clear: bool = True) -> tuple[int, int]:
+    """(status, AMSIM_WAIT_* bits) of the device-side waits that gave up on the
+    current device since the last clear (synchronises the device)."""
+    bits = ctypes.c_uint(0)
+    rc = lib().amsim_device_errors(ctypes.byref(bits), 1 if clear else 0)
+    if rc not in (AMSIM_OK, AMSIM_ETIMEOUT):
+        raise AmsimError("amsim_device_errors", rc)
+    return rc, int(bits.value)
+
+
+def amsim_set_flag_wait_limit(ns: int) -> None:
+    _check("amsim_set_flag_wait_limit", lib().amsim_set_flag_wait_limit(int(ns)))
 
 
 def status_string(status: int) -> str:

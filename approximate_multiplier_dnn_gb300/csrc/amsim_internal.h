@@ -31,6 +31,12 @@ namespace amsim {
 constexpr int kMaxSmemPerCta = 227 * 1024;
 
 int check_lut(amsim_lut_t lut);   // AMSIM_OK if usable on the current device
+// Each translation unit with bounded device waits registers a reader of its
+// wait-status word (OR its AMSIM_WAIT_* bits into *bits, clear when asked)
+// and a writer of its flag-wait limit; both act on the current device.
+using WaitStatusFn = int (*)(unsigned int *bits, int clear);
+using WaitLimitFn = int (*)(long long ns);
+bool register_wait_words(WaitStatusFn status, WaitLimitFn limit);
 void count_launch();              // one kernel enqueued by the library
 int cuda_status(cudaError_t e);   // maps to AMSIM_OK / AMSIM_ECUDA / AMSIM_ENOMEM
 void set_last_path(int bits);     // the calling thread's amsim_last_path() value

@@ -703,12 +703,14 @@ int run_problem(const Problem &p, amsim_lut_t lut, void *ws, size_t ws_bytes, cu
 
 namespace {
 
-// Scratch of a phased launch: a completion flag per phase and CTA, then per
-// tile an arrival ticket and a flag for its first stored part (the other
-// parts of a cut tile are added in C).
+// Scratch of a phased launch: a completion flag per phase and CTA, per tile
+// an arrival ticket and a spare word, then (256-byte aligned) two partial-sum
+// slots of a BU x BL tile per CTA and phase, from which the last part of a cut
+// tile adds all parts in CTA order.
 size_t phased_sk_bytes(int nphase, int G, long long tiles)
 {
-    return ((size_t)nphase * G + 2 * (size_t)tiles) * sizeof(unsigned long long);
+    const size_t words = ((size_t)nphase * G + 2 * (size_t)tiles) * sizeof(unsigned long long);
+    return align256(words) + (size_t)nphase * G * 2 * BU * BL * sizeof(float);
 }
 
 // Problems [first[ph], first[ph + 1]) of phase ph (the last ends at n).

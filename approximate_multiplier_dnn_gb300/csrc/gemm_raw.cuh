@@ -559,9 +559,11 @@ __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lu
                      2 * kRawDec, aborted);
 }
 
-// Scratch of a phased launch: completion flags [phase][cta], then per tile of
-// the launch an arrival ticket (launch epoch in the high half, parts arrived
-// in the low half) and a flag raised once its first arrived part is stored.
+// Scratch of a phased launch: completion flags [phase][cta]; per tile of the
+// launch an arrival ticket (launch epoch in the high half, stages arrived in
+// the low half) and a spare word; then, 256-byte aligned, two partial-sum
+// slots [phase][cta][2][BU * BL] per CTA and phase (slot 0 for the first
+// segment of the CTA's share of the phase, slot 1 for its last).
 __device__ __forceinline__ unsigned long long *phase_done(const KParams &p)
 {
     return reinterpret_cast<unsigned long long *>(p.ws);
@@ -572,16 +574,25 @@ __device__ __forceinline__ unsigned long long *tile_ticket(const KParams &p, lon
     return phase_done(p) + (long long)n_phases(p) * p.ctas + 2 * tile;
 }
 
-// Count this part's arrival at a cut tile; true for the first part of this launch.
-__device__ __forceinline__ bool first_arrival(const KParams &p, long long tile)
+__device__ __forceinline__ float *phased_slot(const KParams &p, long long total_tiles, int ph, int cta, int slot)
+{
+    const long long words = (long long)n_phases(p) * p.ctas + 2 * total_tiles;
+    const long long off = ((words * 8 + 255) & ~255LL) / 4;
+    return p.ws + off + (((long long)ph * p.ctas + cta) * 2 + slot) * (BU * BL);
+}
+
+// Add this part's stages to a cut tile's ticket; true for the part that
+// brings the count to the tile's stage count (the last to arrive).
+__device__ __forceinline__ bool last_arrival(const KParams &p, long long tile, int stages, int kt_total)
 {
     unsigned long long *t = tile_ticket(p, tile);
     const unsigned long long ep = (p.epoch & 0xFFFFFFFFull) << 32;
     unsigned long long v = *reinterpret_cast<volatile unsigned long long *>(t);
     for (;;) {
-        const unsigned long long nv = (v & 0xFFFFFFFF00000000ull) == ep ? v + 1 : ep | 1ull;
+        const unsigned long long nv =
+            (v & 0xFFFFFFFF00000000ull) == ep ? v + (unsigned)stages : ep | (unsigned)stages;
         const unsigned long long old = atomicCAS(t, v, nv);
-        if (old == v) return (nv & 0xFFFFFFFFull) == 1;
+        if (old == v) return (nv & 0xFFFFFFFFull) == (unsigned long long)kt_total;
         v = old;
     }
 }
@@ -590,6 +601,19 @@ __device__ __forceinline__ bool first_arrival(const KParams &p, long long tile)
 __device__ __forceinline__ long long ph_begin(const KParams &p, const PhaseTable &pt, int ph, int c)
 {
     return p.ph_iter0[ph] + pt.bound[ph][c];
+}
+
+// The CTA whose share of phase ph holds launch iteration `it` (the largest c
+// with ph_begin(c) <= it: CTAs with empty shares are passed over).
+__device__ __forceinline__ int ph_owner(const KParams &p, const PhaseTable &pt, int ph, long long it)
+{
+    int lo = 0, hi = p.ctas - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ph_begin(p, pt, ph, mid) <= it) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
 }
 
 // This CTA's launch iterations in order: its share of every phase.  `it` runs
@@ -633,7 +657,7 @@ __device__ __forceinline__ void cursor_next(const KParams &p, const PhaseTable &
 __device__ __forceinline__ void wait_phases(const KParams &p, int nreq, int d, bool &aborted)
 {
     const unsigned long long *done = phase_done(p);
-    for (int i = d; i < nreq * p.ctas; i += kRawDecoders) flag_wait(done + i, p.epoch, aborted);
+    for (int i = d; i < nreq * p.ctas; i += kRawDecoders) flag_wait(done + i, p.epoch, aborted, AMSIM_WAIT_PHASE);
     decoder_bar();
 }
 
@@ -755,73 +779,31 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
     }
 }
 
-// Vector and scalar reductions into global memory (the sum lands in L2).
-__device__ __forceinline__ void red_add4(float *dst, float4 v)
-{
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void red_add1(float *dst, float v)
-{
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(v) : "memory");
-}
-
-// Add alpha * acc of one consumer's block into C (a cut tile of a phased
-// launch, after its last part has been stored).
-__device__ __forceinline__ void add_tile(const ProbParams &q, const float2 (&acc)[TM / 2][TN], int b, int u0, int l0)
-{
-    const int nU = q.U.rows, nL = q.L.rows;
-    float *C = q.c_ptr + (long long)b * q.c_bs;
-    const float alpha = q.alpha;
-    const bool vec_l = (reinterpret_cast<uintptr_t>(C) & 15) == 0 && q.c_sl == 1 && (q.c_su & 3) == 0;
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int u = u0 + i;
-        if (u >= nU) break;
-        if (vec_l && l0 + TN <= nL) {
-#pragma unroll
-            for (int t4 = 0; t4 < TN / 4; ++t4) {
-                const float4 a = acc4(acc, i, 4 * t4);
-                red_add4(C + (long long)u * q.c_su + l0 + 4 * t4,
-                         make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w));
-            }
-        } else {
-#pragma unroll
-            for (int t = 0; t < TN; ++t) {
-                const int l = l0 + t;
-                if (l >= nL) break;
-                red_add1(C + (long long)u * q.c_su + (long long)l * q.c_sl, alpha * accv(acc, i, t));
-            }
-        }
-    }
-}
-
 // The consumers of a phased launch (LUT in shared memory).  A tile that the
-// share boundaries cut is summed in C: the first of its parts to be done (an
-// arrival ticket per tile decides) is stored as alpha * part + beta * C, and a
-// flag is raised; every other part is added with floating-point reductions
-// after that flag -- no CTA waits for another CTA's compute, at a phase's end
-// or anywhere else.  The summation order of cut tiles therefore varies from
-// run to run.
+// share boundaries cut is finished without any CTA waiting for another: each
+// part leaves its partial sum in its CTA's slot and adds its stage count to
+// the tile's ticket; the part that completes the count (the last to arrive)
+// adds every part's partial sum in CTA order -- the order of their stages --
+// and stores alpha * sum + beta * C.  Results are therefore the same from run
+// to run.
 template <int W>
 __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const PhaseTable &pt, const uint8_t *lut,
                                                    const RawSmem &sm)
 {
-    volatile int *first_flag = sm.flags + kRawDec * (kRawDecoders / 32);   // the ticket's verdict
+    volatile int *last_flag = sm.flags + kRawDec * (kRawDecoders / 32);   // the ticket's verdict
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
     const int lcol = wl * 32 * TN + lane * TN;
+    const long long total_tiles = p.pr[p.nprob - 1].tile0 + p.pr[p.nprob - 1].tiles;
     uint32_t g = 0;
     bool aborted = false;
     const int nph = n_phases(p);
     for (int ph = 0; ph < nph; ++ph) {
         const long long it0 = ph_begin(p, pt, ph, blockIdx.x), it1 = ph_begin(p, pt, ph, blockIdx.x + 1);
         walk_segments(p, it0, it1,
-                      [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool) {
+                      [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
             float2 acc[TM / 2][TN];
 #pragma unroll
             for (int i = 0; i < TM / 2; ++i)
@@ -849,25 +831,56 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const Phas
             }
             if (s0 == 0 && s1 == q.kt_total) {
                 store_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
-            } else {
-                const long long tile = q.tile0 + (long long)b * q.tiles_u * q.tiles_l +
-                                       (long long)(u_tile0 / BU) * q.tiles_l + l_tile0 / BL;
-                unsigned long long *stored = tile_ticket(p, tile) + 1;
-                if (tid == 0) *first_flag = first_arrival(p, tile) ? 1 : 0;
-                consumer_bar();
-                const bool first = *first_flag != 0;
-                consumer_bar();         // everyone has read the ticket's verdict
-                if (first) {
-                    store_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
-                    consumer_bar();
-                    if (tid == 0) flag_store(stored, p.epoch);
-                } else {
-                    flag_wait(stored, p.epoch, aborted);
-                    add_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
-                }
+                return;
             }
+            const long long lt = (long long)b * q.tiles_u * q.tiles_l + (long long)(u_tile0 / BU) * q.tiles_l +
+                                 l_tile0 / BL;
+            float *mine = phased_slot(p, total_tiles, ph, blockIdx.x, first ? 0 : 1);
+            if (!idle) {
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int t4 = 0; t4 < TN / 4; ++t4)
+                        __stcg(reinterpret_cast<float4 *>(mine + (urow + i) * BL + lcol + 4 * t4), acc4(acc, i, 4 * t4));
+            }
+            // every consumer's slot writes precede the barrier; thread 0's
+            // fence and ticket update then publish them (cumulative release)
+            consumer_bar();
+            if (tid == 0) {
+                __threadfence();
+                const bool last = last_arrival(p, q.tile0 + lt, s1 - s0, q.kt_total);
+                __threadfence();
+                *last_flag = last ? 1 : 0;
+            }
+            consumer_bar();
+            const bool last = *last_flag != 0;
+            consumer_bar();         // everyone has read the ticket's verdict
+            if (!last || idle) return;
+            const long long tbeg = q.iter0 + lt * q.kt_total, tend = tbeg + q.kt_total;
+            const int c_lo = ph_owner(p, pt, ph, tbeg), c_hi = ph_owner(p, pt, ph, tend - 1);
+            float2 sum[TM / 2][TN];
+#pragma unroll
+            for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) sum[i][j] = make_float2(0.0f, 0.0f);
+            for (int c = c_lo; c <= c_hi; ++c) {
+                const long long cb = ph_begin(p, pt, ph, c);
+                if (cb == ph_begin(p, pt, ph, c + 1)) continue;          // empty share
+                const float *part = phased_slot(p, total_tiles, ph, c, cb >= tbeg ? 0 : 1);
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int t4 = 0; t4 < TN / 4; ++t4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(part + (urow + i) * BL + lcol + 4 * t4));
+                        float2 &lo = sum[i >> 1][4 * t4], &l1 = sum[i >> 1][4 * t4 + 1];
+                        float2 &l2 = sum[i >> 1][4 * t4 + 2], &l3 = sum[i >> 1][4 * t4 + 3];
+                        if (i & 1) { lo.y += v.x; l1.y += v.y; l2.y += v.z; l3.y += v.w; }
+                        else { lo.x += v.x; l1.x += v.y; l2.x += v.z; l3.x += v.w; }
+                    }
+            }
+            store_tile(q, sum, b, u_tile0 + urow, l_tile0 + lcol);
         });
-        // every consumer's stores and reductions of the phase precede the flag
+        // every consumer's stores of the phase precede the flag
         consumer_bar();
         if (tid == 0) flag_store(phase_done(p) + (long long)ph * p.ctas + blockIdx.x, p.epoch);
     }

@@ -6,9 +6,10 @@
 //
 // The two roles hand stages over through mbarriers (full: producers arrive,
 // consumers wait; empty: the reverse).  Every wait is bounded by the global
-// timer: after kWaitLimitNs a thread records the timeout in a device flag,
-// stops waiting and still arrives on every barrier, so the CTA always runs to
-// its end.  Register budgets are rebalanced with setmaxnreg: producers give
+// timer: after kWaitLimitNs (waits on another CTA's flag: the settable
+// g_flag_wait_limit_ns) a thread records the timeout in a device status word
+// that amsim_device_errors reads, stops waiting and still arrives on every
+// barrier, so the CTA always runs to its end.  Register budgets are rebalanced with setmaxnreg: producers give
 // registers back, consumers take them for deeper instruction-level parallelism.
 #pragma once
 
@@ -56,8 +57,36 @@ static_assert(kStages * kStageBytes + kRawStages * kRawBytes >= (BU * BL + 1024 
               "stream-K reduction buffer");
 static_assert(2 * kStages * 8 + 8 + kStages * kProducerWarps * 4 <= 128, "barrier block");
 
-// Set when a bounded wait gave up (one flag per translation unit).
+// Wait status of this translation unit's kernels on the current device: the
+// AMSIM_WAIT_* bits of the waits that gave up.  Every translation unit that
+// includes this header has its own copy of the two words below (device code
+// cannot name another unit's variables without relocatable device code), and
+// registers a reader and a writer for them with the library's registry at
+// load time, so amsim_device_errors and amsim_set_flag_wait_limit reach all
+// of them.
 static __device__ unsigned int g_ws_wait_timeouts;
+// Limit of the waits on flags that other CTAs raise (stream-K partial sums,
+// phase dependencies); copy waits keep kWaitLimitNs.
+static __device__ long long g_flag_wait_limit_ns = kWaitLimitNs;
+
+namespace {
+int tu_wait_status(unsigned int *bits, int clear)
+{
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_ws_wait_timeouts, sizeof(v)) != cudaSuccess) return AMSIM_ECUDA;
+    *bits |= v;
+    if (clear && v) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_ws_wait_timeouts, &zero, sizeof(zero)) != cudaSuccess) return AMSIM_ECUDA;
+    }
+    return AMSIM_OK;
+}
+int tu_flag_wait_limit(long long ns)
+{
+    return cudaMemcpyToSymbol(g_flag_wait_limit_ns, &ns, sizeof(ns)) == cudaSuccess ? AMSIM_OK : AMSIM_ECUDA;
+}
+[[maybe_unused]] const bool g_tu_wait_words = register_wait_words(&tu_wait_status, &tu_flag_wait_limit);
+}  // namespace
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -109,7 +138,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, bool &
     while (!mbar_try_wait(bar, parity)) {
         if (global_ns() - t0 > (unsigned long long)kWaitLimitNs) {
             aborted = true;
-            atomicOr(&g_ws_wait_timeouts, 1u);
+            atomicOr(&g_ws_wait_timeouts, (unsigned)AMSIM_WAIT_COPY);
             return false;
         }
     }
@@ -443,16 +472,19 @@ __device__ __forceinline__ unsigned long long flag_load(const unsigned long long
     return v;
 }
 
-// Wait until *f == v (another CTA of this cooperative launch raised it).
-__device__ __forceinline__ void flag_wait(const unsigned long long *f, unsigned long long v, bool &aborted)
+// Wait until *f == v (another CTA of this cooperative launch raised it);
+// `bit` is the AMSIM_WAIT_* kind recorded if the wait gives up.
+__device__ __forceinline__ void flag_wait(const unsigned long long *f, unsigned long long v, bool &aborted,
+                                          unsigned int bit = AMSIM_WAIT_PARTIAL)
 {
     if (aborted) return;
     if (flag_load(f) == v) return;
+    const unsigned long long limit = (unsigned long long)*(volatile long long *)&g_flag_wait_limit_ns;
     const unsigned long long t0 = global_ns();
     while (flag_load(f) != v) {
-        if (global_ns() - t0 > (unsigned long long)kWaitLimitNs) {
+        if (global_ns() - t0 > limit) {
             aborted = true;
-            atomicOr(&g_ws_wait_timeouts, 2u);
+            atomicOr(&g_ws_wait_timeouts, bit);
             return;
         }
     }

@@ -168,6 +168,7 @@ const char *amsim_status_string(int status)
     case AMSIM_EUNSUPPORTED: return "unsupported mantissa width, kind or LUT entry";
     case AMSIM_ENOMEM: return "out of memory";
     case AMSIM_ECUDA: return "CUDA runtime error";
+    case AMSIM_ETIMEOUT: return "a device-side wait gave up (outputs of some call are wrong)";
     default: return "unknown status";
     }
 }

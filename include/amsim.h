@@ -36,7 +36,10 @@
  *   - Return value: AMSIM_OK or an amsim_status code.  Arguments are checked
  *     on the host before anything is enqueued; on error nothing is enqueued
  *     and outputs are untouched.  A failed launch returns AMSIM_ECUDA.
- *     Kernels contain no device-side asserts or traps.
+ *     Kernels contain no device-side asserts or traps.  Every wait inside a
+ *     kernel (for a copy, or for a flag another CTA raises) is bounded; a wait
+ *     that gives up leaves that call's outputs wrong and is recorded on the
+ *     device, where amsim_device_errors reads it (AMSIM_ETIMEOUT).
  *   - Results are deterministic: the same call on the same inputs with the
  *     same scratch size gives bit-identical outputs.
  */
@@ -63,7 +66,8 @@ enum amsim_status {
     AMSIM_EINVAL = 1,        /* bad argument (null pointer, negative size, bad stride, wrong device) */
     AMSIM_EUNSUPPORTED = 2,  /* M outside [1,11], unknown kind, a LUT entry outside carry 0/1 */
     AMSIM_ENOMEM = 3,        /* the LUT's device (or host) allocation failed */
-    AMSIM_ECUDA = 4          /* a CUDA runtime call or kernel launch failed */
+    AMSIM_ECUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    AMSIM_ETIMEOUT = 5       /* a bounded device-side wait gave up (amsim_device_errors) */
 };
 
 /* Human-readable text for a status code (static storage). */
@@ -89,6 +93,44 @@ enum amsim_path {
     AMSIM_PATH_DW_DIRECT = 2048     /* depthwise: one lane per output element, operands read directly */
 };
 int amsim_last_path(void);
+
+/*
+ * Kinds of device-side waits (bits of amsim_device_errors' *flags):
+ *   AMSIM_WAIT_COPY     a CTA waited for its own asynchronous copies or for
+ *                       another warp of its CTA (limit 2 s);
+ *   AMSIM_WAIT_PARTIAL  a CTA waited for another CTA's partial sums of a
+ *                       tile split across CTAs (stream-K);
+ *   AMSIM_WAIT_PHASE    a CTA of an amsim_gemm_phased launch waited for the
+ *                       earlier phases its phase reads.
+ * The last two wait on other CTAs of the same launch, with the limit that
+ * amsim_set_flag_wait_limit sets (2 s by default).
+ */
+enum amsim_wait_bits { AMSIM_WAIT_COPY = 1, AMSIM_WAIT_PARTIAL = 2, AMSIM_WAIT_PHASE = 4 };
+
+/*
+ * Which bounded waits of the library's kernels have given up on the current
+ * device since the last clear: synchronises the device (so every call enqueued
+ * before it has finished), ORs the AMSIM_WAIT_* bits of every kernel family
+ * into *flags, and clears them when `clear` is nonzero.  A set bit means some
+ * call since the last clear produced wrong outputs (its kernels still ran to
+ * their end and the context stays usable).  Returns AMSIM_OK when no wait gave
+ * up, AMSIM_ETIMEOUT when one did, AMSIM_EINVAL for a null `flags`,
+ * AMSIM_ECUDA when the device cannot be read.  Not for use during stream
+ * capture.  The paper has no counterpart; it is the library's error report.
+ */
+int amsim_device_errors(unsigned int *flags, int clear);
+
+/*
+ * Limit, in nanoseconds, of the device-side waits on flags that other CTAs of
+ * the same launch raise (AMSIM_WAIT_PARTIAL, AMSIM_WAIT_PHASE), for launches
+ * enqueued after the call on the current device; 0 <= ns <= 10 s, default
+ * 2 s.  Those waits normally last microseconds; a watchdog that wants a hung
+ * launch reported sooner can lower it (0 gives up at the first flag not yet
+ * raised, which is how the tests provoke a timeout).  Copy waits keep 2 s.
+ * Synchronising; not for use during stream capture.  Errors: AMSIM_EINVAL
+ * for ns outside the range, AMSIM_ECUDA.  The paper has no counterpart.
+ */
+int amsim_set_flag_wait_limit(long long ns);
 
 /* ------------------------------------------------------------------ LUTs */
 
@@ -282,10 +324,11 @@ size_t amsim_gemm_grouped_workspace_size(int count, const amsim_gemm_problem *pr
  * 256-byte-aligned scratch, every phase runs in one cooperative launch
  * (AMSIM_PATH_PHASED): each SM takes a share of every phase in order and
  * waits, before it loads a phase's operands, until every SM has finished
- * phases 0 .. phase_after[ph] - 1.  Tiles that the shares cut are summed in C
- * with floating-point reductions, so their last bits may differ from run to
- * run (within the contraction tolerance).  Otherwise the phases run as
- * consecutive grouped launches.  Host arrays are read during the call.
+ * phases 0 .. phase_after[ph] - 1.  A tile that the shares cut is finished by
+ * the last of its parts to arrive, which adds every part's partial sum (kept
+ * in scratch) in the parts' order, so repeated calls give identical bits.
+ * Otherwise the phases run as consecutive grouped launches.  Host arrays are
+ * read during the call.
  * Errors: AMSIM_EINVAL for an invalid phase layout or problem, as
  * amsim_gemm_grouped otherwise.
  */

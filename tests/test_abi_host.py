@@ -25,7 +25,7 @@ def test_exports_every_declared_function(L):
 
 
 def test_status_strings(L):
-    for s in range(5):
+    for s in range(6):
         assert am.status_string(s)
     assert am.status_string(99) == "unknown status"
 
@@ -154,3 +154,10 @@ def test_lut_build_from_fn_rejects_before_device_work(L):
     bad = am.APPROX_MUL_FN(lambda a, b: 0.25 * a * b)
     assert L.amsim_lut_build_from_fn(bad, 3, ctypes.byref(h)) == am.AMSIM_EUNSUPPORTED
     assert h.value is None
+
+
+def test_wait_status_calls_check_arguments_first(L):
+    """The wait-status calls reject bad arguments before touching a device."""
+    assert L.amsim_device_errors(None, 1) == am.AMSIM_EINVAL
+    assert L.amsim_set_flag_wait_limit(-5) == am.AMSIM_EINVAL
+    assert L.amsim_set_flag_wait_limit(20_000_000_000) == am.AMSIM_EINVAL

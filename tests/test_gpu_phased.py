@@ -160,6 +160,39 @@ def test_phased_empty_phase_and_small_phases(amd, orc, luts):
     assert_close(host(D), ref, sa, "D")
 
 
+def test_phased_results_bit_identical_across_runs(amd, luts):
+    """Tiles that the CTA shares cut are summed in a fixed order (the parts'
+    CTA order), so repeated calls give the same bits; the MLP step (the bench's
+    phased workload, nine GEMMs in five phases) likewise."""
+    import torch
+    from approximate_multiplier_dnn_gb300 import steps
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    rng = np.random.default_rng(47)
+    lut = luts("mitchell", 7)
+    probs, first, after, outs, h = build_chain(amd, rng)
+    ws = amd.workspace(amd.amsim_gemm_phased_workspace_size(probs, first, after, lut))
+    runs = []
+    for _ in range(3):
+        for _, (buf, view) in outs.items():
+            view.fill_(float("nan"))
+        path = run_phased(amd, lut, probs, first, after, ws=ws)
+        assert path & amd.AMSIM_PATH_PHASED, path
+        runs.append({k: host(v[1]).view(np.uint32).copy() for k, v in outs.items()})
+    for r in runs[1:]:
+        for k in r:
+            assert np.array_equal(r[k], runs[0][k]), f"{k} differs between runs"
+    st = steps.MLPStep(wl.mlp(), lut)
+    res = []
+    for _ in range(3):
+        st.run()
+        torch.cuda.synchronize()
+        assert amd.amsim_last_path() & amd.AMSIM_PATH_PHASED
+        res.append([host(t).view(np.uint32).copy() for t in st.outputs()])
+    for r in res[1:]:
+        for a, b in zip(r, res[0]):
+            assert np.array_equal(a, b), "MLP step outputs differ between runs"
+
+
 def test_phased_without_scratch_runs_phase_by_phase(amd, orc, luts):
     rng = np.random.default_rng(44)
     lut = luts("mitchell", 7)
@@ -184,9 +217,9 @@ def test_phased_rejects_bad_layouts(amd, luts):
 
 @pytest.mark.parametrize("kind", ["mitchell", "exact"])
 def test_phased_alpha_beta_and_transposes(amd, orc, luts, kind):
-    """alpha and beta != 0 on cut tiles (the first-arriving part carries
-    beta * C, the others add alpha * part), all four transpose pairs, and a
-    phase that reads a transposed output of an earlier one."""
+    """alpha and beta != 0 on cut tiles (the last part to arrive adds all
+    parts in order and stores alpha * sum + beta * C), all four transpose
+    pairs, and a phase that reads a transposed output of an earlier one."""
     rng = np.random.default_rng(45)
     lut = luts(kind, 7)
     m, n, k = 300, 520, 700
