@@ -98,6 +98,7 @@ def lib():
         "amsim_lut_entries": ([vp, vp], i32),
         "amsim_lut_info": ([vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "amsim_lut_set_closed_form": ([vp, i32], i32),
+        "amsim_lut_set_exponent_bits": ([vp, i32], i32),
         "amsim_lut_destroy": ([vp], None),
         "amsim_mul": ([vp, vp, vp, i64, vp, vp], i32),
         "amsim_gemm": ([ch, ch, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp, vp, sz, vp], i32),
@@ -247,6 +248,10 @@ class Lut:
         amsim_lut_set_closed_form(self.handle, on)
         return self
 
+    def set_exponent_bits(self, E: int) -> "Lut":
+        amsim_lut_set_exponent_bits(self.handle, E)
+        return self
+
     def close(self):
         if self.handle:
             lib().amsim_lut_destroy(self.handle)
@@ -310,6 +315,11 @@ def amsim_lut_entries(lut, M: int):
 
 def amsim_lut_set_closed_form(lut, on: bool = True) -> None:
     _check("amsim_lut_set_closed_form", lib().amsim_lut_set_closed_form(_h(lut), 1 if on else 0))
+
+
+def amsim_lut_set_exponent_bits(lut, E: int) -> None:
+    """Exponent width E (1..8) of the simulated (1, E, M) multiplier."""
+    _check("amsim_lut_set_exponent_bits", lib().amsim_lut_set_exponent_bits(_h(lut), int(E)))
 
 
 def amsim_lut_info(lut):

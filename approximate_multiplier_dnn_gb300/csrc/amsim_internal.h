@@ -23,7 +23,43 @@ struct amsim_lut_s {
     size_t narrow_bytes = 0;
     int kind = -1;              // AMSIM_EXACT / AMSIM_MITCHELL when built from a kind, else -1
     bool closed_form = false;   // raw-tile launches compute products in registers (kinds only)
+    int exp_bits = 8;           // exponent bits E of the simulated (1, E, M) format
 };
+
+// The exponent cast of a (1, E, M) format with E < 8 (ApproxTrain Sec. V-B,
+// last paragraph), as the kernels apply it.  Bias B = 2^(E-1) - 1; an fp32
+// operand with biased exponent e is zero below lo = 128 - B, infinite above
+// hi = 127 + B, else kept.  Its power-of-two scale is re-biased by `off`
+// (off_u + off_l = B - 127), so that the flush-to-zero scale product sa * sb
+// is zero exactly when Algorithm 2's e0 = eA + eB - B is not above zero; the
+// product v * sa * sb is then multiplied by vscale = 2^(127 - B) (exactly) and
+// becomes an infinity at or above lim = 2^(B + 1), Algorithm 2's overflow.
+// E = 8 gives lo = 1, hi = 254, no offsets, vscale 1 and lim = infinity: the
+// ordinary fp32 path.
+struct ExpFormat {
+    int on;                  // E < 8
+    int lo, hi;
+    int off_u, off_l;        // scale re-bias of the U and L operands (or first and second)
+    int bias, all_ones;      // B and 2^E - 1 (elementwise bit logic)
+    float vscale, lim;
+};
+
+inline ExpFormat exp_format(int E)
+{
+    ExpFormat f{};
+    const int B = (1 << (E - 1)) - 1;
+    f.on = E < 8;
+    f.bias = B;
+    f.all_ones = (1 << E) - 1;
+    f.lo = 128 - B;
+    f.hi = 127 + B;
+    f.off_u = (B - 127) / 2;                 // (B - 127) is even for E >= 2
+    f.off_l = (B - 127) - f.off_u;
+    uint32_t vb = (uint32_t)(127 + 127 - B) << 23, lb = E < 8 ? (uint32_t)(127 + B + 1) << 23 : 0x7F800000u;
+    __builtin_memcpy(&f.vscale, &vb, 4);
+    __builtin_memcpy(&f.lim, &lb, 4);
+    return f;
+}
 
 namespace amsim {
 

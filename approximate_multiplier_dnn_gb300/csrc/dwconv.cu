@@ -48,6 +48,8 @@ namespace {
 using namespace amsim::dw;
 using amsim::kern::expand;
 using amsim::kern::lut_ld;
+using amsim::kern::fmt_product;
+using amsim::kern::fmt_scale_bits;
 
 // ------------------------------------------------------------------ geometry
 struct DwGeo {
@@ -87,6 +89,7 @@ struct DwDirectParams {
     int table_bytes;       // staged table bytes (0: read through the cache)
     int grid_taps;         // data gradient: unit dilation, so the taps on the stride grid can be enumerated
     int G;                 // mode 2: shares of the N*P*Q reduction
+    ExpFormat fmt;         // (1, E, M) format with E < 8 when fmt.on
 };
 
 // Signed power-of-two scale of an operand (zero and denormal inputs a signed
@@ -108,15 +111,25 @@ __device__ __forceinline__ bool dw_on_grid(int v, int s, int lim, int &u)
 }
 
 // AMSim product from the staged (GL false) or global (GL true) narrowed table
-// [first][second], rounded to fp32 before it is added.
+// [first][second], rounded to fp32 before it is added; in a (1, E, M) format
+// with E < 8 the operands are cast first and the product is the format's
+// (fmt_product).
 template <int W, bool GL>
-__device__ __forceinline__ float dw_product_t(float first, float second, const uint8_t *lut, int M, int wlog)
+__device__ __forceinline__ float dw_product_t(float first, float second, const uint8_t *lut, int M, int wlog,
+                                              const ExpFormat &f)
 {
     const uint32_t xa = __float_as_uint(first), xb = __float_as_uint(second);
     const uint32_t idx = ((((xa & 0x7FFFFFu) >> (23 - M)) << M) | ((xb & 0x7FFFFFu) >> (23 - M))) << wlog;
     const float v = expand<W>(lut_ld<W, GL>(lut, idx));
+    if (f.on)
+        return fmt_product(v, fmul_ftz(__uint_as_float(fmt_scale_bits(xa, f.lo, f.hi, f.off_u)),
+                                       __uint_as_float(fmt_scale_bits(xb, f.lo, f.hi, f.off_l))), f);
     return __fmul_rn(v, fmul_ftz(dw_scale(xa), dw_scale(xb)));
 }
+
+// Whether an operand stays finite through the exponent cast (fp32 biased
+// exponent at most hi; hi = 254 for fp32's own exponent: not Inf or NaN).
+__device__ __forceinline__ bool dw_cast_finite(float v, int hi) { return (int)((__float_as_uint(v) >> 23) & 0xFFu) <= hi; }
 
 // Direct kernel: a warp takes one pixel (or, for the weight gradient, one
 // filter tap and one share of the pixels) and 32 consecutive channels, so both
@@ -143,7 +156,7 @@ __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ 
             bool ok = true;
             for (int t = 0; t < g.R * g.S * g.D; ++t) {
                 const int tap = t / g.D, d = t - tap * g.D;
-                ok = ok && isfinite(__ldg(p.b + ((long long)tap * g.C + c) * g.D + d));
+                ok = ok && dw_cast_finite(__ldg(p.b + ((long long)tap * g.C + c) * g.D + d), p.fmt.hi);
             }
             finite[c] = ok;
         }
@@ -173,9 +186,9 @@ __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ 
                         const bool in = hin && (unsigned)w < (unsigned)g.W;
                         // a padded tap multiplies a zero operand: a signed zero, which leaves
                         // the sum unchanged, unless the weight is infinite or NaN (then NaN)
-                        if (!in && isfinite(wv)) continue;
+                        if (!in && dw_cast_finite(wv, p.fmt.hi)) continue;
                         const float xv = in ? __ldg(xn + ((long long)h * g.W + w) * g.C) : 0.0f;
-                        acc = __fadd_rn(acc, dw_product_t<W, GL>(xv, wv, lut, p.M, p.wlog));
+                        acc = __fadd_rn(acc, dw_product_t<W, GL>(xv, wv, lut, p.M, p.wlog, p.fmt));
                     }
                 }
                 p.out[(long long)pix * g.K + k] = acc;
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ 
                             const float *wp = p.b + ((long long)(r * g.S + s) * g.C + c) * g.D;
                             for (int d = 0; d < g.D; ++d)
                                 acc = __fadd_rn(acc, dw_product_t<W, GL>(__ldg(dyp + d), __ldg(wp + d), lut, p.M,
-                                                                         p.wlog));
+                                                                         p.wlog, p.fmt));
                         }
                     }
                     p.out[(long long)pix * g.C + c] = acc;
@@ -224,9 +237,9 @@ __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ 
                             // a tap between stride positions or past the edge multiplies a zero
                             // operand: a signed zero, which leaves the sum unchanged, unless the
                             // weight is infinite or NaN (then NaN)
-                            if (!in && isfinite(wv)) continue;
+                            if (!in && dw_cast_finite(wv, p.fmt.hi)) continue;
                             const float dyv = in ? __ldg(dyp + d) : 0.0f;
-                            acc = __fadd_rn(acc, dw_product_t<W, GL>(dyv, wv, lut, p.M, p.wlog));
+                            acc = __fadd_rn(acc, dw_product_t<W, GL>(dyv, wv, lut, p.M, p.wlog, p.fmt));
                         }
                     }
                 }
@@ -256,9 +269,9 @@ __global__ void __launch_bounds__(256) dw_direct_kernel(const __grid_constant__ 
                     const int h = pp * g.sh - g.ph + r * g.dh, w = q * g.sw - g.pw + s * g.dw;
                     const float dyv = __ldg(p.b + pix * g.K + k);
                     const bool in = (unsigned)h < (unsigned)g.H && (unsigned)w < (unsigned)g.W;
-                    if (in || !isfinite(dyv)) {
+                    if (in || !dw_cast_finite(dyv, p.fmt.hi)) {
                         const float xv = in ? __ldg(p.a + (((long long)n * g.H + h) * g.W + w) * g.C + c) : 0.0f;
-                        acc = __fadd_rn(acc, dw_product_t<W, GL>(xv, dyv, lut, p.M, p.wlog));
+                        acc = __fadd_rn(acc, dw_product_t<W, GL>(xv, dyv, lut, p.M, p.wlog, p.fmt));
                     }
                     if (++q == g.Q) {
                         q = 0;
@@ -312,6 +325,7 @@ bool dw_tile_ok(const DwGeo &g, const amsim_lut_t lut, int which, const float *t
     if (g.D != 1 || g.R != g.S || (g.R != 3 && g.R != 5) || g.sh != 1 || g.sw != 1 || g.dh != 1 || g.dw != 1)
         return false;
     if (g.C % 4 || lut->width_bits == 32 || (int)lut->narrow_bytes > kDwMaxTileLut) return false;
+    if (lut->exp_bits != 8) return false;         // formats run on the direct kernel
     if (!aligned16(t0) || !aligned16(out)) return false;
     if (which == 2 && !aligned16(t1)) return false;
     return true;
@@ -413,6 +427,7 @@ bool dw_s2_ok(const DwGeo &g, const amsim_lut_t lut, int which, const float *t0,
     // class then has fixed taps)
     if (which == 1 && (g.ph != 1 || g.pw != 1)) return false;
     if (g.C % 4 || lut->width_bits == 32 || (int)lut->narrow_bytes > kDwMaxTileLut) return false;
+    if (lut->exp_bits != 8) return false;         // formats run on the direct kernel
     if (!aligned16(t0) || (which != 2 && !aligned16(out)) || (which == 2 && !aligned16(t1))) return false;
     return true;
 }
@@ -713,6 +728,7 @@ int dw_run(const amsim_conv_desc *desc, int which, const float *t0, const float 
         dp.G = 1;
         dp.table_bytes = (width <= 16 && (int)lut->narrow_bytes <= kDwDirectMaxLut) ? (int)lut->narrow_bytes : 0;
         dp.grid_taps = g.dh == 1 && g.dw == 1;
+        dp.fmt = exp_format(lut->exp_bits);
         if (which == 1 && (size_t)g.C + 16 + (size_t)dp.table_bytes > (size_t)amsim::kMaxSmemPerCta)
             return AMSIM_EUNSUPPORTED;     // the channel flags do not fit shared memory
         if (which == 0) {

@@ -1,6 +1,8 @@
 // Elementwise AMSim products c[i] = AMSim(a[i], b[i]) (ApproxTrain Sec. V-B,
 // Algorithm 2), bit-exact.  HBM-bound: 12 bytes per element; the narrowed LUT
 // (<= 64 KB for M <= 7) stays in L1 through read-only loads.
+#include <algorithm>
+
 #include "amsim_internal.h"
 
 namespace {
@@ -35,6 +37,44 @@ __device__ __forceinline__ uint32_t amsim_bits(uint32_t x, uint32_t y, const voi
     if (zero_in || e0 <= 0) return s;
     if (e >= 255) return s | 0x7F800000u;
     return s | ((uint32_t)e << 23) | (entry & 0x7FFFFFu);
+}
+
+// The same in a (1, E, M) format with E < 8 (Sec. V-B, last paragraph): each
+// operand's exponent is cast first -- fp32 biased exponent e below f.lo is a
+// zero, above f.hi an infinity, else re-biased to c = e - 127 + B -- and
+// Algorithm 2 runs with bias B and all-ones exponent 2^E - 1; the result's
+// exponent is re-biased back to fp32's.
+template <int W>
+__device__ __forceinline__ uint32_t amsim_bits_fmt(uint32_t x, uint32_t y, const void *table, int M, int shift,
+                                                   const ExpFormat &f)
+{
+    const uint32_t s = (x ^ y) & 0x80000000u;
+    const uint32_t ex = (x >> 23) & 0xFFu, ey = (y >> 23) & 0xFFu;
+    const uint32_t fx = x & 0x7FFFFFu, fy = y & 0x7FFFFFu;
+    const bool nan_in = (ex == 255u && fx) || (ey == 255u && fy);
+    const bool inf_in = (int)ex > f.hi || (int)ey > f.hi;          // fp32 infinities included
+    const bool zero_in = (int)ex < f.lo || (int)ey < f.lo;         // zero and denormal included
+    if (nan_in || (inf_in && zero_in)) return 0x7FC00000u;
+    if (inf_in) return s | 0x7F800000u;
+    if (zero_in) return s;
+    const uint32_t idx = ((fx >> (23 - M)) << M) | (fy >> (23 - M));
+    const uint32_t entry = narrowed_at<W>(table, idx) << shift;
+    const int e0 = ((int)ex - 127 + f.bias) + ((int)ey - 127 + f.bias) - f.bias;
+    if (e0 <= 0) return s;
+    if (e0 >= f.all_ones) return s | 0x7F800000u;
+    const int e = e0 + (int)(entry >> 23);
+    if (e >= f.all_ones) return s | 0x7F800000u;
+    return s | ((uint32_t)(e - f.bias + 127) << 23) | (entry & 0x7FFFFFu);
+}
+
+template <int W>
+__global__ void __launch_bounds__(256) amsim_mul_fmt_kernel(const float *__restrict__ a, const float *__restrict__ b,
+                                                            float *c, int64_t n, const void *table, int M, int shift,
+                                                            const ExpFormat f)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride)
+        c[j] = __uint_as_float(amsim_bits_fmt<W>(__float_as_uint(a[j]), __float_as_uint(b[j]), table, M, shift, f));
 }
 
 template <int W>
@@ -84,6 +124,19 @@ extern "C" int amsim_mul(const float *a, const float *b, float *c, int64_t n, am
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (lut->exp_bits != 8) {
+        const ExpFormat f = exp_format(lut->exp_bits);
+        blocks = std::min<int64_t>((n + 255) / 256, cap);
+        if (lut->width_bits == 8)
+            amsim_mul_fmt_kernel<8><<<(unsigned)blocks, 256, 0, st>>>(a, b, c, n, lut->d_narrow, lut->M, lut->shift, f);
+        else if (lut->width_bits == 16)
+            amsim_mul_fmt_kernel<16><<<(unsigned)blocks, 256, 0, st>>>(a, b, c, n, lut->d_narrow, lut->M, lut->shift, f);
+        else
+            amsim_mul_fmt_kernel<32><<<(unsigned)blocks, 256, 0, st>>>(a, b, c, n, lut->d_narrow, lut->M, lut->shift, f);
+        rc = amsim::cuda_status(cudaGetLastError());
+        if (rc == AMSIM_OK) amsim::count_launch();
+        return rc;
+    }
     switch (lut->width_bits) {
     case 8:
         amsim_mul_kernel<8><<<(unsigned)blocks, 256, 0, st>>>(a, b, c, n, lut->d_narrow, lut->M, lut->shift, vec4);

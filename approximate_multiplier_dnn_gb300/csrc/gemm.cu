@@ -444,6 +444,7 @@ void fill_params(const Problem *p, int n, const Plan &pl, amsim_lut_t lut, kern:
     kp.ctas = pl.ctas;
     kp.M = lut->M;
     kp.wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
+    kp.fmt = exp_format(lut->exp_bits);
 }
 
 // Raw-tile operands of dense problems: a tensor map per copy-engine-strided
@@ -522,10 +523,12 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     const bool raw_fits = pl.iters < 0x7FFFFFFFLL;
     const bool conv_raw = raw_fits && n == 1 && p[0].conv && pl.tiles[0] > 0 && encode_tiled();
     // Closed-form products exist only in the raw-tile kernel, which then takes
-    // every problem it can read.
+    // every problem it can read.  Formats with fewer than 8 exponent bits run
+    // on the in-kernel-decode kernels only (their decoders apply the cast).
     const int alu = alu_code(lut);
-    if (conv_raw || (raw_fits && encode_tiled() && all_raw_ok(p, n, pl, true) &&
-                     (alu || !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01)))) {
+    const bool fmt = kp.fmt.on != 0;
+    if (!fmt && (conv_raw || (raw_fits && encode_tiled() && all_raw_ok(p, n, pl, true) &&
+                              (alu || !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01))))) {
         bool raw_gl = false;
         const size_t smem = raw_smem(lut, &raw_gl);
         kern::TmaMaps maps = {};
@@ -584,7 +587,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     bool tma_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
     if (!tma_gl && tma_stages(kern::lut_region_bytes((int)lut->narrow_bytes)) == 0) tma_gl = true;
     const size_t tma_lutb = tma_gl ? 0 : kern::lut_region_bytes((int)lut->narrow_bytes);
-    if (ws && encode_tiled() &&
+    if (!fmt && ws && encode_tiled() &&
         plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 && planes_pay(p, n, pl, ps) &&
         ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps)) {
         uint8_t *base = static_cast<uint8_t *>(ws);
@@ -725,6 +728,7 @@ void phase_bounds(const int *first, int nphase, int n, int ph, int *lo, int *hi)
 bool phased_ok(const Problem *p, int n, int nphase, const Plan &pl, amsim_lut_t lut, bool check_ptr)
 {
     if (nphase < 2 || nphase > kern::kMaxPhases || n > kern::kMaxProblems || pl.ctas < 2) return false;
+    if (lut->exp_bits != 8) return false;           // formats run on the in-kernel-decode kernels
     if (pl.ctas > kern::kMaxPhasedCtas) return false;
     if (pl.iters >= 0x7FFFFFFFLL) return false;     // the raw-tile kernel counts iterations in 32 bits
     if (!encode_tiled()) return false;

@@ -132,6 +132,11 @@ struct KParams {
     long long ph_iter0[kMaxPhases + 1];
     int ph_after[kMaxPhases];
     int cv_ch, cv_S, cv_tiles_img, cv_rows_tile, cv_ybase, cv_ystep, cv_xbase, cv_xstep, cv_N, cv_P, cv_Q, cv_rows;
+    // (1, E, M) format with E < 8 (fmt.on): operands are cast and every stage
+    // takes the rounding product path with the format's rescale and overflow
+    // (in-kernel-decode and single-role kernels only; the host routes such
+    // launches to them)
+    ExpFormat fmt;
 };
 
 // Shared-memory layout (bytes) after the LUT region.
@@ -244,6 +249,38 @@ __device__ __forceinline__ void decode(float v, int M, int offshift, uint32_t &o
     if (e == 255u && f) sb = 0x7FC00000u;
     s = __uint_as_float(sb);
     big |= (e >= 191u);
+}
+
+// Scale bits of an operand after the exponent cast of a (1, E, M) format,
+// re-biased by `off` (see ExpFormat): NaN stays NaN, fp32 infinities and
+// operands above the format's range are signed infinities, zero, denormal and
+// operands below its range signed zeros.  E = 8 (lo 1, hi 254, off 0) gives
+// the fp32 scale of decode().
+__device__ __forceinline__ uint32_t fmt_scale_bits(uint32_t x, int lo, int hi, int off)
+{
+    const uint32_t e = (x >> 23) & 0xFFu, sgn = x & 0x80000000u;
+    if (e == 255u) return (x & 0x7FFFFFu) ? 0x7FC00000u : (sgn | 0x7F800000u);
+    if ((int)e < lo) return sgn;
+    if ((int)e > hi) return sgn | 0x7F800000u;
+    return sgn | ((uint32_t)((int)e + off) << 23);
+}
+
+__device__ __forceinline__ void decode_fmt(float v, int M, int offshift, const ExpFormat &f, int off, uint32_t &o,
+                                           float &s)
+{
+    const uint32_t x = __float_as_uint(v);
+    o = ((x & 0x7FFFFFu) >> (23 - M)) << offshift;
+    s = __uint_as_float(fmt_scale_bits(x, f.lo, f.hi, off));
+}
+
+// The product in a (1, E, M) format from the entry value v = 1.mant * 2^carry
+// and the two cast scales: the flush-to-zero scale product is Algorithm 2's
+// zero test, vscale undoes the scales' re-bias exactly, and products at or
+// above 2^(B + 1) are Algorithm 2's overflow.  Rounded to fp32 (it is exact).
+__device__ __forceinline__ float fmt_product(float v, float s, const ExpFormat &f)
+{
+    const float p = __fmul_rn(__fmul_rn(v, s), f.vscale);
+    return fabsf(p) >= f.lim ? __uint_as_float((__float_as_uint(p) & 0x80000000u) | 0x7F800000u) : p;
 }
 
 // ------------------------------------------------------------------ gather state
@@ -396,6 +433,20 @@ struct Loader {
             scl[k * ST + r] = s;
         }
     }
+    // The same with the exponent cast of a (1, E, M) format.
+    template <int ST>
+    __device__ __forceinline__ void store_fmt(uint32_t *off, float *scl, int M, int offshift, const ExpFormat &f,
+                                              int eoff) const
+    {
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            uint32_t o;
+            float s;
+            decode_fmt(v[e], M, offshift, f, eoff, o, s);
+            off[k_of(e) * ST + row_of(e)] = o;
+            scl[k_of(e) * ST + row_of(e)] = s;
+        }
+    }
 };
 
 // ------------------------------------------------------------------ compute
@@ -408,10 +459,13 @@ __device__ __forceinline__ float accv(const float2 (&acc)[TM / 2][TN], int i, in
 // One stage of BK reduction steps.  acc[p][t] holds rows (2p, 2p+1) of the
 // warp's TM uniform rows for lane column t, so the U scales pair up straight
 // from the vector loads and only the L scale is duplicated (once per column).
-template <int W, bool GL, bool SLOW, int USTR = UST, int LSTR = LST>
+// FMT: a (1, E, M) format with E < 8 -- every product through fmt_product
+// (rounded, then added), whatever the stage's magnitudes.
+template <int W, bool GL, bool SLOW, int USTR = UST, int LSTR = LST, bool FMT = false>
 __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                               const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
-                                              const float *__restrict__ Ls, const uint8_t *lut, int urow, int lcol)
+                                              const float *__restrict__ Ls, const uint8_t *lut, int urow, int lcol,
+                                              const ExpFormat *fmt = nullptr)
 {
 #pragma unroll(kKkUnroll)
     for (int kk = 0; kk < BK; ++kk) {
@@ -442,7 +496,10 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
                     const float2 v = make_float2(expand<W>(ea), expand<W>(eb));
                     const float2 s = fmul2_ftz(sa[ip], sb[t]);
                     float2 &a = acc[2 * ig + ip][t];
-                    if constexpr (SLOW) {
+                    if constexpr (FMT) {
+                        a.x = __fadd_rn(a.x, fmt_product(v.x, s.x, *fmt));
+                        a.y = __fadd_rn(a.y, fmt_product(v.y, s.y, *fmt));
+                    } else if constexpr (SLOW) {
                         // product rounded to fp32 first (infinity on overflow), then added;
                         // the _rn intrinsics are never contracted into an FMA
                         a.x = __fadd_rn(a.x, __fmul_rn(v.x, s.x));
@@ -556,8 +613,13 @@ __device__ __forceinline__ void run_stages(const KParams &p, const ProbParams &q
     ldU.load(q.U, sm.rowU, s0, q.K);
     ldL.load(q.L, sm.rowL, s0, q.K);
     int big = 0;
-    ldU.template store<UST>(sm.Uoff, sm.Uscl, p.M, offU, big);
-    ldL.template store<LST>(sm.Loff, sm.Lscl, p.M, offL, big);
+    if (p.fmt.on) {
+        ldU.template store_fmt<UST>(sm.Uoff, sm.Uscl, p.M, offU, p.fmt, p.fmt.off_u);
+        ldL.template store_fmt<LST>(sm.Loff, sm.Lscl, p.M, offL, p.fmt, p.fmt.off_l);
+    } else {
+        ldU.template store<UST>(sm.Uoff, sm.Uscl, p.M, offU, big);
+        ldL.template store<LST>(sm.Loff, sm.Lscl, p.M, offL, big);
+    }
     int slow = __syncthreads_or(big);
 
     const int urow = wu * TM;
@@ -573,13 +635,21 @@ __device__ __forceinline__ void run_stages(const KParams &p, const ProbParams &q
         const float *Us = sm.Uscl + buf * BK * UST;
         const uint32_t *Lo = sm.Loff + buf * BK * LST;
         const float *Ls = sm.Lscl + buf * BK * LST;
-        if (slow) compute_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+        if (p.fmt.on) compute_stage<W, GL, true, UST, LST, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol, &p.fmt);
+        else if (slow) compute_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
         else compute_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
         int nbig = 0;
         if (more) {
             const int nb = buf ^ 1;
-            ldU.template store<UST>(sm.Uoff + nb * BK * UST, sm.Uscl + nb * BK * UST, p.M, offU, nbig);
-            ldL.template store<LST>(sm.Loff + nb * BK * LST, sm.Lscl + nb * BK * LST, p.M, offL, nbig);
+            if (p.fmt.on) {
+                ldU.template store_fmt<UST>(sm.Uoff + nb * BK * UST, sm.Uscl + nb * BK * UST, p.M, offU, p.fmt,
+                                            p.fmt.off_u);
+                ldL.template store_fmt<LST>(sm.Loff + nb * BK * LST, sm.Lscl + nb * BK * LST, p.M, offL, p.fmt,
+                                            p.fmt.off_l);
+            } else {
+                ldU.template store<UST>(sm.Uoff + nb * BK * UST, sm.Uscl + nb * BK * UST, p.M, offU, nbig);
+                ldL.template store<LST>(sm.Loff + nb * BK * LST, sm.Lscl + nb * BK * LST, p.M, offL, nbig);
+            }
         }
         slow = __syncthreads_or(nbig);
     }

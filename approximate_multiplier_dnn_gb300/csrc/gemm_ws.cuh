@@ -331,10 +331,11 @@ struct PIssue {
     }
 };
 
-// Decode this thread's landed elements of a stage into the consumer layout.
+// Decode this thread's landed elements of a stage into the consumer layout
+// (fmt: with the exponent cast of a (1, E, M) format, scale re-bias eoff).
 template <int R, int ST>
 __device__ __forceinline__ void pdecode(const PMap<R> &map, const float *raw, int tid, uint32_t *off, float *scl,
-                                        int M, int offshift, int &big)
+                                        int M, int offshift, int &big, const ExpFormat &fmt, int eoff)
 {
     constexpr int N = PMap<R>::N, CH = PMap<R>::CH;
 #pragma unroll 1
@@ -347,7 +348,8 @@ __device__ __forceinline__ void pdecode(const PMap<R> &map, const float *raw, in
             const int e = c + j;
             uint32_t o;
             float sc;
-            decode(v[j], M, offshift, o, sc, big);
+            if (fmt.on) decode_fmt(v[j], M, offshift, fmt, eoff, o, sc);
+            else decode(v[j], M, offshift, o, sc, big);
             off[map.k_of(e) * ST + map.row_of(e)] = o;
             scl[map.k_of(e) * ST + map.row_of(e)] = sc;
         }
@@ -440,9 +442,10 @@ __device__ __forceinline__ void ws_producer(const KParams &p, const WsSmem &sm)
         mbar_wait(&sm.empty[slot], ((g / kStages) & 1) ^ 1, aborted);
         const float *raw = sm.raw + (size_t)(g % kRawStages) * ((BU + BL) * BK);
         int big = 0;
-        pdecode<BU, UST>(PMap<BU>(q.u_kfast, ptid), raw, ptid, st_Uoff(sm, slot), st_Uscl(sm, slot), p.M, offU, big);
+        pdecode<BU, UST>(PMap<BU>(q.u_kfast, ptid), raw, ptid, st_Uoff(sm, slot), st_Uscl(sm, slot), p.M, offU, big,
+                         p.fmt, p.fmt.off_u);
         pdecode<BL, LST>(PMap<BL>(q.l_kfast, ptid), raw + BU * BK, ptid, st_Loff(sm, slot), st_Lscl(sm, slot), p.M,
-                         offL, big);
+                         offL, big, p.fmt, p.fmt.off_l);
         const int any = __any_sync(0xFFFFFFFFu, big);
         if (lane == 0) sm.flags[slot * kProducerWarps + pwarp] = any;
         mbar_arrive(&sm.full[slot]);
@@ -702,7 +705,11 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
 #pragma unroll
             for (int w = 0; w < kProducerWarps; ++w) any_big |= fl[w];
             const bool slow = any_big != 0;
-            if (slow)
+            if (p.fmt.on)
+                compute_stage<W, GL, true, UST, LST, true>(acc, st_Uoff(sm, slot), st_Uscl(sm, slot),
+                                                           st_Loff(sm, slot), st_Lscl(sm, slot), lut, urow, lcol,
+                                                           &p.fmt);
+            else if (slow)
                 compute_stage<W, GL, true>(acc, st_Uoff(sm, slot), st_Uscl(sm, slot), st_Loff(sm, slot),
                                            st_Lscl(sm, slot), lut, urow, lcol);
             else

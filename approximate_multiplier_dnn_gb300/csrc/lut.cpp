@@ -201,7 +201,17 @@ int amsim_lut_set_closed_form(amsim_lut_t lut, int on)
 {
     if (!lut) return AMSIM_EINVAL;
     if (on && lut->kind != AMSIM_EXACT && lut->kind != AMSIM_MITCHELL) return AMSIM_EUNSUPPORTED;
+    if (on && lut->exp_bits != 8) return AMSIM_EUNSUPPORTED;
     lut->closed_form = on != 0;
+    return AMSIM_OK;
+}
+
+int amsim_lut_set_exponent_bits(amsim_lut_t lut, int E)
+{
+    if (!lut) return AMSIM_EINVAL;
+    if (E < 1 || E > 8) return AMSIM_EUNSUPPORTED;
+    if (E != 8 && lut->closed_form) return AMSIM_EUNSUPPORTED;
+    lut->exp_bits = E;
     return AMSIM_OK;
 }
 

@@ -214,9 +214,33 @@ int amsim_lut_info(amsim_lut_t lut, int *M, int *width_bits, int *shift);
  * launches on other kernel paths keep reading the table.  Such launches add AMSIM_PATH_CLOSED_FORM to the path bits.  The
  * setting belongs to the handle: calls enqueued after it changes see the new
  * setting.  Errors: AMSIM_EINVAL for a null handle; AMSIM_EUNSUPPORTED when
- * on != 0 and the handle was built from entries or a function.
+ * on != 0 and the handle was built from entries or a function, or simulates
+ * an exponent narrower than 8 bits (amsim_lut_set_exponent_bits).
  */
 int amsim_lut_set_closed_form(amsim_lut_t lut, int on);
+
+/*
+ * The exponent width E of the simulated (1, E, M) multiplier (Sec. V-B, last
+ * paragraph: E from 1 to 8 with an exponent casting function); 8, the
+ * default, is fp32's own exponent.  Casting function taken for E < 8 (IEEE
+ * convention, bias B = 2^(E-1) - 1, biased exponent 0 = zero, 2^E - 1 =
+ * Inf/NaN): an fp32 operand's exponent is re-biased to B; an operand below
+ * the format's smallest normal 2^(1-B) becomes a signed zero and one of
+ * magnitude 2^(B+1) or more a signed infinity; Algorithm 2 runs with bias B
+ * (zero when eA + eB - B <= 0, infinity when it or the carried exponent
+ * reaches 2^E - 1); the product returns as fp32 (exact: B + 1 <= 64) and
+ * accumulation stays fp32.  E = 1 leaves no normal magnitudes: |x| < 2
+ * casts to zero and |x| >= 2 to infinity.  The setting belongs to the
+ * handle and applies to every call enqueued after it: elementwise products,
+ * GEMMs (all variants; phased calls then run phase by phase), Conv2D and
+ * depthwise Conv2D.  Such calls run on the in-kernel-decode GEMM kernels and
+ * the direct depthwise kernel, with every product rounded before it is
+ * added (AMSIM_PATH_INKERNEL_DECODE or AMSIM_PATH_SINGLE_ROLE, or
+ * AMSIM_PATH_DW_DIRECT).  Errors: AMSIM_EINVAL for a null handle,
+ * AMSIM_EUNSUPPORTED for E outside [1,8] or E < 8 on a handle with closed
+ * forms on (amsim_lut_set_closed_form then also refuses while E < 8).
+ */
+int amsim_lut_set_exponent_bits(amsim_lut_t lut, int E);
 
 /* Free the handle's device memory.  NULL is ignored. */
 void amsim_lut_destroy(amsim_lut_t lut);

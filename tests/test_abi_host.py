@@ -161,3 +161,7 @@ def test_wait_status_calls_check_arguments_first(L):
     assert L.amsim_device_errors(None, 1) == am.AMSIM_EINVAL
     assert L.amsim_set_flag_wait_limit(-5) == am.AMSIM_EINVAL
     assert L.amsim_set_flag_wait_limit(20_000_000_000) == am.AMSIM_EINVAL
+
+
+def test_exponent_bits_rejects_null_handle(L):
+    assert L.amsim_lut_set_exponent_bits(None, 5) == am.AMSIM_EINVAL
