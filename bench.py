@@ -276,6 +276,46 @@ def lut_residency(lut):
     return "shared" if nbytes <= 160 * 1024 else "global (L2 gather)"
 
 
+# ---------------------------------------------------------------- tables in global memory
+# A table too large for shared memory (M >= 9) is read through L1TEX and L2.
+# In the row-broadcast schedule the 32 lanes of a warp-lookup read random
+# columns of one table row of R 32-byte sectors, touching R (1 - (1 - 1/R)^32)
+# distinct sectors on average (ncu's l1tex__t_sectors_pipe_lsu_mem_global_op_ld
+# per request agrees within 1 % at M = 9 and 11).  Those sectors pass the L1TEX
+# data path, which returns 4 sectors (128 B) per clock per SM; the ones that
+# miss L1 go to L2, whose sector rate on this GPU ncu reports as 564 sectors per
+# L2 clock at 2.016 GHz (lts__t_sectors.sum.peak_sustained,
+# lts__cycles_elapsed.avg.per_second; profiles/lutgemm_global_table_l2.md).
+L1TEX_SECTORS_PER_CLK_PER_SM = 4
+L2_SECTORS_PER_CLK = 564
+L2_CLK_HZ = 2.016e9
+
+
+def distinct_sectors_per_warp_lookup(M, width_bits):
+    R = max(1.0, (1 << M) * width_bits / 8 / 32)
+    return R * (1.0 - (1.0 - 1.0 / R) ** 32)
+
+
+def global_table_roofline(lut, lut_macs, lut_ms, sms, mhz, smem_roofline):
+    """Roofline of a LUT-GEMM whose table is read from global memory: the
+    algorithmic sectors of its gathers against the L1TEX data path (the bound
+    it runs closest to) and against the L2 sector rate."""
+    info = lut.info()
+    spw = distinct_sectors_per_warp_lookup(info["M"], info["width_bits"])
+    sectors_s = lut_macs / 32.0 * spw / (lut_ms * 1e-3)
+    l1_peak = sms * L1TEX_SECTORS_PER_CLK_PER_SM * mhz * 1e6
+    l2_peak = L2_SECTORS_PER_CLK * L2_CLK_HZ
+    return {"bound": "l1tex", "pipe": "L1TEX data path, 4 sectors (128 B) per clock per SM, for the table's gathers",
+            "achieved": sectors_s * 32 / 1e9, "peak": l1_peak * 32 / 1e9, "unit": "GB/s",
+            "frac": sectors_s / l1_peak, "traffic": None,
+            "sectors_per_warp_lookup": spw,
+            "l2": {"achieved": sectors_s * 32 / 1e9, "peak": l2_peak * 32 / 1e9, "unit": "GB/s",
+                   "frac_if_every_sector_missed_l1": sectors_s / l2_peak,
+                   "note": "ncu measures the sectors that reach L2 per launch (profiles/lutgemm_global_table_l2.md)"},
+            "lookup_roofline_frac": smem_roofline["frac"], "lut_residency": "global (L1TEX/L2 gathers)",
+            "kernel": smem_roofline["kernel"], "sms": sms, "sm_mhz": mhz}
+
+
 # ---------------------------------------------------------------- traffic record
 # sources of the LUT-GEMM kernels (the kernel the traffic records measure);
 # a record holds for one version of them
@@ -494,6 +534,8 @@ def main():
                 "lut_residency": lut_residency(step.lut),
                 "lut_share_of_step": round(lut_share, 4), "sms": sms,
                 "sm_mhz": mhz}
+    if lut_residency(step.lut) != "shared" and not args.closed_form:
+        roofline = global_table_roofline(step.lut, lut_macs, lut_ms, sms, mhz, roofline)
     if args.closed_form:
         kinds = sorted({k for k, _ in luts})
         per_clk = min(CLOSED_FORM_PER_CLK_PER_SM[k] for k in kinds)
