@@ -500,8 +500,9 @@ __global__ void __launch_bounds__(kDwThreads, 2) dw_s2_kernel(const __grid_const
 // dx columns 2J, 2J + 1 (J = lane) of all 8 rows and reads dy columns J, J + 1
 // of the tile's 5 x 33 dy window.  The tap is warp-uniform, so lookups read one
 // table row.  Tiles with |x| >= 2^64, infinities or NaN take a slow computation
-// that visits all nine taps of every output (off-parity taps as zero operands,
-// as the page's zero-operand rule has them).
+// that rounds every product before the add and also visits the off-parity taps
+// of every output (as zero operands, as the page's zero-operand rule has them),
+// after the on-parity taps, which it adds in the fast branch's order.
 constexpr int kSdRows = 8, kSdCols = 64, kSdCB = 16;
 constexpr int kSdWR = kSdRows / 2 + 1;        // dy window rows
 constexpr int kSdWC = kSdCols / 2 + 1;        // dy window columns
@@ -549,28 +550,46 @@ __device__ __forceinline__ void sd_channel(float2 (&acc)[kSdRows], const uint32_
             }
         }
     } else {
-        // all nine taps of each output, products rounded before the add
+        // every product rounded before the add: first the on-parity taps in the
+        // fast branch's order (so finite tiles sum exactly as it does), then the
+        // off-parity taps of each output as zero operands (a signed zero, or NaN
+        // when the tap is infinite or NaN, as the page's zero-operand rule has it)
+#pragma unroll
+        for (int ww = 0; ww < kSdWR; ++ww) {
+            const uint32_t d0 = wr[ww * kSdPW], d1 = wr[ww * kSdPW + 1];
+            const uint32_t b0 = dw_scale_bits(d0), b1 = dw_scale_bits(d1);
+            const float2 sd = make_float2(__uint_as_float(b0), __uint_as_float(b1));
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const int row = k == 0 ? 2 * ww : k == 1 ? 2 * ww - 1 : 2 * ww + 1;
+                const int r = k == 0 ? 1 : k == 1 ? 0 : 2;
+                if (row < 0 || row >= kSdRows) continue;
+                const int t1 = r * 3 + 1, t0 = r * 3 + 0, t2 = r * 3 + 2;
+                const float v0 = dw_expand(lut_ld<W, GL>(lut, d0 - b0 + woff[t1]), mul);
+                const float v1 = dw_expand(lut_ld<W, GL>(lut, d1 - b1 + woff[t0]), mul);
+                const float2 sc = fmul2_ftz(make_float2(wsc[t1], wsc[t0]), sd);
+                acc[row].x = __fadd_rn(acc[row].x, __fmul_rn(v0, sc.x));
+                acc[row].y = __fadd_rn(acc[row].y, __fmul_rn(v1, sc.y));
+                const float v2 = dw_expand(lut_ld<W, GL>(lut, d0 - b0 + woff[t2]), mul);
+                acc[row].y = __fadd_rn(acc[row].y, __fmul_rn(v2, fmul_ftz(wsc[t2], sd.x)));
+            }
+        }
 #pragma unroll
         for (int row = 0; row < kSdRows; ++row)
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                float a = 0.0f;
+            for (int b = 0; b < 2; ++b)
 #pragma unroll
                 for (int r = 0; r < 3; ++r)
 #pragma unroll
                     for (int s = 0; s < 3; ++s) {
-                        const int ry = row + 1 - r, cx = b + 1 - s;   // twice the window offsets
-                        const bool on = (ry & 1) == 0 && (cx & 1) == 0 && ry >= 0;
-                        // cx >= -1: cx even means 0 or 2, i.e. dy column J or J + 1
-                        const uint32_t d = on ? wr[(ry >> 1) * kSdPW + (cx >> 1)] : 0u;
-                        const uint32_t sb = dw_scale_bits(d);
+                        // on-parity: row + 1 - r and b + 1 - s both even (added above)
+                        if (((row + 1 - r) & 1) == 0 && ((b + 1 - s) & 1) == 0) continue;
                         const int t = r * 3 + s;
-                        const float v = dw_expand(lut_ld<W, GL>(lut, d - sb + woff[t]), mul);
-                        a = __fadd_rn(a, __fmul_rn(v, fmul_ftz(wsc[t], __uint_as_float(sb))));
+                        const float v = dw_expand(lut_ld<W, GL>(lut, woff[t]), mul);
+                        const float z = __fmul_rn(v, fmul_ftz(wsc[t], 0.0f));
+                        if (b == 0) acc[row].x = __fadd_rn(acc[row].x, z);
+                        else acc[row].y = __fadd_rn(acc[row].y, z);
                     }
-                if (b == 0) acc[row].x = a;
-                else acc[row].y = a;
-            }
     }
 }
 
