@@ -43,7 +43,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
     const float *src = d.src + (long long)b * d.bs;
     uint32_t *po = d.plane + (size_t)b * 2 * d.K * d.rows_pad;
     float *ps = reinterpret_cast<float *>(po + (size_t)d.K * d.rows_pad);
-    int big = 0;
+    int big = 0, small = 0, zero = 0;
     if (d.rowfast) {
         // rows r .. r + 3 at reduction steps k0 + grp + 16 i
         const int r = r0 + lane4;
@@ -67,6 +67,11 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
                 decode(v[1], p.M, d.offshift, o4.y, s4.y, big);
                 decode(v[2], p.M, d.offshift, o4.z, s4.z, big);
                 decode(v[3], p.M, d.offshift, o4.w, s4.w, big);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    small |= r + e < d.rows && is_small_nonzero(v[e]);
+                    zero |= r + e < d.rows && is_small(v[e]) && !is_small_nonzero(v[e]);
+                }
                 // rows_pad is a multiple of 4: the pad columns of a partial quad may be written
                 *reinterpret_cast<uint4 *>(po + (size_t)k * d.rows_pad + r) = o4;
                 *reinterpret_cast<float4 *>(ps + (size_t)k * d.rows_pad + r) = s4;
@@ -106,7 +111,11 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
             for (int e = 0; e < 4; ++e) {
                 uint32_t o = 0;
                 float sc = 0.0f;                 // outside the operand: offset 0, scale +0
-                if (ok[e]) decode(v[e], p.M, d.offshift, o, sc, big);
+                if (ok[e]) {
+                    decode(v[e], p.M, d.offshift, o, sc, big);
+                    small |= is_small_nonzero(v[e]);
+                    zero |= is_small(v[e]) && !is_small_nonzero(v[e]);
+                }
                 t_off[lane4 + e][grp + 16 * i] = o;
                 t_scl[lane4 + e][grp + 16 * i] = sc;
             }
@@ -131,8 +140,11 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
         }
         sync();
     }
-    // every thread of the warp takes part; one store per warp that saw a large element
+    // every thread of the warp takes part; one store per warp that saw a large
+    // (or a small) element
     if (__any_sync(0xFFFFFFFFu, big) && (tid & 31) == 0) *d.flag = p.epoch;
+    if (__any_sync(0xFFFFFFFFu, small) && (tid & 31) == 0) *d.flag_small = p.epoch;
+    if (__any_sync(0xFFFFFFFFu, zero) && (tid & 31) == 0) *d.flag_zero = p.epoch;
 }
 
 }  // namespace kern

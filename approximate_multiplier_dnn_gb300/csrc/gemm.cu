@@ -124,8 +124,11 @@ EncodeTiled encode_tiled()
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-constexpr size_t kFlagBlock = 256;   // kMaxDecodeJobs plane flags of 8 bytes
-static_assert(kern::kMaxDecodeJobs * 8 <= (int)kFlagBlock, "plane flags fit the block");
+// three 8-byte flags per plane: "an element with |x| >= 2^64" at [j], "an
+// element with 0 < |x| < 2^-63" at [kMaxDecodeJobs + j], "a zero or denormal
+// element" at [2 kMaxDecodeJobs + j]
+constexpr size_t kFlagBlock = 512;
+static_assert(kern::kMaxDecodeJobs * 24 <= (int)kFlagBlock, "plane flags fit the block");
 
 struct PlaneKey {
     const float *src;
@@ -619,6 +622,8 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             d.offshift = k.offshift;
             d.plane = reinterpret_cast<uint32_t *>(planes + ps.off[j]);
             d.flag = flags + j;
+            d.flag_small = flags + kern::kMaxDecodeJobs + j;
+            d.flag_zero = flags + 2 * kern::kMaxDecodeJobs + j;
             d.tiles_r = ceil_div(k.rows, kern::kDecodeTileR);
             d.tiles_k = ceil_div(k.K, kern::kDecodeTileK);
             d.tile0 = dtiles;
@@ -637,6 +642,9 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             kern::ProbParams &q = kp.pr[qi++];
             q.u_big = flags + ju;
             q.l_big = flags + jl;
+            q.u_small = flags + kern::kMaxDecodeJobs + ju;
+            q.l_small = flags + kern::kMaxDecodeJobs + jl;
+            q.u_zero = flags + 2 * kern::kMaxDecodeJobs + ju;
             q.u_bsel = ps.key[ju].nb > 1 ? 1 : 0;
             q.l_bsel = ps.key[jl].nb > 1 ? 1 : 0;
         }

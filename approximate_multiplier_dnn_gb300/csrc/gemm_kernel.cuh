@@ -94,6 +94,9 @@ struct ProbParams {
     // with |x| >= 2^64" flag, raised when it equals the launch epoch, and the
     // batch coordinate factor (0 when one plane serves every batch).
     const unsigned long long *u_big, *l_big;
+    // ... its "holds an element with 0 < |x| < 2^-63" and "holds a zero (or a
+    // denormal)" flags
+    const unsigned long long *u_small, *l_small, *u_zero;
     int u_bsel, l_bsel;
     // Raw-tile kernel: the operand is read with plain loads by the decoders
     // (strides the copy engine cannot take) instead of a tensor box.
@@ -283,6 +286,33 @@ __device__ __forceinline__ float fmt_product(float v, float s, const ExpFormat &
     return fabsf(p) >= f.lim ? __uint_as_float((__float_as_uint(p) & 0x80000000u) | 0x7F800000u) : p;
 }
 
+// An operand whose magnitude is below 2^-63 (zero and denormal included).
+// Stages whose operands are all in [2^-63, 2^64) have every e0 = eA + eB - 127
+// in [1, 253]: no product meets Algorithm 2's zero test or its overflow.  A
+// lane operand may also be zero (or denormal): its scale is a signed zero and
+// the folded product v' * 0 is the signed zero Algorithm 2 gives.
+__device__ __forceinline__ bool is_small(float v) { return ((__float_as_uint(v) >> 23) & 0xFFu) < 64u; }
+// ... and not zero or denormal (biased exponent 1 .. 63).
+__device__ __forceinline__ bool is_small_nonzero(float v) { return ((__float_as_uint(v) >> 23) & 0xFFu) - 1u < 63u; }
+
+// v * sa for a uniform operand with scale bits ub = sign | eA << 23, straight
+// from the narrowed entry: adding the entry's bits (carry at bit 23, mantissa
+// below) to ub gives the fp32 bits of +-1.mant * 2^(eA - 127 + carry), exactly
+// as expand() gives those of 1.mant * 2^carry for ub = bits(1.0f).  Valid while
+// eA + carry <= 254 and eA >= 1: a stage whose operands are all in
+// [2^-63, 2^64) (then eA is in [64, 190]).
+template <int W>
+__device__ __forceinline__ float expand_scaled(uint32_t narrowed, uint32_t ub)
+{
+    uint32_t r;
+    if constexpr (W == 32) {
+        r = narrowed + ub;
+    } else {
+        asm("shl.b32 %0, %1, %2;\n\tadd.u32 %0, %0, %3;" : "=r"(r) : "r"(narrowed), "n"(24 - W), "r"(ub));
+    }
+    return __uint_as_float(r);
+}
+
 // ------------------------------------------------------------------ gather state
 struct KState {
     int k0, k1;
@@ -461,7 +491,13 @@ __device__ __forceinline__ float accv(const float2 (&acc)[TM / 2][TN], int i, in
 // from the vector loads and only the L scale is duplicated (once per column).
 // FMT: a (1, E, M) format with E < 8 -- every product through fmt_product
 // (rounded, then added), whatever the stage's magnitudes.
-template <int W, bool GL, bool SLOW, int USTR = UST, int LSTR = LST, bool FMT = false>
+// FOLD: every uniform operand of the stage is in [2^-63, 2^64) and every lane
+// operand too or zero -- the uniform
+// operand's scale is folded into the rebuilt entry (expand_scaled), so a
+// product is v' * sb with no scale product: the same exact value v * (sa * sb)
+// the general form adds, one FMA per two products instead of a multiply and
+// an FMA, and bit-identical sums.
+template <int W, bool GL, bool SLOW, int USTR = UST, int LSTR = LST, bool FMT = false, bool FOLD = false>
 __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                               const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
                                               const float *__restrict__ Ls, const uint8_t *lut, int urow, int lcol,
@@ -487,25 +523,41 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
             const float4 us = *reinterpret_cast<const float4 *>(Us + kk * USTR + urow + 4 * ig);
             const uint32_t uov[4] = {uo.x, uo.y, uo.z, uo.w};
             const float2 sa[2] = {make_float2(us.x, us.y), make_float2(us.z, us.w)};
+            if constexpr (FOLD) {
+                const uint32_t ub[4] = {__float_as_uint(us.x), __float_as_uint(us.y), __float_as_uint(us.z),
+                                        __float_as_uint(us.w)};
 #pragma unroll
-            for (int ip = 0; ip < 2; ++ip) {
+                for (int ip = 0; ip < 2; ++ip) {
 #pragma unroll
-                for (int t = 0; t < TN; ++t) {
-                    const uint32_t ea = lut_ld<W, GL>(lut, uov[2 * ip] + lo[t]);
-                    const uint32_t eb = lut_ld<W, GL>(lut, uov[2 * ip + 1] + lo[t]);
-                    const float2 v = make_float2(expand<W>(ea), expand<W>(eb));
-                    const float2 s = fmul2_ftz(sa[ip], sb[t]);
-                    float2 &a = acc[2 * ig + ip][t];
-                    if constexpr (FMT) {
-                        a.x = __fadd_rn(a.x, fmt_product(v.x, s.x, *fmt));
-                        a.y = __fadd_rn(a.y, fmt_product(v.y, s.y, *fmt));
-                    } else if constexpr (SLOW) {
-                        // product rounded to fp32 first (infinity on overflow), then added;
-                        // the _rn intrinsics are never contracted into an FMA
-                        a.x = __fadd_rn(a.x, __fmul_rn(v.x, s.x));
-                        a.y = __fadd_rn(a.y, __fmul_rn(v.y, s.y));
-                    } else {
-                        a = ffma2(v, s, a);
+                    for (int t = 0; t < TN; ++t) {
+                        const uint32_t ea = lut_ld<W, GL>(lut, uov[2 * ip] + lo[t]);
+                        const uint32_t eb = lut_ld<W, GL>(lut, uov[2 * ip + 1] + lo[t]);
+                        const float2 v =
+                            make_float2(expand_scaled<W>(ea, ub[2 * ip]), expand_scaled<W>(eb, ub[2 * ip + 1]));
+                        acc[2 * ig + ip][t] = ffma2(v, sb[t], acc[2 * ig + ip][t]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ip = 0; ip < 2; ++ip) {
+#pragma unroll
+                    for (int t = 0; t < TN; ++t) {
+                        const uint32_t ea = lut_ld<W, GL>(lut, uov[2 * ip] + lo[t]);
+                        const uint32_t eb = lut_ld<W, GL>(lut, uov[2 * ip + 1] + lo[t]);
+                        const float2 v = make_float2(expand<W>(ea), expand<W>(eb));
+                        const float2 s = fmul2_ftz(sa[ip], sb[t]);
+                        float2 &a = acc[2 * ig + ip][t];
+                        if constexpr (FMT) {
+                            a.x = __fadd_rn(a.x, fmt_product(v.x, s.x, *fmt));
+                            a.y = __fadd_rn(a.y, fmt_product(v.y, s.y, *fmt));
+                        } else if constexpr (SLOW) {
+                            // product rounded to fp32 first (infinity on overflow), then added;
+                            // the _rn intrinsics are never contracted into an FMA
+                            a.x = __fadd_rn(a.x, __fmul_rn(v.x, s.x));
+                            a.y = __fadd_rn(a.y, __fmul_rn(v.y, s.y));
+                        } else {
+                            a = ffma2(v, s, a);
+                        }
                     }
                 }
             }

@@ -68,11 +68,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
 // below the smallest normal, where the table path's scale product flushes them.
 struct StageFlags {
     int big = 0;
+    int small = 0;          // table decode: an element that blocks the folded form (see bits())
     uint32_t amax = 0u, aminm1 = 0xFFFFFFFFu;
     __device__ __forceinline__ int any() const
     {
         return big | (amax >= 0x5F800000u) | (aminm1 < 0x1FFFFFFFu);
     }
+    // bit 0: the stage takes the rounding slow products; bit 1: it may not
+    // fold the uniform scale into the entry -- a uniform (U) operand below
+    // 2^-63 (zero and denormal included, padded positions among them), or a
+    // lane (L) operand below 2^-63 but not zero (zero L operands give exact
+    // zero products in the folded form too)
+    __device__ __forceinline__ int bits() const { return (any() ? 1 : 0) | (small ? 2 : 0); }
 };
 
 // v * 1 with denormals flushed to signed zero (NaN stays NaN with its
@@ -107,17 +114,21 @@ __device__ __forceinline__ void decode_alu(float v, uint32_t keep, uint32_t &off
 // Decode mode DM: 0 the table's (offset, scale), 1 the closed-form truncated
 // value (no scale), 2 the closed-form truncated fraction and scale; aux is the
 // table offset's shift (DM 0) or the mask of the kept fraction bits.
-template <int DM>
+template <int DM, bool LANE = false>
 __device__ __forceinline__ void decode_as(float v, int M, uint32_t aux, uint32_t &off, float &s, StageFlags &fl)
 {
-    if constexpr (DM == 0) decode(v, M, (int)aux, off, s, fl.big);
-    else decode_alu<DM == 2>(v, aux, off, s, fl);
+    if constexpr (DM == 0) {
+        decode(v, M, (int)aux, off, s, fl.big);
+        fl.small |= LANE ? is_small_nonzero(v) : is_small(v);
+    } else {
+        decode_alu<DM == 2>(v, aux, off, s, fl);
+    }
 }
 
 // Decode a raw R-row tile into off/scl [BK][R].  k-fast tiles are [R][BK]
 // fp32 rows of 64 bytes whose 16-byte chunks the copy engine swizzled as
 // chunk ^ ((row >> 1) & 3); row-fast tiles are [BK][R].
-template <int R, int DM>
+template <int R, int DM, bool LANE = false>
 __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint32_t *off, float *scl, int M,
                                            uint32_t aux, int d, StageFlags &fl)
 {
@@ -131,7 +142,7 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
             for (int i = 0; i < 4; ++i) {
                 uint32_t o;
                 float s;
-                decode_as<DM>(e[i], M, aux, o, s, fl);
+                decode_as<DM, LANE>(e[i], M, aux, o, s, fl);
                 off[(4 * c + i) * R + r] = o;
                 if constexpr (DM != 1) scl[(4 * c + i) * R + r] = s;
             }
@@ -143,10 +154,10 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
             const float4 v = *reinterpret_cast<const float4 *>(raw + (k * R + r4) * 4);
             uint4 o;
             float4 s;
-            decode_as<DM>(v.x, M, aux, o.x, s.x, fl);
-            decode_as<DM>(v.y, M, aux, o.y, s.y, fl);
-            decode_as<DM>(v.z, M, aux, o.z, s.z, fl);
-            decode_as<DM>(v.w, M, aux, o.w, s.w, fl);
+            decode_as<DM, LANE>(v.x, M, aux, o.x, s.x, fl);
+            decode_as<DM, LANE>(v.y, M, aux, o.y, s.y, fl);
+            decode_as<DM, LANE>(v.z, M, aux, o.z, s.z, fl);
+            decode_as<DM, LANE>(v.w, M, aux, o.w, s.w, fl);
             *reinterpret_cast<uint4 *>(off + k * R + r4) = o;
             if constexpr (DM != 1) *reinterpret_cast<float4 *>(scl + k * R + r4) = s;
         }
@@ -166,10 +177,10 @@ __device__ __forceinline__ void raw_decode_blocks(const uint8_t *raw, uint32_t *
         const float4 v = *reinterpret_cast<const float4 *>(raw + ((b * BK + k) * 64 + r4) * 4);
         uint4 o;
         float4 s;
-        decode_as<DM>(v.x, M, aux, o.x, s.x, fl);
-        decode_as<DM>(v.y, M, aux, o.y, s.y, fl);
-        decode_as<DM>(v.z, M, aux, o.z, s.z, fl);
-        decode_as<DM>(v.w, M, aux, o.w, s.w, fl);
+        decode_as<DM, true>(v.x, M, aux, o.x, s.x, fl);
+        decode_as<DM, true>(v.y, M, aux, o.y, s.y, fl);
+        decode_as<DM, true>(v.z, M, aux, o.z, s.z, fl);
+        decode_as<DM, true>(v.w, M, aux, o.w, s.w, fl);
         *reinterpret_cast<uint4 *>(off + k * BL + 64 * b + r4) = o;
         if constexpr (DM != 1) *reinterpret_cast<float4 *>(scl + k * BL + 64 * b + r4) = s;
     }
@@ -408,13 +419,26 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
 
 // A decoded stage of the raw-tile kernel: table entries (W = 8, 16, 32) or
 // closed forms (W = 1 Mitchell, 2 exact).
-template <int W, bool GL, bool SLOW>
+template <int W, bool GL, bool SLOW, bool FOLD = false>
 __device__ __forceinline__ void raw_stage(float2 (&acc)[TM / 2][TN], const uint32_t *Uo, const float *Us,
                                           const uint32_t *Lo, const float *Ls, const uint8_t *lut, int urow,
                                           int lcol)
 {
     if constexpr (W <= 2) compute_stage_alu<W, SLOW>(acc, Uo, Us, Lo, Ls, urow, lcol);
-    else compute_stage<W, GL, SLOW, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    else compute_stage<W, GL, SLOW, BU, BL, false, FOLD>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+}
+
+// One stage of a consumer: the rounding slow products when a decoder flagged
+// bit 0, the folded-scale form when no decoder flagged bit 1 (tables only),
+// else the general form.
+template <int W, bool GL>
+__device__ __forceinline__ void raw_stage_by_flags(int fl, float2 (&acc)[TM / 2][TN], const uint32_t *Uo,
+                                                   const float *Us, const uint32_t *Lo, const float *Ls,
+                                                   const uint8_t *lut, int urow, int lcol)
+{
+    if (fl & 1) raw_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    else if (W > 2 && !(fl & 2)) raw_stage<W, GL, false, (W > 2)>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    else raw_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
 }
 
 // The producer warpgroup: thread 0 also issues the copies, kRawRing - 1 stages
@@ -492,10 +516,10 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
             raw_decode_blocks<DL>(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                               reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         else
-            raw_decode<BL, DL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+            raw_decode<BL, DL, true>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                            reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         mbar_arrive(&sm.raw_empty[rs]);
-        const int any = __any_sync(0xFFFFFFFFu, big.any());
+        const int any = __reduce_or_sync(0xFFFFFFFFu, big.bits());
         if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;
         mbar_arrive(&sm.full[ds]);
         if (p.direct && it + kRawRing < it1) {
@@ -542,13 +566,10 @@ __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lu
                 const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
                 const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
                 const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
-                int any_big = 0;
+                int fl = 0;
 #pragma unroll
-                for (int w = 0; w < kRawDecoders / 32; ++w) any_big |= sm.flags[ds * (kRawDecoders / 32) + w];
-                if (any_big)
-                    raw_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-                else
-                    raw_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                for (int w = 0; w < kRawDecoders / 32; ++w) fl |= sm.flags[ds * (kRawDecoders / 32) + w];
+                raw_stage_by_flags<W, GL>(fl, acc, Uo, Us, Lo, Ls, lut, urow, lcol);
             }
             mbar_arrive(&sm.empty[ds]);
         }
@@ -754,10 +775,10 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
             raw_decode_blocks<DL>(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                               reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         else
-            raw_decode<BL, DL>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
+            raw_decode<BL, DL, true>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
                            reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
         mbar_arrive(&sm.raw_empty[rs]);
-        const int any = __any_sync(0xFFFFFFFFu, big.any());
+        const int any = __reduce_or_sync(0xFFFFFFFFu, big.bits());
         if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;
         mbar_arrive(&sm.full[ds]);
         // the tile after the issue position is the next to be copied: pull its
@@ -819,13 +840,10 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const Phas
                     const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
                     const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
                     const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
-                    int any_big = 0;
+                    int fl = 0;
 #pragma unroll
-                    for (int w = 0; w < kRawDecoders / 32; ++w) any_big |= sm.flags[ds * (kRawDecoders / 32) + w];
-                    if (any_big)
-                        raw_stage<W, false, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-                    else
-                        raw_stage<W, false, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                    for (int w = 0; w < kRawDecoders / 32; ++w) fl |= sm.flags[ds * (kRawDecoders / 32) + w];
+                    raw_stage_by_flags<W, false>(fl, acc, Uo, Us, Lo, Ls, lut, urow, lcol);
                 }
                 mbar_arrive(&sm.empty[ds]);
             }

@@ -134,6 +134,10 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
     for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
         // a problem with an operand of magnitude >= 2^64 rounds every product before adding it
         const bool slow = __ldcg(q.u_big) == p.epoch || __ldcg(q.l_big) == p.epoch;
+        // a problem whose operands lie in [2^-63, 2^64) (lane operands: or are zero)
+        // folds the uniform scale into the entry
+        const bool fold = !slow && __ldcg(q.u_small) != p.epoch && __ldcg(q.u_zero) != p.epoch &&
+                          __ldcg(q.l_small) != p.epoch;
         float2 acc[TM / 2][TN];
 #pragma unroll
         for (int i = 0; i < TM / 2; ++i)
@@ -155,6 +159,8 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
             const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
             if (slow)
                 compute_stage<W, GL, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+            else if (fold)
+                compute_stage<W, GL, false, BU, BL, false, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
             else
                 compute_stage<W, GL, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
             mbar_arrive(&empty[slot]);

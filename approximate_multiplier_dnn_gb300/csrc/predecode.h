@@ -11,7 +11,10 @@
 // power-of-two scale (ApproxTrain Sec. V-B Algorithm 2: the operand half of
 // the product -- sign, biased exponent, top-M fraction bits, with denormals
 // as zero and NaN kept).  A job raises *flag to the launch epoch when an
-// element has |x| >= 2^64, the magnitude above which a product may overflow.
+// element has |x| >= 2^64, the magnitude above which a product may overflow,
+// *flag_small when an element of the operand has 0 < |x| < 2^-63 (a product
+// may meet Algorithm 2's zero test), *flag_zero when one is zero or denormal:
+// a plane with none of the three holds only magnitudes in [2^-63, 2^64).
 #pragma once
 
 #include <cstdint>
@@ -34,7 +37,7 @@ struct DecodeJob {
     int rows_pad;                                // row pitch of a plane, multiple of 4
     int offshift;                                // offset = top-M fraction bits << offshift
     uint32_t *plane;                             // [batch][2][K][rows_pad]
-    unsigned long long *flag;
+    unsigned long long *flag, *flag_small, *flag_zero;
     int tiles_r, tiles_k;                        // 64 x 64 tiles per batch
     // row-fast: a dense operand with unit row stride (read and written along
     // rows); vec: 16-byte loads of 4 consecutive rows (row-fast) or steps

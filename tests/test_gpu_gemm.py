@@ -339,6 +339,47 @@ def test_paths_bit_identical_without_stream_k(amd, luts):
         assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32))
 
 
+@pytest.mark.parametrize("zeros_in", ["A", "B", "both"])
+def test_folded_scale_bit_identical_to_general_form(amd, orc, luts, zeros_in):
+    """Stages whose uniform operands lie in [2^-63, 2^64) and whose lane
+    operands do too or are zero fold the uniform scale into the rebuilt entry
+    (raw-tile and plane kernels); the in-kernel-decode kernel keeps the general
+    form (scale product, then FMA).  Both add the same exact products in the
+    same order, so outputs are bit-identical -- with ReLU-like zeros in either
+    operand (zero uniform operands send their stages to the general form) and
+    a few tiny ones (a product below the zero test: general form too)."""
+    import torch
+    rng = np.random.default_rng(16)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    m, n, k = 64 * sms, 200, 100          # one 64 x 256 tile per SM: no stream-K on any path
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    if zeros_in in ("A", "both"):
+        A[rng.random(A.shape) < 0.5] = 0.0
+        A[0, 3] = np.float32(1e-25)
+    if zeros_in in ("B", "both"):
+        B[rng.random(B.shape) < 0.5] = 0.0
+        B[7, 5] = np.float32(-3e-24)
+    lut = luts("mitchell", 7)
+    base = gpu_gemm(amd, lut, A, B, False, False)
+    base_path = amd.amsim_last_path()
+    assert base_path & (amd.AMSIM_PATH_RAW_TILES | amd.AMSIM_PATH_PLANES), base_path
+    # the same A with a leading dimension of k + 1 (not a multiple of 4 elements,
+    # too large for plain loads): the in-kernel-decode kernel
+    A1 = np.zeros((m, k + 1), np.float32)
+    A1[:, :k] = A
+    dA1, dB = to_dev(A1), to_dev(B)
+    C = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    nb = amd.amsim_gemm_workspace_size("N", "N", m, n, k, 1, lut)
+    amd.amsim_gemm("N", "N", m, n, k, 1.0, dA1, k + 1, dB, n, 0.0, C, n, lut, ws=amd.workspace(nb))
+    torch.cuda.synchronize()
+    path = amd.amsim_last_path()
+    assert path & (amd.AMSIM_PATH_INKERNEL_DECODE | amd.AMSIM_PATH_SINGLE_ROLE), path
+    assert np.array_equal(base.view(np.uint32), C.cpu().numpy().view(np.uint32))
+    rows = np.array([0, 7, m - 1])
+    ref, sa = orc.gemm("mitchell", 7, A, B, rows=rows)
+    assert_close(base[rows], ref, sa, f"folded, zeros in {zeros_in}")
+
+
 RAW_SHAPES = [(64, 256, 16), (300, 500, 2000), (130, 520, 40), (257, 10, 500), (5, 7, 4), (700, 90, 332)]
 # (shape, transA, transB) whose leading dimensions are multiples of 4 elements
 # (what selects this path): lda = m for a transposed A, else k; ldb = k for a
