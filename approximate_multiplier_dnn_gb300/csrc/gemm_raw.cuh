@@ -429,15 +429,15 @@ __device__ __forceinline__ void raw_stage(float2 (&acc)[TM / 2][TN], const uint3
 }
 
 // One stage of a consumer: the rounding slow products when a decoder flagged
-// bit 0, the folded-scale form when no decoder flagged bit 1 (tables only),
-// else the general form.
+// bit 0, the folded-scale form when no decoder flagged bit 1 (tables in
+// shared memory only), else the general form.
 template <int W, bool GL>
 __device__ __forceinline__ void raw_stage_by_flags(int fl, float2 (&acc)[TM / 2][TN], const uint32_t *Uo,
                                                    const float *Us, const uint32_t *Lo, const float *Ls,
                                                    const uint8_t *lut, int urow, int lcol)
 {
     if (fl & 1) raw_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-    else if (W > 2 && !(fl & 2)) raw_stage<W, GL, false, (W > 2)>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    else if (W > 2 && !GL && !(fl & 2)) raw_stage<W, GL, false, (W > 2 && !GL)>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
     else raw_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
 }
 

@@ -135,8 +135,10 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
         // a problem with an operand of magnitude >= 2^64 rounds every product before adding it
         const bool slow = __ldcg(q.u_big) == p.epoch || __ldcg(q.l_big) == p.epoch;
         // a problem whose operands lie in [2^-63, 2^64) (lane operands: or are zero)
-        // folds the uniform scale into the entry
-        const bool fold = !slow && __ldcg(q.u_small) != p.epoch && __ldcg(q.u_zero) != p.epoch &&
+        // folds the uniform scale into the entry -- with the table in shared memory;
+        // gathers from a table in global memory are bound by their misses, and
+        // measured slower in the folded form
+        const bool fold = !GL && !slow && __ldcg(q.u_small) != p.epoch && __ldcg(q.u_zero) != p.epoch &&
                           __ldcg(q.l_small) != p.epoch;
         float2 acc[TM / 2][TN];
 #pragma unroll
