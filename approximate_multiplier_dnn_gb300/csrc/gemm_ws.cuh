@@ -169,7 +169,7 @@ struct WsSmem {
     RowInfo *rowU, *rowL;
     uint64_t *full, *empty;
     uint64_t *red;         // completion of the stream-K reduction's bulk copies
-    int *flags;            // [kStages][kProducerWarps]: a stage holds |x| >= 2^64
+    int *flags;            // [kStages][kProducerWarps]: bit 0 a stage holds |x| >= 2^64, bit 1 no folded form
 };
 
 __device__ __forceinline__ uint32_t *st_Uoff(const WsSmem &s, int slot)
@@ -333,9 +333,11 @@ struct PIssue {
 
 // Decode this thread's landed elements of a stage into the consumer layout
 // (fmt: with the exponent cast of a (1, E, M) format, scale re-bias eoff).
-template <int R, int ST>
+// nofold collects the elements that keep the stage in the general form (a
+// uniform operand below 2^-63, zeros included; a nonzero lane operand below it).
+template <int R, int ST, bool LANE>
 __device__ __forceinline__ void pdecode(const PMap<R> &map, const float *raw, int tid, uint32_t *off, float *scl,
-                                        int M, int offshift, int &big, const ExpFormat &fmt, int eoff)
+                                        int M, int offshift, int &big, int &nofold, const ExpFormat &fmt, int eoff)
 {
     constexpr int N = PMap<R>::N, CH = PMap<R>::CH;
 #pragma unroll 1
@@ -348,8 +350,12 @@ __device__ __forceinline__ void pdecode(const PMap<R> &map, const float *raw, in
             const int e = c + j;
             uint32_t o;
             float sc;
-            if (fmt.on) decode_fmt(v[j], M, offshift, fmt, eoff, o, sc);
-            else decode(v[j], M, offshift, o, sc, big);
+            if (fmt.on) {
+                decode_fmt(v[j], M, offshift, fmt, eoff, o, sc);
+            } else {
+                decode(v[j], M, offshift, o, sc, big);
+                nofold |= LANE ? is_small_nonzero(v[j]) : is_small(v[j]);
+            }
             off[map.k_of(e) * ST + map.row_of(e)] = o;
             scl[map.k_of(e) * ST + map.row_of(e)] = sc;
         }
@@ -441,12 +447,13 @@ __device__ __forceinline__ void ws_producer(const KParams &p, const WsSmem &sm)
         const int slot = g % kStages;
         mbar_wait(&sm.empty[slot], ((g / kStages) & 1) ^ 1, aborted);
         const float *raw = sm.raw + (size_t)(g % kRawStages) * ((BU + BL) * BK);
-        int big = 0;
-        pdecode<BU, UST>(PMap<BU>(q.u_kfast, ptid), raw, ptid, st_Uoff(sm, slot), st_Uscl(sm, slot), p.M, offU, big,
-                         p.fmt, p.fmt.off_u);
-        pdecode<BL, LST>(PMap<BL>(q.l_kfast, ptid), raw + BU * BK, ptid, st_Loff(sm, slot), st_Lscl(sm, slot), p.M,
-                         offL, big, p.fmt, p.fmt.off_l);
-        const int any = __any_sync(0xFFFFFFFFu, big);
+        int big = 0, nofold = 0;
+        pdecode<BU, UST, false>(PMap<BU>(q.u_kfast, ptid), raw, ptid, st_Uoff(sm, slot), st_Uscl(sm, slot), p.M, offU,
+                                big, nofold, p.fmt, p.fmt.off_u);
+        pdecode<BL, LST, true>(PMap<BL>(q.l_kfast, ptid), raw + BU * BK, ptid, st_Loff(sm, slot), st_Lscl(sm, slot),
+                               p.M, offL, big, nofold, p.fmt, p.fmt.off_l);
+        // bit 0: rounding slow products; bit 1: no folded-scale form
+        const int any = __reduce_or_sync(0xFFFFFFFFu, (big ? 1 : 0) | (nofold ? 2 : 0));
         if (lane == 0) sm.flags[slot * kProducerWarps + pwarp] = any;
         mbar_arrive(&sm.full[slot]);
     }
@@ -701,11 +708,15 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
                 continue;
             }
             const int *fl = sm.flags + slot * kProducerWarps;
-            int any_big = 0;
+            int fb = 0;
 #pragma unroll
-            for (int w = 0; w < kProducerWarps; ++w) any_big |= fl[w];
-            const bool slow = any_big != 0;
-            if (p.fmt.on)
+            for (int w = 0; w < kProducerWarps; ++w) fb |= fl[w];
+            const bool slow = (fb & 1) != 0;
+            if (!p.fmt.on && !GL && fb == 0)
+                compute_stage<W, GL, false, UST, LST, false, true>(acc, st_Uoff(sm, slot), st_Uscl(sm, slot),
+                                                                   st_Loff(sm, slot), st_Lscl(sm, slot), lut, urow,
+                                                                   lcol);
+            else if (p.fmt.on)
                 compute_stage<W, GL, true, UST, LST, true>(acc, st_Uoff(sm, slot), st_Uscl(sm, slot),
                                                            st_Loff(sm, slot), st_Lscl(sm, slot), lut, urow, lcol,
                                                            &p.fmt);

@@ -343,11 +343,12 @@ def test_paths_bit_identical_without_stream_k(amd, luts):
 def test_folded_scale_bit_identical_to_general_form(amd, orc, luts, zeros_in):
     """Stages whose uniform operands lie in [2^-63, 2^64) and whose lane
     operands do too or are zero fold the uniform scale into the rebuilt entry
-    (raw-tile and plane kernels); the in-kernel-decode kernel keeps the general
-    form (scale product, then FMA).  Both add the same exact products in the
-    same order, so outputs are bit-identical -- with ReLU-like zeros in either
-    operand (zero uniform operands send their stages to the general form) and
-    a few tiny ones (a product below the zero test: general form too)."""
+    (raw-tile, plane and in-kernel-decode kernels, tables in shared memory);
+    the closed form computes the same products in registers with the general
+    order.  All add the same exact products in the same order, so outputs are
+    bit-identical -- with ReLU-like zeros in either operand (zero uniform
+    operands send their stages to the general form) and a few tiny ones (a
+    product below the zero test: general form too)."""
     import torch
     rng = np.random.default_rng(16)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -363,6 +364,14 @@ def test_folded_scale_bit_identical_to_general_form(amd, orc, luts, zeros_in):
     base = gpu_gemm(amd, lut, A, B, False, False)
     base_path = amd.amsim_last_path()
     assert base_path & (amd.AMSIM_PATH_RAW_TILES | amd.AMSIM_PATH_PLANES), base_path
+    # the closed form on the same plan: no table, the general order
+    cf = amd.Lut.build("mitchell", 7).set_closed_form(True)
+    try:
+        alu = gpu_gemm(amd, cf, A, B, False, False)
+        assert amd.amsim_last_path() & amd.AMSIM_PATH_CLOSED_FORM
+    finally:
+        cf.close()
+    assert np.array_equal(base.view(np.uint32), alu.view(np.uint32))
     # the same A with a leading dimension of k + 1 (not a multiple of 4 elements,
     # too large for plain loads): the in-kernel-decode kernel
     A1 = np.zeros((m, k + 1), np.float32)
