@@ -66,6 +66,12 @@ constexpr int NLE = BL * BK / NT;  // L elements loaded per thread per stage
 static_assert(TM % 4 == 0 && TN % 4 == 0, "micro-tile");
 static_assert(NT % BK == 0 && (NT % BU == 0 || BU % NT == 0) && (NT % BL == 0 || BL % NT == 0), "loader mapping");
 static_assert(WU * WL * 32 == NT, "warp layout");
+// Lane columns: register column t of a lane is column lane*4 + col_of(t) of
+// its warp's 32*TN-column span -- groups of four columns, the groups 128
+// columns apart -- so each 128-bit load of one group reads 512 contiguous
+// bytes across the warp (four wavefronts, no bank conflicts) whatever TN is.
+constexpr int kColGroup = 128;
+__host__ __device__ constexpr int col_of(int t) { return (t >> 2) * kColGroup + (t & 3); }
 
 struct RowInfo {
     int y, x;
@@ -509,8 +515,8 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
         float2 sb[TN];
 #pragma unroll
         for (int t4 = 0; t4 < TN / 4; ++t4) {
-            const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * LSTR + lcol + 4 * t4);
-            const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * LSTR + lcol + 4 * t4);
+            const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * LSTR + lcol + kColGroup * t4);
+            const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * LSTR + lcol + kColGroup * t4);
             lo[4 * t4 + 0] = o.x; lo[4 * t4 + 1] = o.y; lo[4 * t4 + 2] = o.z; lo[4 * t4 + 3] = o.w;
             sb[4 * t4 + 0] = make_float2(sc.x, sc.x);
             sb[4 * t4 + 1] = make_float2(sc.y, sc.y);
@@ -591,14 +597,14 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
     const bool aligned = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
     const bool vec_l = aligned && q.c_sl == 1 && (q.c_su & 3) == 0;
     const bool vec_u = aligned && q.c_su == 1 && (q.c_sl & 3) == 0;
-    if (vec_l && l0 + TN <= nL) {
+    if (vec_l && l0 + col_of(TN - 1) < nL) {
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             const int u = u0 + i;
             if (u >= nU) break;
 #pragma unroll
             for (int t4 = 0; t4 < TN / 4; ++t4) {
-                float4 *dst = reinterpret_cast<float4 *>(C + (long long)u * q.c_su + l0 + 4 * t4);
+                float4 *dst = reinterpret_cast<float4 *>(C + (long long)u * q.c_su + l0 + kColGroup * t4);
                 const float4 a = acc4(acc, i, 4 * t4);
                 float4 r = make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w);
                 if (beta != 0.0f) {
@@ -612,7 +618,7 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
     } else if (vec_u && u0 + TM <= nU) {
 #pragma unroll
         for (int t = 0; t < TN; ++t) {
-            const int l = l0 + t;
+            const int l = l0 + col_of(t);
             if (l >= nL) break;
             float *col = C + (long long)l * q.c_sl + u0;
 #pragma unroll
@@ -635,7 +641,7 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
             if (u >= nU) break;
 #pragma unroll
             for (int t = 0; t < TN; ++t) {
-                const int l = l0 + t;
+                const int l = l0 + col_of(t);
                 if (l >= nL) break;
                 float *dst = C + (long long)u * q.c_su + (long long)l * q.c_sl;
                 float r = alpha * accv(acc, i, t);
@@ -675,7 +681,7 @@ __device__ __forceinline__ void run_stages(const KParams &p, const ProbParams &q
     int slow = __syncthreads_or(big);
 
     const int urow = wu * TM;
-    const int lcol = wl * 32 * TN + lane * TN;
+    const int lcol = wl * 32 * TN + lane * 4;
     for (int kt = s0; kt < s1; ++kt) {
         const int buf = (kt - s0) & 1;
         const bool more = kt + 1 < s1;
@@ -791,18 +797,18 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
         run_stages<W, GL>(p, q, sm, b, u_tile0, l_tile0, s0, s1, acc);
 
         const int u0 = u_tile0 + wu * TM;
-        const int l0 = l_tile0 + wl * 32 * TN + lane * TN;
+        const int l0 = l_tile0 + wl * 32 * TN + lane * 4;
         if (s0 == 0 && s1 == S) {
             store_tile(q, acc, b, u0, l0);
         } else {
             // partial tile: slot 0 holds the CTA's first segment, slot 1 its last
             float *slot = p.ws + ((long long)blockIdx.x * 2 + (first_segment ? 0 : 1)) * (BU * BL);
-            const int ur = wu * TM, lr = wl * 32 * TN + lane * TN;
+            const int ur = wu * TM, lr = wl * 32 * TN + lane * 4;
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
                 for (int t4 = 0; t4 < TN / 4; ++t4)
-                    *reinterpret_cast<float4 *>(slot + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
+                    *reinterpret_cast<float4 *>(slot + (ur + i) * BL + lr + kColGroup * t4) = acc4(acc, i, 4 * t4);
         }
         first_segment = false;
         it += s1 - s0;

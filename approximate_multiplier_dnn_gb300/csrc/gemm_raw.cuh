@@ -356,10 +356,10 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
         float2 sb[TN];
 #pragma unroll
         for (int t4 = 0; t4 < TN / 4; ++t4) {
-            const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * BL + lcol + 4 * t4);
+            const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * BL + lcol + kColGroup * t4);
             lo[4 * t4 + 0] = o.x; lo[4 * t4 + 1] = o.y; lo[4 * t4 + 2] = o.z; lo[4 * t4 + 3] = o.w;
             if constexpr (KIND == 1) {
-                const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * BL + lcol + 4 * t4);
+                const float4 sc = *reinterpret_cast<const float4 *>(Ls + kk * BL + lcol + kColGroup * t4);
                 sb[4 * t4 + 0] = make_float2(sc.x, sc.x);
                 sb[4 * t4 + 1] = make_float2(sc.y, sc.y);
                 sb[4 * t4 + 2] = make_float2(sc.z, sc.z);
@@ -545,7 +545,7 @@ __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lu
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
-    const int lcol = wl * 32 * TN + lane * TN;
+    const int lcol = wl * 32 * TN + lane * 4;
     uint32_t g = 0;
     bool aborted = false;
     CutTile cut0, cut1;
@@ -816,7 +816,7 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const Phas
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
-    const int lcol = wl * 32 * TN + lane * TN;
+    const int lcol = wl * 32 * TN + lane * 4;
     const long long total_tiles = p.pr[p.nprob - 1].tile0 + p.pr[p.nprob - 1].tiles;
     uint32_t g = 0;
     bool aborted = false;
@@ -859,7 +859,7 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const Phas
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
                     for (int t4 = 0; t4 < TN / 4; ++t4)
-                        __stcg(reinterpret_cast<float4 *>(mine + (urow + i) * BL + lcol + 4 * t4), acc4(acc, i, 4 * t4));
+                        __stcg(reinterpret_cast<float4 *>(mine + (urow + i) * BL + lcol + kColGroup * t4), acc4(acc, i, 4 * t4));
             }
             // every consumer's slot writes precede the barrier; thread 0's
             // fence and ticket update then publish them (cumulative release)
@@ -889,7 +889,7 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const Phas
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
                     for (int t4 = 0; t4 < TN / 4; ++t4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(part + (urow + i) * BL + lcol + 4 * t4));
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(part + (urow + i) * BL + lcol + kColGroup * t4));
                         float2 &lo = sum[i >> 1][4 * t4], &l1 = sum[i >> 1][4 * t4 + 1];
                         float2 &l2 = sum[i >> 1][4 * t4 + 2], &l3 = sum[i >> 1][4 * t4 + 3];
                         if (i & 1) { lo.y += v.x; l1.y += v.y; l2.y += v.z; l3.y += v.w; }

@@ -124,7 +124,7 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
-    const int lcol = wl * 32 * TN + lane * TN;
+    const int lcol = wl * 32 * TN + lane * 4;
     const int S = p.stages;
     int slot = 0;
     uint32_t phase = 0;

@@ -529,8 +529,8 @@ __device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbPar
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
     const int u0 = u_tile0 + wu * TM;
-    const int l0 = l_tile0 + wl * 32 * TN + lane * TN;
-    const int ur = wu * TM, lr = wl * 32 * TN + lane * TN;
+    const int l0 = l_tile0 + wl * 32 * TN + lane * 4;
+    const int ur = wu * TM, lr = wl * 32 * TN + lane * 4;
     if (s0 == 0 && s1 == q.kt_total) {
         store_tile(q, acc, b, u0, l0);
         return;
@@ -541,7 +541,7 @@ __device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbPar
     for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int t4 = 0; t4 < TN / 4; ++t4)
-            *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + 4 * t4) = acc4(acc, i, 4 * t4);
+            *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + kColGroup * t4) = acc4(acc, i, 4 * t4);
     if (!p.fused) return;
     // every consumer's slot writes precede the barrier; the release store of
     // one thread then publishes all of them (release is cumulative)
@@ -685,7 +685,7 @@ __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
-    const int lcol = wl * 32 * TN + lane * TN;
+    const int lcol = wl * 32 * TN + lane * 4;
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : sm.lut;
     uint32_t g = 0;
     bool aborted = false;
