@@ -152,6 +152,7 @@ AMSIM_PATH_PHASED = 256
 AMSIM_PATH_CLOSED_FORM = 512
 AMSIM_PATH_DW_TILES = 1024
 AMSIM_PATH_DW_DIRECT = 2048
+AMSIM_PATH_WIDE_TILES = 4096
 
 
 def amsim_last_path() -> int:

@@ -54,14 +54,15 @@ struct Plan {
     size_t sk_bytes;   // scratch stream-K would use
 };
 
-Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail)
+// Launch plan for tiles of shape tc (the narrow shape unless given).
+Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail, const kern::TileCfg &tc = kern::kNarrowTiles)
 {
     Plan pl = {};
     for (int i = 0; i < n; ++i) {
         const bool empty = p[i].U.rows == 0 || p[i].L.rows == 0 || p[i].batch == 0;
-        pl.tiles_u[i] = std::max(1, ceil_div(p[i].U.rows, BU));
-        pl.tiles_l[i] = std::max(1, ceil_div(p[i].L.rows, BL));
-        pl.kt[i] = std::max(1, ceil_div(p[i].K, BK));
+        pl.tiles_u[i] = std::max(1, ceil_div(p[i].U.rows, tc.bu));
+        pl.tiles_l[i] = std::max(1, ceil_div(p[i].L.rows, tc.bl));
+        pl.kt[i] = std::max(1, ceil_div(p[i].K, tc.bk));
         pl.tiles[i] = empty ? 0 : (long long)pl.tiles_u[i] * pl.tiles_l[i] * p[i].batch;
         pl.iter0[i] = pl.iters;
         pl.iters += pl.tiles[i] * pl.kt[i];
@@ -69,7 +70,7 @@ Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail)
     }
     pl.ctas = (int)std::min<long long>(std::min(sms, kern::kMaxFixupParts), pl.iters);
     // two partial-sum slots and two flags per CTA
-    pl.sk_bytes = (size_t)2 * pl.ctas * BU * BL * sizeof(float) + (size_t)2 * pl.ctas * sizeof(unsigned long long);
+    pl.sk_bytes = (size_t)2 * pl.ctas * tc.bu * tc.bl * sizeof(float) + (size_t)2 * pl.ctas * sizeof(unsigned long long);
     // Stream-K over (tile, stage) iterations with one persistent CTA per SM,
     // unless the tiles fit in one wave that fills the SMs nearly whole (then
     // one CTA per tile).  Persistent CTAs stage the LUT once and keep the
@@ -206,23 +207,50 @@ bool planes_pay(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
     return planes_bytes_per_mac(p, n, pl, ps) <= 0.05;
 }
 
-// Ring depth of the TMA kernel beside a LUT region of lut_bytes (0 if none fits).
-int tma_stages(size_t lut_bytes)
+// Ring depth of the TMA kernel with tiles of shape tc beside a LUT region of
+// lut_bytes (0 if none fits).
+int tma_stages(size_t lut_bytes, const kern::TileCfg &tc)
 {
-    const long long room = (long long)kMaxSmemPerCta - kern::tma_smem_bytes((int)lut_bytes, 0);
-    long long s = room / kern::kTmaStageBytes;
+    const long long room = (long long)kMaxSmemPerCta - kern::tma_cfg_smem_bytes(tc, (int)lut_bytes, 0);
+    long long s = room / kern::tma_stage_bytes(tc);
     if (s > kern::kTmaMaxStages) s = kern::kTmaMaxStages;
-    return s >= kern::kTmaMinStages ? (int)s : 0;
+    return s >= kern::tma_min_stages(tc) ? (int)s : 0;
 }
 
-int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_rows)
+// Tile shape and LUT placement of the predecoded (TMA) kernel: the wide shape
+// with the table in shared memory when a ring of its minimum depth fits beside
+// it, else the narrow shape with the table in shared memory, else the wide
+// shape reading the table from global memory.  Measured on GB300 (4096^3,
+// Mitchell): M = 7 runs 6.5 % faster and M = 9 25 % faster on wide tiles; at
+// M = 8 (a 128 KB table) the wide ring does not fit, and the narrow kernel's
+// two stages beat the wide kernel reading the table from global memory.
+struct TmaChoice {
+    kern::TileCfg tc;
+    bool wide, gl;
+    int stages;
+    size_t lutb;   // LUT region in shared memory (0 when read from global)
+};
+
+TmaChoice tma_choice(amsim_lut_t lut)
+{
+    TmaChoice c = {kern::kWideTiles, true, true, 0, 0};
+    if (lut->narrow_bytes <= (size_t)kMaxSmemLut) {
+        const size_t lutb = kern::lut_region_bytes((int)lut->narrow_bytes);
+        if (const int s = tma_stages(lutb, kern::kWideTiles)) return {kern::kWideTiles, true, false, s, lutb};
+        if (const int s = tma_stages(lutb, kern::kNarrowTiles)) return {kern::kNarrowTiles, false, false, s, lutb};
+    }
+    c.stages = tma_stages(0, kern::kWideTiles);
+    return c;
+}
+
+int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_rows, int box_k)
 {
     EncodeTiled enc = encode_tiled();
     if (!enc) return AMSIM_EUNSUPPORTED;
     const cuuint64_t pitch = (cuuint64_t)rows_pad(k.rows) * 4;
     const cuuint64_t dims[4] = {(cuuint64_t)k.rows, (cuuint64_t)k.K, 2, (cuuint64_t)k.nb};
     const cuuint64_t strides[3] = {pitch, pitch * (cuuint64_t)k.K, pitch * (cuuint64_t)k.K * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)box_rows, (cuuint32_t)kern::BK, 2, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)box_rows, (cuuint32_t)box_k, 2, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -262,9 +290,16 @@ int encode_raw_spec(CUtensorMap *map, const TmaRawMap &m)
     return r == CUDA_SUCCESS ? AMSIM_OK : AMSIM_EUNSUPPORTED;
 }
 
-int launch_tma(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
-               cudaStream_t st)
+int launch_tma(int width, bool wide, const kern::KParams &kp, const kern::TmaMaps &maps, bool gl, dim3 grid,
+               size_t smem, cudaStream_t st)
 {
+    if (wide) {
+        switch (width) {
+        case 8: return kern_wide::launch_tma_w8(kp, maps, gl, grid, smem, st);
+        case 16: return kern_wide::launch_tma_w16(kp, maps, gl, grid, smem, st);
+        default: return kern_wide::launch_tma_w32(kp, maps, gl, grid, smem, st);
+        }
+    }
     switch (width) {
     case 8: return kern::launch_tma_w8(kp, maps, gl, grid, smem, st);
     case 16: return kern::launch_tma_w16(kp, maps, gl, grid, smem, st);
@@ -275,22 +310,23 @@ int launch_tma(int width, const kern::KParams &kp, const kern::TmaMaps &maps, bo
 // The predecode pass, then the TMA LUT-GEMM over its planes: stream-K plans
 // launch cooperatively and finish cut tiles inside the kernel, else (or
 // without a cooperative launch) the separate fixup kernel does.
-int run_tma(int width, kern::KParams &tp, const kern::TmaMaps &maps, const kern::DecodeParams &dp, bool gl,
-            long long blocks, size_t smem, int sms, bool streamk, cudaStream_t stream)
+int run_tma(int width, bool wide, kern::KParams &tp, const kern::TmaMaps &maps, const kern::DecodeParams &dp,
+            bool gl, long long blocks, size_t smem, int sms, bool streamk, cudaStream_t stream)
 {
     const dim3 grid((unsigned)blocks);
     int rc = kern::launch_predecode(dp, sms, stream);
     if (rc) return rc;
-    const int base = AMSIM_PATH_PLANES | (streamk ? AMSIM_PATH_STREAMK : 0);
+    const int base = AMSIM_PATH_PLANES | (streamk ? AMSIM_PATH_STREAMK : 0) | (wide ? AMSIM_PATH_WIDE_TILES : 0);
     tp.fused = streamk ? 1 : 0;
-    rc = launch_tma(width, tp, maps, gl, grid, smem, stream);
+    rc = launch_tma(width, wide, tp, maps, gl, grid, smem, stream);
     if (rc == kern::AMSIM_ENOTCOOP) {
         tp.fused = 0;
-        rc = launch_tma(width, tp, maps, gl, grid, smem, stream);
+        rc = launch_tma(width, wide, tp, maps, gl, grid, smem, stream);
     }
     if (rc) return rc;
     g_last_path |= base | (streamk && !tp.fused ? AMSIM_PATH_FIXUP : 0);
-    return streamk && !tp.fused ? kern::launch_fixup(tp, tp.ctas - 1, stream) : AMSIM_OK;
+    if (!streamk || tp.fused) return AMSIM_OK;
+    return wide ? kern_wide::launch_fixup(tp, tp.ctas - 1, stream) : kern::launch_fixup(tp, tp.ctas - 1, stream);
 }
 
 // ------------------------------------------------------------------ raw tiles
@@ -393,10 +429,12 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     } else if (lut && encode_tiled() && n == 1 && p[0].conv) {
         // convolution tiles are copied in place as tensor boxes
     } else if (lut && encode_tiled()) {
+        // the predecoded kernel's own plan (its tile shape's stream-K slots), then the planes
         const int wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
+        const Plan tpl = make_plan(p, n, sms, (size_t)-1, tma_choice(lut).tc);
         PlaneSet ps;
-        if (plan_planes(p, n, pl, lut->M, wlog, &ps) && ps.n > 0 && planes_pay(p, n, pl, ps))
-            need += tma_extra(pl.ws_bytes, ps);
+        if (plan_planes(p, n, tpl, lut->M, wlog, &ps) && ps.n > 0 && planes_pay(p, n, tpl, ps))
+            need = std::max(need, tpl.ws_bytes + tma_extra(tpl.ws_bytes, ps));
     }
     return need;
 }
@@ -519,9 +557,13 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     // is cheaper than once per tile (measured on GB300: the 4096^3 GEMM, at
     // 0.004 plane bytes per MAC, runs 5 % faster on planes; attention scores,
     // at 0.03, 1 % slower; attention's P V 11 % slower).
+    // The predecoded kernel's tile shape and its own plan, which it runs only
+    // as planned with unlimited scratch (planes after its stream-K region).
+    const TmaChoice tc = tma_choice(lut);
+    const Plan tpl = make_plan(p, n, sms, (size_t)-1, tc.tc);
     PlaneSet ps;
-    const bool planes_fit = ws && encode_tiled() && plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 &&
-                            ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps);
+    const bool planes_fit = ws && encode_tiled() && plan_planes(p, n, tpl, lut->M, kp.wlog, &ps) && ps.n > 0 &&
+                            ws_bytes >= tpl.ws_bytes + tma_extra(tpl.ws_bytes, ps);
     // (the raw-tile kernel counts a launch's iterations in 32 bits)
     const bool raw_fits = pl.iters < 0x7FFFFFFFLL;
     const bool conv_raw = raw_fits && n == 1 && p[0].conv && pl.tiles[0] > 0 && encode_tiled();
@@ -587,14 +629,13 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     // Predecoded operands copied by TMA, when every operand is dense (or a
     // convolution laid out for TMA) and the scratch holds the planes after the
     // stream-K region.
-    bool tma_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
-    if (!tma_gl && tma_stages(kern::lut_region_bytes((int)lut->narrow_bytes)) == 0) tma_gl = true;
-    const size_t tma_lutb = tma_gl ? 0 : kern::lut_region_bytes((int)lut->narrow_bytes);
-    if (!fmt && ws && encode_tiled() &&
-        plan_planes(p, n, pl, lut->M, kp.wlog, &ps) && ps.n > 0 && planes_pay(p, n, pl, ps) &&
-        ws_bytes >= pl.ws_bytes + tma_extra(pl.ws_bytes, ps)) {
+    const long long tblocks = tpl.streamk ? tpl.ctas : tpl.total_tiles;
+    if (!fmt && planes_fit && planes_pay(p, n, tpl, ps) && tc.stages > 0 && tblocks <= 0x7FFFFFFFLL) {
+        kern::KParams tp = {};
+        fill_params(p, n, tpl, lut, tp);
+        tp.ws = static_cast<float *>(ws);
         uint8_t *base = static_cast<uint8_t *>(ws);
-        const size_t flags_off = align256(pl.ws_bytes);
+        const size_t flags_off = align256(tpl.ws_bytes);
         unsigned long long *flags = reinterpret_cast<unsigned long long *>(base + flags_off);
         uint8_t *planes = base + flags_off + kFlagBlock;
         const unsigned long long epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
@@ -635,11 +676,12 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
         kern::TmaMaps maps = {};
         int erc = AMSIM_OK;
         for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
-            if (pl.tiles[i] == 0) continue;
+            if (tpl.tiles[i] == 0) continue;
             const int ju = ps.slot[2 * i], jl = ps.slot[2 * i + 1];
-            erc = encode_plane_map(&maps.u[qi], ps.key[ju], planes + ps.off[ju], BU);
-            if (erc == AMSIM_OK) erc = encode_plane_map(&maps.l[qi], ps.key[jl], planes + ps.off[jl], BL);
-            kern::ProbParams &q = kp.pr[qi++];
+            erc = encode_plane_map(&maps.u[qi], ps.key[ju], planes + ps.off[ju], tc.tc.bu, tc.tc.bk);
+            if (erc == AMSIM_OK)
+                erc = encode_plane_map(&maps.l[qi], ps.key[jl], planes + ps.off[jl], tc.tc.bl, tc.tc.bk);
+            kern::ProbParams &q = tp.pr[qi++];
             q.u_big = flags + ju;
             q.l_big = flags + jl;
             q.u_small = flags + kern::kMaxDecodeJobs + ju;
@@ -649,12 +691,12 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             q.l_bsel = ps.key[jl].nb > 1 ? 1 : 0;
         }
         if (erc == AMSIM_OK) {
-            kern::KParams tp = kp;
-            tp.table_bytes = tma_gl ? 0 : (int)lut->narrow_bytes;
-            tp.stages = tma_stages(tma_lutb);
+            tp.table_bytes = tc.gl ? 0 : (int)lut->narrow_bytes;
+            tp.stages = tc.stages;
             tp.epoch = epoch;
-            const size_t smem = (size_t)kern::tma_smem_bytes((int)tma_lutb, tp.stages);
-            const int rc = run_tma(lut->width_bits, tp, maps, dp, tma_gl, blocks, smem, sms, pl.streamk, stream);
+            const size_t smem = (size_t)kern::tma_cfg_smem_bytes(tc.tc, (int)tc.lutb, tp.stages);
+            const int rc = run_tma(lut->width_bits, tc.wide, tp, maps, dp, tc.gl, tblocks, smem, sms, tpl.streamk,
+                                   stream);
             if (rc != AMSIM_EUNSUPPORTED) return rc;
         }
     }

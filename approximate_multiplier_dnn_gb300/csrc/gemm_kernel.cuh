@@ -26,6 +26,12 @@
 
 #include "amsim_internal.h"
 
+#ifdef AMSIM_WIDE_TILES
+#define AMSIM_KNS kern_wide
+#else
+#define AMSIM_KNS kern
+#endif
+
 namespace amsim {
 namespace kern {
 
@@ -50,28 +56,17 @@ namespace kern {
 #ifndef AMSIM_KK_UNROLL
 #define AMSIM_KK_UNROLL 1
 #endif
-constexpr int kKkUnroll = AMSIM_KK_UNROLL;   // reduction steps unrolled per loop iteration
-constexpr int NT = AMSIM_NT;       // threads per CTA
-constexpr int BU = AMSIM_BU;       // uniform rows per CTA tile
-constexpr int BL = AMSIM_BL;       // lane columns per CTA tile
-constexpr int BK = AMSIM_BK;       // reduction depth per stage
-constexpr int TM = AMSIM_TM;       // uniform rows per warp (processed in pairs)
-constexpr int TN = AMSIM_TN;       // lane columns per thread
-constexpr int WU = BU / TM;        // warps along U
-constexpr int WL = BL / (32 * TN); // warps along L
-constexpr int UST = BU + 4;        // decoded U row stride (words), 16-B aligned, few bank conflicts
-constexpr int LST = BL + 4;        // decoded L row stride (words)
-constexpr int NUE = BU * BK / NT;  // U elements loaded per thread per stage
-constexpr int NLE = BL * BK / NT;  // L elements loaded per thread per stage
-static_assert(TM % 4 == 0 && TN % 4 == 0, "micro-tile");
-static_assert(NT % BK == 0 && (NT % BU == 0 || BU % NT == 0) && (NT % BL == 0 || BL % NT == 0), "loader mapping");
-static_assert(WU * WL * 32 == NT, "warp layout");
-// Lane columns: register column t of a lane is column lane*4 + col_of(t) of
-// its warp's 32*TN-column span -- groups of four columns, the groups 128
-// columns apart -- so each 128-bit load of one group reads 512 contiguous
-// bytes across the warp (four wavefronts, no bank conflicts) whatever TN is.
-constexpr int kColGroup = 128;
-__host__ __device__ constexpr int col_of(int t) { return (t >> 2) * kColGroup + (t & 3); }
+// Tile shape of a LUT-GEMM kernel instance: BU uniform rows x BL lane columns
+// per CTA tile, BK reduction steps per stage, TM uniform rows per warp and TN
+// lane columns per thread.  Every kernel is built with the narrow shape; the
+// predecoded (TMA) kernel is built with the wide one too, whose eight lane
+// columns per thread halve the shared-memory wavefronts of the uniform
+// operands' loads per lookup (1/TN of a lookup's).
+struct TileCfg {
+    int bu, bl, bk, tm, tn;
+};
+constexpr TileCfg kNarrowTiles = {AMSIM_BU, AMSIM_BL, AMSIM_BK, AMSIM_TM, AMSIM_TN};
+constexpr TileCfg kWideTiles = {128, 256, 16, 16, 8};
 
 struct RowInfo {
     int y, x;
@@ -147,6 +142,42 @@ struct KParams {
     // launches to them)
     ExpFormat fmt;
 };
+
+}  // namespace kern
+
+// Everything below depends on the tile shape and is built once per shape: in
+// namespace kern with the narrow shape, in kern_wide with the wide one (a
+// translation unit that defines AMSIM_WIDE_TILES before including this file).
+namespace AMSIM_KNS {
+
+#ifdef AMSIM_WIDE_TILES
+using namespace ::amsim::kern;
+constexpr TileCfg kTiles = kWideTiles;
+#else
+constexpr TileCfg kTiles = kNarrowTiles;
+#endif
+constexpr int kKkUnroll = AMSIM_KK_UNROLL;   // reduction steps unrolled per loop iteration
+constexpr int NT = AMSIM_NT;       // threads per CTA
+constexpr int BU = kTiles.bu;       // uniform rows per CTA tile
+constexpr int BL = kTiles.bl;       // lane columns per CTA tile
+constexpr int BK = kTiles.bk;       // reduction depth per stage
+constexpr int TM = kTiles.tm;       // uniform rows per warp (processed in pairs)
+constexpr int TN = kTiles.tn;       // lane columns per thread
+constexpr int WU = BU / TM;        // warps along U
+constexpr int WL = BL / (32 * TN); // warps along L
+constexpr int UST = BU + 4;        // decoded U row stride (words), 16-B aligned, few bank conflicts
+constexpr int LST = BL + 4;        // decoded L row stride (words)
+constexpr int NUE = BU * BK / NT;  // U elements loaded per thread per stage
+constexpr int NLE = BL * BK / NT;  // L elements loaded per thread per stage
+static_assert(TM % 4 == 0 && TN % 4 == 0, "micro-tile");
+static_assert(NT % BK == 0 && (NT % BU == 0 || BU % NT == 0) && (NT % BL == 0 || BL % NT == 0), "loader mapping");
+static_assert(WU * WL * 32 == NT, "warp layout");
+// Lane columns: register column t of a lane is column lane*4 + col_of(t) of
+// its warp's 32*TN-column span -- groups of four columns, the groups 128
+// columns apart -- so each 128-bit load of one group reads 512 contiguous
+// bytes across the warp (four wavefronts, no bank conflicts) whatever TN is.
+constexpr int kColGroup = 128;
+__host__ __device__ constexpr int col_of(int t) { return (t >> 2) * kColGroup + (t & 3); }
 
 // Shared-memory layout (bytes) after the LUT region.
 constexpr int kUdecBytes = 2 * BK * UST * 4;   // one array (offsets or scales), 2 stages
@@ -892,11 +923,11 @@ __global__ void __launch_bounds__(kThreads) streamk_fixup(const __grid_constant_
     }
 }
 
-}  // namespace kern
+}  // namespace AMSIM_KNS
 }  // namespace amsim
 
 namespace amsim {
-namespace kern {
+namespace AMSIM_KNS {
 
 // Host-side launcher for one instance; sets the dynamic shared-memory limit
 // once per device.
@@ -923,5 +954,5 @@ int launch_w8(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st
 int launch_w16(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
 int launch_w32(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
 
-}  // namespace kern
+}  // namespace AMSIM_KNS
 }  // namespace amsim

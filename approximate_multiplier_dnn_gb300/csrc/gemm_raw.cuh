@@ -22,6 +22,10 @@
 
 #include "gemm_tma.cuh"
 
+#ifdef AMSIM_WIDE_TILES
+#error "the raw-tile kernel is built with the narrow tile shape only"
+#endif
+
 namespace amsim {
 namespace kern {
 

@@ -25,6 +25,48 @@
 namespace amsim {
 namespace kern {
 
+// Shape-independent parts, seen by the host for both tile shapes.
+constexpr int kTmaMaxStages = 6;
+constexpr int kTmaBarBytes = (2 * kTmaMaxStages + 1) * 8;      // full, empty, reduction
+// One ring stage: offsets then scales of BK reduction steps of the tile's U
+// rows, then the same of its L rows, [k][row].
+__host__ __device__ constexpr int tma_stage_bytes(TileCfg c) { return 2 * c.bk * (c.bu + c.bl) * 4; }
+// The ring doubles as the stream-K reduction buffer: one tile plus 16 bytes
+// per participant (up to 1024).
+__host__ __device__ constexpr int tma_red_bytes(TileCfg c) { return (c.bu * c.bl + 1024 * 4) * 4; }
+__host__ __device__ constexpr int tma_min_stages(TileCfg c)
+{
+    return (tma_red_bytes(c) + tma_stage_bytes(c) - 1) / tma_stage_bytes(c) < 2
+               ? 2 : (tma_red_bytes(c) + tma_stage_bytes(c) - 1) / tma_stage_bytes(c);
+}
+// Shared memory of the TMA kernel for a ring of `stages` and a LUT region of `lut_bytes`.
+__host__ __device__ constexpr int tma_cfg_smem_bytes(TileCfg c, int lut_bytes, int stages)
+{
+    return 128 + lut_bytes + stages * tma_stage_bytes(c) + kTmaBarBytes;
+}
+
+// Tensor maps of the operand planes of every problem of a launch.
+struct TmaMaps {
+    CUtensorMap u[kMaxProblems];
+    CUtensorMap l[kMaxProblems];
+};
+
+}  // namespace kern
+
+// The wide-shape instances (built in their own translation units).
+namespace kern_wide {
+int launch_tma_w8(const kern::KParams &p, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
+                  cudaStream_t st);
+int launch_tma_w16(const kern::KParams &p, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
+                   cudaStream_t st);
+int launch_tma_w32(const kern::KParams &p, const kern::TmaMaps &maps, bool gl, dim3 grid, size_t smem,
+                   cudaStream_t st);
+// stream-K fixup of wide tiles (see launch_fixup)
+int launch_fixup(const kern::KParams &p, int boundaries, cudaStream_t st);
+}  // namespace kern_wide
+
+namespace AMSIM_KNS {
+
 // The copy thread lives in one extra warp; with AMSIM_TMA_PWARPS=4 it gets a
 // whole warpgroup that gives its registers to the consumers (setmaxnreg).
 #ifndef AMSIM_TMA_PWARPS
@@ -41,29 +83,18 @@ static_assert(kTmaProducerWarps == 1 || kTmaProducerWarps == 4, "one copy warp o
 static_assert(kTmaProducerWarps == 1 || (kTmaConsumerRegs <= 256 && kTmaConsumerThreads * kTmaConsumerRegs +
                                          128 * kTmaProducerRegs <= kTmaThreads * kTmaLaunchRegs),
               "register split exceeds the launch allocation");
-constexpr int kTmaMaxStages = 6;
 constexpr int kTmaUBytes = 2 * BK * BU * 4;                    // offsets then scales, [k][row]
 constexpr int kTmaLBytes = 2 * BK * BL * 4;
-constexpr int kTmaStageBytes = kTmaUBytes + kTmaLBytes;        // 40 KB
-constexpr int kTmaBarBytes = (2 * kTmaMaxStages + 1) * 8;        // full, empty, reduction
-// the ring doubles as the stream-K reduction buffer: one tile plus 16 bytes
-// per participant (up to 1024)
-constexpr int kRedBytes = (BU * BL + 1024 * 4) * 4;
-constexpr int kTmaMinStages = (kRedBytes + kTmaStageBytes - 1) / kTmaStageBytes < 2
-                                  ? 2 : (kRedBytes + kTmaStageBytes - 1) / kTmaStageBytes;
+constexpr int kTmaStageBytes = kTmaUBytes + kTmaLBytes;        // 40 KB narrow, 48 KB wide
+constexpr int kRedBytes = tma_red_bytes(kTiles);
+constexpr int kTmaMinStages = tma_min_stages(kTiles);
+static_assert(kTmaStageBytes == tma_stage_bytes(kTiles), "stage layout");
 static_assert(kTmaStageBytes % 128 == 0 && kTmaUBytes % 128 == 0, "stage alignment");
 
-// Shared memory of the TMA kernel for a ring of `stages` and a LUT region of `lut_bytes`.
 __host__ __device__ constexpr int tma_smem_bytes(int lut_bytes, int stages)
 {
-    return 128 + lut_bytes + stages * kTmaStageBytes + kTmaBarBytes;
+    return tma_cfg_smem_bytes(kTiles, lut_bytes, stages);
 }
-
-// Tensor maps of the operand planes of every problem of a launch.
-struct TmaMaps {
-    CUtensorMap u[kMaxProblems];
-    CUtensorMap l[kMaxProblems];
-};
 
 // Box (x, y, z, w) of the 4-D tensor map into shared memory; completes on `bar`.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
@@ -283,5 +314,5 @@ int launch_tma_w8(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, siz
 int launch_tma_w16(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
 int launch_tma_w32(const KParams &p, const TmaMaps &maps, bool gl, dim3 grid, size_t smem, cudaStream_t st);
 
-}  // namespace kern
+}  // namespace AMSIM_KNS
 }  // namespace amsim

@@ -16,7 +16,7 @@
 #include "gemm_kernel.cuh"
 
 namespace amsim {
-namespace kern {
+namespace AMSIM_KNS {
 
 #ifndef AMSIM_WS_PWARPS
 #define AMSIM_WS_PWARPS 8
@@ -846,5 +846,5 @@ int launch_ws_w8(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t
 int launch_ws_w16(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
 int launch_ws_w32(const KParams &p, bool gl, dim3 grid, size_t smem, cudaStream_t st);
 
-}  // namespace kern
+}  // namespace AMSIM_KNS
 }  // namespace amsim

@@ -316,6 +316,12 @@ def global_table_roofline(lut, lut_macs, lut_ms, sms, mhz, smem_roofline):
             "kernel": smem_roofline["kernel"], "sms": sms, "sm_mhz": mhz}
 
 
+def path_names(am, bits):
+    """amsim_last_path bits of a part's last library call, as names."""
+    names = [n[len("AMSIM_PATH_"):].lower() for n in dir(am) if n.startswith("AMSIM_PATH_")]
+    return sorted(n for n in names if bits & getattr(am, "AMSIM_PATH_" + n.upper()))
+
+
 # ---------------------------------------------------------------- traffic record
 # sources of the LUT-GEMM kernels (the kernel the traffic records measure);
 # a record holds for one version of them
@@ -457,9 +463,11 @@ def main():
         step.run()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    part_paths = {}
     for _ in range(5):
         for p in parts:
             p[1]()
+            part_paths[p[0]] = path_names(am, am.amsim_last_path())
     enqueue_s = (time.perf_counter() - t0) / 5
     torch.cuda.synchronize()
     sleep_cycles = int(min(max(2.0 * enqueue_s, 50e-6), 20e-3) * 2.1e9)
@@ -529,7 +537,7 @@ def main():
                 "achieved": achieved, "peak": peak, "unit": "Glookup/s", "frac": achieved / peak,
                 "traffic": traffic,
                 "kernel": "LUT-GEMM calls: lutgemm_raw_kernel, or predecode + lutgemm_tma_kernel "
-                          "(lutgemm_ws_kernel for gathers); see amsim_last_path",
+                          "(lutgemm_ws_kernel for gathers); see paths",
                 "calls_per_step": launches_lut, "kernel_launches_per_step": launches_timed / K,
                 "lut_residency": lut_residency(step.lut),
                 "lut_share_of_step": round(lut_share, 4), "sms": sms,
@@ -737,6 +745,7 @@ def main():
                        "(256 MiB write, outside the timed events)", "parallelism": f"replicas{world}"},
             "roofline": roofline,
             "parts_ms": {p[0]: round(t, 5) for p, t in zip(parts, part_ms)},
+            "paths": part_paths,
             "e2e": e2e,
             "native_fp32": native,
             "gpu_launches": launches_timed,

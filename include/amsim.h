@@ -90,7 +90,8 @@ enum amsim_path {
     AMSIM_PATH_PHASED = 256,        /* every phase of amsim_gemm_phased in one launch */
     AMSIM_PATH_CLOSED_FORM = 512,   /* products computed in registers (amsim_lut_set_closed_form) */
     AMSIM_PATH_DW_TILES = 1024,     /* depthwise: halo tiles in shared memory, one channel per warp */
-    AMSIM_PATH_DW_DIRECT = 2048     /* depthwise: one lane per output element, operands read directly */
+    AMSIM_PATH_DW_DIRECT = 2048,    /* depthwise: one lane per output element, operands read directly */
+    AMSIM_PATH_WIDE_TILES = 4096    /* with AMSIM_PATH_PLANES: 128 x 256 tiles, eight lane columns per thread */
 };
 int amsim_last_path(void);
 

@@ -325,18 +325,51 @@ def test_batched_broadcast_operand(amd, orc, luts, path, k):
 
 
 def test_paths_bit_identical_without_stream_k(amd, luts):
-    """A shape that fills whole waves runs data-parallel on every path; the
-    per-element summation order is the same, so the outputs are bit-identical."""
+    """Shapes that fill whole waves run data-parallel; every output element is
+    then summed in the same order on every path and tile shape, so the outputs
+    are bit-identical: 64-row tiles with and without scratch at m = 64 x SMs,
+    and the predecoded kernel's 128 x 256 tiles (one wave: 38 x 4 tiles on 152
+    SMs) against the kernel without scratch."""
     import torch
     rng = np.random.default_rng(15)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    m, n, k = 64 * sms, 200, 100          # one 64 x 256 tile per SM
-    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
     lut = luts("mitchell", 7)
-    outs = [gpu_gemm(amd, lut, A, B, False, False, ws=_path_ws(amd, lut, p, "N", "N", m, n, k))
-            for p in ("planes", "in_kernel", "none")]
-    for o in outs[1:]:
-        assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32))
+    k = 100
+    cases = [(64 * sms, 200, ("in_kernel", "none"))]
+    if sms % 4 == 0:
+        # n in (768, 1024]: four lane tiles; m / 128 * 4 = SMs; 0.0096 plane bytes per MAC takes the planes
+        cases.append((128 * sms // 4, 1000, ("planes", "none")))
+    for m, n, paths in cases:
+        A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+        outs, bits = [], []
+        for p in paths:
+            outs.append(gpu_gemm(amd, lut, A, B, False, False, ws=_path_ws(amd, lut, p, "N", "N", m, n, k)))
+            bits.append(amd.amsim_last_path())
+        assert not any(b & amd.AMSIM_PATH_STREAMK for b in bits), bits
+        if paths[0] == "planes":
+            assert bits[0] & amd.AMSIM_PATH_PLANES and bits[0] & amd.AMSIM_PATH_WIDE_TILES, bits
+            assert not bits[1] & amd.AMSIM_PATH_WIDE_TILES, bits
+        for o in outs[1:]:
+            assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)), (m, n, paths)
+
+
+@pytest.mark.parametrize("kind,M,wide", [("mitchell", 7, True), ("exact", 7, True), ("mitchell", 8, False),
+                                         ("mitchell", 9, True)])
+def test_predecoded_tile_shape_by_table(amd, orc, luts, kind, M, wide):
+    """The predecoded kernel takes the wide 128 x 256 tiles when their ring fits
+    beside the table in shared memory (8- and 16-bit M = 7 tables) or when the
+    table is read from global memory (M = 9), and the narrow tiles for the
+    128 KB M = 8 table; 98 wide tiles on the SMs cut some tiles by stream-K."""
+    rng = np.random.default_rng(16 + M)
+    m = n = 1700
+    k = 64
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    lut = luts(kind, M)
+    got = gpu_gemm(amd, lut, A, B, False, False)
+    bits = amd.amsim_last_path()
+    assert bits & amd.AMSIM_PATH_PLANES, bits
+    assert bool(bits & amd.AMSIM_PATH_WIDE_TILES) == wide, bits
+    check(orc, kind, M, A, B, False, False, got, what=f"tile shape {kind} M={M}")
 
 
 @pytest.mark.parametrize("zeros_in", ["A", "B", "both"])
