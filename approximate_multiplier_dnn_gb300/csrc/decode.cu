@@ -2,7 +2,7 @@
 // launch is decoded once into (LUT offset, scale) planes that the GEMM copies
 // tile by tile with the Tensor Memory Accelerator (ApproxTrain Sec. V-B,
 // Algorithm 2, the per-operand half of the product).  Memory-bound: 4 bytes
-// read and 8 written per element.  Operands stored row-fast are decoded in
+// read and 4 (packed words) or 8 (two planes) written per element.  Operands stored row-fast are decoded in
 // place order; k-fast ones go through a shared-memory transpose so that both
 // reads and writes stay coalesced.
 #include "decode_unit.cuh"

@@ -24,6 +24,20 @@ __device__ __forceinline__ bool elem_at(const DecodeJob &d, int rh, int rl, int 
     return x >= 0 && x < d.rlim;
 }
 
+// Four decoded elements at word i of the job's planes: packed words, or
+// offsets and scales.
+__device__ __forceinline__ void store_quad(const DecodeJob &d, uint32_t *po, float *ps, size_t i, const uint4 &o4,
+                                           const float4 &s4)
+{
+    if (d.packed) {
+        *reinterpret_cast<uint4 *>(po + i) = make_uint4(pack_operand(o4.x, s4.x), pack_operand(o4.y, s4.y),
+                                                        pack_operand(o4.z, s4.z), pack_operand(o4.w, s4.w));
+    } else {
+        *reinterpret_cast<uint4 *>(po + i) = o4;
+        *reinterpret_cast<float4 *>(ps + i) = s4;
+    }
+}
+
 // Decode unit t of p.  tid in [0, 256); sync() synchronises those 256 threads;
 // t_off / t_scl: kDecodeTileK rows of kDecodePitch words of shared memory each.
 template <class Sync>
@@ -41,8 +55,8 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
     const int rem = lt - b * per_b;
     const int r0 = (rem / d.tiles_k) * TR, k0 = (rem % d.tiles_k) * TK;
     const float *src = d.src + (long long)b * d.bs;
-    uint32_t *po = d.plane + (size_t)b * 2 * d.K * d.rows_pad;
-    float *ps = reinterpret_cast<float *>(po + (size_t)d.K * d.rows_pad);
+    uint32_t *po = d.plane + (size_t)b * (d.packed ? 1 : 2) * d.K * d.rows_pad;
+    float *ps = reinterpret_cast<float *>(po + (size_t)d.K * d.rows_pad);   // two-plane layout only
     int big = 0, small = 0, zero = 0;
     if (d.rowfast) {
         // rows r .. r + 3 at reduction steps k0 + grp + 16 i
@@ -73,8 +87,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
                     zero |= r + e < d.rows && is_small(v[e]) && !is_small_nonzero(v[e]);
                 }
                 // rows_pad is a multiple of 4: the pad columns of a partial quad may be written
-                *reinterpret_cast<uint4 *>(po + (size_t)k * d.rows_pad + r) = o4;
-                *reinterpret_cast<float4 *>(ps + (size_t)k * d.rows_pad + r) = s4;
+                store_quad(d, po, ps, (size_t)k * d.rows_pad + r, o4, s4);
             }
         }
     } else {
@@ -134,8 +147,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
                                             t_off[kk][lane4 + 3]);
                 const float4 s4 = make_float4(t_scl[kk][lane4], t_scl[kk][lane4 + 1], t_scl[kk][lane4 + 2],
                                               t_scl[kk][lane4 + 3]);
-                *reinterpret_cast<uint4 *>(po + (size_t)k2 * d.rows_pad + r) = o4;
-                *reinterpret_cast<float4 *>(ps + (size_t)k2 * d.rows_pad + r) = s4;
+                store_quad(d, po, ps, (size_t)k2 * d.rows_pad + r, o4, s4);
             }
         }
         sync();

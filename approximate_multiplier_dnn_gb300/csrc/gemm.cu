@@ -150,7 +150,11 @@ PlaneKey plane_key(const OperandDesc &d, int K, int batch, int offshift)
 
 int rows_pad(int rows) { return (rows + 3) & ~3; }
 
-size_t plane_bytes(const PlaneKey &k) { return align256((size_t)k.nb * 2 * k.K * rows_pad(k.rows) * 4); }
+// `planes` words per element: one packed word, or an offset and a scale.
+size_t plane_bytes(const PlaneKey &k, int planes)
+{
+    return align256((size_t)k.nb * planes * k.K * rows_pad(k.rows) * 4);
+}
 
 // Distinct planes of problems [0, n) (operand order U0, L0, U1, L1, ...):
 // slot[2i] / slot[2i+1] give the plane index of problem i's U / L operand.
@@ -158,16 +162,19 @@ struct PlaneSet {
     PlaneKey key[kern::kMaxDecodeJobs];
     size_t off[kern::kMaxDecodeJobs];    // from the start of the plane region
     int n;
+    int nplanes[kern::kMaxDecodeJobs];   // 1: packed words, 2: offset and scale planes
     int slot[2 * kern::kMaxProblems];
     size_t bytes;
+    double elems;    // operand elements decoded (padded rows), for the path decision
 };
 
 // False when some problem cannot take the predecoded path (gather operand,
-// empty reduction).
-bool plan_planes(const Problem *p, int n, const Plan &pl, int M, int wlog, PlaneSet *ps)
+// empty reduction).  planes: U operands' plane count + 4 x L operands'.
+bool plan_planes(const Problem *p, int n, const Plan &pl, int M, int wlog, int planes, PlaneSet *ps)
 {
     ps->n = 0;
     ps->bytes = 0;
+    ps->elems = 0.0;
     for (int i = 0; i < n; ++i) {
         if (pl.tiles[i] == 0) continue;
         if (p[i].U.gather || p[i].L.gather || p[i].K <= 0) return false;
@@ -179,7 +186,10 @@ bool plan_planes(const Problem *p, int n, const Plan &pl, int M, int wlog, Plane
             if (j == ps->n) {
                 ps->key[j] = k;
                 ps->off[j] = ps->bytes;
-                ps->bytes += plane_bytes(k);
+                // (U and L planes never coincide: their offset shifts differ)
+                ps->nplanes[j] = r == 0 ? (planes & 3) : (planes >> 2);
+                ps->bytes += plane_bytes(k, ps->nplanes[j]);
+                ps->elems += (double)k.nb * k.K * rows_pad(k.rows);
                 ++ps->n;
             }
             ps->slot[2 * i + r] = j;
@@ -191,66 +201,74 @@ bool plan_planes(const Problem *p, int n, const Plan &pl, int M, int wlog, Plane
 // The planes pay for their extra memory traffic (written once, read at least
 // once) when operand elements are reused by several tiles; a large operand
 // read by a single tile row (attention's P in O = P V) is decoded as cheaply
-// inside the GEMM.  Measured on GB300: 0.03 plane bytes per MAC gains, 0.13
-// loses.  Below 64 MB of planes the pass costs microseconds either way.
+// inside the GEMM.  Measured on GB300 with two-plane (8-byte) elements: 0.03
+// plane bytes per MAC gains, 0.13 loses.  Below 64 MB of planes the pass
+// costs microseconds either way.  The measure stays 8 bytes per decoded
+// element, whatever the planes' layout, so the thresholds keep their meaning.
 double planes_bytes_per_mac(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
 {
     double macs = 0.0;
     for (int i = 0; i < n; ++i)
         if (pl.tiles[i] > 0) macs += (double)p[i].U.rows * p[i].L.rows * (double)p[i].K * p[i].batch;
-    return macs > 0.0 ? (double)ps.bytes / macs : 1e30;
+    return macs > 0.0 ? 8.0 * ps.elems / macs : 1e30;
 }
 
 bool planes_pay(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
 {
-    if (ps.bytes <= ((size_t)64 << 20)) return true;
+    if (8.0 * ps.elems <= (double)((size_t)64 << 20)) return true;
     return planes_bytes_per_mac(p, n, pl, ps) <= 0.05;
 }
 
 // Ring depth of the TMA kernel with tiles of shape tc beside a LUT region of
 // lut_bytes (0 if none fits).
-int tma_stages(size_t lut_bytes, const kern::TileCfg &tc)
+int tma_stages(size_t lut_bytes, const kern::TileCfg &tc, int planes)
 {
-    const long long room = (long long)kMaxSmemPerCta - kern::tma_cfg_smem_bytes(tc, (int)lut_bytes, 0);
-    long long s = room / kern::tma_stage_bytes(tc);
+    const long long room = (long long)kMaxSmemPerCta - kern::tma_cfg_smem_bytes(tc, planes, (int)lut_bytes, 0);
+    long long s = room / kern::tma_stage_bytes(tc, planes);
     if (s > kern::kTmaMaxStages) s = kern::kTmaMaxStages;
-    return s >= kern::tma_min_stages(tc) ? (int)s : 0;
+    return s >= kern::tma_min_stages(tc, planes) ? (int)s : 0;
 }
 
-// Tile shape and LUT placement of the predecoded (TMA) kernel: the wide shape
-// with the table in shared memory when a ring of its minimum depth fits beside
-// it, else the narrow shape with the table in shared memory, else the wide
-// shape reading the table from global memory.  Measured on GB300 (4096^3,
-// Mitchell): M = 7 runs 6.5 % faster and M = 9 25 % faster on wide tiles; at
-// M = 8 (a 128 KB table) the wide ring does not fit, and the narrow kernel's
-// two stages beat the wide kernel reading the table from global memory.
+// Tile shape, LUT placement and plane layout of the predecoded (TMA) kernel:
+// the wide shape with the table in shared memory when a ring of its minimum
+// depth fits beside it, else the narrow shape with the table in shared
+// memory, else the wide shape reading the table from global memory.  With
+// the table in shared memory the planes hold packed operand words (offsets
+// below 2^18); from global memory, whose offsets reach 2^23, two planes.
+// Measured on GB300 (4096^3, Mitchell, two planes): M = 7 runs 6.5 % faster
+// and M = 9 25 % faster on wide tiles; at M = 8 (a 128 KB table) the wide
+// ring does not fit, and the narrow kernel beats the wide kernel reading the
+// table from global memory.
 struct TmaChoice {
     kern::TileCfg tc;
     bool wide, gl;
+    int planes;    // U operands' planes + 4 x L operands' (1: packed words, 2: offset and scale)
     int stages;
     size_t lutb;   // LUT region in shared memory (0 when read from global)
 };
 
 TmaChoice tma_choice(amsim_lut_t lut)
 {
-    TmaChoice c = {kern::kWideTiles, true, true, 0, 0};
     if (lut->narrow_bytes <= (size_t)kMaxSmemLut) {
         const size_t lutb = kern::lut_region_bytes((int)lut->narrow_bytes);
-        if (const int s = tma_stages(lutb, kern::kWideTiles)) return {kern::kWideTiles, true, false, s, lutb};
-        if (const int s = tma_stages(lutb, kern::kNarrowTiles)) return {kern::kNarrowTiles, false, false, s, lutb};
+        const int planes = kern::tma_planes(false);
+        if (const int s = tma_stages(lutb, kern::kWideTiles, planes))
+            return {kern::kWideTiles, true, false, planes, s, lutb};
+        if (const int s = tma_stages(lutb, kern::kNarrowTiles, planes))
+            return {kern::kNarrowTiles, false, false, planes, s, lutb};
     }
-    c.stages = tma_stages(0, kern::kWideTiles);
-    return c;
+    const int planes = kern::tma_planes(true);
+    return {kern::kWideTiles, true, true, planes, tma_stages(0, kern::kWideTiles, planes), 0};
 }
 
-int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_rows, int box_k)
+int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_rows, int box_k, int planes)
 {
     EncodeTiled enc = encode_tiled();
     if (!enc) return AMSIM_EUNSUPPORTED;
     const cuuint64_t pitch = (cuuint64_t)rows_pad(k.rows) * 4;
-    const cuuint64_t dims[4] = {(cuuint64_t)k.rows, (cuuint64_t)k.K, 2, (cuuint64_t)k.nb};
-    const cuuint64_t strides[3] = {pitch, pitch * (cuuint64_t)k.K, pitch * (cuuint64_t)k.K * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)box_rows, (cuuint32_t)box_k, 2, 1};
+    const cuuint64_t dims[4] = {(cuuint64_t)k.rows, (cuuint64_t)k.K, (cuuint64_t)planes, (cuuint64_t)k.nb};
+    const cuuint64_t strides[3] = {pitch, pitch * (cuuint64_t)k.K, pitch * (cuuint64_t)k.K * planes};
+    const cuuint32_t box[4] = {(cuuint32_t)box_rows, (cuuint32_t)box_k, (cuuint32_t)planes, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -424,16 +442,18 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     const int rwlog = lut ? (lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2) : 0;
     if (lut && encode_tiled() && pl.iters < 0x7FFFFFFFLL && all_raw_ok(p, n, pl, false) &&
         (alu_code(lut) ||
-         !(plan_planes(p, n, pl, lut->M, rwlog, &rps) && rps.n > 0 && planes_bytes_per_mac(p, n, pl, rps) < 0.01))) {
+         !(plan_planes(p, n, pl, lut->M, rwlog, 2 + 4 * 2, &rps) && rps.n > 0 &&
+           planes_bytes_per_mac(p, n, pl, rps) < 0.01))) {
         // operand tiles are copied in place and decoded inside the GEMM
     } else if (lut && encode_tiled() && n == 1 && p[0].conv) {
         // convolution tiles are copied in place as tensor boxes
     } else if (lut && encode_tiled()) {
         // the predecoded kernel's own plan (its tile shape's stream-K slots), then the planes
         const int wlog = lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2;
-        const Plan tpl = make_plan(p, n, sms, (size_t)-1, tma_choice(lut).tc);
+        const TmaChoice tc = tma_choice(lut);
+        const Plan tpl = make_plan(p, n, sms, (size_t)-1, tc.tc);
         PlaneSet ps;
-        if (plan_planes(p, n, tpl, lut->M, wlog, &ps) && ps.n > 0 && planes_pay(p, n, tpl, ps))
+        if (plan_planes(p, n, tpl, lut->M, wlog, tc.planes, &ps) && ps.n > 0 && planes_pay(p, n, tpl, ps))
             need = std::max(need, tpl.ws_bytes + tma_extra(tpl.ws_bytes, ps));
     }
     return need;
@@ -562,7 +582,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     const TmaChoice tc = tma_choice(lut);
     const Plan tpl = make_plan(p, n, sms, (size_t)-1, tc.tc);
     PlaneSet ps;
-    const bool planes_fit = ws && encode_tiled() && plan_planes(p, n, tpl, lut->M, kp.wlog, &ps) && ps.n > 0 &&
+    const bool planes_fit = ws && encode_tiled() && plan_planes(p, n, tpl, lut->M, kp.wlog, tc.planes, &ps) && ps.n > 0 &&
                             ws_bytes >= tpl.ws_bytes + tma_extra(tpl.ws_bytes, ps);
     // (the raw-tile kernel counts a launch's iterations in 32 bits)
     const bool raw_fits = pl.iters < 0x7FFFFFFFLL;
@@ -661,6 +681,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             d.batch = k.nb;
             d.rows_pad = rows_pad(k.rows);
             d.offshift = k.offshift;
+            d.packed = ps.nplanes[j] == 1;
             d.plane = reinterpret_cast<uint32_t *>(planes + ps.off[j]);
             d.flag = flags + j;
             d.flag_small = flags + kern::kMaxDecodeJobs + j;
@@ -678,9 +699,9 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
         for (int i = 0, qi = 0; i < n && erc == AMSIM_OK; ++i) {
             if (tpl.tiles[i] == 0) continue;
             const int ju = ps.slot[2 * i], jl = ps.slot[2 * i + 1];
-            erc = encode_plane_map(&maps.u[qi], ps.key[ju], planes + ps.off[ju], tc.tc.bu, tc.tc.bk);
+            erc = encode_plane_map(&maps.u[qi], ps.key[ju], planes + ps.off[ju], tc.tc.bu, tc.tc.bk, ps.nplanes[ju]);
             if (erc == AMSIM_OK)
-                erc = encode_plane_map(&maps.l[qi], ps.key[jl], planes + ps.off[jl], tc.tc.bl, tc.tc.bk);
+                erc = encode_plane_map(&maps.l[qi], ps.key[jl], planes + ps.off[jl], tc.tc.bl, tc.tc.bk, ps.nplanes[jl]);
             kern::ProbParams &q = tp.pr[qi++];
             q.u_big = flags + ju;
             q.l_big = flags + jl;
@@ -694,7 +715,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             tp.table_bytes = tc.gl ? 0 : (int)lut->narrow_bytes;
             tp.stages = tc.stages;
             tp.epoch = epoch;
-            const size_t smem = (size_t)kern::tma_cfg_smem_bytes(tc.tc, (int)tc.lutb, tp.stages);
+            const size_t smem = (size_t)kern::tma_cfg_smem_bytes(tc.tc, tc.planes, (int)tc.lutb, tp.stages);
             const int rc = run_tma(lut->width_bits, tc.wide, tp, maps, dp, tc.gl, tblocks, smem, sms, tpl.streamk,
                                    stream);
             if (rc != AMSIM_EUNSUPPORTED) return rc;

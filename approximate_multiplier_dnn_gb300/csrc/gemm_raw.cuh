@@ -546,7 +546,7 @@ template <int W, bool GL>
 __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lut, const RawSmem &sm, int red_bytes)
 {
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
+    const int lane = tid & 31, warp = uniform_warp();
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
     const int lcol = wl * 32 * TN + lane * 4;
@@ -817,7 +817,7 @@ __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const Phas
 {
     volatile int *last_flag = sm.flags + kRawDec * (kRawDecoders / 32);   // the ticket's verdict
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
+    const int lane = tid & 31, warp = uniform_warp();
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
     const int lcol = wl * 32 * TN + lane * 4;

@@ -26,23 +26,35 @@ namespace amsim {
 namespace kern {
 
 // Shape-independent parts, seen by the host for both tile shapes.
-constexpr int kTmaMaxStages = 6;
+constexpr int kTmaMaxStages = 8;
 constexpr int kTmaBarBytes = (2 * kTmaMaxStages + 1) * 8;      // full, empty, reduction
-// One ring stage: offsets then scales of BK reduction steps of the tile's U
-// rows, then the same of its L rows, [k][row].
-__host__ __device__ constexpr int tma_stage_bytes(TileCfg c) { return 2 * c.bk * (c.bu + c.bl) * 4; }
+// One ring stage: BK reduction steps of the tile's U rows, then of its L rows,
+// [plane][k][row]: one plane of packed operand words (pack_operand) with the
+// table in shared memory, two (offsets, then scales) with the table in global
+// memory, whose offsets reach 2^23.  Measured on GB300 (4096^3 Mitchell M = 7,
+// wide tiles): packed words take the shared-memory wavefronts per lookup from
+// 1.25 to 1.125 for 0.2 more instructions: 2.2 % faster with both operands
+// packed; packing only the uniform operand gained nothing.
+__host__ __device__ constexpr int tma_u_planes(bool gl) { return gl ? 2 : 1; }
+__host__ __device__ constexpr int tma_l_planes(bool gl) { return gl ? 2 : 1; }
+// `planes` encodes both operands' plane counts: U planes + 4 * L planes.
+__host__ __device__ constexpr int tma_planes(bool gl) { return tma_u_planes(gl) + 4 * tma_l_planes(gl); }
+__host__ __device__ constexpr int tma_stage_bytes(TileCfg c, int planes)
+{
+    return c.bk * ((planes & 3) * c.bu + (planes >> 2) * c.bl) * 4;
+}
 // The ring doubles as the stream-K reduction buffer: one tile plus 16 bytes
 // per participant (up to 1024).
 __host__ __device__ constexpr int tma_red_bytes(TileCfg c) { return (c.bu * c.bl + 1024 * 4) * 4; }
-__host__ __device__ constexpr int tma_min_stages(TileCfg c)
+__host__ __device__ constexpr int tma_min_stages(TileCfg c, int planes)
 {
-    return (tma_red_bytes(c) + tma_stage_bytes(c) - 1) / tma_stage_bytes(c) < 2
-               ? 2 : (tma_red_bytes(c) + tma_stage_bytes(c) - 1) / tma_stage_bytes(c);
+    return (tma_red_bytes(c) + tma_stage_bytes(c, planes) - 1) / tma_stage_bytes(c, planes) < 2
+               ? 2 : (tma_red_bytes(c) + tma_stage_bytes(c, planes) - 1) / tma_stage_bytes(c, planes);
 }
 // Shared memory of the TMA kernel for a ring of `stages` and a LUT region of `lut_bytes`.
-__host__ __device__ constexpr int tma_cfg_smem_bytes(TileCfg c, int lut_bytes, int stages)
+__host__ __device__ constexpr int tma_cfg_smem_bytes(TileCfg c, int planes, int lut_bytes, int stages)
 {
-    return 128 + lut_bytes + stages * tma_stage_bytes(c) + kTmaBarBytes;
+    return 128 + lut_bytes + stages * tma_stage_bytes(c, planes) + kTmaBarBytes;
 }
 
 // Tensor maps of the operand planes of every problem of a launch.
@@ -83,18 +95,19 @@ static_assert(kTmaProducerWarps == 1 || kTmaProducerWarps == 4, "one copy warp o
 static_assert(kTmaProducerWarps == 1 || (kTmaConsumerRegs <= 256 && kTmaConsumerThreads * kTmaConsumerRegs +
                                          128 * kTmaProducerRegs <= kTmaThreads * kTmaLaunchRegs),
               "register split exceeds the launch allocation");
-constexpr int kTmaUBytes = 2 * BK * BU * 4;                    // offsets then scales, [k][row]
+// A stage of two planes (offsets then scales, [k][row]), also the decoded
+// stage of the raw-tile kernel.
+constexpr int kTmaUBytes = 2 * BK * BU * 4;
 constexpr int kTmaLBytes = 2 * BK * BL * 4;
-constexpr int kTmaStageBytes = kTmaUBytes + kTmaLBytes;        // 40 KB narrow, 48 KB wide
-constexpr int kRedBytes = tma_red_bytes(kTiles);
-constexpr int kTmaMinStages = tma_min_stages(kTiles);
-static_assert(kTmaStageBytes == tma_stage_bytes(kTiles), "stage layout");
+constexpr int kTmaStageBytes = kTmaUBytes + kTmaLBytes;        // 40 KB narrow
+static_assert(kTmaStageBytes == tma_stage_bytes(kTiles, 2 + 4 * 2), "stage layout");
 static_assert(kTmaStageBytes % 128 == 0 && kTmaUBytes % 128 == 0, "stage alignment");
-
-__host__ __device__ constexpr int tma_smem_bytes(int lut_bytes, int stages)
-{
-    return tma_cfg_smem_bytes(kTiles, lut_bytes, stages);
-}
+// The TMA kernel's stage for its table placement: packed words with the
+// table in shared memory (20 KB narrow, 24 KB wide), two planes with it in
+// global memory.
+template <bool GL> constexpr int kTmaStage = tma_stage_bytes(kTiles, tma_planes(GL));
+template <bool GL> constexpr int kTmaStageU = tma_u_planes(GL) * BK * BU * 4;
+static_assert(kTmaStage<false> % 128 == 0 && kTmaStageU<false> % 128 == 0, "packed stage alignment");
 
 // Box (x, y, z, w) of the 4-D tensor map into shared memory; completes on `bar`.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
@@ -114,6 +127,7 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
 
 // The copy thread: for every iteration of this CTA, wait for the ring slot to
 // be released, announce the stage's bytes and issue the two box copies.
+template <bool GL>
 __device__ __forceinline__ void tma_producer(const KParams &p, const TmaMaps &maps, uint8_t *ring, uint64_t *full,
                                              uint64_t *empty)
 {
@@ -128,10 +142,10 @@ __device__ __forceinline__ void tma_producer(const KParams &p, const TmaMaps &ma
         if (!mbar_wait(&empty[slot], phase ^ 1, aborted)) break;
         const StagePos sp = stage_pos(p, it);
         const ProbParams &q = p.pr[sp.pi];
-        uint8_t *st = ring + (size_t)slot * kTmaStageBytes;
-        mbar_expect_tx(&full[slot], kTmaStageBytes);
+        uint8_t *st = ring + (size_t)slot * kTmaStage<GL>;
+        mbar_expect_tx(&full[slot], kTmaStage<GL>);
         tma_load_4d(st, &maps.u[sp.pi], sp.u_tile0, sp.kt * BK, 0, sp.b * q.u_bsel, &full[slot]);
-        tma_load_4d(st + kTmaUBytes, &maps.l[sp.pi], sp.l_tile0, sp.kt * BK, 0, sp.b * q.l_bsel, &full[slot]);
+        tma_load_4d(st + kTmaStageU<GL>, &maps.l[sp.pi], sp.l_tile0, sp.kt * BK, 0, sp.b * q.l_bsel, &full[slot]);
         ++issued;
         if (++slot == S) { slot = 0; phase ^= 1; }
     }
@@ -152,7 +166,7 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
                                              uint64_t *empty, uint64_t *red)
 {
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
+    const int lane = tid & 31, warp = uniform_warp();
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
     const int lcol = wl * 32 * TN + lane * 4;
@@ -185,24 +199,26 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
                 if (++slot == S) { slot = 0; phase ^= 1; }
                 continue;
             }
-            const uint8_t *st = ring + (size_t)slot * kTmaStageBytes;
+            // (the scale planes exist only in the two-plane stages of global-memory tables)
+            const uint8_t *st = ring + (size_t)slot * kTmaStage<GL>;
             const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
             const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
-            const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
-            const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
+            const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaStageU<GL>);
+            const float *Ls = reinterpret_cast<const float *>(st + kTmaStageU<GL> + BK * BL * 4);
+            constexpr bool PU = tma_u_planes(GL) == 1, PL = tma_l_planes(GL) == 1;
             if (slow)
-                compute_stage<W, GL, true, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                compute_stage<W, GL, true, BU, BL, false, false, PU, PL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
             else if (fold)
-                compute_stage<W, GL, false, BU, BL, false, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                compute_stage<W, GL, false, BU, BL, false, true, PU, PL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
             else
-                compute_stage<W, GL, false, BU, BL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+                compute_stage<W, GL, false, BU, BL, false, false, PU, PL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
             mbar_arrive(&empty[slot]);
             if (++slot == S) { slot = 0; phase ^= 1; }
         }
         segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, cut0, cut1, ncut);
     });
-    // the ring (at least two 40 KB stages) holds the reduction's copies
-    finish_cut_tiles(p, cut0, cut1, ncut, reinterpret_cast<float *>(ring), S * kTmaStageBytes, red, aborted);
+    // the ring (at least the reduction buffer's bytes, tma_min_stages) holds the reduction's copies
+    finish_cut_tiles(p, cut0, cut1, ncut, reinterpret_cast<float *>(ring), S * kTmaStage<GL>, red, aborted);
 }
 
 // All problems of a launch read the same LUT orientation (staged once).
@@ -217,7 +233,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     uint8_t *smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
     const int lut_bytes = GL ? 0 : lut_region_bytes(p.table_bytes);
     uint8_t *ring = smem + lut_bytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.stages * kTmaStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.stages * kTmaStage<GL>);
     uint64_t *empty = full + kTmaMaxStages;
 
     if constexpr (!GL) {
@@ -249,7 +265,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
     if (tid >= kTmaConsumerThreads) {
         if constexpr (kTmaProducerWarps == 4) reg_dealloc<kTmaProducerRegs>();
-        if (tid == kTmaConsumerThreads) tma_producer(p, maps, ring, full, empty);
+        if (tid == kTmaConsumerThreads) tma_producer<GL>(p, maps, ring, full, empty);
     } else {
         if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
         tma_consumer<W, GL>(p, lut, ring, full, empty, empty + kTmaMaxStages);

@@ -682,7 +682,7 @@ template <int W, bool GL>
 __device__ __forceinline__ void ws_consumer(const KParams &p, const WsSmem &sm)
 {
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
+    const int lane = tid & 31, warp = uniform_warp();
     const int wu = warp / WL, wl = warp % WL;
     const int urow = wu * TM;
     const int lcol = wl * 32 * TN + lane * 4;

@@ -1,7 +1,7 @@
 // Operand predecode pass of the TMA-fed LUT-GEMM (internal).
 //
-// Each job turns one operand into two planes laid out [b][plane][k][row] with
-// a row pitch of rows_pad words.  Element (b, r, k) of the operand is
+// Each job turns one operand into planes laid out [b][plane][k][row] with a
+// row pitch of rows_pad words: two planes, or one of packed words.  Element (b, r, k) of the operand is
 //   src[b*bs + (r / rdiv)*s_rhi + (r % rdiv + roff)*s_row + (k / kdiv)*s_khi + (k % kdiv)*s_k]
 // and reads as zero when r % rdiv + roff falls outside [0, rlim) -- a dense
 // matrix (rdiv = rows, kdiv = K), a filter read with its channel axes
@@ -10,7 +10,8 @@
 // element's LUT row (U operands) or column (L operands), plane 1 its signed
 // power-of-two scale (ApproxTrain Sec. V-B Algorithm 2: the operand half of
 // the product -- sign, biased exponent, top-M fraction bits, with denormals
-// as zero and NaN kept).  A job raises *flag to the launch epoch when an
+// as zero and NaN kept); a packed job writes both in one word per element
+// (pack_operand: offset << 10 | the scale's top ten bits).  A job raises *flag to the launch epoch when an
 // element has |x| >= 2^64, the magnitude above which a product may overflow,
 // *flag_small when an element of the operand has 0 < |x| < 2^-63 (a product
 // may meet Algorithm 2's zero test), *flag_zero when one is zero or denormal:
@@ -36,7 +37,8 @@ struct DecodeJob {
     int rows, K, batch;                          // batch: planes written (1 for a broadcast operand)
     int rows_pad;                                // row pitch of a plane, multiple of 4
     int offshift;                                // offset = top-M fraction bits << offshift
-    uint32_t *plane;                             // [batch][2][K][rows_pad]
+    int packed;                                  // one plane of packed words (offsets below 2^22)
+    uint32_t *plane;                             // [batch][packed ? 1 : 2][K][rows_pad]
     unsigned long long *flag, *flag_small, *flag_zero;
     int tiles_r, tiles_k;                        // 64 x 64 tiles per batch
     // row-fast: a dense operand with unit row stride (read and written along
