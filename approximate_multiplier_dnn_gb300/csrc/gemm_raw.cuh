@@ -115,15 +115,18 @@ __device__ __forceinline__ void decode_alu(float v, uint32_t keep, uint32_t &off
     }
 }
 
-// Decode mode DM: 0 the table's (offset, scale), 1 the closed-form truncated
-// value (no scale), 2 the closed-form truncated fraction and scale; aux is the
-// table offset's shift (DM 0) or the mask of the kept fraction bits.
+// Decode mode DM: 0 the table's (offset, scale), 3 the same packed into one
+// word (pack_operand; tables in shared memory, whose offsets stay below
+// 2^18), 1 the closed-form truncated value (no scale), 2 the closed-form
+// truncated fraction and scale; aux is the table offset's shift (DM 0, 3) or
+// the mask of the kept fraction bits.  Modes 1 and 3 store no scale array.
 template <int DM, bool LANE = false>
 __device__ __forceinline__ void decode_as(float v, int M, uint32_t aux, uint32_t &off, float &s, StageFlags &fl)
 {
-    if constexpr (DM == 0) {
+    if constexpr (DM == 0 || DM == 3) {
         decode(v, M, (int)aux, off, s, fl.big);
         fl.small |= LANE ? is_small_nonzero(v) : is_small(v);
+        if constexpr (DM == 3) off = pack_operand(off, s);
     } else {
         decode_alu<DM == 2>(v, aux, off, s, fl);
     }
@@ -148,7 +151,7 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
                 float s;
                 decode_as<DM, LANE>(e[i], M, aux, o, s, fl);
                 off[(4 * c + i) * R + r] = o;
-                if constexpr (DM != 1) scl[(4 * c + i) * R + r] = s;
+                if constexpr (DM != 1 && DM != 3) scl[(4 * c + i) * R + r] = s;
             }
         }
     } else {
@@ -163,7 +166,7 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
             decode_as<DM, LANE>(v.z, M, aux, o.z, s.z, fl);
             decode_as<DM, LANE>(v.w, M, aux, o.w, s.w, fl);
             *reinterpret_cast<uint4 *>(off + k * R + r4) = o;
-            if constexpr (DM != 1) *reinterpret_cast<float4 *>(scl + k * R + r4) = s;
+            if constexpr (DM != 1 && DM != 3) *reinterpret_cast<float4 *>(scl + k * R + r4) = s;
         }
     }
 }
@@ -186,7 +189,7 @@ __device__ __forceinline__ void raw_decode_blocks(const uint8_t *raw, uint32_t *
         decode_as<DM, true>(v.z, M, aux, o.z, s.z, fl);
         decode_as<DM, true>(v.w, M, aux, o.w, s.w, fl);
         *reinterpret_cast<uint4 *>(off + k * BL + 64 * b + r4) = o;
-        if constexpr (DM != 1) *reinterpret_cast<float4 *>(scl + k * BL + 64 * b + r4) = s;
+        if constexpr (DM != 1 && DM != 3) *reinterpret_cast<float4 *>(scl + k * BL + 64 * b + r4) = s;
     }
 }
 
@@ -421,15 +424,16 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
     }
 }
 
-// A decoded stage of the raw-tile kernel: table entries (W = 8, 16, 32) or
-// closed forms (W = 1 Mitchell, 2 exact).
+// A decoded stage of the raw-tile kernel: table entries (W = 8, 16, 32; packed
+// operand words with the table in shared memory) or closed forms (W = 1
+// Mitchell, 2 exact).
 template <int W, bool GL, bool SLOW, bool FOLD = false>
 __device__ __forceinline__ void raw_stage(float2 (&acc)[TM / 2][TN], const uint32_t *Uo, const float *Us,
                                           const uint32_t *Lo, const float *Ls, const uint8_t *lut, int urow,
                                           int lcol)
 {
     if constexpr (W <= 2) compute_stage_alu<W, SLOW>(acc, Uo, Us, Lo, Ls, urow, lcol);
-    else compute_stage<W, GL, SLOW, BU, BL, false, FOLD>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    else compute_stage<W, GL, SLOW, BU, BL, false, FOLD, !GL, !GL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
 }
 
 // One stage of a consumer: the rounding slow products when a decoder flagged
@@ -447,14 +451,16 @@ __device__ __forceinline__ void raw_stage_by_flags(int fl, float2 (&acc)[TM / 2]
 
 // The producer warpgroup: thread 0 also issues the copies, kRawRing - 1 stages
 // ahead.  ALU: 0 table offsets, 1 / 2 Mitchell's / the exact closed form.
-template <int ALU>
+// PK: table offsets and scales packed into one word (table in shared memory).
+template <int ALU, bool PK>
 __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &maps, const RawSmem &sm)
 {
     const int d = threadIdx.x - kTmaConsumerThreads;
     const int lane = d & 31, dw = d >> 5;
     // decode modes and their shift / fraction mask (closed forms: U keeps its
     // sign and exponent; L keeps them for the exact product, not for Mitchell's)
-    constexpr int DU = ALU ? 1 : 0, DL = ALU == 1 ? 2 : ALU ? 1 : 0;
+    constexpr int DT = PK ? 3 : 0;
+    constexpr int DU = ALU ? 1 : DT, DL = ALU == 1 ? 2 : ALU ? 1 : DT;
     const uint32_t keep = ((1u << p.M) - 1u) << (23 - p.M);
     const uint32_t offU = ALU ? keep : (uint32_t)(p.M + p.wlog), offL = ALU ? keep : (uint32_t)p.wlog;
     long long it0, it1;
@@ -696,8 +702,9 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
     const int d = threadIdx.x - kTmaConsumerThreads;
     const int lane = d & 31, dw = d >> 5;
     // decode modes and their shift / fraction mask (closed forms: U keeps its
-    // sign and exponent; L keeps them for the exact product, not for Mitchell's)
-    constexpr int DU = ALU ? 1 : 0, DL = ALU == 1 ? 2 : ALU ? 1 : 0;
+    // sign and exponent; L keeps them for the exact product, not for Mitchell's);
+    // phased launches keep the table in shared memory: packed table words
+    constexpr int DU = ALU ? 1 : 3, DL = ALU == 1 ? 2 : ALU ? 1 : 3;
     const uint32_t keep = ((1u << p.M) - 1u) << (23 - p.M);
     const uint32_t offU = ALU ? keep : (uint32_t)(p.M + p.wlog), offL = ALU ? keep : (uint32_t)p.wlog;
     IterCursor cur = cursor_start(p, pt), iss = cur;
@@ -971,7 +978,7 @@ __device__ __forceinline__ void raw_kernel_body(const KParams &p, const TmaMaps 
         if constexpr (kTmaProducerWarps == 4) reg_dealloc<kTmaProducerRegs>();
         constexpr int ALU = W <= 2 ? W : 0;
         if constexpr (PH) raw_producer_phased<ALU>(p, maps, *pt, sm);
-        else raw_producer<ALU>(p, maps, sm);
+        else raw_producer<ALU, ALU == 0 && !GL>(p, maps, sm);
     } else {
         if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
         if (!GL && p.table_bytes > 0) {
