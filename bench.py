@@ -278,15 +278,20 @@ def lut_residency(lut):
 
 # ---------------------------------------------------------------- tables in global memory
 # A table too large for shared memory (M >= 9) is read through L1TEX and L2.
-# In the row-broadcast schedule the 32 lanes of a warp-lookup read random
-# columns of one table row of R 32-byte sectors, touching R (1 - (1 - 1/R)^32)
-# distinct sectors on average (ncu's l1tex__t_sectors_pipe_lsu_mem_global_op_ld
-# per request agrees within 1 % at M = 9 and 11).  Those sectors pass the L1TEX
-# data path, which returns 4 sectors (128 B) per clock per SM; the ones that
-# miss L1 go to L2, whose sector rate on this GPU ncu reports as 564 sectors per
-# L2 clock at 2.016 GHz (lts__t_sectors.sum.peak_sustained,
-# lts__cycles_elapsed.avg.per_second; profiles/lutgemm_global_table_l2.md).
-L1TEX_SECTORS_PER_CLK_PER_SM = 4
+# The unit that binds is the L1TEX data pipe, one wavefront per clock per SM
+# (ncu: l1tex__data_pipe_lsu_wavefronts.sum.peak_sustained is 1 per SM; the
+# 4096^3 GEMM at M = 9 keeps it 98 % busy, while the tag stage's 16 sectors
+# per clock per SM run at 28 %; profiles/lutgemm_global_table_l2.md).  A
+# warp-lookup gathers 32 random columns of one table row, and a gather that
+# hits L1 is served like a shared-memory access: one wavefront per distinct
+# 4-byte word in the busiest of the 32 banks (bank_degree).  Misses cost more
+# (ncu: 4.27 wavefronts per lookup at M = 9 with 82 % of sectors hitting, 10.5
+# at M = 11 with 33 %), so the fraction below 1 is the miss cost.  The
+# operands' two-plane loads add their wavefronts (1/TN + 2/TM = 0.25 per lookup
+# on 128 x 256 tiles).  Misses go to L2, whose sector rate ncu reports as 564
+# per L2 clock at 2.016 GHz (lts__t_sectors.sum.peak_sustained).
+L1TEX_WAVEFRONTS_PER_CLK_PER_SM = 1
+GL_OPERAND_WAVEFRONTS_PER_LOOKUP = 0.25
 L2_SECTORS_PER_CLK = 564
 L2_CLK_HZ = 2.016e9
 
@@ -296,21 +301,42 @@ def distinct_sectors_per_warp_lookup(M, width_bits):
     return R * (1.0 - (1.0 - 1.0 / R) ** 32)
 
 
+def bank_degree(M, width_bits, trials=20000):
+    """Expected wavefronts of one warp's gather: the most distinct 4-byte words
+    that any of the 32 banks holds among 32 uniformly random columns of a row
+    of 2^M entries of width_bits (rows start on 128-byte boundaries).  Monte
+    Carlo with a fixed seed."""
+    import numpy as np
+    rng = np.random.default_rng(12345)
+    words = np.sort(rng.integers(0, 1 << M, size=(trials, 32)) * (width_bits // 8) // 4, axis=1)
+    first = np.ones_like(words, dtype=bool)
+    first[:, 1:] = words[:, 1:] != words[:, :-1]
+    t = np.repeat(np.arange(trials), 32).reshape(trials, 32)
+    per_bank = np.bincount((t * 32 + words % 32)[first], minlength=trials * 32).reshape(trials, 32)
+    return float(per_bank.max(axis=1).mean())
+
+
 def global_table_roofline(lut, lut_macs, lut_ms, sms, mhz, smem_roofline):
-    """Roofline of a LUT-GEMM whose table is read from global memory: the
-    algorithmic sectors of its gathers against the L1TEX data path (the bound
-    it runs closest to) and against the L2 sector rate."""
+    """Roofline of a LUT-GEMM whose table is read from global memory: its
+    gathers' and operand loads' L1TEX data-pipe wavefronts (the bound it runs
+    closest to), with the L2 sector rate beside it."""
     info = lut.info()
+    deg = bank_degree(info["M"], info["width_bits"])
+    wpl = deg + GL_OPERAND_WAVEFRONTS_PER_LOOKUP
+    lookups_s = lut_macs / 32.0 / (lut_ms * 1e-3)
+    peak = sms * L1TEX_WAVEFRONTS_PER_CLK_PER_SM * mhz * 1e6
     spw = distinct_sectors_per_warp_lookup(info["M"], info["width_bits"])
-    sectors_s = lut_macs / 32.0 * spw / (lut_ms * 1e-3)
-    l1_peak = sms * L1TEX_SECTORS_PER_CLK_PER_SM * mhz * 1e6
+    sectors_s = lookups_s * spw
     l2_peak = L2_SECTORS_PER_CLK * L2_CLK_HZ
-    return {"bound": "l1tex", "pipe": "L1TEX data path, 4 sectors (128 B) per clock per SM, for the table's gathers",
-            "achieved": sectors_s * 32 / 1e9, "peak": l1_peak * 32 / 1e9, "unit": "GB/s",
-            "frac": sectors_s / l1_peak, "traffic": None,
-            "sectors_per_warp_lookup": spw,
+    return {"bound": "l1tex", "pipe": "L1TEX data pipe, 1 wavefront per clock per SM: a warp-lookup's gather costs "
+                                      "its bank degree, plus the operand loads",
+            "achieved": lookups_s * wpl / 1e9, "peak": peak / 1e9, "unit": "Gwavefront/s",
+            "frac": lookups_s * wpl / peak, "traffic": None,
+            "wavefronts_per_warp_lookup": {"gather_bank_degree": round(deg, 3),
+                                           "operands": GL_OPERAND_WAVEFRONTS_PER_LOOKUP},
             "l2": {"achieved": sectors_s * 32 / 1e9, "peak": l2_peak * 32 / 1e9, "unit": "GB/s",
                    "frac_if_every_sector_missed_l1": sectors_s / l2_peak,
+                   "sectors_per_warp_lookup": spw,
                    "note": "ncu measures the sectors that reach L2 per launch (profiles/lutgemm_global_table_l2.md)"},
             "lookup_roofline_frac": smem_roofline["frac"], "lut_residency": "global (L1TEX/L2 gathers)",
             "kernel": smem_roofline["kernel"], "sms": sms, "sm_mhz": mhz}
