@@ -20,7 +20,7 @@ struct amsim_lut_s {
     const uint32_t *d_canon = nullptr;   // 2^(2M) canonical entries, index p<<M|q
     const void *d_narrow = nullptr;      // narrowed, index [first operand][second operand]
     const void *d_narrow_t = nullptr;    // narrowed, index [second operand][first operand]
-    size_t narrow_bytes = 0;
+    size_t narrow_bytes = 0;             // 2^(2M) narrowed entries (each copy is followed by a zero row)
     int kind = -1;              // AMSIM_EXACT / AMSIM_MITCHELL when built from a kind, else -1
     bool closed_form = false;   // raw-tile launches compute products in registers (kinds only)
     int exp_bits = 8;           // exponent bits E of the simulated (1, E, M) format
@@ -59,6 +59,14 @@ inline ExpFormat exp_format(int E)
     __builtin_memcpy(&f.vscale, &vb, 4);
     __builtin_memcpy(&f.lim, &lb, 4);
     return f;
+}
+
+// Bytes of a narrowed table as the LUT-GEMM kernels stage and read it: its
+// 2^(2M) entries, then one row of 2^M zero entries, the row zero uniform
+// operands index (kern::uniform_zero_row).
+inline size_t gemm_table_bytes(const amsim_lut_s *L)
+{
+    return L->narrow_bytes + ((size_t)1 << L->M) * (size_t)(L->width_bits / 8);
 }
 
 namespace amsim {

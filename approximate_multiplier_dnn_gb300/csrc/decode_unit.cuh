@@ -57,7 +57,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
     const float *src = d.src + (long long)b * d.bs;
     uint32_t *po = d.plane + (size_t)b * (d.packed ? 1 : 2) * d.K * d.rows_pad;
     float *ps = reinterpret_cast<float *>(po + (size_t)d.K * d.rows_pad);   // two-plane layout only
-    int big = 0, small = 0, zero = 0;
+    int big = 0, small = 0;
     if (d.rowfast) {
         // rows r .. r + 3 at reduction steps k0 + grp + 16 i
         const int r = r0 + lane4;
@@ -77,14 +77,13 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
                 }
                 uint4 o4;
                 float4 s4;
-                decode(v[0], p.M, d.offshift, o4.x, s4.x, big);
-                decode(v[1], p.M, d.offshift, o4.y, s4.y, big);
-                decode(v[2], p.M, d.offshift, o4.z, s4.z, big);
-                decode(v[3], p.M, d.offshift, o4.w, s4.w, big);
+                decode(v[0], p.M, d.offshift, o4.x, s4.x, big, d.zero_off);
+                decode(v[1], p.M, d.offshift, o4.y, s4.y, big, d.zero_off);
+                decode(v[2], p.M, d.offshift, o4.z, s4.z, big, d.zero_off);
+                decode(v[3], p.M, d.offshift, o4.w, s4.w, big, d.zero_off);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     small |= r + e < d.rows && is_small_nonzero(v[e]);
-                    zero |= r + e < d.rows && is_small(v[e]) && !is_small_nonzero(v[e]);
                 }
                 // rows_pad is a multiple of 4: the pad columns of a partial quad may be written
                 store_quad(d, po, ps, (size_t)k * d.rows_pad + r, o4, s4);
@@ -125,9 +124,8 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
                 uint32_t o = 0;
                 float sc = 0.0f;                 // outside the operand: offset 0, scale +0
                 if (ok[e]) {
-                    decode(v[e], p.M, d.offshift, o, sc, big);
+                    decode(v[e], p.M, d.offshift, o, sc, big, d.zero_off);
                     small |= is_small_nonzero(v[e]);
-                    zero |= is_small(v[e]) && !is_small_nonzero(v[e]);
                 }
                 t_off[lane4 + e][grp + 16 * i] = o;
                 t_scl[lane4 + e][grp + 16 * i] = sc;
@@ -156,7 +154,6 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &p, long long t, 
     // (or a small) element
     if (__any_sync(0xFFFFFFFFu, big) && (tid & 31) == 0) *d.flag = p.epoch;
     if (__any_sync(0xFFFFFFFFu, small) && (tid & 31) == 0) *d.flag_small = p.epoch;
-    if (__any_sync(0xFFFFFFFFu, zero) && (tid & 31) == 0) *d.flag_zero = p.epoch;
 }
 
 }  // namespace kern

@@ -125,11 +125,11 @@ EncodeTiled encode_tiled()
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// three 8-byte flags per plane: "an element with |x| >= 2^64" at [j], "an
-// element with 0 < |x| < 2^-63" at [kMaxDecodeJobs + j], "a zero or denormal
-// element" at [2 kMaxDecodeJobs + j]
+// two 8-byte flags per plane: "an element with |x| >= 2^64" at [j], "an
+// element with 0 < |x| < 2^-63" at [kMaxDecodeJobs + j] (the block keeps its
+// 512 bytes, part of the scratch size callers have been told)
 constexpr size_t kFlagBlock = 512;
-static_assert(kern::kMaxDecodeJobs * 24 <= (int)kFlagBlock, "plane flags fit the block");
+static_assert(kern::kMaxDecodeJobs * 16 <= (int)kFlagBlock, "plane flags fit the block");
 
 struct PlaneKey {
     const float *src;
@@ -163,6 +163,7 @@ struct PlaneSet {
     size_t off[kern::kMaxDecodeJobs];    // from the start of the plane region
     int n;
     int nplanes[kern::kMaxDecodeJobs];   // 1: packed words, 2: offset and scale planes
+    bool uniform[kern::kMaxDecodeJobs];  // the plane of a U operand (its zeros take the table's zero row)
     int slot[2 * kern::kMaxProblems];
     size_t bytes;
     double elems;    // operand elements decoded (padded rows), for the path decision
@@ -188,6 +189,7 @@ bool plan_planes(const Problem *p, int n, const Plan &pl, int M, int wlog, int p
                 ps->off[j] = ps->bytes;
                 // (U and L planes never coincide: their offset shifts differ)
                 ps->nplanes[j] = r == 0 ? (planes & 3) : (planes >> 2);
+                ps->uniform[j] = r == 0;
                 ps->bytes += plane_bytes(k, ps->nplanes[j]);
                 ps->elems += (double)k.nb * k.K * rows_pad(k.rows);
                 ++ps->n;
@@ -205,12 +207,33 @@ bool plan_planes(const Problem *p, int n, const Plan &pl, int M, int wlog, int p
 // plane bytes per MAC gains, 0.13 loses.  Below 64 MB of planes the pass
 // costs microseconds either way.  The measure stays 8 bytes per decoded
 // element, whatever the planes' layout, so the thresholds keep their meaning.
-double planes_bytes_per_mac(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
+double launch_macs(const Problem *p, int n, const Plan &pl)
 {
     double macs = 0.0;
     for (int i = 0; i < n; ++i)
         if (pl.tiles[i] > 0) macs += (double)p[i].U.rows * p[i].L.rows * (double)p[i].K * p[i].batch;
+    return macs;
+}
+
+double planes_bytes_per_mac(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
+{
+    const double macs = launch_macs(p, n, pl);
     return macs > 0.0 ? 8.0 * ps.elems / macs : 1e30;
+}
+
+// Planes rather than raw tiles, for operands the raw-tile kernel could read
+// in place.  Measured on GB300 (plane kernel with wide tiles and packed
+// words, raw-tile kernel with 64 x 256 tiles), in plane bytes per MAC:
+//  * 2048^3 (0.008): planes; 1024^3 (0.016): planes 4 % faster;
+//  * batched 512 x 512 x 64 attention scores and a 1x1 conv's 200704 x 256 x
+//    256 GEMM (0.031): planes 7 % faster;
+//  * 256 x 256 x 16384 and 65536 x 128 x 512 (0.063): raw 2-6 % faster;
+//  * an MLP layer's GEMMs (200 M MACs or fewer, 0.018 - 0.05) and 512^3: raw
+//    9 - 20 % faster -- the predecode launch is not paid back.
+bool planes_beat_raw(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
+{
+    const double bpm = planes_bytes_per_mac(p, n, pl, ps);
+    return bpm < 0.01 || (bpm < 0.04 && launch_macs(p, n, pl) >= 1073741824.0);
 }
 
 bool planes_pay(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
@@ -249,8 +272,8 @@ struct TmaChoice {
 
 TmaChoice tma_choice(amsim_lut_t lut)
 {
-    if (lut->narrow_bytes <= (size_t)kMaxSmemLut) {
-        const size_t lutb = kern::lut_region_bytes((int)lut->narrow_bytes);
+    if (gemm_table_bytes(lut) <= (size_t)kMaxSmemLut) {
+        const size_t lutb = kern::lut_region_bytes((int)gemm_table_bytes(lut));
         const int planes = kern::tma_planes(false);
         if (const int s = tma_stages(lutb, kern::kWideTiles, planes))
             return {kern::kWideTiles, true, false, planes, s, lutb};
@@ -442,8 +465,7 @@ size_t problems_workspace(const Problem *p, int n, amsim_lut_t lut)
     const int rwlog = lut ? (lut->width_bits == 8 ? 0 : lut->width_bits == 16 ? 1 : 2) : 0;
     if (lut && encode_tiled() && pl.iters < 0x7FFFFFFFLL && all_raw_ok(p, n, pl, false) &&
         (alu_code(lut) ||
-         !(plan_planes(p, n, pl, lut->M, rwlog, 2 + 4 * 2, &rps) && rps.n > 0 &&
-           planes_bytes_per_mac(p, n, pl, rps) < 0.01))) {
+         !(plan_planes(p, n, pl, lut->M, rwlog, 2 + 4 * 2, &rps) && rps.n > 0 && planes_beat_raw(p, n, pl, rps)))) {
         // operand tiles are copied in place and decoded inside the GEMM
     } else if (lut && encode_tiled() && n == 1 && p[0].conv) {
         // convolution tiles are copied in place as tensor boxes
@@ -538,10 +560,10 @@ size_t raw_smem(amsim_lut_t lut, bool *gl)
         *gl = false;
         return (size_t)kern::raw_smem_bytes(0);
     }
-    bool raw_gl = lut->narrow_bytes > (size_t)kMaxSmemLut;
-    if (!raw_gl && kern::raw_smem_bytes((int)lut->narrow_bytes) > kMaxSmemPerCta) raw_gl = true;
+    bool raw_gl = gemm_table_bytes(lut) > (size_t)kMaxSmemLut;
+    if (!raw_gl && kern::raw_smem_bytes((int)gemm_table_bytes(lut)) > kMaxSmemPerCta) raw_gl = true;
     *gl = raw_gl;
-    return (size_t)kern::raw_smem_bytes(raw_gl ? 0 : (int)lut->narrow_bytes);
+    return (size_t)kern::raw_smem_bytes(raw_gl ? 0 : (int)gemm_table_bytes(lut));
 }
 
 // One launch for problems that all read the same LUT orientation.
@@ -557,15 +579,15 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
 
     // Shared-memory LUT when it fits beside the warp-specialised kernel's
     // rings; else beside the single-role kernel's stages; else read from global.
-    const size_t lut_smem = kern::lut_region_bytes((int)lut->narrow_bytes);
+    const size_t lut_smem = kern::lut_region_bytes((int)gemm_table_bytes(lut));
     bool use_ws = true, gl = false;
-    if (lut->narrow_bytes > (size_t)kMaxSmemLut) gl = true;
+    if (gemm_table_bytes(lut) > (size_t)kMaxSmemLut) gl = true;
     else if ((size_t)kern::kWsFixedSmem + lut_smem <= (size_t)kMaxSmemPerCta) gl = false;
     else if ((size_t)kern::kFixedSmem + lut_smem <= (size_t)kMaxSmemPerCta) use_ws = false;
     else gl = true;
     kern::KParams kp = {};
     fill_params(p, n, pl, lut, kp);
-    kp.table_bytes = gl ? 0 : (int)lut->narrow_bytes;
+    kp.table_bytes = gl ? 0 : (int)gemm_table_bytes(lut);
     kp.ws = static_cast<float *>(ws);
 
     const long long blocks = pl.streamk ? pl.ctas : pl.total_tiles;
@@ -573,10 +595,8 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
 
     // Raw operand tiles copied in place by TMA and decoded in shared memory,
     // when every operand is dense with copy-engine strides -- unless planes
-    // fit the scratch and are reused so much that decoding each element once
-    // is cheaper than once per tile (measured on GB300: the 4096^3 GEMM, at
-    // 0.004 plane bytes per MAC, runs 5 % faster on planes; attention scores,
-    // at 0.03, 1 % slower; attention's P V 11 % slower).
+    // fit the scratch and beat them (planes_beat_raw: large launches whose
+    // operand elements are reused by many tiles).
     // The predecoded kernel's tile shape and its own plan, which it runs only
     // as planned with unlimited scratch (planes after its stream-K region).
     const TmaChoice tc = tma_choice(lut);
@@ -593,7 +613,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     const int alu = alu_code(lut);
     const bool fmt = kp.fmt.on != 0;
     if (!fmt && (conv_raw || (raw_fits && encode_tiled() && all_raw_ok(p, n, pl, true) &&
-                              (alu || !(planes_fit && planes_bytes_per_mac(p, n, pl, ps) < 0.01))))) {
+                              (alu || !(planes_fit && planes_beat_raw(p, n, pl, ps)))))) {
         bool raw_gl = false;
         const size_t smem = raw_smem(lut, &raw_gl);
         kern::TmaMaps maps = {};
@@ -626,7 +646,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
         }
         if (erc == AMSIM_OK) {
             tp.alu = alu;
-            tp.table_bytes = (raw_gl || alu) ? 0 : (int)lut->narrow_bytes;
+            tp.table_bytes = (raw_gl || alu) ? 0 : (int)gemm_table_bytes(lut);
             tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
             tp.fused = pl.streamk ? 1 : 0;
             const dim3 grid((unsigned)blocks);
@@ -685,7 +705,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             d.plane = reinterpret_cast<uint32_t *>(planes + ps.off[j]);
             d.flag = flags + j;
             d.flag_small = flags + kern::kMaxDecodeJobs + j;
-            d.flag_zero = flags + 2 * kern::kMaxDecodeJobs + j;
+            d.zero_off = ps.uniform[j] ? kern::uniform_zero_row(lut->M, k.offshift) : 0u;
             d.tiles_r = ceil_div(k.rows, kern::kDecodeTileR);
             d.tiles_k = ceil_div(k.K, kern::kDecodeTileK);
             d.tile0 = dtiles;
@@ -707,12 +727,11 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             q.l_big = flags + jl;
             q.u_small = flags + kern::kMaxDecodeJobs + ju;
             q.l_small = flags + kern::kMaxDecodeJobs + jl;
-            q.u_zero = flags + 2 * kern::kMaxDecodeJobs + ju;
             q.u_bsel = ps.key[ju].nb > 1 ? 1 : 0;
             q.l_bsel = ps.key[jl].nb > 1 ? 1 : 0;
         }
         if (erc == AMSIM_OK) {
-            tp.table_bytes = tc.gl ? 0 : (int)lut->narrow_bytes;
+            tp.table_bytes = tc.gl ? 0 : (int)gemm_table_bytes(lut);
             tp.stages = tc.stages;
             tp.epoch = epoch;
             const size_t smem = (size_t)kern::tma_cfg_smem_bytes(tc.tc, tc.planes, (int)tc.lutb, tp.stages);
@@ -906,7 +925,7 @@ int run_phased(const Problem *p, int n, int nphase, const int *first, const int 
         bool gl = false;
         const size_t smem = raw_smem(lut, &gl);
         tp.alu = alu_code(lut);
-        tp.table_bytes = (gl || tp.alu) ? 0 : (int)lut->narrow_bytes;
+        tp.table_bytes = (gl || tp.alu) ? 0 : (int)gemm_table_bytes(lut);
         tp.ws = static_cast<float *>(ws);
         tp.nphase = nphase;
         for (int ph = 0; ph < nphase; ++ph) {

@@ -97,7 +97,7 @@ struct ProbParams {
     const unsigned long long *u_big, *l_big;
     // ... its "holds an element with 0 < |x| < 2^-63" and "holds a zero (or a
     // denormal)" flags
-    const unsigned long long *u_small, *l_small, *u_zero;
+    const unsigned long long *u_small, *l_small;
     int u_bsel, l_bsel;
     // Raw-tile kernel: the operand is read with plain loads by the decoders
     // (strides the copy engine cannot take) instead of a tensor box.
@@ -287,12 +287,15 @@ __device__ __forceinline__ float expand(uint32_t narrowed)
 // Operand decode (once per element per CTA): byte offset of the mantissa's LUT
 // row/column and the signed power-of-two scale 2^(e-127).  Zero and denormal
 // inputs give a signed zero scale, infinities an infinite scale, NaN a NaN scale.
-__device__ __forceinline__ void decode(float v, int M, int offshift, uint32_t &off, float &s, int &big)
+// zoff: for uniform (U) operands the byte offset of the table's zero row
+// (uniform_zero_row), which zero and denormal elements take -- so that the
+// folded form rebuilds a signed zero from them -- and 0 for lane operands.
+__device__ __forceinline__ void decode(float v, int M, int offshift, uint32_t &off, float &s, int &big, uint32_t zoff)
 {
     const uint32_t x = __float_as_uint(v);
     const uint32_t e = (x >> 23) & 0xFFu;
     const uint32_t f = x & 0x7FFFFFu;
-    off = (f >> (23 - M)) << offshift;
+    off = (e == 0u && zoff) ? zoff : (f >> (23 - M)) << offshift;
     uint32_t sb = x & 0xFF800000u;          // e == 0 leaves only the sign
     if (e == 255u && f) sb = 0x7FC00000u;
     s = __uint_as_float(sb);
@@ -317,6 +320,16 @@ __device__ __forceinline__ uint32_t packed_scale_bits(uint32_t w)
     uint32_t r;
     asm("mul.lo.u32 %0, %1, %2;" : "=r"(r) : "r"(w), "n"(1u << (32 - kPackShift)));
     return r;
+}
+
+// Byte offset of the zero row that every narrowed table carries after its 2^M
+// rows (all entries zero): row 2^M of a table whose rows are 2^M entries of
+// 2^(offshift - M) bytes, offshift being the uniform operand's offset shift.
+// With it a zero uniform operand's folded entry is its scale bits alone, a
+// signed zero, and the general form's entry is 1.0 times a zero scale.
+__host__ __device__ __forceinline__ uint32_t uniform_zero_row(int M, int offshift)
+{
+    return (1u << M) << offshift;
 }
 
 // Scale bits of an operand after the exponent cast of a (1, E, M) format,
@@ -515,7 +528,8 @@ struct Loader {
 
     // Decode into the stage buffers: off[k][row], scale[k][row] (row stride ST words).
     template <int ST>
-    __device__ __forceinline__ void store(uint32_t *off, float *scl, int M, int offshift, int &big) const
+    __device__ __forceinline__ void store(uint32_t *off, float *scl, int M, int offshift, int &big,
+                                          uint32_t zoff) const
     {
 #pragma unroll
         for (int e = 0; e < N; ++e) {
@@ -523,7 +537,7 @@ struct Loader {
             const int k = k_of(e);
             uint32_t o;
             float s;
-            decode(v[e], M, offshift, o, s, big);
+            decode(v[e], M, offshift, o, s, big, zoff);
             off[k * ST + r] = o;
             scl[k * ST + r] = s;
         }
@@ -756,8 +770,8 @@ __device__ __forceinline__ void run_stages(const KParams &p, const ProbParams &q
         ldU.template store_fmt<UST>(sm.Uoff, sm.Uscl, p.M, offU, p.fmt, p.fmt.off_u);
         ldL.template store_fmt<LST>(sm.Loff, sm.Lscl, p.M, offL, p.fmt, p.fmt.off_l);
     } else {
-        ldU.template store<UST>(sm.Uoff, sm.Uscl, p.M, offU, big);
-        ldL.template store<LST>(sm.Loff, sm.Lscl, p.M, offL, big);
+        ldU.template store<UST>(sm.Uoff, sm.Uscl, p.M, offU, big, uniform_zero_row(p.M, offU));
+        ldL.template store<LST>(sm.Loff, sm.Lscl, p.M, offL, big, 0u);
     }
     int slow = __syncthreads_or(big);
 
@@ -786,8 +800,9 @@ __device__ __forceinline__ void run_stages(const KParams &p, const ProbParams &q
                 ldL.template store_fmt<LST>(sm.Loff + nb * BK * LST, sm.Lscl + nb * BK * LST, p.M, offL, p.fmt,
                                             p.fmt.off_l);
             } else {
-                ldU.template store<UST>(sm.Uoff + nb * BK * UST, sm.Uscl + nb * BK * UST, p.M, offU, nbig);
-                ldL.template store<LST>(sm.Loff + nb * BK * LST, sm.Lscl + nb * BK * LST, p.M, offL, nbig);
+                ldU.template store<UST>(sm.Uoff + nb * BK * UST, sm.Uscl + nb * BK * UST, p.M, offU, nbig,
+                                        uniform_zero_row(p.M, offU));
+                ldL.template store<LST>(sm.Loff + nb * BK * LST, sm.Lscl + nb * BK * LST, p.M, offL, nbig, 0u);
             }
         }
         slow = __syncthreads_or(nbig);

@@ -79,10 +79,9 @@ struct StageFlags {
         return big | (amax >= 0x5F800000u) | (aminm1 < 0x1FFFFFFFu);
     }
     // bit 0: the stage takes the rounding slow products; bit 1: it may not
-    // fold the uniform scale into the entry -- a uniform (U) operand below
-    // 2^-63 (zero and denormal included, padded positions among them), or a
-    // lane (L) operand below 2^-63 but not zero (zero L operands give exact
-    // zero products in the folded form too)
+    // fold the uniform scale into the entry -- an operand below 2^-63 but not
+    // zero (zero uniform operands take the table's zero row and zero lane
+    // operands a zero scale: both give the exact signed zero product folded)
     __device__ __forceinline__ int bits() const { return (any() ? 1 : 0) | (small ? 2 : 0); }
 };
 
@@ -124,8 +123,8 @@ template <int DM, bool LANE = false>
 __device__ __forceinline__ void decode_as(float v, int M, uint32_t aux, uint32_t &off, float &s, StageFlags &fl)
 {
     if constexpr (DM == 0 || DM == 3) {
-        decode(v, M, (int)aux, off, s, fl.big);
-        fl.small |= LANE ? is_small_nonzero(v) : is_small(v);
+        decode(v, M, (int)aux, off, s, fl.big, LANE ? 0u : uniform_zero_row(M, (int)aux));
+        fl.small |= is_small_nonzero(v);
         if constexpr (DM == 3) off = pack_operand(off, s);
     } else {
         decode_alu<DM == 2>(v, aux, off, s, fl);

@@ -179,12 +179,11 @@ __device__ __forceinline__ void tma_consumer(const KParams &p, const uint8_t *lu
     for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
         // a problem with an operand of magnitude >= 2^64 rounds every product before adding it
         const bool slow = __ldcg(q.u_big) == p.epoch || __ldcg(q.l_big) == p.epoch;
-        // a problem whose operands lie in [2^-63, 2^64) (lane operands: or are zero)
-        // folds the uniform scale into the entry -- with the table in shared memory;
+        // a problem whose operands are zero or lie in [2^-63, 2^64) folds the
+        // uniform scale into the entry -- with the table in shared memory;
         // gathers from a table in global memory are bound by their misses, and
         // measured slower in the folded form
-        const bool fold = !GL && !slow && __ldcg(q.u_small) != p.epoch && __ldcg(q.u_zero) != p.epoch &&
-                          __ldcg(q.l_small) != p.epoch;
+        const bool fold = !GL && !slow && __ldcg(q.u_small) != p.epoch && __ldcg(q.l_small) != p.epoch;
         float2 acc[TM / 2][TN];
 #pragma unroll
         for (int i = 0; i < TM / 2; ++i)

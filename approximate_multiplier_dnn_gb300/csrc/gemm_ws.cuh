@@ -333,8 +333,9 @@ struct PIssue {
 
 // Decode this thread's landed elements of a stage into the consumer layout
 // (fmt: with the exponent cast of a (1, E, M) format, scale re-bias eoff).
-// nofold collects the elements that keep the stage in the general form (a
-// uniform operand below 2^-63, zeros included; a nonzero lane operand below it).
+// nofold collects the elements that keep the stage in the general form: a
+// nonzero operand below 2^-63 (zero uniform operands take the table's zero
+// row, zero lane operands a zero scale; both fold).
 template <int R, int ST, bool LANE>
 __device__ __forceinline__ void pdecode(const PMap<R> &map, const float *raw, int tid, uint32_t *off, float *scl,
                                         int M, int offshift, int &big, int &nofold, const ExpFormat &fmt, int eoff)
@@ -353,8 +354,8 @@ __device__ __forceinline__ void pdecode(const PMap<R> &map, const float *raw, in
             if (fmt.on) {
                 decode_fmt(v[j], M, offshift, fmt, eoff, o, sc);
             } else {
-                decode(v[j], M, offshift, o, sc, big);
-                nofold |= LANE ? is_small_nonzero(v[j]) : is_small(v[j]);
+                decode(v[j], M, offshift, o, sc, big, LANE ? 0u : uniform_zero_row(M, offshift));
+                nofold |= is_small_nonzero(v[j]);
             }
             off[map.k_of(e) * ST + map.row_of(e)] = o;
             scl[map.k_of(e) * ST + map.row_of(e)] = sc;

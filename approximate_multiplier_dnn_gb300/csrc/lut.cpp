@@ -98,9 +98,12 @@ int build_from_entries(const uint32_t *entries, int M, amsim_lut_t *out)
 
     const size_t canon_bytes = n * 4;
     const size_t narrow_bytes = n * (width / 8);
+    // each narrowed copy is followed by a row of zero entries (the host buffer
+    // is zero-filled), which zero uniform operands index in the GEMM kernels
+    const size_t zero_row = side * (width / 8);
     const size_t off_narrow = align256(canon_bytes);
-    const size_t off_narrow_t = align256(off_narrow + narrow_bytes);
-    const size_t total = symmetric ? off_narrow_t : align256(off_narrow_t + narrow_bytes);
+    const size_t off_narrow_t = align256(off_narrow + narrow_bytes + zero_row);
+    const size_t total = symmetric ? off_narrow_t : align256(off_narrow_t + narrow_bytes + zero_row);
 
     std::vector<uint8_t> host(total, 0);
     std::memcpy(host.data(), entries, canon_bytes);

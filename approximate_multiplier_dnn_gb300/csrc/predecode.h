@@ -11,11 +11,13 @@
 // power-of-two scale (ApproxTrain Sec. V-B Algorithm 2: the operand half of
 // the product -- sign, biased exponent, top-M fraction bits, with denormals
 // as zero and NaN kept); a packed job writes both in one word per element
-// (pack_operand: offset << 10 | the scale's top ten bits).  A job raises *flag to the launch epoch when an
-// element has |x| >= 2^64, the magnitude above which a product may overflow,
-// *flag_small when an element of the operand has 0 < |x| < 2^-63 (a product
-// may meet Algorithm 2's zero test), *flag_zero when one is zero or denormal:
-// a plane with none of the three holds only magnitudes in [2^-63, 2^64).
+// (pack_operand: offset << 10 | the scale's top ten bits).  Zero and denormal
+// elements of a uniform (U) operand take the table's zero row (zero_off; 0
+// for lane operands).  A job raises *flag to the launch epoch when an element
+// has |x| >= 2^64, the magnitude above which a product may overflow, and
+// *flag_small when one has 0 < |x| < 2^-63 (a product may meet Algorithm 2's
+// zero test): a plane with neither holds only zeros and magnitudes in
+// [2^-63, 2^64).
 #pragma once
 
 #include <cstdint>
@@ -39,7 +41,8 @@ struct DecodeJob {
     int offshift;                                // offset = top-M fraction bits << offshift
     int packed;                                  // one plane of packed words (offsets below 2^22)
     uint32_t *plane;                             // [batch][packed ? 1 : 2][K][rows_pad]
-    unsigned long long *flag, *flag_small, *flag_zero;
+    unsigned long long *flag, *flag_small;
+    uint32_t zero_off;                           // U planes: the zero row's byte offset; L planes: 0
     int tiles_r, tiles_k;                        // 64 x 64 tiles per batch
     // row-fast: a dense operand with unit row stride (read and written along
     // rows); vec: 16-byte loads of 4 consecutive rows (row-fast) or steps

@@ -335,12 +335,18 @@ def test_paths_bit_identical_without_stream_k(amd, luts):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     lut = luts("mitchell", 7)
     k = 100
-    cases = [(64 * sms, 200, ("in_kernel", "none"))]
+    cases = [(64 * sms, 200, ("in_kernel", "none"), False)]
     if sms % 4 == 0:
         # n in (768, 1024]: four lane tiles; m / 128 * 4 = SMs; 0.0096 plane bytes per MAC takes the planes
-        cases.append((128 * sms // 4, 1000, ("planes", "none")))
-    for m, n, paths in cases:
+        cases.append((128 * sms // 4, 1000, ("planes", "none"), False))
+        # ReLU-like zeros in both operands: the folded form (zero uniform
+        # operands through the table's zero row) on every path
+        cases.append((128 * sms // 4, 1000, ("planes", "none"), True))
+    for m, n, paths, zeros in cases:
         A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+        if zeros:
+            A[A < 0] = 0.0
+            B[B < -0.3] = -0.0
         outs, bits = [], []
         for p in paths:
             outs.append(gpu_gemm(amd, lut, A, B, False, False, ws=_path_ws(amd, lut, p, "N", "N", m, n, k)))
@@ -353,17 +359,25 @@ def test_paths_bit_identical_without_stream_k(amd, luts):
             assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)), (m, n, paths)
 
 
+@pytest.mark.parametrize("zeros", [False, True])
 @pytest.mark.parametrize("kind,M,wide", [("mitchell", 7, True), ("exact", 7, True), ("mitchell", 8, False),
                                          ("mitchell", 9, True)])
-def test_predecoded_tile_shape_by_table(amd, orc, luts, kind, M, wide):
+def test_predecoded_tile_shape_by_table(amd, orc, luts, kind, M, wide, zeros):
     """The predecoded kernel takes the wide 128 x 256 tiles when their ring fits
     beside the table in shared memory (8- and 16-bit M = 7 tables) or when the
     table is read from global memory (M = 9), and the narrow tiles for the
-    128 KB M = 8 table; 98 wide tiles on the SMs cut some tiles by stream-K."""
+    128 KB M = 8 table; 98 wide tiles on the SMs cut some tiles by stream-K.
+    With ReLU-like zeros (and signed zeros, denormals) in both operands the
+    uniform operand's zeros take the table's zero row."""
     rng = np.random.default_rng(16 + M)
     m = n = 1700
     k = 64
     A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    if zeros:
+        A[A < 0.1] = 0.0
+        B[B > 0.2] = -0.0
+        A[::7, ::5] = np.float32(1e-40)
+        B[::5, ::3] = np.float32(-3e-39)
     lut = luts(kind, M)
     got = gpu_gemm(amd, lut, A, B, False, False)
     bits = amd.amsim_last_path()
