@@ -242,6 +242,16 @@ bool planes_pay(const Problem *p, int n, const Plan &pl, const PlaneSet &ps)
     return planes_bytes_per_mac(p, n, pl, ps) <= 0.05;
 }
 
+// Every box dimension of a tiled tensor map must lie in [1, 256].  A launch
+// built with a 512-row box was not refused by the encoder and its copies
+// faulted the GPU (illegal address), so maps are checked here first.
+bool boxes_ok(const cuuint32_t *box, int rank)
+{
+    for (int i = 0; i < rank; ++i)
+        if (box[i] < 1 || box[i] > 256) return false;
+    return true;
+}
+
 // Ring depth of the TMA kernel with tiles of shape tc beside a LUT region of
 // lut_bytes (0 if none fits).
 int tma_stages(size_t lut_bytes, const kern::TileCfg &tc, int planes)
@@ -292,6 +302,7 @@ int encode_plane_map(CUtensorMap *map, const PlaneKey &k, void *base, int box_ro
     const cuuint64_t dims[4] = {(cuuint64_t)k.rows, (cuuint64_t)k.K, (cuuint64_t)planes, (cuuint64_t)k.nb};
     const cuuint64_t strides[3] = {pitch, pitch * (cuuint64_t)k.K, pitch * (cuuint64_t)k.K * planes};
     const cuuint32_t box[4] = {(cuuint32_t)box_rows, (cuuint32_t)box_k, (cuuint32_t)planes, 1};
+    if (!boxes_ok(box, 4)) return AMSIM_EUNSUPPORTED;
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -324,6 +335,7 @@ int encode_raw_spec(CUtensorMap *map, const TmaRawMap &m)
         estr[i] = 1;
         if (i + 1 < m.rank) strides[i] = m.strides[i];
     }
+    if (!boxes_ok(box, m.rank)) return AMSIM_EUNSUPPORTED;
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)m.rank, const_cast<float *>(m.base), dims,
                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            m.swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -423,6 +435,7 @@ int encode_raw_map(CUtensorMap *map, const OperandDesc &d, int K, int batch, int
     const cuuint64_t strides[2] = {outer * 4, bstride};
     const cuuint32_t box[3] = {rowfast ? (cuuint32_t)box_rows : (cuuint32_t)kern::BK,
                                rowfast ? (cuuint32_t)kern::BK : (cuuint32_t)box_rows, 1};
+    if (!boxes_ok(box, 3)) return AMSIM_EUNSUPPORTED;
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(d.ptr), dims, strides, box,
                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
