@@ -386,6 +386,37 @@ def test_predecoded_tile_shape_by_table(amd, orc, luts, kind, M, wide, zeros):
     check(orc, kind, M, A, B, False, False, got, what=f"tile shape {kind} M={M}")
 
 
+def test_raw_or_planes_by_launch_size(amd, orc, luts):
+    """Dense operands the copy engine can read take planes only for large
+    launches whose elements many tiles reuse: a batched 512 x 512 x 64 GEMM
+    (2^30 MACs, 0.031 plane bytes per MAC) takes planes, one MLP layer's
+    256 x 1000 x 784 GEMM (0.039) raw tiles.  Both match the oracle (the large
+    one on sampled batches)."""
+    import torch
+    rng = np.random.default_rng(23)
+    lut = luts("mitchell", 7)
+    batch, m, n, k = 64, 512, 512, 64
+    A = rnd(rng, (batch, m, k))
+    B = rnd(rng, (batch, n, k))
+    nb = amd.amsim_gemm_workspace_size("N", "T", m, n, k, batch, lut)
+    C = torch.empty((batch, m, n), device="cuda")
+    amd.amsim_gemm_strided_batched("N", "T", m, n, k, 1.0, to_dev(A), k, m * k, to_dev(B), k, n * k, 0.0, C, n,
+                                   m * n, batch, lut, ws=amd.workspace(nb))
+    torch.cuda.synchronize()
+    bits = amd.amsim_last_path()
+    assert bits & amd.AMSIM_PATH_PLANES and not bits & amd.AMSIM_PATH_RAW_TILES, bits
+    got = C.cpu().numpy()
+    for b in (0, 37, 63):
+        ref, sa = orc.gemm("mitchell", 7, A[b], B[b], transB=True)
+        assert_close(got[b], ref, sa, f"batch {b}")
+    m, n, k = 256, 1000, 784
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    got = gpu_gemm(amd, lut, A, B, False, False)
+    bits = amd.amsim_last_path()
+    assert bits & amd.AMSIM_PATH_RAW_TILES and not bits & amd.AMSIM_PATH_PLANES, bits
+    check(orc, "mitchell", 7, A, B, False, False, got, what="mlp layer")
+
+
 @pytest.mark.parametrize("zeros_in", ["A", "B", "both"])
 def test_folded_scale_bit_identical_to_general_form(amd, orc, luts, zeros_in):
     """Stages whose uniform operands lie in [2^-63, 2^64) and whose lane
