@@ -364,13 +364,13 @@ __device__ __forceinline__ float fmt_product(float v, float s, const ExpFormat &
     return fabsf(p) >= f.lim ? __uint_as_float((__float_as_uint(p) & 0x80000000u) | 0x7F800000u) : p;
 }
 
-// An operand whose magnitude is below 2^-63 (zero and denormal included).
-// Stages whose operands are all in [2^-63, 2^64) have every e0 = eA + eB - 127
-// in [1, 253]: no product meets Algorithm 2's zero test or its overflow.  A
-// lane operand may also be zero (or denormal): its scale is a signed zero and
-// the folded product v' * 0 is the signed zero Algorithm 2 gives.
-__device__ __forceinline__ bool is_small(float v) { return ((__float_as_uint(v) >> 23) & 0xFFu) < 64u; }
-// ... and not zero or denormal (biased exponent 1 .. 63).
+// A nonzero operand whose magnitude is below 2^-63 (biased exponent 1 .. 63;
+// zero and denormal excluded).  Stages whose operands are all zero or in
+// [2^-63, 2^64) have every e0 = eA + eB - 127 of a nonzero pair in [1, 253]:
+// no product meets Algorithm 2's zero test or its overflow.  A zero (or
+// denormal) lane operand has a signed zero scale, and a zero uniform operand
+// takes the table's zero row: both folded products are the signed zero
+// Algorithm 2 gives.
 __device__ __forceinline__ bool is_small_nonzero(float v) { return ((__float_as_uint(v) >> 23) & 0xFFu) - 1u < 63u; }
 
 // v * sa for a uniform operand with scale bits ub = sign | eA << 23, straight
