@@ -288,9 +288,10 @@ int amsim_gemm_strided_batched(char transA, char transB, int m, int n, int k, fl
 /*
  * Bytes of scratch with which the GEMM calls above run their fastest plan:
  * the split-K (stream-K) partial sums, when the problem needs them, plus the
- * operands decoded once into LUT-offset and scale planes (8 bytes per operand
- * element, per batch unless the batch stride is 0).  Less scratch selects a
- * plan that decodes operands inside the GEMM; none selects one without
+ * operands decoded once into LUT-offset and scale planes, when the plan uses
+ * them (4 bytes per operand element for tables that fit shared memory, 8 for
+ * larger ones; per batch unless the batch stride is 0).  Less scratch selects
+ * a plan that decodes operands inside the GEMM; none selects one without
  * split-K.  All plans give results within the contraction tolerance; a
  * given scratch size always gives the same plan.
  */
