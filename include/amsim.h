@@ -437,10 +437,11 @@ int amsim_conv2d_bwd_filter(const amsim_conv_desc *desc, const float *x, const f
 
 /*
  * which: 0 forward, 1 bwd_data, 2 bwd_filter.  Bytes of scratch for the
- * fastest plan: split-K partial sums plus, for unit strides, the operands
- * decoded into LUT-offset and scale planes laid out for tensor copies (for the
- * forward and data-gradient passes one copy of the activation per filter
- * column).  Less scratch selects the gathering kernel.
+ * fastest plan: the split-K (stream-K) partial sums (unit-stride passes copy
+ * their operands as tensor boxes and others gather them inside the GEMM, so
+ * no operand planes are kept; a 1x1 filter at stride 1 without padding is a
+ * plain GEMM and may also take planes, as amsim_gemm_workspace_size says).
+ * Less scratch selects a plan without split-K.
  */
 size_t amsim_conv2d_workspace_size(const amsim_conv_desc *desc, int which, amsim_lut_t lut);
 
