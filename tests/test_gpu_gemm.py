@@ -300,6 +300,34 @@ def test_special_operands_each_path(amd, orc, luts, path):
         check(orc, kind, 7, A, B, False, False, got, what=f"specials {kind} path={path}")
 
 
+@pytest.mark.parametrize("kind,M,small", [("mitchell", 7, False), ("exact", 7, False), ("mitchell", 8, False),
+                                          ("mitchell", 9, False), ("mitchell", 7, True)])
+def test_special_operands_on_planes(amd, orc, luts, kind, M, small):
+    """Zeros, denormals, infinities, NaNs and |x| >= 2^64 through the
+    predecoded planes: packed operand words (M = 7 wide tiles, M = 8 narrow
+    tiles) and two planes (M = 9, table in global memory).  Operands too large
+    and unaligned for plain loads (k = 1301) force the planes.  small: nonzero
+    magnitudes below 2^-63 instead of the huge ones (the zero test of
+    Algorithm 2, no folded form)."""
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    rng = np.random.default_rng(40 + M)
+    m, n, k = 300, 260, 1301
+    a, b = wl.special_values_mix(m * k + k * n, seed=41)
+    A = a[:m * k].reshape(m, k).copy()
+    B = b[m * k:m * k + k * n].reshape(k, n).copy()
+    A[:, :] = np.where(rng.random(A.shape) < 0.97, rng.standard_normal(A.shape), A).astype(np.float32)
+    B[:, :] = np.where(rng.random(B.shape) < 0.97, rng.standard_normal(B.shape), B).astype(np.float32)
+    if small:
+        for X in (A, B):
+            big = ~np.isfinite(X) | (np.abs(X) >= 2.0 ** 64)
+            X[big] = np.float32(3e-20)
+    lut = luts(kind, M)
+    got = gpu_gemm(amd, lut, A, B, False, False)
+    bits = amd.amsim_last_path()
+    assert bits & amd.AMSIM_PATH_PLANES, bits
+    check(orc, kind, M, A, B, False, False, got, what=f"planes specials {kind} M={M} small={small}")
+
+
 @pytest.mark.parametrize("k", [150, 152])
 @pytest.mark.parametrize("path", ["planes", "none"])
 def test_batched_broadcast_operand(amd, orc, luts, path, k):
