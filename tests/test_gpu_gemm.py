@@ -414,6 +414,19 @@ def test_predecoded_tile_shape_by_table(amd, orc, luts, kind, M, wide, zeros):
     check(orc, kind, M, A, B, False, False, got, what=f"tile shape {kind} M={M}")
 
 
+def test_workspace_counts_plane_bytes_per_element(amd, luts):
+    """The scratch of a plane-path GEMM holds one 4-byte packed word per
+    operand element when the table fits shared memory (M = 7) and an offset
+    and a scale, 8 bytes, when it is read from global memory (M = 9); both
+    use the wide tiles' stream-K slots, so the sizes differ by exactly the
+    second plane: 4 x (m k + k n) bytes."""
+    m = n = k = 4096
+    w7 = amd.amsim_gemm_workspace_size("N", "N", m, n, k, 1, luts("mitchell", 7))
+    w9 = amd.amsim_gemm_workspace_size("N", "N", m, n, k, 1, luts("mitchell", 9))
+    assert w9 - w7 == 4 * (m * k + k * n), (w7, w9)
+    assert w7 > 4 * (m * k + k * n), w7
+
+
 def test_raw_or_planes_by_launch_size(amd, orc, luts):
     """Dense operands the copy engine can read take planes only for large
     launches whose elements many tiles reuse: a batched 512 x 512 x 64 GEMM
