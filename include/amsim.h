@@ -381,8 +381,10 @@ size_t amsim_gemm_phased_workspace_size(int count, const amsim_gemm_problem *pro
  * with the device current; make that first call before any stream capture.
  * All calls on a device share the array and leave their partial sums in it;
  * nothing needs clearing between calls, but calls that may overlap on the GPU
- * (unordered streams) race on it and must not be made.  A problem whose plan
- * needs more scratch than the array holds returns AMSIM_EUNSUPPORTED.
+ * (unordered streams) race on it and must not be made.  The array holds the
+ * stream-K partial sums of one wave on up to 159 SMs; on a larger device the
+ * plan amsim_gemm picks for a workspace of that size is used instead (a
+ * multi-wave problem then runs without stream-K).  Errors as amsim_gemm.
  */
 #define AMSIM_NOALLOC_SCRATCH_BYTES ((size_t)20 << 20)
 int amsim_gemm_noalloc(char transA, char transB, int m, int n, int k, float alpha,

@@ -8,8 +8,10 @@ tolerance the other tests use (1e-5 * sum_k |AMSim product| per element).
 The first shape splits its reduction across CTAs (stream-K), so its partial
 sums really go through the library's array; the test asserts that path.  The
 array holds one stream-K slot pair per SM for up to 159 SMs, so on this GPU no
-problem's plan exceeds it and the over-size rejection (AMSIM_EUNSUPPORTED) is
-never reached; a large multi-wave problem is run to show that it is not."""
+problem's plan exceeds it (a large multi-wave problem is run to show that); on
+a larger device the call takes amsim_gemm's plan for a workspace of the array's
+size, and the last test runs that fallback with a workspace too small for the
+stream-K slots."""
 import ctypes
 
 import numpy as np
@@ -97,3 +99,31 @@ def test_noalloc_large_multi_wave_problem_fits_the_array(amd, orc, luts):
     rows = np.array([0, 1000, m - 1])
     ref, sa = orc.gemm("mitchell", 7, A, B, rows=rows)
     assert_close(out.cpu().numpy()[rows], ref, sa, "noalloc 2048x2048x256")
+
+
+def test_workspace_too_small_for_streamk_drops_it(amd, orc, luts):
+    """The fallback amsim_gemm_noalloc relies on when its array is smaller than
+    a plan's stream-K slots: amsim_gemm, given less scratch than the stream-K
+    plan asks for, runs the GEMM without stream-K and gets the same results
+    within the contraction tolerance."""
+    import torch
+    lut = luts("mitchell", 7)
+    m, n, k = 300, 500, 2000
+    rng = np.random.default_rng(78)
+    A = rng.standard_normal((m, k)).astype(np.float32)
+    B = rng.standard_normal((k, n)).astype(np.float32)
+    dA, dB = to_dev(A), to_dev(B)
+    nb = amd.amsim_gemm_workspace_size("N", "N", m, n, k, 1, lut)
+    assert nb > 1024
+    full = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    amd.amsim_gemm("N", "N", m, n, k, 1.0, dA, k, dB, n, 0.0, full, n, lut, ws=amd.workspace(nb))
+    assert amd.amsim_last_path() & amd.AMSIM_PATH_STREAMK
+    small = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    amd.amsim_gemm("N", "N", m, n, k, 1.0, dA, k, dB, n, 0.0, small, n, lut, ws=amd.workspace(1024))
+    assert not amd.amsim_last_path() & amd.AMSIM_PATH_STREAMK, amd.amsim_last_path()
+    torch.cuda.synchronize()
+    got, want = small.cpu().numpy(), full.cpu().numpy()
+    assert_close(got, want, 2.0 * _scale_bound(A, B), "no stream-K vs stream-K")
+    rows = np.array([0, 150, m - 1])
+    ref, sa = orc.gemm("mitchell", 7, A, B, rows=rows)
+    assert_close(got[rows], ref, sa, "no stream-K vs oracle")
