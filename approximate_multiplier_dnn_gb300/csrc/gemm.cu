@@ -2,6 +2,7 @@
 // operand roles), the deterministic split-K reduction, and the GEMM ABI
 // (ApproxTrain Sec. VI-D GEMM kernel; Sec. VI-C AMDENSE forward and gradients).
 #include <algorithm>
+#include <cmath>
 #include <vector>
 #include <atomic>
 #include <mutex>
@@ -82,6 +83,8 @@ Plan make_plan(const Problem *p, int n, int sms, size_t ws_avail, const kern::Ti
     pl.ws_bytes = pl.streamk ? pl.sk_bytes : 0;
     return pl;
 }
+
+bool streamk_bounds_by_cost(const Problem *p, int n, const Plan &pl, kern::KParams &kp);
 
 int launch_ws(int width, const kern::KParams &kp, bool gl, dim3 grid, size_t smem, cudaStream_t st)
 {
@@ -662,6 +665,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             tp.table_bytes = (raw_gl || alu) ? 0 : (int)gemm_table_bytes(lut);
             tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
             tp.fused = pl.streamk ? 1 : 0;
+            streamk_bounds_by_cost(p, n, pl, tp);
             const dim3 grid((unsigned)blocks);
             int rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
             if (rc == kern::AMSIM_ENOTCOOP) {
@@ -848,14 +852,72 @@ bool phased_ok(const Problem *p, int n, int nphase, const Plan &pl, amsim_lut_t 
 // faster -- measured on GB300 from per-CTA timelines of phased launches, a
 // stage with a fraction f of its warps busy takes about 0.47 + 0.53 f of a
 // full stage (0.6 at f = 1/4) -- so shares are cut by this cost, not by count.
-double stage_cost(const Problem &p, int ut, int lt)
+// A tail tile (all real lane columns in the first column block) runs in the
+// tail layout: each warp does half a warp's lookups, and a stage takes about
+// 0.6 to 0.68 of a full one, measured on GB300 (0.60 for 64 x 64 and
+// 64 x 128 GEMM tiles against 64 x 256 ones; from the 3x3 filter gradient's
+// pass times, 0.61 with the 16-bit exact table and 0.68 with the 8-bit
+// Mitchell one).  A share that overestimates the cost loses less than one
+// that underestimates it, so the model takes 0.67.  (Phased launches keep
+// the regular layout on tail tiles: tail_layout false.)
+double stage_cost(const Problem &p, int ut, int lt, bool tail_layout)
 {
     constexpr int WUn = BU / kern::TM, WLn = BL / (32 * kern::TN);
+    if (tail_layout && kern::tail_tile(lt * BL, p.L.rows)) return 0.67;
     int busy = 0;
     for (int wu = 0; wu < WUn; ++wu)
         for (int wl = 0; wl < WLn; ++wl)
             busy += (ut * BU + wu * kern::TM < p.U.rows && lt * BL + wl * 32 * kern::TN < p.L.rows) ? 1 : 0;
     return 0.47 + 0.53 * busy / (WUn * WLn);
+}
+
+// Stream-K shares of an ordinary raw-tile launch cut by stage cost: CTA c
+// starts where the running cost of the launch's tiles (in iteration order)
+// reaches c / G of the total, rounded to a stage, every share at least one
+// stage.  False (keep the even split) when every stage costs the same, or the
+// table does not hold the CTAs or the iterations.
+bool streamk_bounds_by_cost(const Problem *p, int n, const Plan &pl, kern::KParams &kp)
+{
+    kp.sk_n = 0;
+    const int G = pl.ctas;
+    if (!pl.streamk || G > kern::kMaxPhasedCtas || pl.iters >= 0x7FFFFFFFLL || pl.iters < G) return false;
+    struct Run { long long it0; int kt; double w; };
+    std::vector<Run> runs;                  // tiles in iteration order
+    double C = 0.0;
+    bool uneven = false;
+    for (int i = 0; i < n; ++i) {
+        if (pl.tiles[i] == 0) continue;
+        long long it = pl.iter0[i];
+        for (int b = 0; b < p[i].batch; ++b)
+            for (int ut = 0; ut < pl.tiles_u[i]; ++ut)
+                for (int lt = 0; lt < pl.tiles_l[i]; ++lt) {
+                    const double w = stage_cost(p[i], ut, lt, true);
+                    uneven |= w != 1.0;
+                    runs.push_back({it, pl.kt[i], w});
+                    C += w * pl.kt[i];
+                    it += pl.kt[i];
+                }
+    }
+    if (!uneven) return false;
+    int *bound = kp.sk_bound;
+    bound[0] = 0;
+    size_t r = 0;
+    double before = 0.0;                    // cost of the runs before run r
+    for (int c = 1; c < G; ++c) {
+        const double target = C * c / G;
+        while (r + 1 < runs.size() && before + runs[r].w * runs[r].kt <= target) {
+            before += runs[r].w * runs[r].kt;
+            ++r;
+        }
+        const long long s = std::llround((target - before) / runs[r].w);
+        long long it = runs[r].it0 + std::min<long long>(std::max<long long>(s, 0), runs[r].kt);
+        it = std::max<long long>(it, bound[c - 1] + 1);             // no empty share
+        it = std::min<long long>(it, pl.iters - (G - c));           // room for the shares after it
+        bound[c] = (int)it;
+    }
+    bound[G] = (int)pl.iters;
+    kp.sk_n = G;
+    return true;
 }
 
 // Share boundaries of every phase.  CTAs 0 .. c-1 together get, through
@@ -882,7 +944,7 @@ void phased_bounds_by_cost(const Problem *p, const Plan &pl, const int *first, i
             for (int b = 0; b < p[i].batch; ++b)
                 for (int ut = 0; ut < pl.tiles_u[i]; ++ut)
                     for (int lt = 0; lt < pl.tiles_l[i]; ++lt) {
-                        const double w = stage_cost(p[i], ut, lt);
+                        const double w = stage_cost(p[i], ut, lt, false);
                         runs.push_back({pl.kt[i], w});
                         C += w * pl.kt[i];
                         W += pl.kt[i];

@@ -135,6 +135,11 @@ struct KParams {
     int nphase;
     long long ph_iter0[kMaxPhases + 1];
     int ph_after[kMaxPhases];
+    // Stream-K shares cut by stage cost (raw-tile kernel, ordinary launches):
+    // when sk_n > 0, CTA c takes iterations [sk_bound[c], sk_bound[c + 1]),
+    // strictly increasing; else the even split W * c / G.
+    int sk_n;
+    int sk_bound[kMaxPhasedCtas + 1];
     int cv_ch, cv_S, cv_tiles_img, cv_rows_tile, cv_ybase, cv_ystep, cv_xbase, cv_xstep, cv_N, cv_P, cv_Q, cv_rows;
     // (1, E, M) format with E < 8 (fmt.on): operands are cast and every stage
     // takes the rounding product path with the format's rescale and overflow
@@ -178,6 +183,18 @@ static_assert(WU * WL * 32 == NT, "warp layout");
 // bytes across the warp (four wavefronts, no bank conflicts) whatever TN is.
 constexpr int kColGroup = 128;
 __host__ __device__ constexpr int col_of(int t) { return (t >> 2) * kColGroup + (t & 3); }
+// Tail layout of the two-column-block shape: a tile whose real lane columns
+// all lie in its first column block (at most 32 * TN of them) is computed by
+// all the warps as WU * WL row blocks of TM / 2 rows over that block, instead
+// of leaving the warps of the second block idle -- which, as they are every
+// other warp, would also leave half of the SM's schedulers idle.  Each
+// output's products are summed in the same order either way.
+constexpr bool kTailLayout = WL == 2 && (TM / 2) * WU * WL == BU && TM % 8 == 0;
+constexpr int kTailRows = TM / 2;
+__host__ __device__ constexpr bool tail_tile(int l_tile0, int l_rows)
+{
+    return kTailLayout && l_tile0 + 32 * TN >= l_rows;
+}
 
 // Shared-memory layout (bytes) after the LUT region.
 constexpr int kUdecBytes = 2 * BK * UST * 4;   // one array (offsets or scales), 2 stages
@@ -580,7 +597,7 @@ __device__ __forceinline__ float accv(const float2 (&acc)[TM / 2][TN], int i, in
 // and Us / Ls are not read.  One 128-bit load brings four operands' offsets
 // and scales: half the shared-memory wavefronts of two planes.
 template <int W, bool GL, bool SLOW, int USTR = UST, int LSTR = LST, bool FMT = false, bool FOLD = false,
-          bool PU = false, bool PL = false>
+          bool PU = false, bool PL = false, int ROWS = TM>
 __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                               const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
                                               const float *__restrict__ Ls, const uint8_t *lut, int urow, int lcol,
@@ -610,7 +627,7 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
             sb[4 * t4 + 3] = make_float2(sc.w, sc.w);
         }
 #pragma unroll
-        for (int ig = 0; ig < TM / 4; ++ig) {
+        for (int ig = 0; ig < ROWS / 4; ++ig) {
             uint4 uo;
             float4 us;
             if constexpr (PU) {
@@ -682,7 +699,9 @@ __device__ __forceinline__ float4 acc4(const float2 (&acc)[TM / 2][TN], int i, i
 }
 
 // Write a finished tile: C = alpha*acc + beta*C with 128-bit stores when the
-// output is contiguous along L (or along U, for transposed outputs).
+// output is contiguous along L (or along U, for transposed outputs).  ROWS:
+// the rows this warp holds (TM, or kTailRows in the tail layout).
+template <int ROWS = TM>
 __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&acc)[TM / 2][TN], int b, int u0,
                                            int l0)
 {
@@ -694,7 +713,7 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
     const bool vec_u = aligned && q.c_su == 1 && (q.c_sl & 3) == 0;
     if (vec_l && l0 + col_of(TN - 1) < nL) {
 #pragma unroll
-        for (int i = 0; i < TM; ++i) {
+        for (int i = 0; i < ROWS; ++i) {
             const int u = u0 + i;
             if (u >= nU) break;
 #pragma unroll
@@ -710,14 +729,14 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
                 *dst = r;
             }
         }
-    } else if (vec_u && u0 + TM <= nU) {
+    } else if (vec_u && u0 + ROWS <= nU) {
 #pragma unroll
         for (int t = 0; t < TN; ++t) {
             const int l = l0 + col_of(t);
             if (l >= nL) break;
             float *col = C + (long long)l * q.c_sl + u0;
 #pragma unroll
-            for (int i4 = 0; i4 < TM / 4; ++i4) {
+            for (int i4 = 0; i4 < ROWS / 4; ++i4) {
                 float4 r = make_float4(alpha * accv(acc, 4 * i4, t), alpha * accv(acc, 4 * i4 + 1, t),
                                        alpha * accv(acc, 4 * i4 + 2, t), alpha * accv(acc, 4 * i4 + 3, t));
                 float4 *dst = reinterpret_cast<float4 *>(col + 4 * i4);
@@ -731,7 +750,7 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < TM; ++i) {
+        for (int i = 0; i < ROWS; ++i) {
             const int u = u0 + i;
             if (u >= nU) break;
 #pragma unroll
@@ -809,7 +828,11 @@ __device__ __forceinline__ void run_stages(const KParams &p, const ProbParams &q
     }
 }
 
-__device__ __forceinline__ long long sk_begin(long long W, int G, int c) { return W * c / G; }
+// First launch iteration of stream-K CTA c (c = ctas: the launch's end).
+__device__ __forceinline__ long long sk_begin(const KParams &p, int c)
+{
+    return p.sk_n > 0 ? (long long)p.sk_bound[c] : p.iters * c / p.ctas;
+}
 
 __device__ __forceinline__ int n_phases(const KParams &p) { return p.nphase > 1 ? p.nphase : 1; }
 
@@ -840,8 +863,8 @@ __global__ void __launch_bounds__(NT, 1) lutgemm_kernel(const __grid_constant__ 
 
     long long it, it_end;
     if (p.streamk) {
-        it = sk_begin(p.iters, p.ctas, blockIdx.x);
-        it_end = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
+        it = sk_begin(p, blockIdx.x);
+        it_end = sk_begin(p, blockIdx.x + 1);
     } else {
         // data parallel: CTA x runs the x-th tile of the launch whole
         long long t = blockIdx.x;
@@ -925,7 +948,7 @@ __global__ void __launch_bounds__(kThreads) streamk_fixup(const __grid_constant_
     if (c >= p.ctas) return;
     const long long W = p.iters;
     const int G = p.ctas;
-    const long long bpos = sk_begin(W, G, c);
+    const long long bpos = sk_begin(p, c);
     if (bpos >= W) return;
     int pi = 0;
     while (pi + 1 < p.nprob && bpos >= p.pr[pi + 1].iter0) ++pi;
@@ -935,17 +958,17 @@ __global__ void __launch_bounds__(kThreads) streamk_fixup(const __grid_constant_
     const long long tile = local / S;
     const long long tstart = q.iter0 + tile * S, tend = tstart + S;
     if (bpos == tstart) return;                       // boundary on a tile edge: nothing cut
-    if (sk_begin(W, G, c - 1) > tstart) return;       // an earlier boundary in this tile owns it
+    if (sk_begin(p, c - 1) > tstart) return;          // an earlier boundary in this tile owns it
     const int c_lo = c - 1;
     int c_hi = c;
-    while (c_hi + 1 < G && sk_begin(W, G, c_hi + 1) < tend) ++c_hi;
+    while (c_hi + 1 < G && sk_begin(p, c_hi + 1) < tend) ++c_hi;
 
     // slot offsets of the contributing CTAs, in CTA order (G <= kMaxFixupParts)
     __shared__ long long slot_off[kMaxFixupParts];
     const int nparts = min(c_hi - c_lo + 1, kMaxFixupParts);
     for (int i = threadIdx.x; i < nparts; i += kThreads) {
         const int cc = c_lo + i;
-        const bool first_is_this = sk_begin(W, G, cc) >= tstart;
+        const bool first_is_this = sk_begin(p, cc) >= tstart;
         slot_off[i] = ((long long)cc * 2 + (first_is_this ? 0 : 1)) * (BU * BL);
     }
     __syncthreads();

@@ -351,7 +351,7 @@ __device__ __forceinline__ float trunc_scale(uint32_t t)
 //    is exact and normal (exponent sum >= 1), as the table path's v * s is.
 //  - Other stages rebuild the table path's (v, s) and round the product
 //    before adding it, as compute_stage's slow stages do.
-template <int KIND, bool SLOW>
+template <int KIND, bool SLOW, int ROWS = TM>
 __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                                   const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
                                                   const float *__restrict__ Ls, int urow, int lcol)
@@ -383,7 +383,7 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
             }
         }
 #pragma unroll
-        for (int ig = 0; ig < TM / 4; ++ig) {
+        for (int ig = 0; ig < ROWS / 4; ++ig) {
             const uint4 uo = *reinterpret_cast<const uint4 *>(Uo + kk * BU + urow + 4 * ig);
             const uint32_t uov[4] = {uo.x, uo.y, uo.z, uo.w};
             float2 sa[2];
@@ -425,27 +425,42 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
 
 // A decoded stage of the raw-tile kernel: table entries (W = 8, 16, 32; packed
 // operand words with the table in shared memory) or closed forms (W = 1
-// Mitchell, 2 exact).
-template <int W, bool GL, bool SLOW, bool FOLD = false>
+// Mitchell, 2 exact), over this warp's ROWS uniform rows.
+template <int W, bool GL, bool SLOW, bool FOLD = false, int ROWS = TM>
 __device__ __forceinline__ void raw_stage(float2 (&acc)[TM / 2][TN], const uint32_t *Uo, const float *Us,
                                           const uint32_t *Lo, const float *Ls, const uint8_t *lut, int urow,
                                           int lcol)
 {
-    if constexpr (W <= 2) compute_stage_alu<W, SLOW>(acc, Uo, Us, Lo, Ls, urow, lcol);
-    else compute_stage<W, GL, SLOW, BU, BL, false, FOLD, !GL, !GL>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    if constexpr (W <= 2) compute_stage_alu<W, SLOW, ROWS>(acc, Uo, Us, Lo, Ls, urow, lcol);
+    else compute_stage<W, GL, SLOW, BU, BL, false, FOLD, !GL, !GL, ROWS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
 }
 
 // One stage of a consumer: the rounding slow products when a decoder flagged
 // bit 0, the folded-scale form when no decoder flagged bit 1 (tables in
 // shared memory only), else the general form.
-template <int W, bool GL>
+template <int W, bool GL, int ROWS = TM>
 __device__ __forceinline__ void raw_stage_by_flags(int fl, float2 (&acc)[TM / 2][TN], const uint32_t *Uo,
                                                    const float *Us, const uint32_t *Lo, const float *Ls,
                                                    const uint8_t *lut, int urow, int lcol)
 {
-    if (fl & 1) raw_stage<W, GL, true>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-    else if (W > 2 && !GL && !(fl & 2)) raw_stage<W, GL, false, (W > 2 && !GL)>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-    else raw_stage<W, GL, false>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    if (fl & 1) raw_stage<W, GL, true, false, ROWS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    else if (W > 2 && !GL && !(fl & 2))
+        raw_stage<W, GL, false, (W > 2 && !GL), ROWS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    else raw_stage<W, GL, false, false, ROWS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+}
+
+// This warp's rows and lane columns of a tile in the regular layout (ROWS =
+// TM) or the tail layout (ROWS = kTailRows).
+template <int ROWS>
+__device__ __forceinline__ void warp_span(int warp, int lane, int &urow, int &lcol)
+{
+    if constexpr (ROWS == TM) {
+        urow = (warp / WL) * TM;
+        lcol = (warp % WL) * 32 * TN + lane * 4;
+    } else {
+        urow = warp * ROWS;
+        lcol = lane * 4;
+    }
 }
 
 // The producer warpgroup: thread 0 also issues the copies, kRawRing - 1 stages
@@ -547,42 +562,56 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
     }
 }
 
+// Stages [s0, s1) of one segment of a tile for one consumer warp in the
+// layout ROWS (TM, or kTailRows for a tail tile); `g` counts decoded stages.
+template <int W, bool GL, int ROWS>
+__device__ __forceinline__ void raw_segment(const KParams &p, const ProbParams &q, const uint8_t *lut,
+                                            const RawSmem &sm, int b, int u_tile0, int l_tile0, int s0, int s1,
+                                            bool first, uint32_t &g, bool &aborted, CutTile &cut0, CutTile &cut1,
+                                            int &ncut)
+{
+    const int lane = threadIdx.x & 31;
+    int urow, lcol;
+    warp_span<ROWS>(uniform_warp(), lane, urow, lcol);
+    float2 acc[TM / 2][TN];
+#pragma unroll
+    for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+    const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + lcol - 4 * lane >= q.L.rows;
+    for (int kt = s0; kt < s1; ++kt, ++g) {
+        const int ds = g % kRawDec;
+        mbar_wait(&sm.full[ds], (g / kRawDec) & 1, aborted);
+        if (!idle) {
+            const uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
+            const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
+            const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
+            const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
+            const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
+            int fl = 0;
+#pragma unroll
+            for (int w = 0; w < kRawDecoders / 32; ++w) fl |= sm.flags[ds * (kRawDecoders / 32) + w];
+            raw_stage_by_flags<W, GL, ROWS>(fl, acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+        }
+        mbar_arrive(&sm.empty[ds]);
+    }
+    segment_epilogue<ROWS>(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, cut0, cut1, ncut);
+}
+
 template <int W, bool GL>
 __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lut, const RawSmem &sm, int red_bytes)
 {
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = uniform_warp();
-    const int wu = warp / WL, wl = warp % WL;
-    const int urow = wu * TM;
-    const int lcol = wl * 32 * TN + lane * 4;
     uint32_t g = 0;
     bool aborted = false;
     CutTile cut0, cut1;
     int ncut = 0;
     for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
-        float2 acc[TM / 2][TN];
-#pragma unroll
-        for (int i = 0; i < TM / 2; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-        const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + wl * 32 * TN >= q.L.rows;
-        for (int kt = s0; kt < s1; ++kt, ++g) {
-            const int ds = g % kRawDec;
-            mbar_wait(&sm.full[ds], (g / kRawDec) & 1, aborted);
-            if (!idle) {
-                const uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
-                const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
-                const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
-                const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
-                const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
-                int fl = 0;
-#pragma unroll
-                for (int w = 0; w < kRawDecoders / 32; ++w) fl |= sm.flags[ds * (kRawDecoders / 32) + w];
-                raw_stage_by_flags<W, GL>(fl, acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-            }
-            mbar_arrive(&sm.empty[ds]);
-        }
-        segment_epilogue(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, cut0, cut1, ncut);
+        if (tail_tile(l_tile0, q.L.rows))
+            raw_segment<W, GL, kTailRows>(p, q, lut, sm, b, u_tile0, l_tile0, s0, s1, first, g, aborted, cut0,
+                                          cut1, ncut);
+        else
+            raw_segment<W, GL, TM>(p, q, lut, sm, b, u_tile0, l_tile0, s0, s1, first, g, aborted, cut0, cut1,
+                                   ncut);
     });
     // the rings (decoded, then raw, contiguous) hold the reduction's copies
     finish_cut_tiles(p, cut0, cut1, ncut, reinterpret_cast<float *>(sm.dec), red_bytes, sm.raw_full + 2 * kRawRing +
@@ -817,96 +846,113 @@ __device__ __forceinline__ void raw_producer_phased(const KParams &p, const TmaM
 // adds every part's partial sum in CTA order -- the order of their stages --
 // and stores alpha * sum + beta * C.  Results are therefore the same from run
 // to run.
+// One segment of a phased launch for one consumer warp in the layout ROWS
+// (TM, or kTailRows for a tail tile): its stages, then the tile's store, or
+// this part's partial sum and, for the last part to arrive, the sum of all
+// parts in CTA order.
+template <int W, int ROWS>
+__device__ __forceinline__ void phased_segment(const KParams &p, const PhaseTable &pt, const ProbParams &q,
+                                               const uint8_t *lut, const RawSmem &sm, long long total_tiles, int ph,
+                                               int b, int u_tile0, int l_tile0, int s0, int s1, bool first,
+                                               uint32_t &g, bool &aborted)
+{
+    volatile int *last_flag = sm.flags + kRawDec * (kRawDecoders / 32);   // the ticket's verdict
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    int urow, lcol;
+    warp_span<ROWS>(uniform_warp(), lane, urow, lcol);
+    float2 acc[TM / 2][TN];
+#pragma unroll
+    for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+    const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + lcol - 4 * lane >= q.L.rows;
+    for (int kt = s0; kt < s1; ++kt, ++g) {
+        const int ds = g % kRawDec;
+        mbar_wait(&sm.full[ds], (g / kRawDec) & 1, aborted);
+        if (!idle) {
+            const uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
+            const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
+            const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
+            const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
+            const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
+            int fl = 0;
+#pragma unroll
+            for (int w = 0; w < kRawDecoders / 32; ++w) fl |= sm.flags[ds * (kRawDecoders / 32) + w];
+            raw_stage_by_flags<W, false, ROWS>(fl, acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+        }
+        mbar_arrive(&sm.empty[ds]);
+    }
+    if (s0 == 0 && s1 == q.kt_total) {
+        store_tile<ROWS>(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
+        return;
+    }
+    const long long lt = (long long)b * q.tiles_u * q.tiles_l + (long long)(u_tile0 / BU) * q.tiles_l +
+                         l_tile0 / BL;
+    float *mine = phased_slot(p, total_tiles, ph, blockIdx.x, first ? 0 : 1);
+    if (!idle) {
+#pragma unroll
+        for (int i = 0; i < ROWS; ++i)
+#pragma unroll
+            for (int t4 = 0; t4 < TN / 4; ++t4)
+                __stcg(reinterpret_cast<float4 *>(mine + (urow + i) * BL + lcol + kColGroup * t4), acc4(acc, i, 4 * t4));
+    }
+    // every consumer's slot writes precede the barrier; thread 0's
+    // fence and ticket update then publish them (cumulative release)
+    consumer_bar();
+    if (tid == 0) {
+        __threadfence();
+        const bool last = last_arrival(p, q.tile0 + lt, s1 - s0, q.kt_total);
+        __threadfence();
+        *last_flag = last ? 1 : 0;
+    }
+    consumer_bar();
+    const bool last = *last_flag != 0;
+    consumer_bar();         // everyone has read the ticket's verdict
+    if (!last || idle) return;
+    const long long tbeg = q.iter0 + lt * q.kt_total, tend = tbeg + q.kt_total;
+    const int c_lo = ph_owner(p, pt, ph, tbeg), c_hi = ph_owner(p, pt, ph, tend - 1);
+    float2 sum[TM / 2][TN];
+#pragma unroll
+    for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) sum[i][j] = make_float2(0.0f, 0.0f);
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const long long cb = ph_begin(p, pt, ph, c);
+        if (cb == ph_begin(p, pt, ph, c + 1)) continue;          // empty share
+        const float *part = phased_slot(p, total_tiles, ph, c, cb >= tbeg ? 0 : 1);
+#pragma unroll
+        for (int i = 0; i < ROWS; ++i)
+#pragma unroll
+            for (int t4 = 0; t4 < TN / 4; ++t4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(part + (urow + i) * BL + lcol + kColGroup * t4));
+                float2 &lo = sum[i >> 1][4 * t4], &l1 = sum[i >> 1][4 * t4 + 1];
+                float2 &l2 = sum[i >> 1][4 * t4 + 2], &l3 = sum[i >> 1][4 * t4 + 3];
+                if (i & 1) { lo.y += v.x; l1.y += v.y; l2.y += v.z; l3.y += v.w; }
+                else { lo.x += v.x; l1.x += v.y; l2.x += v.z; l3.x += v.w; }
+            }
+    }
+    store_tile<ROWS>(q, sum, b, u_tile0 + urow, l_tile0 + lcol);
+}
+
 template <int W>
 __device__ __forceinline__ void raw_consumer_phased(const KParams &p, const PhaseTable &pt, const uint8_t *lut,
                                                    const RawSmem &sm)
 {
-    volatile int *last_flag = sm.flags + kRawDec * (kRawDecoders / 32);   // the ticket's verdict
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = uniform_warp();
-    const int wu = warp / WL, wl = warp % WL;
-    const int urow = wu * TM;
-    const int lcol = wl * 32 * TN + lane * 4;
     const long long total_tiles = p.pr[p.nprob - 1].tile0 + p.pr[p.nprob - 1].tiles;
     uint32_t g = 0;
     bool aborted = false;
     const int nph = n_phases(p);
     for (int ph = 0; ph < nph; ++ph) {
         const long long it0 = ph_begin(p, pt, ph, blockIdx.x), it1 = ph_begin(p, pt, ph, blockIdx.x + 1);
+        // (phased launches keep the regular layout on tail tiles: with a
+        // second instance of the stage loops in this kernel the MLP step,
+        // which has no tail tiles, ran about 1 % slower)
         walk_segments(p, it0, it1,
                       [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
-            float2 acc[TM / 2][TN];
-#pragma unroll
-            for (int i = 0; i < TM / 2; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-            const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + wl * 32 * TN >= q.L.rows;
-            for (int kt = s0; kt < s1; ++kt, ++g) {
-                const int ds = g % kRawDec;
-                mbar_wait(&sm.full[ds], (g / kRawDec) & 1, aborted);
-                if (!idle) {
-                    const uint8_t *st = sm.dec + (size_t)ds * kTmaStageBytes;
-                    const uint32_t *Uo = reinterpret_cast<const uint32_t *>(st);
-                    const float *Us = reinterpret_cast<const float *>(st + BK * BU * 4);
-                    const uint32_t *Lo = reinterpret_cast<const uint32_t *>(st + kTmaUBytes);
-                    const float *Ls = reinterpret_cast<const float *>(st + kTmaUBytes + BK * BL * 4);
-                    int fl = 0;
-#pragma unroll
-                    for (int w = 0; w < kRawDecoders / 32; ++w) fl |= sm.flags[ds * (kRawDecoders / 32) + w];
-                    raw_stage_by_flags<W, false>(fl, acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-                }
-                mbar_arrive(&sm.empty[ds]);
-            }
-            if (s0 == 0 && s1 == q.kt_total) {
-                store_tile(q, acc, b, u_tile0 + urow, l_tile0 + lcol);
-                return;
-            }
-            const long long lt = (long long)b * q.tiles_u * q.tiles_l + (long long)(u_tile0 / BU) * q.tiles_l +
-                                 l_tile0 / BL;
-            float *mine = phased_slot(p, total_tiles, ph, blockIdx.x, first ? 0 : 1);
-            if (!idle) {
-#pragma unroll
-                for (int i = 0; i < TM; ++i)
-#pragma unroll
-                    for (int t4 = 0; t4 < TN / 4; ++t4)
-                        __stcg(reinterpret_cast<float4 *>(mine + (urow + i) * BL + lcol + kColGroup * t4), acc4(acc, i, 4 * t4));
-            }
-            // every consumer's slot writes precede the barrier; thread 0's
-            // fence and ticket update then publish them (cumulative release)
-            consumer_bar();
-            if (tid == 0) {
-                __threadfence();
-                const bool last = last_arrival(p, q.tile0 + lt, s1 - s0, q.kt_total);
-                __threadfence();
-                *last_flag = last ? 1 : 0;
-            }
-            consumer_bar();
-            const bool last = *last_flag != 0;
-            consumer_bar();         // everyone has read the ticket's verdict
-            if (!last || idle) return;
-            const long long tbeg = q.iter0 + lt * q.kt_total, tend = tbeg + q.kt_total;
-            const int c_lo = ph_owner(p, pt, ph, tbeg), c_hi = ph_owner(p, pt, ph, tend - 1);
-            float2 sum[TM / 2][TN];
-#pragma unroll
-            for (int i = 0; i < TM / 2; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) sum[i][j] = make_float2(0.0f, 0.0f);
-            for (int c = c_lo; c <= c_hi; ++c) {
-                const long long cb = ph_begin(p, pt, ph, c);
-                if (cb == ph_begin(p, pt, ph, c + 1)) continue;          // empty share
-                const float *part = phased_slot(p, total_tiles, ph, c, cb >= tbeg ? 0 : 1);
-#pragma unroll
-                for (int i = 0; i < TM; ++i)
-#pragma unroll
-                    for (int t4 = 0; t4 < TN / 4; ++t4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(part + (urow + i) * BL + lcol + kColGroup * t4));
-                        float2 &lo = sum[i >> 1][4 * t4], &l1 = sum[i >> 1][4 * t4 + 1];
-                        float2 &l2 = sum[i >> 1][4 * t4 + 2], &l3 = sum[i >> 1][4 * t4 + 3];
-                        if (i & 1) { lo.y += v.x; l1.y += v.y; l2.y += v.z; l3.y += v.w; }
-                        else { lo.x += v.x; l1.x += v.y; l2.x += v.z; l3.x += v.w; }
-                    }
-            }
-            store_tile(q, sum, b, u_tile0 + urow, l_tile0 + lcol);
+            phased_segment<W, TM>(p, pt, q, lut, sm, total_tiles, ph, b, u_tile0, l_tile0, s0, s1, first, g,
+                                  aborted);
         });
         // every consumer's stores of the phase precede the flag
         consumer_bar();

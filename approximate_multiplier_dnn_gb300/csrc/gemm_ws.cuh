@@ -219,8 +219,8 @@ __device__ __forceinline__ void for_each_segment(const KParams &p, F &&f)
 {
     long long it, it_end;
     if (p.streamk) {
-        it = sk_begin(p.iters, p.ctas, blockIdx.x);
-        it_end = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
+        it = sk_begin(p, blockIdx.x);
+        it_end = sk_begin(p, blockIdx.x + 1);
     } else {
         long long t = blockIdx.x;
         int pi = 0;
@@ -389,8 +389,8 @@ __device__ __forceinline__ StagePos stage_pos(const KParams &p, long long it)
 __device__ __forceinline__ void cta_range(const KParams &p, long long &it, long long &it_end)
 {
     if (p.streamk) {
-        it = sk_begin(p.iters, p.ctas, blockIdx.x);
-        it_end = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
+        it = sk_begin(p, blockIdx.x);
+        it_end = sk_begin(p, blockIdx.x + 1);
     } else {
         long long t = blockIdx.x;
         int pi = 0;
@@ -522,6 +522,8 @@ struct CutTile {
 // slot (0 for its first segment, 1 for its last) -- for the separate fixup
 // kernel, or (fused stream-K) raising the slot's flag and recording the tile
 // in `cut` so that finish_cut_tiles reduces it.  Called by all consumer threads.
+// ROWS: TM for the regular warp layout, kTailRows for the tail layout.
+template <int ROWS = TM>
 __device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbParams &q, float2 (&acc)[TM / 2][TN],
                                                  int b, int u_tile0, int l_tile0, int s0, int s1, bool first,
                                                  CutTile &cut0, CutTile &cut1, int &ncut)
@@ -529,17 +531,17 @@ __device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbPar
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
-    const int u0 = u_tile0 + wu * TM;
-    const int l0 = l_tile0 + wl * 32 * TN + lane * 4;
-    const int ur = wu * TM, lr = wl * 32 * TN + lane * 4;
+    const int ur = ROWS == TM ? wu * TM : warp * ROWS;
+    const int lr = ROWS == TM ? wl * 32 * TN + lane * 4 : lane * 4;
+    const int u0 = u_tile0 + ur, l0 = l_tile0 + lr;
     if (s0 == 0 && s1 == q.kt_total) {
-        store_tile(q, acc, b, u0, l0);
+        store_tile<ROWS>(q, acc, b, u0, l0);
         return;
     }
     const int slot = first ? 0 : 1;
     float *slotp = p.ws + ((long long)blockIdx.x * 2 + slot) * (BU * BL);
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
+    for (int i = 0; i < ROWS; ++i)
 #pragma unroll
         for (int t4 = 0; t4 < TN / 4; ++t4)
             *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + kColGroup * t4) = acc4(acc, i, 4 * t4);
@@ -583,19 +585,18 @@ struct CutShare {
 __device__ __forceinline__ CutShare cut_share(const KParams &p, const CutTile &ct)
 {
     constexpr int kUnits = BU * BL / 4;
-    const long long W = p.iters;
     const int G = p.ctas;
     const long long tstart = ct.tstart, tend = tstart + p.pr[ct.pi].kt_total;
     int c_lo = blockIdx.x, c_hi = blockIdx.x;
-    while (c_lo > 0 && sk_begin(W, G, c_lo) > tstart) --c_lo;
-    while (c_hi + 1 < G && sk_begin(W, G, c_hi + 1) < tend) ++c_hi;
+    while (c_lo > 0 && sk_begin(p, c_lo) > tstart) --c_lo;
+    while (c_hi + 1 < G && sk_begin(p, c_hi + 1) < tend) ++c_hi;
     CutShare sh;
     sh.c_lo = c_lo;
     sh.n = c_hi - c_lo + 1;
     // the first participant began before the tile unless it began exactly at
     // its start (then the tile was its first segment); every later one began
     // inside the tile, so the tile was its first segment
-    sh.lo_slot = sk_begin(W, G, c_lo) == tstart ? 0 : 1;
+    sh.lo_slot = sk_begin(p, c_lo) == tstart ? 0 : 1;
     const int j = blockIdx.x - c_lo;
     sh.e_lo = (int)((long long)j * kUnits / sh.n);
     sh.m = (int)((long long)(j + 1) * kUnits / sh.n) - sh.e_lo;

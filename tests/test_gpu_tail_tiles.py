@@ -1,0 +1,138 @@
+"""Tail tiles of the raw-tile kernel: a tile whose real lane columns all lie in
+its first 128 (the last lane tile of an L extent such as a 3x3 filter
+gradient's R*S*C = 576 = 2 x 256 + 64) is computed by all eight consumer warps
+as eight blocks of 8 rows, instead of four warps of 16 rows with four idle.
+Each output's products are still summed in the same order, so the results
+are bit-identical to the in-kernel-decode kernel's regular layout; cut tiles
+(stream-K, with shares cut by stage cost) reduce partial sums written in that
+layout, checked against the oracle."""
+import numpy as np
+import pytest
+
+from gpu_helpers import assert_close, to_dev
+from approximate_multiplier_dnn_gb300 import GemmProblem
+
+pytestmark = pytest.mark.gpu
+
+
+def rnd(rng, shape):
+    return rng.standard_normal(shape).astype(np.float32)
+
+
+def batched(amd, lut, A, lda, B, m, n, k, batch, ws=None):
+    """C[b] = A[b] B[b] with A[b] m x k (leading dimension lda), B[b] k x n."""
+    import torch
+    C = torch.full((batch, m, n), float("nan"), dtype=torch.float32, device="cuda")
+    amd.amsim_gemm_strided_batched("N", "N", m, n, k, 1.0, A, lda, A.shape[1] * lda, B, n, k * n, 0.0, C, n,
+                                   m * n, batch, lut, ws=ws)
+    torch.cuda.synchronize()
+    return C.cpu().numpy(), amd.amsim_last_path()
+
+
+@pytest.mark.parametrize("values", ["normal", "zeros"])
+@pytest.mark.parametrize("n", [320, 260, 300])
+def test_tail_layout_bit_identical_to_regular_layout(amd, luts, n, values):
+    """One wave of whole tiles (no stream-K): 64 x n per batch entry, the
+    second lane tile a tail (n - 256 <= 128 real columns).  Aligned operands
+    take the raw-tile kernel (tail layout); the same operands behind a leading
+    dimension of k + 1 take the in-kernel-decode kernel (regular layout).
+    With ReLU-like zeros the folded form reads the table's zero row."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    batch = max(sms // 2, 1)
+    m, k = 64, 256
+    rng = np.random.default_rng(n + (7 if values == "zeros" else 0))
+    A = rnd(rng, (batch, m, k))
+    B = rnd(rng, (batch, k, n))
+    if values == "zeros":
+        A[A < 0] = 0.0
+        B[B < -0.3] = -0.0
+    lut = luts("mitchell", 7)
+    dA, dB = to_dev(A), to_dev(B)
+    raw, path_raw = batched(amd, lut, dA, k, dB, m, n, k, batch)
+    assert path_raw & amd.AMSIM_PATH_RAW_TILES and not path_raw & amd.AMSIM_PATH_STREAMK, path_raw
+    wide = torch.zeros((batch, m, k + 1), dtype=torch.float32, device="cuda")
+    wide[:, :, :k] = dA
+    reg, path_reg = batched(amd, lut, wide, k + 1, dB, m, n, k, batch)
+    assert path_reg & amd.AMSIM_PATH_INKERNEL_DECODE and not path_reg & amd.AMSIM_PATH_STREAMK, path_reg
+    assert np.array_equal(raw.view(np.uint32), reg.view(np.uint32))
+
+
+@pytest.mark.parametrize("kind", ["mitchell", "exact"])
+@pytest.mark.parametrize("m,n,k", [(64, 320, 20000), (50, 300, 9000), (64, 132, 30000)])
+def test_tail_tiles_cut_by_stream_k(amd, orc, luts, kind, m, n, k):
+    """Few tiles over a long reduction: stream-K cuts the tail tile among many
+    CTAs, whose partial sums (tail layout) the fused reduction adds; U rows
+    past the edge (m = 50) leave the last row block's warps idle."""
+    import torch
+    rng = np.random.default_rng(m + n + k)
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    lut = luts(kind, 7)
+    nb = amd.amsim_gemm_workspace_size("N", "N", m, n, k, 1, lut)
+    C = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+    amd.amsim_gemm("N", "N", m, n, k, 1.0, to_dev(A), k, to_dev(B), n, 0.0, C, n, lut, ws=amd.workspace(nb))
+    torch.cuda.synchronize()
+    taken = amd.amsim_last_path()
+    assert taken & amd.AMSIM_PATH_RAW_TILES and taken & amd.AMSIM_PATH_STREAMK, taken
+    got = C.cpu().numpy()
+    rows = np.array([0, 7, 8, m // 2, m - 1])
+    ref, sa = orc.gemm(kind, 7, A, B, rows=rows)
+    assert_close(got[rows], ref, sa, f"stream-K tail {m}x{n}x{k} {kind}")
+
+
+def test_tail_tiles_with_special_operands(amd, orc, luts):
+    """Zeros, denormals, infinities, NaN and |x| >= 2^64 in a tail tile: the
+    per-stage flags pick the rounding products in the tail layout too."""
+    import torch
+    from approximate_multiplier_dnn_gb300 import workloads as wl
+    m, n, k = 64, 300, 256
+    rng = np.random.default_rng(23)
+    a, b = wl.special_values_mix(m * k + k * n, seed=24)
+    A = a[:m * k].reshape(m, k).copy()
+    B = b[m * k:].reshape(k, n).copy()
+    A[:, :] = np.where(rng.random(A.shape) < 0.95, rng.standard_normal(A.shape), A).astype(np.float32)
+    B[:, :] = np.where(rng.random(B.shape) < 0.95, rng.standard_normal(B.shape), B).astype(np.float32)
+    for kind in ("mitchell", "exact"):
+        lut = luts(kind, 7)
+        C = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        amd.amsim_gemm("N", "N", m, n, k, 1.0, to_dev(A), k, to_dev(B), n, 0.0, C, n, lut)
+        torch.cuda.synchronize()
+        assert amd.amsim_last_path() & amd.AMSIM_PATH_RAW_TILES
+        ref, sa = orc.gemm(kind, 7, A, B)
+        assert_close(C.cpu().numpy(), ref, sa + 1e-30, f"tail specials {kind}")
+
+
+def test_tail_tiles_in_a_phased_launch(amd, orc, luts):
+    """A phased launch whose first phase is a 64 x 576 x 8192 GEMM (a 3x3
+    filter gradient's shape: its third lane tile is a tail, cut among CTAs;
+    phased launches compute it in the regular layout, with the cost model
+    for that layout) and whose second reads its output: checked against the
+    oracle, and two calls are bit-identical (the last part to arrive adds the
+    parts in CTA order)."""
+    import torch
+    rng = np.random.default_rng(25)
+    m, n, k = 64, 576, 8192
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    W2 = rnd(rng, (n, 72))
+    lut = luts("mitchell", 7)
+    dA, dB, dW2 = to_dev(A), to_dev(B), to_dev(W2)
+    outs = []
+    for _ in range(2):
+        C1 = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+        C2 = torch.full((m, 72), float("nan"), dtype=torch.float32, device="cuda")
+        probs = [GemmProblem.make("N", "N", m, n, k, 1.0, dA, k, dB, n, 0.0, C1, n),
+                 GemmProblem.make("N", "N", m, 72, n, 1.0, C1, n, dW2, 72, 0.0, C2, 72)]
+        first, after = [0, 1], [0, 1]
+        nb = amd.amsim_gemm_phased_workspace_size(probs, first, after, lut)
+        amd.amsim_gemm_phased(probs, first, after, lut, ws=amd.workspace(nb))
+        torch.cuda.synchronize()
+        assert amd.amsim_last_path() & amd.AMSIM_PATH_PHASED, amd.amsim_last_path()
+        outs.append((C1.cpu().numpy(), C2.cpu().numpy()))
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    c1, c2 = outs[0]
+    rows = np.array([0, 9, 33, m - 1])
+    ref, sa = orc.gemm("mitchell", 7, A, B, rows=rows)
+    assert_close(c1[rows], ref, sa, "phased tail C1")
+    ref2, sa2 = orc.gemm("mitchell", 7, c1, W2, rows=rows)
+    assert_close(c2[rows], ref2, sa2, "phased C2 (reads C1)")
