@@ -852,18 +852,20 @@ bool phased_ok(const Problem *p, int n, int nphase, const Plan &pl, amsim_lut_t 
 // faster -- measured on GB300 from per-CTA timelines of phased launches, a
 // stage with a fraction f of its warps busy takes about 0.47 + 0.53 f of a
 // full stage (0.6 at f = 1/4) -- so shares are cut by this cost, not by count.
-// A tail tile (all real lane columns in the first column block) runs in the
-// tail layout: each warp does half a warp's lookups, and a stage takes about
-// 0.6 to 0.68 of a full one, measured on GB300 (0.60 for 64 x 64 and
-// 64 x 128 GEMM tiles against 64 x 256 ones; from the 3x3 filter gradient's
-// pass times, 0.61 with the 16-bit exact table and 0.68 with the 8-bit
-// Mitchell one).  A share that overestimates the cost loses less than one
-// that underestimates it, so the model takes 0.67.  (Phased launches keep
-// the regular layout on tail tiles: tail_layout false.)
+// A tail tile (all real lane columns in the first column block) runs in a
+// tail layout, every warp on half (or, with at most 64 real columns, a
+// quarter) of a warp's lookups, and its producer decodes only the columns
+// that layout reads.  Measured on GB300 against a full stage: 0.58 (64 x 128
+// GEMM tiles) and 0.43 (64 x 64) for one tile per SM; 0.51 and 0.45 for the
+// 64-column tail of the 3x3 filter gradient with the 8-bit Mitchell and the
+// 16-bit exact table.  A share that overestimates a stage's cost loses less
+// than one that underestimates it, so the model takes 0.62 and 0.50.
+// (Phased launches keep the regular layout on tail tiles: tail_layout false.)
 double stage_cost(const Problem &p, int ut, int lt, bool tail_layout)
 {
     constexpr int WUn = BU / kern::TM, WLn = BL / (32 * kern::TN);
-    if (tail_layout && kern::tail_tile(lt * BL, p.L.rows)) return 0.67;
+    if (tail_layout && kern::narrow_tail_tile(lt * BL, p.L.rows)) return 0.50;
+    if (tail_layout && kern::tail_tile(lt * BL, p.L.rows)) return 0.62;
     int busy = 0;
     for (int wu = 0; wu < WUn; ++wu)
         for (int wl = 0; wl < WLn; ++wl)

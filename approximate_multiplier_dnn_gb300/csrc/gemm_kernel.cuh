@@ -189,11 +189,18 @@ __host__ __device__ constexpr int col_of(int t) { return (t >> 2) * kColGroup + 
 // of leaving the warps of the second block idle -- which, as they are every
 // other warp, would also leave half of the SM's schedulers idle.  Each
 // output's products are summed in the same order either way.
+// A tile with at most 64 real lane columns takes the narrow tail layout: the
+// same row blocks over 64 columns, two per lane (lane * 2, lane * 2 + 1).
 constexpr bool kTailLayout = WL == 2 && (TM / 2) * WU * WL == BU && TM % 8 == 0;
 constexpr int kTailRows = TM / 2;
+constexpr int kNarrowTailCols = 2;
 __host__ __device__ constexpr bool tail_tile(int l_tile0, int l_rows)
 {
     return kTailLayout && l_tile0 + 32 * TN >= l_rows;
+}
+__host__ __device__ constexpr bool narrow_tail_tile(int l_tile0, int l_rows)
+{
+    return kTailLayout && l_tile0 + 32 * kNarrowTailCols >= l_rows;
 }
 
 // Shared-memory layout (bytes) after the LUT region.
@@ -596,19 +603,38 @@ __device__ __forceinline__ float accv(const float2 (&acc)[TM / 2][TN], int i, in
 // PU / PL: the stage holds packed operand words (pack_operand) in Uo / Lo,
 // and Us / Ls are not read.  One 128-bit load brings four operands' offsets
 // and scales: half the shared-memory wavefronts of two planes.
+// ROWS / COLS: this warp's uniform rows and each lane's columns (TM and TN;
+// the tail layouts' kTailRows with TN, or with kNarrowTailCols adjacent
+// columns from lcol = lane * 2).
 template <int W, bool GL, bool SLOW, int USTR = UST, int LSTR = LST, bool FMT = false, bool FOLD = false,
-          bool PU = false, bool PL = false, int ROWS = TM>
+          bool PU = false, bool PL = false, int ROWS = TM, int COLS = TN>
 __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                               const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
                                               const float *__restrict__ Ls, const uint8_t *lut, int urow, int lcol,
                                               const ExpFormat *fmt = nullptr)
 {
+    static_assert(COLS == TN || COLS == kNarrowTailCols, "lane columns");
 #pragma unroll(kKkUnroll)
     for (int kk = 0; kk < BK; ++kk) {
         uint32_t lo[TN];
         float2 sb[TN];
+        if constexpr (COLS == kNarrowTailCols) {
+            uint2 o;
+            float2 sc;
+            if constexpr (PL) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(Lo + kk * LSTR + lcol);
+                o = make_uint2(packed_off(w.x), packed_off(w.y));
+                sc = make_float2(__uint_as_float(packed_scale_bits(w.x)), __uint_as_float(packed_scale_bits(w.y)));
+            } else {
+                o = *reinterpret_cast<const uint2 *>(Lo + kk * LSTR + lcol);
+                sc = *reinterpret_cast<const float2 *>(Ls + kk * LSTR + lcol);
+            }
+            lo[0] = o.x; lo[1] = o.y;
+            sb[0] = make_float2(sc.x, sc.x);
+            sb[1] = make_float2(sc.y, sc.y);
+        }
 #pragma unroll
-        for (int t4 = 0; t4 < TN / 4; ++t4) {
+        for (int t4 = 0; t4 < (COLS == TN ? TN / 4 : 0); ++t4) {
             uint4 o;
             float4 sc;
             if constexpr (PL) {
@@ -647,7 +673,7 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
 #pragma unroll
                 for (int ip = 0; ip < 2; ++ip) {
 #pragma unroll
-                    for (int t = 0; t < TN; ++t) {
+                    for (int t = 0; t < COLS; ++t) {
                         const uint32_t ea = lut_ld<W, GL>(lut, uov[2 * ip] + lo[t]);
                         const uint32_t eb = lut_ld<W, GL>(lut, uov[2 * ip + 1] + lo[t]);
                         const float2 v =
@@ -659,7 +685,7 @@ __device__ __forceinline__ void compute_stage(float2 (&acc)[TM / 2][TN], const u
 #pragma unroll
                 for (int ip = 0; ip < 2; ++ip) {
 #pragma unroll
-                    for (int t = 0; t < TN; ++t) {
+                    for (int t = 0; t < COLS; ++t) {
                         const uint32_t ea = lut_ld<W, GL>(lut, uov[2 * ip] + lo[t]);
                         const uint32_t eb = lut_ld<W, GL>(lut, uov[2 * ip + 1] + lo[t]);
                         const float2 v = make_float2(expand<W>(ea), expand<W>(eb));
@@ -699,9 +725,9 @@ __device__ __forceinline__ float4 acc4(const float2 (&acc)[TM / 2][TN], int i, i
 }
 
 // Write a finished tile: C = alpha*acc + beta*C with 128-bit stores when the
-// output is contiguous along L (or along U, for transposed outputs).  ROWS:
-// the rows this warp holds (TM, or kTailRows in the tail layout).
-template <int ROWS = TM>
+// output is contiguous along L (or along U, for transposed outputs).  ROWS /
+// COLS: the rows and lane columns this warp holds (see compute_stage).
+template <int ROWS = TM, int COLS = TN>
 __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&acc)[TM / 2][TN], int b, int u0,
                                            int l0)
 {
@@ -711,13 +737,22 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
     const bool aligned = (reinterpret_cast<uintptr_t>(C) & 15) == 0;
     const bool vec_l = aligned && q.c_sl == 1 && (q.c_su & 3) == 0;
     const bool vec_u = aligned && q.c_su == 1 && (q.c_sl & 3) == 0;
-    if (vec_l && l0 + col_of(TN - 1) < nL) {
+    if (vec_l && l0 + col_of(COLS - 1) < nL) {
 #pragma unroll
         for (int i = 0; i < ROWS; ++i) {
             const int u = u0 + i;
             if (u >= nU) break;
+            if constexpr (COLS == kNarrowTailCols) {
+                float2 *dst = reinterpret_cast<float2 *>(C + (long long)u * q.c_su + l0);
+                float2 r = make_float2(alpha * accv(acc, i, 0), alpha * accv(acc, i, 1));
+                if (beta != 0.0f) {
+                    const float2 o = *dst;
+                    r.x = fmaf(beta, o.x, r.x); r.y = fmaf(beta, o.y, r.y);
+                }
+                *dst = r;
+            }
 #pragma unroll
-            for (int t4 = 0; t4 < TN / 4; ++t4) {
+            for (int t4 = 0; t4 < (COLS == TN ? TN / 4 : 0); ++t4) {
                 float4 *dst = reinterpret_cast<float4 *>(C + (long long)u * q.c_su + l0 + kColGroup * t4);
                 const float4 a = acc4(acc, i, 4 * t4);
                 float4 r = make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w);
@@ -731,7 +766,7 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
         }
     } else if (vec_u && u0 + ROWS <= nU) {
 #pragma unroll
-        for (int t = 0; t < TN; ++t) {
+        for (int t = 0; t < COLS; ++t) {
             const int l = l0 + col_of(t);
             if (l >= nL) break;
             float *col = C + (long long)l * q.c_sl + u0;
@@ -754,7 +789,7 @@ __device__ __forceinline__ void store_tile(const ProbParams &q, const float2 (&a
             const int u = u0 + i;
             if (u >= nU) break;
 #pragma unroll
-            for (int t = 0; t < TN; ++t) {
+            for (int t = 0; t < COLS; ++t) {
                 const int l = l0 + col_of(t);
                 if (l >= nL) break;
                 float *dst = C + (long long)u * q.c_su + (long long)l * q.c_sl;

@@ -133,15 +133,17 @@ __device__ __forceinline__ void decode_as(float v, int M, uint32_t aux, uint32_t
 
 // Decode a raw R-row tile into off/scl [BK][R].  k-fast tiles are [R][BK]
 // fp32 rows of 64 bytes whose 16-byte chunks the copy engine swizzled as
-// chunk ^ ((row >> 1) & 3); row-fast tiles are [BK][R].
-template <int R, int DM, bool LANE = false>
+// chunk ^ ((row >> 1) & 3); row-fast tiles are [BK][R].  Only rows 0 .. NR - 1
+// are decoded (a tail tile's consumers read no others).
+template <int R, int DM, bool LANE = false, int NR = R>
 __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint32_t *off, float *scl, int M,
                                            uint32_t aux, int d, StageFlags &fl)
 {
+    static_assert(NR <= R && NR % 4 == 0, "decoded rows");
     if (kfast) {
 #pragma unroll 2
-        for (int task = d; task < R * (BK / 4); task += kRawDecoders) {
-            const int r = task % R, c = task / R;
+        for (int task = d; task < NR * (BK / 4); task += kRawDecoders) {
+            const int r = task % NR, c = task / NR;
             const float4 v = *reinterpret_cast<const float4 *>(raw + r * (BK * 4) + ((c ^ ((r >> 1) & 3)) << 4));
             const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -155,8 +157,8 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
         }
     } else {
 #pragma unroll 2
-        for (int task = d; task < BK * (R / 4); task += kRawDecoders) {
-            const int k = task / (R / 4), r4 = (task % (R / 4)) * 4;
+        for (int task = d; task < BK * (NR / 4); task += kRawDecoders) {
+            const int k = task / (NR / 4), r4 = (task % (NR / 4)) * 4;
             const float4 v = *reinterpret_cast<const float4 *>(raw + (k * R + r4) * 4);
             uint4 o;
             float4 s;
@@ -171,13 +173,14 @@ __device__ __forceinline__ void raw_decode(const uint8_t *raw, bool kfast, uint3
 }
 
 // Decode four row-fast 64-row blocks ([BK][64] each, the filter gradient's
-// L tile) into columns 64 b .. 64 b + 63 of off/scl [BK][BL].
-template <int DM>
+// L tile) into columns 64 b .. 64 b + 63 of off/scl [BK][BL]; only the first
+// NB blocks (a tail tile's consumers read no others).
+template <int DM, int NB = BL / 64>
 __device__ __forceinline__ void raw_decode_blocks(const uint8_t *raw, uint32_t *off, float *scl, int M,
                                                   uint32_t aux, int d, StageFlags &fl)
 {
 #pragma unroll 2
-    for (int task = d; task < (BL / 64) * BK * 16; task += kRawDecoders) {
+    for (int task = d; task < NB * BK * 16; task += kRawDecoders) {
         const int b = task / (BK * 16), rem = task % (BK * 16);
         const int k = rem / 16, r4 = (rem % 16) * 4;
         const float4 v = *reinterpret_cast<const float4 *>(raw + ((b * BK + k) * 64 + r4) * 4);
@@ -351,7 +354,7 @@ __device__ __forceinline__ float trunc_scale(uint32_t t)
 //    is exact and normal (exponent sum >= 1), as the table path's v * s is.
 //  - Other stages rebuild the table path's (v, s) and round the product
 //    before adding it, as compute_stage's slow stages do.
-template <int KIND, bool SLOW, int ROWS = TM>
+template <int KIND, bool SLOW, int ROWS = TM, int COLS = TN>
 __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], const uint32_t *__restrict__ Uo,
                                                   const float *__restrict__ Us, const uint32_t *__restrict__ Lo,
                                                   const float *__restrict__ Ls, int urow, int lcol)
@@ -360,8 +363,24 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
     for (int kk = 0; kk < BK; ++kk) {
         uint32_t lo[TN];
         float2 sb[TN];
+        if constexpr (COLS == kNarrowTailCols) {
+            const uint2 o = *reinterpret_cast<const uint2 *>(Lo + kk * BL + lcol);
+            lo[0] = o.x; lo[1] = o.y;
+            if constexpr (KIND == 1) {
+                const float2 sc = *reinterpret_cast<const float2 *>(Ls + kk * BL + lcol);
+                sb[0] = make_float2(sc.x, sc.x);
+                sb[1] = make_float2(sc.y, sc.y);
+            }
+            if constexpr (SLOW) {
 #pragma unroll
-        for (int t4 = 0; t4 < TN / 4; ++t4) {
+                for (int t = 0; t < COLS; ++t) {
+                    const float b = KIND == 1 ? trunc_scale(__float_as_uint(sb[t].x) | lo[t]) : trunc_scale(lo[t]);
+                    sb[t] = make_float2(b, b);
+                }
+            }
+        }
+#pragma unroll
+        for (int t4 = 0; t4 < (COLS == TN ? TN / 4 : 0); ++t4) {
             const uint4 o = *reinterpret_cast<const uint4 *>(Lo + kk * BL + lcol + kColGroup * t4);
             lo[4 * t4 + 0] = o.x; lo[4 * t4 + 1] = o.y; lo[4 * t4 + 2] = o.z; lo[4 * t4 + 3] = o.w;
             if constexpr (KIND == 1) {
@@ -394,7 +413,7 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
 #pragma unroll
             for (int ip = 0; ip < 2; ++ip) {
 #pragma unroll
-                for (int t = 0; t < TN; ++t) {
+                for (int t = 0; t < COLS; ++t) {
                     float2 &a = acc[2 * ig + ip][t];
                     const uint32_t u0 = uov[2 * ip], u1 = uov[2 * ip + 1];
                     if constexpr (SLOW) {
@@ -425,41 +444,45 @@ __device__ __forceinline__ void compute_stage_alu(float2 (&acc)[TM / 2][TN], con
 
 // A decoded stage of the raw-tile kernel: table entries (W = 8, 16, 32; packed
 // operand words with the table in shared memory) or closed forms (W = 1
-// Mitchell, 2 exact), over this warp's ROWS uniform rows.
-template <int W, bool GL, bool SLOW, bool FOLD = false, int ROWS = TM>
+// Mitchell, 2 exact), over this warp's ROWS uniform rows and each lane's
+// COLS columns.
+template <int W, bool GL, bool SLOW, bool FOLD = false, int ROWS = TM, int COLS = TN>
 __device__ __forceinline__ void raw_stage(float2 (&acc)[TM / 2][TN], const uint32_t *Uo, const float *Us,
                                           const uint32_t *Lo, const float *Ls, const uint8_t *lut, int urow,
                                           int lcol)
 {
-    if constexpr (W <= 2) compute_stage_alu<W, SLOW, ROWS>(acc, Uo, Us, Lo, Ls, urow, lcol);
-    else compute_stage<W, GL, SLOW, BU, BL, false, FOLD, !GL, !GL, ROWS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    if constexpr (W <= 2) compute_stage_alu<W, SLOW, ROWS, COLS>(acc, Uo, Us, Lo, Ls, urow, lcol);
+    else compute_stage<W, GL, SLOW, BU, BL, false, FOLD, !GL, !GL, ROWS, COLS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
 }
 
 // One stage of a consumer: the rounding slow products when a decoder flagged
 // bit 0, the folded-scale form when no decoder flagged bit 1 (tables in
 // shared memory only), else the general form.
-template <int W, bool GL, int ROWS = TM>
+template <int W, bool GL, int ROWS = TM, int COLS = TN>
 __device__ __forceinline__ void raw_stage_by_flags(int fl, float2 (&acc)[TM / 2][TN], const uint32_t *Uo,
                                                    const float *Us, const uint32_t *Lo, const float *Ls,
                                                    const uint8_t *lut, int urow, int lcol)
 {
-    if (fl & 1) raw_stage<W, GL, true, false, ROWS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    if (fl & 1) raw_stage<W, GL, true, false, ROWS, COLS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
     else if (W > 2 && !GL && !(fl & 2))
-        raw_stage<W, GL, false, (W > 2 && !GL), ROWS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
-    else raw_stage<W, GL, false, false, ROWS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+        raw_stage<W, GL, false, (W > 2 && !GL), ROWS, COLS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+    else raw_stage<W, GL, false, false, ROWS, COLS>(acc, Uo, Us, Lo, Ls, lut, urow, lcol);
 }
 
-// This warp's rows and lane columns of a tile in the regular layout (ROWS =
-// TM) or the tail layout (ROWS = kTailRows).
-template <int ROWS>
-__device__ __forceinline__ void warp_span(int warp, int lane, int &urow, int &lcol)
+// This warp's rows, lane columns and column block of a tile in the regular
+// layout (ROWS = TM, COLS = TN) or a tail layout (ROWS = kTailRows; COLS = TN,
+// or kNarrowTailCols adjacent columns per lane).
+template <int ROWS, int COLS>
+__device__ __forceinline__ void warp_span(int warp, int lane, int &urow, int &lcol, int &lblock)
 {
     if constexpr (ROWS == TM) {
         urow = (warp / WL) * TM;
-        lcol = (warp % WL) * 32 * TN + lane * 4;
+        lblock = (warp % WL) * 32 * TN;
+        lcol = lblock + lane * 4;
     } else {
         urow = warp * ROWS;
-        lcol = lane * 4;
+        lblock = 0;
+        lcol = lane * (COLS == TN ? 4 : COLS);
     }
 }
 
@@ -536,12 +559,28 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
         }
         raw_decode<BU, DU>(raw, q.u_kfast, reinterpret_cast<uint32_t *>(st),
                        reinterpret_cast<float *>(st + BK * BU * 4), p.M, offU, d, big);
-        if (p.conv == 2)
-            raw_decode_blocks<DL>(raw + kRawUBytes, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
-                              reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
-        else
-            raw_decode<BL, DL, true>(raw + kRawUBytes, q.l_kfast, reinterpret_cast<uint32_t *>(st + kTmaUBytes),
-                           reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4), p.M, offL, d, big);
+        // the L columns the tile's consumers read: all, or those of a tail layout
+        const int lcols = narrow_tail_tile(sp.l_tile0, q.L.rows) ? 32 * kNarrowTailCols
+                          : tail_tile(sp.l_tile0, q.L.rows)      ? 32 * TN
+                                                                 : BL;
+        uint32_t *lo = reinterpret_cast<uint32_t *>(st + kTmaUBytes);
+        float *ls = reinterpret_cast<float *>(st + kTmaUBytes + BK * BL * 4);
+        if (p.conv == 2) {
+            if (lcols == 32 * kNarrowTailCols)
+                raw_decode_blocks<DL, 32 * kNarrowTailCols / 64>(raw + kRawUBytes, lo, ls, p.M, offL, d, big);
+            else if (lcols == 32 * TN)
+                raw_decode_blocks<DL, 32 * TN / 64>(raw + kRawUBytes, lo, ls, p.M, offL, d, big);
+            else
+                raw_decode_blocks<DL>(raw + kRawUBytes, lo, ls, p.M, offL, d, big);
+        } else {
+            if (lcols == 32 * kNarrowTailCols)
+                raw_decode<BL, DL, true, 32 * kNarrowTailCols>(raw + kRawUBytes, q.l_kfast, lo, ls, p.M, offL, d,
+                                                               big);
+            else if (lcols == 32 * TN)
+                raw_decode<BL, DL, true, 32 * TN>(raw + kRawUBytes, q.l_kfast, lo, ls, p.M, offL, d, big);
+            else
+                raw_decode<BL, DL, true>(raw + kRawUBytes, q.l_kfast, lo, ls, p.M, offL, d, big);
+        }
         mbar_arrive(&sm.raw_empty[rs]);
         const int any = __reduce_or_sync(0xFFFFFFFFu, big.bits());
         if (lane == 0) sm.flags[ds * (kRawDecoders / 32) + dw] = any;
@@ -564,21 +603,20 @@ __device__ __forceinline__ void raw_producer(const KParams &p, const TmaMaps &ma
 
 // Stages [s0, s1) of one segment of a tile for one consumer warp in the
 // layout ROWS (TM, or kTailRows for a tail tile); `g` counts decoded stages.
-template <int W, bool GL, int ROWS>
+template <int W, bool GL, int ROWS, int COLS>
 __device__ __forceinline__ void raw_segment(const KParams &p, const ProbParams &q, const uint8_t *lut,
                                             const RawSmem &sm, int b, int u_tile0, int l_tile0, int s0, int s1,
                                             bool first, uint32_t &g, bool &aborted, CutTile &cut0, CutTile &cut1,
                                             int &ncut)
 {
-    const int lane = threadIdx.x & 31;
-    int urow, lcol;
-    warp_span<ROWS>(uniform_warp(), lane, urow, lcol);
+    int urow, lcol, lblock;
+    warp_span<ROWS, COLS>(uniform_warp(), threadIdx.x & 31, urow, lcol, lblock);
     float2 acc[TM / 2][TN];
 #pragma unroll
     for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-    const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + lcol - 4 * lane >= q.L.rows;
+    const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + lblock >= q.L.rows;
     for (int kt = s0; kt < s1; ++kt, ++g) {
         const int ds = g % kRawDec;
         mbar_wait(&sm.full[ds], (g / kRawDec) & 1, aborted);
@@ -591,11 +629,11 @@ __device__ __forceinline__ void raw_segment(const KParams &p, const ProbParams &
             int fl = 0;
 #pragma unroll
             for (int w = 0; w < kRawDecoders / 32; ++w) fl |= sm.flags[ds * (kRawDecoders / 32) + w];
-            raw_stage_by_flags<W, GL, ROWS>(fl, acc, Uo, Us, Lo, Ls, lut, urow, lcol);
+            raw_stage_by_flags<W, GL, ROWS, COLS>(fl, acc, Uo, Us, Lo, Ls, lut, urow, lcol);
         }
         mbar_arrive(&sm.empty[ds]);
     }
-    segment_epilogue<ROWS>(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, cut0, cut1, ncut);
+    segment_epilogue<ROWS, COLS>(p, q, acc, b, u_tile0, l_tile0, s0, s1, first, cut0, cut1, ncut);
 }
 
 template <int W, bool GL>
@@ -606,12 +644,15 @@ __device__ __forceinline__ void raw_consumer(const KParams &p, const uint8_t *lu
     CutTile cut0, cut1;
     int ncut = 0;
     for_each_segment(p, [&](const ProbParams &q, int b, int u_tile0, int l_tile0, int s0, int s1, bool first) {
-        if (tail_tile(l_tile0, q.L.rows))
-            raw_segment<W, GL, kTailRows>(p, q, lut, sm, b, u_tile0, l_tile0, s0, s1, first, g, aborted, cut0,
-                                          cut1, ncut);
+        if (narrow_tail_tile(l_tile0, q.L.rows))
+            raw_segment<W, GL, kTailRows, kNarrowTailCols>(p, q, lut, sm, b, u_tile0, l_tile0, s0, s1, first, g,
+                                                           aborted, cut0, cut1, ncut);
+        else if (tail_tile(l_tile0, q.L.rows))
+            raw_segment<W, GL, kTailRows, TN>(p, q, lut, sm, b, u_tile0, l_tile0, s0, s1, first, g, aborted, cut0,
+                                              cut1, ncut);
         else
-            raw_segment<W, GL, TM>(p, q, lut, sm, b, u_tile0, l_tile0, s0, s1, first, g, aborted, cut0, cut1,
-                                   ncut);
+            raw_segment<W, GL, TM, TN>(p, q, lut, sm, b, u_tile0, l_tile0, s0, s1, first, g, aborted, cut0, cut1,
+                                       ncut);
     });
     // the rings (decoded, then raw, contiguous) hold the reduction's copies
     finish_cut_tiles(p, cut0, cut1, ncut, reinterpret_cast<float *>(sm.dec), red_bytes, sm.raw_full + 2 * kRawRing +
@@ -859,14 +900,14 @@ __device__ __forceinline__ void phased_segment(const KParams &p, const PhaseTabl
     volatile int *last_flag = sm.flags + kRawDec * (kRawDecoders / 32);   // the ticket's verdict
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    int urow, lcol;
-    warp_span<ROWS>(uniform_warp(), lane, urow, lcol);
+    int urow, lcol, lblock;
+    warp_span<ROWS, TN>(uniform_warp(), lane, urow, lcol, lblock);
     float2 acc[TM / 2][TN];
 #pragma unroll
     for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-    const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + lcol - 4 * lane >= q.L.rows;
+    const bool idle = u_tile0 + urow >= q.U.rows || l_tile0 + lblock >= q.L.rows;
     for (int kt = s0; kt < s1; ++kt, ++g) {
         const int ds = g % kRawDec;
         mbar_wait(&sm.full[ds], (g / kRawDec) & 1, aborted);

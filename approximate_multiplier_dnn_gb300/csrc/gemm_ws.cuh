@@ -522,8 +522,9 @@ struct CutTile {
 // slot (0 for its first segment, 1 for its last) -- for the separate fixup
 // kernel, or (fused stream-K) raising the slot's flag and recording the tile
 // in `cut` so that finish_cut_tiles reduces it.  Called by all consumer threads.
-// ROWS: TM for the regular warp layout, kTailRows for the tail layout.
-template <int ROWS = TM>
+// ROWS / COLS: TM and TN for the regular warp layout; kTailRows with TN or
+// kNarrowTailCols for the tail layouts.
+template <int ROWS = TM, int COLS = TN>
 __device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbParams &q, float2 (&acc)[TM / 2][TN],
                                                  int b, int u_tile0, int l_tile0, int s0, int s1, bool first,
                                                  CutTile &cut0, CutTile &cut1, int &ncut)
@@ -532,19 +533,22 @@ __device__ __forceinline__ void segment_epilogue(const KParams &p, const ProbPar
     const int lane = tid & 31, warp = tid >> 5;
     const int wu = warp / WL, wl = warp % WL;
     const int ur = ROWS == TM ? wu * TM : warp * ROWS;
-    const int lr = ROWS == TM ? wl * 32 * TN + lane * 4 : lane * 4;
+    const int lr = ROWS == TM ? wl * 32 * TN + lane * 4 : lane * (COLS == TN ? 4 : COLS);
     const int u0 = u_tile0 + ur, l0 = l_tile0 + lr;
     if (s0 == 0 && s1 == q.kt_total) {
-        store_tile<ROWS>(q, acc, b, u0, l0);
+        store_tile<ROWS, COLS>(q, acc, b, u0, l0);
         return;
     }
     const int slot = first ? 0 : 1;
     float *slotp = p.ws + ((long long)blockIdx.x * 2 + slot) * (BU * BL);
 #pragma unroll
-    for (int i = 0; i < ROWS; ++i)
+    for (int i = 0; i < ROWS; ++i) {
+        if constexpr (COLS == kNarrowTailCols)
+            *reinterpret_cast<float2 *>(slotp + (ur + i) * BL + lr) = make_float2(accv(acc, i, 0), accv(acc, i, 1));
 #pragma unroll
-        for (int t4 = 0; t4 < TN / 4; ++t4)
+        for (int t4 = 0; t4 < (COLS == TN ? TN / 4 : 0); ++t4)
             *reinterpret_cast<float4 *>(slotp + (ur + i) * BL + lr + kColGroup * t4) = acc4(acc, i, 4 * t4);
+    }
     if (!p.fused) return;
     // every consumer's slot writes precede the barrier; the release store of
     // one thread then publishes all of them (release is cumulative)

@@ -1,7 +1,9 @@
 """Tail tiles of the raw-tile kernel: a tile whose real lane columns all lie in
 its first 128 (the last lane tile of an L extent such as a 3x3 filter
 gradient's R*S*C = 576 = 2 x 256 + 64) is computed by all eight consumer warps
-as eight blocks of 8 rows, instead of four warps of 16 rows with four idle.
+as eight blocks of 8 rows, instead of four warps of 16 rows with four idle:
+four columns per lane, or two (lane * 2, lane * 2 + 1) when at most 64
+columns are real.
 Each output's products are still summed in the same order, so the results
 are bit-identical to the in-kernel-decode kernel's regular layout; cut tiles
 (stream-K, with shares cut by stage cost) reduce partial sums written in that
@@ -30,10 +32,11 @@ def batched(amd, lut, A, lda, B, m, n, k, batch, ws=None):
 
 
 @pytest.mark.parametrize("values", ["normal", "zeros"])
-@pytest.mark.parametrize("n", [320, 260, 300])
+@pytest.mark.parametrize("n", [320, 260, 300, 340, 384])
 def test_tail_layout_bit_identical_to_regular_layout(amd, luts, n, values):
     """One wave of whole tiles (no stream-K): 64 x n per batch entry, the
-    second lane tile a tail (n - 256 <= 128 real columns).  Aligned operands
+    second lane tile a tail (n - 256 <= 128 real columns; two columns per lane
+    up to 64).  Aligned operands
     take the raw-tile kernel (tail layout); the same operands behind a leading
     dimension of k + 1 take the in-kernel-decode kernel (regular layout).
     With ReLU-like zeros the folded form reads the table's zero row."""
@@ -59,7 +62,7 @@ def test_tail_layout_bit_identical_to_regular_layout(amd, luts, n, values):
 
 
 @pytest.mark.parametrize("kind", ["mitchell", "exact"])
-@pytest.mark.parametrize("m,n,k", [(64, 320, 20000), (50, 300, 9000), (64, 132, 30000)])
+@pytest.mark.parametrize("m,n,k", [(64, 320, 20000), (50, 300, 9000), (64, 116, 30000), (64, 360, 20000)])
 def test_tail_tiles_cut_by_stream_k(amd, orc, luts, kind, m, n, k):
     """Few tiles over a long reduction: stream-K cuts the tail tile among many
     CTAs, whose partial sums (tail layout) the fused reduction adds; U rows
@@ -80,12 +83,13 @@ def test_tail_tiles_cut_by_stream_k(amd, orc, luts, kind, m, n, k):
     assert_close(got[rows], ref, sa, f"stream-K tail {m}x{n}x{k} {kind}")
 
 
-def test_tail_tiles_with_special_operands(amd, orc, luts):
+@pytest.mark.parametrize("n", [300, 360])
+def test_tail_tiles_with_special_operands(amd, orc, luts, n):
     """Zeros, denormals, infinities, NaN and |x| >= 2^64 in a tail tile: the
-    per-stage flags pick the rounding products in the tail layout too."""
+    per-stage flags pick the rounding products in the tail layouts too."""
     import torch
     from approximate_multiplier_dnn_gb300 import workloads as wl
-    m, n, k = 64, 300, 256
+    m, k = 64, 256
     rng = np.random.default_rng(23)
     a, b = wl.special_values_mix(m * k + k * n, seed=24)
     A = a[:m * k].reshape(m, k).copy()
@@ -136,3 +140,34 @@ def test_tail_tiles_in_a_phased_launch(amd, orc, luts):
     assert_close(c1[rows], ref, sa, "phased tail C1")
     ref2, sa2 = orc.gemm("mitchell", 7, c1, W2, rows=rows)
     assert_close(c2[rows], ref2, sa2, "phased C2 (reads C1)")
+
+
+@pytest.mark.parametrize("n", [300, 360])
+@pytest.mark.parametrize("kind", ["mitchell", "exact"])
+def test_tail_tiles_with_closed_forms(amd, orc, luts, kind, n):
+    """Closed-form products (computed in registers) in both tail layouts, cut
+    by stream-K: bit-identical to the table's products, within the oracle's
+    tolerance."""
+    import torch
+    rng = np.random.default_rng(26 + n)
+    m, k = 64, 12000
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    dA, dB = to_dev(A), to_dev(B)
+    outs = []
+    cf = amd.Lut.build(kind, 7).set_closed_form(True)
+    try:
+        for lut in (luts(kind, 7), cf):
+            nb = amd.amsim_gemm_workspace_size("N", "N", m, n, k, 1, lut)
+            C = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+            amd.amsim_gemm("N", "N", m, n, k, 1.0, dA, k, dB, n, 0.0, C, n, lut, ws=amd.workspace(nb))
+            torch.cuda.synchronize()
+            taken = amd.amsim_last_path()
+            assert taken & amd.AMSIM_PATH_RAW_TILES and taken & amd.AMSIM_PATH_STREAMK, taken
+            outs.append(C.cpu().numpy())
+        assert taken & amd.AMSIM_PATH_CLOSED_FORM, taken
+    finally:
+        cf.close()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    rows = np.array([0, 31, m - 1])
+    ref, sa = orc.gemm(kind, 7, A, B, rows=rows)
+    assert_close(outs[1][rows], ref, sa, f"closed form tail {kind} n={n}")
