@@ -187,8 +187,9 @@ __host__ __device__ constexpr int col_of(int t) { return (t >> 2) * kColGroup + 
 // all lie in its first column block (at most 32 * TN of them) is computed by
 // all the warps as WU * WL row blocks of TM / 2 rows over that block, instead
 // of leaving the warps of the second block idle -- which, as they are every
-// other warp, would also leave half of the SM's schedulers idle.  Each
-// output's products are summed in the same order either way.
+// other warp and warps go to the SM's four schedulers by warp index modulo 4,
+// would also leave two of the schedulers without a busy warp.  Each output's
+// products are summed in the same order either way.
 // A tile with at most 64 real lane columns takes the narrow tail layout: the
 // same row blocks over 64 columns, two per lane (lane * 2, lane * 2 + 1).
 constexpr bool kTailLayout = WL == 2 && (TM / 2) * WU * WL == BU && TM % 8 == 0;

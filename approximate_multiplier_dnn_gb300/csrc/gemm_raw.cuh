@@ -15,6 +15,12 @@
 // decoders' transposing reads are free of bank conflicts.  No operand planes
 // and no separate decode launch are needed; each CTA decodes its own tiles.
 //
+// A tile whose real lane columns all fit in its first 128 (or 64) is
+// computed in a tail layout (kTailLayout: every consumer warp on 8 rows), and
+// its decoders skip the columns that layout never reads; the host cuts an
+// ordinary launch's stream-K shares by each tile's stage cost.  Phased
+// launches keep the regular layout.
+//
 // Barriers: raw_full (copy bytes), raw_empty (decoders done with a raw slot),
 // full (decoded stage ready), empty (consumers done).  Every wait is bounded
 // by the global timer; copies still in flight at an abort are waited for.
