@@ -38,6 +38,14 @@ namespace kern {
 constexpr int kRawDecoders = 128;                       // the producer warpgroup
 constexpr int kRawThreads = kTmaConsumerThreads + kRawDecoders;
 static_assert(kRawThreads == kTmaThreads, "same block shape as the predecoded kernel");
+// Register split of the decoder warpgroup and the consumers: the decoders'
+// dispatch over full and tail-tile decodes spilled at 56 registers.
+constexpr int kRawProducerRegs = 72;
+constexpr int kRawConsumerRegs =
+    ((kRawThreads * kTmaLaunchRegs - kRawDecoders * kRawProducerRegs) / kTmaConsumerThreads) & ~7;
+static_assert(kRawConsumerRegs <= 256 &&
+                  kTmaConsumerThreads * kRawConsumerRegs + kRawDecoders * kRawProducerRegs <= kRawThreads * kTmaLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kRawUBytes = BU * BK * 4;                 // raw fp32 tile of U
 constexpr int kRawLBytes = BL * BK * 4;
 constexpr int kRawStageBytes = kRawUBytes + kRawLBytes; // 20 KB
@@ -1067,12 +1075,12 @@ __device__ __forceinline__ void raw_kernel_body(const KParams &p, const TmaMaps 
 
     const uint8_t *lut = GL ? static_cast<const uint8_t *>(p.pr[0].table) : smem;
     if (tid >= kTmaConsumerThreads) {
-        if constexpr (kTmaProducerWarps == 4) reg_dealloc<kTmaProducerRegs>();
+        reg_dealloc<kRawProducerRegs>();
         constexpr int ALU = W <= 2 ? W : 0;
         if constexpr (PH) raw_producer_phased<ALU>(p, maps, *pt, sm);
         else raw_producer<ALU, ALU == 0 && !GL>(p, maps, sm);
     } else {
-        if constexpr (kTmaProducerWarps == 4) reg_alloc<kTmaConsumerRegs>();
+        reg_alloc<kRawConsumerRegs>();
         if (!GL && p.table_bytes > 0) {
             bool gave_up = false;
             mbar_wait(lut_bar, 0, gave_up);
@@ -1113,8 +1121,7 @@ int launch_raw_instance(const KParams &p, const TmaMaps &maps, const PhaseTable 
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return cuda_status(e);
-        if (kTmaProducerWarps == 4 &&
-            fa.numRegs * kRawThreads < kTmaConsumerThreads * kTmaConsumerRegs + 128 * kTmaProducerRegs) {
+        if (fa.numRegs * kRawThreads < kTmaConsumerThreads * kRawConsumerRegs + kRawDecoders * kRawProducerRegs) {
             checked[dev] = -1;
         } else {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
