@@ -11,7 +11,7 @@ layout, checked against the oracle."""
 import numpy as np
 import pytest
 
-from gpu_helpers import assert_close, to_dev
+from gpu_helpers import REL, assert_close, to_dev
 from approximate_multiplier_dnn_gb300 import GemmProblem
 
 pytestmark = pytest.mark.gpu
@@ -171,3 +171,33 @@ def test_tail_tiles_with_closed_forms(amd, orc, luts, kind, n):
     rows = np.array([0, 31, m - 1])
     ref, sa = orc.gemm(kind, 7, A, B, rows=rows)
     assert_close(outs[1][rows], ref, sa, f"closed form tail {kind} n={n}")
+
+
+@pytest.mark.parametrize("ldc_pad", [0, 1])
+@pytest.mark.parametrize("ta,tb", [(False, False), (True, False), (False, True), (True, True)])
+@pytest.mark.parametrize("m,n", [(64, 300), (300, 64), (64, 360)])
+def test_tail_tiles_transposes_alpha_beta(amd, orc, luts, m, n, ta, tb, ldc_pad):
+    """Tail tiles through every store path: C along L (m = 64: U is A's rows),
+    C along U (n = 64: the planner swaps the operands, so L is A's rows and
+    stores run down C's columns), and an odd leading dimension of C (scalar
+    stores); alpha and beta both applied."""
+    import torch
+    k = 500
+    rng = np.random.default_rng(1000 * m + n + 2 * ta + tb + 7 * ldc_pad)
+    A = rnd(rng, (k, m) if ta else (m, k))
+    B = rnd(rng, (n, k) if tb else (k, n))
+    ldc = n + ldc_pad
+    C0 = rnd(rng, (m, ldc))
+    lut = luts("mitchell", 7)
+    C = to_dev(C0)
+    alpha, beta = 0.5, -1.25
+    amd.amsim_gemm("T" if ta else "N", "T" if tb else "N", m, n, k, alpha, to_dev(A), A.shape[1], to_dev(B),
+                   B.shape[1], beta, C, ldc, lut)
+    torch.cuda.synchronize()
+    assert amd.amsim_last_path() & amd.AMSIM_PATH_RAW_TILES, amd.amsim_last_path()
+    got = C.cpu().numpy()
+    ref, sa = orc.gemm("mitchell", 7, A, B, transA=ta, transB=tb, alpha=alpha, beta=beta, C0=C0[:, :n].copy())
+    scale = abs(alpha) * sa + abs(beta) * np.abs(C0[:, :n].astype(np.float64)) / REL * 2.0 ** -23
+    assert_close(got[:, :n], ref, scale + 1e-30, f"tail {m}x{n} {ta}{tb} ldc+{ldc_pad}")
+    if ldc_pad:
+        assert np.array_equal(got[:, n:], C0[:, n:])      # the padding column is untouched
