@@ -876,13 +876,16 @@ double stage_cost(const Problem &p, int ut, int lt, bool tail_layout)
 // Stream-K shares of an ordinary raw-tile launch cut by stage cost: CTA c
 // starts where the running cost of the launch's tiles (in iteration order)
 // reaches c / G of the total, rounded to a stage, every share at least one
-// stage.  False (keep the even split) when every stage costs the same, or the
-// table does not hold the CTAs or the iterations.
+// stage.  False (keep the even split) when every stage costs the same, when
+// the launch has more than 16 tiles per CTA (each share then holds a mix of
+// tiles close to the launch's own, and the walk over the tiles would cost
+// host time), or when the table does not hold the CTAs or the iterations.
 bool streamk_bounds_by_cost(const Problem *p, int n, const Plan &pl, kern::KParams &kp)
 {
     kp.sk_n = 0;
     const int G = pl.ctas;
     if (!pl.streamk || G > kern::kMaxPhasedCtas || pl.iters >= 0x7FFFFFFFLL || pl.iters < G) return false;
+    if (pl.total_tiles > 16LL * G) return false;
     struct Run { long long it0; int kt; double w; };
     std::vector<Run> runs;                  // tiles in iteration order
     double C = 0.0;
