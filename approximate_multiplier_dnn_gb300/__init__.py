@@ -90,6 +90,7 @@ def lib():
         "amsim_last_path": ([], i32),
         "amsim_device_errors": ([ctypes.POINTER(ctypes.c_uint), i32], i32),
         "amsim_set_flag_wait_limit": ([ctypes.c_longlong], i32),
+        "amsim_set_cooperative_launches": ([i32], i32),
         "amsim_lut_generate": ([i32, i32, vp], i32),
         "amsim_lut_generate_from_fn": ([APPROX_MUL_FN, i32, vp], i32),
         "amsim_lut_build": ([i32, i32, ctypes.POINTER(vp)], i32),
@@ -177,6 +178,10 @@ def amsim_device_errors(clear: bool = True) -> tuple[int, int]:
 
 def amsim_set_flag_wait_limit(ns: int) -> None:
     _check("amsim_set_flag_wait_limit", lib().amsim_set_flag_wait_limit(int(ns)))
+
+
+def amsim_set_cooperative_launches(on: bool) -> None:
+    _check("amsim_set_cooperative_launches", lib().amsim_set_cooperative_launches(1 if on else 0))
 
 
 def status_string(status: int) -> str:

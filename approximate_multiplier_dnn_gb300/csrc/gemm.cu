@@ -29,6 +29,11 @@ thread_local int g_last_path = 0;
 // scratch by earlier launches never match.
 std::atomic<unsigned long long> g_epoch{0x5EED0001ULL};
 
+// Cooperative launches (amsim_set_cooperative_launches): on, stream-K launches
+// finish cut tiles inside the kernel and phased calls run as one launch.
+std::atomic<bool> g_coop{true};
+bool coop_launches() { return g_coop.load(std::memory_order_relaxed); }
+
 int device_sms(int dev)
 {
     static std::atomic<int> cache[64];
@@ -373,7 +378,7 @@ int run_tma(int width, bool wide, kern::KParams &tp, const kern::TmaMaps &maps, 
     int rc = kern::launch_predecode(dp, sms, stream);
     if (rc) return rc;
     const int base = AMSIM_PATH_PLANES | (streamk ? AMSIM_PATH_STREAMK : 0) | (wide ? AMSIM_PATH_WIDE_TILES : 0);
-    tp.fused = streamk ? 1 : 0;
+    tp.fused = streamk && coop_launches() ? 1 : 0;
     rc = launch_tma(width, wide, tp, maps, gl, grid, smem, stream);
     if (rc == kern::AMSIM_ENOTCOOP) {
         tp.fused = 0;
@@ -664,7 +669,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
             tp.alu = alu;
             tp.table_bytes = (raw_gl || alu) ? 0 : (int)gemm_table_bytes(lut);
             tp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
-            tp.fused = pl.streamk ? 1 : 0;
+            tp.fused = pl.streamk && coop_launches() ? 1 : 0;
             streamk_bounds_by_cost(p, n, pl, tp);
             const dim3 grid((unsigned)blocks);
             int rc = launch_raw(lut->width_bits, tp, maps, raw_gl, grid, smem, stream);
@@ -766,7 +771,7 @@ int run_same_table(const Problem *p, int n, amsim_lut_t lut, void *ws, size_t ws
     if (use_ws) {
         // stream-K: finish cut tiles inside the kernel when a cooperative
         // launch is possible, else run the separate fixup kernel afterwards
-        kp.fused = pl.streamk ? 1 : 0;
+        kp.fused = pl.streamk && coop_launches() ? 1 : 0;
         kp.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
         rc = launch_ws(lut->width_bits, kp, gl, dim3((unsigned)blocks), (size_t)kern::kWsFixedSmem + lutb, stream);
         if (rc == kern::AMSIM_ENOTCOOP) {
@@ -997,7 +1002,7 @@ int run_phased(const Problem *p, int n, int nphase, const int *first, const int 
     const int sms = device_sms(lut->device);
     Plan pl = make_plan(p, std::min(n, kern::kMaxProblems), sms, (size_t)-1);
     if (pl.total_tiles == 0 && n <= kern::kMaxProblems) return AMSIM_OK;
-    if (ws && phased_ok(p, n, nphase, pl, lut, true) &&
+    if (ws && coop_launches() && phased_ok(p, n, nphase, pl, lut, true) &&
         ws_bytes >= phased_sk_bytes(nphase, pl.ctas, pl.total_tiles)) {
         pl.streamk = true;
         kern::KParams tp = {};
@@ -1291,3 +1296,10 @@ size_t amsim_gemm_workspace_size(char transA, char transB, int m, int n, int k, 
 }
 
 }  // extern "C"
+
+extern "C" int amsim_set_cooperative_launches(int on)
+{
+    if (on != 0 && on != 1) return AMSIM_EINVAL;
+    amsim::g_coop.store(on != 0, std::memory_order_relaxed);
+    return AMSIM_OK;
+}

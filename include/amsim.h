@@ -133,6 +133,21 @@ int amsim_device_errors(unsigned int *flags, int clear);
  */
 int amsim_set_flag_wait_limit(long long ns);
 
+/*
+ * Cooperative launches on (1, the default) or off (0), for calls made after
+ * it from any thread.  On: a stream-K GEMM finishes the tiles it cuts between
+ * CTAs inside its own (cooperative) launch, and amsim_gemm_phased runs all of
+ * its phases in one launch.  Off: cut tiles are finished by a second kernel,
+ * the fixup kernel, which adds the same partial sums in the same CTA order,
+ * so the results are bit-identical (AMSIM_PATH_FIXUP in amsim_last_path); and
+ * a phased call runs its phases as consecutive grouped launches.  For hosts
+ * where a launch must not hold every SM until all its CTAs are resident (a
+ * context shared with other work).  A cooperative launch the driver refuses
+ * takes the same route on its own.  Errors: AMSIM_EINVAL for a value other
+ * than 0 or 1.  The paper has no counterpart.
+ */
+int amsim_set_cooperative_launches(int on);
+
 /* ------------------------------------------------------------------ LUTs */
 
 /*
