@@ -24,6 +24,15 @@ def test_exports_every_declared_function(L):
         assert hasattr(L, n), n
 
 
+def test_cooperative_switch_values(L):
+    """The switch is host state only: 0 and 1 are taken, anything else is
+    refused, and it is left on."""
+    assert L.amsim_set_cooperative_launches(2) == am.AMSIM_EINVAL
+    assert L.amsim_set_cooperative_launches(-1) == am.AMSIM_EINVAL
+    assert L.amsim_set_cooperative_launches(0) == am.AMSIM_OK
+    assert L.amsim_set_cooperative_launches(1) == am.AMSIM_OK
+
+
 def test_status_strings(L):
     for s in range(6):
         assert am.status_string(s)

@@ -92,10 +92,3 @@ def test_phased_call_without_cooperative_launches(amd, orc, luts, coop):
     assert_close(c1[rows], ref, sa, "C1")
     ref2, sa2 = orc.gemm("mitchell", 7, c1, W2, rows=rows)
     assert_close(c2[rows], ref2, sa2, "C2")
-
-
-def test_cooperative_switch_rejects_other_values(amd):
-    L = amd.lib()
-    assert L.amsim_set_cooperative_launches(2) == amd.AMSIM_EINVAL
-    assert L.amsim_set_cooperative_launches(-1) == amd.AMSIM_EINVAL
-    assert L.amsim_set_cooperative_launches(1) == amd.AMSIM_OK
