@@ -201,3 +201,25 @@ def test_tail_tiles_transposes_alpha_beta(amd, orc, luts, m, n, ta, tb, ldc_pad)
     assert_close(got[:, :n], ref, scale + 1e-30, f"tail {m}x{n} {ta}{tb} ldc+{ldc_pad}")
     if ldc_pad:
         assert np.array_equal(got[:, n:], C0[:, n:])      # the padding column is untouched
+
+
+@pytest.mark.parametrize("n", [300, 360])
+@pytest.mark.parametrize("kind,M", [("mitchell", 8), ("mitchell", 9), ("exact", 7), ("exact", 4)])
+def test_tail_tiles_other_tables(amd, orc, luts, kind, M, n):
+    """Tail layouts with 16-bit tables in shared memory (M = 8, the exact kind
+    at M = 7) and with the table read from global memory (M = 9: offsets and
+    scales in two arrays), cut by stream-K: within the oracle's tolerance."""
+    import torch
+    rng = np.random.default_rng(40 + M + n)
+    m, k = 64, 9000
+    A, B = rnd(rng, (m, k)), rnd(rng, (k, n))
+    lut = luts(kind, M)
+    nb = amd.amsim_gemm_workspace_size("N", "N", m, n, k, 1, lut)
+    C = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+    amd.amsim_gemm("N", "N", m, n, k, 1.0, to_dev(A), k, to_dev(B), n, 0.0, C, n, lut, ws=amd.workspace(nb))
+    torch.cuda.synchronize()
+    taken = amd.amsim_last_path()
+    assert taken & amd.AMSIM_PATH_RAW_TILES and taken & amd.AMSIM_PATH_STREAMK, taken
+    rows = np.array([0, 17, m - 1])
+    ref, sa = orc.gemm(kind, M, A, B, rows=rows)
+    assert_close(C.cpu().numpy()[rows], ref, sa, f"tail {kind} M={M} n={n}")
