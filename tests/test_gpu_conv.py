@@ -31,6 +31,7 @@ TMA_GEOMS = [
     (2, 16, 16, 32, 48, 3, 3, (1, 1), (1, 1), (1, 1)),    # forward and data gradient
     (2, 16, 16, 16, 16, 3, 5, (1, 1), (2, 2), (2, 1)),    # dilated rows, 3 x 5 filter
     (1, 8, 20, 64, 16, 3, 3, (1, 1), (1, 0), (1, 2)),     # filter gradient, dilated columns
+    (1, 16, 16, 128, 32, 3, 3, (1, 1), (1, 1), (1, 1)),   # filter gradient's R*S*C = 1152: a 128-column tail
 ]
 
 
